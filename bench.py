@@ -1,0 +1,401 @@
+"""Benchmark of the compressed-KV hot path on one GB300 (or N, one process each).
+
+One step = one autoregressive chunk step of a LongCat-like attention layer
+(16 KV heads, head_dim 128, chunks of 3 latent frames of 30x52 = 4680
+tokens): compress the newest chunk's K and V into the cache (k-means with
+C=256 and 8 Lloyd iterations, INT2 residual, group 64) and run attention of
+that chunk's 4680 queries over the whole compressed cache of 8 chunks
+(37,440 tokens), reading codes directly.  Synthetic seeded data shaped like
+the workload; inputs resident in HBM at the start of the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  The reference arm times the CPU oracle on
+the host cores on a bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV compress GB/s and fused INT2 attention tok/s, % of GB300 HBM roofline"
+WORKLOAD = "longcat"
+UNIT = "tok/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def _workload(cache_chunks=None):
+    import dataclasses
+
+    from video_diffusion_kv_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    if cache_chunks:
+        w = dataclasses.replace(w, n_chunks=cache_chunks)
+    return w
+
+
+def _config(w, extra=None):
+    cfg = {
+        "workload": ("longcat-like layer: %d KV heads, d=%d, cache of %d chunks x %d tokens (%d), "
+                     "C=%d, INT%d group %d, %d Lloyd iters; step = compress K+V of the newest chunk "
+                     "+ attention of its %d queries over the cache" %
+                     (w.H, w.d, w.n_chunks, w.N, w.tokens, w.C, w.bits, w.group, w.iters, w.Nq)),
+        "tokens_per_chunk": w.N, "cache_tokens": w.tokens, "heads": w.H, "head_dim": w.d,
+        "clusters": w.C, "bits": w.bits, "group": w.group, "lloyd_iters": w.iters, "stages": w.L,
+    }
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _max_over_ranks(x, ws, device=None):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_step_sample(w, seed=0, heads=None, q_rows=1):
+    """Time the oracle on a bounded sample of one step: compress the newest
+    chunk's K and V for `heads` heads (one thread per head) and attention of
+    `q_rows` query rows per head over the full cache.  Returns (seconds
+    scaled to the whole step, threads used, description)."""
+    import numpy as np
+
+    import oracle
+    from video_diffusion_kv_gb300 import synth
+    oracle.build()
+    cores = os.cpu_count() or 1
+    hs = heads or max(1, min(w.H, cores))
+    last = w.n_chunks - 1
+    k = synth.chunk_kv(w, seed, last, synth.KIND_K)[:, :hs]
+    v = synth.chunk_kv(w, seed, last, synth.KIND_V)[:, :hs]
+    t0 = time.perf_counter()
+    ko = oracle.compress_chunk(k, w.C, w.L, w.bits, w.group, w.iters, seed=seed, chunk=last, nthreads=hs)
+    vo = oracle.compress_chunk(v, w.C, w.L, w.bits, w.group, w.iters, seed=seed, chunk=last, nthreads=hs)
+    t_comp = time.perf_counter() - t0
+    # attention over a cache of n_chunks copies-in-shape of the reconstruction
+    kh = np.concatenate([ko["xhat"]] * w.n_chunks, 0)
+    vh = np.concatenate([vo["xhat"]] * w.n_chunks, 0)
+    q = synth.queries(w, seed, last)[:q_rows, :hs]
+    t0 = time.perf_counter()
+    oracle.attention(q, kh, vh, nthreads=min(cores, hs * q_rows))
+    t_attn = time.perf_counter() - t0
+    rounds_full = -(-w.H // min(cores, w.H))
+    rounds_sample = -(-hs // min(cores, hs))
+    scale_heads = rounds_full / rounds_sample
+    attn_rounds_full = -(-(w.H * w.Nq) // cores)
+    attn_rounds_sample = -(-(hs * q_rows) // min(cores, hs * q_rows))
+    t_full = t_comp * scale_heads + t_attn * attn_rounds_full / attn_rounds_sample
+    desc = ("oracle compress of the newest chunk's K and V for %d of %d heads (%d threads) + fp64 "
+            "attention of %d query row(s) x %d heads over %d cached tokens; scaled to the full step "
+            "(%d heads, %d queries) by rounds of %d-thread parallel work" %
+            (hs, w.H, hs, q_rows, hs, kh.shape[0], w.H, w.Nq, cores))
+    return t_full, min(cores, max(hs, hs * q_rows)), desc, t_comp + t_attn
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    w = _workload()
+    for _ in range(args.warmup):
+        oracle_step_sample(w, seed=1)
+    times, walls, desc, thr = [], [], "", 1
+    for s in range(args.steps):
+        t_full, thr, desc, wall = oracle_step_sample(w, seed=2 + s)
+        times.append(t_full)
+        walls.append(wall)
+    ms = 1e3 * statistics.mean(times)
+    value = w.Nq / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, {"parallelism": "host threads"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "sample_wall_s_per_step": statistics.mean(walls)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ own arm
+
+def launches_per_compress(p):
+    per_stage = 1  # residual quantise
+    if p.C > 0:
+        per_stage += (0 if p.flags & 4 else 1) + 1 + 2 * p.iters + 1
+    return per_stage * p.L + 1  # + chunk table
+
+
+def run_own(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import video_diffusion_kv_gb300 as qvg
+    from video_diffusion_kv_gb300 import synth
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = _workload(args.cache_chunks)
+    seed = 100 + rank
+    p = qvg.Params(C=w.C, L=w.L, bits=w.bits, group=w.group, iters=w.iters, seed=seed)
+    slots_per_chunk = -(-w.N // qvg.QVG_TILE) * qvg.QVG_TILE
+    cap = w.n_chunks * slots_per_chunk
+    kc = qvg.CompressedKV(p, w.H, w.d, cap, w.n_chunks, device=dev)
+    vc = qvg.CompressedKV(p, w.H, w.d, cap, w.n_chunks, device=dev)
+    ws_bytes = qvg.workspace_size(p, qvg.QVG_OP_COMPRESS, w.N, w.H, w.d)
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    last = w.n_chunks - 1
+    for k in range(last):  # prefill the older chunks (untimed)
+        qvg.compress_chunk(p, synth_dev(synth.chunk_kv(w, seed, k, synth.KIND_K), dev), kc, workspace=workspace)
+        qvg.compress_chunk(p, synth_dev(synth.chunk_kv(w, seed, k, synth.KIND_V), dev), vc, workspace=workspace)
+    k_host = synth.chunk_kv(w, seed, last, synth.KIND_K)
+    v_host = synth.chunk_kv(w, seed, last, synth.KIND_V)
+    q_host = synth.queries(w, seed, last)
+    k_new, v_new, q = synth_dev(k_host, dev), synth_dev(v_host, dev), synth_dev(q_host, dev)
+    out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kc.reset(last, last * slots_per_chunk)
+        vc.reset(last, last * slots_per_chunk)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        qvg.compress_chunk(p, k_new, kc, workspace=workspace)
+        e[1].record(stream)
+        qvg.compress_chunk(p, v_new, vc, workspace=workspace)
+        e[2].record(stream)
+        qvg.attention(p, q, kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out)
+        e[3].record(stream)
+        return e
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    assert qvg.get_status() == qvg.QVG_OK
+    torch.cuda.synchronize()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = []
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()  # L2 flush between steps, outside the timed events
+        evs.append(step())
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    _barrier(ws)
+    comp = [e[0].elapsed_time(e[2]) for e in evs]
+    attn = [e[2].elapsed_time(e[3]) for e in evs]
+    tot = [e[0].elapsed_time(e[3]) for e in evs]
+    ms_step = _max_over_ranks(statistics.mean(tot), ws, dev if ws > 1 else None)
+    ms_comp = statistics.mean(comp)
+    ms_attn = statistics.mean(attn)
+    status = qvg.get_status()
+
+    if args.no_e2e:
+        if rank == 0:
+            print(json.dumps({"attention_ms": ms_attn, "compress_ms": ms_comp, "ms_per_step": ms_step,
+                              "device_status": int(status)}), flush=True)
+        return 0
+    # end-to-end through the public API with host buffers
+    pin = lambda a: torch.from_numpy(a).to(torch.bfloat16).pin_memory()
+    k_pin, v_pin, q_pin = pin(k_host), pin(v_host), pin(q_host)
+    out_pin = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    k_d, v_d, q_d = torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(q)
+
+    def e2e_step():
+        kc.reset(last, last * slots_per_chunk)
+        vc.reset(last, last * slots_per_chunk)
+        k_d.copy_(k_pin, non_blocking=True)
+        v_d.copy_(v_pin, non_blocking=True)
+        q_d.copy_(q_pin, non_blocking=True)
+        qvg.compress_chunk(p, k_d, kc, workspace=workspace)
+        qvg.compress_chunk(p, v_d, vc, workspace=workspace)
+        qvg.attention(p, q_d, kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out)
+        out_pin.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(max(3, args.steps // 2)):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms.append(1e3 * (time.perf_counter() - t0))
+    e2e = _max_over_ranks(statistics.mean(e2e_ms), ws, dev if ws > 1 else None)
+    h2d = sum(t.numel() * t.element_size() for t in (k_pin, v_pin, q_pin))
+    d2h = out_pin.numel() * out_pin.element_size()
+
+    if rank != 0:
+        return 0
+    peaks, peak_src = _peaks()
+    flops_attn = 4.0 * w.Nq * w.tokens * w.d * w.Hq
+    achieved = flops_attn / (ms_attn / 1e3) / 1e12
+    # The attention kernel runs QK^T and PV on the tensor cores (fp16
+    # operands, fp32 accumulation): tensor roofline, dense 16-bit peak.
+    tc_peak = peaks["bf16_tflops"]
+    in_bytes = 2 * w.N * w.H * w.d * 2
+    line = {
+        "metric": METRIC, "value": ws * w.Nq / (ms_step / 1e3), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/fp16 MMA, fp32 accum",
+        "data": "synthetic",
+        "config": _config(w, {"parallelism": "replicas (one layer per GPU)" if ws > 1 else "single GPU",
+                               "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                               "out_dtype": "bf16"}),
+        "compress": {"ms": ms_comp, "GB/s": in_bytes / (ms_comp / 1e3) / 1e9,
+                     "frac_hbm": (in_bytes / (ms_comp / 1e3) / 1e9) / peaks["hbm_gbs"],
+                     "gflop": 2.0 * 2 * w.N * w.C * w.d * (w.iters + 1) * w.H / 1e9},
+        "attention": {"ms": ms_attn, "tok/s": w.Nq / (ms_attn / 1e3), "TFLOP/s": achieved},
+        "roofline": {"kernel": "k_attention_tc", "bound": "tensor", "achieved": achieved,
+                     "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                     "traffic": None,
+                     "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json); fp16 runs at the same rate" % peak_src,
+                     "mma_flops_per_algorithmic_flop": 1.5},
+        "clocks": clk,
+        "e2e": {"value": ws * w.Nq / (e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
+        "gpu_launches": args.steps * (2 * launches_per_compress(p) + 1),
+        "device_status": int(status),
+        "wall_s_timed": t_wall,
+        "peaks_source": peak_src,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        t_full, thr, desc, _ = oracle_step_sample(w, seed=seed)
+        line["cpu_baseline"] = {"value": w.Nq / t_full, "unit": UNIT, "cores": thr, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def synth_dev(a, dev):
+    import torch
+    return torch.from_numpy(a).to(dev, torch.bfloat16).contiguous()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="time the device step only (profiling)")
+    ap.add_argument("--cache-chunks", type=int, default=None, help="smaller cache (profiling cases)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "own":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_own(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,159 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function
+include/qvg.h declares, sizes buffers by the stated layout, and rejects bad
+arguments on the host before anything is launched (no GPU needed)."""
+import ctypes as ct
+import os
+import re
+import subprocess
+
+import pytest
+
+import video_diffusion_kv_gb300 as qvg
+from video_diffusion_kv_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qvg.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "qvg.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:qvg|quantwm)_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert set(names) == set(qvg.EXPORTED)
+    nm = subprocess.run(["nm", "-D", "--defined-only", qvg.LIB_PATH], capture_output=True, text=True).stdout
+    for n in names:
+        assert re.search(r"\bT %s$" % n, nm, re.M), n
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert qvg.status_string(s)
+    assert qvg.status_string(99) == "unknown status"
+
+
+def test_cache_bytes_layout(lib):
+    p = qvg.Params(C=256, L=1, bits=2, group=64)
+    s = qvg.cache_bytes(p, H=16, d=128, capacity_tokens=37888, max_chunks=8)
+    assert s["codes"] == 16 * 37888 * 32
+    assert s["scales"] == 16 * 37888 * 2 * 2
+    assert s["ids"] == 16 * 37888
+    assert s["cent"] == 16 * 8 * 256 * 128 * 2
+    assert s["chunk_start"] == s["chunk_len"] == 32
+    assert s["tile_chunk"] == 4 * 37888 // 128
+    assert s["psac_p"] == s["psac_s"] == s["psac_basis"] == 0
+    p2 = qvg.Params(C=16, L=3, bits=4, group=32, flags=qvg.QVG_PSAC)
+    s2 = qvg.cache_bytes(p2, H=2, d=64, capacity_tokens=1024, max_chunks=4)
+    assert s2["codes"] == 3 * 2 * 1024 * 32
+    assert s2["scales"] == 3 * 2 * 1024 * 2 * 2
+    assert s2["psac_p"] == 2 * 1024 * 8 and s2["psac_s"] == 2 * 1024 * 2
+    assert s2["psac_basis"] == 4 * 2 * 64 * 8 * 4
+
+
+def test_compression_ratio_matches_layout(lib):
+    """Closed-form ratio == bf16 bytes / bytes of the buffers a full cache
+    uses, when chunks fill whole tiles (no padding)."""
+    for p, H, d, n, chunks in [(qvg.Params(C=16, L=1, bits=2, group=32), 2, 64, 256, 4),
+                               (qvg.Params(C=16, L=3, bits=2, group=32), 2, 64, 256, 4),
+                               (qvg.Params(C=16, L=2, bits=4, group=32), 2, 64, 256, 4),
+                               (qvg.Params(C=256, L=1, bits=2, group=64), 16, 128, 4608, 8)]:
+        s = qvg.cache_bytes(p, H, d, n * chunks, chunks)
+        used = s["codes"] + s["scales"] + s["ids"] + s["cent"]
+        assert qvg.compression_ratio(p, H, d, n, chunks) == pytest.approx(H * n * chunks * d * 2 / used)
+    # INT2, G=64, d=128, C=256, 4680-token chunks: 32 B codes + 4 B scales
+    # + 1 B id per token and head, plus 64 KiB of centroids per chunk and head.
+    r = qvg.compression_ratio(qvg.Params(C=256, L=1, bits=2, group=64), 16, 128, 4680, 8)
+    assert r == pytest.approx(256 / (37 + 256 * 128 * 2 / 4680))
+
+
+def test_kv_size_formula():
+    """The page's worked example: 32 layers x 4096 hidden (K and V, fp16) is
+    16 KB per token per layer, ~512 KB per token, ~8 GB for 16,000 tokens."""
+    assert qvg.kv_bytes_uncompressed(1, 32, 128, 1) == 16 * 1024
+    assert qvg.kv_bytes_uncompressed(32, 32, 128, 1) == 512 * 1024
+    assert qvg.kv_bytes_uncompressed(32, 32, 128, 16000) / 2 ** 30 == pytest.approx(7.81, abs=0.01)
+
+
+def _params(**kw):
+    return qvg.Params(**kw).c()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=3), qvg.QVG_ERR_INVALID_ARG),
+    (dict(L=0), qvg.QVG_ERR_INVALID_ARG),
+    (dict(group=48), qvg.QVG_ERR_INVALID_ARG),
+    (dict(group=2), qvg.QVG_ERR_UNSUPPORTED),
+    (dict(C=300), qvg.QVG_ERR_UNSUPPORTED),
+    (dict(scale_mode=1, bits=4), qvg.QVG_ERR_INVALID_ARG),
+    (dict(flags=64), qvg.QVG_ERR_INVALID_ARG),
+    (dict(C=0, flags=qvg.QVG_GIVEN_CENTROIDS), qvg.QVG_ERR_INVALID_ARG),
+])
+def test_param_validation(lib, kw, code):
+    out = (ct.c_size_t * qvg.QVG_CACHE_NBUF)()
+    p = _params(**kw)
+    assert lib.qvg_cache_bytes(ct.byref(p), 2, 128, 1024, 4, out) == code
+
+
+def test_unsupported_head_dim(lib):
+    out = (ct.c_size_t * qvg.QVG_CACHE_NBUF)()
+    p = _params(group=32)
+    assert lib.qvg_cache_bytes(ct.byref(p), 2, 96, 1024, 4, out) == qvg.QVG_ERR_UNSUPPORTED
+
+
+def _fake_cache(H=2, d=64, cap=512, max_chunks=2, n_chunks=0, n_tokens=0):
+    # Pointers are never dereferenced: every case below fails validation first.
+    fake = ct.c_void_p(0x1000)
+    return qvg._Cache(H, d, cap, max_chunks, n_chunks, n_tokens, *([fake] * 10))
+
+
+def test_compress_rejects_on_host(lib):
+    p = _params(C=16, group=32)
+    x = ct.c_void_p(0x2000)
+    ws = ct.c_void_p(0x100000)
+    c = _fake_cache()
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 0, None, None, ct.byref(c), ws, 1 << 30, None) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_compress_chunk(ct.byref(p), None, 10, None, None, ct.byref(c), ws, 1 << 30, None) == qvg.QVG_ERR_INVALID_ARG
+    full = _fake_cache(n_chunks=2, n_tokens=256)
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 10, None, None, ct.byref(full), ws, 1 << 30, None) == qvg.QVG_ERR_CAPACITY
+    nearly = _fake_cache(n_chunks=1, n_tokens=384)
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 200, None, None, ct.byref(nearly), ws, 1 << 30, None) == qvg.QVG_ERR_CAPACITY
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 100, None, None, ct.byref(c), ws, 16, None) == qvg.QVG_ERR_WORKSPACE
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 100, None, None, ct.byref(c), None, 0, None) == qvg.QVG_ERR_WORKSPACE
+    pq = _params(C=16, group=32, flags=qvg.QVG_QSAC)
+    assert lib.qvg_compress_chunk(ct.byref(pq), x, 100, None, None, ct.byref(c), ws, 1 << 30, None) == qvg.QVG_ERR_INVALID_ARG
+    bad = _fake_cache(cap=500)
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 100, None, None, ct.byref(bad), ws, 1 << 30, None) == qvg.QVG_ERR_INVALID_ARG
+    # the counters are untouched by a rejected call
+    assert c.n_chunks == 0 and c.n_tokens == 0
+
+
+def test_attention_and_decompress_reject_on_host(lib):
+    p = _params(C=16, group=32)
+    k = _fake_cache(n_chunks=1, n_tokens=128)
+    v = _fake_cache(n_chunks=1, n_tokens=256)
+    q, o = ct.c_void_p(0x3000), ct.c_void_p(0x4000)
+    assert lib.qvg_attention(ct.byref(p), q, 4, 2, ct.byref(k), ct.byref(v), 0.0, o, 0, None, None, None, 0, None) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_attention(ct.byref(p), q, 4, 3, ct.byref(k), ct.byref(k), 0.0, o, 0, None, None, None, 0, None) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_attention(ct.byref(p), q, 4, 2, ct.byref(k), ct.byref(k), 0.0, o, 7, None, None, None, 0, None) == qvg.QVG_ERR_INVALID_ARG
+    empty = _fake_cache()
+    assert lib.qvg_attention(ct.byref(p), q, 4, 2, ct.byref(empty), ct.byref(empty), 0.0, o, 0, None, None, None, 0, None) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_decompress(ct.byref(p), ct.byref(k), 0, 200, o, 0, None) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_decompress(ct.byref(p), ct.byref(k), -1, 10, o, 0, None) == qvg.QVG_ERR_INVALID_ARG
+
+
+def test_quantwm_reject_on_host(lib):
+    f = ct.c_void_p(0x5000)
+    assert lib.quantwm_query_stats(f, 10, 3, 2, 128, 0, f, f, f, None) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.quantwm_query_stats(f, 10, 2, 2, 96, 0, f, f, f, None) == qvg.QVG_ERR_UNSUPPORTED
+    assert lib.quantwm_psac_basis(f, f, 2, 128, 4, f, f, f, None) == qvg.QVG_ERR_UNSUPPORTED
+    assert lib.quantwm_psac_basis(f, f, 2, 256, 8, f, f, f, None) == qvg.QVG_ERR_UNSUPPORTED
+    assert lib.quantwm_psac_basis(None, f, 2, 128, 8, f, f, f, None) == qvg.QVG_ERR_INVALID_ARG

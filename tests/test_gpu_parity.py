@@ -1,0 +1,366 @@
+"""GPU-vs-oracle parity through the C ABI, on the seeded synthetic workloads.
+
+Bars (the arithmetic behind them is in the helpers and below):
+  - cluster ids: equal to the oracle's fp64 argmin over the same centroids,
+    except near ties (relative score gap < 1e-5), which must stay < 0.01 %;
+  - codes and fp16 scales: bit-exact wherever the ids agree (the quantiser is
+    a chain of correctly rounded fp32 operations on both sides);
+  - k-means initialisation: bit-exact centroids;
+  - one Lloyd update from the same assignment: every bf16 centroid within
+    1 ulp of the oracle's (fp32 vs fp64 sums round differently);
+  - reconstruction from the same bytes: bit-exact (same fp32 operation
+    order), PSAC correction within 1e-3 of max|X|;
+  - attention: max|dO| / max|O_oracle| <= 2e-3 per head, oracle in fp64 on
+    the reconstruction of the same compressed cache.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import video_diffusion_kv_gb300 as qvg
+from video_diffusion_kv_gb300 import synth
+
+from _helpers import (ATTN_TOL, NEAR_TIE_RATE, assignment_mismatches, bf16_ulp_diff,
+                      chunk_arrays, chunk_slice, host_cache, oracle_rebuild, to_dev)
+
+pytestmark = pytest.mark.gpu
+NT = 16  # oracle threads
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+W = synth.WORKLOADS
+CASES = {
+    "tiny": (W["tiny"], qvg.Params(C=16, L=1, bits=2, group=32, iters=10, seed=3), 4),
+    "pro_int2_L3": (W["qvgpro"], qvg.Params(C=16, L=3, bits=2, group=32, iters=10, seed=4), 2),
+    "pro_int4_L2": (W["qvgpro"], qvg.Params(C=16, L=2, bits=4, group=32, iters=10, seed=5), 2),
+    "page1_scale": (W["tiny"], qvg.Params(C=16, L=1, bits=2, group=32, iters=10, scale_mode=1, seed=6), 2),
+    "rtn": (W["tiny"], qvg.Params(C=0, L=1, bits=2, group=32, iters=0), 2),
+    "longcat": (W["longcat"], qvg.Params(C=256, L=1, bits=2, group=64, iters=8, seed=7), 2),
+}
+
+
+def _new_cache(w, p, n_chunks, N=None):
+    N = N or w.N
+    cap = n_chunks * (-(-N // 128) * 128)
+    return qvg.CompressedKV(p, w.H, w.d, cap, n_chunks)
+
+
+def _check_against_fed_oracle(x, hc, p, k, w=None, psac_U=None):
+    """The oracle, fed the GPU's stored centroids with zero Lloyd iterations,
+    must reproduce the GPU's ids (modulo near ties) and, on rows whose ids
+    agree at every stage, its codes and scales bit for bit."""
+    codes, scales, ids, cent = chunk_arrays(hc, p, k)
+    cent_in = oracle.bf16_bits_to_f32(cent) if p.C > 0 else None
+    o = oracle.compress_chunk(x, C=p.C, L=p.L, bits=p.bits, group=p.group, iters=0, mode=p.scale_mode,
+                              seed=p.seed, chunk=k, qsac_w=w, psac_U=psac_U, cent_in=cent_in, nthreads=NT)
+    N, H = x.shape[0], x.shape[1]
+    ok_rows = np.ones((H, N), bool)
+    total = near = 0
+    stage_in = x.copy()
+    for l in range(p.L):
+        g = stage_in if l == 0 else synth.bf16_values(stage_in)
+        if p.C > 0:
+            for h in range(H):
+                wh = None if w is None else w[h]
+                rows = ok_rows[h]
+                m, far = assignment_mismatches(g[rows, h], cent[l, h, :min(p.C, N)],
+                                               ids[l, h][rows].astype(np.int32), wh)
+                total += int(rows.sum())
+                near += m
+                assert far == 0, ("assignment mismatch outside near ties", l, h, far)
+                ok_rows[h] &= ids[l, h] == o["ids"][l, h]
+        for h in range(H):
+            np.testing.assert_array_equal(codes[l, h][ok_rows[h]], o["codes"][l, h][ok_rows[h]])
+            np.testing.assert_array_equal(scales[l, h][ok_rows[h]], o["scales"][l, h][ok_rows[h]])
+        # next stage input from the oracle's own residual (bit-exact on ok rows)
+        dq = oracle.decompress(o["codes"][l:l + 1], o["scales"][l:l + 1], o["ids"][l:l + 1],
+                               o["cent"][l:l + 1], p.C, p.bits, p.group)
+        stage_in = stage_in - dq
+    if total:
+        assert near <= max(1, NEAR_TIE_RATE * total), ("near ties", near, total)
+    return o, ok_rows
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_compress_matches_oracle(name):
+    """Full seeded compression on the GPU, checked chunk by chunk: the final
+    assignment and quantisation agree with the oracle run on the GPU's own
+    centroids, and the reconstruction error is that of the oracle's own
+    k-means (same definition, same seeds)."""
+    w, p, n_chunks = CASES[name]
+    kc = _new_cache(w, p, n_chunks)
+    xs = []
+    for k in range(n_chunks):
+        x = synth.chunk_kv(w, 11, k, synth.KIND_K if k % 2 == 0 else synth.KIND_V)
+        xs.append(x)
+        qvg.compress_chunk(p, to_dev(x), kc)
+    assert qvg.get_status() == qvg.QVG_OK
+    hc = host_cache(kc)
+    for k in range(n_chunks):
+        assert hc["length"][k] == w.N and hc["start"][k] % 128 == 0
+        _check_against_fed_oracle(xs[k], hc, p, k)
+    if w.N <= 256:
+        # the oracle's own full run reaches the same reconstruction error
+        for k in range(n_chunks):
+            o = oracle.compress_chunk(xs[k], C=p.C, L=p.L, bits=p.bits, group=p.group, iters=p.iters,
+                                      mode=p.scale_mode, seed=p.seed, chunk=k, nthreads=NT)
+            rg = np.linalg.norm(xs[k] - oracle_rebuild(hc, p, k)) / np.linalg.norm(xs[k])
+            ro = np.linalg.norm(xs[k] - o["xhat"]) / np.linalg.norm(xs[k])
+            assert abs(rg - ro) <= 0.05 * ro + 1e-6, (rg, ro)
+
+
+@pytest.mark.parametrize("name", ["tiny", "pro_int2_L3", "longcat"])
+def test_kmeans_init_exact(name):
+    """Zero Lloyd iterations: the centroids are the seeded picks, bit for bit."""
+    w, p0, _ = CASES[name]
+    p = qvg.Params(**{**p0.__dict__, "iters": 0})
+    kc = _new_cache(w, p, 1)
+    x = synth.chunk_kv(w, 12, 0, synth.KIND_K)
+    qvg.compress_chunk(p, to_dev(x), kc)
+    hc = host_cache(kc)
+    o = oracle.compress_chunk(x, C=p.C, L=p.L, bits=p.bits, group=p.group, iters=0, seed=p.seed, chunk=0,
+                              nthreads=NT)
+    np.testing.assert_array_equal(hc["cent"][0, :, 0], o["cent"][0])
+    _check_against_fed_oracle(x, hc, p, 0)
+
+
+@pytest.mark.parametrize("name", ["tiny", "longcat"])
+def test_lloyd_update_step(name):
+    """From the same centroids c0: GPU ids after one assignment, then the
+    GPU's updated centroids equal the oracle's mean of those members within
+    one bf16 ulp (empty clusters keep c0)."""
+    w, p0, _ = CASES[name]
+    x = synth.chunk_kv(w, 13, 0, synth.KIND_K)
+    rng = np.random.default_rng(0)
+    N = x.shape[0]
+    c0 = np.stack([x[rng.choice(N, p0.C, replace=False), h] for h in range(w.H)])  # [H, C, d]
+    c0_bits = torch.from_numpy(c0).to(torch.bfloat16).view(torch.int16)
+    res = {}
+    for iters in (0, 1):
+        p = qvg.Params(C=p0.C, L=1, bits=p0.bits, group=p0.group, iters=iters, flags=qvg.QVG_GIVEN_CENTROIDS)
+        kc = _new_cache(w, p, 1)
+        kc.view("cent", torch.int16, (1, w.H, 1, p.C, w.d))[0, :, 0] = c0_bits.cuda()
+        qvg.compress_chunk(p, to_dev(x), kc)
+        res[iters] = host_cache(kc)
+    ids0 = res[0]["ids"][0, :, :N].astype(np.int32)
+    c1 = res[1]["cent"][0, :, 0]
+    exact = 0
+    for h in range(w.H):
+        m, far = assignment_mismatches(x[:, h], c0_bits.numpy().view(np.uint16)[h], ids0[h])
+        assert far == 0
+        ref, mean, cnt = oracle.update(x[:, h], ids0[h], c0[h])
+        ref_bits = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        ulps = bf16_ulp_diff(c1[h], ref_bits)
+        assert ulps.max() <= 1, (h, ulps.max())
+        exact += (ulps == 0).sum()
+    assert exact >= 0.99 * w.H * p0.C * w.d
+
+
+def test_decompress_exact_and_bf16():
+    w, p, n_chunks = CASES["pro_int2_L3"]
+    kc = _new_cache(w, p, n_chunks)
+    for k in range(n_chunks):
+        qvg.compress_chunk(p, to_dev(synth.chunk_kv(w, 14, k, synth.KIND_V)), kc)
+    hc = host_cache(kc)
+    full = qvg.decompress(p, kc, 0, kc.n_tokens).cpu().numpy()
+    half = qvg.decompress(p, kc, 0, kc.n_tokens, out_dtype=qvg.QVG_OUT_BF16).float().cpu().numpy()
+    for k in range(n_chunks):
+        sl = chunk_slice(hc, k)
+        ref = oracle_rebuild(hc, p, k)
+        np.testing.assert_array_equal(full[sl], ref)
+        np.testing.assert_array_equal(half[sl], synth.bf16_values(ref))
+
+
+def _cache_with_chunks(w, p, chunks_kv, seed=0):
+    n = len(chunks_kv)
+    cap = sum(-(-c[0].shape[0] // 128) * 128 for c in chunks_kv)
+    kc = qvg.CompressedKV(p, w.H, w.d, cap, n)
+    vc = qvg.CompressedKV(p, w.H, w.d, cap, n)
+    for k, v in chunks_kv:
+        qvg.compress_chunk(p, to_dev(k), kc)
+        qvg.compress_chunk(p, to_dev(v), vc)
+    return kc, vc
+
+
+def _oracle_attention_on(kc, vc, p, q, rows=None):
+    hk, hv = host_cache(kc), host_cache(vc)
+    kh = np.concatenate([oracle_rebuild(hk, p, k) for k in range(kc.n_chunks)], 0)
+    vh = np.concatenate([oracle_rebuild(hv, p, k) for k in range(vc.n_chunks)], 0)
+    qq = q if rows is None else q[rows]
+    out, lse, am = oracle.attention(qq, kh, vh, nthreads=NT)
+    return out, lse, am, kh, hk
+
+
+def _slot_of_token(hk, n_chunks):
+    return np.concatenate([np.arange(hk["start"][k], hk["start"][k] + hk["length"][k]) for k in range(n_chunks)])
+
+
+def _assert_attention(got, ref, Hq):
+    for h in range(Hq):
+        err = np.abs(got[:, h] - ref[:, h]).max() / np.abs(ref[:, h]).max()
+        assert err <= ATTN_TOL, (h, err)
+
+
+@pytest.mark.parametrize("Hq_mult", [1, 2])
+def test_attention_tiny(Hq_mult):
+    w, p, n_chunks = CASES["tiny"]
+    chunks = [(synth.chunk_kv(w, 15, k, synth.KIND_K), synth.chunk_kv(w, 15, k, synth.KIND_V)) for k in range(n_chunks)]
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    q = synth.queries(w, 15, n_chunks)
+    if Hq_mult > 1:
+        q = np.concatenate([q, synth.queries(w, 16, n_chunks)], 1)[:, [0, 2, 1, 3]]
+    out, lse, top1 = qvg.attention(p, to_dev(q), kc, vc, want_lse=True, want_top1=True)
+    ref, rlse, ram, _, hk = _oracle_attention_on(kc, vc, p, q)
+    got = out.cpu().numpy().astype(np.float64)
+    _assert_attention(got, ref, q.shape[1])
+    np.testing.assert_allclose(lse.cpu().numpy(), rlse, atol=2e-3, rtol=0)
+    slots = _slot_of_token(hk, n_chunks)
+    agree = (top1.cpu().numpy() == slots[ram]).mean()
+    assert agree >= 0.99
+    # bf16 output is the rounding of the fp32 one (up to the last bit)
+    o16, _, _ = qvg.attention(p, to_dev(q), kc, vc, out_dtype=qvg.QVG_OUT_BF16)
+    np.testing.assert_allclose(o16.float().cpu().numpy(), got, rtol=2 ** -7, atol=1e-6 * np.abs(got).max())
+
+
+def test_attention_longcat_sampled():
+    """4680 queries over 2 chunks of 4680 tokens (16 heads, d=128); the fp64
+    oracle checks 64 sampled query rows per head."""
+    w, p, _ = CASES["longcat"]
+    chunks = [(synth.chunk_kv(w, 17, k, synth.KIND_K), synth.chunk_kv(w, 17, k, synth.KIND_V)) for k in range(2)]
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    q = synth.queries(w, 17, 2)
+    out, _, _ = qvg.attention(p, to_dev(q), kc, vc)
+    rows = np.random.default_rng(1).choice(q.shape[0], 64, replace=False)
+    ref, _, _, _, _ = _oracle_attention_on(kc, vc, p, q, rows)
+    _assert_attention(out.cpu().numpy()[rows].astype(np.float64), ref, w.Hq)
+
+
+def test_ragged_and_degenerate_chunks():
+    """Chunks of 300 (two tiles plus a ragged 44), 1 token, 10 tokens with
+    C=16 > N, and exactly 128 tokens; attention across all of them."""
+    w = W["tiny"]
+    p = qvg.Params(C=16, L=2, bits=2, group=32, iters=4, seed=9)
+    sizes = [300, 1, 10, 128]
+    base_k = np.concatenate([synth.chunk_kv(w, 18, k, synth.KIND_K) for k in range(3)], 0)
+    base_v = np.concatenate([synth.chunk_kv(w, 18, k, synth.KIND_V) for k in range(3)], 0)
+    chunks, off = [], 0
+    for n in sizes:
+        chunks.append((base_k[off:off + n], base_v[off:off + n]))
+        off += n
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    hk = host_cache(kc)
+    assert list(hk["length"][:4]) == sizes and list(hk["start"][:4]) == [0, 384, 512, 640]
+    for k, (x, _) in enumerate(chunks):
+        _check_against_fed_oracle(x, hk, p, k)
+    full = qvg.decompress(p, kc, 0, kc.n_tokens).cpu().numpy()
+    assert not full[300:384].any()  # padding slots read as zero
+    q = synth.queries(w, 18, 5)[:77]
+    out, _, top1 = qvg.attention(p, to_dev(q), kc, vc, want_top1=True)
+    ref, _, ram, _, _ = _oracle_attention_on(kc, vc, p, q)
+    _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
+    assert np.all(np.isin(top1.cpu().numpy(), _slot_of_token(hk, 4)))
+
+
+def test_single_token_cache_returns_value():
+    w = W["tiny"]
+    p = qvg.Params(C=16, L=1, bits=2, group=32, iters=2)
+    k1 = synth.chunk_kv(w, 19, 0, synth.KIND_K)[:1]
+    v1 = synth.chunk_kv(w, 19, 0, synth.KIND_V)[:1]
+    kc, vc = _cache_with_chunks(w, p, [(k1, v1)])
+    q = synth.queries(w, 19, 1)[:5]
+    out, _, _ = qvg.attention(p, to_dev(q), kc, vc)
+    vhat = qvg.decompress(p, vc, 0, 1).cpu().numpy()
+    np.testing.assert_array_equal(out.cpu().numpy(), np.repeat(vhat, 5, 0))
+
+
+def test_capacity_is_reported():
+    w = W["tiny"]
+    p = qvg.Params(C=16, L=1, bits=2, group=32, iters=1)
+    kc = qvg.CompressedKV(p, w.H, w.d, 256, 1)
+    x = to_dev(synth.chunk_kv(w, 20, 0, synth.KIND_K))
+    qvg.compress_chunk(p, x, kc)
+    with pytest.raises(qvg.QvgError) as e:
+        qvg.compress_chunk(p, x, kc)
+    assert e.value.status == qvg.QVG_ERR_CAPACITY
+    assert kc.n_chunks == 1 and kc.n_tokens == 256
+
+
+# ---------------------------------------------------------------- QuantWM
+
+def _quantwm_small():
+    # QuantWM shapes with 4 KV heads and one 3-frame chunk (2640 tokens)
+    import dataclasses
+    return dataclasses.replace(W["quantwm"], H=4, Hq=4)
+
+
+def test_query_stats_and_basis():
+    w = _quantwm_small()
+    qh = synth.history_queries(w, 21)
+    M, wv, cnt = qvg.query_stats(to_dev(qh), w.H)
+    Mo, co = oracle.query_stats(qh, w.H)
+    assert int(cnt.item()) == co
+    Mg = M.cpu().numpy()
+    assert np.abs(Mg - Mo).max() <= 1e-5 * np.abs(Mo).max()
+    np.testing.assert_allclose(wv.cpu().numpy(), np.einsum("hjj->hj", Mo) / co, rtol=1e-5)
+    M2, _, cnt2 = qvg.query_stats(to_dev(qh), w.H, M=M.clone(), count=cnt.clone(), accumulate=True)
+    assert int(cnt2.item()) == 2 * co
+    np.testing.assert_allclose(M2.cpu().numpy(), 2 * Mg, rtol=1e-6)
+    U, eig, frac = qvg.psac_basis(M, cnt)
+    Uo, eo, fo = oracle.psac_basis(Mg.astype(np.float64), co, 8)
+    np.testing.assert_allclose(eig.cpu().numpy(), eo, rtol=1e-4)
+    np.testing.assert_allclose(frac.cpu().numpy(), fo, atol=1e-5)
+    Ug = U.cpu().numpy()
+    for h in range(w.H):
+        dots = np.einsum("dk,dk->k", Ug[h], Uo[h])
+        assert dots.min() > 1 - 1e-4, dots
+        np.testing.assert_allclose(Ug[h].T @ Ug[h], np.eye(8), atol=1e-5)
+    assert 0.69 < frac.cpu().numpy().min() and frac.cpu().numpy().max() < 0.75
+
+
+@pytest.mark.parametrize("flags", [qvg.QVG_QSAC, qvg.QVG_PSAC, qvg.QVG_QSAC | qvg.QVG_PSAC])
+def test_quantwm_compress_and_attention(flags):
+    w = _quantwm_small()
+    qh = synth.history_queries(w, 22)
+    M, wv, cnt = qvg.query_stats(to_dev(qh), w.H)
+    U, _, _ = qvg.psac_basis(M, cnt)
+    p = qvg.Params(C=256, L=1, bits=2, group=64, iters=8, seed=23, flags=flags)
+    chunks = [(synth.chunk_kv(w, 23, k, synth.KIND_K), synth.chunk_kv(w, 23, k, synth.KIND_V)) for k in range(2)]
+    cap = 2 * (-(-w.N // 128) * 128)
+    kc = qvg.CompressedKV(p, w.H, w.d, cap, 2)
+    pv = qvg.Params(**{**p.__dict__, "flags": 0})
+    vc = qvg.CompressedKV(pv, w.H, w.d, cap, 2)
+    for k, v in chunks:
+        qvg.compress_chunk(p, to_dev(k), kc, qsac_w=wv, psac_basis=U)
+        qvg.compress_chunk(pv, to_dev(v), vc)
+    hk = host_cache(kc)
+    ww = wv.cpu().numpy() if flags & qvg.QVG_QSAC else None
+    Uh = U.cpu().numpy() if flags & qvg.QVG_PSAC else None
+    for k, (x, _) in enumerate(chunks):
+        o, ok = _check_against_fed_oracle(x, hk, p, k, w=ww, psac_U=Uh)
+        if Uh is not None:
+            sl = chunk_slice(hk, k)
+            np.testing.assert_array_equal(hk["psac_basis"][k], Uh)
+            for h in range(w.H):
+                np.testing.assert_array_equal(hk["psac_p"][h, sl][ok[h]], o["psac_p"][h][ok[h]])
+                np.testing.assert_array_equal(hk["psac_s"][h, sl][ok[h]], o["psac_s"][h][ok[h]])
+            gpu = qvg.decompress(p, kc, int(hk["start"][k]), int(hk["length"][k])).cpu().numpy()
+            ref = oracle_rebuild(hk, p, k)
+            assert np.abs(gpu - ref).max() <= 1e-3 * np.abs(ref).max()
+    q = synth.history_queries(w, 24, n_tokens=300, stream=1)
+    out, _, _ = qvg.attention(p, to_dev(q), kc, vc)
+    hv = host_cache(vc)
+    kh = np.concatenate([oracle_rebuild(hk, p, k) for k in range(2)], 0)
+    vh = np.concatenate([oracle_rebuild(hv, pv, k) for k in range(2)], 0)
+    ref, _, _ = oracle.attention(q, kh, vh, nthreads=NT)
+    _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)

@@ -1,0 +1,289 @@
+// api.cu -- the extern "C" entry points of libqvg: argument validation,
+// workspace carving and the launch sequence of each call.
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+
+#include "common.cuh"
+
+namespace qvg {
+__device__ int g_qvg_error = 0;
+
+int *device_error_word() {
+    static int *ptr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!ptr[dev]) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_qvg_error) != cudaSuccess) return nullptr;
+        ptr[dev] = static_cast<int *>(a);
+    }
+    return ptr[dev];
+}
+}
+
+using namespace qvg;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Validation of the method parameters against a head_dim.
+qvg_status check_params(const qvg_params *p, int d) {
+    if (!p) return QVG_ERR_INVALID_ARG;
+    if (p->reserved != 0 || p->L < 1 || p->L > 16 || p->C < 0 || p->iters < 0 ||
+        p->iters > 10000 || (p->bits != 2 && p->bits != 4) || p->group < 1 ||
+        (p->scale_mode != 0 && p->scale_mode != 1) || (p->flags & ~7))
+        return QVG_ERR_INVALID_ARG;
+    if (p->scale_mode == 1 && p->bits != 2) return QVG_ERR_INVALID_ARG;
+    if (p->C > QVG_MAX_CLUSTERS) return QVG_ERR_UNSUPPORTED;
+    if (d < 1 || d % p->group != 0) return QVG_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return QVG_ERR_UNSUPPORTED;
+    const int e = d / 32;  // channels per lane in the row kernels
+    if (p->group < e || !is_pow2(p->group / e) || p->group / e > 32) return QVG_ERR_UNSUPPORTED;
+    if (p->group % 8 != 0) return QVG_ERR_UNSUPPORTED;  // the read path rebuilds 8-channel chunks
+    if ((p->flags & QVG_GIVEN_CENTROIDS) && p->C == 0) return QVG_ERR_INVALID_ARG;
+    return QVG_OK;
+}
+
+qvg_status check_cache(const qvg_params *p, const qvg_cache *c) {
+    if (!c) return QVG_ERR_INVALID_ARG;
+    if (c->H < 1 || c->capacity_tokens <= 0 || c->capacity_tokens % QVG_TILE != 0 ||
+        c->max_chunks < 1 || c->n_chunks < 0 || c->n_chunks > c->max_chunks ||
+        c->n_tokens < 0 || c->n_tokens % QVG_TILE != 0 || c->n_tokens > c->capacity_tokens)
+        return QVG_ERR_INVALID_ARG;
+    if (!c->codes || !c->scales || !c->chunk_start || !c->chunk_len || !c->tile_chunk)
+        return QVG_ERR_INVALID_ARG;
+    if (p->C > 0 && (!c->ids || !c->cent)) return QVG_ERR_INVALID_ARG;
+    if ((p->flags & QVG_PSAC) && (!c->psac_p || !c->psac_s || !c->psac_basis))
+        return QVG_ERR_INVALID_ARG;
+    return QVG_OK;
+}
+
+struct CompressWs {
+    int32_t *ids;
+    float *cnorm;
+    float *delta;
+    uint16_t *gbf;
+    size_t bytes;
+};
+
+CompressWs carve_compress(const qvg_params *p, int N, int H, int d, char *base) {
+    CompressWs w{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *ptr = base ? base + off : nullptr;
+        off += align_up(bytes);
+        return ptr;
+    };
+    w.ids = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * static_cast<size_t>(H) * N));
+    w.cnorm = reinterpret_cast<float *>(take(sizeof(float) * static_cast<size_t>(H) * std::max(p->C, 1)));
+    const bool need_delta = p->L > 1 || (p->flags & QVG_PSAC);
+    w.delta = need_delta ? reinterpret_cast<float *>(take(sizeof(float) * static_cast<size_t>(N) * H * d)) : nullptr;
+    w.gbf = p->L > 1 ? reinterpret_cast<uint16_t *>(take(sizeof(uint16_t) * static_cast<size_t>(N) * H * d)) : nullptr;
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qvg_status_string(qvg_status s) {
+    switch (s) {
+        case QVG_OK: return "ok";
+        case QVG_ERR_INVALID_ARG: return "invalid argument";
+        case QVG_ERR_UNSUPPORTED: return "unsupported configuration";
+        case QVG_ERR_CUDA: return "CUDA error";
+        case QVG_ERR_TIMEOUT: return "device wait exceeded its bound";
+        case QVG_ERR_WORKSPACE: return "workspace missing or too small";
+        case QVG_ERR_CAPACITY: return "cache capacity exceeded";
+    }
+    return "unknown status";
+}
+
+qvg_status qvg_cache_bytes(const qvg_params *p, int32_t H, int32_t d, int32_t cap,
+                           int32_t max_chunks, size_t out[QVG_CACHE_NBUF]) {
+    if (!out) return QVG_ERR_INVALID_ARG;
+    qvg_status s = check_params(p, d);
+    if (s != QVG_OK) return s;
+    if (H < 1 || cap <= 0 || cap % QVG_TILE != 0 || max_chunks < 1) return QVG_ERR_INVALID_ARG;
+    const size_t L = p->L, rows = static_cast<size_t>(H) * cap;
+    out[0] = L * rows * (static_cast<size_t>(d) * p->bits / 8);
+    out[1] = L * rows * (d / p->group) * sizeof(uint16_t);
+    out[2] = p->C > 0 ? L * rows : 0;
+    out[3] = L * H * static_cast<size_t>(max_chunks) * p->C * d * sizeof(uint16_t);
+    out[4] = sizeof(int32_t) * static_cast<size_t>(max_chunks);
+    out[5] = sizeof(int32_t) * static_cast<size_t>(max_chunks);
+    out[6] = sizeof(int32_t) * static_cast<size_t>(cap / QVG_TILE);
+    const bool psac = p->flags & QVG_PSAC;
+    out[7] = psac ? rows * QVG_PSAC_RANK : 0;
+    out[8] = psac ? rows * sizeof(uint16_t) : 0;
+    out[9] = psac ? sizeof(float) * static_cast<size_t>(max_chunks) * H * d * QVG_PSAC_RANK : 0;
+    return QVG_OK;
+}
+
+qvg_status qvg_workspace_size(const qvg_params *p, int32_t op, int32_t n, int32_t H, int32_t d,
+                              int32_t Hq, size_t *bytes) {
+    if (!bytes) return QVG_ERR_INVALID_ARG;
+    qvg_status s = check_params(p, d);
+    if (s != QVG_OK) return s;
+    if (n < 0 || H < 1) return QVG_ERR_INVALID_ARG;
+    (void)Hq;
+    switch (op) {
+        case QVG_OP_COMPRESS: *bytes = carve_compress(p, n, H, d, nullptr).bytes; return QVG_OK;
+        case QVG_OP_ATTENTION: *bytes = 0; return QVG_OK;
+        case QVG_OP_PSAC_BASIS: *bytes = 0; return QVG_OK;
+    }
+    return QVG_ERR_INVALID_ARG;
+}
+
+qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N,
+                              const float *qsac_w, const float *psac_basis, qvg_cache *cache,
+                              void *workspace, size_t ws_bytes, void *stream) {
+    if (!cache || !x_bf16) return QVG_ERR_INVALID_ARG;
+    qvg_status s = check_params(p, cache->d);
+    if (s != QVG_OK) return s;
+    if ((s = check_cache(p, cache)) != QVG_OK) return s;
+    if (N < 1 || N > 65535) return QVG_ERR_INVALID_ARG;
+    if ((p->flags & QVG_QSAC) && !qsac_w) return QVG_ERR_INVALID_ARG;
+    if ((p->flags & QVG_PSAC) && !psac_basis) return QVG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(x_bf16) % 16 != 0) return QVG_ERR_INVALID_ARG;
+    const int H = cache->H, d = cache->d;
+    const int Naligned = ceil_div(N, QVG_TILE) * QVG_TILE;
+    if (cache->n_chunks >= cache->max_chunks || cache->n_tokens + Naligned > cache->capacity_tokens)
+        return QVG_ERR_CAPACITY;
+    const CompressWs need = carve_compress(p, N, H, d, nullptr);
+    if (need.bytes > 0 && (!workspace || ws_bytes < need.bytes)) return QVG_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return QVG_ERR_WORKSPACE;
+    const CompressWs ws = carve_compress(p, N, H, d, static_cast<char *>(workspace));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const int chunk = cache->n_chunks, slot0 = cache->n_tokens;
+    const int C = p->C, Ce = std::min(C, N), L = p->L;
+    const float *w = (p->flags & QVG_QSAC) ? qsac_w : nullptr;
+    const bool psac = p->flags & QVG_PSAC;
+    const size_t cap = cache->capacity_tokens, nb = static_cast<size_t>(d) * p->bits / 8;
+    const size_t ng = d / p->group;
+    const size_t cent_hs = static_cast<size_t>(cache->max_chunks) * C * d;
+    if (psac) {
+        if (cudaMemcpyAsync(cache->psac_basis + static_cast<size_t>(chunk) * H * d * QVG_PSAC_RANK,
+                            psac_basis, sizeof(float) * H * d * QVG_PSAC_RANK,
+                            cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return QVG_ERR_CUDA;
+    }
+    for (int l = 0; l < L; ++l) {
+        const void *xin = l == 0 ? x_bf16 : static_cast<const void *>(ws.delta);
+        const bool f32 = l > 0;
+        const uint16_t *g = l == 0 ? static_cast<const uint16_t *>(x_bf16) : ws.gbf;
+        uint16_t *cent = C > 0 ? cache->cent + (static_cast<size_t>(l) * H * cache->max_chunks + chunk) * C * d : nullptr;
+        if (C > 0) {
+            if (!(p->flags & QVG_GIVEN_CENTROIDS)) {
+                if ((s = launch_kmeans_init(g, N, H, d, C, Ce, p->seed, chunk, l, cent, cent_hs, st)) != QVG_OK) return s;
+            }
+            if ((s = launch_centroid_norms(cent, cent_hs, H, C, d, w, ws.cnorm, st)) != QVG_OK) return s;
+            for (int it = 0; it < p->iters; ++it) {
+                if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.ids, st)) != QVG_OK) return s;
+                if ((s = launch_kmeans_update(xin, f32, N, H, d, ws.ids, cent, cent_hs, Ce, C, w, ws.cnorm, st)) != QVG_OK) return s;
+            }
+            if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.ids, st)) != QVG_OK) return s;
+        }
+        const bool last = l == L - 1;
+        const size_t lrow = static_cast<size_t>(l) * H * cap + slot0;
+        s = launch_residual_quant(
+            xin, f32, N, H, d, cent, cent_hs, C, ws.ids, p->bits, p->group, p->scale_mode,
+            cache->codes + lrow * nb, cache->scales + lrow * ng, C > 0 ? cache->ids + lrow : nullptr, cap,
+            (!last || psac) ? ws.delta : nullptr, !last ? ws.gbf : nullptr,
+            (last && psac) ? psac_basis : nullptr, psac ? cache->psac_p + static_cast<size_t>(slot0) * QVG_PSAC_RANK : nullptr,
+            psac ? cache->psac_s + slot0 : nullptr, cap, st);
+        if (s != QVG_OK) return s;
+    }
+    if ((s = launch_chunk_table(chunk, slot0, N, cache->chunk_start, cache->chunk_len, cache->tile_chunk, st)) != QVG_OK)
+        return s;
+    cache->n_chunks = chunk + 1;
+    cache->n_tokens = slot0 + Naligned;
+    return QVG_OK;
+}
+
+qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache, int32_t tok0, int32_t ntok,
+                          void *out, int32_t out_dtype, void *stream) {
+    if (!cache || !out) return QVG_ERR_INVALID_ARG;
+    qvg_status s = check_params(p, cache->d);
+    if (s != QVG_OK) return s;
+    if ((s = check_cache(p, cache)) != QVG_OK) return s;
+    if (out_dtype != QVG_OUT_F32 && out_dtype != QVG_OUT_BF16) return QVG_ERR_INVALID_ARG;
+    if (tok0 < 0 || ntok < 0 || tok0 + ntok > cache->n_tokens) return QVG_ERR_INVALID_ARG;
+    if (ntok == 0) return QVG_OK;
+    return launch_decompress(p, cache, tok0, ntok, out, out_dtype, static_cast<cudaStream_t>(stream));
+}
+
+qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq, int32_t Hq,
+                         const qvg_cache *k, const qvg_cache *v, float scale, void *out,
+                         int32_t out_dtype, float *lse, int32_t *top1, void *workspace,
+                         size_t ws_bytes, void *stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (!k || !v || (!q_bf16 && Nq > 0) || (!out && Nq > 0)) return QVG_ERR_INVALID_ARG;
+    qvg_status s = check_params(p, k->d);
+    if (s != QVG_OK) return s;
+    if ((s = check_cache(p, k)) != QVG_OK) return s;
+    qvg_params pv = *p;
+    pv.flags &= ~QVG_PSAC;  // PSAC corrects keys only
+    if ((s = check_cache(&pv, v)) != QVG_OK) return s;
+    if (k->H != v->H || k->d != v->d || k->n_tokens != v->n_tokens || k->n_chunks != v->n_chunks ||
+        k->capacity_tokens != v->capacity_tokens || k->max_chunks != v->max_chunks)
+        return QVG_ERR_INVALID_ARG;
+    if (Nq < 0 || Hq < 1 || Hq % k->H != 0) return QVG_ERR_INVALID_ARG;
+    if (k->n_tokens == 0) return QVG_ERR_INVALID_ARG;
+    if (out_dtype != QVG_OUT_F32 && out_dtype != QVG_OUT_BF16) return QVG_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return QVG_ERR_INVALID_ARG;
+    const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(k->d));
+    const float scale_log2 = sc * 1.4426950408889634f;
+    static const char *dbg = getenv("QVG_DEBUG_ATTN");  // TEMP: dev comparison only
+    if (getenv("QVG_DEBUG_SIMT") || (dbg && dbg[0] == 's'))
+        return launch_attention(p, static_cast<const uint16_t *>(q_bf16), Nq, Hq, k, v, scale_log2, out,
+                                out_dtype, lse, top1, static_cast<cudaStream_t>(stream));
+    if (dbg && dbg[0] == 't')
+        return launch_attention_tc(p, static_cast<const uint16_t *>(q_bf16), Nq, Hq, k, v, scale_log2, out,
+                                   out_dtype, lse, top1, static_cast<cudaStream_t>(stream));
+    return launch_attention_ws(p, static_cast<const uint16_t *>(q_bf16), Nq, Hq, k, v, scale_log2, out,
+                               out_dtype, lse, top1, static_cast<cudaStream_t>(stream));
+}
+
+qvg_status quantwm_query_stats(const void *q_hist_bf16, int32_t n, int32_t Hq, int32_t H, int32_t d,
+                               int32_t accumulate, float *M, float *w, int64_t *count,
+                               void *stream) {
+    if (!M || !w || !count || (n > 0 && !q_hist_bf16)) return QVG_ERR_INVALID_ARG;
+    if (n < 0 || H < 1 || Hq < 1 || Hq % H != 0 || (accumulate != 0 && accumulate != 1))
+        return QVG_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return QVG_ERR_UNSUPPORTED;
+    if (n == 0 && !accumulate) return QVG_ERR_INVALID_ARG;
+    return launch_query_stats(static_cast<const uint16_t *>(q_hist_bf16), n, Hq, H, d, accumulate, M, w,
+                              count, static_cast<cudaStream_t>(stream));
+}
+
+qvg_status quantwm_psac_basis(const float *M, const int64_t *count, int32_t H, int32_t d,
+                              int32_t rank, float *U, float *eigvals, float *energy_frac,
+                              void *stream) {
+    if (!M || !count || !U || !eigvals || !energy_frac || H < 1) return QVG_ERR_INVALID_ARG;
+    if (rank != QVG_PSAC_RANK) return QVG_ERR_UNSUPPORTED;
+    if (d < rank || d > 128 || d % 2 != 0) return QVG_ERR_UNSUPPORTED;
+    return launch_psac_basis(M, count, H, d, rank, U, eigvals, energy_frac,
+                             static_cast<cudaStream_t>(stream));
+}
+
+qvg_status qvg_get_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QVG_ERR_CUDA;
+    }
+    int err = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbol(&err, g_qvg_error, sizeof(int)) != cudaSuccess) return QVG_ERR_CUDA;
+    if (err != 0 && cudaMemcpyToSymbol(g_qvg_error, &zero, sizeof(int)) != cudaSuccess) return QVG_ERR_CUDA;
+    return static_cast<qvg_status>(err);
+}
+
+}  // extern "C"

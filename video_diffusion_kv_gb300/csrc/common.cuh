@@ -1,0 +1,122 @@
+// common.cuh -- device helpers shared by the libqvg kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../../include/qvg.h"
+
+namespace qvg {
+
+// ---- number formats -------------------------------------------------------
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ float f16_to_f32(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
+}
+__device__ __forceinline__ uint16_t f32_to_f16(float f) {
+    return __half_as_ushort(__float2half_rn(f));
+}
+
+// ---- per-group symmetric quantiser ----------------------------------------
+// Quant VideoGen notes, "core tension": S = max|r| / (2^{b-1} - 1),
+// q = round(r / S); page-1 toy quantiser (scale_mode 1): S = max|r| / 2,
+// q clamped to [-2, 1].  The scale is stored as fp16 (saturated at 65504)
+// and the codes use the stored value; IEEE division, round-half-even.  Each
+// step is a separately rounded IEEE operation (no contraction), so the
+// codes agree bit for bit with any other IEEE implementation of the same
+// definition.
+
+__device__ __forceinline__ uint16_t group_scale_f16(float amax, int bits, int mode) {
+    const float den = mode == 0 ? static_cast<float>((1 << (bits - 1)) - 1) : 2.0f;
+    float S = __fdiv_rn(amax, den);
+    S = fminf(S, 65504.0f);
+    return f32_to_f16(S);
+}
+
+__device__ __forceinline__ int quant_code(float r, float Sp, int bits) {
+    if (!(Sp > 0.0f)) return 0;
+    const float qmax = static_cast<float>((1 << (bits - 1)) - 1);
+    float t = rintf(__fdiv_rn(r, Sp));
+    t = fminf(fmaxf(t, -qmax - 1.0f), qmax);
+    return static_cast<int>(t);
+}
+
+// ---- sticky device error word --------------------------------------------
+// One int per device (defined in api.cu; kernels get its address).  The
+// first error wins; qvg_get_status reads and clears it.
+__device__ __forceinline__ void raise_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace qvg
+
+// ---- host-side launch plumbing (internal, not part of the ABI) ------------
+
+#define QVG_LAUNCH_CHECK()                                        \
+    do {                                                          \
+        if (cudaPeekAtLastError() != cudaSuccess) {               \
+            (void)cudaGetLastError();                             \
+            return QVG_ERR_CUDA;                                  \
+        }                                                         \
+    } while (0)
+
+namespace qvg {
+
+// Device address of this device's error word (looked up once per device).
+int *device_error_word();
+
+// Launchers implemented in the kernel translation units.  All return a
+// qvg_status and only enqueue work on `st`.
+qvg_status launch_kmeans_init(const uint16_t *g, int N, int H, int d, int C, int Ce,
+                              uint64_t seed, int chunk, int stage,
+                              uint16_t *cent, size_t cent_head_stride, cudaStream_t st);
+qvg_status launch_centroid_norms(const uint16_t *cent, size_t cent_head_stride, int H,
+                                 int C, int d, const float *w, float *cnorm, cudaStream_t st);
+qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d,
+                                const uint16_t *cent, size_t cent_head_stride, int Ce,
+                                const float *cnorm, int C, const float *w, int32_t *ids,
+                                cudaStream_t st);
+qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int d,
+                                const int32_t *ids, uint16_t *cent, size_t cent_head_stride,
+                                int Ce, int C, const float *w, float *cnorm, cudaStream_t st);
+qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, int d,
+                                 const uint16_t *cent, size_t cent_head_stride, int C,
+                                 const int32_t *ids, int bits, int group, int mode,
+                                 uint8_t *codes, uint16_t *scales, uint8_t *ids_out,
+                                 size_t slot_head_stride, float *delta_out,
+                                 uint16_t *gbf_out, const float *psac_U, int8_t *psac_p,
+                                 uint16_t *psac_s, size_t psac_head_stride, cudaStream_t st);
+qvg_status launch_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start,
+                              int32_t *chunk_len, int32_t *tile_chunk, cudaStream_t st);
+qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, int ntok,
+                             void *out, int out_dtype, cudaStream_t st);
+qvg_status launch_attention(const qvg_params *p, const uint16_t *q, int Nq, int Hq,
+                            const qvg_cache *k, const qvg_cache *v, float scale_log2,
+                            void *out, int out_dtype, float *lse, int32_t *top1,
+                            cudaStream_t st);
+qvg_status launch_attention_tc(const qvg_params *p, const uint16_t *q, int Nq, int Hq,
+                               const qvg_cache *k, const qvg_cache *v, float scale_log2,
+                               void *out, int out_dtype, float *lse, int32_t *top1,
+                               cudaStream_t st);
+qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, int Hq,
+                               const qvg_cache *k, const qvg_cache *v, float scale_log2,
+                               void *out, int out_dtype, float *lse, int32_t *top1,
+                               cudaStream_t st);
+qvg_status launch_query_stats(const uint16_t *q, int n, int Hq, int H, int d, int accumulate,
+                              float *M, float *w, int64_t *count, cudaStream_t st);
+qvg_status launch_psac_basis(const float *M, const int64_t *count, int H, int d, int rank,
+                             float *U, float *eig, float *frac, cudaStream_t st);
+
+}  // namespace qvg

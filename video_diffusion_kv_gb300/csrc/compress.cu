@@ -1,0 +1,625 @@
+// compress.cu -- write path of the compressed KV cache (sm_103a).
+//
+// Quant VideoGen notes, "Semantic-Aware Smoothing": per chunk and head,
+// k-means over the chunk's tokens, subtract each token's centroid, quantise
+// the residual per group; "Progressive Residual Quantization": repeat on the
+// dequantisation error for L stages.  QuantWM write-up, QSAC: weight the
+// clustering distance per channel by history-query activity; PSAC: project
+// the remaining key error on the top-8 query eigenvectors and store it as
+// INT8.
+//
+// Kernels (one chunk, all heads per launch):
+//   k_kmeans_init     seeded systematic pick of C tokens as first centroids
+//   k_centroid_norms  ||c||_w^2 for the assignment score
+//   k_kmeans_assign   score(c) = ||c||_w^2 - 2 x.(w*c), argmin (lowest c on ties)
+//   k_kmeans_update   deterministic segmented mean -> bf16 centroid
+//   k_residual_quant  r = x - c_id, per-group scale, codes, packing, stage
+//                     residual for the next stage, PSAC INT8 projection
+#include "common.cuh"
+#include "umma.cuh"
+
+#include <cstdlib>
+
+namespace qvg {
+
+// ---------------------------------------------------------------------------
+// k-means initialisation.  Reading (the pages leave the start open): a seeded
+// systematic sample, one token in each of C equal strata of the chunk's
+// raster order: idx_c = floor((c * 2^32 + u) * N / (C * 2^32)), with u the
+// top 32 bits of the first SplitMix64 output (Steele, Lea, Flood 2014) from
+// state seed ^ (chunk << 40) ^ (head << 20) ^ stage.
+__device__ __forceinline__ uint64_t splitmix64_first(uint64_t state) {
+    uint64_t z = state + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+template <int D>
+__global__ void k_kmeans_init(const uint16_t *__restrict__ g, int N, int H, int C, int Ce,
+                              uint64_t seed, int chunk, int stage, uint16_t *__restrict__ cent,
+                              size_t hs) {
+    const int h = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t st = seed ^ (static_cast<uint64_t>(chunk) << 40) ^
+                        (static_cast<uint64_t>(h) << 20) ^ static_cast<uint64_t>(stage);
+    const uint64_t u = splitmix64_first(st) >> 32;
+    uint16_t *ch = cent + static_cast<size_t>(h) * hs;
+    for (int c = warp; c < C; c += blockDim.x >> 5) {
+        if (c < Ce) {
+            const uint64_t num = ((static_cast<uint64_t>(c) << 32) + u) * static_cast<uint64_t>(N);
+            const int idx = static_cast<int>(num / (static_cast<uint64_t>(Ce) << 32));
+            const uint16_t *src = g + (static_cast<size_t>(idx) * H + h) * D;
+            for (int j = lane; j < D; j += 32) ch[static_cast<size_t>(c) * D + j] = src[j];
+        } else {
+            for (int j = lane; j < D; j += 32) ch[static_cast<size_t>(c) * D + j] = 0;
+        }
+    }
+}
+
+// ||c||_w^2 (fp32) for every centroid; one warp per (head, centroid).
+template <int D>
+__global__ void k_centroid_norms(const uint16_t *__restrict__ cent, size_t hs, int H, int C,
+                                 const float *__restrict__ w, float *__restrict__ cnorm) {
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= H * C) return;
+    const int h = gw / C, c = gw % C;
+    const uint16_t *row = cent + static_cast<size_t>(h) * hs + static_cast<size_t>(c) * D;
+    float s = 0.0f;
+    for (int j = lane; j < D; j += 32) {
+        const float v = bf16_to_f32(row[j]);
+        const float wj = w ? w[h * D + j] : 1.0f;
+        s = fmaf(wj * v, v, s);
+    }
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) cnorm[h * C + c] = s;
+}
+
+// ---------------------------------------------------------------------------
+// Assignment: id = argmin_c ||c||_w^2 - 2 x.(w*c)  (the token's own ||x||_w^2
+// is common to all c and dropped).  One thread per token, the head's
+// weighted centroids staged in shared memory as fp32.
+template <int D>
+__global__ void __launch_bounds__(128) k_kmeans_assign(const uint16_t *__restrict__ g, int N,
+                                                      int H, const uint16_t *__restrict__ cent,
+                                                      size_t hs, int Ce,
+                                                      const float *__restrict__ cnorm, int C,
+                                                      const float *__restrict__ w,
+                                                      int32_t *__restrict__ ids) {
+    extern __shared__ float smem[];
+    float *wc = smem;                       // [Ce][D]
+    float *cn = smem + static_cast<size_t>(Ce) * D;  // [Ce]
+    const int h = blockIdx.y;
+    const uint16_t *ch = cent + static_cast<size_t>(h) * hs;
+    for (int i = threadIdx.x; i < Ce * D; i += blockDim.x) {
+        const int j = i % D;
+        const float wj = w ? w[h * D + j] : 1.0f;
+        wc[i] = wj * bf16_to_f32(ch[i]);
+    }
+    for (int i = threadIdx.x; i < Ce; i += blockDim.x) cn[i] = cnorm[h * C + i];
+    __syncthreads();
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    float x[D];
+    const uint16_t *xr = g + (static_cast<size_t>(n) * H + h) * D;
+#pragma unroll
+    for (int j = 0; j < D; j += 8) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(xr + j);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[j + 2 * k] = __uint_as_float(wv[k] << 16);
+            x[j + 2 * k + 1] = __uint_as_float(wv[k] & 0xffff0000u);
+        }
+    }
+    float best = INFINITY;
+    int arg = 0;
+    for (int c = 0; c < Ce; ++c) {
+        const float *cc = wc + static_cast<size_t>(c) * D;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < D; j += 4) {
+            a0 = fmaf(x[j], cc[j], a0);
+            a1 = fmaf(x[j + 1], cc[j + 1], a1);
+            a2 = fmaf(x[j + 2], cc[j + 2], a2);
+            a3 = fmaf(x[j + 3], cc[j + 3], a3);
+        }
+        const float s = fmaf(-2.0f, (a0 + a1) + (a2 + a3), cn[c]);
+        if (s < best) {
+            best = s;
+            arg = c;
+        }
+    }
+    ids[static_cast<size_t>(h) * N + n] = arg;
+}
+
+// ---------------------------------------------------------------------------
+// Assignment on the tensor cores: one CTA per (128-token tile, head).
+// D[128 x Np] = X_tile (bf16, 128 x D) * B^T with B = the head's centroids
+// (bf16, exact) or, with QSAC weights, the weighted centroids w*c split into
+// a bf16 pair hi + lo (|w c - hi - lo| <= 2^-18 |w c|), accumulated in fp32
+// in tensor memory by tcgen05.mma (M=128, N=Np = Ce rounded up to 16,
+// K=16 per instruction).  Epilogue: thread r owns token row r, reads its Np
+// accumulators from TMEM and takes argmin_c ||c||_w^2 - 2 acc_c (lowest c on
+// ties).  Every wait is bounded; on expiry the CTA records QVG_ERR_TIMEOUT.
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+
+template <int D, int P>
+__global__ void __launch_bounds__(128) k_kmeans_assign_tc(const uint16_t *__restrict__ g, int N, int H,
+                                                         const uint16_t *__restrict__ cent, size_t hs,
+                                                         int Ce, int Np, const float *__restrict__ cnorm,
+                                                         int C, const float *__restrict__ w,
+                                                         int32_t *__restrict__ ids, int *err) {
+    constexpr int KB = D / 64;                       // 64-element K blocks
+    extern __shared__ __align__(1024) uint8_t sm_raw[];
+    // swizzle atoms need a 1024-byte aligned base (the launch adds 1 KB slack)
+    uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
+    uint8_t *As = sm;                                // KB x [128 rows x 128 B]
+    uint8_t *Bs = As + KB * 128 * 128;               // P x KB x [Np rows x 128 B]
+    float *cn = reinterpret_cast<float *>(Bs + static_cast<size_t>(P) * KB * Np * 128);
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y, n0 = blockIdx.x * 128;
+
+    // token tile -> swizzled K-major bf16
+    for (int i = tid; i < 128 * (D / 8); i += 128) {
+        const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (n0 + r < N) v = *reinterpret_cast<const uint4 *>(g + (static_cast<size_t>(n0 + r) * H + h) * D + ci * 8);
+        *reinterpret_cast<uint4 *>(As + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+    }
+    // centroids (or weighted hi/lo pair) -> swizzled K-major bf16
+    const uint16_t *ch = cent + static_cast<size_t>(h) * hs;
+    for (int i = tid; i < Np * (D / 8); i += 128) {
+        const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
+        uint4 v = make_uint4(0, 0, 0, 0), v2 = make_uint4(0, 0, 0, 0);
+        if (r < Ce) {
+            v = *reinterpret_cast<const uint4 *>(ch + static_cast<size_t>(r) * D + ci * 8);
+            if constexpr (P == 2) {
+                uint32_t in[4] = {v.x, v.y, v.z, v.w}, hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t hpair = 0, lpair = 0;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int j = ci * 8 + 2 * k + half;
+                        const float cv = bf16_to_f32(static_cast<uint16_t>(in[k] >> (16 * half)));
+                        const float wv = w[h * D + j] * cv;
+                        const uint16_t hb = f32_to_bf16(wv);
+                        const uint16_t lb = f32_to_bf16(wv - bf16_to_f32(hb));
+                        hpair |= static_cast<uint32_t>(hb) << (16 * half);
+                        lpair |= static_cast<uint32_t>(lb) << (16 * half);
+                    }
+                    hi[k] = hpair;
+                    lo[k] = lpair;
+                }
+                v = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                v2 = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        const size_t off = static_cast<size_t>(kb) * Np * 128 + r * 128 + ((c ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4 *>(Bs + off) = v;
+        if constexpr (P == 2) *reinterpret_cast<uint4 *>(Bs + static_cast<size_t>(KB) * Np * 128 + off) = v2;
+    }
+    for (int i = tid; i < Np; i += 128) cn[i] = i < Ce ? cnorm[h * C + i] : 0.0f;
+    umma::fence_proxy_async_smem();
+    if (warp == 0) {
+        umma::tmem_alloc(&tmem_base, Np <= 32 ? 32 : (Np <= 64 ? 64 : (Np <= 128 ? 128 : 256)));
+        umma::tmem_relinquish();
+    }
+    if (tid == 0) {
+        umma::mbar_init(&bar, 1);
+        umma::fence_barrier_init();
+    }
+    umma::tc_fence_before();
+    __syncthreads();
+    umma::tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    const uint32_t ncols = Np <= 32 ? 32 : (Np <= 64 ? 64 : (Np <= 128 ? 128 : 256));
+    if (tid == 0) {
+        const uint32_t idesc = umma::idesc_f16(128, Np, 1);
+        const uint32_t a0 = umma::smem_u32(As), b0 = umma::smem_u32(Bs);
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s) {
+                const uint64_t ad = umma::desc_sw128(a0 + (s >> 2) * 16384 + (s & 3) * 32);
+                const uint64_t bd = umma::desc_sw128(b0 + (p * KB + (s >> 2)) * Np * 128 + (s & 3) * 32);
+                umma::mma_f16(tmem, ad, bd, idesc, (p | s) != 0);
+            }
+        umma::mma_commit(&bar);
+    }
+    const bool ok = umma::mbar_wait(&bar, 0, kWaitNs);
+    umma::tc_fence_after();
+    if (!ok) {
+        if (tid == 0) raise_error(err, QVG_ERR_TIMEOUT);
+        umma::mbar_wait(&bar, 0, kWaitNs);  // let an in-flight MMA drain before freeing TMEM
+    } else {
+        const int r = warp * 32 + lane;
+        float best = INFINITY;
+        int arg = 0;
+        for (int c0 = 0; c0 < Np; c0 += 32) {
+            uint32_t acc[32];
+            umma::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, acc);
+            umma::tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int c = c0 + k;
+                const float s = fmaf(-2.0f, __uint_as_float(acc[k]), cn[c < Np ? c : 0]);
+                if (c < Ce && s < best) {
+                    best = s;
+                    arg = c;
+                }
+            }
+        }
+        if (n0 + r < N) ids[static_cast<size_t>(h) * N + n0 + r] = arg;
+    }
+    umma::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(tmem, ncols);
+}
+
+// ---------------------------------------------------------------------------
+// Update: each centroid becomes the mean of its members' stage input (fp32
+// sums in a fixed order: ascending token order inside each warp, warps
+// combined in index order), rounded to bf16; empty clusters keep their
+// value.  A diagonal weight leaves the minimiser at the plain mean.
+// One CTA (4 warps) per (head, 8 clusters).
+template <typename T> struct RowLoad;
+template <> struct RowLoad<uint16_t> {
+    template <int E>
+    __device__ static void load(const uint16_t *p, float (&v)[E]) {
+        if constexpr (E == 4) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(p);
+            v[0] = __uint_as_float(u.x << 16);
+            v[1] = __uint_as_float(u.x & 0xffff0000u);
+            v[2] = __uint_as_float(u.y << 16);
+            v[3] = __uint_as_float(u.y & 0xffff0000u);
+        } else {
+            const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+            v[0] = __uint_as_float(u << 16);
+            v[1] = __uint_as_float(u & 0xffff0000u);
+        }
+    }
+};
+template <> struct RowLoad<float> {
+    template <int E>
+    __device__ static void load(const float *p, float (&v)[E]) {
+        if constexpr (E == 4) {
+            const float4 u = *reinterpret_cast<const float4 *>(p);
+            v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+        } else {
+            const float2 u = *reinterpret_cast<const float2 *>(p);
+            v[0] = u.x; v[1] = u.y;
+        }
+    }
+};
+
+template <int D, typename TIn>
+__global__ void __launch_bounds__(128) k_kmeans_update(const TIn *__restrict__ xin, int N, int H,
+                                                      const int32_t *__restrict__ ids,
+                                                      uint16_t *__restrict__ cent, size_t hs,
+                                                      int Ce, const float *__restrict__ w,
+                                                      float *__restrict__ cnorm, int C) {
+    constexpr int E = D / 32;
+    constexpr int KC = 8;  // clusters per CTA
+    __shared__ float part[4][KC][D];
+    __shared__ int pcnt[4][KC];
+    const int h = blockIdx.y, c0 = blockIdx.x * KC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float acc[KC][E];
+    int cnt[KC];
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+        cnt[k] = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[k][e] = 0.0f;
+    }
+    const int nbatch = ceil_div(N, 32);
+    const int32_t *hid = ids + static_cast<size_t>(h) * N;
+    for (int b = warp; b < nbatch; b += 4) {
+        const int n = b * 32 + lane;
+        const int id = n < N ? hid[n] : -1;
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            unsigned m = __ballot_sync(0xffffffffu, id == c0 + k);
+            cnt[k] += __popc(m);
+            while (m) {
+                const int src = __ffs(m) - 1;
+                m &= m - 1;
+                const int nn = b * 32 + src;
+                float v[E];
+                RowLoad<TIn>::template load<E>(xin + (static_cast<size_t>(nn) * H + h) * D + lane * E, v);
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[k][e] += v[e];
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) part[warp][k][lane * E + e] = acc[k][e];
+        if (lane == 0) pcnt[warp][k] = cnt[k];
+    }
+    __syncthreads();
+    // warp w finalises clusters 2w and 2w+1 of this CTA
+    for (int kk = 0; kk < 2; ++kk) {
+        const int k = warp * 2 + kk, c = c0 + k;
+        if (c >= Ce) continue;
+        const int total = pcnt[0][k] + pcnt[1][k] + pcnt[2][k] + pcnt[3][k];
+        if (total == 0) continue;
+        uint16_t *row = cent + static_cast<size_t>(h) * hs + static_cast<size_t>(c) * D;
+        float nrm = 0.0f;
+        for (int j = lane; j < D; j += 32) {
+            const float s = ((part[0][k][j] + part[1][k][j]) + part[2][k][j]) + part[3][k][j];
+            const float mean = __fdiv_rn(s, static_cast<float>(total));
+            const uint16_t cb = f32_to_bf16(mean);
+            row[j] = cb;
+            const float cv = bf16_to_f32(cb);
+            const float wj = w ? w[h * D + j] : 1.0f;
+            nrm = fmaf(wj * cv, cv, nrm);
+        }
+        for (int o = 16; o > 0; o >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o);
+        if (lane == 0) cnorm[h * C + c] = nrm;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Residual quantisation of one stage: one warp per (token, head) row, lane i
+// holding channels [i*E, i*E + E), E = D/32.  Writes codes, fp16 scales and
+// the cluster id; optionally the next stage's input X_{l+1} = X_l - deq (fp32
+// and its bf16 rounding, the next clustering operand); optionally (last stage
+// of a key chunk with PSAC) the INT8 projection of X_{L+1} on the basis U.
+template <int D, int BITS, typename TIn>
+__global__ void __launch_bounds__(256) k_residual_quant(
+    const TIn *__restrict__ xin, int N, int H, const uint16_t *__restrict__ cent, size_t hs, int C,
+    const int32_t *__restrict__ ids, int group, int mode, uint8_t *__restrict__ codes,
+    uint16_t *__restrict__ scales, uint8_t *__restrict__ ids_out, size_t shs,
+    float *__restrict__ delta_out, uint16_t *__restrict__ gbf_out, const float *__restrict__ psacU,
+    int8_t *__restrict__ psac_p, uint16_t *__restrict__ psac_s, size_t phs) {
+    constexpr int E = D / 32;
+    constexpr int NB = D * BITS / 8;  // code bytes per row
+    __shared__ float esh[8][D];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lpg = group / E;  // lanes per quantisation group (power of two)
+    const int ng = D / group;
+    const int nrows = N * H;
+    for (int row = blockIdx.x * 8 + warp; row < nrows; row += gridDim.x * 8) {
+        const int n = row / H, h = row % H;
+        const int id = C > 0 ? ids[static_cast<size_t>(h) * N + n] : 0;
+        float x[E], c[E], r[E];
+        RowLoad<TIn>::template load<E>(xin + static_cast<size_t>(row) * D + lane * E, x);
+        if (C > 0) {
+            const uint16_t *cr = cent + static_cast<size_t>(h) * hs + static_cast<size_t>(id) * D + lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) c[e] = bf16_to_f32(cr[e]);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            r[e] = C > 0 ? __fsub_rn(x[e], c[e]) : x[e];
+            amax = fmaxf(amax, fabsf(r[e]));
+        }
+        for (int o = lpg >> 1; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const uint16_t sb = group_scale_f16(amax, BITS, mode);
+        const float Sp = f16_to_f32(sb);
+        uint32_t packed = 0;
+        float dl[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int q = quant_code(r[e], Sp, BITS);
+            packed |= static_cast<uint32_t>(q + (1 << (BITS - 1))) << (e * BITS);
+            const float rh = __fmul_rn(Sp, static_cast<float>(q));
+            const float deq = C > 0 ? __fadd_rn(rh, c[e]) : rh;
+            dl[e] = __fsub_rn(x[e], deq);
+        }
+        const size_t srow = static_cast<size_t>(h) * shs + n;
+        uint8_t *crow = codes + srow * NB;
+        constexpr int LANE_BITS = E * BITS;
+        if constexpr (LANE_BITS == 8) {
+            crow[lane] = static_cast<uint8_t>(packed);
+        } else if constexpr (LANE_BITS == 16) {
+            reinterpret_cast<uint16_t *>(crow)[lane] = static_cast<uint16_t>(packed);
+        } else {  // 4 bits per lane: pair lanes into one byte
+            const uint32_t hi = __shfl_down_sync(0xffffffffu, packed, 1);
+            if ((lane & 1) == 0) crow[lane >> 1] = static_cast<uint8_t>(packed | (hi << 4));
+        }
+        if ((lane % lpg) == 0) scales[srow * ng + lane / lpg] = sb;
+        if (lane == 0 && ids_out) ids_out[srow] = static_cast<uint8_t>(id);  // no ids without centroids (C = 0)
+        if (delta_out) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                delta_out[static_cast<size_t>(row) * D + lane * E + e] = dl[e];
+                if (gbf_out) gbf_out[static_cast<size_t>(row) * D + lane * E + e] = f32_to_bf16(dl[e]);
+            }
+        }
+        if (psacU) {
+            // P_k = sum_j E_j U[j][k]: fp32 fused multiply-add in ascending j.
+#pragma unroll
+            for (int e = 0; e < E; ++e) esh[warp][lane * E + e] = dl[e];
+            __syncwarp();
+            const float *Uh = psacU + static_cast<size_t>(h) * D * QVG_PSAC_RANK;
+            float P = 0.0f;
+            if (lane < QVG_PSAC_RANK) {
+                for (int j = 0; j < D; ++j) P = fmaf(esh[warp][j], Uh[j * QVG_PSAC_RANK + lane], P);
+            }
+            float pa = lane < QVG_PSAC_RANK ? fabsf(P) : 0.0f;
+            for (int o = 4; o > 0; o >>= 1) pa = fmaxf(pa, __shfl_xor_sync(0xffffffffu, pa, o));
+            const uint16_t psb = f32_to_f16(fminf(__fdiv_rn(pa, 127.0f), 65504.0f));
+            const float pSp = f16_to_f32(psb);
+            if (lane < QVG_PSAC_RANK) {
+                int qp = 0;
+                if (pSp > 0.0f) {
+                    float t = rintf(__fdiv_rn(P, pSp));
+                    t = fminf(fmaxf(t, -127.0f), 127.0f);
+                    qp = static_cast<int>(t);
+                }
+                psac_p[(static_cast<size_t>(h) * phs + n) * QVG_PSAC_RANK + lane] = static_cast<int8_t>(qp);
+            }
+            if (lane == 0) psac_s[static_cast<size_t>(h) * phs + n] = psb;
+            __syncwarp();
+        }
+    }
+}
+
+__global__ void k_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start, int32_t *chunk_len,
+                              int32_t *tile_chunk) {
+    if (threadIdx.x == 0) {
+        chunk_start[chunk] = slot0;
+        chunk_len[chunk] = N;
+    }
+    const int t0 = slot0 / QVG_TILE, nt = ceil_div(N, QVG_TILE);
+    for (int t = threadIdx.x; t < nt; t += blockDim.x) tile_chunk[t0 + t] = chunk;
+}
+
+// ---------------------------------------------------------------------------
+// Launchers.
+
+static int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 152;
+    }
+    return n;
+}
+
+qvg_status launch_kmeans_init(const uint16_t *g, int N, int H, int d, int C, int Ce, uint64_t seed,
+                              int chunk, int stage, uint16_t *cent, size_t hs, cudaStream_t st) {
+    if (d == 64)
+        k_kmeans_init<64><<<H, 256, 0, st>>>(g, N, H, C, Ce, seed, chunk, stage, cent, hs);
+    else
+        k_kmeans_init<128><<<H, 256, 0, st>>>(g, N, H, C, Ce, seed, chunk, stage, cent, hs);
+    QVG_LAUNCH_CHECK();
+    return QVG_OK;
+}
+
+qvg_status launch_centroid_norms(const uint16_t *cent, size_t hs, int H, int C, int d,
+                                 const float *w, float *cnorm, cudaStream_t st) {
+    const int warps = H * C, blocks = ceil_div(warps * 32, 256);
+    if (d == 64)
+        k_centroid_norms<64><<<blocks, 256, 0, st>>>(cent, hs, H, C, w, cnorm);
+    else
+        k_centroid_norms<128><<<blocks, 256, 0, st>>>(cent, hs, H, C, w, cnorm);
+    QVG_LAUNCH_CHECK();
+    return QVG_OK;
+}
+
+template <int D, int P>
+static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t *cent, size_t hs, int Ce,
+                                 const float *cnorm, int C, const float *w, int32_t *ids, cudaStream_t st) {
+    const int Np = std::max(16, ceil_div(Ce, 16) * 16);
+    constexpr int KB = D / 64;
+    size_t smem = static_cast<size_t>(KB) * 128 * 128 + static_cast<size_t>(P) * KB * Np * 128 + Np * 4;
+    // at least ~100 KB so that at most two CTAs (2 x 256 TMEM columns) share an SM
+    smem = std::max<size_t>(smem, 100 * 1024) + 1024;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_kmeans_assign_tc<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        attr = true;
+    }
+    dim3 grid(ceil_div(N, 128), H);
+    k_kmeans_assign_tc<D, P><<<grid, 128, smem, st>>>(g, N, H, cent, hs, Ce, Np, cnorm, C, w, ids,
+                                                      device_error_word());
+    QVG_LAUNCH_CHECK();
+    return QVG_OK;
+}
+
+template <int D>
+static qvg_status assign_impl(const uint16_t *g, int N, int H, const uint16_t *cent, size_t hs,
+                              int Ce, const float *cnorm, int C, const float *w, int32_t *ids,
+                              cudaStream_t st) {
+    const size_t smem = (static_cast<size_t>(Ce) * D + Ce) * sizeof(float);
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_kmeans_assign<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (QVG_MAX_CLUSTERS * D + QVG_MAX_CLUSTERS) * 4);
+        attr = true;
+    }
+    dim3 grid(ceil_div(N, 128), H);
+    k_kmeans_assign<D><<<grid, 128, smem, st>>>(g, N, H, cent, hs, Ce, cnorm, C, w, ids);
+    QVG_LAUNCH_CHECK();
+    return QVG_OK;
+}
+
+qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d, const uint16_t *cent,
+                                size_t hs, int Ce, const float *cnorm, int C, const float *w,
+                                int32_t *ids, cudaStream_t st) {
+    static const bool dbg_simt = getenv("QVG_DEBUG_SIMT") != nullptr;  // TEMP: dev comparison only
+    if (dbg_simt)
+        return d == 64 ? assign_impl<64>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st)
+                       : assign_impl<128>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st);
+    if (d == 64)
+        return w ? assign_tc_impl<64, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st)
+                 : assign_tc_impl<64, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st);
+    return w ? assign_tc_impl<128, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st)
+             : assign_tc_impl<128, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st);
+}
+
+qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int d,
+                                const int32_t *ids, uint16_t *cent, size_t hs, int Ce, int C,
+                                const float *w, float *cnorm, cudaStream_t st) {
+    dim3 grid(ceil_div(Ce, 8), H);
+    if (d == 64) {
+        if (xin_f32)
+            k_kmeans_update<64, float><<<grid, 128, 0, st>>>(static_cast<const float *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C);
+        else
+            k_kmeans_update<64, uint16_t><<<grid, 128, 0, st>>>(static_cast<const uint16_t *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C);
+    } else {
+        if (xin_f32)
+            k_kmeans_update<128, float><<<grid, 128, 0, st>>>(static_cast<const float *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C);
+        else
+            k_kmeans_update<128, uint16_t><<<grid, 128, 0, st>>>(static_cast<const uint16_t *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C);
+    }
+    QVG_LAUNCH_CHECK();
+    return QVG_OK;
+}
+
+template <int D, int BITS>
+static void rq_dispatch(const void *xin, bool f32, int N, int H, const uint16_t *cent, size_t hs,
+                        int C, const int32_t *ids, int group, int mode, uint8_t *codes,
+                        uint16_t *scales, uint8_t *ids_out, size_t shs, float *delta_out,
+                        uint16_t *gbf_out, const float *U, int8_t *pp, uint16_t *ps, size_t phs,
+                        cudaStream_t st) {
+    const int rows = N * H;
+    const int blocks = std::min(ceil_div(rows, 8), sm_count() * 16);
+    if (f32)
+        k_residual_quant<D, BITS, float><<<blocks, 256, 0, st>>>(
+            static_cast<const float *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
+            ids_out, shs, delta_out, gbf_out, U, pp, ps, phs);
+    else
+        k_residual_quant<D, BITS, uint16_t><<<blocks, 256, 0, st>>>(
+            static_cast<const uint16_t *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
+            ids_out, shs, delta_out, gbf_out, U, pp, ps, phs);
+}
+
+qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, int d,
+                                 const uint16_t *cent, size_t hs, int C, const int32_t *ids,
+                                 int bits, int group, int mode, uint8_t *codes, uint16_t *scales,
+                                 uint8_t *ids_out, size_t shs, float *delta_out,
+                                 uint16_t *gbf_out, const float *U, int8_t *pp, uint16_t *ps,
+                                 size_t phs, cudaStream_t st) {
+    if (d == 64 && bits == 2)
+        rq_dispatch<64, 2>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, st);
+    else if (d == 64)
+        rq_dispatch<64, 4>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, st);
+    else if (bits == 2)
+        rq_dispatch<128, 2>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, st);
+    else
+        rq_dispatch<128, 4>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, st);
+    QVG_LAUNCH_CHECK();
+    return QVG_OK;
+}
+
+qvg_status launch_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start, int32_t *chunk_len,
+                              int32_t *tile_chunk, cudaStream_t st) {
+    k_chunk_table<<<1, 256, 0, st>>>(chunk, slot0, N, chunk_start, chunk_len, tile_chunk);
+    QVG_LAUNCH_CHECK();
+    return QVG_OK;
+}
+
+}  // namespace qvg
