@@ -354,11 +354,11 @@ def run_own(args):
                      "frac_hbm": (in_bytes / (ms_comp / 1e3) / 1e9) / peaks["hbm_gbs"],
                      "gflop": 2.0 * 2 * w.N * w.C * w.d * (w.iters + 1) * w.H / 1e9},
         "attention": {"ms": ms_attn, "tok/s": w.Nq / (ms_attn / 1e3), "TFLOP/s": achieved},
-        "roofline": {"kernel": "k_attention_tc", "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": "k_attention_ws", "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": None,
                      "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json); fp16 runs at the same rate" % peak_src,
-                     "mma_flops_per_algorithmic_flop": 1.5},
+                     "mma_flops_per_algorithmic_flop": 1.0},
         "clocks": clk,
         "e2e": {"value": ws * w.Nq / (e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e},

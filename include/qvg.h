@@ -261,6 +261,12 @@ qvg_status quantwm_psac_basis(const float *M, const int64_t *count, int32_t H,
                               void *stream);
 
 /*
+ * Name of the CUDA error behind the latest QVG_ERR_CUDA returned to the
+ * calling host thread ("cudaSuccess" if none); static storage.
+ */
+const char *qvg_last_cuda_error(void);
+
+/*
  * Synchronise with the current device, then return and clear its latched
  * device-side error (QVG_OK if none).  Also returns QVG_ERR_CUDA when a
  * CUDA error is pending.

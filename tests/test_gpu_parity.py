@@ -324,7 +324,9 @@ def test_query_stats_and_basis():
     for h in range(w.H):
         dots = np.einsum("dk,dk->k", Ug[h], Uo[h])
         assert dots.min() > 1 - 1e-4, dots
-        np.testing.assert_allclose(Ug[h].T @ Ug[h], np.eye(8), atol=1e-5)
+        # fp32 Jacobi: each of ~10 sweeps applies d-1 rotations to every
+        # column pair, so orthonormality drifts by ~sweeps * d * 2^-24 ~ 1e-4
+        np.testing.assert_allclose(Ug[h].T @ Ug[h], np.eye(8), atol=2e-4)
     assert 0.69 < frac.cpu().numpy().min() and frac.cpu().numpy().max() < 0.75
 
 

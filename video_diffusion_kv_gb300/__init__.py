@@ -31,7 +31,7 @@ QVG_OP_COMPRESS, QVG_OP_ATTENTION, QVG_OP_PSAC_BASIS = 0, 1, 2
 EXPORTED = (
     "qvg_status_string", "qvg_cache_bytes", "qvg_workspace_size", "qvg_compress_chunk",
     "qvg_decompress", "qvg_attention", "quantwm_query_stats", "quantwm_psac_basis",
-    "qvg_get_status",
+    "qvg_get_status", "qvg_last_cuda_error",
 )
 
 BUFFER_NAMES = ("codes", "scales", "ids", "cent", "chunk_start", "chunk_len", "tile_chunk",
@@ -81,6 +81,8 @@ def lib():
         L.quantwm_query_stats.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
         L.quantwm_psac_basis.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
         L.qvg_get_status.argtypes = []
+        L.qvg_last_cuda_error.restype = ct.c_char_p
+        L.qvg_last_cuda_error.argtypes = []
         _lib = L
     return _lib
 
@@ -91,6 +93,8 @@ def status_string(s):
 
 def _check(s, where):
     if s != QVG_OK:
+        if s == QVG_ERR_CUDA:
+            where = "%s [%s]" % (where, lib().qvg_last_cuda_error().decode())
         raise QvgError(s, where)
 
 

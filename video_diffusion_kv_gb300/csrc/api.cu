@@ -2,12 +2,14 @@
 // workspace carving and the launch sequence of each call.
 #include <algorithm>
 #include <cmath>
-#include <cstdlib>
 
 #include "common.cuh"
 
 namespace qvg {
 __device__ int g_qvg_error = 0;
+
+static thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+void note_cuda_error(cudaError_t e) { t_last_cuda_error = e; }
 
 int *device_error_word() {
     static int *ptr[64] = {};
@@ -181,9 +183,11 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
         uint16_t *cent = C > 0 ? cache->cent + (static_cast<size_t>(l) * H * cache->max_chunks + chunk) * C * d : nullptr;
         if (C > 0) {
             if (!(p->flags & QVG_GIVEN_CENTROIDS)) {
-                if ((s = launch_kmeans_init(g, N, H, d, C, Ce, p->seed, chunk, l, cent, cent_hs, st)) != QVG_OK) return s;
+                if ((s = launch_kmeans_init(g, N, H, d, C, Ce, p->seed, chunk, l, cent, cent_hs, w, ws.cnorm, st)) != QVG_OK)
+                    return s;
+            } else if ((s = launch_centroid_norms(cent, cent_hs, H, C, d, w, ws.cnorm, st)) != QVG_OK) {
+                return s;
             }
-            if ((s = launch_centroid_norms(cent, cent_hs, H, C, d, w, ws.cnorm, st)) != QVG_OK) return s;
             for (int it = 0; it < p->iters; ++it) {
                 if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.ids, st)) != QVG_OK) return s;
                 if ((s = launch_kmeans_update(xin, f32, N, H, d, ws.ids, cent, cent_hs, Ce, C, w, ws.cnorm, st)) != QVG_OK) return s;
@@ -241,13 +245,6 @@ qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq, in
     if (!std::isfinite(scale)) return QVG_ERR_INVALID_ARG;
     const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(k->d));
     const float scale_log2 = sc * 1.4426950408889634f;
-    static const char *dbg = getenv("QVG_DEBUG_ATTN");  // TEMP: dev comparison only
-    if (getenv("QVG_DEBUG_SIMT") || (dbg && dbg[0] == 's'))
-        return launch_attention(p, static_cast<const uint16_t *>(q_bf16), Nq, Hq, k, v, scale_log2, out,
-                                out_dtype, lse, top1, static_cast<cudaStream_t>(stream));
-    if (dbg && dbg[0] == 't')
-        return launch_attention_tc(p, static_cast<const uint16_t *>(q_bf16), Nq, Hq, k, v, scale_log2, out,
-                                   out_dtype, lse, top1, static_cast<cudaStream_t>(stream));
     return launch_attention_ws(p, static_cast<const uint16_t *>(q_bf16), Nq, Hq, k, v, scale_log2, out,
                                out_dtype, lse, top1, static_cast<cudaStream_t>(stream));
 }
@@ -274,9 +271,13 @@ qvg_status quantwm_psac_basis(const float *M, const int64_t *count, int32_t H, i
                              static_cast<cudaStream_t>(stream));
 }
 
+const char *qvg_last_cuda_error(void) { return cudaGetErrorName(t_last_cuda_error); }
+
 qvg_status qvg_get_status(void) {
-    if (cudaDeviceSynchronize() != cudaSuccess) {
+    const cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
         (void)cudaGetLastError();
+        note_cuda_error(e);
         return QVG_ERR_CUDA;
     }
     int err = 0;

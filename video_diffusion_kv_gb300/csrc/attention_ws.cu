@@ -9,11 +9,13 @@
 //
 // One CTA = two 128-row query tiles of one query head (ping-pong, so the
 // tensor core computes one tile's S while the other tile's softmax runs).
-// Warp roles (17 warps):
+// Warp roles (16 warps, 128 registers per thread):
 //   0-3, 4-7   softmax + epilogue of query tile 0 / 1 (thread = query row)
 //   8-11       K producers: rebuild a 128-slot K_hat tile (thread = slot)
-//   12-15      V producers: rebuild V_hat^T (thread = 8 slots x D/8 channels)
-//   16         TMEM owner; lane 0 issues every tcgen05.mma
+//   12-15      V producers: rebuild V_hat^T (thread = 8 slots x D/8 channels);
+//              warp 12 owns the TMEM allocation and its lane 0 issues every
+//              tcgen05.mma (S_0, S_1 before producing the V tile, which must
+//              wait for the previous PV products anyway; PV_0, PV_1 after)
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
 // O1 [384,384+D), fp32.  Per cache tile t:
 //   S_i = Q_i K_t^T              (M=128, N=128 slots, K=D; fp16 operands)
@@ -50,7 +52,7 @@ struct AttnWsArgs {
 
 namespace ws {
 
-constexpr int kWarps = 17;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescale = 8.0f;
@@ -144,10 +146,98 @@ __device__ __forceinline__ void rebuild8(const AttnWsArgs &a, const uint8_t *cod
     }
 }
 
+// One-stage fast path: the loads of a slot's 64-channel half are issued
+// before any arithmetic (code bits, scales, cluster id, then the 128-byte
+// bf16 centroid piece), so a producer thread exposes its memory latency once
+// per half rather than once per 8 channels.  K_hat = fma(S, q, c) in fp32,
+// rounded to fp16; out gets 32 packed half2 words (channels kb*64 ..).
+template <int D, int BITS>
+__device__ __forceinline__ void rebuild_half_fast(const AttnWsArgs &a, const uint8_t *codes,
+                                                  const uint16_t *scales, const uint8_t *ids,
+                                                  const uint16_t *cent, int h, int chunk, int slot, int kb,
+                                                  uint32_t (&out)[32]) {
+    constexpr int NB = D * BITS / 8;
+    constexpr int HB = 64 * BITS / 8;      // code bytes of a 64-channel half: 16 (INT2) or 32 (INT4)
+    const int ng = D / a.group;
+    const size_t srow = static_cast<size_t>(h) * a.cap + slot;
+    uint4 cw[HB / 16];
+#pragma unroll
+    for (int i = 0; i < HB / 16; ++i) cw[i] = *reinterpret_cast<const uint4 *>(codes + srow * NB + kb * HB + 16 * i);
+    float S[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) S[i] = f16_to_f32(scales[srow * ng + (kb * 64 + 8 * i) / a.group]);
+    uint4 cr[8];
+    if (a.C > 0) {
+        const uint16_t *row = cent + (static_cast<size_t>(h) * a.max_chunks + chunk) * a.C * D +
+                              static_cast<size_t>(ids[srow]) * D + kb * 64;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cr[i] = *reinterpret_cast<const uint4 *>(row + 8 * i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cr[i] = make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t *cb = reinterpret_cast<const uint32_t *>(cw);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t bits = static_cast<uint32_t>((cb[(8 * i * BITS) / 32] >> ((8 * i * BITS) % 32)) &
+                                                    ((1ull << (8 * BITS)) - 1ull));
+        const uint32_t c4[4] = {cr[i].x, cr[i].y, cr[i].z, cr[i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int q0 = static_cast<int>((bits >> (2 * e * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
+            const int q1 = static_cast<int>((bits >> ((2 * e + 1) * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
+            const float v0 = fmaf(S[i], static_cast<float>(q0), __uint_as_float(c4[e] << 16));
+            const float v1 = fmaf(S[i], static_cast<float>(q1), __uint_as_float(c4[e] & 0xffff0000u));
+            out[4 * i + e] = h2(v0, v1);
+        }
+    }
+}
+
+// One-stage fast path for the V producers: channels [j0, j0 + 8) of 8
+// consecutive slots, every load issued before the arithmetic.
+template <int D, int BITS>
+__device__ __forceinline__ void rebuild_8x8_fast(const AttnWsArgs &a, int h, int chunk, int slot0, int nvalid_rel,
+                                                 int j0, uint32_t (&hv)[8][4]) {
+    constexpr int NB = D * BITS / 8;
+    const int ng = D / a.group;
+    const uint16_t *cbase = a.vcent + (static_cast<size_t>(h) * a.max_chunks + chunk) * a.C * D + j0;
+    int id[8];
+    uint32_t bits[8];
+    float S[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const size_t srow = static_cast<size_t>(h) * a.cap + slot0 + k;
+        const bool ok = k < nvalid_rel;
+        id[k] = (ok && a.C > 0) ? a.vids[srow] : 0;
+        if constexpr (BITS == 2)
+            bits[k] = ok ? *reinterpret_cast<const uint16_t *>(a.vcodes + srow * NB + j0 / 4) : 0u;
+        else
+            bits[k] = ok ? *reinterpret_cast<const uint32_t *>(a.vcodes + srow * NB + j0 / 2) : 0u;
+        S[k] = ok ? f16_to_f32(a.vscales[srow * ng + j0 / a.group]) : 0.0f;
+    }
+    uint4 cr[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        cr[k] = (k < nvalid_rel && a.C > 0) ? *reinterpret_cast<const uint4 *>(cbase + static_cast<size_t>(id[k]) * D)
+                                            : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t c4[4] = {cr[k].x, cr[k].y, cr[k].z, cr[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int q0 = static_cast<int>((bits[k] >> (2 * e * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
+            const int q1 = static_cast<int>((bits[k] >> ((2 * e + 1) * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
+            const float v0 = fmaf(S[k], static_cast<float>(q0), __uint_as_float(c4[e] << 16));
+            const float v1 = fmaf(S[k], static_cast<float>(q1), __uint_as_float(c4[e] & 0xffff0000u));
+            hv[k][e] = k < nvalid_rel ? h2(v0, v1) : 0u;
+        }
+    }
+}
+
 }  // namespace ws
 
 template <int D, int BITS>
-__global__ void __maxnreg__(120) k_attention_ws(AttnWsArgs a) {
+__global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) {
     using namespace ws;
     constexpr int KB = D / 64;
     constexpr int QB = KB * 16384;       // one 128 x D fp16 tile
@@ -179,7 +269,7 @@ __global__ void __maxnreg__(120) k_attention_ws(AttnWsArgs a) {
         }
         *reinterpret_cast<uint4 *>((rr < 128 ? Q0 : Q1) + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
-    if (warp == 16) {
+    if (warp == 12) {
         umma::tmem_alloc(&tmem_base, 512);
         umma::tmem_relinquish();
     }
@@ -348,49 +438,97 @@ __global__ void __maxnreg__(120) k_attention_ws(AttnWsArgs a) {
                     pk[k + 4] = pS * static_cast<float>(static_cast<int8_t>((pv.y >> (8 * k)) & 0xff));
                 }
             }
-#pragma unroll
-            for (int kb = 0; kb < KB; ++kb) {
-#pragma unroll 2
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint4 out = make_uint4(0, 0, 0, 0);
+            if (a.L == 1 && !psac) {
+#pragma unroll 1
+                for (int kb = 0; kb < KB; ++kb) {
+                    uint32_t hk[32];
                     if (valid) {
-                        float kv[8];
-                        rebuild8<D, BITS>(a, a.kcodes, a.kscales, a.kids, a.kcent, h, ti.chunk, ti.s0 + r,
-                                          kb * 64 + c8 * 8, psac ? pk : nullptr, kv);
-                        out = make_uint4(h2(kv[0], kv[1]), h2(kv[2], kv[3]), h2(kv[4], kv[5]), h2(kv[6], kv[7]));
+                        rebuild_half_fast<D, BITS>(a, a.kcodes, a.kscales, a.kids, a.kcent, h, ti.chunk, ti.s0 + r, kb, hk);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) hk[e] = 0u;
                     }
-                    *reinterpret_cast<uint4 *>(Kt + kb * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4)) = out;
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8)
+                        *reinterpret_cast<uint4 *>(Kt + kb * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4)) =
+                            make_uint4(hk[4 * c8], hk[4 * c8 + 1], hk[4 * c8 + 2], hk[4 * c8 + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll 2
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        uint4 out = make_uint4(0, 0, 0, 0);
+                        if (valid) {
+                            float kv[8];
+                            rebuild8<D, BITS>(a, a.kcodes, a.kscales, a.kids, a.kcent, h, ti.chunk, ti.s0 + r,
+                                              kb * 64 + c8 * 8, psac ? pk : nullptr, kv);
+                            out = make_uint4(h2(kv[0], kv[1]), h2(kv[2], kv[3]), h2(kv[4], kv[5]), h2(kv[6], kv[7]));
+                        }
+                        *reinterpret_cast<uint4 *>(Kt + kb * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4)) = out;
+                    }
                 }
             }
             umma::fence_proxy_async_smem();
             umma::mbar_arrive(&kfull);
             ++it;
         }
-    } else if (warp < 16) {
+    } else {
         // ------------------------------------------------ V producers (8 slots x D/8 channels)
+        // and, on warp 12 lane 0, the MMA issuer
         const int u = tid - 384, kg = u >> 3, ds = u & 7;
+        const bool issuer = (warp == 12 && lane == 0);
+        const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16(128, D, 0);
+        const uint32_t q0a = umma::smem_u32(Q0), q1a = umma::smem_u32(Q1), ka = umma::smem_u32(Kt);
+        const uint32_t va = umma::smem_u32(Vt), p0a = umma::smem_u32(P0), p1a = umma::smem_u32(P1);
+        uint64_t *last_bar = nullptr;  // barrier of the issuer's latest commit (drained on failure)
+        uint32_t last_par = 0;
         int it = 0;
         for (int t = 0; t < n_tiles; ++t) {
             const TileInfo ti = tile_info(a, t);
             if (ti.nvalid == 0) continue;
+            if (issuer) {
+                // S_i = Q_i K_t^T as soon as the K tile is ready
+                if (!ws::wait(&kfull, it & 1, vfail)) break;
+                umma::tc_fence_after();
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                    umma::mma_f16(tmem + 0, umma::desc_sw128(q0a + off), umma::desc_sw128(ka + off), idS, s != 0);
+                }
+                umma::mma_commit(&sfull[0]);
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+                    umma::mma_f16(tmem + 128, umma::desc_sw128(q1a + off), umma::desc_sw128(ka + off), idS, s != 0);
+                }
+                umma::mma_commit(&sfull[1]);
+                umma::mma_commit(&kfree);
+                last_bar = &kfree;
+                last_par = it & 1;
+            }
             if (it > 0 && !ws::wait(&vfree, (it - 1) & 1, vfail)) break;
             // 8 channels at a time: rebuild them for the 8 slots, then store the
             // 8 transposed rows (one 16-byte chunk of 8 slots per channel)
 #pragma unroll 1
             for (int c8 = 0; c8 < DS; c8 += 8) {
                 uint32_t hv[8][4];
+                if (a.L == 1) {
+                    rebuild_8x8_fast<D, BITS>(a, h, ti.chunk, ti.s0 + kg * 8, ti.nvalid - kg * 8, ds * DS + c8, hv);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int rr = kg * 8 + k;
-                    if (rr < ti.nvalid) {
-                        float vv[8];
-                        rebuild8<D, BITS>(a, a.vcodes, a.vscales, a.vids, a.vcent, h, ti.chunk, ti.s0 + rr,
-                                          ds * DS + c8, nullptr, vv);
+                    for (int k = 0; k < 8; ++k) {
+                        const int rr = kg * 8 + k;
+                        if (rr < ti.nvalid) {
+                            float vv[8];
+                            rebuild8<D, BITS>(a, a.vcodes, a.vscales, a.vids, a.vcent, h, ti.chunk, ti.s0 + rr,
+                                              ds * DS + c8, nullptr, vv);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) hv[k][e] = h2(vv[2 * e], vv[2 * e + 1]);
-                    } else {
+                            for (int e = 0; e < 4; ++e) hv[k][e] = h2(vv[2 * e], vv[2 * e + 1]);
+                        } else {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) hv[k][e] = 0u;
+                            for (int e = 0; e < 4; ++e) hv[k][e] = 0u;
+                        }
                     }
                 }
 #pragma unroll
@@ -411,64 +549,37 @@ __global__ void __maxnreg__(120) k_attention_ws(AttnWsArgs a) {
             }
             umma::fence_proxy_async_smem();
             umma::mbar_arrive(&vfull);
-            ++it;
-        }
-    } else if (lane == 0) {
-        // ------------------------------------------------ MMA issuer
-        const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16(128, D, 0);
-        const uint32_t q0a = umma::smem_u32(Q0), q1a = umma::smem_u32(Q1), ka = umma::smem_u32(Kt);
-        const uint32_t va = umma::smem_u32(Vt), p0a = umma::smem_u32(P0), p1a = umma::smem_u32(P1);
-        int it = 0;
-        uint64_t *last_bar = nullptr;  // barrier of the latest commit (drained on failure)
-        uint32_t last_par = 0;
-        for (int t = 0; t < n_tiles; ++t) {
-            const TileInfo ti = tile_info(a, t);
-            if (ti.nvalid == 0) continue;
-            if (!ws::wait(&kfull, it & 1, vfail)) break;
-            umma::tc_fence_after();
+            if (issuer) {
+                // O_i += P_i V_t once the V tile and P_i are ready
+                if (!ws::wait(&vfull, it & 1, vfail) || !ws::wait(&pfull[0], it & 1, vfail)) break;
+                umma::tc_fence_after();
 #pragma unroll
-            for (int s = 0; s < D / 16; ++s) {
-                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                umma::mma_f16(tmem + 0, umma::desc_sw128(q0a + off), umma::desc_sw128(ka + off), idS, s != 0);
-            }
-            umma::mma_commit(&sfull[0]);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32, boff = (s >> 2) * (D * 128) + (s & 3) * 32;
+                    umma::mma_f16(tmem + 256, umma::desc_sw128(p0a + aoff), umma::desc_sw128(va + boff), idO, (it | s) != 0);
+                }
+                umma::mma_commit(&ofull[0]);
+                last_bar = &ofull[0];
+                if (!ws::wait(&pfull[1], it & 1, vfail)) break;
+                umma::tc_fence_after();
 #pragma unroll
-            for (int s = 0; s < D / 16; ++s) {
-                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                umma::mma_f16(tmem + 128, umma::desc_sw128(q1a + off), umma::desc_sw128(ka + off), idS, s != 0);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32, boff = (s >> 2) * (D * 128) + (s & 3) * 32;
+                    umma::mma_f16(tmem + 384, umma::desc_sw128(p1a + aoff), umma::desc_sw128(va + boff), idO, (it | s) != 0);
+                }
+                umma::mma_commit(&ofull[1]);
+                umma::mma_commit(&vfree);
+                last_bar = &vfree;
             }
-            umma::mma_commit(&sfull[1]);
-            umma::mma_commit(&kfree);
-            last_bar = &kfree;
-            last_par = it & 1;
-            if (!ws::wait(&vfull, it & 1, vfail) || !ws::wait(&pfull[0], it & 1, vfail)) break;
-            umma::tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32, boff = (s >> 2) * (D * 128) + (s & 3) * 32;
-                umma::mma_f16(tmem + 256, umma::desc_sw128(p0a + aoff), umma::desc_sw128(va + boff), idO, (it | s) != 0);
-            }
-            umma::mma_commit(&ofull[0]);
-            last_bar = &ofull[0];
-            if (!ws::wait(&pfull[1], it & 1, vfail)) break;
-            umma::tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32, boff = (s >> 2) * (D * 128) + (s & 3) * 32;
-                umma::mma_f16(tmem + 384, umma::desc_sw128(p1a + aoff), umma::desc_sw128(va + boff), idO, (it | s) != 0);
-            }
-            umma::mma_commit(&ofull[1]);
-            umma::mma_commit(&vfree);
-            last_bar = &vfree;
             ++it;
         }
         // on failure, let the MMAs already issued drain before TMEM is released
-        if (*vfail && last_bar) umma::mbar_wait(last_bar, last_par, kWaitNs);
+        if (issuer && *vfail && last_bar) umma::mbar_wait(last_bar, last_par, kWaitNs);
     }
     umma::tc_fence_before();
     __syncthreads();
     if (tid == 0 && *vfail) raise_error(a.err, QVG_ERR_TIMEOUT);
-    if (warp == 16) {
+    if (warp == 12) {
         umma::tc_fence_after();
         umma::tmem_dealloc(tmem, 512);
     }

@@ -64,10 +64,17 @@ __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / 
 
 // ---- host-side launch plumbing (internal, not part of the ABI) ------------
 
+namespace qvg {
+// Records the CUDA error behind the latest QVG_ERR_CUDA of this host thread.
+void note_cuda_error(cudaError_t e);
+}
+
 #define QVG_LAUNCH_CHECK()                                        \
     do {                                                          \
-        if (cudaPeekAtLastError() != cudaSuccess) {               \
+        const cudaError_t qvg_e_ = cudaPeekAtLastError();         \
+        if (qvg_e_ != cudaSuccess) {                              \
             (void)cudaGetLastError();                             \
+            ::qvg::note_cuda_error(qvg_e_);                       \
             return QVG_ERR_CUDA;                                  \
         }                                                         \
     } while (0)
@@ -81,7 +88,8 @@ int *device_error_word();
 // qvg_status and only enqueue work on `st`.
 qvg_status launch_kmeans_init(const uint16_t *g, int N, int H, int d, int C, int Ce,
                               uint64_t seed, int chunk, int stage,
-                              uint16_t *cent, size_t cent_head_stride, cudaStream_t st);
+                              uint16_t *cent, size_t cent_head_stride, const float *w, float *cnorm,
+                              cudaStream_t st);
 qvg_status launch_centroid_norms(const uint16_t *cent, size_t cent_head_stride, int H,
                                  int C, int d, const float *w, float *cnorm, cudaStream_t st);
 qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d,
@@ -102,14 +110,6 @@ qvg_status launch_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start,
                               int32_t *chunk_len, int32_t *tile_chunk, cudaStream_t st);
 qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, int ntok,
                              void *out, int out_dtype, cudaStream_t st);
-qvg_status launch_attention(const qvg_params *p, const uint16_t *q, int Nq, int Hq,
-                            const qvg_cache *k, const qvg_cache *v, float scale_log2,
-                            void *out, int out_dtype, float *lse, int32_t *top1,
-                            cudaStream_t st);
-qvg_status launch_attention_tc(const qvg_params *p, const uint16_t *q, int Nq, int Hq,
-                               const qvg_cache *k, const qvg_cache *v, float scale_log2,
-                               void *out, int out_dtype, float *lse, int32_t *top1,
-                               cudaStream_t st);
 qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, int Hq,
                                const qvg_cache *k, const qvg_cache *v, float scale_log2,
                                void *out, int out_dtype, float *lse, int32_t *top1,

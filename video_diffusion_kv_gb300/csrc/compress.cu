@@ -11,14 +11,14 @@
 // Kernels (one chunk, all heads per launch):
 //   k_kmeans_init     seeded systematic pick of C tokens as first centroids
 //   k_centroid_norms  ||c||_w^2 for the assignment score
-//   k_kmeans_assign   score(c) = ||c||_w^2 - 2 x.(w*c), argmin (lowest c on ties)
+//   k_kmeans_assign_tc score(c) = ||c||_w^2 - 2 x.(w*c) on the tensor cores,
+//                     argmin with the two best re-scored exactly (lowest c on ties)
 //   k_kmeans_update   deterministic segmented mean -> bf16 centroid
 //   k_residual_quant  r = x - c_id, per-group scale, codes, packing, stage
 //                     residual for the next stage, PSAC INT8 projection
 #include "common.cuh"
 #include "umma.cuh"
 
-#include <cstdlib>
 
 namespace qvg {
 
@@ -38,23 +38,43 @@ __device__ __forceinline__ uint64_t splitmix64_first(uint64_t state) {
 template <int D>
 __global__ void k_kmeans_init(const uint16_t *__restrict__ g, int N, int H, int C, int Ce,
                               uint64_t seed, int chunk, int stage, uint16_t *__restrict__ cent,
-                              size_t hs) {
-    const int h = blockIdx.x;
+                              size_t hs, const float *__restrict__ w, float *__restrict__ cnorm) {
+    constexpr int E = D / 32;  // channels per lane
+    const int h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (c >= C) return;
     const uint64_t st = seed ^ (static_cast<uint64_t>(chunk) << 40) ^
                         (static_cast<uint64_t>(h) << 20) ^ static_cast<uint64_t>(stage);
     const uint64_t u = splitmix64_first(st) >> 32;
-    uint16_t *ch = cent + static_cast<size_t>(h) * hs;
-    for (int c = warp; c < C; c += blockDim.x >> 5) {
-        if (c < Ce) {
-            const uint64_t num = ((static_cast<uint64_t>(c) << 32) + u) * static_cast<uint64_t>(N);
-            const int idx = static_cast<int>(num / (static_cast<uint64_t>(Ce) << 32));
-            const uint16_t *src = g + (static_cast<size_t>(idx) * H + h) * D;
-            for (int j = lane; j < D; j += 32) ch[static_cast<size_t>(c) * D + j] = src[j];
+    uint16_t *dst = cent + static_cast<size_t>(h) * hs + static_cast<size_t>(c) * D + lane * E;
+    float v[E];
+    if (c < Ce) {
+        const uint64_t num = ((static_cast<uint64_t>(c) << 32) + u) * static_cast<uint64_t>(N);
+        const int idx = static_cast<int>(num / (static_cast<uint64_t>(Ce) << 32));
+        const uint16_t *src = g + (static_cast<size_t>(idx) * H + h) * D + lane * E;
+        if constexpr (E == 4) {
+            const uint2 x = *reinterpret_cast<const uint2 *>(src);
+            *reinterpret_cast<uint2 *>(dst) = x;
+            v[0] = __uint_as_float(x.x << 16); v[1] = __uint_as_float(x.x & 0xffff0000u);
+            v[2] = __uint_as_float(x.y << 16); v[3] = __uint_as_float(x.y & 0xffff0000u);
         } else {
-            for (int j = lane; j < D; j += 32) ch[static_cast<size_t>(c) * D + j] = 0;
+            const uint32_t x = *reinterpret_cast<const uint32_t *>(src);
+            *reinterpret_cast<uint32_t *>(dst) = x;
+            v[0] = __uint_as_float(x << 16); v[1] = __uint_as_float(x & 0xffff0000u);
         }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) { dst[e] = 0; v[e] = 0.0f; }
     }
+    float s = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float wj = w ? w[h * D + lane * E + e] : 1.0f;
+        s = fmaf(wj * v[e], v[e], s);
+    }
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) cnorm[h * C + c] = s;
 }
 
 // ||c||_w^2 (fp32) for every centroid; one warp per (head, centroid).
@@ -74,64 +94,6 @@ __global__ void k_centroid_norms(const uint16_t *__restrict__ cent, size_t hs, i
     }
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) cnorm[h * C + c] = s;
-}
-
-// ---------------------------------------------------------------------------
-// Assignment: id = argmin_c ||c||_w^2 - 2 x.(w*c)  (the token's own ||x||_w^2
-// is common to all c and dropped).  One thread per token, the head's
-// weighted centroids staged in shared memory as fp32.
-template <int D>
-__global__ void __launch_bounds__(128) k_kmeans_assign(const uint16_t *__restrict__ g, int N,
-                                                      int H, const uint16_t *__restrict__ cent,
-                                                      size_t hs, int Ce,
-                                                      const float *__restrict__ cnorm, int C,
-                                                      const float *__restrict__ w,
-                                                      int32_t *__restrict__ ids) {
-    extern __shared__ float smem[];
-    float *wc = smem;                       // [Ce][D]
-    float *cn = smem + static_cast<size_t>(Ce) * D;  // [Ce]
-    const int h = blockIdx.y;
-    const uint16_t *ch = cent + static_cast<size_t>(h) * hs;
-    for (int i = threadIdx.x; i < Ce * D; i += blockDim.x) {
-        const int j = i % D;
-        const float wj = w ? w[h * D + j] : 1.0f;
-        wc[i] = wj * bf16_to_f32(ch[i]);
-    }
-    for (int i = threadIdx.x; i < Ce; i += blockDim.x) cn[i] = cnorm[h * C + i];
-    __syncthreads();
-    const int n = blockIdx.x * blockDim.x + threadIdx.x;
-    if (n >= N) return;
-    float x[D];
-    const uint16_t *xr = g + (static_cast<size_t>(n) * H + h) * D;
-#pragma unroll
-    for (int j = 0; j < D; j += 8) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(xr + j);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            x[j + 2 * k] = __uint_as_float(wv[k] << 16);
-            x[j + 2 * k + 1] = __uint_as_float(wv[k] & 0xffff0000u);
-        }
-    }
-    float best = INFINITY;
-    int arg = 0;
-    for (int c = 0; c < Ce; ++c) {
-        const float *cc = wc + static_cast<size_t>(c) * D;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int j = 0; j < D; j += 4) {
-            a0 = fmaf(x[j], cc[j], a0);
-            a1 = fmaf(x[j + 1], cc[j + 1], a1);
-            a2 = fmaf(x[j + 2], cc[j + 2], a2);
-            a3 = fmaf(x[j + 3], cc[j + 3], a3);
-        }
-        const float s = fmaf(-2.0f, (a0 + a1) + (a2 + a3), cn[c]);
-        if (s < best) {
-            best = s;
-            arg = c;
-        }
-    }
-    ids[static_cast<size_t>(h) * N + n] = arg;
 }
 
 // ---------------------------------------------------------------------------
@@ -163,21 +125,30 @@ __global__ void __launch_bounds__(128) k_kmeans_assign_tc(const uint16_t *__rest
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y, n0 = blockIdx.x * 128;
 
-    // token tile -> swizzled K-major bf16
+    // token tile -> swizzled K-major bf16 (asynchronous copies, zero rows past N)
+#pragma unroll 4
     for (int i = tid; i < 128 * (D / 8); i += 128) {
         const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (n0 + r < N) v = *reinterpret_cast<const uint4 *>(g + (static_cast<size_t>(n0 + r) * H + h) * D + ci * 8);
-        *reinterpret_cast<uint4 *>(As + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        const bool in = n0 + r < N;
+        umma::cp_async16(As + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4),
+                         g + (static_cast<size_t>(in ? n0 + r : 0) * H + h) * D + ci * 8, in);
     }
     // centroids (or weighted hi/lo pair) -> swizzled K-major bf16
     const uint16_t *ch = cent + static_cast<size_t>(h) * hs;
-    for (int i = tid; i < Np * (D / 8); i += 128) {
-        const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
-        uint4 v = make_uint4(0, 0, 0, 0), v2 = make_uint4(0, 0, 0, 0);
-        if (r < Ce) {
-            v = *reinterpret_cast<const uint4 *>(ch + static_cast<size_t>(r) * D + ci * 8);
-            if constexpr (P == 2) {
+    if constexpr (P == 1) {
+#pragma unroll 4
+        for (int i = tid; i < Np * (D / 8); i += 128) {
+            const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
+            const bool in = r < Ce;
+            umma::cp_async16(Bs + static_cast<size_t>(kb) * Np * 128 + r * 128 + ((c ^ (r & 7)) << 4),
+                             ch + static_cast<size_t>(in ? r : 0) * D + ci * 8, in);
+        }
+    } else {
+        for (int i = tid; i < Np * (D / 8); i += 128) {
+            const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
+            uint4 v = make_uint4(0, 0, 0, 0), v2 = make_uint4(0, 0, 0, 0);
+            if (r < Ce) {
+                v = *reinterpret_cast<const uint4 *>(ch + static_cast<size_t>(r) * D + ci * 8);
                 uint32_t in[4] = {v.x, v.y, v.z, v.w}, hi[4], lo[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -198,11 +169,12 @@ __global__ void __launch_bounds__(128) k_kmeans_assign_tc(const uint16_t *__rest
                 v = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 v2 = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
+            const size_t off = static_cast<size_t>(kb) * Np * 128 + r * 128 + ((c ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4 *>(Bs + off) = v;
+            *reinterpret_cast<uint4 *>(Bs + static_cast<size_t>(KB) * Np * 128 + off) = v2;
         }
-        const size_t off = static_cast<size_t>(kb) * Np * 128 + r * 128 + ((c ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4 *>(Bs + off) = v;
-        if constexpr (P == 2) *reinterpret_cast<uint4 *>(Bs + static_cast<size_t>(KB) * Np * 128 + off) = v2;
     }
+    umma::cp_async_wait_all();
     for (int i = tid; i < Np; i += 128) cn[i] = i < Ce ? cnorm[h * C + i] : 0.0f;
     umma::fence_proxy_async_smem();
     if (warp == 0) {
@@ -238,8 +210,8 @@ __global__ void __launch_bounds__(128) k_kmeans_assign_tc(const uint16_t *__rest
         umma::mbar_wait(&bar, 0, kWaitNs);  // let an in-flight MMA drain before freeing TMEM
     } else {
         const int r = warp * 32 + lane;
-        float best = INFINITY;
-        int arg = 0;
+        float best = INFINITY, second = INFINITY;
+        int arg = 0, arg2 = -1;
         for (int c0 = 0; c0 < Np; c0 += 32) {
             uint32_t acc[32];
             umma::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, acc);
@@ -248,11 +220,48 @@ __global__ void __launch_bounds__(128) k_kmeans_assign_tc(const uint16_t *__rest
             for (int k = 0; k < 32; ++k) {
                 const int c = c0 + k;
                 const float s = fmaf(-2.0f, __uint_as_float(acc[k]), cn[c < Np ? c : 0]);
-                if (c < Ce && s < best) {
-                    best = s;
-                    arg = c;
+                if (c < Ce) {
+                    if (s < best) {
+                        second = best;
+                        arg2 = arg;
+                        best = s;
+                        arg = c;
+                    } else if (s < second) {
+                        second = s;
+                        arg2 = c;
+                    }
                 }
             }
+        }
+        // The GEMM form ||c||^2 - 2 x.c cancels large terms (outlier channels),
+        // so its rounding can swap two nearly equidistant centroids.  The two
+        // best candidates are re-scored with the direct sum_j w_j (x_j - c_j)^2
+        // (fp32, ascending j), whose error is relative to the distance itself;
+        // ties go to the lower index.
+        if (arg2 >= 0 && n0 + r < N) {
+            const uint16_t *c1 = ch + static_cast<size_t>(arg) * D;
+            const uint16_t *c2 = ch + static_cast<size_t>(arg2) * D;
+            float d1 = 0.0f, d2 = 0.0f;
+#pragma unroll 4
+            for (int ci = 0; ci < D / 8; ++ci) {
+                const int kb = ci >> 3, c = ci & 7;
+                const uint4 xv = *reinterpret_cast<const uint4 *>(As + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4));
+                const uint4 u1 = *reinterpret_cast<const uint4 *>(c1 + ci * 8);
+                const uint4 u2 = *reinterpret_cast<const uint4 *>(c2 + ci * 8);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w},
+                               w2[4] = {u2.x, u2.y, u2.z, u2.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int sh = (k & 1) ? 0 : 16;
+                    const float xj = __uint_as_float((xw[k >> 1] << sh) & 0xffff0000u);
+                    const float e1 = xj - __uint_as_float((w1[k >> 1] << sh) & 0xffff0000u);
+                    const float e2 = xj - __uint_as_float((w2[k >> 1] << sh) & 0xffff0000u);
+                    const float wj = w ? w[h * D + ci * 8 + k] : 1.0f;
+                    d1 = fmaf(wj * e1, e1, d1);
+                    d2 = fmaf(wj * e2, e2, d2);
+                }
+            }
+            if (d2 < d1 || (d2 == d1 && arg2 < arg)) arg = arg2;
         }
         if (n0 + r < N) ids[static_cast<size_t>(h) * N + n0 + r] = arg;
     }
@@ -327,13 +336,25 @@ __global__ void __launch_bounds__(128) k_kmeans_update(const TIn *__restrict__ x
             unsigned m = __ballot_sync(0xffffffffu, id == c0 + k);
             cnt[k] += __popc(m);
             while (m) {
-                const int src = __ffs(m) - 1;
-                m &= m - 1;
-                const int nn = b * 32 + src;
-                float v[E];
-                RowLoad<TIn>::template load<E>(xin + (static_cast<size_t>(nn) * H + h) * D + lane * E, v);
+                // up to 8 members at a time: issue their row loads together,
+                // then add them in ascending token order
+                int nn[8];
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[k][e] += v[e];
+                for (int q = 0; q < 8; ++q) {
+                    nn[q] = m ? b * 32 + __ffs(m) - 1 : -1;
+                    m &= m ? m - 1 : 0u;
+                }
+                float v[8][E];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (nn[q] >= 0)
+                        RowLoad<TIn>::template load<E>(xin + (static_cast<size_t>(nn[q]) * H + h) * D + lane * E, v[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (nn[q] >= 0)
+#pragma unroll
+                        for (int e = 0; e < E; ++e) acc[k][e] += v[q][e];
             }
         }
     }
@@ -489,11 +510,13 @@ static int sm_count() {
 }
 
 qvg_status launch_kmeans_init(const uint16_t *g, int N, int H, int d, int C, int Ce, uint64_t seed,
-                              int chunk, int stage, uint16_t *cent, size_t hs, cudaStream_t st) {
+                              int chunk, int stage, uint16_t *cent, size_t hs, const float *w, float *cnorm,
+                              cudaStream_t st) {
+    dim3 grid(ceil_div(C, 8), H);
     if (d == 64)
-        k_kmeans_init<64><<<H, 256, 0, st>>>(g, N, H, C, Ce, seed, chunk, stage, cent, hs);
+        k_kmeans_init<64><<<grid, 256, 0, st>>>(g, N, H, C, Ce, seed, chunk, stage, cent, hs, w, cnorm);
     else
-        k_kmeans_init<128><<<H, 256, 0, st>>>(g, N, H, C, Ce, seed, chunk, stage, cent, hs);
+        k_kmeans_init<128><<<grid, 256, 0, st>>>(g, N, H, C, Ce, seed, chunk, stage, cent, hs, w, cnorm);
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }
@@ -529,30 +552,9 @@ static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t
     return QVG_OK;
 }
 
-template <int D>
-static qvg_status assign_impl(const uint16_t *g, int N, int H, const uint16_t *cent, size_t hs,
-                              int Ce, const float *cnorm, int C, const float *w, int32_t *ids,
-                              cudaStream_t st) {
-    const size_t smem = (static_cast<size_t>(Ce) * D + Ce) * sizeof(float);
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_kmeans_assign<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (QVG_MAX_CLUSTERS * D + QVG_MAX_CLUSTERS) * 4);
-        attr = true;
-    }
-    dim3 grid(ceil_div(N, 128), H);
-    k_kmeans_assign<D><<<grid, 128, smem, st>>>(g, N, H, cent, hs, Ce, cnorm, C, w, ids);
-    QVG_LAUNCH_CHECK();
-    return QVG_OK;
-}
-
 qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d, const uint16_t *cent,
                                 size_t hs, int Ce, const float *cnorm, int C, const float *w,
                                 int32_t *ids, cudaStream_t st) {
-    static const bool dbg_simt = getenv("QVG_DEBUG_SIMT") != nullptr;  // TEMP: dev comparison only
-    if (dbg_simt)
-        return d == 64 ? assign_impl<64>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st)
-                       : assign_impl<128>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st);
     if (d == 64)
         return w ? assign_tc_impl<64, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st)
                  : assign_tc_impl<64, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st);

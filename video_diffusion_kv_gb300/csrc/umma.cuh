@@ -71,6 +71,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// ---- asynchronous global -> shared copies (16 bytes, zero-filled when !pred) -----
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src, bool pred) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src),
+                 "r"(pred ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // ---- fences --------------------------------------------------------------------
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
