@@ -200,6 +200,36 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16,
                               void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Size of the fixed device scratch behind qvg_compress_chunk_noalloc: 32 MiB,
+ * reserved on every device that loads the library, until the process exits.
+ */
+#define QVG_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * qvg_compress_chunk without a caller workspace (the pages have no
+ * counterpart: this serves callers that cannot allocate device memory, such
+ * as code inside a framework whose memory pool owns the whole device and
+ * forbids further cudaMalloc calls, or code that must not risk the
+ * device-wide synchronisation of cudaMalloc / cudaFree).  Same arguments,
+ * results and errors as qvg_compress_chunk, which it calls; the workspace is
+ * a fixed scratch array of QVG_NOALLOC_SCRATCH_BYTES inside the library.
+ *   - Returns QVG_ERR_WORKSPACE, before anything is launched, when
+ *     qvg_workspace_size(QVG_OP_COMPRESS) for this call exceeds the scratch
+ *     (for example L > 1 or PSAC on large chunks: use qvg_compress_chunk).
+ *   - The first call on a device, made with that device current, looks up
+ *     the scratch's device address (cudaGetSymbolAddress); make that first
+ *     call before any stream capture.  It allocates nothing, ever.
+ *   - Every call on a device shares the one scratch array, which keeps the
+ *     last call's contents; nothing in it needs to start at zero.  Calls
+ *     whose work overlaps on the GPU (different streams, or different host
+ *     threads without ordering) race on the scratch: order them.
+ */
+qvg_status qvg_compress_chunk_noalloc(const qvg_params *p, const void *x_bf16,
+                                      int32_t N, const float *qsac_w,
+                                      const float *psac_basis, qvg_cache *cache,
+                                      void *stream);
+
+/*
  * Rebuild ntok token slots starting at slot tok0 ([QVG] "overall
  * framework": X_hat = S_X * X_INT + C_i, summed over stages per
  * "Progressive Residual Quantization"; with PSAC data present, plus the

@@ -31,8 +31,9 @@ QVG_OP_COMPRESS, QVG_OP_ATTENTION, QVG_OP_PSAC_BASIS = 0, 1, 2
 EXPORTED = (
     "qvg_status_string", "qvg_cache_bytes", "qvg_workspace_size", "qvg_compress_chunk",
     "qvg_decompress", "qvg_attention", "quantwm_query_stats", "quantwm_psac_basis",
-    "qvg_get_status", "qvg_last_cuda_error",
+    "qvg_get_status", "qvg_last_cuda_error", "qvg_compress_chunk_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 BUFFER_NAMES = ("codes", "scales", "ids", "cent", "chunk_start", "chunk_len", "tile_chunk",
                 "psac_p", "psac_s", "psac_basis")
@@ -76,6 +77,7 @@ def lib():
         L.qvg_cache_bytes.argtypes = [vp, i32, i32, i32, i32, vp]
         L.qvg_workspace_size.argtypes = [vp, i32, i32, i32, i32, i32, vp]
         L.qvg_compress_chunk.argtypes = [vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.qvg_compress_chunk_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, vp]
         L.qvg_decompress.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         L.qvg_attention.argtypes = [vp, vp, i32, i32, vp, vp, ct.c_float, vp, i32, vp, vp, vp, sz, vp]
         L.quantwm_query_stats.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
@@ -206,6 +208,24 @@ def compress_chunk(params: Params, x, cache: CompressedKV, qsac_w=None, psac_bas
     s = lib().qvg_compress_chunk(ct.byref(p), _ptr(x), N, _ptr(qsac_w), _ptr(psac_basis), ct.byref(c),
                                  _ptr(workspace), workspace.numel(), _stream(stream))
     _check(s, "qvg_compress_chunk")
+    cache.n_chunks, cache.n_tokens = c.n_chunks, c.n_tokens
+    return slot0
+
+
+def compress_chunk_noalloc(params: Params, x, cache: CompressedKV, qsac_w=None, psac_basis=None,
+                           stream=None):
+    """compress_chunk without a workspace argument: for callers that cannot
+    allocate device memory, the library uses its own fixed 32 MiB device
+    scratch (see qvg_compress_chunk_noalloc in include/qvg.h; calls that
+    overlap on the GPU race on it).  Returns the first token slot."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.is_contiguous() and x.dim() == 3
+    c = cache.c()
+    p = params.c()
+    slot0 = cache.n_tokens
+    s = lib().qvg_compress_chunk_noalloc(ct.byref(p), _ptr(x), x.shape[0], _ptr(qsac_w), _ptr(psac_basis),
+                                         ct.byref(c), _stream(stream))
+    _check(s, "qvg_compress_chunk_noalloc")
     cache.n_chunks, cache.n_tokens = c.n_chunks, c.n_tokens
     return slot0
 
