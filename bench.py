@@ -215,9 +215,11 @@ def run_reference(args):
 # ------------------------------------------------------------------ own arm
 
 def launches_per_compress(p):
-    per_stage = 1  # residual quantise
+    """Kernels one qvg_compress_chunk call launches (see csrc/api.cu)."""
+    per_stage = 1  # residual quantise (+ pack, stage residual, PSAC)
     if p.C > 0:
-        per_stage += (0 if p.flags & 4 else 1) + 1 + 2 * p.iters + 1
+        # init with norms (or norms of given centroids), iters x (assign, update), final assign
+        per_stage += 1 + 2 * p.iters + 1
     return per_stage * p.L + 1  # + chunk table
 
 
@@ -375,6 +377,144 @@ def run_own(args):
     return 0
 
 
+# ------------------------------------------------------------------ studies of the other workloads
+
+def _rel(x, y):
+    import numpy as np
+    return float(np.linalg.norm((x - y).astype(np.float64)) / np.linalg.norm(x.astype(np.float64)))
+
+
+def study_qvgpro(args):
+    """QVG-Pro on the tiny shapes: INT2 G=32 with L = 1, 2, 3 and INT4 G=32
+    with L = 1, 2; relative Frobenius error of K and V after each stage count
+    and the compression ratio counting codes, fp16 scales, ids and bf16
+    centroids."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import video_diffusion_kv_gb300 as qvg
+    from video_diffusion_kv_gb300 import synth
+    w = synth.WORKLOADS["qvgpro"]
+    arms = []
+    for bits, stages in ((2, 3), (4, 2)):
+        for L in range(1, stages + 1):
+            p = qvg.Params(C=w.C, L=L, bits=bits, group=w.group, iters=w.iters, seed=5)
+            errs = {}
+            for kind, name in ((synth.KIND_K, "K"), (synth.KIND_V, "V")):
+                c = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * 256, w.n_chunks)
+                xs = [synth.chunk_kv(w, 5, k, kind) for k in range(w.n_chunks)]
+                for x in xs:
+                    qvg.compress_chunk(p, synth_dev(x, "cuda"), c)
+                xh = qvg.decompress(p, c, 0, c.n_tokens).cpu().numpy()
+                import numpy as np
+                errs[name] = _rel(np.concatenate(xs, 0), xh)
+            rtn = qvg.Params(C=0, L=1, bits=bits, group=w.group, iters=0)
+            arms.append({"bits": bits, "stages": L, "rel_err_K": errs["K"], "rel_err_V": errs["V"],
+                         "ratio": qvg.compression_ratio(p, w.H, w.d, 256, w.n_chunks),
+                         "ratio_rtn_same_bits": qvg.compression_ratio(rtn, w.H, w.d, 256, w.n_chunks)})
+    print(json.dumps({"study": "qvgpro", "workload": "2 heads, d=64, 4 chunks x 256 tokens, C=16, G=32, 10 iters",
+                      "arms": arms}), flush=True)
+    return 0
+
+
+def study_quantwm(args):
+    """QuantWM world-model cache: 24 heads, d=128, 8 chunks of 3 frames of
+    22x40 (21,120 tokens).  History queries (4 frames) give the QSAC weights
+    and the PSAC basis; the top-1 attention-token shift rate of an 880-token
+    query frame is measured against the oracle's argmax over the bf16 cache
+    for the arms QVG, +QSAC, +PSAC and both."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    import video_diffusion_kv_gb300 as qvg
+    from video_diffusion_kv_gb300 import synth
+    w = synth.WORKLOADS["quantwm"]
+    seed = 7
+    qh = synth_dev(synth.history_queries(w, seed), "cuda")
+    M, wq, cnt = qvg.query_stats(qh, w.H)
+    U, eig, frac = qvg.psac_basis(M, cnt)
+    ks = [synth.chunk_kv(w, seed, k, synth.KIND_K) for k in range(w.n_chunks)]
+    vs = [synth.chunk_kv(w, seed, k, synth.KIND_V) for k in range(w.n_chunks)]
+    qf = synth.history_queries(w, seed, n_tokens=880, stream=1)
+    kall = np.concatenate(ks, 0)
+    ref = oracle.top1(qf, kall, nthreads=os.cpu_count() or 1)     # [Hq, Nq] token indices
+    arms = {}
+    for name, flags in (("QVG", 0), ("QSAC", qvg.QVG_QSAC), ("PSAC", qvg.QVG_PSAC),
+                        ("QSAC+PSAC", qvg.QVG_QSAC | qvg.QVG_PSAC)):
+        p = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=seed, flags=flags)
+        pv = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=seed)
+        cap = w.n_chunks * (-(-w.N // 128) * 128)
+        kc = qvg.CompressedKV(p, w.H, w.d, cap, w.n_chunks)
+        vc = qvg.CompressedKV(pv, w.H, w.d, cap, w.n_chunks)
+        for k in range(w.n_chunks):
+            qvg.compress_chunk(p, synth_dev(ks[k], "cuda"), kc, qsac_w=wq, psac_basis=U)
+            qvg.compress_chunk(pv, synth_dev(vs[k], "cuda"), vc)
+        _, _, top1 = qvg.attention(p, synth_dev(qf, "cuda"), kc, vc, want_top1=True)
+        slots = top1.cpu().numpy()
+        # slot -> token index (chunks start at multiples of 128 slots)
+        per = -(-w.N // 128) * 128
+        tok = (slots // per) * w.N + slots % per
+        kh = qvg.decompress(p, kc, 0, kc.n_tokens).cpu().numpy()
+        keep = np.concatenate([np.arange(k * per, k * per + w.N) for k in range(w.n_chunks)])
+        arms[name] = {"shift_rate": float((tok != ref).mean()),
+                      "rel_err_K": _rel(kall, kh[keep]),
+                      "ratio_K": qvg.compression_ratio(p, w.H, w.d, w.N, w.n_chunks,
+                                                      with_psac=bool(flags & qvg.QVG_PSAC))}
+    print(json.dumps({"study": "quantwm", "workload": "24 heads, d=128, 8 chunks x 2640 tokens, C=256, INT2 G=64, 8 iters; 880 query tokens",
+                      "energy_frac_top8": [float(x) for x in frac.cpu().numpy()[:4]],
+                      "energy_frac_mean": float(frac.mean().item()), "arms": arms}), flush=True)
+    return 0
+
+
+def study_rollout(args):
+    """One-minute rollout: 288 frames of 30x52 streamed in 96 chunks of 4680
+    tokens, 8 heads, d=128, INT2 C=256.  After compressing each chunk its
+    4680 queries attend over the whole compressed cache; attention time is
+    reported against the cache length.  Chunks are drawn from the stationary
+    16-prototype mixture; 12 distinct chunks are generated and cycled."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import video_diffusion_kv_gb300 as qvg
+    from video_diffusion_kv_gb300 import synth
+    w = synth.WORKLOADS["rollout"]
+    p = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=9)
+    per = -(-w.N // 128) * 128
+    kc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks)
+    vc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks)
+    uniq = 12
+    K = [synth_dev(synth.chunk_kv(w, 9, k, synth.KIND_K), "cuda") for k in range(uniq)]
+    V = [synth_dev(synth.chunk_kv(w, 9, k, synth.KIND_V), "cuda") for k in range(uniq)]
+    Q = [synth_dev(synth.queries(w, 9, k), "cuda") for k in range(uniq)]
+    out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    points = []
+    for k in range(w.n_chunks):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        qvg.compress_chunk(p, K[k % uniq], kc)
+        qvg.compress_chunk(p, V[k % uniq], vc)
+        e[1].record()
+        qvg.attention(p, Q[k % uniq], kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out)
+        e[2].record()
+        torch.cuda.synchronize()
+        if k in (0, 7, 23, 47, 71, 95):
+            nk = (k + 1) * w.N
+            ms = e[1].elapsed_time(e[2])
+            points.append({"chunks": k + 1, "cache_tokens": nk, "compress_ms": e[0].elapsed_time(e[1]),
+                           "attention_ms": ms, "attention_TFLOP/s": 4.0 * w.Nq * nk * w.d * w.Hq / ms / 1e9})
+    comp = kc.nbytes + vc.nbytes
+    print(json.dumps({"study": "rollout", "workload": "8 heads, d=128, 96 chunks x 4680 tokens (449,280), C=256, INT2 G=64, 8 iters",
+                      "status": qvg.get_status(), "points": points,
+                      "cache_bytes_compressed": comp,
+                      "cache_bytes_bf16": qvg.kv_bytes_uncompressed(1, w.H, w.d, w.tokens)}), flush=True)
+    return 0
+
+
 def synth_dev(a, dev):
     import torch
     return torch.from_numpy(a).to(dev, torch.bfloat16).contiguous()
@@ -389,11 +529,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="time the device step only (profiling)")
     ap.add_argument("--cache-chunks", type=int, default=None, help="smaller cache (profiling cases)")
+    ap.add_argument("--workload", default="longcat", choices=["longcat", "qvgpro", "quantwm", "rollout"],
+                    help="longcat: the benchmark line; the others print their study line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "own":
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "longcat":
+        return {"qvgpro": study_qvgpro, "quantwm": study_quantwm, "rollout": study_rollout}[args.workload](args)
     return run_own(args)
 
 

@@ -190,7 +190,9 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
             }
             for (int it = 0; it < p->iters; ++it) {
                 if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.ids, st)) != QVG_OK) return s;
-                if ((s = launch_kmeans_update(xin, f32, N, H, d, ws.ids, cent, cent_hs, Ce, C, w, ws.cnorm, st)) != QVG_OK) return s;
+                if ((s = launch_kmeans_update(xin, f32, N, H, d, ws.ids, cent, cent_hs, Ce, C, w, ws.cnorm, st)) !=
+                    QVG_OK)
+                    return s;
             }
             if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.ids, st)) != QVG_OK) return s;
         }

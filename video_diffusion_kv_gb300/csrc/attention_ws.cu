@@ -12,7 +12,7 @@
 // Warp roles (16 warps, 128 registers per thread):
 //   0-3, 4-7   softmax + epilogue of query tile 0 / 1 (thread = query row)
 //   8-11       K producers: rebuild a 128-slot K_hat tile (thread = slot)
-//   12-15      V producers: rebuild V_hat^T (thread = 8 slots x D/8 channels);
+//   12-15      V producers: rebuild V_hat^T (thread = slot, double-buffered);
 //              warp 12 owns the TMEM allocation and its lane 0 issues every
 //              tcgen05.mma (S_0, S_1 before producing the V tile, which must
 //              wait for the previous PV products anyway; PV_0, PV_1 after)
@@ -62,6 +62,14 @@ __device__ __forceinline__ uint32_t h2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// 2^x with the hardware approximation (MUFU.EX2, relative error ~2^-22);
+// -inf gives 0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Bounded wait that also gives up as soon as another role has failed.
 __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, volatile int *fail) {
     if (umma::mbar_try_wait(bar, parity)) return true;
@@ -90,8 +98,10 @@ __device__ __forceinline__ TileInfo tile_info(const AttnWsArgs &a, int t) {
 }
 
 // K_hat channels [j0, j0 + 8) of one slot (fp32, stage order, then PSAC).
+// The general path (several stages, PSAC): kept out of line so the one-stage
+// fast path's loop stays small in the instruction cache.
 template <int D, int BITS>
-__device__ __forceinline__ void rebuild8(const AttnWsArgs &a, const uint8_t *codes, const uint16_t *scales,
+__device__ __noinline__ void rebuild8(const AttnWsArgs &a, const uint8_t *codes, const uint16_t *scales,
                                          const uint8_t *ids, const uint16_t *cent, int h, int chunk, int slot,
                                          int j0, const float *pk, float (&acc)[8]) {
     constexpr int NB = D * BITS / 8;
@@ -164,8 +174,14 @@ __device__ __forceinline__ void rebuild_half_fast(const AttnWsArgs &a, const uin
 #pragma unroll
     for (int i = 0; i < HB / 16; ++i) cw[i] = *reinterpret_cast<const uint4 *>(codes + srow * NB + kb * HB + 16 * i);
     float S[8];
+    if (a.group >= 64) {
+        const float s0 = f16_to_f32(scales[srow * ng + (kb * 64) / a.group]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) S[i] = f16_to_f32(scales[srow * ng + (kb * 64 + 8 * i) / a.group]);
+        for (int i = 0; i < 8; ++i) S[i] = s0;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) S[i] = f16_to_f32(scales[srow * ng + (kb * 64 + 8 * i) / a.group]);
+    }
     uint4 cr[8];
     if (a.C > 0) {
         const uint16_t *row = cent + (static_cast<size_t>(h) * a.max_chunks + chunk) * a.C * D +
@@ -236,7 +252,7 @@ __device__ __forceinline__ void rebuild_8x8_fast(const AttnWsArgs &a, int h, int
 
 }  // namespace ws
 
-template <int D, int BITS>
+template <int D, int BITS, bool TOP1>
 __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) {
     using namespace ws;
     constexpr int KB = D / 64;
@@ -246,8 +262,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     constexpr int DS = D / 8;            // V channels per producer thread
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
-    uint8_t *Q0 = sm, *Q1 = Q0 + QB, *Kt = Q1 + QB, *Vt = Kt + QB, *P0 = Vt + VB, *P1 = P0 + PB;
-    __shared__ uint64_t kfull, vfull, kfree, vfree, sfull[2], pfull[2], ofull[2];
+    uint8_t *Q0 = sm, *Q1 = Q0 + QB, *Kt = Q1 + QB, *Vt0 = Kt + QB, *P0 = Vt0 + 2 * VB, *P1 = P0 + PB;
+    __shared__ uint64_t kfull, vfull[2], kfree, vfree[2], sfull[2], pfull[2], ofull[2];
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
 
@@ -275,10 +291,10 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     }
     if (tid == 0) {
         umma::mbar_init(&kfull, 128);
-        umma::mbar_init(&vfull, 128);
         umma::mbar_init(&kfree, 1);
-        umma::mbar_init(&vfree, 1);
         for (int i = 0; i < 2; ++i) {
+            umma::mbar_init(&vfull[i], 128);
+            umma::mbar_init(&vfree[i], 1);
             umma::mbar_init(&sfull[i], 1);
             umma::mbar_init(&pfull[i], 128);
             umma::mbar_init(&ofull[i], 1);
@@ -306,30 +322,52 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             if (ti.nvalid == 0) continue;
             if (!ws::wait(&sfull[i], it & 1, vfail)) break;
             umma::tc_fence_after();
-            float tmax = -INFINITY;
+            // row maximum of the raw logits (the scale is positive), then scaled
+            // once; four independent chains (the top-1 variant keeps one chain
+            // so that ties resolve to the lowest slot)
+            float rmax = -INFINITY;
             int targ = 0;
+            if constexpr (TOP1) {
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-                uint32_t v[32];
-                umma::tmem_ld32(tS + c0, v);
-                umma::tmem_ld_wait();
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t v[32];
+                    umma::tmem_ld32(tS + c0, v);
+                    umma::tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float s = c0 + k < ti.nvalid ? __uint_as_float(v[k]) * a.scale_log2 : -INFINITY;
-                    if (s > tmax) {
-                        tmax = s;
-                        targ = c0 + k;
+                    for (int k = 0; k < 32; ++k) {
+                        const float x = c0 + k < ti.nvalid ? __uint_as_float(v[k]) : -INFINITY;
+                        if (x > rmax) { rmax = x; targ = c0 + k; }
                     }
                 }
+            } else {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t v[32];
+                    umma::tmem_ld32(tS + c0, v);
+                    umma::tmem_ld_wait();
+                    if (c0 + 32 <= ti.nvalid) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(v[k]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            if (c0 + k < ti.nvalid) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(v[k]));
+                    }
+                }
+                rmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
-            if (tmax > best) {
-                best = tmax;
-                best_slot = ti.s0 + targ;
+            const float tmax = rmax * a.scale_log2;
+            if constexpr (TOP1) {
+                if (tmax > best) {
+                    best = tmax;
+                    best_slot = ti.s0 + targ;
+                }
             }
             float corr = 1.0f;
             bool rescale = false;
             if (tmax > m_used + kRescale) {
-                corr = exp2f(m_used - tmax);
+                corr = ex2(m_used - tmax);
                 rescale = it > 0;
                 m_used = tmax;
             }
@@ -350,21 +388,27 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                     umma::tmem_st_wait();
                 }
             }
-            float ls = 0.0f;
+            float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
                 uint32_t v[32];
                 umma::tmem_ld32(tS + c0, v);
                 umma::tmem_ld_wait();
                 uint32_t pk[16];
+                const float nm = -m_used;
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const int c = c0 + 2 * k;
-                    const float p0 = c < ti.nvalid ? exp2f(fmaf(__uint_as_float(v[2 * k]), a.scale_log2, -m_used)) : 0.0f;
-                    const float p1 = c + 1 < ti.nvalid ? exp2f(fmaf(__uint_as_float(v[2 * k + 1]), a.scale_log2, -m_used)) : 0.0f;
+                    float p0 = ex2(fmaf(__uint_as_float(v[2 * k]), a.scale_log2, nm));
+                    float p1 = ex2(fmaf(__uint_as_float(v[2 * k + 1]), a.scale_log2, nm));
+                    if (c0 + 32 > ti.nvalid) {
+                        p0 = c < ti.nvalid ? p0 : 0.0f;
+                        p1 = c + 1 < ti.nvalid ? p1 : 0.0f;
+                    }
                     pk[k] = h2(p0, p1);
-                    const __half2 hp = *reinterpret_cast<const __half2 *>(&pk[k]);
-                    ls += __low2float(hp) + __high2float(hp);
+                    // the row sum adds the fp16 values the PV product uses
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&pk[k]));
+                    ls4[k & 3] += f.x + f.y;
                 }
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
@@ -373,6 +417,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                         make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
                 }
             }
+            const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
             l_sum = l_sum * corr + ls;
             umma::fence_proxy_async_smem();
             umma::tc_fence_before();
@@ -414,7 +459,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             }
             if (qi < a.Nq) {
                 if (a.lse) a.lse[static_cast<size_t>(hq) * a.Nq + qi] = (m_used + log2f(l_sum)) * 0.69314718055994531f;
-                if (a.top1) a.top1[static_cast<size_t>(hq) * a.Nq + qi] = best_slot;
+                if constexpr (TOP1) a.top1[static_cast<size_t>(hq) * a.Nq + qi] = best_slot;
             }
         }
     } else if (warp < 12) {
@@ -476,11 +521,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     } else {
         // ------------------------------------------------ V producers (8 slots x D/8 channels)
         // and, on warp 12 lane 0, the MMA issuer
-        const int u = tid - 384, kg = u >> 3, ds = u & 7;
+        const int u = tid - 384;
         const bool issuer = (warp == 12 && lane == 0);
         const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16(128, D, 0);
         const uint32_t q0a = umma::smem_u32(Q0), q1a = umma::smem_u32(Q1), ka = umma::smem_u32(Kt);
-        const uint32_t va = umma::smem_u32(Vt), p0a = umma::smem_u32(P0), p1a = umma::smem_u32(P1);
+        const uint32_t v0a = umma::smem_u32(Vt0), p0a = umma::smem_u32(P0), p1a = umma::smem_u32(P1);
         uint64_t *last_bar = nullptr;  // barrier of the issuer's latest commit (drained on failure)
         uint32_t last_par = 0;
         int it = 0;
@@ -507,56 +552,54 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 last_bar = &kfree;
                 last_par = it & 1;
             }
-            if (it > 0 && !ws::wait(&vfree, (it - 1) & 1, vfail)) break;
-            // 8 channels at a time: rebuild them for the 8 slots, then store the
-            // 8 transposed rows (one 16-byte chunk of 8 slots per channel)
+            // V tiles are double-buffered: tile `it` uses buffer it & 1, free
+            // once the PV products of tile it - 2 are done
+            const int vb = it & 1;
+            uint8_t *Vt = Vt0 + vb * VB;
+            if (it >= 2 && !ws::wait(&vfree[vb], ((it >> 1) - 1) & 1, vfail)) break;
+            // thread = slot: rebuild the slot's V_hat row (64 channels at a time,
+            // every load issued first) and store it as column `r` of V_hat^T
+            const int r = u;
+            const bool valid = r < ti.nvalid;
+            const int kbs = r >> 6, cs = (r & 63) >> 3, es = (r & 7) * 2;
 #pragma unroll 1
-            for (int c8 = 0; c8 < DS; c8 += 8) {
-                uint32_t hv[8][4];
-                if (a.L == 1) {
-                    rebuild_8x8_fast<D, BITS>(a, h, ti.chunk, ti.s0 + kg * 8, ti.nvalid - kg * 8, ds * DS + c8, hv);
+            for (int kb = 0; kb < KB; ++kb) {
+                uint32_t hv[32];
+                if (valid && a.L == 1) {
+                    rebuild_half_fast<D, BITS>(a, a.vcodes, a.vscales, a.vids, a.vcent, h, ti.chunk, ti.s0 + r, kb, hv);
+                } else if (valid) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        float vv[8];
+                        rebuild8<D, BITS>(a, a.vcodes, a.vscales, a.vids, a.vcent, h, ti.chunk, ti.s0 + r,
+                                          kb * 64 + c8 * 8, nullptr, vv);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) hv[4 * c8 + e] = h2(vv[2 * e], vv[2 * e + 1]);
+                    }
                 } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int rr = kg * 8 + k;
-                        if (rr < ti.nvalid) {
-                            float vv[8];
-                            rebuild8<D, BITS>(a, a.vcodes, a.vscales, a.vids, a.vcent, h, ti.chunk, ti.s0 + rr,
-                                              ds * DS + c8, nullptr, vv);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) hv[k][e] = h2(vv[2 * e], vv[2 * e + 1]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) hv[k][e] = 0u;
-                        }
-                    }
+                    for (int e = 0; e < 32; ++e) hv[e] = 0u;
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = ds * DS + c8 + e;
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int k2 = 0; k2 < 4; ++k2) {
-                        const uint32_t a0 = hv[2 * k2][e >> 1], a1 = hv[2 * k2 + 1][e >> 1];
-                        const uint32_t lo16 = (e & 1) ? (a0 >> 16) : (a0 & 0xffffu);
-                        const uint32_t hi16 = (e & 1) ? (a1 >> 16) : (a1 & 0xffffu);
-                        w4[k2] = lo16 | (hi16 << 16);
-                    }
-                    const int kb = kg >> 3, c = kg & 7;
-                    *reinterpret_cast<uint4 *>(Vt + kb * (D * 128) + j * 128 + ((c ^ (j & 7)) << 4)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                for (int e = 0; e < 32; ++e) {
+                    const int j = kb * 64 + 2 * e;
+                    uint8_t *col = Vt + kbs * (D * 128) + es;
+                    *reinterpret_cast<uint16_t *>(col + j * 128 + ((cs ^ (j & 7)) << 4)) =
+                        static_cast<uint16_t>(hv[e] & 0xffffu);
+                    *reinterpret_cast<uint16_t *>(col + (j + 1) * 128 + ((cs ^ ((j + 1) & 7)) << 4)) =
+                        static_cast<uint16_t>(hv[e] >> 16);
                 }
             }
             umma::fence_proxy_async_smem();
-            umma::mbar_arrive(&vfull);
+            umma::mbar_arrive(&vfull[vb]);
             if (issuer) {
                 // O_i += P_i V_t once the V tile and P_i are ready
-                if (!ws::wait(&vfull, it & 1, vfail) || !ws::wait(&pfull[0], it & 1, vfail)) break;
+                if (!ws::wait(&vfull[vb], (it >> 1) & 1, vfail) || !ws::wait(&pfull[0], it & 1, vfail)) break;
                 umma::tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32, boff = (s >> 2) * (D * 128) + (s & 3) * 32;
-                    umma::mma_f16(tmem + 256, umma::desc_sw128(p0a + aoff), umma::desc_sw128(va + boff), idO, (it | s) != 0);
+                    umma::mma_f16(tmem + 256, umma::desc_sw128(p0a + aoff), umma::desc_sw128(v0a + vb * VB + boff), idO, (it | s) != 0);
                 }
                 umma::mma_commit(&ofull[0]);
                 last_bar = &ofull[0];
@@ -565,11 +608,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32, boff = (s >> 2) * (D * 128) + (s & 3) * 32;
-                    umma::mma_f16(tmem + 384, umma::desc_sw128(p1a + aoff), umma::desc_sw128(va + boff), idO, (it | s) != 0);
+                    umma::mma_f16(tmem + 384, umma::desc_sw128(p1a + aoff), umma::desc_sw128(v0a + vb * VB + boff), idO, (it | s) != 0);
                 }
                 umma::mma_commit(&ofull[1]);
-                umma::mma_commit(&vfree);
-                last_bar = &vfree;
+                umma::mma_commit(&vfree[vb]);
+                last_bar = &vfree[vb];
+                last_par = (it >> 1) & 1;
             }
             ++it;
         }
@@ -585,18 +629,29 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     }
 }
 
-template <int D, int BITS>
-static qvg_status attn_ws(const AttnWsArgs &a, cudaStream_t st) {
-    constexpr size_t smem = 3 * (D / 64) * 16384 + D * 256 + 2 * 32768 + 1024;
+template <int D, int BITS, bool TOP1>
+static qvg_status attn_ws_t(const AttnWsArgs &a, cudaStream_t st) {
+    constexpr size_t smem = 3 * (D / 64) * 16384 + 2 * D * 256 + 2 * 32768 + 1024;
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_attention_ws<D, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        const cudaError_t e = cudaFuncSetAttribute(k_attention_ws<D, BITS, TOP1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            note_cuda_error(e);
+            return QVG_ERR_CUDA;
+        }
         attr = true;
     }
     dim3 grid(ceil_div(a.Nq, 256), a.Hq);
-    k_attention_ws<D, BITS><<<grid, ws::kThreads, smem, st>>>(a);
+    k_attention_ws<D, BITS, TOP1><<<grid, ws::kThreads, smem, st>>>(a);
     QVG_LAUNCH_CHECK();
     return QVG_OK;
+}
+
+template <int D, int BITS>
+static qvg_status attn_ws(const AttnWsArgs &a, cudaStream_t st) {
+    return a.top1 ? attn_ws_t<D, BITS, true>(a, st) : attn_ws_t<D, BITS, false>(a, st);
 }
 
 qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, int Hq, const qvg_cache *k,

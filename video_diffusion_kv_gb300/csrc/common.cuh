@@ -97,8 +97,8 @@ qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d,
                                 const float *cnorm, int C, const float *w, int32_t *ids,
                                 cudaStream_t st);
 qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int d,
-                                const int32_t *ids, uint16_t *cent, size_t cent_head_stride,
-                                int Ce, int C, const float *w, float *cnorm, cudaStream_t st);
+                                const int32_t *ids, uint16_t *cent, size_t cent_head_stride, int Ce, int C,
+                                const float *w, float *cnorm, cudaStream_t st);
 qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, int d,
                                  const uint16_t *cent, size_t cent_head_stride, int C,
                                  const int32_t *ids, int bits, int group, int mode,

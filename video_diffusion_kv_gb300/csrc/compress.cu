@@ -13,7 +13,8 @@
 //   k_centroid_norms  ||c||_w^2 for the assignment score
 //   k_kmeans_assign_tc score(c) = ||c||_w^2 - 2 x.(w*c) on the tensor cores,
 //                     argmin with the two best re-scored exactly (lowest c on ties)
-//   k_kmeans_update   deterministic segmented mean -> bf16 centroid
+//   k_kmeans_update   stable order of a head's tokens by cluster, then the
+//                     members summed in token order -> bf16 centroid + norm
 //   k_residual_quant  r = x - c_id, per-group scale, codes, packing, stage
 //                     residual for the next stage, PSAC INT8 projection
 #include "common.cuh"
@@ -97,54 +98,73 @@ __global__ void k_centroid_norms(const uint16_t *__restrict__ cent, size_t hs, i
 }
 
 // ---------------------------------------------------------------------------
-// Assignment on the tensor cores: one CTA per (128-token tile, head).
-// D[128 x Np] = X_tile (bf16, 128 x D) * B^T with B = the head's centroids
-// (bf16, exact) or, with QSAC weights, the weighted centroids w*c split into
-// a bf16 pair hi + lo (|w c - hi - lo| <= 2^-18 |w c|), accumulated in fp32
-// in tensor memory by tcgen05.mma (M=128, N=Np = Ce rounded up to 16,
-// K=16 per instruction).  Epilogue: thread r owns token row r, reads its Np
-// accumulators from TMEM and takes argmin_c ||c||_w^2 - 2 acc_c (lowest c on
-// ties).  Every wait is bounded; on expiry the CTA records QVG_ERR_TIMEOUT.
+// Assignment on the tensor cores.  A CTA owns one head's centroids (staged
+// once in shared memory) and walks several 128-token tiles of that head:
+//   D_t[128 x Np] = X_t (bf16, 128 x D) * B^T,  B = the centroids (bf16,
+//   exact) or, with QSAC weights, the weighted centroids w*c as a bf16 pair
+//   hi + lo (|w c - hi - lo| <= 2^-18 |w c|),
+// accumulated in fp32 in tensor memory by tcgen05.mma (M=128, N=Np = Ce
+// rounded up to 16, K=16 per instruction).  Tensor memory holds two
+// accumulators, so the epilogue of tile t (thread r owns token r: argmin_c
+// ||c||_w^2 - 2 acc_c over the TMEM row) overlaps the MMA of tile t+1 and
+// the cp.async loads of tile t+2.  The GEMM form cancels large outlier
+// products, so the two best candidates are re-scored with the direct
+// sum_j w_j (x_j - c_j)^2 (fp32, ascending j); ties go to the lower index.
+// Every wait is bounded; on expiry the CTA records QVG_ERR_TIMEOUT.
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 
+constexpr int kAssignThreads = 256;
+
 template <int D, int P>
-__global__ void __launch_bounds__(128) k_kmeans_assign_tc(const uint16_t *__restrict__ g, int N, int H,
+__global__ void __launch_bounds__(kAssignThreads) k_kmeans_assign_tc(const uint16_t *__restrict__ g, int N, int H,
                                                          const uint16_t *__restrict__ cent, size_t hs,
                                                          int Ce, int Np, const float *__restrict__ cnorm,
                                                          int C, const float *__restrict__ w,
                                                          int32_t *__restrict__ ids, int *err) {
     constexpr int KB = D / 64;                       // 64-element K blocks
+    constexpr int AB = KB * 128 * 128;               // one token tile
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     // swizzle atoms need a 1024-byte aligned base (the launch adds 1 KB slack)
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
-    uint8_t *As = sm;                                // KB x [128 rows x 128 B]
-    uint8_t *Bs = As + KB * 128 * 128;               // P x KB x [Np rows x 128 B]
+    uint8_t *As = sm;                                // 2 x KB x [128 rows x 128 B]
+    uint8_t *Bs = As + 2 * AB;                       // P x KB x [Np rows x 128 B]
     float *cn = reinterpret_cast<float *>(Bs + static_cast<size_t>(P) * KB * Np * 128);
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bar[2];
     __shared__ uint32_t tmem_base;
+    __shared__ float xb[128][2];     // warp group 1's best / second score per row
+    __shared__ int xi[128][2];       // ... and their clusters
+    __shared__ float xd[128];        // group 1's exact distance of the second candidate
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.y, n0 = blockIdx.x * 128;
+    const int grp = warp >> 2;       // warp group: 32-column chunks grp, grp + 2, ...
+    const int h = blockIdx.y;
+    const int n_tiles = ceil_div(N, 128);
+    const int t0 = blockIdx.x, tstep = gridDim.x;
+    const uint32_t ncols = Np <= 32 ? 32 : (Np <= 64 ? 64 : (Np <= 128 ? 128 : 256));
 
-    // token tile -> swizzled K-major bf16 (asynchronous copies, zero rows past N)
+    auto load_tile = [&](int t, int buf) {
+        const int n0 = t * 128;
+        uint8_t *dst = As + buf * AB;
 #pragma unroll 4
-    for (int i = tid; i < 128 * (D / 8); i += 128) {
-        const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
-        const bool in = n0 + r < N;
-        umma::cp_async16(As + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4),
-                         g + (static_cast<size_t>(in ? n0 + r : 0) * H + h) * D + ci * 8, in);
-    }
-    // centroids (or weighted hi/lo pair) -> swizzled K-major bf16
+        for (int i = tid; i < 128 * (D / 8); i += kAssignThreads) {
+            const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
+            const bool in = n0 + r < N;
+            umma::cp_async16(dst + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4),
+                             g + (static_cast<size_t>(in ? n0 + r : 0) * H + h) * D + ci * 8, in);
+        }
+    };
+
+    // centroids (or weighted hi/lo pair) -> swizzled K-major bf16, once
     const uint16_t *ch = cent + static_cast<size_t>(h) * hs;
     if constexpr (P == 1) {
 #pragma unroll 4
-        for (int i = tid; i < Np * (D / 8); i += 128) {
+        for (int i = tid; i < Np * (D / 8); i += kAssignThreads) {
             const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
             const bool in = r < Ce;
             umma::cp_async16(Bs + static_cast<size_t>(kb) * Np * 128 + r * 128 + ((c ^ (r & 7)) << 4),
                              ch + static_cast<size_t>(in ? r : 0) * D + ci * 8, in);
         }
     } else {
-        for (int i = tid; i < Np * (D / 8); i += 128) {
+        for (int i = tid; i < Np * (D / 8); i += kAssignThreads) {
             const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
             uint4 v = make_uint4(0, 0, 0, 0), v2 = make_uint4(0, 0, 0, 0);
             if (r < Ce) {
@@ -174,108 +194,183 @@ __global__ void __launch_bounds__(128) k_kmeans_assign_tc(const uint16_t *__rest
             *reinterpret_cast<uint4 *>(Bs + static_cast<size_t>(KB) * Np * 128 + off) = v2;
         }
     }
+    if (t0 < n_tiles) load_tile(t0, 0);
+    // padded columns score +inf, so no column needs a bounds test
+    for (int i = tid; i < Np; i += kAssignThreads) cn[i] = i < Ce ? cnorm[h * C + i] : INFINITY;
     umma::cp_async_wait_all();
-    for (int i = tid; i < Np; i += 128) cn[i] = i < Ce ? cnorm[h * C + i] : 0.0f;
     umma::fence_proxy_async_smem();
     if (warp == 0) {
-        umma::tmem_alloc(&tmem_base, Np <= 32 ? 32 : (Np <= 64 ? 64 : (Np <= 128 ? 128 : 256)));
+        umma::tmem_alloc(&tmem_base, 2 * ncols);
         umma::tmem_relinquish();
     }
     if (tid == 0) {
-        umma::mbar_init(&bar, 1);
+        umma::mbar_init(&bar[0], 1);
+        umma::mbar_init(&bar[1], 1);
         umma::fence_barrier_init();
     }
     umma::tc_fence_before();
     __syncthreads();
     umma::tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t ncols = Np <= 32 ? 32 : (Np <= 64 ? 64 : (Np <= 128 ? 128 : 256));
-    if (tid == 0) {
-        const uint32_t idesc = umma::idesc_f16(128, Np, 1);
-        const uint32_t a0 = umma::smem_u32(As), b0 = umma::smem_u32(Bs);
+    const uint32_t idesc = umma::idesc_f16(128, Np, 1);
+    const uint32_t b0 = umma::smem_u32(Bs);
+    auto issue = [&](int buf) {
+        const uint32_t a0 = umma::smem_u32(As + buf * AB);
 #pragma unroll
         for (int p = 0; p < P; ++p)
 #pragma unroll
             for (int s = 0; s < D / 16; ++s) {
                 const uint64_t ad = umma::desc_sw128(a0 + (s >> 2) * 16384 + (s & 3) * 32);
                 const uint64_t bd = umma::desc_sw128(b0 + (p * KB + (s >> 2)) * Np * 128 + (s & 3) * 32);
-                umma::mma_f16(tmem, ad, bd, idesc, (p | s) != 0);
+                umma::mma_f16(tmem + buf * ncols, ad, bd, idesc, (p | s) != 0);
             }
-        umma::mma_commit(&bar);
-    }
-    const bool ok = umma::mbar_wait(&bar, 0, kWaitNs);
-    umma::tc_fence_after();
-    if (!ok) {
-        if (tid == 0) raise_error(err, QVG_ERR_TIMEOUT);
-        umma::mbar_wait(&bar, 0, kWaitNs);  // let an in-flight MMA drain before freeing TMEM
-    } else {
-        const int r = warp * 32 + lane;
-        float best = INFINITY, second = INFINITY;
-        int arg = 0, arg2 = -1;
-        for (int c0 = 0; c0 < Np; c0 += 32) {
-            uint32_t acc[32];
-            umma::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, acc);
-            umma::tmem_ld_wait();
+        umma::mma_commit(&bar[buf]);
+    };
+    if (tid == 0 && t0 < n_tiles) issue(0);
+    bool ok = true;
+    int k = 0;  // local tile counter
+    for (int t = t0; t < n_tiles; t += tstep, ++k) {
+        const int buf = k & 1, nxt = t + tstep;
+        // the other buffer's previous tile (MMA and epilogue) finished before the
+        // barrier that ended the last iteration, so its rows can be reloaded
+        if (nxt < n_tiles) load_tile(nxt, buf ^ 1);
+        if (!umma::mbar_wait(&bar[buf], (k >> 1) & 1, kWaitNs)) ok = false;
+        ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
+        umma::tc_fence_after();
+        // epilogue of tile t while the next tile's loads are in flight.  Row r
+        // (token n) is read by one thread of each warp group; each keeps four
+        // independent (best, second) chains over its columns, merged by
+        // (score, index) so that ties still go to the lowest cluster.
+        const int r = (warp & 3) * 32 + lane, n = t * 128 + r;
+        float bv[4], sv[4];
+        int bi[4], si[4];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int c = c0 + k;
-                const float s = fmaf(-2.0f, __uint_as_float(acc[k]), cn[c < Np ? c : 0]);
-                if (c < Ce) {
-                    if (s < best) {
-                        second = best;
-                        arg2 = arg;
-                        best = s;
-                        arg = c;
-                    } else if (s < second) {
-                        second = s;
-                        arg2 = c;
+        for (int q = 0; q < 4; ++q) {
+            bv[q] = INFINITY;
+            sv[q] = INFINITY;
+            bi[q] = 0x7fffffff;
+            si[q] = 0x7fffffff;
+        }
+        if (ok) {
+            for (int c0 = grp * 32; c0 < Np; c0 += 64) {
+                uint32_t acc[32];
+                umma::tmem_ld32(tmem + buf * ncols + (static_cast<uint32_t>((warp & 3) * 32) << 16) + c0, acc);
+                umma::tmem_ld_wait();
+#pragma unroll
+                for (int kk = 0; kk < 32; ++kk) {
+                    const int c = c0 + kk, q = kk & 3;
+                    // columns past Np were not written by the MMA; cn is +inf past Ce
+                    const float sc = c < Np ? fmaf(-2.0f, __uint_as_float(acc[kk]), cn[c]) : INFINITY;
+                    if (sc < bv[q]) {
+                        sv[q] = bv[q];
+                        si[q] = bi[q];
+                        bv[q] = sc;
+                        bi[q] = c;
+                    } else if (sc < sv[q]) {
+                        sv[q] = sc;
+                        si[q] = c;
                     }
                 }
             }
         }
-        // The GEMM form ||c||^2 - 2 x.c cancels large terms (outlier channels),
-        // so its rounding can swap two nearly equidistant centroids.  The two
-        // best candidates are re-scored with the direct sum_j w_j (x_j - c_j)^2
-        // (fp32, ascending j), whose error is relative to the distance itself;
-        // ties go to the lower index.
-        if (arg2 >= 0 && n0 + r < N) {
-            const uint16_t *c1 = ch + static_cast<size_t>(arg) * D;
-            const uint16_t *c2 = ch + static_cast<size_t>(arg2) * D;
-            float d1 = 0.0f, d2 = 0.0f;
-#pragma unroll 4
+        auto less = [](float a, int ia, float b, int ib) { return a < b || (a == b && ia < ib); };
+        auto merge = [&](float &best, int &arg, float &second, int &arg2, float b2, int i2, float s2, int j2) {
+            if (less(b2, i2, best, arg)) {
+                if (less(best, arg, s2, j2)) {
+                    second = best;
+                    arg2 = arg;
+                } else {
+                    second = s2;
+                    arg2 = j2;
+                }
+                best = b2;
+                arg = i2;
+            } else if (less(b2, i2, second, arg2)) {
+                second = b2;
+                arg2 = i2;
+            }
+        };
+        float best = bv[0], second = sv[0];
+        int arg = bi[0], arg2 = si[0];
+#pragma unroll
+        for (int q = 1; q < 4; ++q) merge(best, arg, second, arg2, bv[q], bi[q], sv[q], si[q]);
+        if (grp == 1) {
+            xb[r][0] = best;
+            xb[r][1] = second;
+            xi[r][0] = arg;
+            xi[r][1] = arg2;
+        }
+        __syncthreads();
+        if (grp == 0) {
+            merge(best, arg, second, arg2, xb[r][0], xi[r][0], xb[r][1], xi[r][1]);
+            if (arg == 0x7fffffff) arg = 0;
+            if (arg2 == 0x7fffffff || !(second < INFINITY)) arg2 = -1;
+            xi[r][0] = arg;
+            xi[r][1] = arg2;
+        }
+        __syncthreads();
+        arg = xi[r][0];
+        arg2 = xi[r][1];
+        // The GEMM form cancels large outlier products; the two candidates are
+        // re-scored with the direct sum_j w_j (x_j - c_j)^2 (fp32, ascending j):
+        // group 0 scores the best, group 1 the second.  x comes from the token
+        // tile; c from the centroid tile (P == 1: it holds c itself) or from
+        // global memory (P == 2: the tile holds w*c).
+        float dd = 0.0f;
+        const int cand = grp == 0 ? arg : arg2;
+        if (arg2 >= 0 && n < N) {
+            const uint8_t *Ab = As + buf * AB;
+            const uint16_t *cg = ch + static_cast<size_t>(cand) * D;
+#pragma unroll
             for (int ci = 0; ci < D / 8; ++ci) {
                 const int kb = ci >> 3, c = ci & 7;
-                const uint4 xv = *reinterpret_cast<const uint4 *>(As + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4));
-                const uint4 u1 = *reinterpret_cast<const uint4 *>(c1 + ci * 8);
-                const uint4 u2 = *reinterpret_cast<const uint4 *>(c2 + ci * 8);
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w},
-                               w2[4] = {u2.x, u2.y, u2.z, u2.w};
+                const uint4 xv = *reinterpret_cast<const uint4 *>(Ab + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4));
+                uint4 u;
+                if constexpr (P == 1)
+                    u = *reinterpret_cast<const uint4 *>(Bs + static_cast<size_t>(kb) * Np * 128 + cand * 128 +
+                                                         ((c ^ (cand & 7)) << 4));
+                else
+                    u = *reinterpret_cast<const uint4 *>(cg + ci * 8);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int sh = (k & 1) ? 0 : 16;
-                    const float xj = __uint_as_float((xw[k >> 1] << sh) & 0xffff0000u);
-                    const float e1 = xj - __uint_as_float((w1[k >> 1] << sh) & 0xffff0000u);
-                    const float e2 = xj - __uint_as_float((w2[k >> 1] << sh) & 0xffff0000u);
-                    const float wj = w ? w[h * D + ci * 8 + k] : 1.0f;
-                    d1 = fmaf(wj * e1, e1, d1);
-                    d2 = fmaf(wj * e2, e2, d2);
+                for (int e = 0; e < 8; ++e) {
+                    const int sh = (e & 1) ? 0 : 16;
+                    const float xj = __uint_as_float((xw[e >> 1] << sh) & 0xffff0000u);
+                    const float df = xj - __uint_as_float((uw[e >> 1] << sh) & 0xffff0000u);
+                    const float wj = w ? w[h * D + ci * 8 + e] : 1.0f;
+                    dd = fmaf(wj * df, df, dd);
                 }
             }
-            if (d2 < d1 || (d2 == d1 && arg2 < arg)) arg = arg2;
         }
-        if (n0 + r < N) ids[static_cast<size_t>(h) * N + n0 + r] = arg;
+        if (grp == 1) xd[r] = dd;
+        __syncthreads();
+        if (grp == 0) {
+            if (arg2 >= 0 && (xd[r] < dd || (xd[r] == dd && arg2 < arg))) arg = arg2;
+            if (ok && n < N) ids[static_cast<size_t>(h) * N + n] = arg;
+        }
+        // the next tile's operands are in shared memory: start its MMA
+        umma::cp_async_wait_all();
+        umma::fence_proxy_async_smem();
+        umma::tc_fence_before();
+        if (!__syncthreads_and(ok)) {
+            ok = false;
+            break;
+        }
+        umma::tc_fence_after();
+        if (tid == 0 && nxt < n_tiles) issue(buf ^ 1);
+    }    if (!ok) {
+        if (tid == 0) raise_error(err, QVG_ERR_TIMEOUT);
+        // let in-flight MMAs drain before TMEM is released
+        umma::mbar_wait(&bar[0], 0, kWaitNs);
     }
     umma::tc_fence_before();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(tmem, ncols);
+    if (warp == 0) {
+        umma::tc_fence_after();
+        umma::tmem_dealloc(tmem, 2 * ncols);
+    }
 }
 
-// ---------------------------------------------------------------------------
-// Update: each centroid becomes the mean of its members' stage input (fp32
-// sums in a fixed order: ascending token order inside each warp, warps
-// combined in index order), rounded to bf16; empty clusters keep their
-// value.  A diagonal weight leaves the minimiser at the plain mean.
-// One CTA (4 warps) per (head, 8 clusters).
 template <typename T> struct RowLoad;
 template <> struct RowLoad<uint16_t> {
     template <int E>
@@ -306,80 +401,121 @@ template <> struct RowLoad<float> {
     }
 };
 
+// ---------------------------------------------------------------------------
+// Update, one kernel: each CTA (kUpdSplit per head) first orders the head's
+// token indices by cluster in shared memory, stably (ascending token index
+// inside each cluster): per-cluster counts, an exclusive scan, then rounds of
+// 1024 tokens in which each token's place is its cluster's running offset
+// plus the number of earlier same-cluster tokens of the round (warp match +
+// popc inside a warp, per-warp counts across warps).  Then one warp per
+// cluster of the CTA's share sums the members' stage input in that order
+// (fp32, eight row loads in flight), divides by the count, rounds to bf16
+// and writes the centroid and its weighted norm; an empty cluster keeps its
+// centroid.  Deterministic, with no atomic accumulation of values.  A
+// diagonal weight leaves the minimiser at the plain mean.
+constexpr int kUpdThreads = 1024;
+constexpr int kUpdSplit = 4;  // CTAs per head, each finalising a quarter of the clusters
+
 template <int D, typename TIn>
-__global__ void __launch_bounds__(128) k_kmeans_update(const TIn *__restrict__ xin, int N, int H,
-                                                      const int32_t *__restrict__ ids,
-                                                      uint16_t *__restrict__ cent, size_t hs,
-                                                      int Ce, const float *__restrict__ w,
-                                                      float *__restrict__ cnorm, int C) {
+__global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__restrict__ xin, int N, int H,
+                                                              const int32_t *__restrict__ ids,
+                                                              uint16_t *__restrict__ cent, size_t hs, int Ce,
+                                                              const float *__restrict__ w,
+                                                              float *__restrict__ cnorm, int C) {
+    constexpr int W = kUpdThreads / 32;
     constexpr int E = D / 32;
-    constexpr int KC = 8;  // clusters per CTA
-    __shared__ float part[4][KC][D];
-    __shared__ int pcnt[4][KC];
-    const int h = blockIdx.y, c0 = blockIdx.x * KC;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float acc[KC][E];
-    int cnt[KC];
-#pragma unroll
-    for (int k = 0; k < KC; ++k) {
-        cnt[k] = 0;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[k][e] = 0.0f;
-    }
-    const int nbatch = ceil_div(N, 32);
+    extern __shared__ __align__(16) uint16_t order[];          // [N] token indices, by cluster
+    __shared__ int cnt[QVG_MAX_CLUSTERS + 1];
+    __shared__ int run[QVG_MAX_CLUSTERS];
+    __shared__ int wc[W][QVG_MAX_CLUSTERS];                   // per-warp counts of a round
+    const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t *hid = ids + static_cast<size_t>(h) * N;
-    for (int b = warp; b < nbatch; b += 4) {
-        const int n = b * 32 + lane;
-        const int id = n < N ? hid[n] : -1;
+    for (int c = tid; c <= Ce; c += kUpdThreads) cnt[c] = 0;
+    __syncthreads();
+    for (int n = tid; n < N; n += kUpdThreads) atomicAdd(&cnt[hid[n]], 1);
+    __syncthreads();
+    // exclusive scan of the counts by warp 0 (Ce <= 256: 8 per lane)
+    if (warp == 0) {
+        int v[8], tot = 0;
 #pragma unroll
-        for (int k = 0; k < KC; ++k) {
-            unsigned m = __ballot_sync(0xffffffffu, id == c0 + k);
-            cnt[k] += __popc(m);
-            while (m) {
-                // up to 8 members at a time: issue their row loads together,
-                // then add them in ascending token order
-                int nn[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    nn[q] = m ? b * 32 + __ffs(m) - 1 : -1;
-                    m &= m ? m - 1 : 0u;
-                }
-                float v[8][E];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (nn[q] >= 0)
-                        RowLoad<TIn>::template load<E>(xin + (static_cast<size_t>(nn[q]) * H + h) * D + lane * E, v[q]);
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (nn[q] >= 0)
-#pragma unroll
-                        for (int e = 0; e < E; ++e) acc[k][e] += v[q][e];
-            }
+        for (int i = 0; i < 8; ++i) {
+            const int c = lane * 8 + i;
+            v[i] = c < Ce ? cnt[c] : 0;
+            tot += v[i];
         }
-    }
+        int incl = tot;
 #pragma unroll
-    for (int k = 0; k < KC; ++k) {
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int acc = incl - tot;
 #pragma unroll
-        for (int e = 0; e < E; ++e) part[warp][k][lane * E + e] = acc[k][e];
-        if (lane == 0) pcnt[warp][k] = cnt[k];
+        for (int i = 0; i < 8; ++i) {
+            const int c = lane * 8 + i;
+            if (c < Ce) {
+                run[c] = acc;
+                cnt[c] = acc;  // cnt now holds each cluster's first position
+            }
+            acc += v[i];
+        }
+        if (lane == 31) cnt[Ce] = incl;
     }
     __syncthreads();
-    // warp w finalises clusters 2w and 2w+1 of this CTA
-    for (int kk = 0; kk < 2; ++kk) {
-        const int k = warp * 2 + kk, c = c0 + k;
-        if (c >= Ce) continue;
-        const int total = pcnt[0][k] + pcnt[1][k] + pcnt[2][k] + pcnt[3][k];
-        if (total == 0) continue;
-        uint16_t *row = cent + static_cast<size_t>(h) * hs + static_cast<size_t>(c) * D;
+    // stable placement, rounds of 1024 tokens
+    for (int base = 0; base < N; base += kUpdThreads) {
+        for (int i = tid; i < W * Ce; i += kUpdThreads) wc[i / Ce][i % Ce] = 0;
+        __syncthreads();
+        const int n = base + tid;
+        const int c = n < N ? hid[n] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, c);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (c >= 0 && rank == 0) wc[warp][c] = __popc(peers);
+        __syncthreads();
+        if (c >= 0) {
+            int before = 0;
+            for (int w2 = 0; w2 < warp; ++w2) before += wc[w2][c];
+            order[run[c] + before + rank] = static_cast<uint16_t>(n);
+        }
+        __syncthreads();
+        for (int cc = tid; cc < Ce; cc += kUpdThreads) {
+            int t = 0;
+            for (int w2 = 0; w2 < W; ++w2) t += wc[w2][cc];
+            run[cc] += t;
+        }
+        __syncthreads();
+    }
+    // this CTA's clusters: one warp each, members summed in token order
+    for (int c = blockIdx.x + kUpdSplit * warp; c < Ce; c += kUpdSplit * W) {
+        const int beg = cnt[c], end = cnt[c + 1];
+        if (end == beg) continue;  // empty: keep the centroid
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+        for (int i0 = beg; i0 < end; i0 += 8) {
+            int nn[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) nn[q] = i0 + q < end ? static_cast<int>(order[i0 + q]) : -1;
+            float v[8][E];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (nn[q] >= 0)
+                    RowLoad<TIn>::template load<E>(xin + (static_cast<size_t>(nn[q]) * H + h) * D + lane * E, v[q]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (nn[q] >= 0)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] += v[q][e];
+        }
+        const float cntf = static_cast<float>(end - beg);
+        uint16_t *row = cent + static_cast<size_t>(h) * hs + static_cast<size_t>(c) * D + lane * E;
         float nrm = 0.0f;
-        for (int j = lane; j < D; j += 32) {
-            const float s = ((part[0][k][j] + part[1][k][j]) + part[2][k][j]) + part[3][k][j];
-            const float mean = __fdiv_rn(s, static_cast<float>(total));
-            const uint16_t cb = f32_to_bf16(mean);
-            row[j] = cb;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const uint16_t cb = f32_to_bf16(__fdiv_rn(acc[e], cntf));
+            row[e] = cb;
             const float cv = bf16_to_f32(cb);
-            const float wj = w ? w[h * D + j] : 1.0f;
+            const float wj = w ? w[h * D + lane * E + e] : 1.0f;
             nrm = fmaf(wj * cv, cv, nrm);
         }
         for (int o = 16; o > 0; o >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o);
@@ -537,17 +673,30 @@ static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t
                                  const float *cnorm, int C, const float *w, int32_t *ids, cudaStream_t st) {
     const int Np = std::max(16, ceil_div(Ce, 16) * 16);
     constexpr int KB = D / 64;
-    size_t smem = static_cast<size_t>(KB) * 128 * 128 + static_cast<size_t>(P) * KB * Np * 128 + Np * 4;
-    // at least ~100 KB so that at most two CTAs (2 x 256 TMEM columns) share an SM
-    smem = std::max<size_t>(smem, 100 * 1024) + 1024;
+    const size_t smem = 2 * static_cast<size_t>(KB) * 128 * 128 + static_cast<size_t>(P) * KB * Np * 128 +
+                        Np * 4 + 1024;
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_kmeans_assign_tc<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        // the largest request of this instantiation (Np = 256)
+        const size_t most = 2 * static_cast<size_t>(KB) * 128 * 128 +
+                            static_cast<size_t>(P) * KB * QVG_MAX_CLUSTERS * 128 + QVG_MAX_CLUSTERS * 4 + 1024;
+        const cudaError_t e = cudaFuncSetAttribute(k_kmeans_assign_tc<D, P>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(most));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            note_cuda_error(e);
+            return QVG_ERR_CUDA;
+        }
         attr = true;
     }
-    dim3 grid(ceil_div(N, 128), H);
-    k_kmeans_assign_tc<D, P><<<grid, 128, smem, st>>>(g, N, H, cent, hs, Ce, Np, cnorm, C, w, ids,
-                                                      device_error_word());
+    // one CTA per SM in total, spread over the heads; each walks
+    // ceil(tiles / ctas_per_head) token tiles of its head
+    const int n_tiles = ceil_div(N, 128);
+    const int per_head = std::max(1, std::min(n_tiles, sm_count() / std::max(1, H)));
+    dim3 grid(per_head, H);
+    k_kmeans_assign_tc<D, P><<<grid, kAssignThreads, smem, st>>>(g, N, H, cent, hs, Ce, Np, cnorm, C, w, ids,
+                                                                 device_error_word());
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }
@@ -563,20 +712,32 @@ qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d, const ui
 }
 
 qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int d,
-                                const int32_t *ids, uint16_t *cent, size_t hs, int Ce, int C,
-                                const float *w, float *cnorm, cudaStream_t st) {
-    dim3 grid(ceil_div(Ce, 8), H);
+                                const int32_t *ids, uint16_t *cent, size_t hs, int Ce, int C, const float *w,
+                                float *cnorm, cudaStream_t st) {
+    const size_t smem = static_cast<size_t>(N) * sizeof(uint16_t);
+    dim3 grid(kUpdSplit, H);
+#define QVG_UPD(D_, T_)                                                                                     \
+    do {                                                                                                    \
+        static bool attr = false;                                                                           \
+        if (!attr) {                                                                                        \
+            const cudaError_t e = cudaFuncSetAttribute(k_kmeans_update<D_, T_>,                             \
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 131072); \
+            if (e != cudaSuccess) {                                                                         \
+                (void)cudaGetLastError();                                                                   \
+                note_cuda_error(e);                                                                         \
+                return QVG_ERR_CUDA;                                                                        \
+            }                                                                                               \
+            attr = true;                                                                                    \
+        }                                                                                                   \
+        k_kmeans_update<D_, T_><<<grid, kUpdThreads, smem, st>>>(static_cast<const T_ *>(xin), N, H, ids,   \
+                                                                 cent, hs, Ce, w, cnorm, C);                \
+    } while (0)
     if (d == 64) {
-        if (xin_f32)
-            k_kmeans_update<64, float><<<grid, 128, 0, st>>>(static_cast<const float *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C);
-        else
-            k_kmeans_update<64, uint16_t><<<grid, 128, 0, st>>>(static_cast<const uint16_t *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C);
+        if (xin_f32) QVG_UPD(64, float); else QVG_UPD(64, uint16_t);
     } else {
-        if (xin_f32)
-            k_kmeans_update<128, float><<<grid, 128, 0, st>>>(static_cast<const float *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C);
-        else
-            k_kmeans_update<128, uint16_t><<<grid, 128, 0, st>>>(static_cast<const uint16_t *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C);
+        if (xin_f32) QVG_UPD(128, float); else QVG_UPD(128, uint16_t);
     }
+#undef QVG_UPD
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }

@@ -226,8 +226,13 @@ qvg_status launch_psac_basis(const float *M, const int64_t *count, int H, int d,
     const size_t smem = (2 * static_cast<size_t>(d) * d + JD) * sizeof(float) + JD * sizeof(int);
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_psac_jacobi, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const cudaError_t e = cudaFuncSetAttribute(k_psac_jacobi, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>((2 * JD * JD + JD) * sizeof(float) + JD * sizeof(int)));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            note_cuda_error(e);
+            return QVG_ERR_CUDA;
+        }
         attr = true;
     }
     k_psac_jacobi<<<H, 512, smem, st>>>(M, count, d, rank, U, eig, frac);
