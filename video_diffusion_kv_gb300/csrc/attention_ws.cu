@@ -8,14 +8,8 @@
 // memory.
 //
 // One CTA = two 128-row query tiles of one query head (ping-pong, so the
-// tensor core computes one tile's S while the other tile's softmax runs).
-// Warp roles (16 warps, 128 registers per thread):
-//   0-3, 4-7   softmax + epilogue of query tile 0 / 1 (thread = query row)
-//   8-11       K producers: rebuild a 128-slot K_hat tile (thread = slot)
-//   12-15      V producers: rebuild V_hat^T (thread = slot, double-buffered);
-//              warp 12 owns the TMEM allocation and its lane 0 issues every
-//              tcgen05.mma (S_0, S_1 before producing the V tile, which must
-//              wait for the previous PV products anyway; PV_0, PV_1 after)
+// tensor core computes one tile's products while the other tile's softmax
+// runs); the warp roles and barriers are listed above the kernel.
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
 // O1 [384,384+D), fp32.  Per cache tile t:
 //   S_i = Q_i K_t^T              (M=128, N=128 slots, K=D; fp16 operands)
@@ -52,8 +46,9 @@ struct AttnWsArgs {
 
 namespace ws {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 17;
 constexpr int kThreads = kWarps * 32;
+constexpr int kIssuerWarp = 16;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescale = 8.0f;
 
@@ -156,114 +151,257 @@ __device__ __noinline__ void rebuild8(const AttnWsArgs &a, const uint8_t *codes,
     }
 }
 
-// One-stage fast path: the loads of a slot's 64-channel half are issued
-// before any arithmetic (code bits, scales, cluster id, then the 128-byte
-// bf16 centroid piece), so a producer thread exposes its memory latency once
-// per half rather than once per 8 channels.  K_hat = fma(S, q, c) in fp32,
-// rounded to fp16; out gets 32 packed half2 words (channels kb*64 ..).
+// One-stage fast path, split into its loads and its arithmetic so that a
+// producer can put the loads of a 64-channel half in flight before it waits
+// for its buffer.  K_hat (or V_hat) = fma(S, q, c) in fp32, rounded to fp16.
+template <int BITS>
+struct HalfData {
+    uint4 cw[BITS == 2 ? 1 : 2];  // 64 codes
+    float S[8];                   // scale of each 8-channel block
+    uint4 cr[8];                  // 64 bf16 centroid channels
+};
+
 template <int D, int BITS>
-__device__ __forceinline__ void rebuild_half_fast(const AttnWsArgs &a, const uint8_t *codes,
-                                                  const uint16_t *scales, const uint8_t *ids,
-                                                  const uint16_t *cent, int h, int chunk, int slot, int kb,
-                                                  uint32_t (&out)[32]) {
+__device__ __forceinline__ void load_half(const AttnWsArgs &a, const uint8_t *codes, const uint16_t *scales,
+                                          const uint16_t *cent, int h, int chunk, int slot, int id, int kb,
+                                          HalfData<BITS> &hd) {
     constexpr int NB = D * BITS / 8;
-    constexpr int HB = 64 * BITS / 8;      // code bytes of a 64-channel half: 16 (INT2) or 32 (INT4)
+    constexpr int HB = 64 * BITS / 8;
     const int ng = D / a.group;
     const size_t srow = static_cast<size_t>(h) * a.cap + slot;
-    uint4 cw[HB / 16];
 #pragma unroll
-    for (int i = 0; i < HB / 16; ++i) cw[i] = *reinterpret_cast<const uint4 *>(codes + srow * NB + kb * HB + 16 * i);
-    float S[8];
+    for (int i = 0; i < HB / 16; ++i) hd.cw[i] = *reinterpret_cast<const uint4 *>(codes + srow * NB + kb * HB + 16 * i);
     if (a.group >= 64) {
         const float s0 = f16_to_f32(scales[srow * ng + (kb * 64) / a.group]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) S[i] = s0;
+        for (int i = 0; i < 8; ++i) hd.S[i] = s0;
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) S[i] = f16_to_f32(scales[srow * ng + (kb * 64 + 8 * i) / a.group]);
+        for (int i = 0; i < 8; ++i) hd.S[i] = f16_to_f32(scales[srow * ng + (kb * 64 + 8 * i) / a.group]);
     }
-    uint4 cr[8];
     if (a.C > 0) {
-        const uint16_t *row = cent + (static_cast<size_t>(h) * a.max_chunks + chunk) * a.C * D +
-                              static_cast<size_t>(ids[srow]) * D + kb * 64;
+        const uint16_t *row = cent + ((static_cast<size_t>(h) * a.max_chunks + chunk) * a.C + id) * D + kb * 64;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cr[i] = *reinterpret_cast<const uint4 *>(row + 8 * i);
+        for (int i = 0; i < 8; ++i) hd.cr[i] = *reinterpret_cast<const uint4 *>(row + 8 * i);
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cr[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 8; ++i) hd.cr[i] = make_uint4(0, 0, 0, 0);
     }
-    const uint32_t *cb = reinterpret_cast<const uint32_t *>(cw);
+}
+
+// Decodes the half and stores it as the eight swizzled 16-byte chunks of the
+// slot's 128-byte line `dst` (chunk c at position c ^ (r % 8)), one chunk as
+// soon as its four words are ready.
+template <int BITS>
+__device__ __forceinline__ void decode_store_half(const HalfData<BITS> &hd, uint8_t *dst, int r) {
+    const uint32_t *cb = reinterpret_cast<const uint32_t *>(hd.cw);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint32_t bits = static_cast<uint32_t>((cb[(8 * i * BITS) / 32] >> ((8 * i * BITS) % 32)) &
                                                     ((1ull << (8 * BITS)) - 1ull));
-        const uint32_t c4[4] = {cr[i].x, cr[i].y, cr[i].z, cr[i].w};
+        const uint32_t c4[4] = {hd.cr[i].x, hd.cr[i].y, hd.cr[i].z, hd.cr[i].w};
+        uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int q0 = static_cast<int>((bits >> (2 * e * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
             const int q1 = static_cast<int>((bits >> ((2 * e + 1) * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
-            const float v0 = fmaf(S[i], static_cast<float>(q0), __uint_as_float(c4[e] << 16));
-            const float v1 = fmaf(S[i], static_cast<float>(q1), __uint_as_float(c4[e] & 0xffff0000u));
-            out[4 * i + e] = h2(v0, v1);
+            const float v0 = fmaf(hd.S[i], static_cast<float>(q0), __uint_as_float(c4[e] << 16));
+            const float v1 = fmaf(hd.S[i], static_cast<float>(q1), __uint_as_float(c4[e] & 0xffff0000u));
+            w[e] = h2(v0, v1);
         }
+        *reinterpret_cast<uint4 *>(dst + ((i ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
-// One-stage fast path for the V producers: channels [j0, j0 + 8) of 8
-// consecutive slots, every load issued before the arithmetic.
-template <int D, int BITS>
-__device__ __forceinline__ void rebuild_8x8_fast(const AttnWsArgs &a, int h, int chunk, int slot0, int nvalid_rel,
-                                                 int j0, uint32_t (&hv)[8][4]) {
-    constexpr int NB = D * BITS / 8;
-    const int ng = D / a.group;
-    const uint16_t *cbase = a.vcent + (static_cast<size_t>(h) * a.max_chunks + chunk) * a.C * D + j0;
-    int id[8];
-    uint32_t bits[8];
-    float S[8];
+// Packed fp32 pairs (Blackwell f32x2 arithmetic).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Adds the two fp16 halves of a packed pair to two fp32 sums (sm_100-family
+// mixed-precision add: the fp16 value is widened exactly).
+__device__ __forceinline__ void add_f16x2_to(uint32_t p, float &s0, float &s1) {
+    asm("{\n\t.reg .f16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "add.rn.f32.f16 %0, h0, %0;\n\tadd.rn.f32.f16 %1, h1, %1;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "r"(p));
+}
+
+// P = exp2(s * scale_log2 - m) for 32 logits of one row, rounded to fp16 and
+// stored as four 16-byte chunks of the row's swizzled P_i line.  The row sum
+// adds the same fp16 values the PV product uses, so the weights of O are
+// normalised exactly (a one-slot cache returns V_hat unchanged).  Columns at
+// or past nvalid (relative to c0) give 0.
+__device__ __forceinline__ void softmax_chunk(const uint32_t (&v)[32], int c0, int nvalid, uint64_t sl2,
+                                              uint64_t nm2, uint8_t *Prow, int r, float (&acc)[4]) {
+    uint32_t pk[16];
+    const bool full = c0 + 32 <= nvalid;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const size_t srow = static_cast<size_t>(h) * a.cap + slot0 + k;
-        const bool ok = k < nvalid_rel;
-        id[k] = (ok && a.C > 0) ? a.vids[srow] : 0;
-        if constexpr (BITS == 2)
-            bits[k] = ok ? *reinterpret_cast<const uint16_t *>(a.vcodes + srow * NB + j0 / 4) : 0u;
-        else
-            bits[k] = ok ? *reinterpret_cast<const uint32_t *>(a.vcodes + srow * NB + j0 / 2) : 0u;
-        S[k] = ok ? f16_to_f32(a.vscales[srow * ng + j0 / a.group]) : 0.0f;
-    }
-    uint4 cr[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        cr[k] = (k < nvalid_rel && a.C > 0) ? *reinterpret_cast<const uint4 *>(cbase + static_cast<size_t>(id[k]) * D)
-                                            : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t c4[4] = {cr[k].x, cr[k].y, cr[k].z, cr[k].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int q0 = static_cast<int>((bits[k] >> (2 * e * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
-            const int q1 = static_cast<int>((bits[k] >> ((2 * e + 1) * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
-            const float v0 = fmaf(S[k], static_cast<float>(q0), __uint_as_float(c4[e] << 16));
-            const float v1 = fmaf(S[k], static_cast<float>(q1), __uint_as_float(c4[e] & 0xffff0000u));
-            hv[k][e] = k < nvalid_rel ? h2(v0, v1) : 0u;
+    for (int k = 0; k < 16; ++k) {
+        float y0, y1;
+        up2(fma2(pk2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), sl2, nm2), y0, y1);
+        float p0 = ex2(y0), p1 = ex2(y1);
+        if (!full) {
+            p0 = c0 + 2 * k < nvalid ? p0 : 0.0f;
+            p1 = c0 + 2 * k + 1 < nvalid ? p1 : 0.0f;
         }
+        pk[k] = h2(p0, p1);
+        add_f16x2_to(pk[k], acc[2 * (k & 1)], acc[2 * (k & 1) + 1]);
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int ci = c0 / 8 + x, kb = ci >> 3, c = ci & 7;
+        *reinterpret_cast<uint4 *>(Prow + kb * 16384 + ((c ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+    }
+}
+
+// One producer role: the compressed stream it rebuilds and its buffers.
+// Tile t goes to buffer t % nbuf (QVG_TILE slots x D channels, 64-channel
+// blocks of 128-byte swizzled lines); full[b] gets one arrival per slot
+// thread, free[b] is committed by the MMAs that read the buffer.
+struct Producer {
+    const uint8_t *codes;
+    const uint16_t *scales;
+    const uint8_t *ids;
+    const uint16_t *cent;
+    uint8_t *buf0;
+    uint64_t *full, *freeb;
+    int nbuf;
+    bool psac;
+};
+
+// One stage, no PSAC.  A tile's first-half loads are issued before the wait
+// for its buffer; the next tile's table entry and cluster id are loaded one
+// tile ahead (slot (t + 1) * QVG_TILE + r < n_slots <= capacity: in bounds).
+template <int D, int BITS>
+__device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer &pr, int h, int r, int n_tiles,
+                                             volatile int *vfail) {
+    constexpr int KB = D / 64, TB = KB * 16384;
+    const size_t id_row = static_cast<size_t>(h) * a.cap + r;
+    TileInfo ti{};
+    int id = 0;
+    if (n_tiles > 0) {
+        ti = tile_info(a, 0);
+        if (a.C > 0) id = pr.ids[id_row];
+    }
+    for (int t = 0; t < n_tiles; ++t) {
+        const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
+        uint8_t *T = pr.buf0 + b * TB + r * 128;
+        TileInfo tn{};
+        int idn = 0;
+        if (t + 1 < n_tiles) {
+            tn = tile_info(a, t + 1);
+            if (a.C > 0) idn = pr.ids[id_row + static_cast<size_t>(t + 1) * QVG_TILE];
+        }
+        const bool valid = r < ti.nvalid;
+        HalfData<BITS> hd;
+        if (valid) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti.chunk, ti.s0 + r, id, 0, hd);
+        if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) {
+            if (valid) {
+                decode_store_half<BITS>(hd, T + kb * 16384, r);
+            } else {
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4 *>(T + kb * 16384 + (c8 << 4)) = make_uint4(0, 0, 0, 0);
+            }
+            if (valid && kb + 1 < KB)
+                load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti.chunk, ti.s0 + r, id, kb + 1, hd);
+        }
+        umma::fence_proxy_async_smem();
+        umma::mbar_arrive(&pr.full[b]);
+        ti = tn;
+        id = idn;
+    }
+}
+
+// Several stages and/or PSAC: 8 channels at a time through rebuild8.
+template <int D, int BITS>
+__device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer &pr, int h, int r, int n_tiles,
+                                             volatile int *vfail) {
+    constexpr int KB = D / 64, TB = KB * 16384;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
+        uint8_t *T = pr.buf0 + b * TB + r * 128;
+        const TileInfo ti = tile_info(a, t);
+        const bool valid = r < ti.nvalid;
+        if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
+        float pk[QVG_PSAC_RANK];
+        if (pr.psac && valid) {
+            const size_t prow = static_cast<size_t>(h) * a.cap + ti.s0 + r;
+            const float pS = f16_to_f32(a.psac_s[prow]);
+            const int2 pv = *reinterpret_cast<const int2 *>(a.psac_p + prow * QVG_PSAC_RANK);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                pk[k] = pS * static_cast<float>(static_cast<int8_t>((pv.x >> (8 * k)) & 0xff));
+                pk[k + 4] = pS * static_cast<float>(static_cast<int8_t>((pv.y >> (8 * k)) & 0xff));
+            }
+        }
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll 2
+            for (int c8 = 0; c8 < 8; ++c8) {
+                uint4 o = make_uint4(0, 0, 0, 0);
+                if (valid) {
+                    float kv[8];
+                    rebuild8<D, BITS>(a, pr.codes, pr.scales, pr.ids, pr.cent, h, ti.chunk, ti.s0 + r, kb * 64 + c8 * 8,
+                                      pr.psac ? pk : nullptr, kv);
+                    o = make_uint4(h2(kv[0], kv[1]), h2(kv[2], kv[3]), h2(kv[4], kv[5]), h2(kv[6], kv[7]));
+                }
+                *reinterpret_cast<uint4 *>(T + kb * 16384 + ((c8 ^ (r & 7)) << 4)) = o;
+            }
+        }
+        umma::fence_proxy_async_smem();
+        umma::mbar_arrive(&pr.full[b]);
     }
 }
 
 }  // namespace ws
 
+// Warp roles (17 warps):
+//   0-3, 4-7   softmax + epilogue of query tile 0 / 1 (thread = query row)
+//   8-11       K producers: rebuild the 128-slot K_hat tile (thread = slot)
+//   12-15      V producers: rebuild V_hat into one of two buffers (thread = slot)
+//   16         owns the TMEM allocation; its lane 0 issues every tcgen05.mma
+// Both producers write a tile as [64-channel block][slot][64 channels] with
+// the 128-byte swizzle: K-major for the S = Q K_hat^T product (N = slots,
+// K = channels) and, read through an MN-major descriptor, the B operand of
+// O += P V_hat (N = channels, K = slots), so V needs no transpose.
+// Barriers (phase = tile index, per buffer for V):
+//   kfull/vfull  producers -> issuer    tile written
+//   kfree/vfree  MMA commit -> producer tile consumed (after S_1 / after PV_1)
+//   sfull[i]     MMA commit -> softmax  S_i ready
+//   sfree[i]     softmax -> issuer      S_i read out (TMEM columns reusable)
+//   pfull[i]     softmax -> issuer      P_i in shared memory, O_i rescaled
+//   ofull[i]     MMA commit -> softmax  PV_i done (P_i free, O_i settled)
+// The issuer polls and issues whatever is ready in the order S_0, S_1, PV_0,
+// PV_1 of each tile, so S of the next tile overlaps the softmax of this one.
 template <int D, int BITS, bool TOP1>
 __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) {
     using namespace ws;
     constexpr int KB = D / 64;
-    constexpr int QB = KB * 16384;       // one 128 x D fp16 tile
-    constexpr int VB = D * 256;          // D x 128 fp16 (two 64-slot K blocks)
+    constexpr int TB = KB * 16384;       // one 128 x D fp16 tile
     constexpr int PB = 32768;            // 128 x 128 fp16
-    constexpr int DS = D / 8;            // V channels per producer thread
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
-    uint8_t *Q0 = sm, *Q1 = Q0 + QB, *Kt = Q1 + QB, *Vt0 = Kt + QB, *P0 = Vt0 + 2 * VB, *P1 = P0 + PB;
-    __shared__ uint64_t kfull, vfull[2], kfree, vfree[2], sfull[2], pfull[2], ofull[2];
+    uint8_t *Q0 = sm, *Q1 = Q0 + TB, *Kt = Q1 + TB, *Vt0 = Kt + TB, *P0 = Vt0 + 2 * TB, *P1 = P0 + PB;
+    __shared__ uint64_t kfull, kfree, vfull[2], vfree[2], sfull[2], sfree[2], pfull[2], ofull[2], drain;
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
 
@@ -285,17 +423,19 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         }
         *reinterpret_cast<uint4 *>((rr < 128 ? Q0 : Q1) + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
-    if (warp == 12) {
+    if (warp == kIssuerWarp) {
         umma::tmem_alloc(&tmem_base, 512);
         umma::tmem_relinquish();
     }
     if (tid == 0) {
         umma::mbar_init(&kfull, 128);
         umma::mbar_init(&kfree, 1);
+        umma::mbar_init(&drain, 1);
         for (int i = 0; i < 2; ++i) {
             umma::mbar_init(&vfull[i], 128);
             umma::mbar_init(&vfree[i], 1);
             umma::mbar_init(&sfull[i], 1);
+            umma::mbar_init(&sfree[i], 128);
             umma::mbar_init(&pfull[i], 128);
             umma::mbar_init(&ofull[i], 1);
         }
@@ -314,17 +454,16 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         const int i = warp >> 2, r = tid & 127;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + i * 128 + lane_off, tO = tmem + 256 + i * 128 + lane_off;
-        uint8_t *Pi = i ? P1 : P0;
+        uint8_t *Prow = (i ? P1 : P0) + r * 128;
         float m_used = -INFINITY, l_sum = 0.0f, best = -INFINITY;
-        int best_slot = 0, it = 0;
-        for (int t = 0; t < n_tiles; ++t) {
+        int best_slot = 0, t = 0;
+        for (; t < n_tiles; ++t) {
             const TileInfo ti = tile_info(a, t);
-            if (ti.nvalid == 0) continue;
-            if (!ws::wait(&sfull[i], it & 1, vfail)) break;
+            if (!ws::wait(&sfull[i], t & 1, vfail)) break;
             umma::tc_fence_after();
-            // row maximum of the raw logits (the scale is positive), then scaled
-            // once; four independent chains (the top-1 variant keeps one chain
-            // so that ties resolve to the lowest slot)
+            // row maximum of the raw logits (the scale is positive), scaled
+            // once; the top-1 variant keeps one in-order chain so that ties
+            // resolve to the lowest slot
             float rmax = -INFINITY;
             int targ = 0;
             if constexpr (TOP1) {
@@ -332,7 +471,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t v[32];
                     umma::tmem_ld32(tS + c0, v);
-                    umma::tmem_ld_wait();
+                    umma::tmem_ld_wait_regs(v);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         const float x = c0 + k < ti.nvalid ? __uint_as_float(v[k]) : -INFINITY;
@@ -345,10 +484,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t v[32];
                     umma::tmem_ld32(tS + c0, v);
-                    umma::tmem_ld_wait();
+                    umma::tmem_ld_wait_regs(v);
                     if (c0 + 32 <= ti.nvalid) {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(v[k]));
+                        for (int k = 0; k < 16; ++k)
+                            m4[k & 3] = max3(m4[k & 3], __uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
                     } else {
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
@@ -368,11 +508,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             bool rescale = false;
             if (tmax > m_used + kRescale) {
                 corr = ex2(m_used - tmax);
-                rescale = it > 0;
+                rescale = t > 0;
                 m_used = tmax;
             }
-            if (it > 0) {  // PV_i of the previous tile done: P_i is free and O_i settled
-                if (!ws::wait(&ofull[i], (it - 1) & 1, vfail)) break;
+            if (t > 0) {  // PV_i of the previous tile done: P_i is free and O_i settled
+                if (!ws::wait(&ofull[i], (t - 1) & 1, vfail)) break;
                 umma::tc_fence_after();
                 if (__any_sync(0xffffffffu, rescale)) {
                     const float f = rescale ? corr : 1.0f;
@@ -380,7 +520,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t v[32];
                         umma::tmem_ld32(tO + c0, v);
-                        umma::tmem_ld_wait();
+                        umma::tmem_ld_wait_regs(v);
 #pragma unroll
                         for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
                         umma::tmem_st32(tO + c0, v);
@@ -388,44 +528,28 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                     umma::tmem_st_wait();
                 }
             }
-            float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // P_i: the next 32 columns load while the current 32 are processed;
+            // S_i is released as soon as its last columns are in registers
+            const uint64_t sl2 = pk2(a.scale_log2, a.scale_log2), nm2 = pk2(-m_used, -m_used);
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
                 uint32_t v[32];
                 umma::tmem_ld32(tS + c0, v);
-                umma::tmem_ld_wait();
-                uint32_t pk[16];
-                const float nm = -m_used;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int c = c0 + 2 * k;
-                    float p0 = ex2(fmaf(__uint_as_float(v[2 * k]), a.scale_log2, nm));
-                    float p1 = ex2(fmaf(__uint_as_float(v[2 * k + 1]), a.scale_log2, nm));
-                    if (c0 + 32 > ti.nvalid) {
-                        p0 = c < ti.nvalid ? p0 : 0.0f;
-                        p1 = c + 1 < ti.nvalid ? p1 : 0.0f;
-                    }
-                    pk[k] = h2(p0, p1);
-                    // the row sum adds the fp16 values the PV product uses
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&pk[k]));
-                    ls4[k & 3] += f.x + f.y;
+                umma::tmem_ld_wait_regs(v);
+                if (c0 == 96) {
+                    umma::tc_fence_before();
+                    umma::mbar_arrive(&sfree[i]);
                 }
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const int ci = c0 / 8 + x, kb = ci >> 3, c = ci & 7;
-                    *reinterpret_cast<uint4 *>(Pi + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
-                }
+                softmax_chunk(v, c0, ti.nvalid, sl2, nm2, Prow, r, acc);
             }
-            const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-            l_sum = l_sum * corr + ls;
+            l_sum = l_sum * corr + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
             umma::fence_proxy_async_smem();
             umma::tc_fence_before();
             umma::mbar_arrive(&pfull[i]);
-            ++it;
         }
         // epilogue: O_i / l
-        bool ok = !*vfail && it > 0 && ws::wait(&ofull[i], (it - 1) & 1, vfail);
+        bool ok = !*vfail && t == n_tiles && n_tiles > 0 && ws::wait(&ofull[i], (t - 1) & 1, vfail);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             umma::tc_fence_after();
@@ -435,7 +559,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t v[32];
                 umma::tmem_ld32(tO + c0, v);
-                umma::tmem_ld_wait();
+                umma::tmem_ld_wait_regs(v);
                 if (qi < a.Nq) {
                     const size_t o = (static_cast<size_t>(qi) * a.Hq + hq) * D + c0;
                     if (a.out32) {
@@ -462,168 +586,84 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 if constexpr (TOP1) a.top1[static_cast<size_t>(hq) * a.Nq + qi] = best_slot;
             }
         }
-    } else if (warp < 12) {
-        // ------------------------------------------------ K producers (thread = slot)
-        const int r = tid - 256;
-        const bool psac = a.psac_p != nullptr;
-        int it = 0;
-        for (int t = 0; t < n_tiles; ++t) {
-            const TileInfo ti = tile_info(a, t);
-            if (ti.nvalid == 0) continue;
-            if (it > 0 && !ws::wait(&kfree, (it - 1) & 1, vfail)) break;
-            const bool valid = r < ti.nvalid;
-            float pk[QVG_PSAC_RANK];
-            if (psac && valid) {
-                const size_t prow = static_cast<size_t>(h) * a.cap + ti.s0 + r;
-                const float pS = f16_to_f32(a.psac_s[prow]);
-                const int2 pv = *reinterpret_cast<const int2 *>(a.psac_p + prow * QVG_PSAC_RANK);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    pk[k] = pS * static_cast<float>(static_cast<int8_t>((pv.x >> (8 * k)) & 0xff));
-                    pk[k + 4] = pS * static_cast<float>(static_cast<int8_t>((pv.y >> (8 * k)) & 0xff));
-                }
-            }
-            if (a.L == 1 && !psac) {
-#pragma unroll 1
-                for (int kb = 0; kb < KB; ++kb) {
-                    uint32_t hk[32];
-                    if (valid) {
-                        rebuild_half_fast<D, BITS>(a, a.kcodes, a.kscales, a.kids, a.kcent, h, ti.chunk, ti.s0 + r, kb, hk);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) hk[e] = 0u;
-                    }
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8)
-                        *reinterpret_cast<uint4 *>(Kt + kb * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4)) =
-                            make_uint4(hk[4 * c8], hk[4 * c8 + 1], hk[4 * c8 + 2], hk[4 * c8 + 3]);
-                }
-            } else {
-#pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-#pragma unroll 2
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        uint4 out = make_uint4(0, 0, 0, 0);
-                        if (valid) {
-                            float kv[8];
-                            rebuild8<D, BITS>(a, a.kcodes, a.kscales, a.kids, a.kcent, h, ti.chunk, ti.s0 + r,
-                                              kb * 64 + c8 * 8, psac ? pk : nullptr, kv);
-                            out = make_uint4(h2(kv[0], kv[1]), h2(kv[2], kv[3]), h2(kv[4], kv[5]), h2(kv[6], kv[7]));
-                        }
-                        *reinterpret_cast<uint4 *>(Kt + kb * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4)) = out;
-                    }
-                }
-            }
-            umma::fence_proxy_async_smem();
-            umma::mbar_arrive(&kfull);
-            ++it;
-        }
-    } else {
-        // ------------------------------------------------ V producers (8 slots x D/8 channels)
-        // and, on warp 12 lane 0, the MMA issuer
-        const int u = tid - 384;
-        const bool issuer = (warp == 12 && lane == 0);
-        const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16(128, D, 0);
-        const uint32_t q0a = umma::smem_u32(Q0), q1a = umma::smem_u32(Q1), ka = umma::smem_u32(Kt);
-        const uint32_t v0a = umma::smem_u32(Vt0), p0a = umma::smem_u32(P0), p1a = umma::smem_u32(P1);
-        uint64_t *last_bar = nullptr;  // barrier of the issuer's latest commit (drained on failure)
-        uint32_t last_par = 0;
-        int it = 0;
-        for (int t = 0; t < n_tiles; ++t) {
-            const TileInfo ti = tile_info(a, t);
-            if (ti.nvalid == 0) continue;
-            if (issuer) {
-                // S_i = Q_i K_t^T as soon as the K tile is ready
-                if (!ws::wait(&kfull, it & 1, vfail)) break;
+    } else if (warp < 16) {
+        // ------------------------------------------------ K / V producers (thread = slot)
+        const bool isv = warp >= 12;
+        const Producer pr{isv ? a.vcodes : a.kcodes, isv ? a.vscales : a.kscales, isv ? a.vids : a.kids,
+                          isv ? a.vcent : a.kcent, isv ? Vt0 : Kt, isv ? vfull : &kfull, isv ? vfree : &kfree,
+                          isv ? 2 : 1, !isv && a.psac_p != nullptr};
+        if (a.L == 1 && !pr.psac)
+            produce_fast<D, BITS>(a, pr, h, tid & 127, n_tiles, vfail);
+        else
+            produce_general<D, BITS>(a, pr, h, tid & 127, n_tiles, vfail);
+    } else if (lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16_bmn(128, D, 0);
+        const uint32_t qa0 = umma::smem_u32(Q0), qa1 = umma::smem_u32(Q1), pa0 = umma::smem_u32(P0),
+                       pa1 = umma::smem_u32(P1), ka = umma::smem_u32(Kt), va0 = umma::smem_u32(Vt0);
+        int js = 0, half = 0, jp[2] = {0, 0}, spins = 0;
+        uint64_t idle_since = 0;
+        while (jp[1] < n_tiles) {
+            bool prog = false;
+            // S_half of tile js: K tile written, S_half of tile js - 1 read out
+            if (js < n_tiles && umma::mbar_test_wait(&kfull, js & 1) &&
+                (js == 0 || umma::mbar_test_wait(&sfree[half], (js - 1) & 1))) {
                 umma::tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                    umma::mma_f16(tmem + 0, umma::desc_sw128(q0a + off), umma::desc_sw128(ka + off), idS, s != 0);
+                    umma::mma_f16(tmem + half * 128, umma::desc_sw128((half ? qa1 : qa0) + off),
+                                  umma::desc_sw128(ka + off), idS, s != 0);
                 }
-                umma::mma_commit(&sfull[0]);
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                    umma::mma_f16(tmem + 128, umma::desc_sw128(q1a + off), umma::desc_sw128(ka + off), idS, s != 0);
+                umma::mma_commit(&sfull[half]);
+                if (half == 1) {
+                    umma::mma_commit(&kfree);
+                    ++js;
                 }
-                umma::mma_commit(&sfull[1]);
-                umma::mma_commit(&kfree);
-                last_bar = &kfree;
-                last_par = it & 1;
+                half ^= 1;
+                prog = true;
             }
-            // V tiles are double-buffered: tile `it` uses buffer it & 1, free
-            // once the PV products of tile it - 2 are done
-            const int vb = it & 1;
-            uint8_t *Vt = Vt0 + vb * VB;
-            if (it >= 2 && !ws::wait(&vfree[vb], ((it >> 1) - 1) & 1, vfail)) break;
-            // thread = slot: rebuild the slot's V_hat row (64 channels at a time,
-            // every load issued first) and store it as column `r` of V_hat^T
-            const int r = u;
-            const bool valid = r < ti.nvalid;
-            const int kbs = r >> 6, cs = (r & 63) >> 3, es = (r & 7) * 2;
-#pragma unroll 1
-            for (int kb = 0; kb < KB; ++kb) {
-                uint32_t hv[32];
-                if (valid && a.L == 1) {
-                    rebuild_half_fast<D, BITS>(a, a.vcodes, a.vscales, a.vids, a.vcent, h, ti.chunk, ti.s0 + r, kb, hv);
-                } else if (valid) {
+            // PV_i of tile jp[i]: V tile written, P_i written; PV_1 follows PV_0
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        float vv[8];
-                        rebuild8<D, BITS>(a, a.vcodes, a.vscales, a.vids, a.vcent, h, ti.chunk, ti.s0 + r,
-                                          kb * 64 + c8 * 8, nullptr, vv);
+            for (int i = 0; i < 2; ++i) {
+                const int j = jp[i];
+                if ((i == 0 ? j < n_tiles : j < jp[0]) && umma::mbar_test_wait(&vfull[j & 1], (j >> 1) & 1) &&
+                    umma::mbar_test_wait(&pfull[i], j & 1)) {
+                    umma::tc_fence_after();
+                    const uint32_t vb = va0 + (j & 1) * TB;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) hv[4 * c8 + e] = h2(vv[2 * e], vv[2 * e + 1]);
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32;
+                        umma::mma_f16(tmem + 256 + i * 128, umma::desc_sw128((i ? pa1 : pa0) + aoff),
+                                      umma::desc_sw128_mn(vb + s * 2048, 16384), idO, (j | s) != 0);
                     }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) hv[e] = 0u;
-                }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = kb * 64 + 2 * e;
-                    uint8_t *col = Vt + kbs * (D * 128) + es;
-                    *reinterpret_cast<uint16_t *>(col + j * 128 + ((cs ^ (j & 7)) << 4)) =
-                        static_cast<uint16_t>(hv[e] & 0xffffu);
-                    *reinterpret_cast<uint16_t *>(col + (j + 1) * 128 + ((cs ^ ((j + 1) & 7)) << 4)) =
-                        static_cast<uint16_t>(hv[e] >> 16);
+                    umma::mma_commit(&ofull[i]);
+                    if (i == 1) umma::mma_commit(&vfree[j & 1]);
+                    ++jp[i];
+                    prog = true;
                 }
             }
-            umma::fence_proxy_async_smem();
-            umma::mbar_arrive(&vfull[vb]);
-            if (issuer) {
-                // O_i += P_i V_t once the V tile and P_i are ready
-                if (!ws::wait(&vfull[vb], (it >> 1) & 1, vfail) || !ws::wait(&pfull[0], it & 1, vfail)) break;
-                umma::tc_fence_after();
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32, boff = (s >> 2) * (D * 128) + (s & 3) * 32;
-                    umma::mma_f16(tmem + 256, umma::desc_sw128(p0a + aoff), umma::desc_sw128(v0a + vb * VB + boff), idO, (it | s) != 0);
+            if (prog) {
+                spins = 0;
+            } else if (spins++ == 0) {
+                idle_since = umma::globaltimer_ns();
+            } else if ((spins & 63) == 0) {
+                if (*vfail) break;
+                if (umma::globaltimer_ns() - idle_since > kWaitNs) {
+                    *vfail = 1;
+                    break;
                 }
-                umma::mma_commit(&ofull[0]);
-                last_bar = &ofull[0];
-                if (!ws::wait(&pfull[1], it & 1, vfail)) break;
-                umma::tc_fence_after();
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32, boff = (s >> 2) * (D * 128) + (s & 3) * 32;
-                    umma::mma_f16(tmem + 384, umma::desc_sw128(p1a + aoff), umma::desc_sw128(v0a + vb * VB + boff), idO, (it | s) != 0);
-                }
-                umma::mma_commit(&ofull[1]);
-                umma::mma_commit(&vfree[vb]);
-                last_bar = &vfree[vb];
-                last_par = (it >> 1) & 1;
             }
-            ++it;
         }
-        // on failure, let the MMAs already issued drain before TMEM is released
-        if (issuer && *vfail && last_bar) umma::mbar_wait(last_bar, last_par, kWaitNs);
+        // every MMA issued so far completes before TMEM is released
+        umma::mma_commit(&drain);
+        umma::mbar_wait(&drain, 0, kWaitNs);
     }
+    __syncwarp();
     umma::tc_fence_before();
     __syncthreads();
     if (tid == 0 && *vfail) raise_error(a.err, QVG_ERR_TIMEOUT);
-    if (warp == 12) {
+    if (warp == kIssuerWarp) {
         umma::tc_fence_after();
         umma::tmem_dealloc(tmem, 512);
     }
@@ -631,7 +671,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
 
 template <int D, int BITS, bool TOP1>
 static qvg_status attn_ws_t(const AttnWsArgs &a, cudaStream_t st) {
-    constexpr size_t smem = 3 * (D / 64) * 16384 + 2 * D * 256 + 2 * 32768 + 1024;
+    constexpr size_t smem = 5 * (D / 64) * 16384 + 2 * 32768 + 1024;
     static bool attr = false;
     if (!attr) {
         const cudaError_t e = cudaFuncSetAttribute(k_attention_ws<D, BITS, TOP1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
