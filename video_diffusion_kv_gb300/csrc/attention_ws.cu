@@ -46,9 +46,8 @@ struct AttnWsArgs {
 
 namespace ws {
 
-constexpr int kWarps = 17;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kIssuerWarp = 16;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescale = 8.0f;
 
@@ -65,9 +64,12 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Bounded wait that also gives up as soon as another role has failed.
+// Bounded wait that also gives up as soon as another role has failed.  The
+// global timer (slow to read) is consulted only after 32 unsuccessful
+// try_waits, so a short wait never reads it.
 __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, volatile int *fail) {
-    if (umma::mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 32; ++i)
+        if (umma::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = umma::globaltimer_ns();
     for (;;) {
         for (int i = 0; i < 32; ++i)
@@ -78,6 +80,11 @@ __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, volatile in
             return false;
         }
     }
+}
+
+// Named barrier over the 128 threads of one softmax group (ids 1 and 2).
+__device__ __forceinline__ void group_sync(int i) {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + i) : "memory");
 }
 
 struct TileInfo {
@@ -157,7 +164,7 @@ __device__ __noinline__ void rebuild8(const AttnWsArgs &a, const uint8_t *codes,
 template <int BITS>
 struct HalfData {
     uint4 cw[BITS == 2 ? 1 : 2];  // 64 codes
-    float S[8];                   // scale of each 8-channel block
+    uint32_t s2[4];               // fp16 scales of the 8-channel blocks, two per word
     uint4 cr[8];                  // 64 bf16 centroid channels
 };
 
@@ -172,12 +179,14 @@ __device__ __forceinline__ void load_half(const AttnWsArgs &a, const uint8_t *co
 #pragma unroll
     for (int i = 0; i < HB / 16; ++i) hd.cw[i] = *reinterpret_cast<const uint4 *>(codes + srow * NB + kb * HB + 16 * i);
     if (a.group >= 64) {
-        const float s0 = f16_to_f32(scales[srow * ng + (kb * 64) / a.group]);
+        const uint32_t s0 = scales[srow * ng + (kb * 64) / a.group];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) hd.S[i] = s0;
+        for (int i = 0; i < 4; ++i) hd.s2[i] = s0 | (s0 << 16);
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) hd.S[i] = f16_to_f32(scales[srow * ng + (kb * 64 + 8 * i) / a.group]);
+        for (int i = 0; i < 4; ++i)
+            hd.s2[i] = static_cast<uint32_t>(scales[srow * ng + (kb * 64 + 16 * i) / a.group]) |
+                       (static_cast<uint32_t>(scales[srow * ng + (kb * 64 + 16 * i + 8) / a.group]) << 16);
     }
     if (a.C > 0) {
         const uint16_t *row = cent + ((static_cast<size_t>(h) * a.max_chunks + chunk) * a.C + id) * D + kb * 64;
@@ -189,28 +198,10 @@ __device__ __forceinline__ void load_half(const AttnWsArgs &a, const uint8_t *co
     }
 }
 
-// Decodes the half and stores it as the eight swizzled 16-byte chunks of the
-// slot's 128-byte line `dst` (chunk c at position c ^ (r % 8)), one chunk as
-// soon as its four words are ready.
-template <int BITS>
-__device__ __forceinline__ void decode_store_half(const HalfData<BITS> &hd, uint8_t *dst, int r) {
-    const uint32_t *cb = reinterpret_cast<const uint32_t *>(hd.cw);
+// Zeroes one slot's 128-byte line of a 64-channel block (padding slots).
+__device__ __forceinline__ void zero_line(uint8_t *dst) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t bits = static_cast<uint32_t>((cb[(8 * i * BITS) / 32] >> ((8 * i * BITS) % 32)) &
-                                                    ((1ull << (8 * BITS)) - 1ull));
-        const uint32_t c4[4] = {hd.cr[i].x, hd.cr[i].y, hd.cr[i].z, hd.cr[i].w};
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int q0 = static_cast<int>((bits >> (2 * e * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
-            const int q1 = static_cast<int>((bits >> ((2 * e + 1) * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
-            const float v0 = fmaf(hd.S[i], static_cast<float>(q0), __uint_as_float(c4[e] << 16));
-            const float v1 = fmaf(hd.S[i], static_cast<float>(q1), __uint_as_float(c4[e] & 0xffff0000u));
-            w[e] = h2(v0, v1);
-        }
-        *reinterpret_cast<uint4 *>(dst + ((i ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4 *>(dst + (c8 << 4)) = make_uint4(0, 0, 0, 0);
 }
 
 // Packed fp32 pairs (Blackwell f32x2 arithmetic).
@@ -231,6 +222,43 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
+}
+
+// Decodes the half and stores it as the eight swizzled 16-byte chunks of the
+// slot's 128-byte line `dst` (chunk c at position c ^ (r % 8)), one chunk as
+// soon as its four words are ready.  Codes become floats without a
+// conversion instruction: OR-ing a B-bit code c into the mantissa of 2^23
+// (0x4B000000) gives the float 2^23 + c exactly, or 2^23 + c 2^B for the
+// odd code of a pair left at bit B; one packed FMA with (1, 2^-B) and the
+// matching offsets gives q = c - 2^(B-1) exactly (every intermediate is an
+// integer below 2^24), and K_hat = fma(S, q, c_bf16) has the single
+// rounding of the plain fp32 expression.
+template <int BITS>
+__device__ __forceinline__ void decode_store_half(const HalfData<BITS> &hd, uint8_t *dst, int r) {
+    constexpr uint32_t M = (1u << BITS) - 1u, MAGIC = 0x4B000000u;
+    constexpr float E23 = 8388608.0f, HALF = static_cast<float>(1 << (BITS - 1));
+    const uint64_t P2 = pk2(1.0f, 1.0f / static_cast<float>(1 << BITS));
+    const uint64_t N2 = pk2(-(E23 + HALF), -(E23 / static_cast<float>(1 << BITS) + HALF));
+    const uint32_t *cb = reinterpret_cast<const uint32_t *>(hd.cw);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t blk = cb[(8 * i * BITS) / 32] >> ((8 * i * BITS) % 32);
+        const float S = f16_to_f32(static_cast<uint16_t>(hd.s2[i >> 1] >> (16 * (i & 1))));
+        const uint64_t S2 = pk2(S, S);
+        const uint32_t c4[4] = {hd.cr[i].x, hd.cr[i].y, hd.cr[i].z, hd.cr[i].w};
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t x = blk >> (2 * e * BITS);
+            const uint64_t mag = pk2(__uint_as_float((x & M) | MAGIC), __uint_as_float((x & (M << BITS)) | MAGIC));
+            const uint64_t q2 = fma2(mag, P2, N2);
+            const uint64_t v2 = fma2(S2, q2, pk2(__uint_as_float(c4[e] << 16), __uint_as_float(c4[e] & 0xffff0000u)));
+            float v0, v1;
+            up2(v2, v0, v1);
+            w[e] = h2(v0, v1);
+        }
+        *reinterpret_cast<uint4 *>(dst + ((i ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
 }
 
 // Adds the two fp16 halves of a packed pair to two fp32 sums (sm_100-family
@@ -286,48 +314,65 @@ struct Producer {
     bool psac;
 };
 
-// One stage, no PSAC.  A tile's first-half loads are issued before the wait
-// for its buffer; the next tile's table entry and cluster id are loaded one
-// tile ahead (slot (t + 1) * QVG_TILE + r < n_slots <= capacity: in bounds).
+// One stage, no PSAC.  The loads of one 64-channel half are always in
+// flight while the previous half is decoded (two register sets, A for the
+// first half of a tile and B for the second when D = 128); table entries and
+// cluster ids run two tiles ahead (slot t * QVG_TILE + r < n_slots <=
+// capacity for every tile t: in bounds).
 template <int D, int BITS>
 __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer &pr, int h, int r, int n_tiles,
                                              volatile int *vfail) {
     constexpr int KB = D / 64, TB = KB * 16384;
     const size_t id_row = static_cast<size_t>(h) * a.cap + r;
-    TileInfo ti{};
-    int id = 0;
+    TileInfo ti0{}, ti1{};
+    int id0 = 0, id1 = 0;
     if (n_tiles > 0) {
-        ti = tile_info(a, 0);
-        if (a.C > 0) id = pr.ids[id_row];
+        ti0 = tile_info(a, 0);
+        if (a.C > 0) id0 = pr.ids[id_row];
     }
+    if (n_tiles > 1) {
+        ti1 = tile_info(a, 1);
+        if (a.C > 0) id1 = pr.ids[id_row + QVG_TILE];
+    }
+    HalfData<BITS> A, B;
+    if (n_tiles > 0 && r < ti0.nvalid) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti0.chunk, ti0.s0 + r, id0, 0, A);
     for (int t = 0; t < n_tiles; ++t) {
         const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
         uint8_t *T = pr.buf0 + b * TB + r * 128;
-        TileInfo tn{};
-        int idn = 0;
-        if (t + 1 < n_tiles) {
-            tn = tile_info(a, t + 1);
-            if (a.C > 0) idn = pr.ids[id_row + static_cast<size_t>(t + 1) * QVG_TILE];
+        TileInfo ti2{};
+        int id2 = 0;
+        if (t + 2 < n_tiles) {
+            ti2 = tile_info(a, t + 2);
+            if (a.C > 0) id2 = pr.ids[id_row + static_cast<size_t>(t + 2) * QVG_TILE];
         }
-        const bool valid = r < ti.nvalid;
-        HalfData<BITS> hd;
-        if (valid) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti.chunk, ti.s0 + r, id, 0, hd);
-        if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb) {
-            if (valid) {
-                decode_store_half<BITS>(hd, T + kb * 16384, r);
-            } else {
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4 *>(T + kb * 16384 + (c8 << 4)) = make_uint4(0, 0, 0, 0);
-            }
-            if (valid && kb + 1 < KB)
-                load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti.chunk, ti.s0 + r, id, kb + 1, hd);
+        const bool valid = r < ti0.nvalid, valid1 = t + 1 < n_tiles && r < ti1.nvalid;
+        if constexpr (KB == 2) {
+            if (valid) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti0.chunk, ti0.s0 + r, id0, 1, B);
+            if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
+            if (valid)
+                decode_store_half<BITS>(A, T, r);
+            else
+                zero_line(T);
+            if (valid1) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti1.chunk, ti1.s0 + r, id1, 0, A);
+            if (valid)
+                decode_store_half<BITS>(B, T + 16384, r);
+            else
+                zero_line(T + 16384);
+        } else {
+            B = A;
+            if (valid1) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti1.chunk, ti1.s0 + r, id1, 0, A);
+            if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
+            if (valid)
+                decode_store_half<BITS>(B, T, r);
+            else
+                zero_line(T);
         }
         umma::fence_proxy_async_smem();
         umma::mbar_arrive(&pr.full[b]);
-        ti = tn;
-        id = idn;
+        ti0 = ti1;
+        id0 = id1;
+        ti1 = ti2;
+        id1 = id2;
     }
 }
 
@@ -374,24 +419,25 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 
 }  // namespace ws
 
-// Warp roles (17 warps):
-//   0-3, 4-7   softmax + epilogue of query tile 0 / 1 (thread = query row)
+// Warp roles (16 warps):
+//   0-3, 4-7   softmax + epilogue of query tile i = 0 / 1 (thread = query row);
+//              lane 0 of warp 4i issues the tcgen05.mma of tile i (S_i and
+//              PV_i), and warp 0 owns the TMEM allocation
 //   8-11       K producers: rebuild the 128-slot K_hat tile (thread = slot)
 //   12-15      V producers: rebuild V_hat into one of two buffers (thread = slot)
-//   16         owns the TMEM allocation; its lane 0 issues every tcgen05.mma
 // Both producers write a tile as [64-channel block][slot][64 channels] with
 // the 128-byte swizzle: K-major for the S = Q K_hat^T product (N = slots,
 // K = channels) and, read through an MN-major descriptor, the B operand of
 // O += P V_hat (N = channels, K = slots), so V needs no transpose.
-// Barriers (phase = tile index, per buffer for V):
-//   kfull/vfull  producers -> issuer    tile written
-//   kfree/vfree  MMA commit -> producer tile consumed (after S_1 / after PV_1)
-//   sfull[i]     MMA commit -> softmax  S_i ready
-//   sfree[i]     softmax -> issuer      S_i read out (TMEM columns reusable)
-//   pfull[i]     softmax -> issuer      P_i in shared memory, O_i rescaled
-//   ofull[i]     MMA commit -> softmax  PV_i done (P_i free, O_i settled)
-// The issuer polls and issues whatever is ready in the order S_0, S_1, PV_0,
-// PV_1 of each tile, so S of the next tile overlaps the softmax of this one.
+// Per cache tile t, group i: once all its threads hold the last columns of
+// S_i(t) (named barrier), S_i(t + 1) is issued if K(t + 1) is already
+// written; once P_i(t) is in shared memory (named barrier), PV_i(t) is issued
+// after V(t) is written, then S_i(t + 1) if it was deferred.
+// mbarriers (phase = tile index, per buffer for V):
+//   kfull/vfull  producers -> issuers   tile written (one arrival per slot)
+//   kfree/vfree  MMA commits -> producer tile consumed (S_0 and S_1 / PV_0 and PV_1)
+//   sfull[i]     MMA commit -> group i   S_i ready
+//   ofull[i]     MMA commit -> group i   PV_i done (P_i free, O_i settled)
 template <int D, int BITS, bool TOP1>
 __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) {
     using namespace ws;
@@ -401,7 +447,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
     uint8_t *Q0 = sm, *Q1 = Q0 + TB, *Kt = Q1 + TB, *Vt0 = Kt + TB, *P0 = Vt0 + 2 * TB, *P1 = P0 + PB;
-    __shared__ uint64_t kfull, kfree, vfull[2], vfree[2], sfull[2], sfree[2], pfull[2], ofull[2], drain;
+    __shared__ uint64_t kfull, kfree, vfull[2], vfree[2], sfull[2], ofull[2], drain;
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
 
@@ -423,20 +469,18 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         }
         *reinterpret_cast<uint4 *>((rr < 128 ? Q0 : Q1) + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
-    if (warp == kIssuerWarp) {
+    if (warp == 0) {
         umma::tmem_alloc(&tmem_base, 512);
         umma::tmem_relinquish();
     }
     if (tid == 0) {
         umma::mbar_init(&kfull, 128);
-        umma::mbar_init(&kfree, 1);
-        umma::mbar_init(&drain, 1);
+        umma::mbar_init(&kfree, 2);
+        umma::mbar_init(&drain, 2);
         for (int i = 0; i < 2; ++i) {
             umma::mbar_init(&vfull[i], 128);
-            umma::mbar_init(&vfree[i], 1);
+            umma::mbar_init(&vfree[i], 2);
             umma::mbar_init(&sfull[i], 1);
-            umma::mbar_init(&sfree[i], 128);
-            umma::mbar_init(&pfull[i], 128);
             umma::mbar_init(&ofull[i], 1);
         }
         umma::fence_barrier_init();
@@ -452,104 +496,171 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     if (warp < 8) {
         // ------------------------------------------------ softmax of tile i
         const int i = warp >> 2, r = tid & 127;
+        const bool issuer = (warp & 3) == 0 && lane == 0;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + i * 128 + lane_off, tO = tmem + 256 + i * 128 + lane_off;
-        uint8_t *Prow = (i ? P1 : P0) + r * 128;
-        float m_used = -INFINITY, l_sum = 0.0f, best = -INFINITY;
-        int best_slot = 0, t = 0;
-        for (; t < n_tiles; ++t) {
-            const TileInfo ti = tile_info(a, t);
-            if (!ws::wait(&sfull[i], t & 1, vfail)) break;
+        uint8_t *Pi = i ? P1 : P0;
+        uint8_t *Prow = Pi + r * 128;
+        const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16_bmn(128, D, 0);
+        const uint32_t qa = umma::smem_u32(i ? Q1 : Q0), pa = umma::smem_u32(Pi);
+        const uint32_t ka = umma::smem_u32(Kt), va0 = umma::smem_u32(Vt0);
+        // S_i = Q_i K_t^T into TMEM columns [128 i, 128 i + 128)
+        // (issue loops are kept rolled so that their descriptors are not
+        // hoisted into registers held across the whole tile loop; a
+        // descriptor's low 14 bits are the shared address / 16, which the
+        // offsets below never carry out of)
+        auto issue_S = [&]() {
             umma::tc_fence_after();
-            // row maximum of the raw logits (the scale is positive), scaled
-            // once; the top-1 variant keeps one in-order chain so that ties
-            // resolve to the lowest slot
-            float rmax = -INFINITY;
-            int targ = 0;
-            if constexpr (TOP1) {
-#pragma unroll
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    uint32_t v[32];
-                    umma::tmem_ld32(tS + c0, v);
-                    umma::tmem_ld_wait_regs(v);
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float x = c0 + k < ti.nvalid ? __uint_as_float(v[k]) : -INFINITY;
-                        if (x > rmax) { rmax = x; targ = c0 + k; }
-                    }
-                }
-            } else {
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    uint32_t v[32];
-                    umma::tmem_ld32(tS + c0, v);
-                    umma::tmem_ld_wait_regs(v);
-                    if (c0 + 32 <= ti.nvalid) {
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            m4[k & 3] = max3(m4[k & 3], __uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            if (c0 + k < ti.nvalid) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(v[k]));
-                    }
-                }
-                rmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            const uint64_t dq = umma::desc_sw128(qa), dk = umma::desc_sw128(ka);
+#pragma unroll 1
+            for (int s = 0; s < D / 16; ++s) {
+                const uint32_t off16 = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+                umma::mma_f16(tmem + i * 128, dq + off16, dk + off16, idS, s != 0);
             }
-            const float tmax = rmax * a.scale_log2;
-            if constexpr (TOP1) {
-                if (tmax > best) {
-                    best = tmax;
-                    best_slot = ti.s0 + targ;
-                }
-            }
+            umma::mma_commit(&sfull[i]);
+            umma::mma_commit(&kfree);
+        };
+        // A group never leaves its tile loop early: the named barriers below
+        // are executed by all four warps on every tile, and after a failed
+        // wait a warp only stops doing work (live is warp-uniform).
+        bool ok_issue = true;
+        if (issuer && n_tiles > 0) {
+            if (ws::wait(&kfull, 0, vfail))
+                issue_S();
+            else
+                ok_issue = false;
+        }
+        bool live = __all_sync(0xffffffffu, ok_issue);
+        float m_used = -INFINITY, l_sum = 0.0f, best = -INFINITY;
+        int best_slot = 0;
+        for (int t = 0; t < n_tiles; ++t) {
+            const TileInfo ti = tile_info(a, t);
+            if (live) live = __all_sync(0xffffffffu, ws::wait(&sfull[i], t & 1, vfail));
             float corr = 1.0f;
-            bool rescale = false;
-            if (tmax > m_used + kRescale) {
-                corr = ex2(m_used - tmax);
-                rescale = t > 0;
-                m_used = tmax;
-            }
-            if (t > 0) {  // PV_i of the previous tile done: P_i is free and O_i settled
-                if (!ws::wait(&ofull[i], (t - 1) & 1, vfail)) break;
+            if (live) {
                 umma::tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
-                    const float f = rescale ? corr : 1.0f;
+                // row maximum of the raw logits (the scale is positive), scaled
+                // once; the top-1 variant keeps one in-order chain so that ties
+                // resolve to the lowest slot
+                float rmax = -INFINITY;
+                int targ = 0;
+                if constexpr (TOP1) {
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = 0; c0 < 128; c0 += 32) {
                         uint32_t v[32];
-                        umma::tmem_ld32(tO + c0, v);
+                        umma::tmem_ld32(tS + c0, v);
                         umma::tmem_ld_wait_regs(v);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
-                        umma::tmem_st32(tO + c0, v);
+                        for (int k = 0; k < 32; ++k) {
+                            const float x = c0 + k < ti.nvalid ? __uint_as_float(v[k]) : -INFINITY;
+                            if (x > rmax) { rmax = x; targ = c0 + k; }
+                        }
                     }
-                    umma::tmem_st_wait();
+                } else {
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int c0 = 0; c0 < 128; c0 += 32) {
+                        uint32_t v[32];
+                        umma::tmem_ld32(tS + c0, v);
+                        umma::tmem_ld_wait_regs(v);
+                        if (c0 + 32 <= ti.nvalid) {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                m4[k & 3] = max3(m4[k & 3], __uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if (c0 + k < ti.nvalid) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(v[k]));
+                        }
+                    }
+                    rmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                }
+                const float tmax = rmax * a.scale_log2;
+                if constexpr (TOP1) {
+                    if (tmax > best) {
+                        best = tmax;
+                        best_slot = ti.s0 + targ;
+                    }
+                }
+                bool rescale = false;
+                if (tmax > m_used + kRescale) {
+                    corr = ex2(m_used - tmax);
+                    rescale = t > 0;
+                    m_used = tmax;
+                }
+                if (t > 0) {  // PV_i of the previous tile done: P_i is free and O_i settled
+                    live = __all_sync(0xffffffffu, ws::wait(&ofull[i], (t - 1) & 1, vfail));
+                    if (live) {
+                        umma::tc_fence_after();
+                        if (__any_sync(0xffffffffu, rescale)) {
+                            const float f = rescale ? corr : 1.0f;
+#pragma unroll
+                            for (int c0 = 0; c0 < D; c0 += 32) {
+                                uint32_t v[32];
+                                umma::tmem_ld32(tO + c0, v);
+                                umma::tmem_ld_wait_regs(v);
+#pragma unroll
+                                for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
+                                umma::tmem_st32(tO + c0, v);
+                            }
+                            umma::tmem_st_wait();
+                        }
+                    }
                 }
             }
-            // P_i: the next 32 columns load while the current 32 are processed;
-            // S_i is released as soon as its last columns are in registers
             const uint64_t sl2 = pk2(a.scale_log2, a.scale_log2), nm2 = pk2(-m_used, -m_used);
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const bool more = t + 1 < n_tiles;
+            bool s_next = false;
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
                 uint32_t v[32];
-                umma::tmem_ld32(tS + c0, v);
-                umma::tmem_ld_wait_regs(v);
-                if (c0 == 96) {
-                    umma::tc_fence_before();
-                    umma::mbar_arrive(&sfree[i]);
+                if (live) {
+                    umma::tmem_ld32(tS + c0, v);
+                    umma::tmem_ld_wait_regs(v);
                 }
-                softmax_chunk(v, c0, ti.nvalid, sl2, nm2, Prow, r, acc);
+                if (c0 == 96) {
+                    // every thread of the group holds its last S_i columns:
+                    // S_i(t + 1) may overwrite them if K(t + 1) is ready
+                    umma::tc_fence_before();
+                    group_sync(i);
+                    if (issuer && live && more && umma::mbar_test_wait(&kfull, (t + 1) & 1)) {
+                        issue_S();
+                        s_next = true;
+                    }
+                }
+                if (live) softmax_chunk(v, c0, ti.nvalid, sl2, nm2, Prow, r, acc);
             }
             l_sum = l_sum * corr + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+            // P_i(t) complete in shared memory (and O_i rescaled): PV_i(t)
             umma::fence_proxy_async_smem();
             umma::tc_fence_before();
-            umma::mbar_arrive(&pfull[i]);
+            group_sync(i);
+            if (issuer && live) {
+                if (ws::wait(&vfull[t & 1], (t >> 1) & 1, vfail)) {
+                    umma::tc_fence_after();
+                    const uint64_t dp = umma::desc_sw128(pa), dv = umma::desc_sw128_mn(va0 + (t & 1) * TB, 16384);
+#pragma unroll 1
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t aoff16 = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+                        umma::mma_f16(tmem + 256 + i * 128, dp + aoff16, dv + ((s * 2048) >> 4), idO, (t | s) != 0);
+                    }
+                    umma::mma_commit(&ofull[i]);
+                    umma::mma_commit(&vfree[t & 1]);
+                    if (more && !s_next) {
+                        if (ws::wait(&kfull, (t + 1) & 1, vfail))
+                            issue_S();
+                        else
+                            ok_issue = false;
+                    }
+                } else {
+                    ok_issue = false;
+                }
+            }
+            live = live && __all_sync(0xffffffffu, ok_issue);
         }
         // epilogue: O_i / l
-        bool ok = !*vfail && t == n_tiles && n_tiles > 0 && ws::wait(&ofull[i], (t - 1) & 1, vfail);
+        bool ok = live && !*vfail && n_tiles > 0 && ws::wait(&ofull[i], (n_tiles - 1) & 1, vfail);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             umma::tc_fence_after();
@@ -586,6 +697,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 if constexpr (TOP1) a.top1[static_cast<size_t>(hq) * a.Nq + qi] = best_slot;
             }
         }
+        // every MMA this group issued completes before TMEM is released
+        if (issuer) {
+            umma::mma_commit(&drain);
+            umma::mbar_wait(&drain, 0, kWaitNs);
+        }
     } else if (warp < 16) {
         // ------------------------------------------------ K / V producers (thread = slot)
         const bool isv = warp >= 12;
@@ -596,74 +712,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             produce_fast<D, BITS>(a, pr, h, tid & 127, n_tiles, vfail);
         else
             produce_general<D, BITS>(a, pr, h, tid & 127, n_tiles, vfail);
-    } else if (lane == 0) {
-        // ------------------------------------------------ MMA issuer
-        const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16_bmn(128, D, 0);
-        const uint32_t qa0 = umma::smem_u32(Q0), qa1 = umma::smem_u32(Q1), pa0 = umma::smem_u32(P0),
-                       pa1 = umma::smem_u32(P1), ka = umma::smem_u32(Kt), va0 = umma::smem_u32(Vt0);
-        int js = 0, half = 0, jp[2] = {0, 0}, spins = 0;
-        uint64_t idle_since = 0;
-        while (jp[1] < n_tiles) {
-            bool prog = false;
-            // S_half of tile js: K tile written, S_half of tile js - 1 read out
-            if (js < n_tiles && umma::mbar_test_wait(&kfull, js & 1) &&
-                (js == 0 || umma::mbar_test_wait(&sfree[half], (js - 1) & 1))) {
-                umma::tc_fence_after();
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-                    umma::mma_f16(tmem + half * 128, umma::desc_sw128((half ? qa1 : qa0) + off),
-                                  umma::desc_sw128(ka + off), idS, s != 0);
-                }
-                umma::mma_commit(&sfull[half]);
-                if (half == 1) {
-                    umma::mma_commit(&kfree);
-                    ++js;
-                }
-                half ^= 1;
-                prog = true;
-            }
-            // PV_i of tile jp[i]: V tile written, P_i written; PV_1 follows PV_0
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int j = jp[i];
-                if ((i == 0 ? j < n_tiles : j < jp[0]) && umma::mbar_test_wait(&vfull[j & 1], (j >> 1) & 1) &&
-                    umma::mbar_test_wait(&pfull[i], j & 1)) {
-                    umma::tc_fence_after();
-                    const uint32_t vb = va0 + (j & 1) * TB;
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t aoff = (s >> 2) * 16384 + (s & 3) * 32;
-                        umma::mma_f16(tmem + 256 + i * 128, umma::desc_sw128((i ? pa1 : pa0) + aoff),
-                                      umma::desc_sw128_mn(vb + s * 2048, 16384), idO, (j | s) != 0);
-                    }
-                    umma::mma_commit(&ofull[i]);
-                    if (i == 1) umma::mma_commit(&vfree[j & 1]);
-                    ++jp[i];
-                    prog = true;
-                }
-            }
-            if (prog) {
-                spins = 0;
-            } else if (spins++ == 0) {
-                idle_since = umma::globaltimer_ns();
-            } else if ((spins & 63) == 0) {
-                if (*vfail) break;
-                if (umma::globaltimer_ns() - idle_since > kWaitNs) {
-                    *vfail = 1;
-                    break;
-                }
-            }
-        }
-        // every MMA issued so far completes before TMEM is released
-        umma::mma_commit(&drain);
-        umma::mbar_wait(&drain, 0, kWaitNs);
     }
     __syncwarp();
     umma::tc_fence_before();
     __syncthreads();
     if (tid == 0 && *vfail) raise_error(a.err, QVG_ERR_TIMEOUT);
-    if (warp == kIssuerWarp) {
+    if (warp == 0) {
         umma::tc_fence_after();
         umma::tmem_dealloc(tmem, 512);
     }

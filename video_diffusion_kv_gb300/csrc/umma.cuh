@@ -75,8 +75,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Wait until the phase with the given parity has completed, at most
 // `limit_ns` nanoseconds.  Returns false when the bound was reached.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    for (int i = 0; i < 32; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();  // slow to read: only for long waits
     for (;;) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
