@@ -67,6 +67,7 @@ qvg_status check_cache(const qvg_params *p, const qvg_cache *c) {
 struct CompressWs {
     int32_t *ids;
     float *cnorm;
+    float *xnorm;
     float *delta;
     uint16_t *gbf;
     size_t bytes;
@@ -82,6 +83,7 @@ CompressWs carve_compress(const qvg_params *p, int N, int H, int d, char *base) 
     };
     w.ids = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * static_cast<size_t>(H) * N));
     w.cnorm = reinterpret_cast<float *>(take(sizeof(float) * static_cast<size_t>(H) * std::max(p->C, 1)));
+    w.xnorm = reinterpret_cast<float *>(take(sizeof(float) * static_cast<size_t>(H) * N));
     const bool need_delta = p->L > 1 || (p->flags & QVG_PSAC);
     w.delta = need_delta ? reinterpret_cast<float *>(take(sizeof(float) * static_cast<size_t>(N) * H * d)) : nullptr;
     w.gbf = p->L > 1 ? reinterpret_cast<uint16_t *>(take(sizeof(uint16_t) * static_cast<size_t>(N) * H * d)) : nullptr;
@@ -188,13 +190,18 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
             } else if ((s = launch_centroid_norms(cent, cent_hs, H, C, d, w, ws.cnorm, st)) != QVG_OK) {
                 return s;
             }
+            // the first assignment of the stage also records ||x||_w^2 per token
             for (int it = 0; it < p->iters; ++it) {
-                if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.ids, st)) != QVG_OK) return s;
+                if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.xnorm, it == 0,
+                                              ws.ids, st)) != QVG_OK)
+                    return s;
                 if ((s = launch_kmeans_update(xin, f32, N, H, d, ws.ids, cent, cent_hs, Ce, C, w, ws.cnorm, st)) !=
                     QVG_OK)
                     return s;
             }
-            if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.ids, st)) != QVG_OK) return s;
+            if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.xnorm, p->iters == 0,
+                                          ws.ids, st)) != QVG_OK)
+                return s;
         }
         const bool last = l == L - 1;
         const size_t lrow = static_cast<size_t>(l) * H * cap + slot0;

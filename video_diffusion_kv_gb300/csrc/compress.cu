@@ -104,46 +104,103 @@ __global__ void k_centroid_norms(const uint16_t *__restrict__ cent, size_t hs, i
 //   exact) or, with QSAC weights, the weighted centroids w*c as a bf16 pair
 //   hi + lo (|w c - hi - lo| <= 2^-18 |w c|),
 // accumulated in fp32 in tensor memory by tcgen05.mma (M=128, N=Np = Ce
-// rounded up to 16, K=16 per instruction).  Tensor memory holds two
-// accumulators, so the epilogue of tile t (thread r owns token r: argmin_c
-// ||c||_w^2 - 2 acc_c over the TMEM row) overlaps the MMA of tile t+1 and
-// the cp.async loads of tile t+2.  The GEMM form cancels large outlier
-// products, so the two best candidates are re-scored with the direct
-// sum_j w_j (x_j - c_j)^2 (fp32, ascending j); ties go to the lower index.
+// rounded up to 16, K=16 per instruction).  Token tiles arrive by cp.async
+// into NA buffers (completion counted on an mbarrier per buffer), and the MMA
+// of tile k+1 runs while the epilogue of tile k reads the other accumulator.
+//
+// Epilogue, thread = token row (the two warp groups take alternating
+// 32-column chunks): score s_c = ||c||_w^2 - 2 acc_c in fp32; four
+// independent (best, second) chains per thread, merged in (score, index)
+// order so that ties go to the lower cluster.
+//
+// Exactness: the ranking must be that of d_c = sum_j w_j (x_j - c_j)^2 =
+// ||x||_w^2 + s_c.  The tensor-core sum (<= 2^-16 sum w|x c|, products exact),
+// the hi/lo split (2^-18), the fp32 norm (2^-16 ||c||^2) and the FMA bound
+// the score error, with sum w|x c| <= ||x||_w ||c||_w <= (||x||_w^2 +
+// ||c||_w^2) / 2, by
+//   E <= 2^-14 (||x||_w^2 + max_c ||c||_w^2).
+// When the two best scores differ by more than tau (||x||_w^2 +
+// max||c||_w^2) with tau = 2^-11 (= 8 E), the best score is the exact argmin
+// (no tie possible).  Otherwise the two candidates are re-scored with the
+// direct sum: the 32 lanes of the row's warp each take D/32 consecutive
+// channels (fp32, ascending), the partial sums are added by an xor
+// butterfly, and the smaller distance wins (ties to the lower index).
+// ||x||_w^2 is computed by the first assignment of a stage (xmode 1) and
+// stored in xnorm for the later ones.
 // Every wait is bounded; on expiry the CTA records QVG_ERR_TIMEOUT.
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 
 constexpr int kAssignThreads = 256;
+constexpr float kAssignTau = 1.0f / 2048.0f;
+
+// (score, index) order: lower score, then lower index
+__device__ __forceinline__ bool sc_less(float a, int ia, float b, int ib) { return a < b || (a == b && ia < ib); }
+// merge the ordered pair (ov, oi) <= (pv, pi) into (best, second)
+__device__ __forceinline__ void merge2(float &bv, int &bi, float &sv, int &si, float ov, int oi, float pv, int pi) {
+    if (sc_less(ov, oi, bv, bi)) {
+        if (sc_less(bv, bi, pv, pi)) {
+            sv = bv;
+            si = bi;
+        } else {
+            sv = pv;
+            si = pi;
+        }
+        bv = ov;
+        bi = oi;
+    } else if (sc_less(ov, oi, sv, si)) {
+        sv = ov;
+        si = oi;
+    }
+}
 
 template <int D, int P>
-__global__ void __launch_bounds__(kAssignThreads) k_kmeans_assign_tc(const uint16_t *__restrict__ g, int N, int H,
-                                                         const uint16_t *__restrict__ cent, size_t hs,
-                                                         int Ce, int Np, const float *__restrict__ cnorm,
-                                                         int C, const float *__restrict__ w,
-                                                         int32_t *__restrict__ ids, int *err) {
+__global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const uint16_t *__restrict__ g, int N, int H,
+                                                            const uint16_t *__restrict__ cent, size_t hs,
+                                                            int Ce, int Np, const float *__restrict__ cnorm,
+                                                            int C, const float *__restrict__ w,
+                                                            float *__restrict__ xnorm, int xmode,
+                                                            int32_t *__restrict__ ids, int *err) {
     constexpr int KB = D / 64;                       // 64-element K blocks
     constexpr int AB = KB * 128 * 128;               // one token tile
+    constexpr int NA = P == 1 ? 3 : 2;               // token tile buffers
+    constexpr int E = D / 32;                        // channels per lane in the re-scoring
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     // swizzle atoms need a 1024-byte aligned base (the launch adds 1 KB slack)
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
-    uint8_t *As = sm;                                // 2 x KB x [128 rows x 128 B]
-    uint8_t *Bs = As + 2 * AB;                       // P x KB x [Np rows x 128 B]
-    float *cn = reinterpret_cast<float *>(Bs + static_cast<size_t>(P) * KB * Np * 128);
-    __shared__ uint64_t bar[2];
+    uint8_t *As = sm;                                // NA x KB x [128 rows x 128 B]
+    uint8_t *Bs = As + NA * AB;                      // P x KB x [Np rows x 128 B]
+    float *cn = reinterpret_cast<float *>(Bs + static_cast<size_t>(P) * KB * Np * 128);  // Np + 32
+    __shared__ uint64_t bar_mma[2], bar_a[NA], bar_drain;
     __shared__ uint32_t tmem_base;
-    __shared__ float xb[128][2];     // warp group 1's best / second score per row
-    __shared__ int xi[128][2];       // ... and their clusters
-    __shared__ float xd[128];        // group 1's exact distance of the second candidate
+    __shared__ float xs[128][2];     // warp group 1's two best scores per row
+    __shared__ int xk[128][2];       // ... and their clusters
+    __shared__ float red[kAssignThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = warp >> 2;       // warp group: 32-column chunks grp, grp + 2, ...
     const int h = blockIdx.y;
     const int n_tiles = ceil_div(N, 128);
     const int t0 = blockIdx.x, tstep = gridDim.x;
+    const int my_tiles = t0 < n_tiles ? ceil_div(n_tiles - t0, tstep) : 0;
     const uint32_t ncols = Np <= 32 ? 32 : (Np <= 64 ? 64 : (Np <= 128 ? 128 : 256));
+    const uint16_t *ch = cent + static_cast<size_t>(h) * hs;
 
-    auto load_tile = [&](int t, int buf) {
-        const int n0 = t * 128;
-        uint8_t *dst = As + buf * AB;
+    if (warp == 0) {
+        umma::tmem_alloc(&tmem_base, 2 * ncols);
+        umma::tmem_relinquish();
+    }
+    if (tid == 0) {
+        umma::mbar_init(&bar_mma[0], 1);
+        umma::mbar_init(&bar_mma[1], 1);
+        umma::mbar_init(&bar_drain, 1);
+        for (int i = 0; i < NA; ++i) umma::mbar_init(&bar_a[i], kAssignThreads);
+        umma::fence_barrier_init();
+    }
+    __syncthreads();
+
+    // token tile k -> buffer k % NA; each thread's copies arrive on bar_a once done
+    auto load_tile = [&](int k) {
+        const int n0 = (t0 + k * tstep) * 128;
+        uint8_t *dst = As + (k % NA) * AB;
 #pragma unroll 4
         for (int i = tid; i < 128 * (D / 8); i += kAssignThreads) {
             const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
@@ -151,10 +208,10 @@ __global__ void __launch_bounds__(kAssignThreads) k_kmeans_assign_tc(const uint1
             umma::cp_async16(dst + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4),
                              g + (static_cast<size_t>(in ? n0 + r : 0) * H + h) * D + ci * 8, in);
         }
+        umma::cp_async_arrive_noinc(&bar_a[k % NA]);
     };
 
     // centroids (or weighted hi/lo pair) -> swizzled K-major bf16, once
-    const uint16_t *ch = cent + static_cast<size_t>(h) * hs;
     if constexpr (P == 1) {
 #pragma unroll 4
         for (int i = tid; i < Np * (D / 8); i += kAssignThreads) {
@@ -163,6 +220,7 @@ __global__ void __launch_bounds__(kAssignThreads) k_kmeans_assign_tc(const uint1
             umma::cp_async16(Bs + static_cast<size_t>(kb) * Np * 128 + r * 128 + ((c ^ (r & 7)) << 4),
                              ch + static_cast<size_t>(in ? r : 0) * D + ci * 8, in);
         }
+        umma::cp_async_commit();
     } else {
         for (int i = tid; i < Np * (D / 8); i += kAssignThreads) {
             const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
@@ -194,175 +252,209 @@ __global__ void __launch_bounds__(kAssignThreads) k_kmeans_assign_tc(const uint1
             *reinterpret_cast<uint4 *>(Bs + static_cast<size_t>(KB) * Np * 128 + off) = v2;
         }
     }
-    if (t0 < n_tiles) load_tile(t0, 0);
-    // padded columns score +inf, so no column needs a bounds test
-    for (int i = tid; i < Np; i += kAssignThreads) cn[i] = i < Ce ? cnorm[h * C + i] : INFINITY;
-    umma::cp_async_wait_all();
+    for (int k = 0; k < NA - 1 && k < my_tiles; ++k) load_tile(k);
+    // padded columns score +inf; the largest real norm bounds the score error
+    float cm = 0.0f;
+    for (int i = tid; i < Np + 32; i += kAssignThreads) {
+        const float v = i < Ce ? cnorm[h * C + i] : INFINITY;
+        cn[i] = v;
+        if (i < Ce) cm = fmaxf(cm, v);
+    }
+    for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+    if (lane == 0) red[warp] = cm;
+    // the centroid copies form the only committed group; the token tiles are
+    // tracked by their mbarriers instead
+    umma::cp_async_wait_group<0>();
     umma::fence_proxy_async_smem();
-    if (warp == 0) {
-        umma::tmem_alloc(&tmem_base, 2 * ncols);
-        umma::tmem_relinquish();
-    }
-    if (tid == 0) {
-        umma::mbar_init(&bar[0], 1);
-        umma::mbar_init(&bar[1], 1);
-        umma::fence_barrier_init();
-    }
     umma::tc_fence_before();
     __syncthreads();
     umma::tc_fence_after();
+    float cmax2 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kAssignThreads / 32; ++i) cmax2 = fmaxf(cmax2, red[i]);
     const uint32_t tmem = tmem_base;
     const uint32_t idesc = umma::idesc_f16(128, Np, 1);
     const uint32_t b0 = umma::smem_u32(Bs);
-    auto issue = [&](int buf) {
-        const uint32_t a0 = umma::smem_u32(As + buf * AB);
-#pragma unroll
+    auto issue = [&](int k) {
+        const uint32_t a0 = umma::smem_u32(As + (k % NA) * AB);
+#pragma unroll 1
         for (int p = 0; p < P; ++p)
-#pragma unroll
+#pragma unroll 1
             for (int s = 0; s < D / 16; ++s) {
                 const uint64_t ad = umma::desc_sw128(a0 + (s >> 2) * 16384 + (s & 3) * 32);
                 const uint64_t bd = umma::desc_sw128(b0 + (p * KB + (s >> 2)) * Np * 128 + (s & 3) * 32);
-                umma::mma_f16(tmem + buf * ncols, ad, bd, idesc, (p | s) != 0);
+                umma::mma_f16(tmem + (k & 1) * ncols, ad, bd, idesc, (p | s) != 0);
             }
-        umma::mma_commit(&bar[buf]);
+        umma::mma_commit(&bar_mma[k & 1]);
     };
-    if (tid == 0 && t0 < n_tiles) issue(0);
     bool ok = true;
-    int k = 0;  // local tile counter
-    for (int t = t0; t < n_tiles; t += tstep, ++k) {
-        const int buf = k & 1, nxt = t + tstep;
-        // the other buffer's previous tile (MMA and epilogue) finished before the
-        // barrier that ended the last iteration, so its rows can be reloaded
-        if (nxt < n_tiles) load_tile(nxt, buf ^ 1);
-        if (!umma::mbar_wait(&bar[buf], (k >> 1) & 1, kWaitNs)) ok = false;
+    if (tid == 0 && my_tiles > 0) {
+        if (umma::mbar_wait(&bar_a[0], 0, kWaitNs)) {
+            umma::tc_fence_after();
+            issue(0);
+        } else {
+            ok = false;
+        }
+    }
+    ok = __syncthreads_and(ok);
+    for (int k = 0; ok && k < my_tiles; ++k) {
+        const int t = t0 + k * tstep;
+        const int buf = k % NA;
+        // (1) with three buffers, tile k+1 is already loaded: start its MMA now
+        // (its accumulator's previous tile, k-1, ended at the last barrier)
+        if (NA == 3 && tid == 0 && k + 1 < my_tiles) {
+            if (umma::mbar_wait(&bar_a[(k + 1) % NA], ((k + 1) / NA) & 1, kWaitNs)) {
+                umma::tc_fence_after();
+                issue(k + 1);
+            } else {
+                ok = false;
+            }
+        }
+        // (2) refill the buffer of tile k - 1 (its epilogue ended at the last barrier)
+        if (k + NA - 1 < my_tiles) load_tile(k + NA - 1);
+        // (3) epilogue of tile k
+        if (!umma::mbar_wait(&bar_mma[k & 1], (k >> 1) & 1, kWaitNs)) ok = false;
         ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
         umma::tc_fence_after();
-        // epilogue of tile t while the next tile's loads are in flight.  Row r
-        // (token n) is read by one thread of each warp group; each keeps four
-        // independent (best, second) chains over its columns, merged by
-        // (score, index) so that ties still go to the lowest cluster.
         const int r = (warp & 3) * 32 + lane, n = t * 128 + r;
+        const uint8_t *Ab = As + buf * AB;
+        float xn = 0.0f;
+        if (grp == 0 && xmode == 0 && n < N) xn = xnorm[static_cast<size_t>(h) * N + n];
         float bv[4], sv[4];
         int bi[4], si[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            bv[q] = INFINITY;
-            sv[q] = INFINITY;
-            bi[q] = 0x7fffffff;
-            si[q] = 0x7fffffff;
+            bv[q] = sv[q] = INFINITY;
+            bi[q] = si[q] = 0x7fffffff;
         }
         if (ok) {
             for (int c0 = grp * 32; c0 < Np; c0 += 64) {
                 uint32_t acc[32];
-                umma::tmem_ld32(tmem + buf * ncols + (static_cast<uint32_t>((warp & 3) * 32) << 16) + c0, acc);
-                umma::tmem_ld_wait();
+                umma::tmem_ld32(tmem + (k & 1) * ncols + (static_cast<uint32_t>((warp & 3) * 32) << 16) + c0, acc);
+                umma::tmem_ld_wait_regs(acc);
 #pragma unroll
                 for (int kk = 0; kk < 32; ++kk) {
                     const int c = c0 + kk, q = kk & 3;
                     // columns past Np were not written by the MMA; cn is +inf past Ce
                     const float sc = c < Np ? fmaf(-2.0f, __uint_as_float(acc[kk]), cn[c]) : INFINITY;
-                    if (sc < bv[q]) {
-                        sv[q] = bv[q];
-                        si[q] = bi[q];
-                        bv[q] = sc;
-                        bi[q] = c;
-                    } else if (sc < sv[q]) {
-                        sv[q] = sc;
-                        si[q] = c;
+                    if (sc < sv[q]) {
+                        if (sc < bv[q]) {
+                            sv[q] = bv[q];
+                            si[q] = bi[q];
+                            bv[q] = sc;
+                            bi[q] = c;
+                        } else {
+                            sv[q] = sc;
+                            si[q] = c;
+                        }
                     }
                 }
             }
         }
-        auto less = [](float a, int ia, float b, int ib) { return a < b || (a == b && ia < ib); };
-        auto merge = [&](float &best, int &arg, float &second, int &arg2, float b2, int i2, float s2, int j2) {
-            if (less(b2, i2, best, arg)) {
-                if (less(best, arg, s2, j2)) {
-                    second = best;
-                    arg2 = arg;
-                } else {
-                    second = s2;
-                    arg2 = j2;
-                }
-                best = b2;
-                arg = i2;
-            } else if (less(b2, i2, second, arg2)) {
-                second = b2;
-                arg2 = i2;
-            }
-        };
-        float best = bv[0], second = sv[0];
-        int arg = bi[0], arg2 = si[0];
 #pragma unroll
-        for (int q = 1; q < 4; ++q) merge(best, arg, second, arg2, bv[q], bi[q], sv[q], si[q]);
+        for (int q = 1; q < 4; ++q) merge2(bv[0], bi[0], sv[0], si[0], bv[q], bi[q], sv[q], si[q]);
         if (grp == 1) {
-            xb[r][0] = best;
-            xb[r][1] = second;
-            xi[r][0] = arg;
-            xi[r][1] = arg2;
+            xs[r][0] = bv[0];
+            xs[r][1] = sv[0];
+            xk[r][0] = bi[0];
+            xk[r][1] = si[0];
         }
         __syncthreads();
         if (grp == 0) {
-            merge(best, arg, second, arg2, xb[r][0], xi[r][0], xb[r][1], xi[r][1]);
-            if (arg == 0x7fffffff) arg = 0;
-            if (arg2 == 0x7fffffff || !(second < INFINITY)) arg2 = -1;
-            xi[r][0] = arg;
-            xi[r][1] = arg2;
-        }
-        __syncthreads();
-        arg = xi[r][0];
-        arg2 = xi[r][1];
-        // The GEMM form cancels large outlier products; the two candidates are
-        // re-scored with the direct sum_j w_j (x_j - c_j)^2 (fp32, ascending j):
-        // group 0 scores the best, group 1 the second.  x comes from the token
-        // tile; c from the centroid tile (P == 1: it holds c itself) or from
-        // global memory (P == 2: the tile holds w*c).
-        float dd = 0.0f;
-        const int cand = grp == 0 ? arg : arg2;
-        if (arg2 >= 0 && n < N) {
-            const uint8_t *Ab = As + buf * AB;
-            const uint16_t *cg = ch + static_cast<size_t>(cand) * D;
+            merge2(bv[0], bi[0], sv[0], si[0], xs[r][0], xk[r][0], xs[r][1], xk[r][1]);
+            int arg = bi[0] == 0x7fffffff ? 0 : bi[0];
+            const int arg2 = (si[0] == 0x7fffffff || !(sv[0] < INFINITY)) ? -1 : si[0];
+            if (xmode == 1 && n < N) {
+                // ||x||_w^2 of this row from the token tile (fp32, ascending j)
+                float sx = 0.0f;
 #pragma unroll
-            for (int ci = 0; ci < D / 8; ++ci) {
-                const int kb = ci >> 3, c = ci & 7;
-                const uint4 xv = *reinterpret_cast<const uint4 *>(Ab + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4));
-                uint4 u;
-                if constexpr (P == 1)
-                    u = *reinterpret_cast<const uint4 *>(Bs + static_cast<size_t>(kb) * Np * 128 + cand * 128 +
-                                                         ((c ^ (cand & 7)) << 4));
-                else
-                    u = *reinterpret_cast<const uint4 *>(cg + ci * 8);
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, uw[4] = {u.x, u.y, u.z, u.w};
+                for (int ci = 0; ci < D / 8; ++ci) {
+                    const int kb = ci >> 3, c = ci & 7;
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(Ab + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4));
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int sh = (e & 1) ? 0 : 16;
-                    const float xj = __uint_as_float((xw[e >> 1] << sh) & 0xffff0000u);
-                    const float df = xj - __uint_as_float((uw[e >> 1] << sh) & 0xffff0000u);
-                    const float wj = w ? w[h * D + ci * 8 + e] : 1.0f;
-                    dd = fmaf(wj * df, df, dd);
+                    for (int e = 0; e < 8; ++e) {
+                        const float xj = __uint_as_float((xw[e >> 1] << ((e & 1) ? 0 : 16)) & 0xffff0000u);
+                        const float wj = w ? w[h * D + ci * 8 + e] : 1.0f;
+                        sx = fmaf(wj * xj, xj, sx);
+                    }
                 }
+                xn = sx;
+                xnorm[static_cast<size_t>(h) * N + n] = sx;
             }
-        }
-        if (grp == 1) xd[r] = dd;
-        __syncthreads();
-        if (grp == 0) {
-            if (arg2 >= 0 && (xd[r] < dd || (xd[r] == dd && arg2 < arg))) arg = arg2;
+            const bool flag = ok && n < N && arg2 >= 0 && !(sv[0] - bv[0] > kAssignTau * (xn + cmax2));
+            // warp-cooperative exact re-scoring of the flagged rows
+            unsigned m = __ballot_sync(0xffffffffu, flag);
+            while (m) {
+                const int l = __ffs(m) - 1;
+                m &= m - 1;
+                const int rr = (warp & 3) * 32 + l;
+                const int ca = __shfl_sync(0xffffffffu, arg, l), cb = __shfl_sync(0xffffffffu, arg2, l);
+                const int j0 = lane * E, kb = j0 >> 6, e0 = j0 & 63, c8 = e0 >> 3, boff = (e0 & 7) * 2;
+                float xv[E], va[E], vb[E];
+                auto ld_row = [&](const uint8_t *base, size_t kb_stride, int row, float (&v)[E]) {
+                    const uint8_t *pp = base + kb * kb_stride + row * 128 + ((c8 ^ (row & 7)) << 4) + boff;
+                    if constexpr (E == 4) {
+                        const uint2 u = *reinterpret_cast<const uint2 *>(pp);
+                        v[0] = __uint_as_float(u.x << 16);
+                        v[1] = __uint_as_float(u.x & 0xffff0000u);
+                        v[2] = __uint_as_float(u.y << 16);
+                        v[3] = __uint_as_float(u.y & 0xffff0000u);
+                    } else {
+                        const uint32_t u = *reinterpret_cast<const uint32_t *>(pp);
+                        v[0] = __uint_as_float(u << 16);
+                        v[1] = __uint_as_float(u & 0xffff0000u);
+                    }
+                };
+                ld_row(Ab, 16384, rr, xv);
+                if constexpr (P == 1) {
+                    ld_row(Bs, static_cast<size_t>(Np) * 128, ca, va);
+                    ld_row(Bs, static_cast<size_t>(Np) * 128, cb, vb);
+                } else {
+                    const uint16_t *pa = ch + static_cast<size_t>(ca) * D + j0, *pb = ch + static_cast<size_t>(cb) * D + j0;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        va[e] = bf16_to_f32(pa[e]);
+                        vb[e] = bf16_to_f32(pb[e]);
+                    }
+                }
+                float da = 0.0f, db = 0.0f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float wj = w ? w[h * D + j0 + e] : 1.0f;
+                    const float fa = xv[e] - va[e], fb = xv[e] - vb[e];
+                    da = fmaf(wj * fa, fa, da);
+                    db = fmaf(wj * fb, fb, db);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    da += __shfl_xor_sync(0xffffffffu, da, o);
+                    db += __shfl_xor_sync(0xffffffffu, db, o);
+                }
+                if (lane == l && (db < da || (db == da && cb < ca))) arg = cb;
+            }
             if (ok && n < N) ids[static_cast<size_t>(h) * N + n] = arg;
         }
-        // the next tile's operands are in shared memory: start its MMA
-        umma::cp_async_wait_all();
-        umma::fence_proxy_async_smem();
-        umma::tc_fence_before();
-        if (!__syncthreads_and(ok)) {
-            ok = false;
-            break;
+        // (4) with two buffers, tile k+1's loads were issued in (2): start its MMA
+        if (NA == 2 && tid == 0 && k + 1 < my_tiles) {
+            if (umma::mbar_wait(&bar_a[(k + 1) % NA], ((k + 1) / NA) & 1, kWaitNs)) {
+                umma::tc_fence_after();
+                issue(k + 1);
+            } else {
+                ok = false;
+            }
         }
+        umma::tc_fence_before();
+        ok = __syncthreads_and(ok);
         umma::tc_fence_after();
-        if (tid == 0 && nxt < n_tiles) issue(buf ^ 1);
-    }    if (!ok) {
-        if (tid == 0) raise_error(err, QVG_ERR_TIMEOUT);
-        // let in-flight MMAs drain before TMEM is released
-        umma::mbar_wait(&bar[0], 0, kWaitNs);
     }
+    if (!ok && tid == 0) raise_error(err, QVG_ERR_TIMEOUT);
+    // every MMA issued by thread 0 completes before TMEM is released
+    if (tid == 0 && my_tiles > 0) {
+        umma::mma_commit(&bar_drain);
+        umma::mbar_wait(&bar_drain, 0, kWaitNs);
+    }
+    umma::cp_async_wait_all();
     umma::tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -670,16 +762,18 @@ qvg_status launch_centroid_norms(const uint16_t *cent, size_t hs, int H, int C, 
 
 template <int D, int P>
 static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t *cent, size_t hs, int Ce,
-                                 const float *cnorm, int C, const float *w, int32_t *ids, cudaStream_t st) {
+                                 const float *cnorm, int C, const float *w, float *xnorm, int xmode, int32_t *ids,
+                                 cudaStream_t st) {
     const int Np = std::max(16, ceil_div(Ce, 16) * 16);
-    constexpr int KB = D / 64;
-    const size_t smem = 2 * static_cast<size_t>(KB) * 128 * 128 + static_cast<size_t>(P) * KB * Np * 128 +
-                        Np * 4 + 1024;
+    constexpr int KB = D / 64, NA = P == 1 ? 3 : 2;
+    // cn holds Np + 32 floats: a 32-column chunk may extend past Np
+    const size_t smem = NA * static_cast<size_t>(KB) * 128 * 128 + static_cast<size_t>(P) * KB * Np * 128 +
+                        (Np + 32) * 4 + 1024;
     static bool attr = false;
     if (!attr) {
         // the largest request of this instantiation (Np = 256)
-        const size_t most = 2 * static_cast<size_t>(KB) * 128 * 128 +
-                            static_cast<size_t>(P) * KB * QVG_MAX_CLUSTERS * 128 + QVG_MAX_CLUSTERS * 4 + 1024;
+        const size_t most = NA * static_cast<size_t>(KB) * 128 * 128 +
+                            static_cast<size_t>(P) * KB * QVG_MAX_CLUSTERS * 128 + (QVG_MAX_CLUSTERS + 32) * 4 + 1024;
         const cudaError_t e = cudaFuncSetAttribute(k_kmeans_assign_tc<D, P>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(most));
@@ -695,20 +789,20 @@ static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t
     const int n_tiles = ceil_div(N, 128);
     const int per_head = std::max(1, std::min(n_tiles, sm_count() / std::max(1, H)));
     dim3 grid(per_head, H);
-    k_kmeans_assign_tc<D, P><<<grid, kAssignThreads, smem, st>>>(g, N, H, cent, hs, Ce, Np, cnorm, C, w, ids,
-                                                                 device_error_word());
+    k_kmeans_assign_tc<D, P><<<grid, kAssignThreads, smem, st>>>(g, N, H, cent, hs, Ce, Np, cnorm, C, w, xnorm,
+                                                                 xmode, ids, device_error_word());
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }
 
 qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d, const uint16_t *cent,
                                 size_t hs, int Ce, const float *cnorm, int C, const float *w,
-                                int32_t *ids, cudaStream_t st) {
+                                float *xnorm, int xmode, int32_t *ids, cudaStream_t st) {
     if (d == 64)
-        return w ? assign_tc_impl<64, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st)
-                 : assign_tc_impl<64, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st);
-    return w ? assign_tc_impl<128, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st)
-             : assign_tc_impl<128, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, ids, st);
+        return w ? assign_tc_impl<64, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, xmode, ids, st)
+                 : assign_tc_impl<64, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, xmode, ids, st);
+    return w ? assign_tc_impl<128, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, xmode, ids, st)
+             : assign_tc_impl<128, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, xmode, ids, st);
 }
 
 qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int d,
