@@ -108,10 +108,11 @@ __global__ void k_centroid_norms(const uint16_t *__restrict__ cent, size_t hs, i
 // into NA buffers (completion counted on an mbarrier per buffer), and the MMA
 // of tile k+1 runs while the epilogue of tile k reads the other accumulator.
 //
-// Epilogue, thread = token row (the two warp groups take alternating
+// Epilogue, thread = token row (the four warp groups take interleaved
 // 32-column chunks): score s_c = ||c||_w^2 - 2 acc_c in fp32; four
 // independent (best, second) chains per thread, merged in (score, index)
-// order so that ties go to the lower cluster.
+// order so that ties go to the lower cluster.  The per-group results meet in
+// shared memory; each warp then finishes 8 rows.
 //
 // Exactness: the ranking must be that of d_c = sum_j w_j (x_j - c_j)^2 =
 // ||x||_w^2 + s_c.  The tensor-core sum (<= 2^-16 sum w|x c|, products exact),
@@ -122,15 +123,16 @@ __global__ void k_centroid_norms(const uint16_t *__restrict__ cent, size_t hs, i
 // When the two best scores differ by more than tau (||x||_w^2 +
 // max||c||_w^2) with tau = 2^-11 (= 8 E), the best score is the exact argmin
 // (no tie possible).  Otherwise the two candidates are re-scored with the
-// direct sum: the 32 lanes of the row's warp each take D/32 consecutive
-// channels (fp32, ascending), the partial sums are added by an xor
-// butterfly, and the smaller distance wins (ties to the lower index).
+// direct sum: the 32 lanes of a warp each take D/32 consecutive channels of
+// the row (fp32, ascending), the partial sums are added by an xor butterfly,
+// and the smaller distance wins (ties to the lower index).
 // ||x||_w^2 is computed by the first assignment of a stage (xmode 1) and
 // stored in xnorm for the later ones.
 // Every wait is bounded; on expiry the CTA records QVG_ERR_TIMEOUT.
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 
-constexpr int kAssignThreads = 256;
+constexpr int kAssignThreads = 512;
+constexpr int kAssignGroups = kAssignThreads / 128;  // warp groups sharing the columns
 constexpr float kAssignTau = 1.0f / 2048.0f;
 
 // (score, index) order: lower score, then lower index
@@ -172,11 +174,11 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
     float *cn = reinterpret_cast<float *>(Bs + static_cast<size_t>(P) * KB * Np * 128);  // Np + 32
     __shared__ uint64_t bar_mma[2], bar_a[NA], bar_drain;
     __shared__ uint32_t tmem_base;
-    __shared__ float xs[128][2];     // warp group 1's two best scores per row
-    __shared__ int xk[128][2];       // ... and their clusters
+    __shared__ float xs[kAssignGroups][128][2];  // each warp group's two best scores per row
+    __shared__ int xk[kAssignGroups][128][2];    // ... and their clusters
     __shared__ float red[kAssignThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int grp = warp >> 2;       // warp group: 32-column chunks grp, grp + 2, ...
+    const int grp = warp >> 2;       // warp group: 32-column chunks grp, grp + G, ... (G groups)
     const int h = blockIdx.y;
     const int n_tiles = ceil_div(N, 128);
     const int t0 = blockIdx.x, tstep = gridDim.x;
@@ -316,10 +318,8 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         if (!umma::mbar_wait(&bar_mma[k & 1], (k >> 1) & 1, kWaitNs)) ok = false;
         ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
         umma::tc_fence_after();
-        const int r = (warp & 3) * 32 + lane, n = t * 128 + r;
+        const int r = (warp & 3) * 32 + lane;
         const uint8_t *Ab = As + buf * AB;
-        float xn = 0.0f;
-        if (grp == 0 && xmode == 0 && n < N) xn = xnorm[static_cast<size_t>(h) * N + n];
         float bv[4], sv[4];
         int bi[4], si[4];
 #pragma unroll
@@ -328,24 +328,32 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
             bi[q] = si[q] = 0x7fffffff;
         }
         if (ok) {
-            for (int c0 = grp * 32; c0 < Np; c0 += 64) {
+            for (int c0 = grp * 32; c0 < Np; c0 += 32 * kAssignGroups) {
                 uint32_t acc[32];
                 umma::tmem_ld32(tmem + (k & 1) * ncols + (static_cast<uint32_t>((warp & 3) * 32) << 16) + c0, acc);
                 umma::tmem_ld_wait_regs(acc);
+                const float4 *cn4 = reinterpret_cast<const float4 *>(cn + c0);
+                // columns past Np were not written by the MMA: masked in a partial chunk
+                const bool full = c0 + 32 <= Np;
 #pragma unroll
-                for (int kk = 0; kk < 32; ++kk) {
-                    const int c = c0 + kk, q = kk & 3;
-                    // columns past Np were not written by the MMA; cn is +inf past Ce
-                    const float sc = c < Np ? fmaf(-2.0f, __uint_as_float(acc[kk]), cn[c]) : INFINITY;
-                    if (sc < sv[q]) {
-                        if (sc < bv[q]) {
-                            sv[q] = bv[q];
-                            si[q] = bi[q];
-                            bv[q] = sc;
-                            bi[q] = c;
-                        } else {
-                            sv[q] = sc;
-                            si[q] = c;
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 cv = cn4[k4];
+                    const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int kk = 4 * k4 + e, c = c0 + kk;
+                        float sc = fmaf(-2.0f, __uint_as_float(acc[kk]), cc[e]);
+                        if (!full && c >= Np) sc = INFINITY;
+                        if (sc < sv[e]) {
+                            if (sc < bv[e]) {
+                                sv[e] = bv[e];
+                                si[e] = bi[e];
+                                bv[e] = sc;
+                                bi[e] = c;
+                            } else {
+                                sv[e] = sc;
+                                si[e] = c;
+                            }
                         }
                     }
                 }
@@ -353,59 +361,65 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         }
 #pragma unroll
         for (int q = 1; q < 4; ++q) merge2(bv[0], bi[0], sv[0], si[0], bv[q], bi[q], sv[q], si[q]);
-        if (grp == 1) {
-            xs[r][0] = bv[0];
-            xs[r][1] = sv[0];
-            xk[r][0] = bi[0];
-            xk[r][1] = si[0];
-        }
+        xs[grp][r][0] = bv[0];
+        xs[grp][r][1] = sv[0];
+        xk[grp][r][0] = bi[0];
+        xk[grp][r][1] = si[0];
         __syncthreads();
-        if (grp == 0) {
-            merge2(bv[0], bi[0], sv[0], si[0], xs[r][0], xk[r][0], xs[r][1], xk[r][1]);
-            int arg = bi[0] == 0x7fffffff ? 0 : bi[0];
-            const int arg2 = (si[0] == 0x7fffffff || !(sv[0] < INFINITY)) ? -1 : si[0];
-            if (xmode == 1 && n < N) {
-                // ||x||_w^2 of this row from the token tile (fp32, ascending j)
-                float sx = 0.0f;
+        // finalisation: warp W takes rows 8W .. 8W+7, lane l < 8 merges row 8W + l
+        {
+            const int fr = 8 * warp + (lane & 7), n = t * 128 + fr;
+            float b1 = xs[0][fr][0], b2 = xs[0][fr][1];
+            int a1 = xk[0][fr][0], a2 = xk[0][fr][1];
 #pragma unroll
-                for (int ci = 0; ci < D / 8; ++ci) {
-                    const int kb = ci >> 3, c = ci & 7;
-                    const uint4 xv = *reinterpret_cast<const uint4 *>(Ab + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4));
-                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float xj = __uint_as_float((xw[e >> 1] << ((e & 1) ? 0 : 16)) & 0xffff0000u);
-                        const float wj = w ? w[h * D + ci * 8 + e] : 1.0f;
-                        sx = fmaf(wj * xj, xj, sx);
-                    }
+            for (int gq = 1; gq < kAssignGroups; ++gq) merge2(b1, a1, b2, a2, xs[gq][fr][0], xk[gq][fr][0], xs[gq][fr][1], xk[gq][fr][1]);
+            int arg = a1 == 0x7fffffff ? 0 : a1;
+            const int arg2 = (a2 == 0x7fffffff || !(b2 < INFINITY)) ? -1 : a2;
+            const int j0 = lane * E, kb = j0 >> 6, e0 = j0 & 63, c8 = e0 >> 3, boff = (e0 & 7) * 2;
+            auto ld_row = [&](const uint8_t *base, size_t kb_stride, int row, float (&v)[E]) {
+                const uint8_t *pp = base + kb * kb_stride + row * 128 + ((c8 ^ (row & 7)) << 4) + boff;
+                if constexpr (E == 4) {
+                    const uint2 u = *reinterpret_cast<const uint2 *>(pp);
+                    v[0] = __uint_as_float(u.x << 16);
+                    v[1] = __uint_as_float(u.x & 0xffff0000u);
+                    v[2] = __uint_as_float(u.y << 16);
+                    v[3] = __uint_as_float(u.y & 0xffff0000u);
+                } else {
+                    const uint32_t u = *reinterpret_cast<const uint32_t *>(pp);
+                    v[0] = __uint_as_float(u << 16);
+                    v[1] = __uint_as_float(u & 0xffff0000u);
                 }
-                xn = sx;
-                xnorm[static_cast<size_t>(h) * N + n] = sx;
+            };
+            float wl[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) wl[e] = w ? w[h * D + j0 + e] : 1.0f;
+            float xn = 0.0f;
+            if (xmode == 0) {
+                if (lane < 8 && n < N) xn = xnorm[static_cast<size_t>(h) * N + n];
+            } else {
+                // ||x||_w^2 of the warp's 8 rows: D/32 channels per lane, xor-butterfly sum
+#pragma unroll 1
+                for (int l = 0; l < 8; ++l) {
+                    float xv[E];
+                    ld_row(Ab, 16384, 8 * warp + l, xv);
+                    float sx = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) sx = fmaf(wl[e] * xv[e], xv[e], sx);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+                    if (lane == l) xn = sx;
+                }
+                if (lane < 8 && n < N) xnorm[static_cast<size_t>(h) * N + n] = xn;
             }
-            const bool flag = ok && n < N && arg2 >= 0 && !(sv[0] - bv[0] > kAssignTau * (xn + cmax2));
+            const bool flag = ok && lane < 8 && n < N && arg2 >= 0 && !(b2 - b1 > kAssignTau * (xn + cmax2));
             // warp-cooperative exact re-scoring of the flagged rows
             unsigned m = __ballot_sync(0xffffffffu, flag);
             while (m) {
                 const int l = __ffs(m) - 1;
                 m &= m - 1;
-                const int rr = (warp & 3) * 32 + l;
+                const int rr = 8 * warp + l;
                 const int ca = __shfl_sync(0xffffffffu, arg, l), cb = __shfl_sync(0xffffffffu, arg2, l);
-                const int j0 = lane * E, kb = j0 >> 6, e0 = j0 & 63, c8 = e0 >> 3, boff = (e0 & 7) * 2;
                 float xv[E], va[E], vb[E];
-                auto ld_row = [&](const uint8_t *base, size_t kb_stride, int row, float (&v)[E]) {
-                    const uint8_t *pp = base + kb * kb_stride + row * 128 + ((c8 ^ (row & 7)) << 4) + boff;
-                    if constexpr (E == 4) {
-                        const uint2 u = *reinterpret_cast<const uint2 *>(pp);
-                        v[0] = __uint_as_float(u.x << 16);
-                        v[1] = __uint_as_float(u.x & 0xffff0000u);
-                        v[2] = __uint_as_float(u.y << 16);
-                        v[3] = __uint_as_float(u.y & 0xffff0000u);
-                    } else {
-                        const uint32_t u = *reinterpret_cast<const uint32_t *>(pp);
-                        v[0] = __uint_as_float(u << 16);
-                        v[1] = __uint_as_float(u & 0xffff0000u);
-                    }
-                };
                 ld_row(Ab, 16384, rr, xv);
                 if constexpr (P == 1) {
                     ld_row(Bs, static_cast<size_t>(Np) * 128, ca, va);
@@ -421,10 +435,9 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
                 float da = 0.0f, db = 0.0f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    const float wj = w ? w[h * D + j0 + e] : 1.0f;
                     const float fa = xv[e] - va[e], fb = xv[e] - vb[e];
-                    da = fmaf(wj * fa, fa, da);
-                    db = fmaf(wj * fb, fb, db);
+                    da = fmaf(wl[e] * fa, fa, da);
+                    db = fmaf(wl[e] * fb, fb, db);
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) {
@@ -433,7 +446,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
                 }
                 if (lane == l && (db < da || (db == da && cb < ca))) arg = cb;
             }
-            if (ok && n < N) ids[static_cast<size_t>(h) * N + n] = arg;
+            if (ok && lane < 8 && n < N) ids[static_cast<size_t>(h) * N + n] = arg;
         }
         // (4) with two buffers, tile k+1's loads were issued in (2): start its MMA
         if (NA == 2 && tid == 0 && k + 1 < my_tiles) {
