@@ -190,17 +190,17 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
             } else if ((s = launch_centroid_norms(cent, cent_hs, H, C, d, w, ws.cnorm, st)) != QVG_OK) {
                 return s;
             }
-            // the first assignment of the stage also records ||x||_w^2 per token
+            if ((s = launch_row_norms(g, N, H, d, w, ws.xnorm, st)) != QVG_OK) return s;
             for (int it = 0; it < p->iters; ++it) {
-                if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.xnorm, it == 0,
-                                              ws.ids, st)) != QVG_OK)
+                if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.xnorm, ws.ids, st)) !=
+                    QVG_OK)
                     return s;
                 if ((s = launch_kmeans_update(xin, f32, N, H, d, ws.ids, cent, cent_hs, Ce, C, w, ws.cnorm, st)) !=
                     QVG_OK)
                     return s;
             }
-            if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.xnorm, p->iters == 0,
-                                          ws.ids, st)) != QVG_OK)
+            if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.xnorm, ws.ids, st)) !=
+                QVG_OK)
                 return s;
         }
         const bool last = l == L - 1;

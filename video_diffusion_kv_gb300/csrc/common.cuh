@@ -92,12 +92,13 @@ qvg_status launch_kmeans_init(const uint16_t *g, int N, int H, int d, int C, int
                               cudaStream_t st);
 qvg_status launch_centroid_norms(const uint16_t *cent, size_t cent_head_stride, int H,
                                  int C, int d, const float *w, float *cnorm, cudaStream_t st);
-// xnorm [H][N]: ||x||_w^2 per token, written when xmode == 1 (the first
-// assignment of a stage) and read otherwise.
+// xnorm [H][N]: ||x||_w^2 per token (launch_row_norms, once per stage).
 qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d,
                                 const uint16_t *cent, size_t cent_head_stride, int Ce,
-                                const float *cnorm, int C, const float *w, float *xnorm, int xmode,
+                                const float *cnorm, int C, const float *w, const float *xnorm,
                                 int32_t *ids, cudaStream_t st);
+qvg_status launch_row_norms(const uint16_t *g, int N, int H, int d, const float *w, float *xnorm,
+                            cudaStream_t st);
 qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int d,
                                 const int32_t *ids, uint16_t *cent, size_t cent_head_stride, int Ce, int C,
                                 const float *w, float *cnorm, cudaStream_t st);

@@ -100,40 +100,60 @@ __global__ void k_centroid_norms(const uint16_t *__restrict__ cent, size_t hs, i
 // ---------------------------------------------------------------------------
 // Assignment on the tensor cores.  A CTA owns one head's centroids (staged
 // once in shared memory) and walks several 128-token tiles of that head:
-//   D_t[128 x Np] = X_t (bf16, 128 x D) * B^T,  B = the centroids (bf16,
-//   exact) or, with QSAC weights, the weighted centroids w*c as a bf16 pair
-//   hi + lo (|w c - hi - lo| <= 2^-18 |w c|),
-// accumulated in fp32 in tensor memory by tcgen05.mma (M=128, N=Np = Ce
-// rounded up to 16, K=16 per instruction).  Token tiles arrive by cp.async
-// into NA buffers (completion counted on an mbarrier per buffer), and the MMA
-// of tile k+1 runs while the epilogue of tile k reads the other accumulator.
+//   F_t[128 x Np] = [X_t | e_t] [B | b]^T,  f_c = x.c - ||c||_w^2/2 - ||x||_w^2/2
+// with B = the centroids (bf16, exact) or, with QSAC weights, the weighted
+// centroids w*c as a bf16 pair hi + lo (|w c - hi - lo| <= 2^-18 |w c|), and
+// one extra K=16 block: e_t = (-1, -1, -1, -x1, -x2, -x3, 0...) per token,
+// b = (n1, n2, n3, 1, 1, 1, 0...) per centroid, where x1+x2+x3 and n1+n2+n3
+// are ||x||_w^2 / 2 and ||c||_w^2 / 2 split into three bf16 parts (exact to
+// 2^-24).  So f_c = -d_c / 2 with d_c = sum_j w_j (x_j - c_j)^2, accumulated in
+// fp32 in tensor memory by tcgen05.mma (M=128, N=Np = Ce rounded up to 16).
+// Token tiles arrive by cp.async into NA buffers (completion counted on an
+// mbarrier per buffer), and the MMA of tile k+1 runs while the epilogue of
+// tile k reads the other accumulator.
 //
 // Epilogue, thread = token row (the four warp groups take interleaved
-// 32-column chunks): score s_c = ||c||_w^2 - 2 acc_c in fp32; four
-// independent (best, second) chains per thread, merged in (score, index)
-// order so that ties go to the lower cluster.  The per-group results meet in
-// shared memory; each warp then finishes 8 rows.
+// 32-column chunks).  For f <= 0 a larger f has a smaller bit pattern as an
+// unsigned integer, so the best clusters are the smallest keys
+// (bits(f) with the low 4 bits replaced by the column's place in the
+// thread's chain): three unsigned min/max per column keep the two best of
+// each of four chains.  A slightly positive f (d within rounding of 0) ranks
+// first as well.  The chains and groups are merged in (score, index) order,
+// ties to the lower cluster; each warp then finishes 8 rows.
 //
-// Exactness: the ranking must be that of d_c = sum_j w_j (x_j - c_j)^2 =
-// ||x||_w^2 + s_c.  The tensor-core sum (<= 2^-16 sum w|x c|, products exact),
-// the hi/lo split (2^-18), the fp32 norm (2^-16 ||c||^2) and the FMA bound
-// the score error, with sum w|x c| <= ||x||_w ||c||_w <= (||x||_w^2 +
-// ||c||_w^2) / 2, by
-//   E <= 2^-14 (||x||_w^2 + max_c ||c||_w^2).
-// When the two best scores differ by more than tau (||x||_w^2 +
-// max||c||_w^2) with tau = 2^-11 (= 8 E), the best score is the exact argmin
-// (no tie possible).  Otherwise the two candidates are re-scored with the
-// direct sum: the 32 lanes of a warp each take D/32 consecutive channels of
-// the row (fp32, ascending), the partial sums are added by an xor butterfly,
-// and the smaller distance wins (ties to the lower index).
-// ||x||_w^2 is computed by the first assignment of a stage (xmode 1) and
-// stored in xnorm for the later ones.
+// Exactness: the tensor-core sum (<= 2^-16 of the sum of |terms|, products
+// exact), the hi/lo split (2^-18), the norm splits (2^-24) and the key
+// truncation (2^-19 |f|) bound the error of d_c, with sum w|x c| <=
+// ||x||_w ||c||_w <= (||x||_w^2 + ||c||_w^2) / 2, by
+//   E_c <= 2^-14 (||x||_w^2 + ||c||_w^2) <= 2^-14 (3 ||x||_w^2 + 2 d_c),
+// since ||c||_w <= ||x||_w + sqrt(d_c).  The computed best b is the exact
+// argmin (no tie possible) when d_c - d_b > E_c + E_b for every other c; that
+// margin grows with d_c, so the second best s decides it, and with a factor
+// two to spare the test is
+//   d_s - d_b > 2^-12 (3 ||x||_w^2 + d_s + d_b).
+// Otherwise the two candidates are re-scored with the direct sum: the 32
+// lanes of a warp each take D/32 consecutive channels of the row (fp32,
+// ascending), the partial sums are added by an xor butterfly, and the smaller
+// distance wins (ties to the lower index).  ||x||_w^2 comes from
+// k_row_norms, run once per stage.
 // Every wait is bounded; on expiry the CTA records QVG_ERR_TIMEOUT.
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 
 constexpr int kAssignThreads = 512;
 constexpr int kAssignGroups = kAssignThreads / 128;  // warp groups sharing the columns
-constexpr float kAssignTau = 1.0f / 2048.0f;
+constexpr float kAssignTau = 1.0f / 4096.0f;
+
+// v = p0 + p1 + p2 in bf16 parts (each the rounding of what is left)
+__device__ __forceinline__ void split3(float v, uint16_t &p0, uint16_t &p1, uint16_t &p2) {
+    p0 = f32_to_bf16(v);
+    const float r1 = v - bf16_to_f32(p0);
+    p1 = f32_to_bf16(r1);
+    p2 = f32_to_bf16(r1 - bf16_to_f32(p1));
+}
+__device__ __forceinline__ uint32_t bf16pair(uint16_t lo, uint16_t hi) {
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+constexpr uint16_t kBf16One = 0x3f80, kBf16MinusOne = 0xbf80;
 
 // (score, index) order: lower score, then lower index
 __device__ __forceinline__ bool sc_less(float a, int ia, float b, int ib) { return a < b || (a == b && ia < ib); }
@@ -160,7 +180,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
                                                             const uint16_t *__restrict__ cent, size_t hs,
                                                             int Ce, int Np, const float *__restrict__ cnorm,
                                                             int C, const float *__restrict__ w,
-                                                            float *__restrict__ xnorm, int xmode,
+                                                            const float *__restrict__ xnorm,
                                                             int32_t *__restrict__ ids, int *err) {
     constexpr int KB = D / 64;                       // 64-element K blocks
     constexpr int AB = KB * 128 * 128;               // one token tile
@@ -170,13 +190,13 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
     // swizzle atoms need a 1024-byte aligned base (the launch adds 1 KB slack)
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
     uint8_t *As = sm;                                // NA x KB x [128 rows x 128 B]
-    uint8_t *Bs = As + NA * AB;                      // P x KB x [Np rows x 128 B]
-    float *cn = reinterpret_cast<float *>(Bs + static_cast<size_t>(P) * KB * Np * 128);  // Np + 32
+    uint8_t *Ax = As + NA * AB;                      // NA x extra K block of the tokens (4 KB)
+    uint8_t *Bs = Ax + NA * 4096;                    // P x KB x [Np rows x 128 B]
+    uint8_t *Bx = Bs + static_cast<size_t>(P) * KB * Np * 128;  // extra K block of the centroids
     __shared__ uint64_t bar_mma[2], bar_a[NA], bar_drain;
     __shared__ uint32_t tmem_base;
     __shared__ float xs[kAssignGroups][128][2];  // each warp group's two best scores per row
     __shared__ int xk[kAssignGroups][128][2];    // ... and their clusters
-    __shared__ float red[kAssignThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = warp >> 2;       // warp group: 32-column chunks grp, grp + G, ... (G groups)
     const int h = blockIdx.y;
@@ -194,12 +214,14 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         umma::mbar_init(&bar_mma[0], 1);
         umma::mbar_init(&bar_mma[1], 1);
         umma::mbar_init(&bar_drain, 1);
-        for (int i = 0; i < NA; ++i) umma::mbar_init(&bar_a[i], kAssignThreads);
+        for (int i = 0; i < NA; ++i) umma::mbar_init(&bar_a[i], 2 * kAssignThreads);
         umma::fence_barrier_init();
     }
     __syncthreads();
 
-    // token tile k -> buffer k % NA; each thread's copies arrive on bar_a once done
+    // token tile k -> buffer k % NA: each thread's copies arrive on bar_a once
+    // done, and each thread arrives once more after its part of the extra K
+    // block (core matrix layout: row r, K half kh at (r/8)*256 + kh*128 + (r%8)*16)
     auto load_tile = [&](int k) {
         const int n0 = (t0 + k * tstep) * 128;
         uint8_t *dst = As + (k % NA) * AB;
@@ -211,6 +233,19 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
                              g + (static_cast<size_t>(in ? n0 + r : 0) * H + h) * D + ci * 8, in);
         }
         umma::cp_async_arrive_noinc(&bar_a[k % NA]);
+        if (tid < 256) {
+            const int r = tid >> 1, kh = tid & 1;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (kh == 0) {
+                const float xh = n0 + r < N ? 0.5f * xnorm[static_cast<size_t>(h) * N + n0 + r] : 0.0f;
+                uint16_t p0, p1, p2;
+                split3(-xh, p0, p1, p2);
+                v = make_uint4(bf16pair(kBf16MinusOne, kBf16MinusOne), bf16pair(kBf16MinusOne, p0), bf16pair(p1, p2), 0u);
+            }
+            *reinterpret_cast<uint4 *>(Ax + (k % NA) * 4096 + (r >> 3) * 256 + kh * 128 + (r & 7) * 16) = v;
+            umma::fence_proxy_async_smem();
+        }
+        umma::mbar_arrive(&bar_a[k % NA]);
     };
 
     // centroids (or weighted hi/lo pair) -> swizzled K-major bf16, once
@@ -255,15 +290,19 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         }
     }
     for (int k = 0; k < NA - 1 && k < my_tiles; ++k) load_tile(k);
-    // padded columns score +inf; the largest real norm bounds the score error
-    float cm = 0.0f;
-    for (int i = tid; i < Np + 32; i += kAssignThreads) {
-        const float v = i < Ce ? cnorm[h * C + i] : INFINITY;
-        cn[i] = v;
-        if (i < Ce) cm = fmaxf(cm, v);
+    // extra K block of the centroids; padded columns get a huge norm (f far
+    // below any real column)
+    for (int i = tid; i < 2 * Np; i += kAssignThreads) {
+        const int c = i >> 1, kh = i & 1;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (kh == 0) {
+            const float nrm = c < Ce ? cnorm[h * C + c] : 2.0e38f;
+            uint16_t p0, p1, p2;
+            split3(0.5f * nrm, p0, p1, p2);
+            v = make_uint4(bf16pair(p0, p1), bf16pair(p2, kBf16One), bf16pair(kBf16One, kBf16One), 0u);
+        }
+        *reinterpret_cast<uint4 *>(Bx + (c >> 3) * 256 + kh * 128 + (c & 7) * 16) = v;
     }
-    for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-    if (lane == 0) red[warp] = cm;
     // the centroid copies form the only committed group; the token tiles are
     // tracked by their mbarriers instead
     umma::cp_async_wait_group<0>();
@@ -271,9 +310,6 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
     umma::tc_fence_before();
     __syncthreads();
     umma::tc_fence_after();
-    float cmax2 = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kAssignThreads / 32; ++i) cmax2 = fmaxf(cmax2, red[i]);
     const uint32_t tmem = tmem_base;
     const uint32_t idesc = umma::idesc_f16(128, Np, 1);
     const uint32_t b0 = umma::smem_u32(Bs);
@@ -287,6 +323,8 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
                 const uint64_t bd = umma::desc_sw128(b0 + (p * KB + (s >> 2)) * Np * 128 + (s & 3) * 32);
                 umma::mma_f16(tmem + (k & 1) * ncols, ad, bd, idesc, (p | s) != 0);
             }
+        umma::mma_f16(tmem + (k & 1) * ncols, umma::desc_noswz(umma::smem_u32(Ax + (k % NA) * 4096), 128, 256),
+                      umma::desc_noswz(umma::smem_u32(Bx), 128, 256), idesc, 1u);
         umma::mma_commit(&bar_mma[k & 1]);
     };
     bool ok = true;
@@ -320,44 +358,54 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         umma::tc_fence_after();
         const int r = (warp & 3) * 32 + lane;
         const uint8_t *Ab = As + buf * AB;
+        // ||x||_w^2 of the row this lane finishes later (issued before the scan)
+        const int fr = 8 * warp + (lane & 7), fn = t * 128 + fr;
+        const float xn_pre = (lane < 8 && fn < N) ? xnorm[static_cast<size_t>(h) * N + fn] : 0.0f;
+        uint32_t b1[4], b2[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) b1[q] = b2[q] = 0xffffffffu;
+        if (ok) {
+            // a thread's columns: chunk m = 0, 1 of 32 at grp*32 + 128 m (Np <= 256);
+            // both loads in flight before the one wait
+            const uint32_t trow = tmem + (k & 1) * ncols + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            const int ca0 = grp * 32, ca1 = grp * 32 + 128;
+            uint32_t acc[2][32];
+            if (ca0 < Np) umma::tmem_ld32(trow + ca0, acc[0]);
+            if (ca1 < Np) umma::tmem_ld32(trow + ca1, acc[1]);
+            umma::tmem_ld_wait_regs(acc[0]);
+            umma::reg_fence32(acc[1]);
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int c0 = m ? ca1 : ca0;
+                if (c0 >= Np) continue;
+                // columns past Np were not written by the MMA: masked in a partial chunk
+                const bool full = c0 + 32 <= Np;
+#pragma unroll
+                for (int kk = 0; kk < 32; ++kk) {
+                    uint32_t key = (acc[m][kk] & ~0xfu) | static_cast<uint32_t>((m << 3) | (kk >> 2));
+                    if (!full && c0 + kk >= Np) key = 0xffffffffu;
+                    const uint32_t hi = max(b1[kk & 3], key);
+                    b1[kk & 3] = min(b1[kk & 3], key);
+                    b2[kk & 3] = min(b2[kk & 3], hi);
+                }
+            }
+        }
+        // keys -> (d, cluster): d = -2 f; an empty slot scores +inf
         float bv[4], sv[4];
         int bi[4], si[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            bv[q] = sv[q] = INFINITY;
-            bi[q] = si[q] = 0x7fffffff;
-        }
-        if (ok) {
-            for (int c0 = grp * 32; c0 < Np; c0 += 32 * kAssignGroups) {
-                uint32_t acc[32];
-                umma::tmem_ld32(tmem + (k & 1) * ncols + (static_cast<uint32_t>((warp & 3) * 32) << 16) + c0, acc);
-                umma::tmem_ld_wait_regs(acc);
-                const float4 *cn4 = reinterpret_cast<const float4 *>(cn + c0);
-                // columns past Np were not written by the MMA: masked in a partial chunk
-                const bool full = c0 + 32 <= Np;
-#pragma unroll
-                for (int k4 = 0; k4 < 8; ++k4) {
-                    const float4 cv = cn4[k4];
-                    const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int kk = 4 * k4 + e, c = c0 + kk;
-                        float sc = fmaf(-2.0f, __uint_as_float(acc[kk]), cc[e]);
-                        if (!full && c >= Np) sc = INFINITY;
-                        if (sc < sv[e]) {
-                            if (sc < bv[e]) {
-                                sv[e] = bv[e];
-                                si[e] = bi[e];
-                                bv[e] = sc;
-                                bi[e] = c;
-                            } else {
-                                sv[e] = sc;
-                                si[e] = c;
-                            }
-                        }
-                    }
+            auto dec = [&](uint32_t key, float &d, int &c) {
+                if (key == 0xffffffffu) {
+                    d = INFINITY;
+                    c = 0x7fffffff;
+                } else {
+                    d = -2.0f * __uint_as_float(key & ~0xfu);
+                    c = grp * 32 + 128 * static_cast<int>((key >> 3) & 1u) + 4 * static_cast<int>(key & 7u) + q;
                 }
-            }
+            };
+            dec(b1[q], bv[q], bi[q]);
+            dec(b2[q], sv[q], si[q]);
         }
 #pragma unroll
         for (int q = 1; q < 4; ++q) merge2(bv[0], bi[0], sv[0], si[0], bv[q], bi[q], sv[q], si[q]);
@@ -368,7 +416,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         __syncthreads();
         // finalisation: warp W takes rows 8W .. 8W+7, lane l < 8 merges row 8W + l
         {
-            const int fr = 8 * warp + (lane & 7), n = t * 128 + fr;
+            const int n = fn;
             float b1 = xs[0][fr][0], b2 = xs[0][fr][1];
             int a1 = xk[0][fr][0], a2 = xk[0][fr][1];
 #pragma unroll
@@ -393,25 +441,9 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
             float wl[E];
 #pragma unroll
             for (int e = 0; e < E; ++e) wl[e] = w ? w[h * D + j0 + e] : 1.0f;
-            float xn = 0.0f;
-            if (xmode == 0) {
-                if (lane < 8 && n < N) xn = xnorm[static_cast<size_t>(h) * N + n];
-            } else {
-                // ||x||_w^2 of the warp's 8 rows: D/32 channels per lane, xor-butterfly sum
-#pragma unroll 1
-                for (int l = 0; l < 8; ++l) {
-                    float xv[E];
-                    ld_row(Ab, 16384, 8 * warp + l, xv);
-                    float sx = 0.0f;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) sx = fmaf(wl[e] * xv[e], xv[e], sx);
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
-                    if (lane == l) xn = sx;
-                }
-                if (lane < 8 && n < N) xnorm[static_cast<size_t>(h) * N + n] = xn;
-            }
-            const bool flag = ok && lane < 8 && n < N && arg2 >= 0 && !(b2 - b1 > kAssignTau * (xn + cmax2));
+            const float xn = xn_pre;
+            const bool flag = ok && lane < 8 && n < N && arg2 >= 0 &&
+                              !(b2 - b1 > kAssignTau * (3.0f * xn + fmaxf(b1, 0.0f) + fmaxf(b2, 0.0f)));
             // warp-cooperative exact re-scoring of the flagged rows
             unsigned m = __ballot_sync(0xffffffffu, flag);
             while (m) {
@@ -775,18 +807,17 @@ qvg_status launch_centroid_norms(const uint16_t *cent, size_t hs, int H, int C, 
 
 template <int D, int P>
 static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t *cent, size_t hs, int Ce,
-                                 const float *cnorm, int C, const float *w, float *xnorm, int xmode, int32_t *ids,
+                                 const float *cnorm, int C, const float *w, const float *xnorm, int32_t *ids,
                                  cudaStream_t st) {
     const int Np = std::max(16, ceil_div(Ce, 16) * 16);
     constexpr int KB = D / 64, NA = P == 1 ? 3 : 2;
-    // cn holds Np + 32 floats: a 32-column chunk may extend past Np
-    const size_t smem = NA * static_cast<size_t>(KB) * 128 * 128 + static_cast<size_t>(P) * KB * Np * 128 +
-                        (Np + 32) * 4 + 1024;
+    const size_t smem = NA * (static_cast<size_t>(KB) * 128 * 128 + 4096) + static_cast<size_t>(P) * KB * Np * 128 +
+                        static_cast<size_t>(Np) * 32 + 1024;
     static bool attr = false;
     if (!attr) {
         // the largest request of this instantiation (Np = 256)
-        const size_t most = NA * static_cast<size_t>(KB) * 128 * 128 +
-                            static_cast<size_t>(P) * KB * QVG_MAX_CLUSTERS * 128 + (QVG_MAX_CLUSTERS + 32) * 4 + 1024;
+        const size_t most = NA * (static_cast<size_t>(KB) * 128 * 128 + 4096) +
+                            static_cast<size_t>(P) * KB * QVG_MAX_CLUSTERS * 128 + QVG_MAX_CLUSTERS * 32 + 1024;
         const cudaError_t e = cudaFuncSetAttribute(k_kmeans_assign_tc<D, P>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(most));
@@ -803,19 +834,54 @@ static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t
     const int per_head = std::max(1, std::min(n_tiles, sm_count() / std::max(1, H)));
     dim3 grid(per_head, H);
     k_kmeans_assign_tc<D, P><<<grid, kAssignThreads, smem, st>>>(g, N, H, cent, hs, Ce, Np, cnorm, C, w, xnorm,
-                                                                 xmode, ids, device_error_word());
+                                                                 ids, device_error_word());
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }
 
 qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d, const uint16_t *cent,
                                 size_t hs, int Ce, const float *cnorm, int C, const float *w,
-                                float *xnorm, int xmode, int32_t *ids, cudaStream_t st) {
+                                const float *xnorm, int32_t *ids, cudaStream_t st) {
     if (d == 64)
-        return w ? assign_tc_impl<64, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, xmode, ids, st)
-                 : assign_tc_impl<64, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, xmode, ids, st);
-    return w ? assign_tc_impl<128, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, xmode, ids, st)
-             : assign_tc_impl<128, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, xmode, ids, st);
+        return w ? assign_tc_impl<64, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, ids, st)
+                 : assign_tc_impl<64, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, ids, st);
+    return w ? assign_tc_impl<128, 2>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, ids, st)
+             : assign_tc_impl<128, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, ids, st);
+}
+
+// ||x||_w^2 per (token, head) row of the clustering operand: one warp per row,
+// D/32 consecutive channels per lane (fp32, ascending), xor-butterfly sum.
+template <int D>
+__global__ void __launch_bounds__(256) k_row_norms(const uint16_t *__restrict__ g, int N, int H,
+                                                   const float *__restrict__ w, float *__restrict__ xnorm) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= static_cast<long long>(N) * H) return;
+    const int n = static_cast<int>(row / H), h = static_cast<int>(row % H);
+    float v[E];
+    RowLoad<uint16_t>::template load<E>(g + static_cast<size_t>(row) * D + lane * E, v);
+    float sx = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float wj = w ? w[h * D + lane * E + e] : 1.0f;
+        sx = fmaf(wj * v[e], v[e], sx);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+    if (lane == 0) xnorm[static_cast<size_t>(h) * N + n] = sx;
+}
+
+qvg_status launch_row_norms(const uint16_t *g, int N, int H, int d, const float *w, float *xnorm,
+                            cudaStream_t st) {
+    const long long rows = static_cast<long long>(N) * H;
+    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    if (d == 64)
+        k_row_norms<64><<<blocks, 256, 0, st>>>(g, N, H, w, xnorm);
+    else
+        k_row_norms<128><<<blocks, 256, 0, st>>>(g, N, H, w, xnorm);
+    QVG_LAUNCH_CHECK();
+    return QVG_OK;
 }
 
 qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int d,

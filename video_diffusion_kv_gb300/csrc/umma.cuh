@@ -168,6 +168,20 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t smem_addr, uint32_t l
     return d;
 }
 
+// Shared-memory matrix descriptor without swizzle, K-major: the operand is
+// made of 8-row x 16-byte core matrices, each stored as 128 contiguous bytes
+// (row i of the core matrix at byte 16 i); `lbo` is the byte distance
+// between the two core matrices adjacent along K (a K=16 step of 16-bit
+// elements spans two), `sbo` the distance between 8-row groups.
+__device__ __forceinline__ uint64_t desc_noswz(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;  // version; layout type 0 = no swizzle
+    return d;
+}
+
 // Instruction descriptor, kind::f16: D fp32, A and B both fp16 (ab = 0) or
 // both bf16 (ab = 1), both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t ab) {
