@@ -541,15 +541,18 @@ template <> struct RowLoad<float> {
 // ---------------------------------------------------------------------------
 // Update, one kernel: each CTA (kUpdSplit per head) first orders the head's
 // token indices by cluster in shared memory, stably (ascending token index
-// inside each cluster): per-cluster counts, an exclusive scan, then rounds of
-// 1024 tokens in which each token's place is its cluster's running offset
-// plus the number of earlier same-cluster tokens of the round (warp match +
-// popc inside a warp, per-warp counts across warps).  Then one warp per
-// cluster of the CTA's share sums the members' stage input in that order
-// (fp32, eight row loads in flight), divides by the count, rounds to bf16
-// and writes the centroid and its weighted norm; an empty cluster keeps its
-// centroid.  Deterministic, with no atomic accumulation of values.  A
-// diagonal weight leaves the minimiser at the plain mean.
+// inside each cluster).  Warp w owns a contiguous range of tokens: pass 1
+// counts its tokens per cluster (warp match: the lowest lane of each group of
+// equal ids adds the group size), pass 2 turns the per-warp counts of each
+// cluster into offsets (earlier warps first) and scans the cluster totals,
+// pass 3 walks the range again and places each token at its cluster's start
+// + the offset of its warp + its rank among the earlier equal ids of the
+// warp.  Then one warp per cluster of the CTA's share sums the members' stage
+// input in that order (fp32, eight row loads in flight), divides by the
+// count, rounds to bf16 and writes the centroid and its weighted norm; an
+// empty cluster keeps its centroid.  Deterministic, with no atomic
+// accumulation of values.  A diagonal weight leaves the minimiser at the
+// plain mean.
 constexpr int kUpdThreads = 1024;
 constexpr int kUpdSplit = 4;  // CTAs per head, each finalising a quarter of the clusters
 
@@ -562,16 +565,34 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
     constexpr int W = kUpdThreads / 32;
     constexpr int E = D / 32;
     extern __shared__ __align__(16) uint16_t order[];          // [N] token indices, by cluster
-    __shared__ int cnt[QVG_MAX_CLUSTERS + 1];
-    __shared__ int run[QVG_MAX_CLUSTERS];
-    __shared__ int wc[W][QVG_MAX_CLUSTERS];                   // per-warp counts of a round
+    __shared__ int cnt[QVG_MAX_CLUSTERS + 1];                   // cluster start positions
+    __shared__ int wc[W][QVG_MAX_CLUSTERS];                    // per-warp counts, then offsets
     const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t *hid = ids + static_cast<size_t>(h) * N;
-    for (int c = tid; c <= Ce; c += kUpdThreads) cnt[c] = 0;
+    const int span = ceil_div(ceil_div(N, W), 32) * 32;        // tokens per warp, whole batches
+    const int n_beg = warp * span, n_end = min(N, n_beg + span);
+    for (int i = tid; i < W * QVG_MAX_CLUSTERS; i += kUpdThreads) (&wc[0][0])[i] = 0;
     __syncthreads();
-    for (int n = tid; n < N; n += kUpdThreads) atomicAdd(&cnt[hid[n]], 1);
+    // pass 1: per-warp counts
+    for (int b0 = n_beg; b0 < n_end; b0 += 32) {
+        const int n = b0 + lane;
+        const int c = n < n_end ? hid[n] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, c);
+        if (c >= 0 && (peers & ((1u << lane) - 1u)) == 0) wc[warp][c] += __popc(peers);
+        __syncwarp();
+    }
     __syncthreads();
-    // exclusive scan of the counts by warp 0 (Ce <= 256: 8 per lane)
+    // pass 2: per-cluster offsets of the warps, then the exclusive scan of the totals
+    if (tid < Ce) {
+        int run = 0;
+        for (int w2 = 0; w2 < W; ++w2) {
+            const int t = wc[w2][tid];
+            wc[w2][tid] = run;
+            run += t;
+        }
+        cnt[tid] = run;
+    }
+    __syncthreads();
     if (warp == 0) {
         int v[8], tot = 0;
 #pragma unroll
@@ -590,38 +611,24 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int c = lane * 8 + i;
-            if (c < Ce) {
-                run[c] = acc;
-                cnt[c] = acc;  // cnt now holds each cluster's first position
-            }
+            if (c < Ce) cnt[c] = acc;  // each cluster's first position
             acc += v[i];
         }
         if (lane == 31) cnt[Ce] = incl;
     }
     __syncthreads();
-    // stable placement, rounds of 1024 tokens
-    for (int base = 0; base < N; base += kUpdThreads) {
-        for (int i = tid; i < W * Ce; i += kUpdThreads) wc[i / Ce][i % Ce] = 0;
-        __syncthreads();
-        const int n = base + tid;
-        const int c = n < N ? hid[n] : -1;
+    // pass 3: placement in token order
+    for (int b0 = n_beg; b0 < n_end; b0 += 32) {
+        const int n = b0 + lane;
+        const int c = n < n_end ? hid[n] : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, c);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        if (c >= 0 && rank == 0) wc[warp][c] = __popc(peers);
-        __syncthreads();
-        if (c >= 0) {
-            int before = 0;
-            for (int w2 = 0; w2 < warp; ++w2) before += wc[w2][c];
-            order[run[c] + before + rank] = static_cast<uint16_t>(n);
-        }
-        __syncthreads();
-        for (int cc = tid; cc < Ce; cc += kUpdThreads) {
-            int t = 0;
-            for (int w2 = 0; w2 < W; ++w2) t += wc[w2][cc];
-            run[cc] += t;
-        }
-        __syncthreads();
+        const unsigned before = peers & ((1u << lane) - 1u);
+        if (c >= 0) order[cnt[c] + wc[warp][c] + __popc(before)] = static_cast<uint16_t>(n);
+        __syncwarp();
+        if (c >= 0 && before == 0) wc[warp][c] += __popc(peers);
+        __syncwarp();
     }
+    __syncthreads();
     // this CTA's clusters: one warp each, members summed in token order
     for (int c = blockIdx.x + kUpdSplit * warp; c < Ce; c += kUpdSplit * W) {
         const int beg = cnt[c], end = cnt[c + 1];
