@@ -554,7 +554,7 @@ template <> struct RowLoad<float> {
 // accumulation of values.  A diagonal weight leaves the minimiser at the
 // plain mean.
 constexpr int kUpdThreads = 1024;
-constexpr int kUpdSplit = 4;  // CTAs per head, each finalising a quarter of the clusters
+constexpr int kUpdSplit = 8;  // CTAs per head, each finalising an eighth of the clusters
 
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__restrict__ xin, int N, int H,
