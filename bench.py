@@ -33,6 +33,25 @@ UNIT = "tok/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# DRAM bytes (read + write) of one k_attention_ws launch of the bench
+# workload, from an ncu capture of `dram__bytes_read.sum,dram__bytes_write.sum`
+# (profiles/k_attention_ws_longcat_8chunks.md), keyed by the SHA-256 of the
+# kernel's sources so that a changed kernel reports null until re-measured.
+ATTN_SOURCES = ("attention_ws.cu", "umma.cuh", "common.cuh")
+ATTN_TRAFFIC = {
+    "86ed491b7c939949769afcc083928cf41f8f480d36042558589f4d1144074b13": 80417280 + 4183808,
+}
+
+
+def _attn_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ATTN_SOURCES:
+        with open(os.path.join(ROOT, "video_diffusion_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -218,8 +237,9 @@ def launches_per_compress(p):
     """Kernels one qvg_compress_chunk call launches (see csrc/api.cu)."""
     per_stage = 1  # residual quantise (+ pack, stage residual, PSAC)
     if p.C > 0:
-        # init with norms (or norms of given centroids), iters x (assign, update), final assign
-        per_stage += 1 + 2 * p.iters + 1
+        # row norms, init with norms (or norms of given centroids), iters x (assign, update),
+        # final assign
+        per_stage += 1 + 1 + 2 * p.iters + 1
     return per_stage * p.L + 1  # + chunk table
 
 
@@ -358,7 +378,7 @@ def run_own(args):
         "attention": {"ms": ms_attn, "tok/s": w.Nq / (ms_attn / 1e3), "TFLOP/s": achieved},
         "roofline": {"kernel": "k_attention_ws", "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
-                     "traffic": None,
+                     "traffic": ATTN_TRAFFIC.get(_attn_source_hash()),
                      "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json); fp16 runs at the same rate" % peak_src,
                      "mma_flops_per_algorithmic_flop": 1.0},
         "clocks": clk,
