@@ -60,6 +60,15 @@ __device__ __forceinline__ void raise_error(int *err, int code) {
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Programmatic dependent launch (launch_pdl below): a kernel may run its
+// prologue while the previous kernel of the stream finishes; pdl_wait()
+// blocks until that kernel has completed and its writes are visible (a no-op
+// for a normal launch), pdl_trigger() lets the next kernel start its own
+// prologue.  Kernels here trigger only after their own wait, so two kernels
+// back in the stream have always completed when a kernel starts.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace qvg
 
 // ---- host-side launch plumbing (internal, not part of the ABI) ------------
@@ -80,6 +89,23 @@ void note_cuda_error(cudaError_t e);
     } while (0)
 
 namespace qvg {
+
+// Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Device address of this device's error word (looked up once per device).
 int *device_error_word();

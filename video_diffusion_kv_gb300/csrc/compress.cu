@@ -121,16 +121,18 @@ __global__ void k_centroid_norms(const uint16_t *__restrict__ cent, size_t hs, i
 // first as well.  The chains and groups are merged in (score, index) order,
 // ties to the lower cluster; each warp then finishes 8 rows.
 //
-// Exactness: the tensor-core sum (<= 2^-16 of the sum of |terms|, products
-// exact), the hi/lo split (2^-18), the norm splits (2^-24) and the key
-// truncation (2^-19 |f|) bound the error of d_c, with sum w|x c| <=
-// ||x||_w ||c||_w <= (||x||_w^2 + ||c||_w^2) / 2, by
-//   E_c <= 2^-14 (||x||_w^2 + ||c||_w^2) <= 2^-14 (3 ||x||_w^2 + 2 d_c),
-// since ||c||_w <= ||x||_w + sqrt(d_c).  The computed best b is the exact
-// argmin (no tie possible) when d_c - d_b > E_c + E_b for every other c; that
-// margin grows with d_c, so the second best s decides it, and with a factor
-// two to spare the test is
-//   d_s - d_b > 2^-12 (3 ||x||_w^2 + d_s + d_b).
+// Exactness: the tensor core sums K = D + 16 exact products in steps of 16,
+// so the fp32 accumulation makes at most ~25 roundings of at most 2^-23
+// (truncation) each, <= 2^-18 of the sum of |terms|; the hi/lo split of w*c
+// adds 2^-18 (QSAC), the norm splits 2^-24 and the key truncation 2^-19 |f|.
+// With sum w|x c| <= ||x||_w ||c||_w <= (||x||_w^2 + ||c||_w^2) / 2 this
+// bounds the error of d_c = -2 f_c by
+//   E_c <= 2^-16 (||x||_w^2 + ||c||_w^2) <= 2^-16 (3 ||x||_w^2 + 2 d_c)
+// (2^-15 with QSAC), since ||c||_w <= ||x||_w + sqrt(d_c).  The computed
+// best b is the exact argmin (no tie possible) when d_c - d_b > E_c + E_b
+// for every other c; that margin grows with d_c, so the second best s
+// decides it, and with a factor two to spare the test is
+//   d_s - d_b > tau (3 ||x||_w^2 + d_s + d_b),  tau = 2^-14 (2^-13 with QSAC).
 // Otherwise the two candidates are re-scored with the direct sum: the 32
 // lanes of a warp each take D/32 consecutive channels of the row (fp32,
 // ascending), the partial sums are added by an xor butterfly, and the smaller
@@ -141,7 +143,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 
 constexpr int kAssignThreads = 512;
 constexpr int kAssignGroups = kAssignThreads / 128;  // warp groups sharing the columns
-constexpr float kAssignTau = 1.0f / 4096.0f;
+constexpr float kAssignTau = 1.0f / 16384.0f;  // doubled with QSAC
 
 // v = p0 + p1 + p2 in bf16 parts (each the rounding of what is left)
 __device__ __forceinline__ void split3(float v, uint16_t &p0, uint16_t &p1, uint16_t &p2) {
@@ -248,6 +250,11 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         umma::mbar_arrive(&bar_a[k % NA]);
     };
 
+    // before the previous kernel (the centroid update) has finished: only the
+    // token tiles (this stage's input, written earlier) and their norms
+    for (int k = 0; k < NA - 1 && k < my_tiles; ++k) load_tile(k);
+    pdl_wait();
+    pdl_trigger();
     // centroids (or weighted hi/lo pair) -> swizzled K-major bf16, once
     if constexpr (P == 1) {
 #pragma unroll 4
@@ -289,7 +296,6 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
             *reinterpret_cast<uint4 *>(Bs + static_cast<size_t>(KB) * Np * 128 + off) = v2;
         }
     }
-    for (int k = 0; k < NA - 1 && k < my_tiles; ++k) load_tile(k);
     // extra K block of the centroids; padded columns get a huge norm (f far
     // below any real column)
     for (int i = tid; i < 2 * Np; i += kAssignThreads) {
@@ -303,8 +309,9 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         }
         *reinterpret_cast<uint4 *>(Bx + (c >> 3) * 256 + kh * 128 + (c & 7) * 16) = v;
     }
-    // the centroid copies form the only committed group; the token tiles are
-    // tracked by their mbarriers instead
+    // the centroid copies (and the earlier token-tile copies, which the
+    // commit sweeps into the same group) have landed; the tiles' mbarriers
+    // count them as well
     umma::cp_async_wait_group<0>();
     umma::fence_proxy_async_smem();
     umma::tc_fence_before();
@@ -359,8 +366,8 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         const int r = (warp & 3) * 32 + lane;
         const uint8_t *Ab = As + buf * AB;
         // ||x||_w^2 of the row this lane finishes later (issued before the scan)
-        const int fr = 8 * warp + (lane & 7), fn = t * 128 + fr;
-        const float xn_pre = (lane < 8 && fn < N) ? xnorm[static_cast<size_t>(h) * N + fn] : 0.0f;
+        const int fr = 8 * warp + (lane >> 2), fn = t * 128 + fr;
+        const float xn_pre = fn < N ? xnorm[static_cast<size_t>(h) * N + fn] : 0.0f;
         uint32_t b1[4], b2[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) b1[q] = b2[q] = 0xffffffffu;
@@ -414,13 +421,19 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         xk[grp][r][0] = bi[0];
         xk[grp][r][1] = si[0];
         __syncthreads();
-        // finalisation: warp W takes rows 8W .. 8W+7, lane l < 8 merges row 8W + l
+        // finalisation: warp W takes rows 8W .. 8W+7; the four lanes 4l .. 4l+3
+        // hold the four groups' pairs of row 8W + l and merge them by xor
+        // shuffles, so every lane ends with the row's two best
         {
-            const int n = fn;
-            float b1 = xs[0][fr][0], b2 = xs[0][fr][1];
-            int a1 = xk[0][fr][0], a2 = xk[0][fr][1];
+            const int gq = lane & 3, n = fn;
+            float b1 = xs[gq][fr][0], b2 = xs[gq][fr][1];
+            int a1 = xk[gq][fr][0], a2 = xk[gq][fr][1];
 #pragma unroll
-            for (int gq = 1; gq < kAssignGroups; ++gq) merge2(b1, a1, b2, a2, xs[gq][fr][0], xk[gq][fr][0], xs[gq][fr][1], xk[gq][fr][1]);
+            for (int o = 1; o <= 2; o <<= 1) {
+                const float ob1 = __shfl_xor_sync(0xffffffffu, b1, o), ob2 = __shfl_xor_sync(0xffffffffu, b2, o);
+                const int oa1 = __shfl_xor_sync(0xffffffffu, a1, o), oa2 = __shfl_xor_sync(0xffffffffu, a2, o);
+                merge2(b1, a1, b2, a2, ob1, oa1, ob2, oa2);
+            }
             int arg = a1 == 0x7fffffff ? 0 : a1;
             const int arg2 = (a2 == 0x7fffffff || !(b2 < INFINITY)) ? -1 : a2;
             const int j0 = lane * E, kb = j0 >> 6, e0 = j0 & 63, c8 = e0 >> 3, boff = (e0 & 7) * 2;
@@ -442,14 +455,15 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
 #pragma unroll
             for (int e = 0; e < E; ++e) wl[e] = w ? w[h * D + j0 + e] : 1.0f;
             const float xn = xn_pre;
-            const bool flag = ok && lane < 8 && n < N && arg2 >= 0 &&
-                              !(b2 - b1 > kAssignTau * (3.0f * xn + fmaxf(b1, 0.0f) + fmaxf(b2, 0.0f)));
+            const bool flag = ok && gq == 0 && n < N && arg2 >= 0 &&
+                              !(b2 - b1 > (P == 1 ? kAssignTau : 2.0f * kAssignTau) *
+                                              (3.0f * xn + fmaxf(b1, 0.0f) + fmaxf(b2, 0.0f)));
             // warp-cooperative exact re-scoring of the flagged rows
             unsigned m = __ballot_sync(0xffffffffu, flag);
             while (m) {
                 const int l = __ffs(m) - 1;
                 m &= m - 1;
-                const int rr = 8 * warp + l;
+                const int rr = 8 * warp + (l >> 2);
                 const int ca = __shfl_sync(0xffffffffu, arg, l), cb = __shfl_sync(0xffffffffu, arg2, l);
                 float xv[E], va[E], vb[E];
                 ld_row(Ab, 16384, rr, xv);
@@ -478,7 +492,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
                 }
                 if (lane == l && (db < da || (db == da && cb < ca))) arg = cb;
             }
-            if (ok && lane < 8 && n < N) ids[static_cast<size_t>(h) * N + n] = arg;
+            if (ok && gq == 0 && n < N) ids[static_cast<size_t>(h) * N + n] = arg;
         }
         // (4) with two buffers, tile k+1's loads were issued in (2): start its MMA
         if (NA == 2 && tid == 0 && k + 1 < my_tiles) {
@@ -572,6 +586,8 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
     const int span = ceil_div(ceil_div(N, W), 32) * 32;        // tokens per warp, whole batches
     const int n_beg = warp * span, n_end = min(N, n_beg + span);
     for (int i = tid; i < W * QVG_MAX_CLUSTERS; i += kUpdThreads) (&wc[0][0])[i] = 0;
+    pdl_wait();  // the assignment that wrote ids has finished
+    pdl_trigger();
     __syncthreads();
     // pass 1: per-warp counts
     for (int b0 = n_beg; b0 < n_end; b0 += 32) {
@@ -840,9 +856,13 @@ static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t
     const int n_tiles = ceil_div(N, 128);
     const int per_head = std::max(1, std::min(n_tiles, sm_count() / std::max(1, H)));
     dim3 grid(per_head, H);
-    k_kmeans_assign_tc<D, P><<<grid, kAssignThreads, smem, st>>>(g, N, H, cent, hs, Ce, Np, cnorm, C, w, xnorm,
-                                                                 ids, device_error_word());
-    QVG_LAUNCH_CHECK();
+    const cudaError_t e = launch_pdl(k_kmeans_assign_tc<D, P>, grid, dim3(kAssignThreads), smem, st, g, N, H, cent,
+                                     hs, Ce, Np, cnorm, C, w, xnorm, ids, device_error_word());
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        note_cuda_error(e);
+        return QVG_ERR_CUDA;
+    }
     return QVG_OK;
 }
 
@@ -909,8 +929,13 @@ qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int
             }                                                                                               \
             attr = true;                                                                                    \
         }                                                                                                   \
-        k_kmeans_update<D_, T_><<<grid, kUpdThreads, smem, st>>>(static_cast<const T_ *>(xin), N, H, ids,   \
-                                                                 cent, hs, Ce, w, cnorm, C);                \
+        const cudaError_t le = launch_pdl(k_kmeans_update<D_, T_>, grid, dim3(kUpdThreads), smem, st,        \
+                                          static_cast<const T_ *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C); \
+        if (le != cudaSuccess) {                                                                            \
+            (void)cudaGetLastError();                                                                       \
+            note_cuda_error(le);                                                                            \
+            return QVG_ERR_CUDA;                                                                            \
+        }                                                                                                   \
     } while (0)
     if (d == 64) {
         if (xin_f32) QVG_UPD(64, float); else QVG_UPD(64, uint16_t);
