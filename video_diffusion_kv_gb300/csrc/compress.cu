@@ -41,6 +41,8 @@ __global__ void k_kmeans_init(const uint16_t *__restrict__ g, int N, int H, int 
                               uint64_t seed, int chunk, int stage, uint16_t *__restrict__ cent,
                               size_t hs, const float *__restrict__ w, float *__restrict__ cnorm) {
     constexpr int E = D / 32;  // channels per lane
+    pdl_wait();
+    pdl_trigger();
     const int h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -699,6 +701,8 @@ __global__ void __launch_bounds__(256) k_residual_quant(
     constexpr int E = D / 32;
     constexpr int NB = D * BITS / 8;  // code bytes per row
     __shared__ float esh[8][D];
+    pdl_wait();  // the final assignment (which reads this stage's operand) has finished
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int lpg = group / E;  // lanes per quantisation group (power of two)
     const int ng = D / group;
@@ -783,6 +787,8 @@ __global__ void __launch_bounds__(256) k_residual_quant(
 
 __global__ void k_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start, int32_t *chunk_len,
                               int32_t *tile_chunk) {
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x == 0) {
         chunk_start[chunk] = slot0;
         chunk_len[chunk] = N;
@@ -809,11 +815,15 @@ qvg_status launch_kmeans_init(const uint16_t *g, int N, int H, int d, int C, int
                               int chunk, int stage, uint16_t *cent, size_t hs, const float *w, float *cnorm,
                               cudaStream_t st) {
     dim3 grid(ceil_div(C, 8), H);
-    if (d == 64)
-        k_kmeans_init<64><<<grid, 256, 0, st>>>(g, N, H, C, Ce, seed, chunk, stage, cent, hs, w, cnorm);
-    else
-        k_kmeans_init<128><<<grid, 256, 0, st>>>(g, N, H, C, Ce, seed, chunk, stage, cent, hs, w, cnorm);
-    QVG_LAUNCH_CHECK();
+    const cudaError_t e = d == 64 ? launch_pdl(k_kmeans_init<64>, grid, dim3(256), 0, st, g, N, H, C, Ce, seed,
+                                               chunk, stage, cent, hs, w, cnorm)
+                                  : launch_pdl(k_kmeans_init<128>, grid, dim3(256), 0, st, g, N, H, C, Ce, seed,
+                                               chunk, stage, cent, hs, w, cnorm);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        note_cuda_error(e);
+        return QVG_ERR_CUDA;
+    }
     return QVG_OK;
 }
 
@@ -882,6 +892,8 @@ template <int D>
 __global__ void __launch_bounds__(256) k_row_norms(const uint16_t *__restrict__ g, int N, int H,
                                                    const float *__restrict__ w, float *__restrict__ xnorm) {
     constexpr int E = D / 32;
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (row >= static_cast<long long>(N) * H) return;
@@ -903,11 +915,13 @@ qvg_status launch_row_norms(const uint16_t *g, int N, int H, int d, const float 
                             cudaStream_t st) {
     const long long rows = static_cast<long long>(N) * H;
     const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-    if (d == 64)
-        k_row_norms<64><<<blocks, 256, 0, st>>>(g, N, H, w, xnorm);
-    else
-        k_row_norms<128><<<blocks, 256, 0, st>>>(g, N, H, w, xnorm);
-    QVG_LAUNCH_CHECK();
+    const cudaError_t e = d == 64 ? launch_pdl(k_row_norms<64>, dim3(blocks), dim3(256), 0, st, g, N, H, w, xnorm)
+                                  : launch_pdl(k_row_norms<128>, dim3(blocks), dim3(256), 0, st, g, N, H, w, xnorm);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        note_cuda_error(e);
+        return QVG_ERR_CUDA;
+    }
     return QVG_OK;
 }
 
@@ -955,14 +969,16 @@ static void rq_dispatch(const void *xin, bool f32, int N, int H, const uint16_t 
                         cudaStream_t st) {
     const int rows = N * H;
     const int blocks = std::min(ceil_div(rows, 8), sm_count() * 16);
+    cudaError_t e;
     if (f32)
-        k_residual_quant<D, BITS, float><<<blocks, 256, 0, st>>>(
-            static_cast<const float *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
-            ids_out, shs, delta_out, gbf_out, U, pp, ps, phs);
+        e = launch_pdl(k_residual_quant<D, BITS, float>, dim3(blocks), dim3(256), 0, st,
+                       static_cast<const float *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
+                       ids_out, shs, delta_out, gbf_out, U, pp, ps, phs);
     else
-        k_residual_quant<D, BITS, uint16_t><<<blocks, 256, 0, st>>>(
-            static_cast<const uint16_t *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
-            ids_out, shs, delta_out, gbf_out, U, pp, ps, phs);
+        e = launch_pdl(k_residual_quant<D, BITS, uint16_t>, dim3(blocks), dim3(256), 0, st,
+                       static_cast<const uint16_t *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
+                       ids_out, shs, delta_out, gbf_out, U, pp, ps, phs);
+    if (e != cudaSuccess) note_cuda_error(e);
 }
 
 qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, int d,
@@ -985,8 +1001,13 @@ qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, in
 
 qvg_status launch_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start, int32_t *chunk_len,
                               int32_t *tile_chunk, cudaStream_t st) {
-    k_chunk_table<<<1, 256, 0, st>>>(chunk, slot0, N, chunk_start, chunk_len, tile_chunk);
-    QVG_LAUNCH_CHECK();
+    const cudaError_t e = launch_pdl(k_chunk_table, dim3(1), dim3(256), 0, st, chunk, slot0, N, chunk_start,
+                                     chunk_len, tile_chunk);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        note_cuda_error(e);
+        return QVG_ERR_CUDA;
+    }
     return QVG_OK;
 }
 
