@@ -243,6 +243,52 @@ def launches_per_compress(p):
     return per_stage * p.L + 1  # + chunk table
 
 
+def kernel_extras(qvg, p, w, kc, vc, q, flush, dev, last, slots_per_chunk, reps=5):
+    """Separately timed kernels on the same cache (outside the step): the
+    decompress of the newest chunk (fp32 and bf16 output) and a decode-like
+    attention point (16 queries over the whole cache), each with its
+    algorithmic bytes and the fraction of the measured HBM peak."""
+    import torch
+    peaks, _ = _peaks()
+    hbm = peaks["hbm_gbs"]
+    nb, ng = w.d * w.bits // 8, w.d // w.group
+    row_bytes = nb + 2 * ng + (1 if w.C > 0 else 0)          # codes + fp16 scales + id, per token and head
+    cent_bytes = w.C * w.d * 2 * w.H                           # one chunk's bf16 centroids (all heads)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    res = {}
+    tok0 = last * slots_per_chunk
+    for name, dt, osz in (("decompress_f32", qvg.QVG_OUT_F32, 4), ("decompress_bf16", qvg.QVG_OUT_BF16, 2)):
+        dout = torch.empty((w.N, w.H, w.d), dtype=torch.float32 if osz == 4 else torch.bfloat16, device=dev)
+        ms = timed(lambda: qvg.decompress(p, kc, tok0, w.N, out_dtype=dt, out=dout))
+        nbytes = w.N * w.H * row_bytes + cent_bytes + w.N * w.H * w.d * osz
+        res[name] = {"ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                     "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm,
+                     "what": "newest chunk of the K cache (%d tokens x %d heads)" % (w.N, w.H)}
+    q16 = q[:16].contiguous()
+    out16 = torch.empty((16, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    ms = timed(lambda: qvg.attention(p, q16, kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out16))
+    nbytes = 2 * (w.tokens * w.H * row_bytes + w.n_chunks * cent_bytes)
+    res["attention_decode16"] = {"ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                                 "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm,
+                                 "what": "16 queries over the whole compressed K and V cache"}
+    assert qvg.get_status() == qvg.QVG_OK
+    return res
+
+
 def run_own(args):
     import numpy as np
     import torch
@@ -318,10 +364,12 @@ def run_own(args):
     ms_attn = statistics.mean(attn)
     status = qvg.get_status()
 
+    extras = kernel_extras(qvg, p, w, kc, vc, q, flush, dev, last, slots_per_chunk) if rank == 0 else {}
+
     if args.no_e2e:
         if rank == 0:
             print(json.dumps({"attention_ms": ms_attn, "compress_ms": ms_comp, "ms_per_step": ms_step,
-                              "device_status": int(status)}), flush=True)
+                              "device_status": int(status), "kernels": extras}), flush=True)
         return 0
     # end-to-end through the public API with host buffers
     pin = lambda a: torch.from_numpy(a).to(torch.bfloat16).pin_memory()
@@ -376,6 +424,7 @@ def run_own(args):
                      "frac_hbm": (in_bytes / (ms_comp / 1e3) / 1e9) / peaks["hbm_gbs"],
                      "gflop": 2.0 * 2 * w.N * w.C * w.d * (w.iters + 1) * w.H / 1e9},
         "attention": {"ms": ms_attn, "tok/s": w.Nq / (ms_attn / 1e3), "TFLOP/s": achieved},
+        "kernels": extras,
         "roofline": {"kernel": "k_attention_ws", "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": ATTN_TRAFFIC.get(_attn_source_hash()),

@@ -135,10 +135,12 @@ qvg_status qvg_workspace_size(const qvg_params *p, int32_t op, int32_t n, int32_
     qvg_status s = check_params(p, d);
     if (s != QVG_OK) return s;
     if (n < 0 || H < 1) return QVG_ERR_INVALID_ARG;
-    (void)Hq;
     switch (op) {
         case QVG_OP_COMPRESS: *bytes = carve_compress(p, n, H, d, nullptr).bytes; return QVG_OK;
-        case QVG_OP_ATTENTION: *bytes = 0; return QVG_OK;
+        case QVG_OP_ATTENTION:
+            if (Hq < 1) return QVG_ERR_INVALID_ARG;
+            *bytes = attention_split_bytes(n, Hq, d, attention_splits(n, Hq, -1));
+            return QVG_OK;
         case QVG_OP_PSAC_BASIS: *bytes = 0; return QVG_OK;
     }
     return QVG_ERR_INVALID_ARG;
@@ -236,8 +238,6 @@ qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq, in
                          const qvg_cache *k, const qvg_cache *v, float scale, void *out,
                          int32_t out_dtype, float *lse, int32_t *top1, void *workspace,
                          size_t ws_bytes, void *stream) {
-    (void)workspace;
-    (void)ws_bytes;
     if (!k || !v || (!q_bf16 && Nq > 0) || (!out && Nq > 0)) return QVG_ERR_INVALID_ARG;
     qvg_status s = check_params(p, k->d);
     if (s != QVG_OK) return s;
@@ -254,8 +254,9 @@ qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq, in
     if (!std::isfinite(scale)) return QVG_ERR_INVALID_ARG;
     const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(k->d));
     const float scale_log2 = sc * 1.4426950408889634f;
+    if (workspace && reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return QVG_ERR_WORKSPACE;
     return launch_attention_ws(p, static_cast<const uint16_t *>(q_bf16), Nq, Hq, k, v, scale_log2, out,
-                               out_dtype, lse, top1, static_cast<cudaStream_t>(stream));
+                               out_dtype, lse, top1, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 qvg_status quantwm_query_stats(const void *q_hist_bf16, int32_t n, int32_t Hq, int32_t H, int32_t d,

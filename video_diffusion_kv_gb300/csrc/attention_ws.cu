@@ -41,6 +41,7 @@ struct AttnWsArgs {
     uint16_t *out16;
     float *lse;
     int32_t *top1;
+    float *best;  // split mode with top-1: each split's best scaled logit
     int *err;
 };
 
@@ -320,18 +321,18 @@ struct Producer {
 // cluster ids run two tiles ahead (slot t * QVG_TILE + r < n_slots <=
 // capacity for every tile t: in bounds).
 template <int D, int BITS>
-__device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer &pr, int h, int r, int n_tiles,
-                                             volatile int *vfail) {
+__device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
+                                             int n_tiles, volatile int *vfail) {
     constexpr int KB = D / 64, TB = KB * 16384;
-    const size_t id_row = static_cast<size_t>(h) * a.cap + r;
+    const size_t id_row = static_cast<size_t>(h) * a.cap + static_cast<size_t>(tb) * QVG_TILE + r;
     TileInfo ti0{}, ti1{};
     int id0 = 0, id1 = 0;
     if (n_tiles > 0) {
-        ti0 = tile_info(a, 0);
+        ti0 = tile_info(a, tb);
         if (a.C > 0) id0 = pr.ids[id_row];
     }
     if (n_tiles > 1) {
-        ti1 = tile_info(a, 1);
+        ti1 = tile_info(a, tb + 1);
         if (a.C > 0) id1 = pr.ids[id_row + QVG_TILE];
     }
     HalfData<BITS> A, B;
@@ -342,7 +343,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         TileInfo ti2{};
         int id2 = 0;
         if (t + 2 < n_tiles) {
-            ti2 = tile_info(a, t + 2);
+            ti2 = tile_info(a, tb + t + 2);
             if (a.C > 0) id2 = pr.ids[id_row + static_cast<size_t>(t + 2) * QVG_TILE];
         }
         const bool valid = r < ti0.nvalid, valid1 = t + 1 < n_tiles && r < ti1.nvalid;
@@ -378,13 +379,13 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
 
 // Several stages and/or PSAC: 8 channels at a time through rebuild8.
 template <int D, int BITS>
-__device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer &pr, int h, int r, int n_tiles,
-                                             volatile int *vfail) {
+__device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
+                                             int n_tiles, volatile int *vfail) {
     constexpr int KB = D / 64, TB = KB * 16384;
     for (int t = 0; t < n_tiles; ++t) {
         const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
         uint8_t *T = pr.buf0 + b * TB + r * 128;
-        const TileInfo ti = tile_info(a, t);
+        const TileInfo ti = tile_info(a, tb + t);
         const bool valid = r < ti.nvalid;
         if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
         float pk[QVG_PSAC_RANK];
@@ -453,7 +454,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hq = blockIdx.y, h = hq / a.grp, q0 = blockIdx.x * 256;
-    const int n_tiles = a.n_slots / QVG_TILE;
+    // split z of gridDim.z takes cache tiles [tb, tb + n_tiles); every barrier
+    // phase below counts tiles from tb
+    const int n_all = a.n_slots / QVG_TILE, z = blockIdx.z;
+    const int tb = static_cast<int>(static_cast<long long>(n_all) * z / gridDim.z);
+    const int n_tiles = static_cast<int>(static_cast<long long>(n_all) * (z + 1) / gridDim.z) - tb;
 
     // Q tiles -> fp16 (exact for bf16 values in fp16's normal range), swizzled K-major
     for (int i = tid; i < 256 * (D / 8); i += kThreads) {
@@ -534,7 +539,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         float m_used = -INFINITY, l_sum = 0.0f, best = -INFINITY;
         int best_slot = 0;
         for (int t = 0; t < n_tiles; ++t) {
-            const TileInfo ti = tile_info(a, t);
+            const TileInfo ti = tile_info(a, tb + t);
             if (live) live = __all_sync(0xffffffffu, ws::wait(&sfull[i], t & 1, vfail));
             float corr = 1.0f;
             if (live) {
@@ -672,7 +677,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 umma::tmem_ld32(tO + c0, v);
                 umma::tmem_ld_wait_regs(v);
                 if (qi < a.Nq) {
-                    const size_t o = (static_cast<size_t>(qi) * a.Hq + hq) * D + c0;
+                    // split z writes its own [Nq][Hq][D] slice (z = 0 without a split)
+                    const size_t o = ((static_cast<size_t>(z) * a.Nq + qi) * a.Hq + hq) * D + c0;
                     if (a.out32) {
 #pragma unroll
                         for (int k = 0; k < 32; k += 4)
@@ -693,8 +699,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 }
             }
             if (qi < a.Nq) {
-                if (a.lse) a.lse[static_cast<size_t>(hq) * a.Nq + qi] = (m_used + log2f(l_sum)) * 0.69314718055994531f;
-                if constexpr (TOP1) a.top1[static_cast<size_t>(hq) * a.Nq + qi] = best_slot;
+                const size_t li = (static_cast<size_t>(z) * a.Hq + hq) * a.Nq + qi;
+                if (a.lse) a.lse[li] = (m_used + log2f(l_sum)) * 0.69314718055994531f;
+                if constexpr (TOP1) {
+                    a.top1[li] = best_slot;
+                    if (a.best) a.best[li] = best;
+                }
             }
         }
         // every MMA this group issued completes before TMEM is released
@@ -709,9 +719,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                           isv ? a.vcent : a.kcent, isv ? Vt0 : Kt, isv ? vfull : &kfull, isv ? vfree : &kfree,
                           isv ? 2 : 1, !isv && a.psac_p != nullptr};
         if (a.L == 1 && !pr.psac)
-            produce_fast<D, BITS>(a, pr, h, tid & 127, n_tiles, vfail);
+            produce_fast<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         else
-            produce_general<D, BITS>(a, pr, h, tid & 127, n_tiles, vfail);
+            produce_general<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
     }
     __syncwarp();
     umma::tc_fence_before();
@@ -723,8 +733,63 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     }
 }
 
+// Split-cache merge: split z produced O_z (normalised, fp32) and its
+// log-sum-exp lse_z over its share of the cache; the whole-cache result is
+// O = sum_z e^{lse_z - m} O_z / sum_z e^{lse_z - m}, lse = m + log sum_z
+// e^{lse_z - m} (m = max_z lse_z), and the top-1 slot is that of the largest
+// best logit (the first split on ties, i.e. the lowest slot).  One warp per
+// (query, query head), lane = D/32 channels.
+template <int D>
+__global__ void __launch_bounds__(256) k_attn_merge(const float *__restrict__ po, const float *__restrict__ plse,
+                                                   const float *__restrict__ pbest, const int32_t *__restrict__ parg,
+                                                   int S, int Nq, int Hq, float *__restrict__ out32,
+                                                   uint16_t *__restrict__ out16, float *__restrict__ lse,
+                                                   int32_t *__restrict__ top1) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= static_cast<long long>(Nq) * Hq) return;
+    const int qi = static_cast<int>(row / Hq), hq = static_cast<int>(row % Hq);
+    float m = -INFINITY;
+    for (int z = 0; z < S; ++z) m = fmaxf(m, plse[(static_cast<size_t>(z) * Hq + hq) * Nq + qi]);
+    float acc[E], den = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+    for (int z = 0; z < S; ++z) {
+        const float wz = expf(plse[(static_cast<size_t>(z) * Hq + hq) * Nq + qi] - m);
+        const float *oz = po + ((static_cast<size_t>(z) * Nq + qi) * Hq + hq) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(wz, oz[e], acc[e]);
+        den += wz;
+    }
+    const float inv = 1.0f / den;
+    const size_t o = (static_cast<size_t>(qi) * Hq + hq) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        if (out32)
+            out32[o + e] = acc[e] * inv;
+        else
+            out16[o + e] = f32_to_bf16(acc[e] * inv);
+    }
+    if (lane == 0) {
+        if (lse) lse[static_cast<size_t>(hq) * Nq + qi] = m + logf(den);
+        if (top1) {
+            float bb = -INFINITY;
+            int arg = 0;
+            for (int z = 0; z < S; ++z) {
+                const size_t li = (static_cast<size_t>(z) * Hq + hq) * Nq + qi;
+                if (pbest[li] > bb) {
+                    bb = pbest[li];
+                    arg = parg[li];
+                }
+            }
+            top1[static_cast<size_t>(hq) * Nq + qi] = arg;
+        }
+    }
+}
+
 template <int D, int BITS, bool TOP1>
-static qvg_status attn_ws_t(const AttnWsArgs &a, cudaStream_t st) {
+static qvg_status attn_ws_t(const AttnWsArgs &a, int a_splits, cudaStream_t st) {
     constexpr size_t smem = 5 * (D / 64) * 16384 + 2 * 32768 + 1024;
     static bool attr = false;
     if (!attr) {
@@ -737,20 +802,53 @@ static qvg_status attn_ws_t(const AttnWsArgs &a, cudaStream_t st) {
         }
         attr = true;
     }
-    dim3 grid(ceil_div(a.Nq, 256), a.Hq);
+    dim3 grid(ceil_div(a.Nq, 256), a.Hq, a_splits);
     k_attention_ws<D, BITS, TOP1><<<grid, ws::kThreads, smem, st>>>(a);
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }
 
 template <int D, int BITS>
-static qvg_status attn_ws(const AttnWsArgs &a, cudaStream_t st) {
-    return a.top1 ? attn_ws_t<D, BITS, true>(a, st) : attn_ws_t<D, BITS, false>(a, st);
+static qvg_status attn_ws(const AttnWsArgs &a, int splits, cudaStream_t st) {
+    return a.top1 ? attn_ws_t<D, BITS, true>(a, splits, st) : attn_ws_t<D, BITS, false>(a, splits, st);
+}
+
+static int attn_sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 152;
+    }
+    return n;
+}
+
+// Number of cache splits: when (query blocks x query heads) CTAs leave SMs
+// idle, each (block, head) pair is split over enough CTAs to reach about two
+// per SM, with at least kMinSplitTiles cache tiles per split, at most
+// kMaxSplits.
+constexpr int kMaxSplits = 32, kMinSplitTiles = 4;
+int attention_splits(int Nq, int Hq, int n_tiles) {
+    const int ctas = ceil_div(std::max(Nq, 1), 256) * Hq;
+    const int sm = attn_sm_count();
+    if (ctas >= sm) return 1;
+    int s = std::min(kMaxSplits, ceil_div(2 * sm, ctas));
+    if (n_tiles >= 0) s = std::min(s, std::max(1, n_tiles / kMinSplitTiles));
+    return std::max(1, s);
+}
+
+size_t attention_split_bytes(int Nq, int Hq, int d, int splits) {
+    if (splits <= 1) return 0;
+    const size_t rows = static_cast<size_t>(splits) * Nq * Hq;
+    // O (fp32, d) + lse + best logit + best slot per (split, query, head), 256-byte aligned parts
+    auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+    return al(rows * d * 4) + 3 * al(rows * 4);
 }
 
 qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, int Hq, const qvg_cache *k,
                                const qvg_cache *v, float scale_log2, void *out, int out_dtype, float *lse,
-                               int32_t *top1, cudaStream_t st) {
+                               int32_t *top1, void *workspace, size_t ws_bytes, cudaStream_t st) {
     AttnWsArgs a{};
     a.q = q;
     a.Nq = Nq;
@@ -785,8 +883,43 @@ qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, i
     a.top1 = top1;
     a.err = device_error_word();
     if (Nq == 0) return QVG_OK;
-    if (k->d == 64) return p->bits == 2 ? attn_ws<64, 2>(a, st) : attn_ws<64, 4>(a, st);
-    return p->bits == 2 ? attn_ws<128, 2>(a, st) : attn_ws<128, 4>(a, st);
+    const int d = k->d;
+    // split the cache over more CTAs when the query blocks alone leave SMs idle
+    // (needs the workspace qvg_workspace_size reports for this Nq, Hq, d)
+    int splits = attention_splits(Nq, Hq, a.n_slots / QVG_TILE);
+    if (splits > 1 && (!workspace || ws_bytes < attention_split_bytes(Nq, Hq, d, splits))) splits = 1;
+    float *po = nullptr, *plse = nullptr, *pbest = nullptr;
+    int32_t *parg = nullptr;
+    if (splits > 1) {
+        const size_t rows = static_cast<size_t>(splits) * Nq * Hq;
+        auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+        char *base = static_cast<char *>(workspace);
+        po = reinterpret_cast<float *>(base);
+        plse = reinterpret_cast<float *>(base + al(rows * d * 4));
+        pbest = reinterpret_cast<float *>(base + al(rows * d * 4) + al(rows * 4));
+        parg = reinterpret_cast<int32_t *>(base + al(rows * d * 4) + 2 * al(rows * 4));
+        a.out32 = po;
+        a.out16 = nullptr;
+        a.lse = plse;
+        a.top1 = top1 ? parg : nullptr;
+        a.best = top1 ? pbest : nullptr;
+    }
+    qvg_status s;
+    if (d == 64)
+        s = p->bits == 2 ? attn_ws<64, 2>(a, splits, st) : attn_ws<64, 4>(a, splits, st);
+    else
+        s = p->bits == 2 ? attn_ws<128, 2>(a, splits, st) : attn_ws<128, 4>(a, splits, st);
+    if (s != QVG_OK || splits == 1) return s;
+    const long long rows = static_cast<long long>(Nq) * Hq;
+    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    float *o32 = out_dtype == QVG_OUT_F32 ? static_cast<float *>(out) : nullptr;
+    uint16_t *o16 = out_dtype == QVG_OUT_BF16 ? static_cast<uint16_t *>(out) : nullptr;
+    if (d == 64)
+        k_attn_merge<64><<<blocks, 256, 0, st>>>(po, plse, pbest, parg, splits, Nq, Hq, o32, o16, lse, top1);
+    else
+        k_attn_merge<128><<<blocks, 256, 0, st>>>(po, plse, pbest, parg, splits, Nq, Hq, o32, o16, lse, top1);
+    QVG_LAUNCH_CHECK();
+    return QVG_OK;
 }
 
 }  // namespace qvg

@@ -142,7 +142,11 @@ qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, 
 qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, int Hq,
                                const qvg_cache *k, const qvg_cache *v, float scale_log2,
                                void *out, int out_dtype, float *lse, int32_t *top1,
-                               cudaStream_t st);
+                               void *workspace, size_t ws_bytes, cudaStream_t st);
+// Cache splits qvg_attention uses for Nq queries x Hq heads (n_tiles < 0:
+// the most any cache length can need), and the workspace they take.
+int attention_splits(int Nq, int Hq, int n_tiles);
+size_t attention_split_bytes(int Nq, int Hq, int d, int splits);
 qvg_status launch_query_stats(const uint16_t *q, int n, int Hq, int H, int d, int accumulate,
                               float *M, float *w, int64_t *count, cudaStream_t st);
 qvg_status launch_psac_basis(const float *M, const int64_t *count, int H, int d, int rank,

@@ -686,11 +686,42 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
 }
 
 // ---------------------------------------------------------------------------
-// Residual quantisation of one stage: one warp per (token, head) row, lane i
-// holding channels [i*E, i*E + E), E = D/32.  Writes codes, fp16 scales and
-// the cluster id; optionally the next stage's input X_{l+1} = X_l - deq (fp32
-// and its bf16 rounding, the next clustering operand); optionally (last stage
-// of a key chunk with PSAC) the INT8 projection of X_{L+1} on the basis U.
+// Residual quantisation of one stage, thread = (token, head) row: a warp
+// takes 32 consecutive tokens of one head (their ids, codes and scales are
+// contiguous), each thread its own row in blocks of 32 channels.  Pass 1
+// takes each group's amax of r = x - c; pass 2 recomputes r, quantises,
+// packs and writes.  Writes codes, fp16 scales and the cluster id;
+// optionally the next stage's input X_{l+1} = X_l - deq (fp32 and its bf16
+// rounding, the next clustering operand); optionally (last stage of a key
+// chunk with PSAC) the INT8 projection of X_{L+1} on the basis U, an fp32
+// FMA chain in ascending channel order.
+template <typename TIn>
+__device__ __forceinline__ void load32(const TIn *p, float (&v)[32]);
+template <>
+__device__ __forceinline__ void load32<uint16_t>(const uint16_t *p, float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p + 8 * i);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[8 * i + 2 * k] = __uint_as_float(w4[k] << 16);
+            v[8 * i + 2 * k + 1] = __uint_as_float(w4[k] & 0xffff0000u);
+        }
+    }
+}
+template <>
+__device__ __forceinline__ void load32<float>(const float *p, float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 u = *reinterpret_cast<const float4 *>(p + 4 * i);
+        v[4 * i] = u.x;
+        v[4 * i + 1] = u.y;
+        v[4 * i + 2] = u.z;
+        v[4 * i + 3] = u.w;
+    }
+}
+
 template <int D, int BITS, typename TIn>
 __global__ void __launch_bounds__(256) k_residual_quant(
     const TIn *__restrict__ xin, int N, int H, const uint16_t *__restrict__ cent, size_t hs, int C,
@@ -698,90 +729,149 @@ __global__ void __launch_bounds__(256) k_residual_quant(
     uint16_t *__restrict__ scales, uint8_t *__restrict__ ids_out, size_t shs,
     float *__restrict__ delta_out, uint16_t *__restrict__ gbf_out, const float *__restrict__ psacU,
     int8_t *__restrict__ psac_p, uint16_t *__restrict__ psac_s, size_t phs) {
-    constexpr int E = D / 32;
-    constexpr int NB = D * BITS / 8;  // code bytes per row
-    __shared__ float esh[8][D];
+    constexpr int NB = D * BITS / 8, CB = 32 * BITS / 8;  // code bytes per row / per 32-channel block
+    constexpr int NG8 = D / 8;                             // 8-channel blocks
     pdl_wait();  // the final assignment (which reads this stage's operand) has finished
     pdl_trigger();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int lpg = group / E;  // lanes per quantisation group (power of two)
-    const int ng = D / group;
-    const int nrows = N * H;
-    for (int row = blockIdx.x * 8 + warp; row < nrows; row += gridDim.x * 8) {
-        const int n = row / H, h = row % H;
-        const int id = C > 0 ? ids[static_cast<size_t>(h) * N + n] : 0;
-        float x[E], c[E], r[E];
-        RowLoad<TIn>::template load<E>(xin + static_cast<size_t>(row) * D + lane * E, x);
-        if (C > 0) {
-            const uint16_t *cr = cent + static_cast<size_t>(h) * hs + static_cast<size_t>(id) * D + lane * E;
+    const int lane = threadIdx.x & 31;
+    const int nblk = ceil_div(N, 32);
+    const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (wid >= static_cast<long long>(H) * nblk) return;
+    const int h = static_cast<int>(wid / nblk), n = static_cast<int>(wid % nblk) * 32 + lane;
+    if (n >= N) return;
+    const int ng = D / group, g8 = group / 8;  // groups per row, 8-channel blocks per group
+    const int id = C > 0 ? ids[static_cast<size_t>(h) * N + n] : 0;
+    const size_t trow = static_cast<size_t>(n) * H + h;  // token-major row of the stage buffers
+    const TIn *xr = xin + trow * D;
+    const uint16_t *cr = C > 0 ? cent + static_cast<size_t>(h) * hs + static_cast<size_t>(id) * D : nullptr;
+    // pass 1: amax of each 8-channel block, then of each group
+    float am8[NG8];
+#pragma unroll 1
+    for (int cb = 0; cb < D / 32; ++cb) {
+        float x[32], c[32];
+        load32<TIn>(xr + cb * 32, x);
+        if (C > 0) load32<uint16_t>(cr + cb * 32, c);
 #pragma unroll
-            for (int e = 0; e < E; ++e) c[e] = bf16_to_f32(cr[e]);
-        }
-        float amax = 0.0f;
+        for (int b8 = 0; b8 < 4; ++b8) {
+            float m = 0.0f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            r[e] = C > 0 ? __fsub_rn(x[e], c[e]) : x[e];
-            amax = fmaxf(amax, fabsf(r[e]));
+            for (int e = 0; e < 8; ++e) {
+                const float r = C > 0 ? __fsub_rn(x[8 * b8 + e], c[8 * b8 + e]) : x[8 * b8 + e];
+                m = fmaxf(m, fabsf(r));
+            }
+            // cb is a loop variable: keep am8 in registers through a static index
+#pragma unroll
+            for (int q = 0; q < NG8 / 4; ++q)
+                if (q == cb) am8[4 * q + b8] = m;
         }
-        for (int o = lpg >> 1; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const uint16_t sb = group_scale_f16(amax, BITS, mode);
+    }
+    float Sp8[NG8];  // the scale each 8-channel block uses
+    const size_t srow = static_cast<size_t>(h) * shs + n;
+#pragma unroll
+    for (int g = 0; g < NG8; ++g) Sp8[g] = 0.0f;
+    for (int gi = 0; gi < ng; ++gi) {
+        float m = 0.0f;
+#pragma unroll
+        for (int g = 0; g < NG8; ++g)
+            if (g / g8 == gi) m = fmaxf(m, am8[g]);
+        const uint16_t sb = group_scale_f16(m, BITS, mode);
+        scales[srow * ng + gi] = sb;
         const float Sp = f16_to_f32(sb);
-        uint32_t packed = 0;
-        float dl[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int q = quant_code(r[e], Sp, BITS);
-            packed |= static_cast<uint32_t>(q + (1 << (BITS - 1))) << (e * BITS);
+        for (int g = 0; g < NG8; ++g)
+            if (g / g8 == gi) Sp8[g] = Sp;
+    }
+    if (ids_out) ids_out[srow] = static_cast<uint8_t>(id);  // no ids without centroids (C = 0)
+    float P[QVG_PSAC_RANK];
+#pragma unroll
+    for (int k = 0; k < QVG_PSAC_RANK; ++k) P[k] = 0.0f;
+    const float *Uh = psacU ? psacU + static_cast<size_t>(h) * D * QVG_PSAC_RANK : nullptr;
+    // pass 2: quantise, pack, residual for the next stage, PSAC projection
+#pragma unroll 1
+    for (int cb = 0; cb < D / 32; ++cb) {
+        float x[32], c[32];
+        load32<TIn>(xr + cb * 32, x);
+        if (C > 0) load32<uint16_t>(cr + cb * 32, c);
+        float Sb[4];
+#pragma unroll
+        for (int b8 = 0; b8 < 4; ++b8) {
+            Sb[b8] = 0.0f;
+#pragma unroll
+            for (int q = 0; q < NG8 / 4; ++q)
+                if (q == cb) Sb[b8] = Sp8[4 * q + b8];
+        }
+        uint32_t pw[CB / 4];
+#pragma unroll
+        for (int k = 0; k < CB / 4; ++k) pw[k] = 0u;
+        float dl[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const float Sp = Sb[e >> 3];
+            const float r = C > 0 ? __fsub_rn(x[e], c[e]) : x[e];
+            const int q = quant_code(r, Sp, BITS);
+            pw[(e * BITS) / 32] |= static_cast<uint32_t>(q + (1 << (BITS - 1))) << ((e * BITS) % 32);
             const float rh = __fmul_rn(Sp, static_cast<float>(q));
             const float deq = C > 0 ? __fadd_rn(rh, c[e]) : rh;
             dl[e] = __fsub_rn(x[e], deq);
         }
-        const size_t srow = static_cast<size_t>(h) * shs + n;
-        uint8_t *crow = codes + srow * NB;
-        constexpr int LANE_BITS = E * BITS;
-        if constexpr (LANE_BITS == 8) {
-            crow[lane] = static_cast<uint8_t>(packed);
-        } else if constexpr (LANE_BITS == 16) {
-            reinterpret_cast<uint16_t *>(crow)[lane] = static_cast<uint16_t>(packed);
-        } else {  // 4 bits per lane: pair lanes into one byte
-            const uint32_t hi = __shfl_down_sync(0xffffffffu, packed, 1);
-            if ((lane & 1) == 0) crow[lane >> 1] = static_cast<uint8_t>(packed | (hi << 4));
-        }
-        if ((lane % lpg) == 0) scales[srow * ng + lane / lpg] = sb;
-        if (lane == 0 && ids_out) ids_out[srow] = static_cast<uint8_t>(id);  // no ids without centroids (C = 0)
+        uint8_t *cdst = codes + srow * NB + cb * CB;
+        if constexpr (CB == 8)
+            *reinterpret_cast<uint2 *>(cdst) = make_uint2(pw[0], pw[1]);
+        else
+            *reinterpret_cast<uint4 *>(cdst) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         if (delta_out) {
+            float4 *dp = reinterpret_cast<float4 *>(delta_out + trow * D + cb * 32);
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                delta_out[static_cast<size_t>(row) * D + lane * E + e] = dl[e];
-                if (gbf_out) gbf_out[static_cast<size_t>(row) * D + lane * E + e] = f32_to_bf16(dl[e]);
-            }
-        }
-        if (psacU) {
-            // P_k = sum_j E_j U[j][k]: fp32 fused multiply-add in ascending j.
+            for (int i = 0; i < 8; ++i) dp[i] = make_float4(dl[4 * i], dl[4 * i + 1], dl[4 * i + 2], dl[4 * i + 3]);
+            if (gbf_out) {
+                uint4 *gp = reinterpret_cast<uint4 *>(gbf_out + trow * D + cb * 32);
 #pragma unroll
-            for (int e = 0; e < E; ++e) esh[warp][lane * E + e] = dl[e];
-            __syncwarp();
-            const float *Uh = psacU + static_cast<size_t>(h) * D * QVG_PSAC_RANK;
-            float P = 0.0f;
-            if (lane < QVG_PSAC_RANK) {
-                for (int j = 0; j < D; ++j) P = fmaf(esh[warp][j], Uh[j * QVG_PSAC_RANK + lane], P);
-            }
-            float pa = lane < QVG_PSAC_RANK ? fabsf(P) : 0.0f;
-            for (int o = 4; o > 0; o >>= 1) pa = fmaxf(pa, __shfl_xor_sync(0xffffffffu, pa, o));
-            const uint16_t psb = f32_to_f16(fminf(__fdiv_rn(pa, 127.0f), 65504.0f));
-            const float pSp = f16_to_f32(psb);
-            if (lane < QVG_PSAC_RANK) {
-                int qp = 0;
-                if (pSp > 0.0f) {
-                    float t = rintf(__fdiv_rn(P, pSp));
-                    t = fminf(fmaxf(t, -127.0f), 127.0f);
-                    qp = static_cast<int>(t);
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        w4[k] = static_cast<uint32_t>(f32_to_bf16(dl[8 * i + 2 * k])) |
+                                (static_cast<uint32_t>(f32_to_bf16(dl[8 * i + 2 * k + 1])) << 16);
+                    gp[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
-                psac_p[(static_cast<size_t>(h) * phs + n) * QVG_PSAC_RANK + lane] = static_cast<int8_t>(qp);
             }
-            if (lane == 0) psac_s[static_cast<size_t>(h) * phs + n] = psb;
-            __syncwarp();
         }
+        if (Uh) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float4 u0 = *reinterpret_cast<const float4 *>(Uh + (cb * 32 + e) * QVG_PSAC_RANK);
+                const float4 u1 = *reinterpret_cast<const float4 *>(Uh + (cb * 32 + e) * QVG_PSAC_RANK + 4);
+                const float de = dl[e];
+                P[0] = fmaf(de, u0.x, P[0]);
+                P[1] = fmaf(de, u0.y, P[1]);
+                P[2] = fmaf(de, u0.z, P[2]);
+                P[3] = fmaf(de, u0.w, P[3]);
+                P[4] = fmaf(de, u1.x, P[4]);
+                P[5] = fmaf(de, u1.y, P[5]);
+                P[6] = fmaf(de, u1.z, P[6]);
+                P[7] = fmaf(de, u1.w, P[7]);
+            }
+        }
+    }
+    if (Uh) {
+        float pa = 0.0f;
+#pragma unroll
+        for (int k = 0; k < QVG_PSAC_RANK; ++k) pa = fmaxf(pa, fabsf(P[k]));
+        const uint16_t psb = f32_to_f16(fminf(__fdiv_rn(pa, 127.0f), 65504.0f));
+        const float pSp = f16_to_f32(psb);
+        uint32_t pq[2] = {0u, 0u};
+#pragma unroll
+        for (int k = 0; k < QVG_PSAC_RANK; ++k) {
+            int qp = 0;
+            if (pSp > 0.0f) {
+                float t = rintf(__fdiv_rn(P[k], pSp));
+                t = fminf(fmaxf(t, -127.0f), 127.0f);
+                qp = static_cast<int>(t);
+            }
+            pq[k >> 2] |= (static_cast<uint32_t>(qp) & 0xffu) << (8 * (k & 3));
+        }
+        *reinterpret_cast<uint2 *>(psac_p + (static_cast<size_t>(h) * phs + n) * QVG_PSAC_RANK) = make_uint2(pq[0], pq[1]);
+        psac_s[static_cast<size_t>(h) * phs + n] = psb;
     }
 }
 
@@ -967,8 +1057,8 @@ static void rq_dispatch(const void *xin, bool f32, int N, int H, const uint16_t 
                         uint16_t *scales, uint8_t *ids_out, size_t shs, float *delta_out,
                         uint16_t *gbf_out, const float *U, int8_t *pp, uint16_t *ps, size_t phs,
                         cudaStream_t st) {
-    const int rows = N * H;
-    const int blocks = std::min(ceil_div(rows, 8), sm_count() * 16);
+    const long long warps = static_cast<long long>(H) * ceil_div(std::max(N, 1), 32);
+    const int blocks = static_cast<int>((warps + 7) / 8);
     cudaError_t e;
     if (f32)
         e = launch_pdl(k_residual_quant<D, BITS, float>, dim3(blocks), dim3(256), 0, st,

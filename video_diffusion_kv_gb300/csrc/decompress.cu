@@ -20,68 +20,107 @@ struct CacheView {
     int H, cap, max_chunks;
 };
 
-// Code of channel j of a packed row.
-template <int BITS>
-__device__ __forceinline__ int code_at(const uint8_t *row, int j) {
-    const uint32_t u = (static_cast<uint32_t>(row[(j * BITS) >> 3]) >> ((j * BITS) & 7)) &
-                       ((1u << BITS) - 1u);
-    return static_cast<int>(u) - (1 << (BITS - 1));
-}
-
-template <int D, int BITS>
+// Thread = token slot: a warp rebuilds 32 consecutive slots of one head
+// (their codes, scales and ids are contiguous), each thread its own row in
+// blocks of 32 channels (the block's codes, scales and centroid piece are
+// loaded before its arithmetic).  Per element, in stage order:
+// acc += fl(fl(S q) + c), then the PSAC term as an fp32 FMA chain over the
+// rank -- the same operations, in the same order, as any other rebuild.
+template <int D, int BITS, bool PSAC>
 __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, int group,
                                                    int tok0, int ntok, float *out32,
                                                    uint16_t *out16) {
-    constexpr int E = D / 32, NB = D * BITS / 8;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int NB = D * BITS / 8, CB = 32 * BITS / 8;  // code bytes per row / per 32-channel block
+    const int lane = threadIdx.x & 31;
     const int H = cv.H, ng = D / group;
-    const int nrows = ntok * H;
-    for (int row = blockIdx.x * 8 + warp; row < nrows; row += gridDim.x * 8) {
-        const int t = row / H, h = row % H, slot = tok0 + t;
-        const int chunk = cv.tile_chunk[slot / QVG_TILE];
-        const int start = cv.chunk_start[chunk], len = cv.chunk_len[chunk];
-        const bool valid = slot >= start && slot < start + len;
-        float acc[E];
+    const int nblk = ceil_div(ntok, 32);
+    const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (wid >= static_cast<long long>(H) * nblk) return;
+    const int h = static_cast<int>(wid / nblk), t = static_cast<int>(wid % nblk) * 32 + lane;
+    if (t >= ntok) return;
+    const int slot = tok0 + t;
+    const int chunk = cv.tile_chunk[slot / QVG_TILE];
+    const bool valid = slot >= cv.chunk_start[chunk] && slot < cv.chunk_start[chunk] + cv.chunk_len[chunk];
+    float pk[QVG_PSAC_RANK];
+    const float *U = nullptr;
+    if (PSAC && valid) {
+        const size_t prow = static_cast<size_t>(h) * cv.cap + slot;
+        const float pSp = f16_to_f32(cv.psac_s[prow]);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+        for (int k = 0; k < QVG_PSAC_RANK; ++k) pk[k] = pSp * static_cast<float>(cv.psac_p[prow * QVG_PSAC_RANK + k]);
+        U = cv.psac_basis + (static_cast<size_t>(chunk) * H + h) * D * QVG_PSAC_RANK;
+    }
+    const size_t orow = (static_cast<size_t>(t) * H + h) * D;
+#pragma unroll 1
+    for (int cb = 0; cb < D / 32; ++cb) {
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
         if (valid) {
             for (int l = 0; l < L; ++l) {
                 const size_t srow = (static_cast<size_t>(l) * H + h) * cv.cap + slot;
-                const uint8_t *crow = cv.codes + srow * NB;
-                const float Sp = f16_to_f32(cv.scales[srow * ng + (lane * E) / group]);
-                const uint16_t *cr = nullptr;
-                if (C > 0)
-                    cr = cv.cent + ((static_cast<size_t>(l) * H + h) * cv.max_chunks + chunk) * C * D +
-                         static_cast<size_t>(cv.ids[srow]) * D;
+                uint32_t cw[CB / 4];
+                if constexpr (CB == 8) {
+                    const uint2 u = *reinterpret_cast<const uint2 *>(cv.codes + srow * NB + cb * CB);
+                    cw[0] = u.x;
+                    cw[1] = u.y;
+                } else {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(cv.codes + srow * NB + cb * CB);
+                    cw[0] = u.x;
+                    cw[1] = u.y;
+                    cw[2] = u.z;
+                    cw[3] = u.w;
+                }
+                float S[4];
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const int j = lane * E + e;
-                    float v = __fmul_rn(Sp, static_cast<float>(code_at<BITS>(crow, j)));
-                    if (C > 0) v = __fadd_rn(v, bf16_to_f32(cr[j]));
+                for (int g8 = 0; g8 < 4; ++g8) S[g8] = f16_to_f32(cv.scales[srow * ng + (cb * 32 + g8 * 8) / group]);
+                uint4 cr[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                               make_uint4(0, 0, 0, 0)};
+                if (C > 0) {
+                    const uint16_t *crow = cv.cent + ((static_cast<size_t>(l) * H + h) * cv.max_chunks + chunk) * C * D +
+                                           static_cast<size_t>(cv.ids[srow]) * D + cb * 32;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cr[i] = *reinterpret_cast<const uint4 *>(crow + 8 * i);
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const uint32_t word = cw[(e * BITS) / 32];
+                    const int q = static_cast<int>((word >> ((e * BITS) % 32)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
+                    float v = __fmul_rn(S[e >> 3], static_cast<float>(q));
+                    if (C > 0) {
+                        const uint4 c4 = cr[e >> 3];
+                        const uint32_t cwd = (e & 7) < 2 ? c4.x : (e & 7) < 4 ? c4.y : (e & 7) < 6 ? c4.z : c4.w;
+                        v = __fadd_rn(v, __uint_as_float((e & 1) ? (cwd & 0xffff0000u) : (cwd << 16)));
+                    }
                     acc[e] = __fadd_rn(acc[e], v);
                 }
             }
-            if (cv.psac_p) {
-                const size_t prow = static_cast<size_t>(h) * cv.cap + slot;
-                const float pSp = f16_to_f32(cv.psac_s[prow]);
-                const float *U = cv.psac_basis + (static_cast<size_t>(chunk) * H + h) * D * QVG_PSAC_RANK;
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const int j = lane * E + e;
+            if (U) {
+#pragma unroll 4
+                for (int e = 0; e < 32; ++e) {
+                    const float *u = U + (cb * 32 + e) * QVG_PSAC_RANK;
                     float corr = 0.0f;
 #pragma unroll
-                    for (int k = 0; k < QVG_PSAC_RANK; ++k)
-                        corr = fmaf(pSp * static_cast<float>(cv.psac_p[prow * QVG_PSAC_RANK + k]),
-                                    U[j * QVG_PSAC_RANK + k], corr);
+                    for (int k = 0; k < QVG_PSAC_RANK; ++k) corr = fmaf(pk[k], u[k], corr);
                     acc[e] = acc[e] + corr;
                 }
             }
         }
-        const size_t o = static_cast<size_t>(row) * D + lane * E;
+        if (out32) {
+            float4 *o = reinterpret_cast<float4 *>(out32 + orow + cb * 32);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            if (out32) out32[o + e] = acc[e];
-            else out16[o + e] = f32_to_bf16(acc[e]);
+            for (int i = 0; i < 8; ++i) o[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        } else {
+            uint4 *o = reinterpret_cast<uint4 *>(out16 + orow + cb * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    w4[k] = static_cast<uint32_t>(f32_to_bf16(acc[8 * i + 2 * k])) |
+                            (static_cast<uint32_t>(f32_to_bf16(acc[8 * i + 2 * k + 1])) << 16);
+                o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
         }
     }
 }
@@ -94,9 +133,11 @@ qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, 
     if (!(p->flags & QVG_PSAC)) cv.psac_p = nullptr;
     float *o32 = out_dtype == QVG_OUT_F32 ? static_cast<float *>(out) : nullptr;
     uint16_t *o16 = out_dtype == QVG_OUT_BF16 ? static_cast<uint16_t *>(out) : nullptr;
-    const int rows = ntok * c->H;
-    const int blocks = std::max(1, std::min(ceil_div(rows, 8), 152 * 16));
-#define QVG_DQ(D_, B_) k_decompress<D_, B_><<<blocks, 256, 0, st>>>(cv, p->L, p->C, p->group, tok0, ntok, o32, o16)
+    const long long warps = static_cast<long long>(c->H) * ceil_div(std::max(ntok, 1), 32);
+    const int blocks = static_cast<int>(std::max(1LL, (warps + 7) / 8));
+#define QVG_DQ(D_, B_)                                                                                        \
+    (cv.psac_p ? k_decompress<D_, B_, true><<<blocks, 256, 0, st>>>(cv, p->L, p->C, p->group, tok0, ntok, o32, o16) \
+               : k_decompress<D_, B_, false><<<blocks, 256, 0, st>>>(cv, p->L, p->C, p->group, tok0, ntok, o32, o16))
     if (c->d == 64) {
         if (p->bits == 2) QVG_DQ(64, 2); else QVG_DQ(64, 4);
     } else {
