@@ -164,6 +164,9 @@ qvg_status qvg_cache_bytes(const qvg_params *p, int32_t H, int32_t d,
  * queries (attention), H KV heads, head_dim d and Hq query heads.  The
  * caller allocates it (256-byte aligned) and passes it to the call; its
  * contents need no initialisation and are dead after the call completes.
+ * For attention it is 0 when n queries already fill the GPU (the cache is
+ * then not split) and otherwise enough for the largest split the current
+ * device's SM count can call for.
  */
 qvg_status qvg_workspace_size(const qvg_params *p, int32_t op, int32_t n,
                               int32_t H, int32_t d, int32_t Hq, size_t *bytes);
@@ -252,8 +255,17 @@ qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache,
  *   out      [Nq][Hq][d] fp32 or bf16.
  *   lse      fp32 [Hq][Nq] natural-log log-sum-exp of the scaled logits, or NULL.
  *   top1     int32 [Hq][Nq] slot of the largest logit (lowest on ties), or NULL.
+ *   workspace, ws_bytes  optional device scratch (256-byte aligned).  When
+ *            ceil(Nq / 256) * Hq work units cannot occupy every SM (a few
+ *            queries, as in decoding), a workspace of at least
+ *            qvg_workspace_size(QVG_OP_ATTENTION, Nq, H, d, Hq) lets the call
+ *            split the cache over more CTAs: each split writes its
+ *            normalised fp32 output, log-sum-exp and best logit there, and a
+ *            second kernel merges them (weights e^{lse_split - max}).  With no
+ *            workspace, or a smaller one, the call runs unsplit; the results
+ *            agree within fp32 rounding of the merge.
  * No mask: every cached token precedes the queries.  k and v must hold the
- * same chunks.
+ * same chunks.  Errors: QVG_ERR_WORKSPACE for a misaligned workspace.
  */
 qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq,
                          int32_t Hq, const qvg_cache *k, const qvg_cache *v,

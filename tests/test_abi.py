@@ -157,3 +157,14 @@ def test_quantwm_reject_on_host(lib):
     assert lib.quantwm_psac_basis(f, f, 2, 128, 4, f, f, f, None) == qvg.QVG_ERR_UNSUPPORTED
     assert lib.quantwm_psac_basis(f, f, 2, 256, 8, f, f, f, None) == qvg.QVG_ERR_UNSUPPORTED
     assert lib.quantwm_psac_basis(None, f, 2, 128, 8, f, f, f, None) == qvg.QVG_ERR_INVALID_ARG
+
+
+def test_attention_workspace_only_for_split_queries(lib):
+    """qvg_attention splits the cache over extra CTAs only when the query
+    blocks alone cannot fill the GPU: few queries need a workspace (partial
+    outputs, log-sum-exp, best logits), a full chunk of queries none."""
+    p = qvg.Params(C=256, L=1, bits=2, group=64, iters=8)
+    small = qvg.workspace_size(p, qvg.QVG_OP_ATTENTION, 16, 16, 128, 16)
+    assert small >= 2 * 16 * 16 * (128 + 3) * 4  # at least two splits
+    assert small % 256 == 0
+    assert qvg.workspace_size(p, qvg.QVG_OP_ATTENTION, 4680, 16, 128, 16) == 0

@@ -246,6 +246,47 @@ def test_attention_longcat_sampled():
     _assert_attention(out.cpu().numpy()[rows].astype(np.float64), ref, w.Hq)
 
 
+@pytest.mark.parametrize("Nq", [16, 300])
+def test_attention_split_cache(Nq):
+    """Few queries (16: one block, 300: two blocks, x 16 heads) over 2 LongCat
+    chunks: qvg_attention splits the cache over extra CTAs and merges the
+    splits' partial outputs by their log-sum-exp.  Checked against the fp64
+    oracle (output, lse, top-1) and against the same call without a
+    workspace, which runs unsplit."""
+    w, p, _ = CASES["longcat"]
+    chunks = [(synth.chunk_kv(w, 23, k, synth.KIND_K), synth.chunk_kv(w, 23, k, synth.KIND_V)) for k in range(2)]
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    q = np.ascontiguousarray(synth.queries(w, 23, 2)[:Nq])
+    need = qvg.workspace_size(p, qvg.QVG_OP_ATTENTION, Nq, w.H, w.d, w.Hq)
+    assert need > 0
+    out, lse, top1 = qvg.attention(p, to_dev(q), kc, vc, want_lse=True, want_top1=True)
+    ref, rlse, ram, _, hk = _oracle_attention_on(kc, vc, p, q)
+    got = out.cpu().numpy().astype(np.float64)
+    _assert_attention(got, ref, w.Hq)
+    np.testing.assert_allclose(lse.cpu().numpy(), rlse, atol=2e-3, rtol=0)
+    # top-1 against fp64: LongCat-like patches hold near-duplicate keys, whose
+    # maxima fp16 operand rounding can reorder
+    slots = _slot_of_token(hk, 2)
+    assert (top1.cpu().numpy() == slots[ram]).mean() >= 0.95
+    # the unsplit path (no workspace) on the same inputs: same logits, so the
+    # same top-1; the outputs and lse differ only by the rounding of P and of
+    # the merge (each split normalises by its own running max)
+    import ctypes as ct
+    qd = to_dev(q)
+    one = torch.empty_like(out)
+    lse1 = torch.empty_like(lse)
+    top11 = torch.empty_like(top1)
+    k, v, pc = kc.c(), vc.c(), p.c()
+    st = qvg.lib().qvg_attention(ct.byref(pc), ct.c_void_p(qd.data_ptr()), Nq, w.Hq, ct.byref(k), ct.byref(v),
+                                 ct.c_float(0.0), ct.c_void_p(one.data_ptr()), qvg.QVG_OUT_F32,
+                                 ct.c_void_p(lse1.data_ptr()), ct.c_void_p(top11.data_ptr()), None, 0, None)
+    assert st == qvg.QVG_OK
+    one_np = one.cpu().numpy().astype(np.float64)
+    assert np.abs(one_np - got).max() <= 1e-4 * np.abs(one_np).max()
+    np.testing.assert_allclose(lse1.cpu().numpy(), lse.cpu().numpy(), atol=1e-3, rtol=0)
+    assert (top11.cpu().numpy() == top1.cpu().numpy()).mean() >= 0.999
+
+
 def test_ragged_and_degenerate_chunks():
     """Chunks of 300 (two tiles plus a ragged 44), 1 token, 10 tokens with
     C=16 > N, and exactly 128 tokens; attention across all of them."""
