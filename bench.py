@@ -243,11 +243,13 @@ def launches_per_compress(p):
     return per_stage * p.L + 1  # + chunk table
 
 
-def kernel_extras(qvg, p, w, kc, vc, q, flush, dev, last, slots_per_chunk, reps=5):
+def kernel_extras(qvg, p, w, kc, vc, q, k_raw, flush, dev, last, slots_per_chunk, reps=5):
     """Separately timed kernels on the same cache (outside the step): the
     decompress of the newest chunk (fp32 and bf16 output) and a decode-like
     attention point (16 queries over the whole cache), each with its
-    algorithmic bytes and the fraction of the measured HBM peak."""
+    algorithmic bytes and the fraction of the measured HBM peak; and the
+    attention of one AR step (older chunks compressed, the newest chunk raw),
+    with its FLOP rate."""
     import torch
     peaks, _ = _peaks()
     hbm = peaks["hbm_gbs"]
@@ -285,6 +287,21 @@ def kernel_extras(qvg, p, w, kc, vc, q, flush, dev, last, slots_per_chunk, reps=
     res["attention_decode16"] = {"ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms / 1e3) / 1e9,
                                  "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm,
                                  "what": "16 queries over the whole compressed K and V cache"}
+    # one AR step's attention: the newest chunk's queries over the older
+    # chunks (compressed) and the newest chunk's own raw bf16 K/V
+    tc_peak = peaks["bf16_tflops"]
+    kc.reset(last, last * slots_per_chunk)
+    vc.reset(last, last * slots_per_chunk)
+    k_cur, v_cur = k_raw
+    out_ar = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    ms = timed(lambda: qvg.attention_ar(p, q, kc, vc, k_cur, v_cur, out_dtype=qvg.QVG_OUT_BF16, out=out_ar))
+    kc.reset(last + 1, (last + 1) * slots_per_chunk)
+    vc.reset(last + 1, (last + 1) * slots_per_chunk)
+    flops = 4.0 * w.Nq * w.tokens * w.d * w.Hq
+    res["attention_ar_step"] = {"ms": ms, "TFLOP/s": flops / (ms / 1e3) / 1e12,
+                                "frac_tensor": flops / (ms / 1e3) / 1e12 / tc_peak,
+                                "what": "%d queries over %d compressed chunks + the current chunk's %d raw tokens"
+                                        % (w.Nq, last, w.N)}
     assert qvg.get_status() == qvg.QVG_OK
     return res
 
@@ -364,7 +381,7 @@ def run_own(args):
     ms_attn = statistics.mean(attn)
     status = qvg.get_status()
 
-    extras = kernel_extras(qvg, p, w, kc, vc, q, flush, dev, last, slots_per_chunk) if rank == 0 else {}
+    extras = kernel_extras(qvg, p, w, kc, vc, q, (k_new, v_new), flush, dev, last, slots_per_chunk) if rank == 0 else {}
 
     if args.no_e2e:
         if rank == 0:

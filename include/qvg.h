@@ -274,6 +274,35 @@ qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq,
                          void *stream);
 
 /*
+ * Attention of one autoregressive step: the Nq queries of the chunk being
+ * generated attend to every token of the compressed cache (the earlier
+ * chunks) and to the chunk's own n_cur tokens, whose K/V are still raw bf16
+ * ([QVG] research background: chunk-by-chunk generation in which each chunk
+ * attends to the cached K/V of the chunks before it; within a chunk there is
+ * no mask).  The keys are the concatenation [K_hat ; K_cur] and the values
+ * [V_hat ; V_cur], in one softmax:
+ *   O = softmax(scale * Q [K_hat ; K_cur]^T) [V_hat ; V_cur].
+ *   k_cur_bf16, v_cur_bf16  bf16 [n_cur][H][d], 16-byte aligned (the layout
+ *            qvg_compress_chunk takes, so the same buffers are compressed
+ *            into the cache after the step); read only, owned by the caller.
+ *   n_cur    >= 0; 0 gives qvg_attention.  The cache may be empty (first
+ *            chunk) when n_cur > 0.
+ *   top1     current-chunk token j is reported as slot k->n_tokens + j, the
+ *            slot it takes once the chunk is compressed into this cache.
+ * The other arguments, the workspace rule and the outputs are those of
+ * qvg_attention.  The raw rows are rounded to fp16 for the tensor core like
+ * the reconstructed ones (exact inside fp16's normal range).
+ * Errors: QVG_ERR_INVALID_ARG for n_cur < 0, a missing or misaligned raw
+ * buffer, or no keys at all.
+ */
+qvg_status qvg_attention_ar(const qvg_params *p, const void *q_bf16, int32_t Nq,
+                            int32_t Hq, const qvg_cache *k, const qvg_cache *v,
+                            const void *k_cur_bf16, const void *v_cur_bf16,
+                            int32_t n_cur, float scale, void *out,
+                            int32_t out_dtype, float *lse, int32_t *top1,
+                            void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * History-query statistics ([QWM] QSAC: per-channel activity of history
  * queries; PSAC: their second-moment matrix).  For KV head h, the query
  * heads hq with hq / (Hq/H) == h are pooled:

@@ -220,6 +220,23 @@ def attention(q, k, v, scale=0.0, nthreads=1):
     return out, lse, am
 
 
+def attention_ar(q, k_hat, v_hat, k_cur, v_cur, cache_slots, n_slots, scale=0.0, nthreads=1):
+    """Attention of one autoregressive step (Quant VideoGen notes, research
+    background: each new chunk attends to the cached K/V of every earlier
+    chunk; reading: no mask inside the chunk).  The keys are the cached
+    tokens followed by the chunk's own tokens, in one softmax:
+        O = softmax(scale q [k_hat; k_cur]^T) [v_hat; v_cur].
+    k_hat/v_hat [Nc,H,d] hold the reconstructed cache tokens, whose slot
+    numbers are cache_slots [Nc]; current-chunk token j is slot n_slots + j.
+    Returns out fp64 [Nq,Hq,d], lse [Hq,Nq] and the top-1 slot [Hq,Nq]."""
+    k = np.concatenate([np.asarray(k_hat, np.float32), np.asarray(k_cur, np.float32)], 0)
+    v = np.concatenate([np.asarray(v_hat, np.float32), np.asarray(v_cur, np.float32)], 0)
+    out, lse, am = attention(q, k, v, scale, nthreads)
+    slot_of = np.concatenate([np.asarray(cache_slots, np.int64),
+                              n_slots + np.arange(len(k_cur), dtype=np.int64)])
+    return out, lse, slot_of[am].astype(np.int32)
+
+
 def top1(q, k, nthreads=1):
     lib = _load()
     q, k = _f32(q), _f32(k)

@@ -150,6 +150,31 @@ def test_attention_and_decompress_reject_on_host(lib):
     assert lib.qvg_decompress(ct.byref(p), ct.byref(k), -1, 10, o, 0, None) == qvg.QVG_ERR_INVALID_ARG
 
 
+def test_attention_ar_rejects_on_host(lib):
+    """The AR-step call: raw current-chunk buffers must be present and
+    16-byte aligned, n_cur >= 0, and there must be at least one key."""
+    p = _params(C=16, group=32)
+    k = _fake_cache(n_chunks=1, n_tokens=128)
+    empty = _fake_cache()
+    q, o = ct.c_void_p(0x3000), ct.c_void_p(0x4000)
+    kr, vr = ct.c_void_p(0x6000), ct.c_void_p(0x7000)
+    f = lib.qvg_attention_ar
+
+    def call(kc, vc, kcur, vcur, n):
+        return f(ct.byref(p), q, 4, 2, ct.byref(kc), ct.byref(vc), kcur, vcur, n, 0.0, o, 0, None, None, None, 0, None)
+
+    assert call(k, k, kr, vr, -1) == qvg.QVG_ERR_INVALID_ARG
+    assert call(k, k, None, vr, 10) == qvg.QVG_ERR_INVALID_ARG
+    assert call(k, k, kr, None, 10) == qvg.QVG_ERR_INVALID_ARG
+    assert call(k, k, ct.c_void_p(0x6008), vr, 10) == qvg.QVG_ERR_INVALID_ARG
+    assert call(empty, empty, kr, vr, 0) == qvg.QVG_ERR_INVALID_ARG  # no keys
+    assert call(empty, empty, None, None, 0) == qvg.QVG_ERR_INVALID_ARG
+    assert call(k, k, kr, vr, 2 ** 31 - 100) == qvg.QVG_ERR_INVALID_ARG  # slot numbers overflow int32
+    # no query: nothing to launch
+    assert f(ct.byref(p), q, 0, 2, ct.byref(empty), ct.byref(empty), kr, vr, 10, 0.0, o, 0, None, None, None, 0,
+             None) == qvg.QVG_OK
+
+
 def test_quantwm_reject_on_host(lib):
     f = ct.c_void_p(0x5000)
     assert lib.quantwm_query_stats(f, 10, 3, 2, 128, 0, f, f, f, None) == qvg.QVG_ERR_INVALID_ARG

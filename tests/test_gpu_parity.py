@@ -287,6 +287,83 @@ def test_attention_split_cache(Nq):
     assert (top11.cpu().numpy() == top1.cpu().numpy()).mean() >= 0.999
 
 
+def _oracle_ar(kc, vc, p, q, k_cur, v_cur, rows=None):
+    hk, hv = host_cache(kc), host_cache(vc)
+    n = kc.n_chunks
+    d = kc.d
+    kh = np.concatenate([oracle_rebuild(hk, p, k) for k in range(n)] + [np.zeros((0, kc.H, d), np.float32)], 0)
+    vh = np.concatenate([oracle_rebuild(hv, p, k) for k in range(n)] + [np.zeros((0, kc.H, d), np.float32)], 0)
+    qq = q if rows is None else q[rows]
+    return oracle.attention_ar(qq, kh, vh, k_cur, v_cur, _slot_of_token(hk, n) if n else np.zeros(0, np.int64),
+                               kc.n_tokens, nthreads=NT)
+
+
+def _ar_case(w, p, seed, n_cache, raw_len=None):
+    chunks = [(synth.chunk_kv(w, seed, k, synth.KIND_K), synth.chunk_kv(w, seed, k, synth.KIND_V))
+              for k in range(n_cache)]
+    if n_cache:
+        kc, vc = _cache_with_chunks(w, p, chunks)
+    else:
+        kc, vc = _new_cache(w, p, 1), _new_cache(w, p, 1)
+    k_cur = synth.chunk_kv(w, seed, n_cache, synth.KIND_K)
+    v_cur = synth.chunk_kv(w, seed, n_cache, synth.KIND_V)
+    if raw_len is not None:
+        k_cur, v_cur = k_cur[:raw_len], v_cur[:raw_len]
+    q = synth.queries(w, seed, n_cache)
+    return kc, vc, k_cur, v_cur, q
+
+
+@pytest.mark.parametrize("case,n_cache,raw_len", [("tiny", 3, None), ("tiny", 2, 300), ("pro_int2_L3", 1, 45),
+                                                  ("tiny", 0, 200), ("tiny", 0, 1)])
+def test_attention_ar_step(case, n_cache, raw_len):
+    """One AR step: the chunk's queries over the compressed cache plus the
+    chunk's own raw bf16 K/V (ragged raw tails, a three-stage cache on the
+    general rebuild path, the first chunk with an empty cache, a one-token
+    chunk), against the fp64 oracle on the same concatenated keys."""
+    w, p, _ = CASES[case]
+    kc, vc, k_cur, v_cur, q = _ar_case(w, p, 31, n_cache, raw_len)
+    out, lse, top1 = qvg.attention_ar(p, to_dev(q), kc, vc, to_dev(k_cur), to_dev(v_cur), want_lse=True,
+                                      want_top1=True)
+    ref, rlse, rtop = _oracle_ar(kc, vc, p, q, k_cur, v_cur)
+    got = out.cpu().numpy().astype(np.float64)
+    _assert_attention(got, ref, q.shape[1])
+    np.testing.assert_allclose(lse.cpu().numpy(), rlse, atol=2e-3, rtol=0)
+    assert (top1.cpu().numpy() == rtop).mean() >= 0.99
+    if len(k_cur) == 1 and n_cache == 0:  # a single key returns its value (fp16-rounded)
+        np.testing.assert_allclose(got, np.broadcast_to(v_cur[0], got.shape), rtol=2 ** -11, atol=2 ** -24)
+
+
+def test_attention_ar_without_current_chunk_is_attention():
+    """n_cur = 0 is qvg_attention, bit for bit."""
+    w, p, _ = CASES["tiny"]
+    kc, vc, k_cur, v_cur, q = _ar_case(w, p, 32, 2)
+    qd = to_dev(q)
+    a, la, ta = qvg.attention(p, qd, kc, vc, want_lse=True, want_top1=True)
+    z = to_dev(k_cur[:0])
+    b, lb, tb = qvg.attention_ar(p, qd, kc, vc, z, z, want_lse=True, want_top1=True)
+    assert torch.equal(a, b) and torch.equal(la, lb) and torch.equal(ta, tb)
+
+
+@pytest.mark.parametrize("Nq", [4680, 16])
+def test_attention_ar_longcat(Nq):
+    """LongCat-like AR step (16 heads, d=128): 2 cached chunks of 4680
+    tokens plus the current chunk's 4680 raw tokens; 4680 queries (64
+    sampled rows per head checked) and 16 queries (split-cache path)."""
+    w, p, _ = CASES["longcat"]
+    kc, vc, k_cur, v_cur, q = _ar_case(w, p, 33, 2)
+    q = np.ascontiguousarray(q[:Nq])
+    out, lse, top1 = qvg.attention_ar(p, to_dev(q), kc, vc, to_dev(k_cur), to_dev(v_cur), want_lse=True,
+                                      want_top1=True)
+    rows = np.random.default_rng(2).choice(Nq, min(Nq, 64), replace=False)
+    ref, rlse, rtop = _oracle_ar(kc, vc, p, q, k_cur, v_cur, rows)
+    _assert_attention(out.cpu().numpy()[rows].astype(np.float64), ref, w.Hq)
+    np.testing.assert_allclose(lse.cpu().numpy()[:, rows], rlse, atol=2e-3, rtol=0)
+    # near-duplicate keys in a LongCat-like patch: fp16 operand rounding may reorder maxima
+    assert (top1.cpu().numpy()[:, rows] == rtop).mean() >= 0.95
+    # current-chunk slots are numbered after the cache
+    assert top1.max().item() < kc.n_tokens + len(k_cur)
+
+
 def test_ragged_and_degenerate_chunks():
     """Chunks of 300 (two tiles plus a ragged 44), 1 token, 10 tokens with
     C=16 > N, and exactly 128 tokens; attention across all of them."""
@@ -406,4 +483,10 @@ def test_quantwm_compress_and_attention(flags):
     kh = np.concatenate([oracle_rebuild(hk, p, k) for k in range(2)], 0)
     vh = np.concatenate([oracle_rebuild(hv, pv, k) for k in range(2)], 0)
     ref, _, _ = oracle.attention(q, kh, vh, nthreads=NT)
+    _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
+    # AR step on the same cache: the third chunk's raw K/V join the keys
+    # (the PSAC term corrects cached keys only)
+    kr, vr = synth.chunk_kv(w, 23, 2, synth.KIND_K)[:700], synth.chunk_kv(w, 23, 2, synth.KIND_V)[:700]
+    out, _, _ = qvg.attention_ar(p, to_dev(q), kc, vc, to_dev(kr), to_dev(vr))
+    ref, _, _ = oracle.attention_ar(q, kh, vh, kr, vr, _slot_of_token(hk, 2), kc.n_tokens, nthreads=NT)
     _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)

@@ -305,6 +305,41 @@ def test_attention_exact_when_lossless(orc):
     np.testing.assert_array_equal(a, b)
 
 
+def test_attention_ar_is_the_lse_merge(orc):
+    """Attention over [cache; current chunk] equals the two partial
+    attentions merged by their log-sum-exps,
+    O = (e^{l1} O1 + e^{l2} O2) / (e^{l1} + e^{l2}), lse = log(e^{l1} + e^{l2}):
+    a softmax identity, here computed by a different route (two separate
+    softmaxes).  An empty cache reduces to plain attention over the chunk."""
+    rng = np.random.default_rng(21)
+    Nq, Hq, H, d, Nc, Ncur = 6, 4, 2, 16, 9, 5
+    q = rng.standard_normal((Nq, Hq, d)).astype(np.float32)
+    kh = rng.standard_normal((Nc, H, d)).astype(np.float32)
+    vh = rng.standard_normal((Nc, H, d)).astype(np.float32)
+    kr = rng.standard_normal((Ncur, H, d)).astype(np.float32)
+    vr = rng.standard_normal((Ncur, H, d)).astype(np.float32)
+    slots = np.array([0, 1, 2, 3, 128, 129, 130, 256, 257])
+    out, lse, top = orc.attention_ar(q, kh, vh, kr, vr, slots, 384)
+    o1, l1, a1 = orc.attention(q, kh, vh)
+    o2, l2, a2 = orc.attention(q, kr, vr)
+    m = np.maximum(l1, l2)
+    w1, w2 = np.exp(l1 - m), np.exp(l2 - m)
+    ref = (w1.T[:, :, None] * o1 + w2.T[:, :, None] * o2) / (w1 + w2).T[:, :, None]
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, m + np.log(w1 + w2), rtol=1e-12)
+    # top-1: the larger of the two partial maxima, numbered by slot
+    for hq in range(Hq):
+        h = hq // (Hq // H)
+        s1 = (q[:, hq].astype(np.float64) @ kh[:, h].T.astype(np.float64)).max(-1)
+        s2 = (q[:, hq].astype(np.float64) @ kr[:, h].T.astype(np.float64)).max(-1)
+        want = np.where(s2 > s1, 384 + a2[hq], slots[a1[hq]])
+        np.testing.assert_array_equal(top[hq], want)
+    # first chunk: no cache
+    o0, l0, t0 = orc.attention_ar(q, kh[:0], vh[:0], kr, vr, slots[:0], 0)
+    np.testing.assert_array_equal(o0, o2)
+    np.testing.assert_array_equal(t0, a2)
+
+
 def test_query_stats(orc):
     rng = np.random.default_rng(8)
     q = rng.standard_normal((30, 4, 8)).astype(np.float32)

@@ -31,7 +31,7 @@ QVG_OP_COMPRESS, QVG_OP_ATTENTION, QVG_OP_PSAC_BASIS = 0, 1, 2
 EXPORTED = (
     "qvg_status_string", "qvg_cache_bytes", "qvg_workspace_size", "qvg_compress_chunk",
     "qvg_decompress", "qvg_attention", "quantwm_query_stats", "quantwm_psac_basis",
-    "qvg_get_status", "qvg_last_cuda_error", "qvg_compress_chunk_noalloc",
+    "qvg_get_status", "qvg_last_cuda_error", "qvg_compress_chunk_noalloc", "qvg_attention_ar",
 )
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -80,6 +80,8 @@ def lib():
         L.qvg_compress_chunk_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, vp]
         L.qvg_decompress.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         L.qvg_attention.argtypes = [vp, vp, i32, i32, vp, vp, ct.c_float, vp, i32, vp, vp, vp, sz, vp]
+        L.qvg_attention_ar.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, i32, ct.c_float, vp, i32, vp, vp, vp,
+                                       sz, vp]
         L.quantwm_query_stats.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
         L.quantwm_psac_basis.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
         L.qvg_get_status.argtypes = []
@@ -265,6 +267,38 @@ def attention(params: Params, q, kc: CompressedKV, vc: CompressedKV, scale=0.0,
                             _ptr(out), out_dtype, _ptr(lse), _ptr(top1), _ptr(workspace),
                             0 if workspace is None else workspace.numel(), _stream(stream))
     _check(s, "qvg_attention")
+    return out, lse, top1
+
+
+def attention_ar(params: Params, q, kc: CompressedKV, vc: CompressedKV, k_cur, v_cur, scale=0.0,
+                 out_dtype=QVG_OUT_F32, want_lse=False, want_top1=False, out=None, workspace=None,
+                 stream=None):
+    """One autoregressive step: softmax(scale Q [K_hat; K_cur]^T) [V_hat; V_cur]
+    over the cached tokens and the current chunk's raw bf16 rows.
+    q: bf16 [Nq, Hq, d]; k_cur, v_cur: bf16 [n_cur, H, d].  Returns
+    (out, lse or None, top1 or None); current-chunk token j is slot
+    kc.n_tokens + j in top1."""
+    import torch
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 3
+    for x in (k_cur, v_cur):
+        assert x.dtype == torch.bfloat16 and x.is_contiguous() and x.dim() == 3
+    assert k_cur.shape == v_cur.shape and k_cur.shape[1:] == (kc.H, kc.d)
+    Nq, Hq, d = q.shape
+    n_cur = k_cur.shape[0]
+    dt = torch.float32 if out_dtype == QVG_OUT_F32 else torch.bfloat16
+    if out is None:
+        out = torch.empty((Nq, Hq, d), dtype=dt, device=q.device)
+    lse = torch.empty((Hq, Nq), dtype=torch.float32, device=q.device) if want_lse else None
+    top1 = torch.empty((Hq, Nq), dtype=torch.int32, device=q.device) if want_top1 else None
+    need = workspace_size(params, QVG_OP_ATTENTION, Nq, kc.H, d, Hq)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    k, v = kc.c(), vc.c()
+    p = params.c()
+    s = lib().qvg_attention_ar(ct.byref(p), _ptr(q), Nq, Hq, ct.byref(k), ct.byref(v), _ptr(k_cur), _ptr(v_cur),
+                               n_cur, float(scale), _ptr(out), out_dtype, _ptr(lse), _ptr(top1), _ptr(workspace),
+                               0 if workspace is None else workspace.numel(), _stream(stream))
+    _check(s, "qvg_attention_ar")
     return out, lse, top1
 
 

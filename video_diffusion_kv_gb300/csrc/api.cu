@@ -234,11 +234,15 @@ qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache, int32_t t
     return launch_decompress(p, cache, tok0, ntok, out, out_dtype, static_cast<cudaStream_t>(stream));
 }
 
-qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq, int32_t Hq,
-                         const qvg_cache *k, const qvg_cache *v, float scale, void *out,
-                         int32_t out_dtype, float *lse, int32_t *top1, void *workspace,
-                         size_t ws_bytes, void *stream) {
+qvg_status qvg_attention_ar(const qvg_params *p, const void *q_bf16, int32_t Nq, int32_t Hq,
+                            const qvg_cache *k, const qvg_cache *v, const void *k_cur_bf16,
+                            const void *v_cur_bf16, int32_t n_cur, float scale, void *out,
+                            int32_t out_dtype, float *lse, int32_t *top1, void *workspace,
+                            size_t ws_bytes, void *stream) {
     if (!k || !v || (!q_bf16 && Nq > 0) || (!out && Nq > 0)) return QVG_ERR_INVALID_ARG;
+    if (n_cur < 0 || (n_cur > 0 && (!k_cur_bf16 || !v_cur_bf16))) return QVG_ERR_INVALID_ARG;
+    if (n_cur > 0 && ((reinterpret_cast<uintptr_t>(k_cur_bf16) | reinterpret_cast<uintptr_t>(v_cur_bf16)) & 15u))
+        return QVG_ERR_INVALID_ARG;
     qvg_status s = check_params(p, k->d);
     if (s != QVG_OK) return s;
     if ((s = check_cache(p, k)) != QVG_OK) return s;
@@ -249,14 +253,26 @@ qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq, in
         k->capacity_tokens != v->capacity_tokens || k->max_chunks != v->max_chunks)
         return QVG_ERR_INVALID_ARG;
     if (Nq < 0 || Hq < 1 || Hq % k->H != 0) return QVG_ERR_INVALID_ARG;
-    if (k->n_tokens == 0) return QVG_ERR_INVALID_ARG;
+    if (k->n_tokens == 0 && n_cur == 0) return QVG_ERR_INVALID_ARG;
+    if (n_cur > INT32_MAX - QVG_TILE - k->n_tokens) return QVG_ERR_INVALID_ARG;  // slot numbers stay int32
     if (out_dtype != QVG_OUT_F32 && out_dtype != QVG_OUT_BF16) return QVG_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return QVG_ERR_INVALID_ARG;
     const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(k->d));
     const float scale_log2 = sc * 1.4426950408889634f;
     if (workspace && reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return QVG_ERR_WORKSPACE;
-    return launch_attention_ws(p, static_cast<const uint16_t *>(q_bf16), Nq, Hq, k, v, scale_log2, out,
-                               out_dtype, lse, top1, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+    if (Nq == 0) return QVG_OK;
+    return launch_attention_ws(p, static_cast<const uint16_t *>(q_bf16), Nq, Hq, k, v, scale_log2,
+                               static_cast<const uint16_t *>(k_cur_bf16), static_cast<const uint16_t *>(v_cur_bf16),
+                               n_cur, out, out_dtype, lse, top1, workspace, ws_bytes,
+                               static_cast<cudaStream_t>(stream));
+}
+
+qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq, int32_t Hq,
+                         const qvg_cache *k, const qvg_cache *v, float scale, void *out,
+                         int32_t out_dtype, float *lse, int32_t *top1, void *workspace,
+                         size_t ws_bytes, void *stream) {
+    return qvg_attention_ar(p, q_bf16, Nq, Hq, k, v, nullptr, nullptr, 0, scale, out, out_dtype, lse, top1,
+                            workspace, ws_bytes, stream);
 }
 
 qvg_status quantwm_query_stats(const void *q_hist_bf16, int32_t n, int32_t Hq, int32_t H, int32_t d,

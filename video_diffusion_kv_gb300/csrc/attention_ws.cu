@@ -43,6 +43,10 @@ struct AttnWsArgs {
     int32_t *top1;
     float *best;  // split mode with top-1: each split's best scaled logit
     int *err;
+    // the current chunk's own K/V (bf16 [n_raw][H][D]), attended after the
+    // n_ctiles = n_slots / QVG_TILE cache tiles; raw row j is slot n_slots + j
+    const uint16_t *kraw, *vraw;
+    int n_raw, n_ctiles;
 };
 
 namespace ws {
@@ -88,6 +92,9 @@ __device__ __forceinline__ void group_sync(int i) {
     asm volatile("bar.sync %0, 128;" ::"r"(1 + i) : "memory");
 }
 
+// Tile t covers slots [s0, s0 + QVG_TILE) of which the first nvalid hold
+// tokens.  Tiles below n_ctiles are cache tiles (chunk = the chunk that owns
+// them); the rest hold the current chunk's raw rows (chunk = -1).
 struct TileInfo {
     int s0, chunk, nvalid;
 };
@@ -95,9 +102,22 @@ struct TileInfo {
 __device__ __forceinline__ TileInfo tile_info(const AttnWsArgs &a, int t) {
     TileInfo ti;
     ti.s0 = t * QVG_TILE;
-    ti.chunk = a.tile_chunk[t];
-    ti.nvalid = min(QVG_TILE, max(0, a.chunk_start[ti.chunk] + a.chunk_len[ti.chunk] - ti.s0));
+    if (t < a.n_ctiles) {
+        ti.chunk = a.tile_chunk[t];
+        ti.nvalid = min(QVG_TILE, max(0, a.chunk_start[ti.chunk] + a.chunk_len[ti.chunk] - ti.s0));
+    } else {
+        ti.chunk = -1;
+        ti.nvalid = min(QVG_TILE, a.n_raw - (t - a.n_ctiles) * QVG_TILE);
+    }
     return ti;
+}
+
+// Eight bf16 values -> eight fp16 values (exact inside fp16's normal range).
+__device__ __forceinline__ uint4 bf16x8_to_f16(uint4 b) {
+    return make_uint4(h2(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xffff0000u)),
+                      h2(__uint_as_float(b.y << 16), __uint_as_float(b.y & 0xffff0000u)),
+                      h2(__uint_as_float(b.z << 16), __uint_as_float(b.z & 0xffff0000u)),
+                      h2(__uint_as_float(b.w << 16), __uint_as_float(b.w & 0xffff0000u)));
 }
 
 // K_hat channels [j0, j0 + 8) of one slot (fp32, stage order, then PSAC).
@@ -197,6 +217,20 @@ __device__ __forceinline__ void load_half(const AttnWsArgs &a, const uint8_t *co
 #pragma unroll
         for (int i = 0; i < 8; ++i) hd.cr[i] = make_uint4(0, 0, 0, 0);
     }
+}
+
+// A raw bf16 row of the current chunk in the same form: scale 0 and the row
+// in place of the centroid, so the decode's fma(0, q, x) = x rounds the bf16
+// value straight to fp16.
+template <int D, int BITS>
+__device__ __forceinline__ void load_half_raw(const uint16_t *raw, int H, int h, int j, int kb, HalfData<BITS> &hd) {
+#pragma unroll
+    for (int i = 0; i < (BITS == 2 ? 1 : 2); ++i) hd.cw[i] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hd.s2[i] = 0u;
+    const uint16_t *row = raw + (static_cast<size_t>(j) * H + h) * D + kb * 64;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hd.cr[i] = *reinterpret_cast<const uint4 *>(row + 8 * i);
 }
 
 // Zeroes one slot's 128-byte line of a 64-channel block (padding slots).
@@ -309,17 +343,27 @@ struct Producer {
     const uint16_t *scales;
     const uint8_t *ids;
     const uint16_t *cent;
+    const uint16_t *raw;  // the current chunk's rows (raw tiles)
     uint8_t *buf0;
     uint64_t *full, *freeb;
     int nbuf;
     bool psac;
 };
 
+template <int D, int BITS>
+__device__ __forceinline__ void load_tile_half(const AttnWsArgs &a, const Producer &pr, int h, const TileInfo &ti,
+                                               int r, int id, int kb, HalfData<BITS> &hd) {
+    if (ti.chunk >= 0)
+        load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti.chunk, ti.s0 + r, id, kb, hd);
+    else
+        load_half_raw<D, BITS>(pr.raw, a.H, h, ti.s0 - a.n_slots + r, kb, hd);
+}
+
 // One stage, no PSAC.  The loads of one 64-channel half are always in
 // flight while the previous half is decoded (two register sets, A for the
 // first half of a tile and B for the second when D = 128); table entries and
-// cluster ids run two tiles ahead (slot t * QVG_TILE + r < n_slots <=
-// capacity for every tile t: in bounds).
+// cluster ids run two tiles ahead (ids are read for cache tiles only, whose
+// slots t * QVG_TILE + r < n_slots <= capacity: in bounds).
 template <int D, int BITS>
 __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
                                              int n_tiles, volatile int *vfail) {
@@ -329,14 +373,14 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
     int id0 = 0, id1 = 0;
     if (n_tiles > 0) {
         ti0 = tile_info(a, tb);
-        if (a.C > 0) id0 = pr.ids[id_row];
+        if (a.C > 0 && ti0.chunk >= 0) id0 = pr.ids[id_row];
     }
     if (n_tiles > 1) {
         ti1 = tile_info(a, tb + 1);
-        if (a.C > 0) id1 = pr.ids[id_row + QVG_TILE];
+        if (a.C > 0 && ti1.chunk >= 0) id1 = pr.ids[id_row + QVG_TILE];
     }
     HalfData<BITS> A, B;
-    if (n_tiles > 0 && r < ti0.nvalid) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti0.chunk, ti0.s0 + r, id0, 0, A);
+    if (n_tiles > 0 && r < ti0.nvalid) load_tile_half<D, BITS>(a, pr, h, ti0, r, id0, 0, A);
     for (int t = 0; t < n_tiles; ++t) {
         const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
         uint8_t *T = pr.buf0 + b * TB + r * 128;
@@ -344,24 +388,24 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         int id2 = 0;
         if (t + 2 < n_tiles) {
             ti2 = tile_info(a, tb + t + 2);
-            if (a.C > 0) id2 = pr.ids[id_row + static_cast<size_t>(t + 2) * QVG_TILE];
+            if (a.C > 0 && ti2.chunk >= 0) id2 = pr.ids[id_row + static_cast<size_t>(t + 2) * QVG_TILE];
         }
         const bool valid = r < ti0.nvalid, valid1 = t + 1 < n_tiles && r < ti1.nvalid;
         if constexpr (KB == 2) {
-            if (valid) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti0.chunk, ti0.s0 + r, id0, 1, B);
+            if (valid) load_tile_half<D, BITS>(a, pr, h, ti0, r, id0, 1, B);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
             if (valid)
                 decode_store_half<BITS>(A, T, r);
             else
                 zero_line(T);
-            if (valid1) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti1.chunk, ti1.s0 + r, id1, 0, A);
+            if (valid1) load_tile_half<D, BITS>(a, pr, h, ti1, r, id1, 0, A);
             if (valid)
                 decode_store_half<BITS>(B, T + 16384, r);
             else
                 zero_line(T + 16384);
         } else {
             B = A;
-            if (valid1) load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti1.chunk, ti1.s0 + r, id1, 0, A);
+            if (valid1) load_tile_half<D, BITS>(a, pr, h, ti1, r, id1, 0, A);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
             if (valid)
                 decode_store_half<BITS>(B, T, r);
@@ -388,8 +432,9 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
         const TileInfo ti = tile_info(a, tb + t);
         const bool valid = r < ti.nvalid;
         if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
+        const bool raw = ti.chunk < 0;
         float pk[QVG_PSAC_RANK];
-        if (pr.psac && valid) {
+        if (pr.psac && valid && !raw) {
             const size_t prow = static_cast<size_t>(h) * a.cap + ti.s0 + r;
             const float pS = f16_to_f32(a.psac_s[prow]);
             const int2 pv = *reinterpret_cast<const int2 *>(a.psac_p + prow * QVG_PSAC_RANK);
@@ -404,7 +449,10 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 #pragma unroll 2
             for (int c8 = 0; c8 < 8; ++c8) {
                 uint4 o = make_uint4(0, 0, 0, 0);
-                if (valid) {
+                if (valid && raw) {
+                    o = bf16x8_to_f16(*reinterpret_cast<const uint4 *>(
+                        pr.raw + (static_cast<size_t>(ti.s0 - a.n_slots + r) * a.H + h) * D + kb * 64 + c8 * 8));
+                } else if (valid) {
                     float kv[8];
                     rebuild8<D, BITS>(a, pr.codes, pr.scales, pr.ids, pr.cent, h, ti.chunk, ti.s0 + r, kb * 64 + c8 * 8,
                                       pr.psac ? pk : nullptr, kv);
@@ -456,7 +504,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     const int hq = blockIdx.y, h = hq / a.grp, q0 = blockIdx.x * 256;
     // split z of gridDim.z takes cache tiles [tb, tb + n_tiles); every barrier
     // phase below counts tiles from tb
-    const int n_all = a.n_slots / QVG_TILE, z = blockIdx.z;
+    const int n_all = a.n_ctiles + ceil_div(a.n_raw, QVG_TILE), z = blockIdx.z;
     const int tb = static_cast<int>(static_cast<long long>(n_all) * z / gridDim.z);
     const int n_tiles = static_cast<int>(static_cast<long long>(n_all) * (z + 1) / gridDim.z) - tb;
 
@@ -466,11 +514,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         const int r = rr & 127;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (q0 + rr < a.Nq) {
-            const uint4 b = *reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(q0 + rr) * a.Hq + hq) * D + ci * 8);
-            v = make_uint4(h2(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xffff0000u)),
-                           h2(__uint_as_float(b.y << 16), __uint_as_float(b.y & 0xffff0000u)),
-                           h2(__uint_as_float(b.z << 16), __uint_as_float(b.z & 0xffff0000u)),
-                           h2(__uint_as_float(b.w << 16), __uint_as_float(b.w & 0xffff0000u)));
+            v = bf16x8_to_f16(
+                *reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(q0 + rr) * a.Hq + hq) * D + ci * 8));
         }
         *reinterpret_cast<uint4 *>((rr < 128 ? Q0 : Q1) + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
@@ -716,7 +761,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         // ------------------------------------------------ K / V producers (thread = slot)
         const bool isv = warp >= 12;
         const Producer pr{isv ? a.vcodes : a.kcodes, isv ? a.vscales : a.kscales, isv ? a.vids : a.kids,
-                          isv ? a.vcent : a.kcent, isv ? Vt0 : Kt, isv ? vfull : &kfull, isv ? vfree : &kfree,
+                          isv ? a.vcent : a.kcent, isv ? a.vraw : a.kraw, isv ? Vt0 : Kt, isv ? vfull : &kfull,
+                          isv ? vfree : &kfree,
                           isv ? 2 : 1, !isv && a.psac_p != nullptr};
         if (a.L == 1 && !pr.psac)
             produce_fast<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
@@ -847,8 +893,9 @@ size_t attention_split_bytes(int Nq, int Hq, int d, int splits) {
 }
 
 qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, int Hq, const qvg_cache *k,
-                               const qvg_cache *v, float scale_log2, void *out, int out_dtype, float *lse,
-                               int32_t *top1, void *workspace, size_t ws_bytes, cudaStream_t st) {
+                               const qvg_cache *v, float scale_log2, const uint16_t *k_cur, const uint16_t *v_cur,
+                               int n_cur, void *out, int out_dtype, float *lse, int32_t *top1, void *workspace,
+                               size_t ws_bytes, cudaStream_t st) {
     AttnWsArgs a{};
     a.q = q;
     a.Nq = Nq;
@@ -861,6 +908,10 @@ qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, i
     a.cap = k->capacity_tokens;
     a.max_chunks = k->max_chunks;
     a.n_slots = k->n_tokens;
+    a.n_ctiles = k->n_tokens / QVG_TILE;
+    a.kraw = k_cur;
+    a.vraw = v_cur;
+    a.n_raw = n_cur;
     a.kcodes = k->codes;
     a.vcodes = v->codes;
     a.kscales = k->scales;
@@ -886,7 +937,7 @@ qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, i
     const int d = k->d;
     // split the cache over more CTAs when the query blocks alone leave SMs idle
     // (needs the workspace qvg_workspace_size reports for this Nq, Hq, d)
-    int splits = attention_splits(Nq, Hq, a.n_slots / QVG_TILE);
+    int splits = attention_splits(Nq, Hq, a.n_ctiles + ceil_div(n_cur, QVG_TILE));
     if (splits > 1 && (!workspace || ws_bytes < attention_split_bytes(Nq, Hq, d, splits))) splits = 1;
     float *po = nullptr, *plse = nullptr, *pbest = nullptr;
     int32_t *parg = nullptr;

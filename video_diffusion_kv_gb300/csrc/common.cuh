@@ -141,6 +141,7 @@ qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, 
                              void *out, int out_dtype, cudaStream_t st);
 qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, int Hq,
                                const qvg_cache *k, const qvg_cache *v, float scale_log2,
+                               const uint16_t *k_cur, const uint16_t *v_cur, int n_cur,
                                void *out, int out_dtype, float *lse, int32_t *top1,
                                void *workspace, size_t ws_bytes, cudaStream_t st);
 // Cache splits qvg_attention uses for Nq queries x Hq heads (n_tiles < 0:
