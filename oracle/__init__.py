@@ -63,6 +63,23 @@ def quant_group(r, bits=2, mode=0):
     return s[0], q, rh
 
 
+def quant_group_outlier(r, bits=2, mode=0):
+    """One group with the outlier split: returns (fp16 scale bits, int codes,
+    dequantised fp32, fp16 outlier bits, outlier index or 0xFF)."""
+    lib = _load()
+    r = _f32(r)
+    s = np.zeros(1, np.uint16)
+    q = np.zeros(r.size, np.int32)
+    rh = np.zeros(r.size, np.float32)
+    ov = np.zeros(1, np.uint16)
+    oi = np.zeros(1, np.uint8)
+    rc = lib.orc_quant_group_outlier(_p(r), ct.c_int(r.size), ct.c_int(bits), ct.c_int(mode),
+                                     _p(s), _p(q), _p(rh), _p(ov), _p(oi))
+    if rc != 0:
+        raise ValueError("oracle: outlier split needs 2 <= G <= 100")
+    return s[0], q, rh, ov[0], int(oi[0])
+
+
 def pack_row(q, bits):
     lib = _load()
     q = np.ascontiguousarray(q, dtype=np.int32)
@@ -137,11 +154,12 @@ def psac_encode_token(E, U):
 
 
 def compress_chunk(x, C, L, bits, group, iters, mode=0, seed=0, chunk=0,
-                   qsac_w=None, psac_U=None, cent_in=None, nthreads=1):
+                   qsac_w=None, psac_U=None, cent_in=None, outlier=False, nthreads=1):
     """Compress one chunk x [N,H,d].  Returns a dict with codes [L,H,N,nb],
     scales (fp16 bits) [L,H,N,d/G], ids [L,H,N], cent (bf16 bits) [L,H,C,d],
     means [L,H,C,d], psac_p [H,N,r], psac_s [H,N], xhat [N,H,d] and
-    resid [N,H,d] (the residual after the last stage)."""
+    resid [N,H,d] (the residual after the last stage); with outlier=True
+    also outl_val (fp16 bits) and outl_idx [L,H,N,d/G]."""
     lib = _load()
     x = _f32(x)
     N, H, d = x.shape
@@ -158,6 +176,9 @@ def compress_chunk(x, C, L, bits, group, iters, mode=0, seed=0, chunk=0,
         xhat=np.zeros((N, H, d), np.float32),
         resid=np.zeros((N, H, d), np.float32),
     )
+    if outlier:
+        out["outl_val"] = np.zeros((L, H, N, d // group), np.uint16)
+        out["outl_idx"] = np.zeros((L, H, N, d // group), np.uint8)
     qsac_w = None if qsac_w is None else _f32(qsac_w)
     psac_U = None if psac_U is None else _f32(psac_U)
     cent_in = None if cent_in is None else _f32(cent_in)
@@ -167,7 +188,8 @@ def compress_chunk(x, C, L, bits, group, iters, mode=0, seed=0, chunk=0,
         ct.c_uint64(seed), ct.c_int(chunk), _p(qsac_w), _p(psac_U), ct.c_int(r),
         _p(cent_in), _p(out["codes"]), _p(out["scales"]), _p(out["ids"]),
         _p(out["cent"]), _p(out["means"]), _p(out["psac_p"]), _p(out["psac_s"]),
-        _p(out["xhat"]), _p(out["resid"]), ct.c_int(nthreads))
+        _p(out["xhat"]), _p(out["resid"]), _p(out.get("outl_val")), _p(out.get("outl_idx")),
+        ct.c_int(nthreads))
     if rc != 0:
         raise ValueError("oracle: unsupported compression arguments")
     if C == 0:
@@ -179,7 +201,7 @@ def compress_chunk(x, C, L, bits, group, iters, mode=0, seed=0, chunk=0,
 
 
 def decompress(codes, scales, ids, cent, C, bits, group, psac_p=None,
-               psac_s=None, psac_U=None):
+               psac_s=None, psac_U=None, outl_val=None, outl_idx=None):
     """Rebuild [N,H,d] fp32 from the stored layout (see orc_decompress)."""
     lib = _load()
     L, H, N, _ = codes.shape
@@ -190,6 +212,9 @@ def decompress(codes, scales, ids, cent, C, bits, group, psac_p=None,
     ids = np.ascontiguousarray(ids, np.uint8)
     cent = np.ascontiguousarray(cent, np.uint16) if C > 0 else np.zeros(1, np.uint16)
     r = 0
+    if outl_val is not None:
+        outl_val = np.ascontiguousarray(outl_val, np.uint16)
+        outl_idx = np.ascontiguousarray(outl_idx, np.uint8)
     if psac_p is not None:
         psac_p = np.ascontiguousarray(psac_p, np.int8)
         psac_s = np.ascontiguousarray(psac_s, np.uint16)
@@ -198,7 +223,7 @@ def decompress(codes, scales, ids, cent, C, bits, group, psac_p=None,
     lib.orc_decompress(_p(codes), _p(scales), _p(ids), _p(cent), ct.c_int(N),
                        ct.c_int(H), ct.c_int(d), ct.c_int(C), ct.c_int(L),
                        ct.c_int(bits), ct.c_int(group), _p(psac_p), _p(psac_s),
-                       _p(psac_U), ct.c_int(r), _p(out))
+                       _p(psac_U), ct.c_int(r), _p(outl_val), _p(outl_idx), _p(out))
     return out
 
 

@@ -122,6 +122,66 @@ void orc_quant_group(const float *r, int G, int bits, int mode,
 }
 
 /*
+ * Outlier split ([P2] section 3.4, "outlier separation"): before a block is
+ * quantised, each value whose magnitude is above the block's 99th
+ * percentile is taken out of the block and kept in fp16; the block's scale
+ * and codes come from the values that remain, so one large value no longer
+ * widens the step of all the others.  Readings:
+ *   - the block is the quantisation group (G consecutive channels of one
+ *     token's residual);
+ *   - the percentile is the linear-interpolation one: with the magnitudes
+ *     sorted ascending, a_0 <= ... <= a_{G-1}, position p = 0.99 (G - 1),
+ *     T = a_k + (p - k)(a_{k+1} - a_k), k = floor(p) (numpy's default);
+ *     a value is an outlier when |r| > T, strictly;
+ *   - the fp16 copy saturates at +-65504 (like the scales);
+ *   - an outlier's code is 0 and it is rebuilt as its fp16 value (plus the
+ *     centroid), its channel index within the group kept as a uint8;
+ *   - the side list holds one (value, index) pair per group, index 0xFF
+ *     meaning "none": for G <= 100, p > G - 2, so at most the largest value
+ *     can lie above T.  Larger groups are refused (return -1).
+ * The page's companion "dynamic clipping" (an adaptive per-block range) is
+ * what the per-group scale of the remaining values already is; it gives no
+ * formula for a clip below their maximum, so none is applied.
+ */
+static int cmp_double(const void *a, const void *b) {
+    const double x = *(const double *)a, y = *(const double *)b;
+    return (x > y) - (x < y);
+}
+
+int orc_quant_group_outlier(const float *r, int G, int bits, int mode,
+                            uint16_t *scale_f16, int32_t *q, float *rhat,
+                            uint16_t *outl_f16, uint8_t *outl_idx) {
+    if (G < 2 || G > 100) return -1;
+    double a[100];
+    for (int j = 0; j < G; ++j) a[j] = fabs((double)r[j]);
+    qsort(a, (size_t)G, sizeof(double), cmp_double);
+    const double p = 0.99 * (double)(G - 1);
+    const int k = (int)floor(p);
+    const double T = a[k] + (p - (double)k) * (a[k + 1] - a[k]);
+    int out = -1, count = 0;
+    for (int j = 0; j < G; ++j)
+        if (fabs((double)r[j]) > T) { out = j; ++count; }
+    if (count > 1) return -1;
+    /* quantise the remaining values (the outlier's slot holds 0) */
+    float rest[100];
+    for (int j = 0; j < G; ++j) rest[j] = (j == out) ? 0.0f : r[j];
+    orc_quant_group(rest, G, bits, mode, scale_f16, q, rhat);
+    if (out < 0) {
+        *outl_f16 = 0;
+        *outl_idx = 0xFF;
+        return 0;
+    }
+    float o = r[out];
+    if (o > 65504.0f) o = 65504.0f;
+    if (o < -65504.0f) o = -65504.0f;
+    *outl_f16 = f32_to_f16(o);
+    *outl_idx = (uint8_t)out;
+    q[out] = 0;
+    rhat[out] = f16_to_f32(*outl_f16);
+    return 0;
+}
+
+/*
  * Packing ([QVG] "algorithm-system co-design": 2-bit codes are stored as a
  * packed integer representation).  Reading: offset-binary u = q + 2^{b-1};
  * element j of a row occupies bits [(j*b) mod 8, +b) of byte (j*b)/8.
@@ -313,7 +373,7 @@ void orc_psac_encode_token(const float *E, const float *U, int d, int r,
 /* ------------------------------------------------------------------ */
 
 typedef struct {
-    int C, L, bits, group, iters, mode;
+    int C, L, bits, group, iters, mode, outlier;
     uint64_t seed;
 } orc_params;
 
@@ -334,6 +394,8 @@ typedef struct {
     uint16_t *psac_s;     /* [H][N] */
     float *xhat;          /* [N][H][d] or NULL: sum over stages of dequant */
     float *resid;         /* [N][H][d] or NULL: residual after the last stage */
+    uint16_t *outl_val;   /* [L][H][N][d/G] fp16 (outlier split) */
+    uint8_t *outl_idx;    /* [L][H][N][d/G] channel within the group, 0xFF none */
 } compress_job;
 
 /*
@@ -342,7 +404,9 @@ typedef struct {
  *   stage input X_1 = X (fp32 values of the bf16 chunk), X_{l+1} = X_l - deq_l;
  *   clustering operand = X_1 (stage 1) or bf16(X_l) (later stages, reading);
  *   k-means: init, `iters` x (assign, update), one final assign;
- *   residual R = X_l - C_id (fp32), per-group quantisation, deq_l = S'q + C_id;
+ *   residual R = X_l - C_id (fp32), per-group quantisation (with the
+ *   outlier split when p->outlier), deq_l = S'q + C_id (fp16 outlier + C_id
+ *   at an outlier's channel);
  *   reconstruction = deq_1 + deq_2 + ... (fp32, stage order).
  * C = 0 is plain per-group quantisation (RTN): no centroid.
  * C > N clusters with C_eff = N; centroid rows C_eff..C-1 are stored as 0.
@@ -404,9 +468,14 @@ static void compress_head(const compress_job *J, int h) {
             J->ids[lh * N + n] = (uint8_t)ids[n];
             for (int j = 0; j < d; ++j) rr[j] = (C > 0) ? xr[j] - cr[j] : xr[j];
             for (int gi = 0; gi < ng; ++gi) {
-                orc_quant_group(rr + gi * G, G, bits, p->mode,
-                                &J->scales[(lh * N + n) * ng + gi], q + gi * G,
-                                rh + gi * G);
+                const size_t gidx = (lh * N + n) * ng + gi;
+                if (p->outlier)
+                    orc_quant_group_outlier(rr + gi * G, G, bits, p->mode, &J->scales[gidx],
+                                            q + gi * G, rh + gi * G, &J->outl_val[gidx],
+                                            &J->outl_idx[gidx]);
+                else
+                    orc_quant_group(rr + gi * G, G, bits, p->mode, &J->scales[gidx], q + gi * G,
+                                    rh + gi * G);
             }
             orc_pack_row(q, d, bits, &J->codes[(lh * N + n) * nb]);
             for (int j = 0; j < d; ++j) deq[j] = (C > 0) ? rh[j] + cr[j] : rh[j];
@@ -479,15 +548,17 @@ int orc_compress_chunk(const float *x, int N, int H, int d, int C, int L,
                        int psac_r, const float *cent_in, uint8_t *codes,
                        uint16_t *scales, uint8_t *ids, uint16_t *cent,
                        float *means, int8_t *psac_p, uint16_t *psac_s,
-                       float *xhat, float *resid, int nthreads) {
+                       float *xhat, float *resid, uint16_t *outl_val,
+                       uint8_t *outl_idx, int nthreads) {
+    const int outlier = outl_val != NULL;
     if (N < 1 || H < 1 || d < 1 || d > 1024 || L < 1 || group < 1 ||
         d % group != 0 || (bits != 2 && bits != 4) || (d * bits) % 8 != 0 ||
         C < 0 || C > 256 || iters < 0 || (mode == 1 && bits != 2) ||
-        psac_r > 64)
+        psac_r > 64 || (outlier && (!outl_idx || group < 2 || group > 100)))
         return -1;
-    compress_job J = {x, N, H, d, chunk, {C, L, bits, group, iters, mode, seed},
+    compress_job J = {x, N, H, d, chunk, {C, L, bits, group, iters, mode, outlier, seed},
                       qsac_w, psac_U, psac_r, cent_in, codes, scales, ids,
-                      cent, means, psac_p, psac_s, xhat, resid};
+                      cent, means, psac_p, psac_s, xhat, resid, outl_val, outl_idx};
     run_units(compress_unit, &J, H, nthreads);
     return 0;
 }
@@ -499,15 +570,17 @@ int orc_compress_chunk(const float *x, int N, int H, int d, int C, int L,
 /*
  * Rebuild X_hat = sum_l (S'_l q_l + C_{l,id}) from stored codes, fp16
  * scales, ids and bf16 centroids ([QVG] "overall framework": dequant adds
- * S_X * X_INT + C_i back), fp32, in stage order; plus, when PSAC data are
- * given, the correction P_hat U^T computed in fp64.  Layouts as in
- * orc_compress_chunk with N tokens.  out is [N][H][d].
+ * S_X * X_INT + C_i back), fp32, in stage order; at a split-off outlier's
+ * channel the stage's term is its fp16 value + C_{l,id} ([P2] section 3.4);
+ * plus, when PSAC data are given, the correction P_hat U^T computed in
+ * fp64.  Layouts as in orc_compress_chunk with N tokens.  out is [N][H][d].
  */
 int orc_decompress(const uint8_t *codes, const uint16_t *scales,
                    const uint8_t *ids, const uint16_t *cent, int N, int H,
                    int d, int C, int L, int bits, int group,
                    const int8_t *psac_p, const uint16_t *psac_s,
-                   const float *psac_U, int psac_r, float *out) {
+                   const float *psac_U, int psac_r, const uint16_t *outl_val,
+                   const uint8_t *outl_idx, float *out) {
     const int nb = d * bits / 8, ng = d / group;
     int32_t q[1024];
     for (int h = 0; h < H; ++h)
@@ -518,8 +591,10 @@ int orc_decompress(const uint8_t *codes, const uint16_t *scales,
                 const size_t lh = (size_t)l * H + h;
                 orc_unpack_row(&codes[(lh * N + n) * nb], d, bits, q);
                 for (int j = 0; j < d; ++j) {
-                    const float S = f16_to_f32(scales[(lh * N + n) * ng + j / group]);
+                    const size_t gidx = (lh * N + n) * ng + j / group;
+                    const float S = f16_to_f32(scales[gidx]);
                     float v = S * (float)q[j];
+                    if (outl_val && outl_idx[gidx] == j % group) v = f16_to_f32(outl_val[gidx]);
                     if (C > 0) v = v + bf16_to_f32(cent[(lh * C + ids[lh * N + n]) * d + j]);
                     acc[j] = acc[j] + v;
                 }

@@ -430,3 +430,92 @@ def test_psac_encode(orc):
     e0 = np.linalg.norm((x - out["xhat"]).astype(np.float64) @ U)
     e1 = np.linalg.norm((x - rebuilt).astype(np.float64) @ U)
     assert e1 < 0.1 * e0
+
+
+# ---------------------------------------------------------------- outlier split
+
+def test_outlier_split_hand_example(orc):
+    """G = 8, INT2 (q in [-2, 1], S = amax / 1).  |r| sorted is
+    [0, .25, .5, .5, .75, 1, 1, 12]; the 99th percentile sits at position
+    0.99 * 7 = 6.93, T = 1 + 0.93 * (12 - 1) = 11.23, so only 12.0 (channel
+    3) is split off.  The remaining amax is 1, S = 1, and round-half-even
+    gives codes [0, -1, 0, 0, -1, 0, 1, 0]; 12.0 is kept as fp16 0x4A00."""
+    r = np.array([0.5, -1.0, 0.25, 12.0, -0.75, 0.0, 1.0, -0.5], np.float32)
+    s, q, rh, ov, oi = orc.quant_group_outlier(r, bits=2)
+    assert s == 0x3C00 and oi == 3 and ov == 0x4A00
+    np.testing.assert_array_equal(q, [0, -1, 0, 0, -1, 0, 1, 0])
+    np.testing.assert_array_equal(rh, [0, -1, 0, 12.0, -1, 0, 1, 0])
+    # without the split the outlier sets the step: S = 12, every small value -> 0
+    s0, q0, _ = orc.quant_group(r, bits=2)
+    assert s0 == 0x4A00 and np.count_nonzero(q0) == 1
+
+
+@pytest.mark.parametrize("G", [8, 16, 32, 64])
+def test_outlier_split_is_the_p99_exceedance(orc, G):
+    """The split-off channel is exactly the set {j : |r_j| > P99(|r|)} of
+    numpy's percentile (linear interpolation), on random groups with and
+    without a planted outlier and with ties at the top (no split)."""
+    rng = np.random.default_rng(40 + G)
+    for t in range(300):
+        r = rng.standard_normal(G).astype(np.float32)
+        if t % 3 == 0:
+            r[rng.integers(G)] *= 50.0
+        if t % 7 == 0:  # a tie for the largest magnitude: nothing is split off
+            i, j = rng.choice(G, 2, replace=False)
+            r[i] = np.float32(2 * np.abs(r).max())
+            r[j] = -r[i]
+        a = np.abs(r.astype(np.float64))
+        want = np.nonzero(a > np.percentile(a, 99))[0]
+        s, q, rh, ov, oi = orc.quant_group_outlier(r, bits=2)
+        assert len(want) <= 1
+        if t % 7 == 0:
+            assert len(want) == 0
+        if len(want):
+            assert oi == want[0]
+            assert rh[oi] == orc.f16_bits_to_f32(np.array([ov], np.uint16))[0]
+            assert abs(rh[oi] - r[oi]) <= 2 ** -11 * abs(r[oi])
+            rest = np.delete(r, oi)
+        else:
+            assert oi == 0xFF and ov == 0
+            rest = r
+        # the scale is the plain quantiser's on the remaining values
+        S = orc.f16_bits_to_f32(np.array([s], np.uint16))[0]
+        assert S == orc.f16_bits_to_f32(np.array([orc.quant_group(rest, bits=2)[0]], np.uint16))[0]
+        keep = np.arange(G) != (oi if oi != 0xFF else -1)
+        # unclipped kept values are within half a step
+        inside = keep & (np.abs(r) <= S)
+        assert np.all(np.abs(r[inside] - rh[inside]) <= S / 2)
+
+
+def test_outlier_split_refuses_large_groups(orc):
+    with pytest.raises(ValueError):
+        orc.quant_group_outlier(np.ones(128, np.float32))
+
+
+def test_outlier_split_lowers_error_and_rebuilds(orc):
+    """On synthetic K and V with token-varying outlier channels (x50 K,
+    x300 V) the split lowers the reconstruction error of QVG and of RTN; the
+    stored layout (codes, scales, side list) rebuilds X_hat exactly; at most
+    one value per group is split off."""
+    w = synth.WORKLOADS["tiny"]
+    for kind in (synth.KIND_K, synth.KIND_V):
+        x = synth.chunk_kv(w, 11, 0, kind)
+        for C in (16, 0):
+            base = orc.compress_chunk(x, C=C, L=1, bits=2, group=32, iters=10 if C else 0)
+            out = orc.compress_chunk(x, C=C, L=1, bits=2, group=32, iters=10 if C else 0, outlier=True)
+            np.testing.assert_array_equal(out["ids"], base["ids"])  # clustering is unchanged
+            assert _rel_err(x, out["xhat"]) < _rel_err(x, base["xhat"])
+            rebuilt = orc.decompress(out["codes"], out["scales"], out["ids"], out["cent"], C, 2, 32,
+                                     outl_val=out["outl_val"], outl_idx=out["outl_idx"])
+            np.testing.assert_array_equal(rebuilt, out["xhat"])
+            oi = out["outl_idx"]
+            assert np.all((oi < 32) | (oi == 0xFF))
+            assert np.all(out["outl_val"][oi == 0xFF] == 0)
+    # two stages: the second stage splits its own residual's outliers
+    x = synth.chunk_kv(w, 11, 1, synth.KIND_V)
+    one = orc.compress_chunk(x, C=16, L=1, bits=2, group=32, iters=10, outlier=True)
+    two = orc.compress_chunk(x, C=16, L=2, bits=2, group=32, iters=10, outlier=True)
+    rebuilt = orc.decompress(two["codes"], two["scales"], two["ids"], two["cent"], 16, 2, 32,
+                             outl_val=two["outl_val"], outl_idx=two["outl_idx"])
+    np.testing.assert_array_equal(rebuilt, two["xhat"])
+    assert _rel_err(x, two["xhat"]) <= _rel_err(x, one["xhat"])
