@@ -601,6 +601,84 @@ def study_rollout(args):
     return 0
 
 
+def study_outlier(args):
+    """Outlier split on the LongCat-like layer (16 heads, d=128, 8 chunks of
+    4680 tokens, C=256, INT2 G=64): with and without the split, the
+    relative Frobenius error of K and V over the whole cache, the
+    compression ratio counting the side list, the time to compress the
+    newest chunk (K and V) and the attention of its 4680 queries over the
+    whole compressed cache (median of 5, L2 flushed before each)."""
+    import statistics
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import video_diffusion_kv_gb300 as qvg
+    from video_diffusion_kv_gb300 import synth
+    w = synth.WORKLOADS["longcat"]
+    seed = 12
+    per = -(-w.N // 128) * 128
+    ks = [synth.chunk_kv(w, seed, k, synth.KIND_K) for k in range(w.n_chunks)]
+    vs = [synth.chunk_kv(w, seed, k, synth.KIND_V) for k in range(w.n_chunks)]
+    q = synth_dev(synth.queries(w, seed, w.n_chunks - 1), "cuda")
+    kd = [synth_dev(x, "cuda") for x in ks]
+    vd = [synth_dev(x, "cuda") for x in vs]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    keep = np.concatenate([np.arange(k * per, k * per + w.N) for k in range(w.n_chunks)])
+    arms = {}
+    for name, flags in (("plain", 0), ("outlier_split", qvg.QVG_OUTLIER)):
+        p = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=seed, flags=flags)
+        kc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks)
+        vc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks)
+        ws = torch.empty(max(qvg.workspace_size(p, qvg.QVG_OP_COMPRESS, w.N, w.H, w.d), 1), dtype=torch.uint8,
+                         device="cuda")
+        for k in range(w.n_chunks):
+            qvg.compress_chunk(p, kd[k], kc, workspace=ws)
+            qvg.compress_chunk(p, vd[k], vc, workspace=ws)
+        errs = {}
+        for nm, c, xs in (("K", kc, ks), ("V", vc, vs)):
+            xh = qvg.decompress(p, c, 0, c.n_tokens).cpu().numpy()[keep]
+            errs[nm] = _rel(np.concatenate(xs, 0), xh)
+        last = w.n_chunks - 1
+
+        def timed(fn):
+            ts = []
+            for rep in range(7):
+                kc.reset(last, last * per)
+                vc.reset(last, last * per)
+                if fn is attend:  # attention reads the whole cache: put the newest chunk back
+                    kc.reset(last + 1, (last + 1) * per)
+                    vc.reset(last + 1, (last + 1) * per)
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                if rep >= 2:
+                    ts.append(e0.elapsed_time(e1))
+            return statistics.median(ts)
+
+        def compress():
+            qvg.compress_chunk(p, kd[last], kc, workspace=ws)
+            qvg.compress_chunk(p, vd[last], vc, workspace=ws)
+
+        def attend():
+            qvg.attention(p, q, kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out)
+
+        tcs = timed(compress)
+        ms_a = timed(attend)
+        arms[name] = {"rel_err_K": errs["K"], "rel_err_V": errs["V"],
+                      "ratio": qvg.compression_ratio(p, w.H, w.d, w.N, w.n_chunks),
+                      "compress_ms_KV": tcs, "attention_ms": ms_a,
+                      "attention_TFLOP/s": 4.0 * w.Nq * w.tokens * w.d * w.Hq / ms_a / 1e9}
+    print(json.dumps({"study": "outlier", "workload": "16 heads, d=128, 8 chunks x 4680 tokens, C=256, INT2 G=64, 8 iters",
+                      "status": qvg.get_status(), "arms": arms}), flush=True)
+    return 0
+
+
 def synth_dev(a, dev):
     import torch
     return torch.from_numpy(a).to(dev, torch.bfloat16).contiguous()
@@ -615,7 +693,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="time the device step only (profiling)")
     ap.add_argument("--cache-chunks", type=int, default=None, help="smaller cache (profiling cases)")
-    ap.add_argument("--workload", default="longcat", choices=["longcat", "qvgpro", "quantwm", "rollout"],
+    ap.add_argument("--workload", default="longcat", choices=["longcat", "qvgpro", "quantwm", "rollout", "outlier"],
                     help="longcat: the benchmark line; the others print their study line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "own":
@@ -623,7 +701,8 @@ def main():
     if args.impl == "reference":
         return run_reference(args)
     if args.workload != "longcat":
-        return {"qvgpro": study_qvgpro, "quantwm": study_quantwm, "rollout": study_rollout}[args.workload](args)
+        return {"qvgpro": study_qvgpro, "quantwm": study_quantwm, "rollout": study_rollout,
+                "outlier": study_outlier}[args.workload](args)
     return run_own(args)
 
 

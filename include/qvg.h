@@ -51,11 +51,14 @@ typedef enum {
 #define QVG_PSAC 2            /* store the rank-8 key-error projection            */
 #define QVG_GIVEN_CENTROIDS 4 /* start k-means from centroids the caller wrote   */
                               /* into this chunk's centroid slot                 */
+#define QVG_OUTLIER 8         /* outlier split in the residual quantiser: per    */
+                              /* group, a value above the group's P99 is kept   */
+                              /* in fp16 (G <= 64; see outl_val below)           */
 
 #define QVG_TILE 128      /* chunks start at multiples of this many token slots */
 #define QVG_PSAC_RANK 8   /* PSAC subspace rank ([QWM] PSAC: top-8 directions)  */
 #define QVG_MAX_CLUSTERS 256
-#define QVG_CACHE_NBUF 10
+#define QVG_CACHE_NBUF 12
 
 /* Output element types of qvg_decompress / qvg_attention. */
 #define QVG_OUT_F32 0
@@ -115,6 +118,15 @@ typedef struct {
  *   psac_s     fp16  [H][capacity]     PSAC per-token scales (or NULL).
  *   psac_basis fp32  [max_chunks][H][d][8] basis each chunk was encoded with
  *              (or NULL).
+ *   outl_val   fp16  [L][H][capacity][d/G]  outlier split ([P2] section 3.4,
+ *              "outlier separation"; with QVG_OUTLIER, else NULL): per group
+ *              of a stage's residual, the value above the group's 99th
+ *              percentile of |r| (linear interpolation; for G <= 100 at most
+ *              the largest), fp16, saturated at 65504.  The group's scale and
+ *              codes come from the other values; the outlier's code is 0 and
+ *              it is rebuilt as outl_val + centroid.
+ *   outl_idx   uint8 [L][H][capacity][d/G]  its channel within the group,
+ *              0xFF when no value lies above the percentile (0 in outl_val).
  * n_chunks and n_tokens are host-side counters that qvg_compress_chunk
  * advances; set both to 0 for an empty cache.  A cache can be saved and
  * restored by copying its buffers and these two counters.
@@ -136,6 +148,8 @@ typedef struct {
     int8_t *psac_p;
     uint16_t *psac_s;
     float *psac_basis;
+    uint16_t *outl_val;
+    uint8_t *outl_idx;
 } qvg_cache;
 
 /* Text for a status code (static storage; never NULL). */
@@ -143,9 +157,9 @@ const char *qvg_status_string(qvg_status s);
 
 /*
  * Bytes of each cache buffer, in the order codes, scales, ids, cent,
- * chunk_start, chunk_len, tile_chunk, psac_p, psac_s, psac_basis
- * (out_sizes has QVG_CACHE_NBUF entries).  The PSAC entries are 0 unless
- * p->flags has QVG_PSAC.  capacity_tokens must be a positive multiple of
+ * chunk_start, chunk_len, tile_chunk, psac_p, psac_s, psac_basis, outl_val,
+ * outl_idx (out_sizes has QVG_CACHE_NBUF entries).  The PSAC entries are 0
+ * unless p->flags has QVG_PSAC, the outlier entries 0 unless QVG_OUTLIER.  capacity_tokens must be a positive multiple of
  * QVG_TILE.  The total is the compressed footprint; [P1] section 1 gives
  * the uncompressed one, 2 (K and V) x layers x heads x head_dim x tokens x
  * bytes per element.

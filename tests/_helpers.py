@@ -34,6 +34,10 @@ def host_cache(c: qvg.CompressedKV):
         out["psac_p"] = c.view("psac_p", torch.int8, (H, cap, 8)).cpu().numpy()
         out["psac_s"] = c.view("psac_s", torch.int16, (H, cap)).cpu().numpy().view(np.uint16)
         out["psac_basis"] = c.view("psac_basis", torch.float32, (c.max_chunks, H, d, 8)).cpu().numpy()
+    if p.flags & qvg.QVG_OUTLIER:
+        ng = d // p.group
+        out["outl_val"] = c.view("outl_val", torch.int16, (L, H, cap, ng)).cpu().numpy().view(np.uint16)
+        out["outl_idx"] = c.view("outl_idx", torch.uint8, (L, H, cap, ng)).cpu().numpy()
     return out
 
 
@@ -54,9 +58,11 @@ def oracle_rebuild(hc, p, k):
     """Oracle reconstruction [N,H,d] of chunk k from the GPU's stored bytes."""
     codes, scales, ids, cent = chunk_arrays(hc, p, k)
     kw = {}
+    sl = chunk_slice(hc, k)
     if "psac_p" in hc:
-        sl = chunk_slice(hc, k)
         kw = dict(psac_p=hc["psac_p"][:, sl], psac_s=hc["psac_s"][:, sl], psac_U=hc["psac_basis"][k])
+    if "outl_val" in hc:
+        kw.update(outl_val=hc["outl_val"][:, :, sl], outl_idx=hc["outl_idx"][:, :, sl])
     return oracle.decompress(codes, scales, ids, cent, p.C, p.bits, p.group, **kw)
 
 

@@ -112,7 +112,7 @@ def test_unsupported_head_dim(lib):
 def _fake_cache(H=2, d=64, cap=512, max_chunks=2, n_chunks=0, n_tokens=0):
     # Pointers are never dereferenced: every case below fails validation first.
     fake = ct.c_void_p(0x1000)
-    return qvg._Cache(H, d, cap, max_chunks, n_chunks, n_tokens, *([fake] * 10))
+    return qvg._Cache(H, d, cap, max_chunks, n_chunks, n_tokens, *([fake] * qvg.QVG_CACHE_NBUF))
 
 
 def test_compress_rejects_on_host(lib):
@@ -148,6 +148,25 @@ def test_attention_and_decompress_reject_on_host(lib):
     assert lib.qvg_attention(ct.byref(p), q, 4, 2, ct.byref(empty), ct.byref(empty), 0.0, o, 0, None, None, None, 0, None) == qvg.QVG_ERR_INVALID_ARG
     assert lib.qvg_decompress(ct.byref(p), ct.byref(k), 0, 200, o, 0, None) == qvg.QVG_ERR_INVALID_ARG
     assert lib.qvg_decompress(ct.byref(p), ct.byref(k), -1, 10, o, 0, None) == qvg.QVG_ERR_INVALID_ARG
+
+
+def test_outlier_split_arguments(lib):
+    """QVG_OUTLIER: groups above 64 channels are refused (above 100 values a
+    group can hold more than one value over its P99); the cache must carry
+    the two side-list buffers, which qvg_cache_bytes sizes."""
+    p = _params(C=16, group=32, flags=qvg.QVG_OUTLIER)
+    out = (ct.c_size_t * qvg.QVG_CACHE_NBUF)()
+    assert lib.qvg_cache_bytes(ct.byref(p), 2, 64, 512, 2, out) == qvg.QVG_OK
+    assert out[10] == 2 * 512 * 2 * 2 and out[11] == 2 * 512 * 2
+    p0 = _params(C=16, group=32)
+    assert lib.qvg_cache_bytes(ct.byref(p0), 2, 64, 512, 2, out) == qvg.QVG_OK
+    assert out[10] == 0 and out[11] == 0
+    big = _params(C=16, group=128, flags=qvg.QVG_OUTLIER)
+    assert lib.qvg_cache_bytes(ct.byref(big), 2, 128, 512, 2, out) == qvg.QVG_ERR_UNSUPPORTED
+    c = _fake_cache()
+    c.outl_val = None
+    x, ws = ct.c_void_p(0x2000), ct.c_void_p(0x100000)
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 100, None, None, ct.byref(c), ws, 1 << 30, None) == qvg.QVG_ERR_INVALID_ARG
 
 
 def test_attention_ar_rejects_on_host(lib):

@@ -47,7 +47,13 @@ CASES = {
     "page1_scale": (W["tiny"], qvg.Params(C=16, L=1, bits=2, group=32, iters=10, scale_mode=1, seed=6), 2),
     "rtn": (W["tiny"], qvg.Params(C=0, L=1, bits=2, group=32, iters=0), 2),
     "longcat": (W["longcat"], qvg.Params(C=256, L=1, bits=2, group=64, iters=8, seed=7), 2),
+    # outlier split (fp16 side list of each group's value above its P99)
+    "tiny_outlier": (W["tiny"], qvg.Params(C=16, L=1, bits=2, group=32, iters=10, seed=24, flags=qvg.QVG_OUTLIER), 2),
+    "pro_outlier_L2": (W["qvgpro"], qvg.Params(C=16, L=2, bits=2, group=32, iters=10, seed=25, flags=qvg.QVG_OUTLIER), 2),
+    "rtn_outlier_g8": (W["tiny"], qvg.Params(C=0, L=1, bits=4, group=8, iters=0, flags=qvg.QVG_OUTLIER), 2),
+    "longcat_outlier": (W["longcat"], qvg.Params(C=256, L=1, bits=2, group=64, iters=8, seed=26, flags=qvg.QVG_OUTLIER), 2),
 }
+OUTL = lambda p: bool(p.flags & qvg.QVG_OUTLIER)
 
 
 def _new_cache(w, p, n_chunks, N=None):
@@ -63,7 +69,8 @@ def _check_against_fed_oracle(x, hc, p, k, w=None, psac_U=None):
     codes, scales, ids, cent = chunk_arrays(hc, p, k)
     cent_in = oracle.bf16_bits_to_f32(cent) if p.C > 0 else None
     o = oracle.compress_chunk(x, C=p.C, L=p.L, bits=p.bits, group=p.group, iters=0, mode=p.scale_mode,
-                              seed=p.seed, chunk=k, qsac_w=w, psac_U=psac_U, cent_in=cent_in, nthreads=NT)
+                              seed=p.seed, chunk=k, qsac_w=w, psac_U=psac_U, cent_in=cent_in, outlier=OUTL(p),
+                              nthreads=NT)
     N, H = x.shape[0], x.shape[1]
     ok_rows = np.ones((H, N), bool)
     total = near = 0
@@ -80,12 +87,17 @@ def _check_against_fed_oracle(x, hc, p, k, w=None, psac_U=None):
                 near += m
                 assert far == 0, ("assignment mismatch outside near ties", l, h, far)
                 ok_rows[h] &= ids[l, h] == o["ids"][l, h]
+        sl = chunk_slice(hc, k)
         for h in range(H):
             np.testing.assert_array_equal(codes[l, h][ok_rows[h]], o["codes"][l, h][ok_rows[h]])
             np.testing.assert_array_equal(scales[l, h][ok_rows[h]], o["scales"][l, h][ok_rows[h]])
+            if OUTL(p):
+                np.testing.assert_array_equal(hc["outl_idx"][l, h, sl][ok_rows[h]], o["outl_idx"][l, h][ok_rows[h]])
+                np.testing.assert_array_equal(hc["outl_val"][l, h, sl][ok_rows[h]], o["outl_val"][l, h][ok_rows[h]])
         # next stage input from the oracle's own residual (bit-exact on ok rows)
+        kw = dict(outl_val=o["outl_val"][l:l + 1], outl_idx=o["outl_idx"][l:l + 1]) if OUTL(p) else {}
         dq = oracle.decompress(o["codes"][l:l + 1], o["scales"][l:l + 1], o["ids"][l:l + 1],
-                               o["cent"][l:l + 1], p.C, p.bits, p.group)
+                               o["cent"][l:l + 1], p.C, p.bits, p.group, **kw)
         stage_in = stage_in - dq
     if total:
         assert near <= max(1, NEAR_TIE_RATE * total), ("near ties", near, total)
@@ -114,7 +126,7 @@ def test_compress_matches_oracle(name):
         # the oracle's own full run reaches the same reconstruction error
         for k in range(n_chunks):
             o = oracle.compress_chunk(xs[k], C=p.C, L=p.L, bits=p.bits, group=p.group, iters=p.iters,
-                                      mode=p.scale_mode, seed=p.seed, chunk=k, nthreads=NT)
+                                      mode=p.scale_mode, seed=p.seed, chunk=k, outlier=OUTL(p), nthreads=NT)
             rg = np.linalg.norm(xs[k] - oracle_rebuild(hc, p, k)) / np.linalg.norm(xs[k])
             ro = np.linalg.norm(xs[k] - o["xhat"]) / np.linalg.norm(xs[k])
             assert abs(rg - ro) <= 0.05 * ro + 1e-6, (rg, ro)
@@ -167,8 +179,9 @@ def test_lloyd_update_step(name):
     assert exact >= 0.99 * w.H * p0.C * w.d
 
 
-def test_decompress_exact_and_bf16():
-    w, p, n_chunks = CASES["pro_int2_L3"]
+@pytest.mark.parametrize("name", ["pro_int2_L3", "pro_outlier_L2", "rtn_outlier_g8"])
+def test_decompress_exact_and_bf16(name):
+    w, p, n_chunks = CASES[name]
     kc = _new_cache(w, p, n_chunks)
     for k in range(n_chunks):
         qvg.compress_chunk(p, to_dev(synth.chunk_kv(w, 14, k, synth.KIND_V)), kc)
@@ -204,6 +217,28 @@ def _oracle_attention_on(kc, vc, p, q, rows=None):
 
 def _slot_of_token(hk, n_chunks):
     return np.concatenate([np.arange(hk["start"][k], hk["start"][k] + hk["length"][k]) for k in range(n_chunks)])
+
+
+def _assert_top1(top1, q, kh, slots, ram, min_agree=0.95):
+    """Top-1 slots: equal to the oracle's argmax except at near ties, where
+    the GPU's pick must be within the fp16 rounding of the logits of the
+    best: q and k_hat enter the tensor core as fp16 (relative rounding
+    2^-11 each), so a logit moves by at most ~2^-10 sum_j |q_j k_j|; the
+    bound allows 2^-9."""
+    Nq, Hq, d = q.shape
+    H = kh.shape[1]
+    tok_of = {int(s): i for i, s in enumerate(slots)}
+    agree = (top1 == slots[ram])
+    assert agree.mean() >= min_agree, agree.mean()
+    for hq, i in zip(*np.nonzero(~agree)):
+        h = hq // (Hq // H)
+        t_gpu = tok_of[int(top1[hq, i])]
+        t_ref = int(ram[hq, i])
+        qq = q[i, hq].astype(np.float64)
+        s_gpu = qq @ kh[t_gpu, h].astype(np.float64)
+        s_ref = qq @ kh[t_ref, h].astype(np.float64)
+        mag = np.abs(qq) @ np.maximum(np.abs(kh[t_gpu, h]), np.abs(kh[t_ref, h])).astype(np.float64)
+        assert s_ref - s_gpu <= 2 ** -9 * mag, (hq, i, s_ref - s_gpu, mag)
 
 
 def _assert_attention(got, ref, Hq):
@@ -362,6 +397,53 @@ def test_attention_ar_longcat(Nq):
     assert (top1.cpu().numpy()[:, rows] == rtop).mean() >= 0.95
     # current-chunk slots are numbered after the cache
     assert top1.max().item() < kc.n_tokens + len(k_cur)
+
+
+@pytest.mark.parametrize("name", ["tiny_outlier", "pro_outlier_L2", "rtn_outlier_g8"])
+def test_attention_with_outlier_split(name):
+    """Attention and the AR step over caches whose K and V carry the
+    outlier side list (one and two stages, RTN with G = 8), against the fp64
+    oracle on the rebuild of the same bytes."""
+    w, p, n_chunks = CASES[name]
+    chunks = [(synth.chunk_kv(w, 27, k, synth.KIND_K), synth.chunk_kv(w, 27, k, synth.KIND_V)) for k in range(n_chunks)]
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    q = synth.queries(w, 27, n_chunks)
+    out, lse, top1 = qvg.attention(p, to_dev(q), kc, vc, want_lse=True, want_top1=True)
+    ref, rlse, ram, kh, hk = _oracle_attention_on(kc, vc, p, q)
+    _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
+    np.testing.assert_allclose(lse.cpu().numpy(), rlse, atol=2e-3, rtol=0)
+    _assert_top1(top1.cpu().numpy(), q, kh, _slot_of_token(hk, n_chunks), ram)
+    kr = synth.chunk_kv(w, 27, n_chunks, synth.KIND_K)[:150]
+    vr = synth.chunk_kv(w, 27, n_chunks, synth.KIND_V)[:150]
+    out, _, _ = qvg.attention_ar(p, to_dev(q), kc, vc, to_dev(kr), to_dev(vr))
+    ref, _, _ = _oracle_ar(kc, vc, p, q, kr, vr)
+    _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
+
+
+def test_outlier_split_longcat():
+    """LongCat-like chunks (16 heads, d=128, C=256, INT2 G=64): the split
+    lowers the GPU's reconstruction error of V (x300 outlier channels) and
+    of K, and attention over the split cache matches the oracle on 64
+    sampled query rows."""
+    w, p, _ = CASES["longcat_outlier"]
+    p0 = qvg.Params(**{**p.__dict__, "flags": 0})
+    errs = {}
+    for name, pp in (("split", p), ("plain", p0)):
+        for kind in (synth.KIND_K, synth.KIND_V):
+            x = synth.chunk_kv(w, 28, 0, kind)
+            c = _new_cache(w, pp, 1)
+            qvg.compress_chunk(pp, to_dev(x), c)
+            xh = qvg.decompress(pp, c, 0, w.N).cpu().numpy()
+            errs[name, kind] = np.linalg.norm(x - xh) / np.linalg.norm(x)
+    for kind in (synth.KIND_K, synth.KIND_V):
+        assert errs["split", kind] < errs["plain", kind], errs
+    chunks = [(synth.chunk_kv(w, 28, k, synth.KIND_K), synth.chunk_kv(w, 28, k, synth.KIND_V)) for k in range(2)]
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    q = synth.queries(w, 28, 2)
+    out, _, _ = qvg.attention(p, to_dev(q), kc, vc)
+    rows = np.random.default_rng(3).choice(q.shape[0], 64, replace=False)
+    ref, _, _, _, _ = _oracle_attention_on(kc, vc, p, q, rows)
+    _assert_attention(out.cpu().numpy()[rows].astype(np.float64), ref, w.Hq)
 
 
 def test_ragged_and_degenerate_chunks():

@@ -21,10 +21,10 @@ LIB_PATH = os.path.join(_HERE, "libqvg.so")
 
 QVG_OK, QVG_ERR_INVALID_ARG, QVG_ERR_UNSUPPORTED, QVG_ERR_CUDA = 0, 1, 2, 3
 QVG_ERR_TIMEOUT, QVG_ERR_WORKSPACE, QVG_ERR_CAPACITY = 4, 5, 6
-QVG_QSAC, QVG_PSAC, QVG_GIVEN_CENTROIDS = 1, 2, 4
+QVG_QSAC, QVG_PSAC, QVG_GIVEN_CENTROIDS, QVG_OUTLIER = 1, 2, 4, 8
 QVG_TILE = 128
 QVG_PSAC_RANK = 8
-QVG_CACHE_NBUF = 10
+QVG_CACHE_NBUF = 12
 QVG_OUT_F32, QVG_OUT_BF16 = 0, 1
 QVG_OP_COMPRESS, QVG_OP_ATTENTION, QVG_OP_PSAC_BASIS = 0, 1, 2
 
@@ -36,7 +36,7 @@ EXPORTED = (
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 BUFFER_NAMES = ("codes", "scales", "ids", "cent", "chunk_start", "chunk_len", "tile_chunk",
-                "psac_p", "psac_s", "psac_basis")
+                "psac_p", "psac_s", "psac_basis", "outl_val", "outl_idx")
 
 
 class QvgError(RuntimeError):
@@ -57,7 +57,7 @@ class _Cache(ct.Structure):
                 ("codes", ct.c_void_p), ("scales", ct.c_void_p), ("ids", ct.c_void_p),
                 ("cent", ct.c_void_p), ("chunk_start", ct.c_void_p), ("chunk_len", ct.c_void_p),
                 ("tile_chunk", ct.c_void_p), ("psac_p", ct.c_void_p), ("psac_s", ct.c_void_p),
-                ("psac_basis", ct.c_void_p)]
+                ("psac_basis", ct.c_void_p), ("outl_val", ct.c_void_p), ("outl_idx", ct.c_void_p)]
 
 
 _lib = None
@@ -338,10 +338,13 @@ def get_status():
 
 def compression_ratio(params: Params, H, d, tokens_per_chunk, n_chunks, with_psac=False):
     """bf16 bytes / compressed bytes for n_chunks chunks, counting codes,
-    fp16 scales, 1-byte ids, bf16 centroids and (optionally) the PSAC data,
-    at the stored sizes (padding slots excluded)."""
+    fp16 scales, 1-byte ids, bf16 centroids, the outlier side list (fp16
+    value + 1-byte channel per group and stage, with QVG_OUTLIER) and
+    (optionally) the PSAC data, at the stored sizes (padding slots
+    excluded)."""
     N = tokens_per_chunk * n_chunks
-    per_tok = params.L * (d * params.bits / 8 + 2 * d / params.group + (1 if params.C > 0 else 0))
+    side = 3 * d / params.group if params.flags & QVG_OUTLIER else 0
+    per_tok = params.L * (d * params.bits / 8 + 2 * d / params.group + (1 if params.C > 0 else 0) + side)
     if with_psac:
         per_tok += QVG_PSAC_RANK + 2
     comp = H * N * per_tok + params.L * H * n_chunks * params.C * d * 2

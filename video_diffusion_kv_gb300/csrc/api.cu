@@ -37,7 +37,7 @@ qvg_status check_params(const qvg_params *p, int d) {
     if (!p) return QVG_ERR_INVALID_ARG;
     if (p->reserved != 0 || p->L < 1 || p->L > 16 || p->C < 0 || p->iters < 0 ||
         p->iters > 10000 || (p->bits != 2 && p->bits != 4) || p->group < 1 ||
-        (p->scale_mode != 0 && p->scale_mode != 1) || (p->flags & ~7))
+        (p->scale_mode != 0 && p->scale_mode != 1) || (p->flags & ~15))
         return QVG_ERR_INVALID_ARG;
     if (p->scale_mode == 1 && p->bits != 2) return QVG_ERR_INVALID_ARG;
     if (p->C > QVG_MAX_CLUSTERS) return QVG_ERR_UNSUPPORTED;
@@ -47,6 +47,8 @@ qvg_status check_params(const qvg_params *p, int d) {
     if (p->group < e || !is_pow2(p->group / e) || p->group / e > 32) return QVG_ERR_UNSUPPORTED;
     if (p->group % 8 != 0) return QVG_ERR_UNSUPPORTED;  // the read path rebuilds 8-channel chunks
     if ((p->flags & QVG_GIVEN_CENTROIDS) && p->C == 0) return QVG_ERR_INVALID_ARG;
+    // outlier split: at most one value per group lies above its P99 when G <= 100
+    if ((p->flags & QVG_OUTLIER) && p->group > 64) return QVG_ERR_UNSUPPORTED;
     return QVG_OK;
 }
 
@@ -61,6 +63,7 @@ qvg_status check_cache(const qvg_params *p, const qvg_cache *c) {
     if (p->C > 0 && (!c->ids || !c->cent)) return QVG_ERR_INVALID_ARG;
     if ((p->flags & QVG_PSAC) && (!c->psac_p || !c->psac_s || !c->psac_basis))
         return QVG_ERR_INVALID_ARG;
+    if ((p->flags & QVG_OUTLIER) && (!c->outl_val || !c->outl_idx)) return QVG_ERR_INVALID_ARG;
     return QVG_OK;
 }
 
@@ -126,6 +129,9 @@ qvg_status qvg_cache_bytes(const qvg_params *p, int32_t H, int32_t d, int32_t ca
     out[7] = psac ? rows * QVG_PSAC_RANK : 0;
     out[8] = psac ? rows * sizeof(uint16_t) : 0;
     out[9] = psac ? sizeof(float) * static_cast<size_t>(max_chunks) * H * d * QVG_PSAC_RANK : 0;
+    const bool outl = p->flags & QVG_OUTLIER;
+    out[10] = outl ? L * rows * (d / p->group) * sizeof(uint16_t) : 0;
+    out[11] = outl ? L * rows * (d / p->group) : 0;
     return QVG_OK;
 }
 
@@ -170,7 +176,7 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
     const int chunk = cache->n_chunks, slot0 = cache->n_tokens;
     const int C = p->C, Ce = std::min(C, N), L = p->L;
     const float *w = (p->flags & QVG_QSAC) ? qsac_w : nullptr;
-    const bool psac = p->flags & QVG_PSAC;
+    const bool psac = p->flags & QVG_PSAC, outl = p->flags & QVG_OUTLIER;
     const size_t cap = cache->capacity_tokens, nb = static_cast<size_t>(d) * p->bits / 8;
     const size_t ng = d / p->group;
     const size_t cent_hs = static_cast<size_t>(cache->max_chunks) * C * d;
@@ -212,7 +218,8 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
             cache->codes + lrow * nb, cache->scales + lrow * ng, C > 0 ? cache->ids + lrow : nullptr, cap,
             (!last || psac) ? ws.delta : nullptr, !last ? ws.gbf : nullptr,
             (last && psac) ? psac_basis : nullptr, psac ? cache->psac_p + static_cast<size_t>(slot0) * QVG_PSAC_RANK : nullptr,
-            psac ? cache->psac_s + slot0 : nullptr, cap, st);
+            psac ? cache->psac_s + slot0 : nullptr, cap, outl ? cache->outl_val + lrow * ng : nullptr,
+            outl ? cache->outl_idx + lrow * ng : nullptr, st);
         if (s != QVG_OK) return s;
     }
     if ((s = launch_chunk_table(chunk, slot0, N, cache->chunk_start, cache->chunk_len, cache->tile_chunk, st)) != QVG_OK)

@@ -47,6 +47,10 @@ struct AttnWsArgs {
     // n_ctiles = n_slots / QVG_TILE cache tiles; raw row j is slot n_slots + j
     const uint16_t *kraw, *vraw;
     int n_raw, n_ctiles;
+    // outlier split (blog "project X", section 3.4): per stage and group, the
+    // fp16 value split off and its channel in the group (0xFF: none), or NULL
+    const uint16_t *koutv, *voutv;
+    const uint8_t *kouti, *vouti;
 };
 
 namespace ws {
@@ -121,12 +125,15 @@ __device__ __forceinline__ uint4 bf16x8_to_f16(uint4 b) {
 }
 
 // K_hat channels [j0, j0 + 8) of one slot (fp32, stage order, then PSAC).
-// The general path (several stages, PSAC): kept out of line so the one-stage
-// fast path's loop stays small in the instruction cache.
+// The general path (several stages, PSAC, outlier split): kept out of line
+// so the one-stage fast path's loop stays small in the instruction cache.
+// With the outlier split, the stage value at the channel split off from the
+// group (code 0) is fl(o + c), o the stored fp16 value.
 template <int D, int BITS>
 __device__ __noinline__ void rebuild8(const AttnWsArgs &a, const uint8_t *codes, const uint16_t *scales,
-                                         const uint8_t *ids, const uint16_t *cent, int h, int chunk, int slot,
-                                         int j0, const float *pk, float (&acc)[8]) {
+                                         const uint8_t *ids, const uint16_t *cent, const uint16_t *outv,
+                                         const uint8_t *outi, int h, int chunk, int slot, int j0,
+                                         const float *pk, float (&acc)[8]) {
     constexpr int NB = D * BITS / 8;
     const int ng = D / a.group;
 #pragma unroll
@@ -134,6 +141,15 @@ __device__ __noinline__ void rebuild8(const AttnWsArgs &a, const uint8_t *codes,
     for (int l = 0; l < a.L; ++l) {
         const size_t srow = (static_cast<size_t>(l) * a.H + h) * a.cap + slot;
         const float Sp = f16_to_f32(scales[srow * ng + j0 / a.group]);  // 8 | G: one group
+        int eo = -1;  // element of this 8-channel block split off as an outlier, if any
+        float ov = 0.0f;
+        if (outi) {
+            const int gi = j0 / a.group, oi = outi[srow * ng + gi];
+            if (oi != 0xFF && gi * a.group + oi - j0 >= 0 && gi * a.group + oi - j0 < 8) {
+                eo = gi * a.group + oi - j0;
+                ov = f16_to_f32(outv[srow * ng + gi]);
+            }
+        }
         uint32_t bits;
         if constexpr (BITS == 2)
             bits = *reinterpret_cast<const uint16_t *>(codes + srow * NB + j0 / 4);
@@ -154,7 +170,7 @@ __device__ __noinline__ void rebuild8(const AttnWsArgs &a, const uint8_t *codes,
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int q = static_cast<int>((bits >> (e * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
-            float v = __fmul_rn(Sp, static_cast<float>(q));
+            float v = e == eo ? ov : __fmul_rn(Sp, static_cast<float>(q));
             if (a.C > 0) v = __fadd_rn(v, c[e]);
             acc[e] = __fadd_rn(acc[e], v);
         }
@@ -187,16 +203,29 @@ struct HalfData {
     uint4 cw[BITS == 2 ? 1 : 2];  // 64 codes
     uint32_t s2[4];               // fp16 scales of the 8-channel blocks, two per word
     uint4 cr[8];                  // 64 bf16 centroid channels
+    uint32_t oi, ov;              // outlier split, groups of >= 32 channels: per group of the
+                                  // half, the channel split off (byte; 0xFF none) and its fp16
 };
 
-template <int D, int BITS>
+template <int D, int BITS, bool OUTL>
 __device__ __forceinline__ void load_half(const AttnWsArgs &a, const uint8_t *codes, const uint16_t *scales,
-                                          const uint16_t *cent, int h, int chunk, int slot, int id, int kb,
-                                          HalfData<BITS> &hd) {
+                                          const uint16_t *cent, const uint16_t *outv, const uint8_t *outi, int h,
+                                          int chunk, int slot, int id, int kb, HalfData<BITS> &hd) {
     constexpr int NB = D * BITS / 8;
     constexpr int HB = 64 * BITS / 8;
     const int ng = D / a.group;
     const size_t srow = static_cast<size_t>(h) * a.cap + slot;
+    hd.oi = 0xFFFFu;
+    hd.ov = 0u;
+    if (OUTL) {  // one group per half (G = 64) or two (G = 32)
+        const int g0 = (kb * 64) / a.group;
+        hd.oi = (hd.oi & 0xFF00u) | outi[srow * ng + g0];
+        hd.ov = outv[srow * ng + g0];
+        if (a.group == 32) {
+            hd.oi = (hd.oi & 0x00FFu) | (static_cast<uint32_t>(outi[srow * ng + g0 + 1]) << 8);
+            hd.ov |= static_cast<uint32_t>(outv[srow * ng + g0 + 1]) << 16;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < HB / 16; ++i) hd.cw[i] = *reinterpret_cast<const uint4 *>(codes + srow * NB + kb * HB + 16 * i);
     if (a.group >= 64) {
@@ -228,6 +257,8 @@ __device__ __forceinline__ void load_half_raw(const uint16_t *raw, int H, int h,
     for (int i = 0; i < (BITS == 2 ? 1 : 2); ++i) hd.cw[i] = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) hd.s2[i] = 0u;
+    hd.oi = 0xFFFFu;
+    hd.ov = 0u;
     const uint16_t *row = raw + (static_cast<size_t>(j) * H + h) * D + kb * 64;
 #pragma unroll
     for (int i = 0; i < 8; ++i) hd.cr[i] = *reinterpret_cast<const uint4 *>(row + 8 * i);
@@ -296,6 +327,29 @@ __device__ __forceinline__ void decode_store_half(const HalfData<BITS> &hd, uint
     }
 }
 
+// Outlier split, one stage: the channel a group split off holds code 0, so
+// the decode above wrote fp16(c) there; it becomes fp16(fl(o + c)), the
+// rebuild of an outlier, o its stored fp16 value.  c is read back from that
+// slot: bf16 -> fp16 is exact for |c| >= 2^-14 (and for 0), and only a
+// centroid channel in fp16's subnormal range is re-read from the row.
+template <int D, int BITS>
+__device__ __forceinline__ void patch_outliers(const AttnWsArgs &a, const uint16_t *cent, const HalfData<BITS> &hd,
+                                               int h, int chunk, int id, int kb, uint8_t *dst, int r) {
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        const uint32_t oi = (hd.oi >> (8 * g)) & 0xFFu;
+        if (oi != 0xFFu && (g == 0 || a.group == 32)) {
+            const int j = g * a.group + static_cast<int>(oi);  // channel within the half
+            __half *p = reinterpret_cast<__half *>(dst + (((j >> 3) ^ (r & 7)) << 4) + (j & 7) * 2);
+            float c = __half2float(*p);
+            if (a.C > 0 && c != 0.0f && fabsf(c) < 6.103515625e-05f)
+                c = __uint_as_float(static_cast<uint32_t>(
+                        cent[((static_cast<size_t>(h) * a.max_chunks + chunk) * a.C + id) * D + kb * 64 + j]) << 16);
+            *p = __float2half_rn(__fadd_rn(f16_to_f32(static_cast<uint16_t>(hd.ov >> (16 * g))), c));
+        }
+    }
+}
+
 // Adds the two fp16 halves of a packed pair to two fp32 sums (sm_100-family
 // mixed-precision add: the fp16 value is widened exactly).
 __device__ __forceinline__ void add_f16x2_to(uint32_t p, float &s0, float &s1) {
@@ -344,17 +398,19 @@ struct Producer {
     const uint8_t *ids;
     const uint16_t *cent;
     const uint16_t *raw;  // the current chunk's rows (raw tiles)
+    const uint16_t *outv;  // outlier split side list, or NULL
+    const uint8_t *outi;
     uint8_t *buf0;
     uint64_t *full, *freeb;
     int nbuf;
     bool psac;
 };
 
-template <int D, int BITS>
+template <int D, int BITS, bool OUTL>
 __device__ __forceinline__ void load_tile_half(const AttnWsArgs &a, const Producer &pr, int h, const TileInfo &ti,
                                                int r, int id, int kb, HalfData<BITS> &hd) {
     if (ti.chunk >= 0)
-        load_half<D, BITS>(a, pr.codes, pr.scales, pr.cent, h, ti.chunk, ti.s0 + r, id, kb, hd);
+        load_half<D, BITS, OUTL>(a, pr.codes, pr.scales, pr.cent, pr.outv, pr.outi, h, ti.chunk, ti.s0 + r, id, kb, hd);
     else
         load_half_raw<D, BITS>(pr.raw, a.H, h, ti.s0 - a.n_slots + r, kb, hd);
 }
@@ -364,7 +420,7 @@ __device__ __forceinline__ void load_tile_half(const AttnWsArgs &a, const Produc
 // first half of a tile and B for the second when D = 128); table entries and
 // cluster ids run two tiles ahead (ids are read for cache tiles only, whose
 // slots t * QVG_TILE + r < n_slots <= capacity: in bounds).
-template <int D, int BITS>
+template <int D, int BITS, bool OUTL>
 __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
                                              int n_tiles, volatile int *vfail) {
     constexpr int KB = D / 64, TB = KB * 16384;
@@ -380,7 +436,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         if (a.C > 0 && ti1.chunk >= 0) id1 = pr.ids[id_row + QVG_TILE];
     }
     HalfData<BITS> A, B;
-    if (n_tiles > 0 && r < ti0.nvalid) load_tile_half<D, BITS>(a, pr, h, ti0, r, id0, 0, A);
+    if (n_tiles > 0 && r < ti0.nvalid) load_tile_half<D, BITS, OUTL>(a, pr, h, ti0, r, id0, 0, A);
     for (int t = 0; t < n_tiles; ++t) {
         const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
         uint8_t *T = pr.buf0 + b * TB + r * 128;
@@ -392,25 +448,31 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         }
         const bool valid = r < ti0.nvalid, valid1 = t + 1 < n_tiles && r < ti1.nvalid;
         if constexpr (KB == 2) {
-            if (valid) load_tile_half<D, BITS>(a, pr, h, ti0, r, id0, 1, B);
+            if (valid) load_tile_half<D, BITS, OUTL>(a, pr, h, ti0, r, id0, 1, B);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
-            if (valid)
+            if (valid) {
                 decode_store_half<BITS>(A, T, r);
-            else
+                if (OUTL) patch_outliers<D, BITS>(a, pr.cent, A, h, ti0.chunk, id0, 0, T, r);
+            } else {
                 zero_line(T);
-            if (valid1) load_tile_half<D, BITS>(a, pr, h, ti1, r, id1, 0, A);
-            if (valid)
+            }
+            if (valid1) load_tile_half<D, BITS, OUTL>(a, pr, h, ti1, r, id1, 0, A);
+            if (valid) {
                 decode_store_half<BITS>(B, T + 16384, r);
-            else
+                if (OUTL) patch_outliers<D, BITS>(a, pr.cent, B, h, ti0.chunk, id0, 1, T + 16384, r);
+            } else {
                 zero_line(T + 16384);
+            }
         } else {
             B = A;
-            if (valid1) load_tile_half<D, BITS>(a, pr, h, ti1, r, id1, 0, A);
+            if (valid1) load_tile_half<D, BITS, OUTL>(a, pr, h, ti1, r, id1, 0, A);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
-            if (valid)
+            if (valid) {
                 decode_store_half<BITS>(B, T, r);
-            else
+                if (OUTL) patch_outliers<D, BITS>(a, pr.cent, B, h, ti0.chunk, id0, 0, T, r);
+            } else {
                 zero_line(T);
+            }
         }
         umma::fence_proxy_async_smem();
         umma::mbar_arrive(&pr.full[b]);
@@ -419,6 +481,14 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         ti1 = ti2;
         id1 = id2;
     }
+}
+
+// The outlier-split variant, out of line so that its register allocation
+// stays apart from the plain path's (inlined, both spill).
+template <int D, int BITS>
+__device__ __noinline__ void produce_fast_outl(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
+                                               int n_tiles, volatile int *vfail) {
+    produce_fast<D, BITS, true>(a, pr, h, r, tb, n_tiles, vfail);
 }
 
 // Several stages and/or PSAC: 8 channels at a time through rebuild8.
@@ -454,8 +524,8 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
                         pr.raw + (static_cast<size_t>(ti.s0 - a.n_slots + r) * a.H + h) * D + kb * 64 + c8 * 8));
                 } else if (valid) {
                     float kv[8];
-                    rebuild8<D, BITS>(a, pr.codes, pr.scales, pr.ids, pr.cent, h, ti.chunk, ti.s0 + r, kb * 64 + c8 * 8,
-                                      pr.psac ? pk : nullptr, kv);
+                    rebuild8<D, BITS>(a, pr.codes, pr.scales, pr.ids, pr.cent, pr.outv, pr.outi, h, ti.chunk,
+                                      ti.s0 + r, kb * 64 + c8 * 8, pr.psac ? pk : nullptr, kv);
                     o = make_uint4(h2(kv[0], kv[1]), h2(kv[2], kv[3]), h2(kv[4], kv[5]), h2(kv[6], kv[7]));
                 }
                 *reinterpret_cast<uint4 *>(T + kb * 16384 + ((c8 ^ (r & 7)) << 4)) = o;
@@ -761,11 +831,14 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         // ------------------------------------------------ K / V producers (thread = slot)
         const bool isv = warp >= 12;
         const Producer pr{isv ? a.vcodes : a.kcodes, isv ? a.vscales : a.kscales, isv ? a.vids : a.kids,
-                          isv ? a.vcent : a.kcent, isv ? a.vraw : a.kraw, isv ? Vt0 : Kt, isv ? vfull : &kfull,
+                          isv ? a.vcent : a.kcent, isv ? a.vraw : a.kraw, isv ? a.voutv : a.koutv,
+                          isv ? a.vouti : a.kouti, isv ? Vt0 : Kt, isv ? vfull : &kfull,
                           isv ? vfree : &kfree,
                           isv ? 2 : 1, !isv && a.psac_p != nullptr};
-        if (a.L == 1 && !pr.psac)
-            produce_fast<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+        if (a.L == 1 && !pr.psac && !pr.outi)
+            produce_fast<D, BITS, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+        else if (a.L == 1 && !pr.psac && a.group >= 32)
+            produce_fast_outl<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         else
             produce_general<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
     }
@@ -839,8 +912,8 @@ static qvg_status attn_ws_t(const AttnWsArgs &a, int a_splits, cudaStream_t st) 
     constexpr size_t smem = 5 * (D / 64) * 16384 + 2 * 32768 + 1024;
     static bool attr = false;
     if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(k_attention_ws<D, BITS, TOP1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+        const cudaError_t e = cudaFuncSetAttribute(k_attention_ws<D, BITS, TOP1>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             note_cuda_error(e);
@@ -927,6 +1000,12 @@ qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, i
     a.psac_p = psac ? k->psac_p : nullptr;
     a.psac_s = k->psac_s;
     a.psac_basis = k->psac_basis;
+    if (p->flags & QVG_OUTLIER) {
+        a.koutv = k->outl_val;
+        a.kouti = k->outl_idx;
+        a.voutv = v->outl_val;
+        a.vouti = v->outl_idx;
+    }
     a.scale_log2 = scale_log2;
     a.out32 = out_dtype == QVG_OUT_F32 ? static_cast<float *>(out) : nullptr;
     a.out16 = out_dtype == QVG_OUT_BF16 ? static_cast<uint16_t *>(out) : nullptr;

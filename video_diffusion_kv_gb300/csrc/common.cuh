@@ -134,7 +134,8 @@ qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, in
                                  uint8_t *codes, uint16_t *scales, uint8_t *ids_out,
                                  size_t slot_head_stride, float *delta_out,
                                  uint16_t *gbf_out, const float *psac_U, int8_t *psac_p,
-                                 uint16_t *psac_s, size_t psac_head_stride, cudaStream_t st);
+                                 uint16_t *psac_s, size_t psac_head_stride, uint16_t *outl_val,
+                                 uint8_t *outl_idx, cudaStream_t st);
 qvg_status launch_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start,
                               int32_t *chunk_len, int32_t *tile_chunk, cudaStream_t st);
 qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, int ntok,

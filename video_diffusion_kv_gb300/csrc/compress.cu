@@ -695,6 +695,13 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
 // rounding, the next clustering operand); optionally (last stage of a key
 // chunk with PSAC) the INT8 projection of X_{L+1} on the basis U, an fp32
 // FMA chain in ascending channel order.
+// OUTL (outlier split): pass 1 also keeps, per group, the second-largest
+// |r| and the signed value and channel of the largest.  The largest is an
+// outlier exactly when it is strictly above the second: for G <= 100 the
+// group's linear-interpolation 99th percentile lies strictly between the
+// two.  The scale then comes from the second-largest (the largest of the
+// values that remain; equal to the largest when nothing is split off), the
+// outlier's code is 0 and its stage value is fp16(r) + c.
 template <typename TIn>
 __device__ __forceinline__ void load32(const TIn *p, float (&v)[32]);
 template <>
@@ -722,13 +729,14 @@ __device__ __forceinline__ void load32<float>(const float *p, float (&v)[32]) {
     }
 }
 
-template <int D, int BITS, typename TIn>
+template <int D, int BITS, typename TIn, bool OUTL>
 __global__ void __launch_bounds__(256) k_residual_quant(
     const TIn *__restrict__ xin, int N, int H, const uint16_t *__restrict__ cent, size_t hs, int C,
     const int32_t *__restrict__ ids, int group, int mode, uint8_t *__restrict__ codes,
     uint16_t *__restrict__ scales, uint8_t *__restrict__ ids_out, size_t shs,
     float *__restrict__ delta_out, uint16_t *__restrict__ gbf_out, const float *__restrict__ psacU,
-    int8_t *__restrict__ psac_p, uint16_t *__restrict__ psac_s, size_t phs) {
+    int8_t *__restrict__ psac_p, uint16_t *__restrict__ psac_s, size_t phs, uint16_t *__restrict__ outl_val,
+    uint8_t *__restrict__ outl_idx) {
     constexpr int NB = D * BITS / 8, CB = 32 * BITS / 8;  // code bytes per row / per 32-channel block
     constexpr int NG8 = D / 8;                             // 8-channel blocks
     pdl_wait();  // the final assignment (which reads this stage's operand) has finished
@@ -744,8 +752,11 @@ __global__ void __launch_bounds__(256) k_residual_quant(
     const size_t trow = static_cast<size_t>(n) * H + h;  // token-major row of the stage buffers
     const TIn *xr = xin + trow * D;
     const uint16_t *cr = C > 0 ? cent + static_cast<size_t>(h) * hs + static_cast<size_t>(id) * D : nullptr;
-    // pass 1: amax of each 8-channel block, then of each group
-    float am8[NG8];
+    // pass 1: amax of each 8-channel block, then of each group (with the
+    // outlier split: also the second-largest |r| and the largest's signed
+    // value and channel, the first one on ties)
+    float am8[NG8], sm8[NG8], rv8[NG8];
+    int ix8[NG8];
 #pragma unroll 1
     for (int cb = 0; cb < D / 32; ++cb) {
         float x[32], c[32];
@@ -753,33 +764,89 @@ __global__ void __launch_bounds__(256) k_residual_quant(
         if (C > 0) load32<uint16_t>(cr + cb * 32, c);
 #pragma unroll
         for (int b8 = 0; b8 < 4; ++b8) {
-            float m = 0.0f;
+            float m = 0.0f, m2 = 0.0f, rv = 0.0f;
+            int ix = 0;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float r = C > 0 ? __fsub_rn(x[8 * b8 + e], c[8 * b8 + e]) : x[8 * b8 + e];
-                m = fmaxf(m, fabsf(r));
+                const float a = fabsf(r);
+                if constexpr (OUTL) {
+                    if (a > m) {
+                        m2 = m;
+                        m = a;
+                        rv = r;
+                        ix = e;
+                    } else {
+                        m2 = fmaxf(m2, a);
+                    }
+                } else {
+                    m = fmaxf(m, a);
+                }
             }
-            // cb is a loop variable: keep am8 in registers through a static index
+            // cb is a loop variable: keep the block values in registers through a static index
 #pragma unroll
             for (int q = 0; q < NG8 / 4; ++q)
-                if (q == cb) am8[4 * q + b8] = m;
+                if (q == cb) {
+                    am8[4 * q + b8] = m;
+                    if constexpr (OUTL) {
+                        sm8[4 * q + b8] = m2;
+                        rv8[4 * q + b8] = rv;
+                        ix8[4 * q + b8] = (4 * q + b8) * 8 + ix;
+                    }
+                }
         }
     }
     float Sp8[NG8];  // the scale each 8-channel block uses
+    int oc8[NG8];    // (outlier split) the channel split off in the block's group, or -1
+    float ov8[NG8];  // and its fp16 value
     const size_t srow = static_cast<size_t>(h) * shs + n;
 #pragma unroll
-    for (int g = 0; g < NG8; ++g) Sp8[g] = 0.0f;
+    for (int g = 0; g < NG8; ++g) {
+        Sp8[g] = 0.0f;
+        oc8[g] = -1;
+        ov8[g] = 0.0f;
+    }
     for (int gi = 0; gi < ng; ++gi) {
-        float m = 0.0f;
+        float m = 0.0f, m2 = 0.0f, rv = 0.0f;
+        int ix = 0;
 #pragma unroll
         for (int g = 0; g < NG8; ++g)
-            if (g / g8 == gi) m = fmaxf(m, am8[g]);
-        const uint16_t sb = group_scale_f16(m, BITS, mode);
+            if (g / g8 == gi) {
+                if constexpr (OUTL) {
+                    if (am8[g] > m) {
+                        m2 = fmaxf(m, sm8[g]);
+                        m = am8[g];
+                        rv = rv8[g];
+                        ix = ix8[g];
+                    } else {
+                        m2 = fmaxf(m2, am8[g]);
+                    }
+                } else {
+                    m = fmaxf(m, am8[g]);
+                }
+            }
+        const uint16_t sb = group_scale_f16(OUTL ? m2 : m, BITS, mode);
         scales[srow * ng + gi] = sb;
         const float Sp = f16_to_f32(sb);
+        int oc = -1;
+        float ov = 0.0f;
+        if constexpr (OUTL) {
+            uint16_t ob = 0;
+            if (m > m2) {
+                oc = ix;
+                ob = f32_to_f16(fminf(fmaxf(rv, -65504.0f), 65504.0f));
+                ov = f16_to_f32(ob);
+            }
+            outl_val[srow * ng + gi] = ob;
+            outl_idx[srow * ng + gi] = static_cast<uint8_t>(oc < 0 ? 0xFF : oc - gi * group);
+        }
 #pragma unroll
         for (int g = 0; g < NG8; ++g)
-            if (g / g8 == gi) Sp8[g] = Sp;
+            if (g / g8 == gi) {
+                Sp8[g] = Sp;
+                oc8[g] = oc;
+                ov8[g] = ov;
+            }
     }
     if (ids_out) ids_out[srow] = static_cast<uint8_t>(id);  // no ids without centroids (C = 0)
     float P[QVG_PSAC_RANK];
@@ -792,13 +859,22 @@ __global__ void __launch_bounds__(256) k_residual_quant(
         float x[32], c[32];
         load32<TIn>(xr + cb * 32, x);
         if (C > 0) load32<uint16_t>(cr + cb * 32, c);
-        float Sb[4];
+        float Sb[4], ob[4];
+        int ocb[4];
 #pragma unroll
         for (int b8 = 0; b8 < 4; ++b8) {
             Sb[b8] = 0.0f;
+            ob[b8] = 0.0f;
+            ocb[b8] = -1;
 #pragma unroll
             for (int q = 0; q < NG8 / 4; ++q)
-                if (q == cb) Sb[b8] = Sp8[4 * q + b8];
+                if (q == cb) {
+                    Sb[b8] = Sp8[4 * q + b8];
+                    if constexpr (OUTL) {
+                        ob[b8] = ov8[4 * q + b8];
+                        ocb[b8] = oc8[4 * q + b8];
+                    }
+                }
         }
         uint32_t pw[CB / 4];
 #pragma unroll
@@ -808,9 +884,10 @@ __global__ void __launch_bounds__(256) k_residual_quant(
         for (int e = 0; e < 32; ++e) {
             const float Sp = Sb[e >> 3];
             const float r = C > 0 ? __fsub_rn(x[e], c[e]) : x[e];
-            const int q = quant_code(r, Sp, BITS);
+            const bool is_out = OUTL && cb * 32 + e == ocb[e >> 3];
+            const int q = is_out ? 0 : quant_code(r, Sp, BITS);
             pw[(e * BITS) / 32] |= static_cast<uint32_t>(q + (1 << (BITS - 1))) << ((e * BITS) % 32);
-            const float rh = __fmul_rn(Sp, static_cast<float>(q));
+            const float rh = is_out ? ob[e >> 3] : __fmul_rn(Sp, static_cast<float>(q));
             const float deq = C > 0 ? __fadd_rn(rh, c[e]) : rh;
             dl[e] = __fsub_rn(x[e], deq);
         }
@@ -1051,23 +1128,34 @@ qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int
     return QVG_OK;
 }
 
+template <int D, int BITS, bool OUTL>
+static cudaError_t rq_launch(const void *xin, bool f32, int N, int H, const uint16_t *cent, size_t hs,
+                             int C, const int32_t *ids, int group, int mode, uint8_t *codes,
+                             uint16_t *scales, uint8_t *ids_out, size_t shs, float *delta_out,
+                             uint16_t *gbf_out, const float *U, int8_t *pp, uint16_t *ps, size_t phs,
+                             uint16_t *ov, uint8_t *oi, cudaStream_t st) {
+    const long long warps = static_cast<long long>(H) * ceil_div(std::max(N, 1), 32);
+    const int blocks = static_cast<int>((warps + 7) / 8);
+    if (f32)
+        return launch_pdl(k_residual_quant<D, BITS, float, OUTL>, dim3(blocks), dim3(256), 0, st,
+                          static_cast<const float *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
+                          ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, ov, oi);
+    return launch_pdl(k_residual_quant<D, BITS, uint16_t, OUTL>, dim3(blocks), dim3(256), 0, st,
+                      static_cast<const uint16_t *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
+                      ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, ov, oi);
+}
+
 template <int D, int BITS>
 static void rq_dispatch(const void *xin, bool f32, int N, int H, const uint16_t *cent, size_t hs,
                         int C, const int32_t *ids, int group, int mode, uint8_t *codes,
                         uint16_t *scales, uint8_t *ids_out, size_t shs, float *delta_out,
                         uint16_t *gbf_out, const float *U, int8_t *pp, uint16_t *ps, size_t phs,
-                        cudaStream_t st) {
-    const long long warps = static_cast<long long>(H) * ceil_div(std::max(N, 1), 32);
-    const int blocks = static_cast<int>((warps + 7) / 8);
-    cudaError_t e;
-    if (f32)
-        e = launch_pdl(k_residual_quant<D, BITS, float>, dim3(blocks), dim3(256), 0, st,
-                       static_cast<const float *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
-                       ids_out, shs, delta_out, gbf_out, U, pp, ps, phs);
-    else
-        e = launch_pdl(k_residual_quant<D, BITS, uint16_t>, dim3(blocks), dim3(256), 0, st,
-                       static_cast<const uint16_t *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
-                       ids_out, shs, delta_out, gbf_out, U, pp, ps, phs);
+                        uint16_t *ov, uint8_t *oi, cudaStream_t st) {
+    const cudaError_t e =
+        ov ? rq_launch<D, BITS, true>(xin, f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs,
+                                      delta_out, gbf_out, U, pp, ps, phs, ov, oi, st)
+           : rq_launch<D, BITS, false>(xin, f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs,
+                                       delta_out, gbf_out, U, pp, ps, phs, ov, oi, st);
     if (e != cudaSuccess) note_cuda_error(e);
 }
 
@@ -1076,15 +1164,15 @@ qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, in
                                  int bits, int group, int mode, uint8_t *codes, uint16_t *scales,
                                  uint8_t *ids_out, size_t shs, float *delta_out,
                                  uint16_t *gbf_out, const float *U, int8_t *pp, uint16_t *ps,
-                                 size_t phs, cudaStream_t st) {
+                                 size_t phs, uint16_t *ov, uint8_t *oi, cudaStream_t st) {
     if (d == 64 && bits == 2)
-        rq_dispatch<64, 2>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, st);
+        rq_dispatch<64, 2>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, ov, oi, st);
     else if (d == 64)
-        rq_dispatch<64, 4>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, st);
+        rq_dispatch<64, 4>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, ov, oi, st);
     else if (bits == 2)
-        rq_dispatch<128, 2>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, st);
+        rq_dispatch<128, 2>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, ov, oi, st);
     else
-        rq_dispatch<128, 4>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, st);
+        rq_dispatch<128, 4>(xin, xin_f32, N, H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, ov, oi, st);
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }

@@ -3,7 +3,9 @@
 // Quant VideoGen notes, "overall framework": X_hat = S_X * X_INT + C_i;
 // "Progressive Residual Quantization": X_hat = X_hat_1 + Delta_hat_1 + ...
 // (stages summed in fp32 in stage order).  QuantWM write-up, PSAC: the
-// stored projection of the key error is added back as P_hat U^T.
+// stored projection of the key error is added back as P_hat U^T.  Blog
+// "project X", section 3.4 (outlier separation): a value split off from its
+// group is rebuilt from its fp16 copy.
 #include "common.cuh"
 
 namespace qvg {
@@ -17,6 +19,8 @@ struct CacheView {
     const int8_t *psac_p;
     const uint16_t *psac_s;
     const float *psac_basis;
+    const uint16_t *outl_val;
+    const uint8_t *outl_idx;
     int H, cap, max_chunks;
 };
 
@@ -26,7 +30,9 @@ struct CacheView {
 // loaded before its arithmetic).  Per element, in stage order:
 // acc += fl(fl(S q) + c), then the PSAC term as an fp32 FMA chain over the
 // rank -- the same operations, in the same order, as any other rebuild.
-template <int D, int BITS, bool PSAC>
+// OUTL: at the channel a stage split off from its group (code 0), the
+// stage's value is fl(o + c), o the stored fp16 outlier.
+template <int D, int BITS, bool PSAC, bool OUTL>
 __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, int group,
                                                    int tok0, int ntok, float *out32,
                                                    uint16_t *out16) {
@@ -71,9 +77,22 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
                     cw[2] = u.z;
                     cw[3] = u.w;
                 }
-                float S[4];
+                float S[4], ov[4];
+                int oc[4];  // channel split off in each 8-channel block's group, or -1
 #pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) S[g8] = f16_to_f32(cv.scales[srow * ng + (cb * 32 + g8 * 8) / group]);
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    const int gi = (cb * 32 + g8 * 8) / group;
+                    S[g8] = f16_to_f32(cv.scales[srow * ng + gi]);
+                    oc[g8] = -1;
+                    ov[g8] = 0.0f;
+                    if constexpr (OUTL) {
+                        const int oi = cv.outl_idx[srow * ng + gi];
+                        if (oi != 0xFF) {
+                            oc[g8] = gi * group + oi;
+                            ov[g8] = f16_to_f32(cv.outl_val[srow * ng + gi]);
+                        }
+                    }
+                }
                 uint4 cr[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                                make_uint4(0, 0, 0, 0)};
                 if (C > 0) {
@@ -87,6 +106,7 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
                     const uint32_t word = cw[(e * BITS) / 32];
                     const int q = static_cast<int>((word >> ((e * BITS) % 32)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
                     float v = __fmul_rn(S[e >> 3], static_cast<float>(q));
+                    if (OUTL && cb * 32 + e == oc[e >> 3]) v = ov[e >> 3];
                     if (C > 0) {
                         const uint4 c4 = cr[e >> 3];
                         const uint32_t cwd = (e & 7) < 2 ? c4.x : (e & 7) < 4 ? c4.y : (e & 7) < 6 ? c4.z : c4.w;
@@ -128,22 +148,25 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
 qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, int ntok,
                              void *out, int out_dtype, cudaStream_t st) {
     CacheView cv{c->codes, c->scales, c->ids, c->cent, c->chunk_start, c->chunk_len,
-                 c->tile_chunk, c->psac_p, c->psac_s, c->psac_basis, c->H,
+                 c->tile_chunk, c->psac_p, c->psac_s, c->psac_basis, c->outl_val, c->outl_idx, c->H,
                  c->capacity_tokens, c->max_chunks};
     if (!(p->flags & QVG_PSAC)) cv.psac_p = nullptr;
+    if (!(p->flags & QVG_OUTLIER)) cv.outl_idx = nullptr;
     float *o32 = out_dtype == QVG_OUT_F32 ? static_cast<float *>(out) : nullptr;
     uint16_t *o16 = out_dtype == QVG_OUT_BF16 ? static_cast<uint16_t *>(out) : nullptr;
     const long long warps = static_cast<long long>(c->H) * ceil_div(std::max(ntok, 1), 32);
     const int blocks = static_cast<int>(std::max(1LL, (warps + 7) / 8));
-#define QVG_DQ(D_, B_)                                                                                        \
-    (cv.psac_p ? k_decompress<D_, B_, true><<<blocks, 256, 0, st>>>(cv, p->L, p->C, p->group, tok0, ntok, o32, o16) \
-               : k_decompress<D_, B_, false><<<blocks, 256, 0, st>>>(cv, p->L, p->C, p->group, tok0, ntok, o32, o16))
+#define QVG_DQ2(D_, B_, O_)                                                                                        \
+    (cv.psac_p ? k_decompress<D_, B_, true, O_><<<blocks, 256, 0, st>>>(cv, p->L, p->C, p->group, tok0, ntok, o32, o16) \
+               : k_decompress<D_, B_, false, O_><<<blocks, 256, 0, st>>>(cv, p->L, p->C, p->group, tok0, ntok, o32, o16))
+#define QVG_DQ(D_, B_) (cv.outl_idx ? QVG_DQ2(D_, B_, true) : QVG_DQ2(D_, B_, false))
     if (c->d == 64) {
         if (p->bits == 2) QVG_DQ(64, 2); else QVG_DQ(64, 4);
     } else {
         if (p->bits == 2) QVG_DQ(128, 2); else QVG_DQ(128, 4);
     }
 #undef QVG_DQ
+#undef QVG_DQ2
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }
