@@ -679,6 +679,81 @@ def study_outlier(args):
     return 0
 
 
+def study_paths(args):
+    """Attention read paths on the LongCat-like layer (16 heads, d=128, 8
+    chunks of 4680 tokens, C=256, 8 iters): 4680 queries over the whole
+    compressed cache for one-stage INT2 G=64 (plain, and with the outlier
+    split), the split with G=16, two stages (QVG-Pro) and PSAC on the keys
+    (rank-8 orthonormal basis, seeded).  Median of 5 launches, L2 flushed
+    before each; plus the time to compress the newest chunk (K and V)."""
+    import statistics
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import video_diffusion_kv_gb300 as qvg
+    from video_diffusion_kv_gb300 import synth
+    w = synth.WORKLOADS["longcat"]
+    seed = 13
+    per = -(-w.N // 128) * 128
+    kd = [synth_dev(synth.chunk_kv(w, seed, k, synth.KIND_K), "cuda") for k in range(w.n_chunks)]
+    vd = [synth_dev(synth.chunk_kv(w, seed, k, synth.KIND_V), "cuda") for k in range(w.n_chunks)]
+    q = synth_dev(synth.queries(w, seed, w.n_chunks - 1), "cuda")
+    rng = np.random.default_rng(seed)
+    U = np.stack([np.linalg.qr(rng.standard_normal((w.d, qvg.QVG_PSAC_RANK)))[0] for _ in range(w.H)])
+    U = torch.from_numpy(U.astype(np.float32)).cuda()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    arms = {}
+    for name, kw in (("L1_G64", {}), ("outlier_G64", dict(flags=qvg.QVG_OUTLIER)),
+                     ("outlier_G16", dict(flags=qvg.QVG_OUTLIER, group=16)), ("L2_G64", dict(L=2)),
+                     ("psac_G64", dict(flags=qvg.QVG_PSAC))):
+        p = qvg.Params(**{**dict(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=seed), **kw})
+        pv = qvg.Params(**{**p.__dict__, "flags": p.flags & ~qvg.QVG_PSAC})
+        kc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks)
+        vc = qvg.CompressedKV(pv, w.H, w.d, w.n_chunks * per, w.n_chunks)
+        ws = torch.empty(max(qvg.workspace_size(p, qvg.QVG_OP_COMPRESS, w.N, w.H, w.d), 1), dtype=torch.uint8,
+                         device="cuda")
+        psac = U if p.flags & qvg.QVG_PSAC else None
+
+        def compress(k):
+            qvg.compress_chunk(p, kd[k], kc, psac_basis=psac, workspace=ws)
+            qvg.compress_chunk(pv, vd[k], vc, workspace=ws)
+
+        for k in range(w.n_chunks):
+            compress(k)
+        last = w.n_chunks - 1
+
+        def timed(fn, before=None):
+            ts = []
+            for rep in range(7):
+                if before:
+                    before()
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                if rep >= 2:
+                    ts.append(e0.elapsed_time(e1))
+            return statistics.median(ts)
+
+        def rewind():
+            kc.reset(last, last * per)
+            vc.reset(last, last * per)
+
+        ms_c = timed(lambda: compress(last), rewind)
+        ms_a = timed(lambda: qvg.attention(p, q, kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out))
+        arms[name] = {"attention_ms": ms_a, "attention_TFLOP/s": 4.0 * w.Nq * w.tokens * w.d * w.Hq / ms_a / 1e9,
+                      "compress_ms_KV": ms_c}
+        del kc, vc
+    print(json.dumps({"study": "paths", "workload": "16 heads, d=128, 8 chunks x 4680 tokens, C=256, INT2, 8 iters; "
+                      "4680 queries", "status": qvg.get_status(), "arms": arms}), flush=True)
+    return 0
+
+
 def synth_dev(a, dev):
     import torch
     return torch.from_numpy(a).to(dev, torch.bfloat16).contiguous()
@@ -693,7 +768,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="time the device step only (profiling)")
     ap.add_argument("--cache-chunks", type=int, default=None, help="smaller cache (profiling cases)")
-    ap.add_argument("--workload", default="longcat", choices=["longcat", "qvgpro", "quantwm", "rollout", "outlier"],
+    ap.add_argument("--workload", default="longcat", choices=["longcat", "qvgpro", "quantwm", "rollout", "outlier", "paths"],
                     help="longcat: the benchmark line; the others print their study line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "own":
@@ -702,7 +777,7 @@ def main():
         return run_reference(args)
     if args.workload != "longcat":
         return {"qvgpro": study_qvgpro, "quantwm": study_quantwm, "rollout": study_rollout,
-                "outlier": study_outlier}[args.workload](args)
+                "outlier": study_outlier, "paths": study_paths}[args.workload](args)
     return run_own(args)
 
 

@@ -124,77 +124,6 @@ __device__ __forceinline__ uint4 bf16x8_to_f16(uint4 b) {
                       h2(__uint_as_float(b.w << 16), __uint_as_float(b.w & 0xffff0000u)));
 }
 
-// K_hat channels [j0, j0 + 8) of one slot (fp32, stage order, then PSAC).
-// The general path (several stages, PSAC, outlier split): kept out of line
-// so the one-stage fast path's loop stays small in the instruction cache.
-// With the outlier split, the stage value at the channel split off from the
-// group (code 0) is fl(o + c), o the stored fp16 value.
-template <int D, int BITS>
-__device__ __noinline__ void rebuild8(const AttnWsArgs &a, const uint8_t *codes, const uint16_t *scales,
-                                         const uint8_t *ids, const uint16_t *cent, const uint16_t *outv,
-                                         const uint8_t *outi, int h, int chunk, int slot, int j0,
-                                         const float *pk, float (&acc)[8]) {
-    constexpr int NB = D * BITS / 8;
-    const int ng = D / a.group;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-    for (int l = 0; l < a.L; ++l) {
-        const size_t srow = (static_cast<size_t>(l) * a.H + h) * a.cap + slot;
-        const float Sp = f16_to_f32(scales[srow * ng + j0 / a.group]);  // 8 | G: one group
-        int eo = -1;  // element of this 8-channel block split off as an outlier, if any
-        float ov = 0.0f;
-        if (outi) {
-            const int gi = j0 / a.group, oi = outi[srow * ng + gi];
-            if (oi != 0xFF && gi * a.group + oi - j0 >= 0 && gi * a.group + oi - j0 < 8) {
-                eo = gi * a.group + oi - j0;
-                ov = f16_to_f32(outv[srow * ng + gi]);
-            }
-        }
-        uint32_t bits;
-        if constexpr (BITS == 2)
-            bits = *reinterpret_cast<const uint16_t *>(codes + srow * NB + j0 / 4);
-        else
-            bits = *reinterpret_cast<const uint32_t *>(codes + srow * NB + j0 / 2);
-        float c[8];
-        if (a.C > 0) {
-            const uint4 cv = *reinterpret_cast<const uint4 *>(
-                cent + ((static_cast<size_t>(l) * a.H + h) * a.max_chunks + chunk) * a.C * D +
-                static_cast<size_t>(ids[srow]) * D + j0);
-            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                c[2 * k] = __uint_as_float(cw[k] << 16);
-                c[2 * k + 1] = __uint_as_float(cw[k] & 0xffff0000u);
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int q = static_cast<int>((bits >> (e * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
-            float v = e == eo ? ov : __fmul_rn(Sp, static_cast<float>(q));
-            if (a.C > 0) v = __fadd_rn(v, c[e]);
-            acc[e] = __fadd_rn(acc[e], v);
-        }
-    }
-    if (pk) {
-        const float *U = a.psac_basis + (static_cast<size_t>(chunk) * a.H + h) * D * QVG_PSAC_RANK;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 u0 = *reinterpret_cast<const float4 *>(U + (j0 + e) * QVG_PSAC_RANK);
-            const float4 u1 = *reinterpret_cast<const float4 *>(U + (j0 + e) * QVG_PSAC_RANK + 4);
-            float corr = 0.0f;
-            corr = fmaf(pk[0], u0.x, corr);
-            corr = fmaf(pk[1], u0.y, corr);
-            corr = fmaf(pk[2], u0.z, corr);
-            corr = fmaf(pk[3], u0.w, corr);
-            corr = fmaf(pk[4], u1.x, corr);
-            corr = fmaf(pk[5], u1.y, corr);
-            corr = fmaf(pk[6], u1.z, corr);
-            corr = fmaf(pk[7], u1.w, corr);
-            acc[e] = acc[e] + corr;
-        }
-    }
-}
-
 // One-stage fast path, split into its loads and its arithmetic so that a
 // producer can put the loads of a 64-channel half in flight before it waits
 // for its buffer.  K_hat (or V_hat) = fma(S, q, c) in fp32, rounded to fp16.
@@ -491,48 +420,255 @@ __device__ __noinline__ void produce_fast_outl(const AttnWsArgs &a, const Produc
     produce_fast<D, BITS, true>(a, pr, h, r, tb, n_tiles, vfail);
 }
 
-// Several stages and/or PSAC: 8 channels at a time through rebuild8.
-template <int D, int BITS>
+// Several stages, PSAC, or the outlier split with groups under 32 channels.
+// Work runs in steps of one 32-channel quarter of the slot's row and one
+// stage, in the order (tile, quarter, stage).  Each step's codes, scales,
+// centroid slice and outlier entries are loaded one step ahead (register
+// sets A and B); the next tile's stage ids, table entry and PSAC codes one
+// tile ahead.  A quarter's stages accumulate in fp32 as
+// acc = fl(acc + fl(S q + c)) -- S q is exact (an fp16 scale times a code
+// of at most 4 bits), so one FMA gives the stage value -- with fl(o + c) at
+// a channel the stage split off; after the last stage the PSAC term
+// sum_k P_hat_k U_jk (fp32 FMA chain, ascending k) is added and the quarter
+// is rounded to fp16 and stored.
+template <int BITS>
+struct QuarterData {
+    uint32_t cw[BITS];  // 32 codes
+    uint32_t s2[2];     // fp16 scales of the four 8-channel blocks, two per word
+    uint4 cr[4];        // 32 bf16 centroid channels (a raw tile: the row itself)
+    uint32_t oe;        // per 8-channel block (byte b): the element split off, 0xFF none
+    uint2 ov;           // and its fp16 value (half b)
+};
+
+// Stage l's cluster id from four words of packed 8-bit ids (L <= 16).
+__device__ __forceinline__ int stage_id(const uint32_t (&w)[4], int l) {
+    uint32_t x = w[0];
+    x = l >= 4 ? w[1] : x;
+    x = l >= 8 ? w[2] : x;
+    x = l >= 12 ? w[3] : x;
+    return static_cast<int>((x >> (8 * (l & 3))) & 0xFFu);
+}
+
+template <int D>
+__device__ __forceinline__ void load_stage_ids(const AttnWsArgs &a, const Producer &pr, int h, const TileInfo &ti,
+                                               int r, uint32_t (&w)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = 0u;
+    if (a.C == 0 || ti.chunk < 0 || r >= ti.nvalid) return;
+    for (int l = 0; l < a.L; ++l) {
+        const uint32_t v = pr.ids[(static_cast<size_t>(l) * a.H + h) * a.cap + ti.s0 + r];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i == (l >> 2)) w[i] |= v << (8 * (l & 3));
+    }
+}
+
+template <int D, int BITS, bool OUTL>
+__device__ __forceinline__ void load_quarter(const AttnWsArgs &a, const Producer &pr, int h, const TileInfo &ti,
+                                             int r, int id, int l, int qt, QuarterData<BITS> &qd) {
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) qd.cw[i] = 0u;
+    qd.s2[0] = qd.s2[1] = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) qd.cr[i] = make_uint4(0, 0, 0, 0);
+    qd.oe = 0xFFFFFFFFu;
+    qd.ov = make_uint2(0, 0);
+    if (r >= ti.nvalid) return;
+    if (ti.chunk < 0) {  // the current chunk's raw row, in stage 0
+        if (l == 0) {
+            const uint16_t *row = pr.raw + (static_cast<size_t>(ti.s0 - a.n_slots + r) * a.H + h) * D + qt * 32;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qd.cr[i] = *reinterpret_cast<const uint4 *>(row + 8 * i);
+        }
+        return;
+    }
+    const int ng = D / a.group;
+    const size_t srow = (static_cast<size_t>(l) * a.H + h) * a.cap + ti.s0 + r;
+    const uint8_t *cp = pr.codes + srow * (D * BITS / 8) + qt * (4 * BITS);
+    if constexpr (BITS == 2) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(cp);
+        qd.cw[0] = u.x;
+        qd.cw[1] = u.y;
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4 *>(cp);
+        qd.cw[0] = u.x;
+        qd.cw[1] = u.y;
+        qd.cw[2] = u.z;
+        qd.cw[3] = u.w;
+    }
+    if (a.group >= 32) {
+        const uint32_t s0 = pr.scales[srow * ng + (qt * 32) / a.group];
+        qd.s2[0] = qd.s2[1] = s0 | (s0 << 16);
+    } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            qd.s2[b >> 1] |= static_cast<uint32_t>(pr.scales[srow * ng + (qt * 32 + 8 * b) / a.group]) << (16 * (b & 1));
+    }
+    if (a.C > 0) {
+        const uint16_t *crow =
+            pr.cent + ((static_cast<size_t>(l) * a.H + h) * a.max_chunks + ti.chunk) * a.C * D + static_cast<size_t>(id) * D +
+            qt * 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qd.cr[i] = *reinterpret_cast<const uint4 *>(crow + 8 * i);
+    }
+    if constexpr (OUTL) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int gi = (qt * 32 + 8 * b) / a.group;
+            const int oi = pr.outi[srow * ng + gi];
+            const int e = gi * a.group + oi - (qt * 32 + 8 * b);
+            if (oi != 0xFF && e >= 0 && e < 8) {
+                qd.oe = (qd.oe & ~(0xFFu << (8 * b))) | (static_cast<uint32_t>(e) << (8 * b));
+                const uint32_t o = pr.outv[srow * ng + gi];
+                if (b < 2)
+                    qd.ov.x |= o << (16 * b);
+                else
+                    qd.ov.y |= o << (16 * (b - 2));
+            }
+        }
+    }
+}
+
+// acc (16 packed fp32 pairs) += this stage's values of the quarter.
+template <int BITS, bool OUTL>
+__device__ __forceinline__ void accumulate_quarter(const QuarterData<BITS> &qd, uint64_t (&acc)[16]) {
+    constexpr uint32_t M = (1u << BITS) - 1u, MAGIC = 0x4B000000u;
+    constexpr float E23 = 8388608.0f, HALF = static_cast<float>(1 << (BITS - 1));
+    const uint64_t P2 = pk2(1.0f, 1.0f / static_cast<float>(1 << BITS));
+    const uint64_t N2 = pk2(-(E23 + HALF), -(E23 / static_cast<float>(1 << BITS) + HALF));
+    const uint64_t ONE2 = pk2(1.0f, 1.0f);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t blk = qd.cw[(8 * b * BITS) / 32] >> ((8 * b * BITS) % 32);
+        const float S = f16_to_f32(static_cast<uint16_t>(qd.s2[b >> 1] >> (16 * (b & 1))));
+        const uint64_t S2 = pk2(S, S);
+        const uint32_t c4[4] = {qd.cr[b].x, qd.cr[b].y, qd.cr[b].z, qd.cr[b].w};
+        const uint32_t eo = (qd.oe >> (8 * b)) & 0xFFu;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t x = blk >> (2 * k * BITS);
+            const uint64_t mag = pk2(__uint_as_float((x & M) | MAGIC), __uint_as_float((x & (M << BITS)) | MAGIC));
+            uint64_t v2 = fma2(S2, fma2(mag, P2, N2),
+                               pk2(__uint_as_float(c4[k] << 16), __uint_as_float(c4[k] & 0xffff0000u)));
+            if (OUTL && (eo >> 1) == static_cast<uint32_t>(k)) {  // code 0 there: v = c, becomes fl(o + c)
+                const float o = f16_to_f32(static_cast<uint16_t>((b < 2 ? qd.ov.x : qd.ov.y) >> (16 * (b & 1))));
+                float v0, v1;
+                up2(v2, v0, v1);
+                if (eo & 1u)
+                    v1 = __fadd_rn(o, v1);
+                else
+                    v0 = __fadd_rn(o, v0);
+                v2 = pk2(v0, v1);
+            }
+            acc[4 * b + k] = fma2(acc[4 * b + k], ONE2, v2);
+        }
+    }
+}
+
+template <int D, int BITS, bool OUTL>
 __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
                                              int n_tiles, volatile int *vfail) {
-    constexpr int KB = D / 64, TB = KB * 16384;
-    for (int t = 0; t < n_tiles; ++t) {
-        const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
-        uint8_t *T = pr.buf0 + b * TB + r * 128;
-        const TileInfo ti = tile_info(a, tb + t);
-        const bool valid = r < ti.nvalid;
-        if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
-        const bool raw = ti.chunk < 0;
-        float pk[QVG_PSAC_RANK];
-        if (pr.psac && valid && !raw) {
-            const size_t prow = static_cast<size_t>(h) * a.cap + ti.s0 + r;
-            const float pS = f16_to_f32(a.psac_s[prow]);
-            const int2 pv = *reinterpret_cast<const int2 *>(a.psac_p + prow * QVG_PSAC_RANK);
+    constexpr int KB = D / 64, TB = KB * 16384, Q = D / 32;
+    const int L = a.L, per_tile = Q * L;
+    const long long total = static_cast<long long>(n_tiles) * per_tile;
+    TileInfo ti{}, tn{};
+    uint32_t idw[4], idn[4];
+    float pk[QVG_PSAC_RANK];
+    if (n_tiles > 0) {
+        ti = tile_info(a, tb);
+        load_stage_ids<D>(a, pr, h, ti, r, idw);
+    }
+    if (n_tiles > 1) {
+        tn = tile_info(a, tb + 1);
+        load_stage_ids<D>(a, pr, h, tn, r, idn);
+    }
+    QuarterData<BITS> cur, nxt;
+    if (total > 0) load_quarter<D, BITS, OUTL>(a, pr, h, ti, r, stage_id(idw, 0), 0, 0, cur);
+    uint64_t acc[16];
+    int t = 0, qt = 0, l = 0;
+    for (long long u = 0; u < total; ++u) {
+        if (qt == 0 && l == 0) {
+            // start of tile t: its PSAC codes (used after the first quarter's stages)
+            if (pr.psac && ti.chunk >= 0 && r < ti.nvalid) {
+                const size_t prow = static_cast<size_t>(h) * a.cap + ti.s0 + r;
+                const float pS = f16_to_f32(a.psac_s[prow]);
+                const int2 pv = *reinterpret_cast<const int2 *>(a.psac_p + prow * QVG_PSAC_RANK);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                pk[k] = pS * static_cast<float>(static_cast<int8_t>((pv.x >> (8 * k)) & 0xff));
-                pk[k + 4] = pS * static_cast<float>(static_cast<int8_t>((pv.y >> (8 * k)) & 0xff));
-            }
-        }
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb) {
-#pragma unroll 2
-            for (int c8 = 0; c8 < 8; ++c8) {
-                uint4 o = make_uint4(0, 0, 0, 0);
-                if (valid && raw) {
-                    o = bf16x8_to_f16(*reinterpret_cast<const uint4 *>(
-                        pr.raw + (static_cast<size_t>(ti.s0 - a.n_slots + r) * a.H + h) * D + kb * 64 + c8 * 8));
-                } else if (valid) {
-                    float kv[8];
-                    rebuild8<D, BITS>(a, pr.codes, pr.scales, pr.ids, pr.cent, pr.outv, pr.outi, h, ti.chunk,
-                                      ti.s0 + r, kb * 64 + c8 * 8, pr.psac ? pk : nullptr, kv);
-                    o = make_uint4(h2(kv[0], kv[1]), h2(kv[2], kv[3]), h2(kv[4], kv[5]), h2(kv[6], kv[7]));
+                for (int k = 0; k < 4; ++k) {
+                    pk[k] = pS * static_cast<float>(static_cast<int8_t>((pv.x >> (8 * k)) & 0xff));
+                    pk[k + 4] = pS * static_cast<float>(static_cast<int8_t>((pv.y >> (8 * k)) & 0xff));
                 }
-                *reinterpret_cast<uint4 *>(T + kb * 16384 + ((c8 ^ (r & 7)) << 4)) = o;
             }
         }
-        umma::fence_proxy_async_smem();
-        umma::mbar_arrive(&pr.full[b]);
+        // prefetch step u + 1
+        int l1 = l + 1, q1 = qt, t1 = t;
+        if (l1 == L) {
+            l1 = 0;
+            if (++q1 == Q) {
+                q1 = 0;
+                ++t1;
+            }
+        }
+        if (u + 1 < total) {
+            if (t1 == t)
+                load_quarter<D, BITS, OUTL>(a, pr, h, ti, r, stage_id(idw, l1), l1, q1, nxt);
+            else
+                load_quarter<D, BITS, OUTL>(a, pr, h, tn, r, stage_id(idn, l1), l1, q1, nxt);
+        }
+        if (l == 0) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc[k] = 0ull;
+        }
+        accumulate_quarter<BITS, OUTL>(cur, acc);
+        if (l == L - 1) {
+            const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
+            uint8_t *T = pr.buf0 + b * TB + r * 128;
+            if (qt == 0 && use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
+            float v[32];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) up2(acc[k], v[2 * k], v[2 * k + 1]);
+            if (pr.psac && ti.chunk >= 0 && r < ti.nvalid) {
+                const float *U = a.psac_basis + ((static_cast<size_t>(ti.chunk) * a.H + h) * D + qt * 32) * QVG_PSAC_RANK;
+#pragma unroll 4
+                for (int e = 0; e < 32; ++e) {
+                    const float4 u0 = *reinterpret_cast<const float4 *>(U + e * QVG_PSAC_RANK);
+                    const float4 u1 = *reinterpret_cast<const float4 *>(U + e * QVG_PSAC_RANK + 4);
+                    float corr = 0.0f;
+                    corr = fmaf(pk[0], u0.x, corr);
+                    corr = fmaf(pk[1], u0.y, corr);
+                    corr = fmaf(pk[2], u0.z, corr);
+                    corr = fmaf(pk[3], u0.w, corr);
+                    corr = fmaf(pk[4], u1.x, corr);
+                    corr = fmaf(pk[5], u1.y, corr);
+                    corr = fmaf(pk[6], u1.z, corr);
+                    corr = fmaf(pk[7], u1.w, corr);
+                    v[e] = v[e] + corr;
+                }
+            }
+            const int kb = qt >> 1, c0 = (qt & 1) * 4;
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                *reinterpret_cast<uint4 *>(T + kb * 16384 + (((c0 + x) ^ (r & 7)) << 4)) =
+                    make_uint4(h2(v[8 * x], v[8 * x + 1]), h2(v[8 * x + 2], v[8 * x + 3]),
+                               h2(v[8 * x + 4], v[8 * x + 5]), h2(v[8 * x + 6], v[8 * x + 7]));
+            if (qt == Q - 1) {
+                umma::fence_proxy_async_smem();
+                umma::mbar_arrive(&pr.full[b]);
+            }
+        }
+        cur = nxt;
+        if (t1 != t) {  // next tile: shift the tile state, fetch the one after
+            ti = tn;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) idw[i] = idn[i];
+            if (t1 + 1 < n_tiles) {
+                tn = tile_info(a, tb + t1 + 1);
+                load_stage_ids<D>(a, pr, h, tn, r, idn);
+            }
+        }
+        t = t1;
+        qt = q1;
+        l = l1;
     }
 }
 
@@ -839,8 +975,10 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             produce_fast<D, BITS, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         else if (a.L == 1 && !pr.psac && a.group >= 32)
             produce_fast_outl<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+        else if (pr.outi)
+            produce_general<D, BITS, true>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         else
-            produce_general<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+            produce_general<D, BITS, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
     }
     __syncwarp();
     umma::tc_fence_before();

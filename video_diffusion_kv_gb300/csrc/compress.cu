@@ -563,12 +563,19 @@ template <> struct RowLoad<float> {
 // cluster into offsets (earlier warps first) and scans the cluster totals,
 // pass 3 walks the range again and places each token at its cluster's start
 // + the offset of its warp + its rank among the earlier equal ids of the
-// warp.  Then one warp per cluster of the CTA's share sums the members' stage
-// input in that order (fp32, eight row loads in flight), divides by the
-// count, rounds to bf16 and writes the centroid and its weighted norm; an
-// empty cluster keeps its centroid.  Deterministic, with no atomic
-// accumulation of values.  A diagonal weight leaves the minimiser at the
-// plain mean.
+// warp.  CTA x then finalises the contiguous cluster range
+// [x Ce / kUpdSplit, (x + 1) Ce / kUpdSplit), whose members are contiguous in
+// that order; the slice is cut into one equal run of positions per warp, so
+// one very large cluster (the smallest-norm centroid collects the tiny
+// residuals of a later stage) is summed by many warps.  Each warp sums the
+// members' stage input over its run in order (fp32, eight row loads in
+// flight); a cluster that lies inside the run is finalised at once, a
+// cluster cut by the run's ends leaves a partial sum in shared memory, and
+// the warp holding the cluster's first member adds the partials in warp
+// order.  Finalising divides by the count, rounds to bf16 and writes the
+// centroid and its weighted norm; an empty cluster keeps its centroid.
+// Deterministic, with no atomic accumulation of values.  A diagonal weight
+// leaves the minimiser at the plain mean.
 constexpr int kUpdThreads = 1024;
 constexpr int kUpdSplit = 8;  // CTAs per head, each finalising an eighth of the clusters
 
@@ -647,29 +654,18 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
         __syncwarp();
     }
     __syncthreads();
-    // this CTA's clusters: one warp each, members summed in token order
-    for (int c = blockIdx.x + kUpdSplit * warp; c < Ce; c += kUpdSplit * W) {
-        const int beg = cnt[c], end = cnt[c + 1];
-        if (end == beg) continue;  // empty: keep the centroid
-        float acc[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = 0.0f;
-        for (int i0 = beg; i0 < end; i0 += 8) {
-            int nn[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) nn[q] = i0 + q < end ? static_cast<int>(order[i0 + q]) : -1;
-            float v[8][E];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (nn[q] >= 0)
-                    RowLoad<TIn>::template load<E>(xin + (static_cast<size_t>(nn[q]) * H + h) * D + lane * E, v[q]);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (nn[q] >= 0)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) acc[e] += v[q][e];
-        }
-        const float cntf = static_cast<float>(end - beg);
+    // this CTA's clusters and its warps' runs of the sorted order; wc is free
+    // again and holds the partial sums, two rows per warp ([0]: the run's
+    // first cluster, begun before the run; [1]: its last, going on after it)
+    float (*part)[2][D] = reinterpret_cast<float (*)[2][D]>(&wc[0][0]);
+    static_assert(sizeof(float) * W * 2 * D <= sizeof(int) * W * QVG_MAX_CLUSTERS, "partials fit in wc");
+    const int c_lo = static_cast<int>(static_cast<long long>(Ce) * blockIdx.x / kUpdSplit);
+    const int c_hi = static_cast<int>(static_cast<long long>(Ce) * (blockIdx.x + 1) / kUpdSplit);
+    const int p_lo = cnt[c_lo], M = cnt[c_hi] - p_lo;
+    auto run_beg = [&](int w2) { return p_lo + static_cast<int>(static_cast<long long>(M) * w2 / W); };
+    const int a = run_beg(warp), b = run_beg(warp + 1);
+    auto finalise = [&](int c, const float (&acc)[E]) {
+        const float cntf = static_cast<float>(cnt[c + 1] - cnt[c]);
         uint16_t *row = cent + static_cast<size_t>(h) * hs + static_cast<size_t>(c) * D + lane * E;
         float nrm = 0.0f;
 #pragma unroll
@@ -682,6 +678,56 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
         }
         for (int o = 16; o > 0; o >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o);
         if (lane == 0) cnorm[h * C + c] = nrm;
+    };
+    int split_c = -1;  // a cluster that starts in this run and goes on after it
+    if (a < b) {
+        int c = c_lo;
+        while (cnt[c + 1] <= a) ++c;
+        for (int pos = a; pos < b; ++c) {
+            if (cnt[c + 1] <= pos) continue;  // empty cluster
+            const int end = min(b, cnt[c + 1]);
+            float acc[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+            for (int i0 = pos; i0 < end; i0 += 8) {
+                int nn[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) nn[q] = i0 + q < end ? static_cast<int>(order[i0 + q]) : -1;
+                float v[8][E];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (nn[q] >= 0)
+                        RowLoad<TIn>::template load<E>(xin + (static_cast<size_t>(nn[q]) * H + h) * D + lane * E, v[q]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (nn[q] >= 0)
+#pragma unroll
+                        for (int e = 0; e < E; ++e) acc[e] += v[q][e];
+            }
+            const bool head = cnt[c] >= a, tail = cnt[c + 1] <= b;
+            if (head && tail) {
+                finalise(c, acc);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) part[warp][head ? 1 : 0][lane * E + e] = acc[e];
+                if (head) split_c = c;
+            }
+            pos = end;
+        }
+    }
+    __syncthreads();
+    if (split_c >= 0) {  // add the later runs' partials of split_c, in warp order
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = part[warp][1][lane * E + e];
+        for (int w2 = warp + 1; w2 < W; ++w2) {
+            const int a2 = run_beg(w2), b2 = run_beg(w2 + 1);
+            if (a2 >= cnt[split_c + 1]) break;
+            if (a2 < b2)
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] += part[w2][0][lane * E + e];
+        }
+        finalise(split_c, acc);
     }
 }
 
