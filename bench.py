@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's sources so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "86ed491b7c939949769afcc083928cf41f8f480d36042558589f4d1144074b13": 80417280 + 4183808,
+    "516e47cb19b38dcd393889e44fe5ea42948db7944015b5fdc5b536c4c17869be": 80465664 + 4174080,
 }
 
 
