@@ -754,6 +754,81 @@ def study_paths(args):
     return 0
 
 
+def study_layers(args):
+    """Multi-layer streaming rollout: a 48-layer stack of LongCat-like layers
+    (16 KV heads, d=128; INT2 C=256 G=64, 8 iterations) generates 8 chunks of
+    4680 tokens (37,440 tokens, about the 38K-token, 5-second LongCat-Video
+    clip of the QVG notes).  Each chunk step runs, for every layer in order,
+    the AR-step attention of the chunk's 4680 queries over the layer's
+    compressed history plus the chunk's own raw K/V (qvg_attention_ar), then
+    compresses the chunk's K and V into that layer's cache.  Reports the
+    time of each chunk step, and the memory held against the uncompressed
+    size 2 x layers x KV heads x head_dim x tokens x 2 B ("The 2-bit
+    quantisation trap", section 1).  Layers draw from a pool of 4 synthetic
+    chunk sets (seeded per position), cycled over the layers."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import video_diffusion_kv_gb300 as qvg
+    from video_diffusion_kv_gb300 import synth
+    w = synth.WORKLOADS["longcat"]
+    layers, pool = 48, 4
+    p = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=21)
+    per = -(-w.N // 128) * 128
+    cap = w.n_chunks * per
+    base = torch.cuda.memory_allocated()
+    kcs = [qvg.CompressedKV(p, w.H, w.d, cap, w.n_chunks) for _ in range(layers)]
+    vcs = [qvg.CompressedKV(p, w.H, w.d, cap, w.n_chunks) for _ in range(layers)]
+    held = torch.cuda.memory_allocated() - base
+    K = [[synth_dev(synth.chunk_kv(w, 21 + j, k, synth.KIND_K), "cuda") for k in range(w.n_chunks)] for j in range(pool)]
+    V = [[synth_dev(synth.chunk_kv(w, 21 + j, k, synth.KIND_V), "cuda") for k in range(w.n_chunks)] for j in range(pool)]
+    Q = [[synth_dev(synth.queries(w, 21 + j, k), "cuda") for k in range(w.n_chunks)] for j in range(pool)]
+    ws = torch.empty(qvg.workspace_size(p, qvg.QVG_OP_COMPRESS, w.N, w.H, w.d), dtype=torch.uint8, device="cuda")
+    aws = torch.empty(max(qvg.workspace_size(p, qvg.QVG_OP_ATTENTION, w.Nq, w.H, w.d, w.Hq), 1), dtype=torch.uint8,
+                      device="cuda")
+    out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    steps = []
+    for k in range(w.n_chunks):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        evs = []
+        e[0].record()
+        for li in range(layers):
+            j = li % pool
+            ea = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ea[0].record()
+            qvg.attention_ar(p, Q[j][k], kcs[li], vcs[li], K[j][k], V[j][k], out_dtype=qvg.QVG_OUT_BF16, out=out,
+                             workspace=aws)
+            ea[1].record()
+            qvg.compress_chunk(p, K[j][k], kcs[li], workspace=ws)
+            qvg.compress_chunk(p, V[j][k], vcs[li], workspace=ws)
+            ea[2].record()
+            evs.append(ea)
+        e[1].record()
+        torch.cuda.synchronize()
+        ta = sum(ea[0].elapsed_time(ea[1]) for ea in evs)
+        tc = sum(ea[1].elapsed_time(ea[2]) for ea in evs)
+        tokens = (k + 1) * w.N
+        steps.append({"chunk": k + 1, "cache_tokens_after": tokens, "step_ms": e[0].elapsed_time(e[1]),
+                      "attention_ms": ta, "compress_ms": tc})
+    tokens = w.tokens
+    comp = sum(c.nbytes for c in kcs + vcs)
+    bf16 = qvg.kv_bytes_uncompressed(layers, w.H, w.d, tokens)
+    ratio = qvg.compression_ratio(p, w.H, w.d, w.N, w.n_chunks)
+    print(json.dumps({"study": "layers", "workload": "48 layers x 16 KV heads x d=128, 8 chunks x 4680 tokens "
+                      "(37,440), INT2 C=256 G=64, 8 iters; per layer: AR-step attention then compress K and V",
+                      "status": qvg.get_status(), "steps": steps,
+                      "total_ms": sum(x["step_ms"] for x in steps),
+                      "memory": {"cache_bytes_allocated": held, "cache_bytes_sized": comp,
+                                 "bf16_bytes_same_tokens": bf16, "ratio_stored": ratio,
+                                 "device_bytes_in_use": torch.cuda.memory_allocated()},
+                      "page_scale": {"what": "32 KV heads x d=128 x 48 layers (a LongCat-Video-sized stack) at 37,440 tokens",
+                                     "bf16_bytes": qvg.kv_bytes_uncompressed(layers, 32, w.d, tokens),
+                                     "compressed_bytes": qvg.kv_bytes_uncompressed(layers, 32, w.d, tokens) / ratio}}),
+          flush=True)
+    return 0
+
+
 def synth_dev(a, dev):
     import torch
     return torch.from_numpy(a).to(dev, torch.bfloat16).contiguous()
@@ -768,7 +843,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="time the device step only (profiling)")
     ap.add_argument("--cache-chunks", type=int, default=None, help="smaller cache (profiling cases)")
-    ap.add_argument("--workload", default="longcat", choices=["longcat", "qvgpro", "quantwm", "rollout", "outlier", "paths"],
+    ap.add_argument("--workload", default="longcat", choices=["longcat", "qvgpro", "quantwm", "rollout", "outlier", "paths", "layers"],
                     help="longcat: the benchmark line; the others print their study line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "own":
@@ -777,7 +852,7 @@ def main():
         return run_reference(args)
     if args.workload != "longcat":
         return {"qvgpro": study_qvgpro, "quantwm": study_quantwm, "rollout": study_rollout,
-                "outlier": study_outlier, "paths": study_paths}[args.workload](args)
+                "outlier": study_outlier, "paths": study_paths, "layers": study_layers}[args.workload](args)
     return run_own(args)
 
 

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
                 }
             }
             if (U) {
-#pragma unroll 4
+#pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const float *u = U + (cb * 32 + e) * QVG_PSAC_RANK;
                     float corr = 0.0f;
