@@ -683,8 +683,9 @@ def study_paths(args):
     """Attention read paths on the LongCat-like layer (16 heads, d=128, 8
     chunks of 4680 tokens, C=256, 8 iters): 4680 queries over the whole
     compressed cache for one-stage INT2 G=64 (plain, and with the outlier
-    split), the split with G=16, two stages (QVG-Pro) and PSAC on the keys
-    (rank-8 orthonormal basis, seeded).  Median of 5 launches, L2 flushed
+    split), the split with G=16, two stages (QVG-Pro), PSAC on the keys
+    (rank-8 orthonormal basis, seeded) and temporal anchors (chunks 0 and 4
+    kept as bf16, read as raw tiles between the INT2 ones).  Median of 5 launches, L2 flushed
     before each; plus the time to compress the newest chunk (K and V)."""
     import statistics
     import numpy as np
@@ -708,7 +709,7 @@ def study_paths(args):
     arms = {}
     for name, kw in (("L1_G64", {}), ("outlier_G64", dict(flags=qvg.QVG_OUTLIER)),
                      ("outlier_G16", dict(flags=qvg.QVG_OUTLIER, group=16)), ("L2_G64", dict(L=2)),
-                     ("psac_G64", dict(flags=qvg.QVG_PSAC))):
+                     ("psac_G64", dict(flags=qvg.QVG_PSAC)), ("anchors_every4", dict(anchor_every=4))):
         p = qvg.Params(**{**dict(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=seed), **kw})
         pv = qvg.Params(**{**p.__dict__, "flags": p.flags & ~qvg.QVG_PSAC})
         kc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks)
@@ -747,7 +748,7 @@ def study_paths(args):
         ms_c = timed(lambda: compress(last), rewind)
         ms_a = timed(lambda: qvg.attention(p, q, kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out))
         arms[name] = {"attention_ms": ms_a, "attention_TFLOP/s": 4.0 * w.Nq * w.tokens * w.d * w.Hq / ms_a / 1e9,
-                      "compress_ms_KV": ms_c}
+                      "compress_ms_KV": ms_c, "ratio": qvg.compression_ratio(p, w.H, w.d, w.N, w.n_chunks)}
         del kc, vc
     print(json.dumps({"study": "paths", "workload": "16 heads, d=128, 8 chunks x 4680 tokens, C=256, INT2, 8 iters; "
                       "4680 queries", "status": qvg.get_status(), "arms": arms}), flush=True)

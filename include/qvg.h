@@ -58,7 +58,7 @@ typedef enum {
 #define QVG_TILE 128      /* chunks start at multiples of this many token slots */
 #define QVG_PSAC_RANK 8   /* PSAC subspace rank ([QWM] PSAC: top-8 directions)  */
 #define QVG_MAX_CLUSTERS 256
-#define QVG_CACHE_NBUF 12
+#define QVG_CACHE_NBUF 14
 
 /* Output element types of qvg_decompress / qvg_attention. */
 #define QVG_OUT_F32 0
@@ -80,7 +80,12 @@ typedef enum {
  *   iters      Lloyd iterations (assign + update) before the final assign.
  *   scale_mode 0: S = max|r| / (2^{b-1} - 1)  ([QVG] "core tension");
  *              1: S = max|r| / 2, codes in [-2, 1]  ([P1] section 2; bits = 2).
- *   flags      QVG_QSAC | QVG_PSAC | QVG_GIVEN_CENTROIDS.
+ *   flags      QVG_QSAC | QVG_PSAC | QVG_GIVEN_CENTROIDS | QVG_OUTLIER.
+ *   anchor_every  temporal anchors ([P2] section 3.3: the first frames of
+ *              each window are kept at high precision so that errors do not
+ *              pile up from window to window): 0 = none; k > 0 = chunk c of
+ *              a cache (0-based) with c % k == 0 is stored as its bf16 K/V
+ *              in the cache's anchor arena instead of being compressed.
  *   seed       k-means initialisation seed.
  * A cache must always be used with the C, L, bits and group it was sized for.
  */
@@ -92,7 +97,7 @@ typedef struct {
     int32_t iters;
     int32_t scale_mode;
     int32_t flags;
-    int32_t reserved; /* must be 0 */
+    int32_t anchor_every;
     uint64_t seed;
 } qvg_params;
 
@@ -127,6 +132,14 @@ typedef struct {
  *              it is rebuilt as outl_val + centroid.
  *   outl_idx   uint8 [L][H][capacity][d/G]  its channel within the group,
  *              0xFF when no value lies above the percentile (0 in outl_val).
+ *   anchor     bf16  [A][H][d]  anchor chunks' K or V as given (with
+ *              anchor_every > 0, else NULL).  Anchor chunk c starts at row
+ *              (c / anchor_every) * S, S = capacity / max_chunks rounded up
+ *              to QVG_TILE, and A = ceil(max_chunks / anchor_every) * S; an
+ *              anchor chunk longer than S is refused (QVG_ERR_CAPACITY).  Its
+ *              token slots in the other buffers are reserved but unused.
+ *   chunk_anchor int32 [max_chunks]  first anchor row of each chunk, -1 for
+ *              a compressed chunk (with anchor_every > 0, else NULL).
  * n_chunks and n_tokens are host-side counters that qvg_compress_chunk
  * advances; set both to 0 for an empty cache.  A cache can be saved and
  * restored by copying its buffers and these two counters.
@@ -150,6 +163,8 @@ typedef struct {
     float *psac_basis;
     uint16_t *outl_val;
     uint8_t *outl_idx;
+    uint16_t *anchor;
+    int32_t *chunk_anchor;
 } qvg_cache;
 
 /* Text for a status code (static storage; never NULL). */
@@ -158,8 +173,9 @@ const char *qvg_status_string(qvg_status s);
 /*
  * Bytes of each cache buffer, in the order codes, scales, ids, cent,
  * chunk_start, chunk_len, tile_chunk, psac_p, psac_s, psac_basis, outl_val,
- * outl_idx (out_sizes has QVG_CACHE_NBUF entries).  The PSAC entries are 0
- * unless p->flags has QVG_PSAC, the outlier entries 0 unless QVG_OUTLIER.  capacity_tokens must be a positive multiple of
+ * outl_idx, anchor, chunk_anchor (out_sizes has QVG_CACHE_NBUF entries).
+ * The PSAC entries are 0 unless p->flags has QVG_PSAC, the outlier entries
+ * 0 unless QVG_OUTLIER, the anchor entries 0 unless p->anchor_every > 0.  capacity_tokens must be a positive multiple of
  * QVG_TILE.  The total is the compressed footprint; [P1] section 1 gives
  * the uncompressed one, 2 (K and V) x layers x heads x head_dim x tokens x
  * bytes per element.

@@ -38,6 +38,9 @@ def host_cache(c: qvg.CompressedKV):
         ng = d // p.group
         out["outl_val"] = c.view("outl_val", torch.int16, (L, H, cap, ng)).cpu().numpy().view(np.uint16)
         out["outl_idx"] = c.view("outl_idx", torch.uint8, (L, H, cap, ng)).cpu().numpy()
+    if p.anchor_every > 0:
+        out["anchor"] = c.view("anchor", torch.int16, (-1, H, d)).cpu().numpy().view(np.uint16)
+        out["chunk_anchor"] = c.view("chunk_anchor", torch.int32, (c.max_chunks,)).cpu().numpy()
     return out
 
 
@@ -55,7 +58,11 @@ def chunk_arrays(hc, p, k):
 
 
 def oracle_rebuild(hc, p, k):
-    """Oracle reconstruction [N,H,d] of chunk k from the GPU's stored bytes."""
+    """Oracle reconstruction [N,H,d] of chunk k from the GPU's stored bytes
+    (an anchor chunk: its stored bf16 rows, as they are)."""
+    if "chunk_anchor" in hc and hc["chunk_anchor"][k] >= 0:
+        r0, n = int(hc["chunk_anchor"][k]), int(hc["length"][k])
+        return oracle.bf16_bits_to_f32(hc["anchor"][r0:r0 + n])
     codes, scales, ids, cent = chunk_arrays(hc, p, k)
     kw = {}
     sl = chunk_slice(hc, k)

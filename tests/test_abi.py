@@ -169,6 +169,31 @@ def test_outlier_split_arguments(lib):
     assert lib.qvg_compress_chunk(ct.byref(p), x, 100, None, None, ct.byref(c), ws, 1 << 30, None) == qvg.QVG_ERR_INVALID_ARG
 
 
+def test_anchor_arguments(lib):
+    """Temporal anchors: anchor_every >= 0; with anchors the cache carries
+    the bf16 anchor arena (ceil(max_chunks / k) chunks of S rows, S the
+    capacity per chunk rounded up to a tile) and the per-chunk table; an
+    anchor chunk longer than S is refused."""
+    p = _params(C=16, group=32, anchor_every=2)
+    out = (ct.c_size_t * qvg.QVG_CACHE_NBUF)()
+    assert lib.qvg_cache_bytes(ct.byref(p), 2, 64, 512, 4, out) == qvg.QVG_OK
+    assert out[12] == 2 * 128 * 2 * 64 * 2 and out[13] == 4 * 4
+    p3 = _params(C=16, group=32, anchor_every=3)
+    assert lib.qvg_cache_bytes(ct.byref(p3), 2, 64, 512, 4, out) == qvg.QVG_OK
+    assert out[12] == 2 * 128 * 2 * 64 * 2
+    p0 = _params(C=16, group=32)
+    assert lib.qvg_cache_bytes(ct.byref(p0), 2, 64, 512, 4, out) == qvg.QVG_OK
+    assert out[12] == 0 and out[13] == 0
+    bad = _params(C=16, group=32, anchor_every=-1)
+    assert lib.qvg_cache_bytes(ct.byref(bad), 2, 64, 512, 4, out) == qvg.QVG_ERR_INVALID_ARG
+    x, ws = ct.c_void_p(0x2000), ct.c_void_p(0x100000)
+    c = _fake_cache(cap=512, max_chunks=2)  # S = 256 rows per anchor chunk
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 300, None, None, ct.byref(c), ws, 1 << 30, None) == qvg.QVG_ERR_CAPACITY
+    c.anchor = None
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 100, None, None, ct.byref(c), ws, 1 << 30, None) == qvg.QVG_ERR_INVALID_ARG
+    assert c.n_chunks == 0 and c.n_tokens == 0
+
+
 def test_attention_ar_rejects_on_host(lib):
     """The AR-step call: raw current-chunk buffers must be present and
     16-byte aligned, n_cur >= 0, and there must be at least one key."""

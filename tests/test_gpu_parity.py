@@ -446,6 +446,61 @@ def test_outlier_split_longcat():
     _assert_attention(out.cpu().numpy()[rows].astype(np.float64), ref, w.Hq)
 
 
+@pytest.mark.parametrize("case,every,n_chunks", [("tiny", 2, 4), ("pro_int2_L3", 2, 3), ("tiny_outlier", 3, 4)])
+def test_anchor_chunks(case, every, n_chunks):
+    """Temporal anchors: every `every`-th chunk is kept as its bf16 K/V.  Its
+    stored rows are the input bit for bit, decompress returns them exactly,
+    the compressed chunks still match the fed oracle, and attention and the
+    AR step over the mixed cache (bf16 anchor tiles between INT2 tiles, one
+    and three stages, with the outlier split) match the fp64 oracle."""
+    w, p0, _ = CASES[case]
+    p = qvg.Params(**{**p0.__dict__, "anchor_every": every})
+    chunks = [(synth.chunk_kv(w, 29, k, synth.KIND_K), synth.chunk_kv(w, 29, k, synth.KIND_V)) for k in range(n_chunks)]
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    hk = host_cache(kc)
+    full = qvg.decompress(p, kc, 0, kc.n_tokens).cpu().numpy()
+    for k, (x, _) in enumerate(chunks):
+        sl = chunk_slice(hk, k)
+        if k % every == 0:
+            assert hk["chunk_anchor"][k] >= 0
+            np.testing.assert_array_equal(oracle_rebuild(hk, p, k), x)
+            np.testing.assert_array_equal(full[sl], x)
+        else:
+            assert hk["chunk_anchor"][k] == -1
+            _check_against_fed_oracle(x, hk, p, k)
+            np.testing.assert_array_equal(full[sl], oracle_rebuild(hk, p, k))
+    q = synth.queries(w, 29, n_chunks)
+    out, lse, top1 = qvg.attention(p, to_dev(q), kc, vc, want_lse=True, want_top1=True)
+    ref, rlse, ram, kh, hk = _oracle_attention_on(kc, vc, p, q)
+    _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
+    np.testing.assert_allclose(lse.cpu().numpy(), rlse, atol=2e-3, rtol=0)
+    _assert_top1(top1.cpu().numpy(), q, kh, _slot_of_token(hk, n_chunks), ram)
+    kr = synth.chunk_kv(w, 29, n_chunks, synth.KIND_K)[:100]
+    vr = synth.chunk_kv(w, 29, n_chunks, synth.KIND_V)[:100]
+    out, _, _ = qvg.attention_ar(p, to_dev(q), kc, vc, to_dev(kr), to_dev(vr))
+    ref, _, _ = _oracle_ar(kc, vc, p, q, kr, vr)
+    _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
+
+
+def test_anchor_chunks_longcat():
+    """LongCat-like (16 heads, d=128, INT2 G=64): the first of 2 chunks is an
+    anchor; attention of 4680 queries (64 sampled rows per head checked)
+    and 16 queries (split cache) against the oracle."""
+    w, p0, _ = CASES["longcat"]
+    p = qvg.Params(**{**p0.__dict__, "anchor_every": 2})
+    chunks = [(synth.chunk_kv(w, 30, k, synth.KIND_K), synth.chunk_kv(w, 30, k, synth.KIND_V)) for k in range(2)]
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    q = synth.queries(w, 30, 2)
+    out, _, _ = qvg.attention(p, to_dev(q), kc, vc)
+    rows = np.random.default_rng(4).choice(q.shape[0], 64, replace=False)
+    ref, _, _, _, _ = _oracle_attention_on(kc, vc, p, q, rows)
+    _assert_attention(out.cpu().numpy()[rows].astype(np.float64), ref, w.Hq)
+    q16 = np.ascontiguousarray(q[:16])
+    out, _, _ = qvg.attention(p, to_dev(q16), kc, vc)
+    ref, _, _, _, _ = _oracle_attention_on(kc, vc, p, q16)
+    _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
+
+
 def test_ragged_and_degenerate_chunks():
     """Chunks of 300 (two tiles plus a ragged 44), 1 token, 10 tokens with
     C=16 > N, and exactly 128 tokens; attention across all of them."""

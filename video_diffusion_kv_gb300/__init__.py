@@ -24,7 +24,7 @@ QVG_ERR_TIMEOUT, QVG_ERR_WORKSPACE, QVG_ERR_CAPACITY = 4, 5, 6
 QVG_QSAC, QVG_PSAC, QVG_GIVEN_CENTROIDS, QVG_OUTLIER = 1, 2, 4, 8
 QVG_TILE = 128
 QVG_PSAC_RANK = 8
-QVG_CACHE_NBUF = 12
+QVG_CACHE_NBUF = 14
 QVG_OUT_F32, QVG_OUT_BF16 = 0, 1
 QVG_OP_COMPRESS, QVG_OP_ATTENTION, QVG_OP_PSAC_BASIS = 0, 1, 2
 
@@ -36,7 +36,7 @@ EXPORTED = (
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 BUFFER_NAMES = ("codes", "scales", "ids", "cent", "chunk_start", "chunk_len", "tile_chunk",
-                "psac_p", "psac_s", "psac_basis", "outl_val", "outl_idx")
+                "psac_p", "psac_s", "psac_basis", "outl_val", "outl_idx", "anchor", "chunk_anchor")
 
 
 class QvgError(RuntimeError):
@@ -48,7 +48,7 @@ class QvgError(RuntimeError):
 class _Params(ct.Structure):
     _fields_ = [("C", ct.c_int32), ("L", ct.c_int32), ("bits", ct.c_int32),
                 ("group", ct.c_int32), ("iters", ct.c_int32), ("scale_mode", ct.c_int32),
-                ("flags", ct.c_int32), ("reserved", ct.c_int32), ("seed", ct.c_uint64)]
+                ("flags", ct.c_int32), ("anchor_every", ct.c_int32), ("seed", ct.c_uint64)]
 
 
 class _Cache(ct.Structure):
@@ -57,7 +57,8 @@ class _Cache(ct.Structure):
                 ("codes", ct.c_void_p), ("scales", ct.c_void_p), ("ids", ct.c_void_p),
                 ("cent", ct.c_void_p), ("chunk_start", ct.c_void_p), ("chunk_len", ct.c_void_p),
                 ("tile_chunk", ct.c_void_p), ("psac_p", ct.c_void_p), ("psac_s", ct.c_void_p),
-                ("psac_basis", ct.c_void_p), ("outl_val", ct.c_void_p), ("outl_idx", ct.c_void_p)]
+                ("psac_basis", ct.c_void_p), ("outl_val", ct.c_void_p), ("outl_idx", ct.c_void_p),
+                ("anchor", ct.c_void_p), ("chunk_anchor", ct.c_void_p)]
 
 
 _lib = None
@@ -113,10 +114,11 @@ class Params:
     scale_mode: int = 0
     flags: int = 0
     seed: int = 0
+    anchor_every: int = 0
 
     def c(self):
         return _Params(self.C, self.L, self.bits, self.group, self.iters, self.scale_mode,
-                       self.flags, 0, self.seed)
+                       self.flags, self.anchor_every, self.seed)
 
 
 def _ptr(t):
@@ -339,15 +341,19 @@ def get_status():
 def compression_ratio(params: Params, H, d, tokens_per_chunk, n_chunks, with_psac=False):
     """bf16 bytes / compressed bytes for n_chunks chunks, counting codes,
     fp16 scales, 1-byte ids, bf16 centroids, the outlier side list (fp16
-    value + 1-byte channel per group and stage, with QVG_OUTLIER) and
-    (optionally) the PSAC data, at the stored sizes (padding slots
-    excluded)."""
-    N = tokens_per_chunk * n_chunks
+    value + 1-byte channel per group and stage, with QVG_OUTLIER),
+    (optionally) the PSAC data, and anchor chunks (anchor_every > 0) at
+    their bf16 size, at the stored sizes (padding slots, and the slots an
+    anchor chunk reserves in the compressed buffers, excluded)."""
+    n_anchor = -(-n_chunks // params.anchor_every) if params.anchor_every > 0 else 0
+    n_comp = n_chunks - n_anchor
+    N = tokens_per_chunk * n_comp
     side = 3 * d / params.group if params.flags & QVG_OUTLIER else 0
     per_tok = params.L * (d * params.bits / 8 + 2 * d / params.group + (1 if params.C > 0 else 0) + side)
     if with_psac:
         per_tok += QVG_PSAC_RANK + 2
-    comp = H * N * per_tok + params.L * H * n_chunks * params.C * d * 2
+    comp = H * N * per_tok + params.L * H * n_comp * params.C * d * 2
     if with_psac:
-        comp += n_chunks * H * d * QVG_PSAC_RANK * 4
-    return (H * N * d * 2) / comp
+        comp += n_comp * H * d * QVG_PSAC_RANK * 4
+    comp += n_anchor * tokens_per_chunk * H * d * 2
+    return (H * tokens_per_chunk * n_chunks * d * 2) / comp

@@ -35,7 +35,7 @@ bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 // Validation of the method parameters against a head_dim.
 qvg_status check_params(const qvg_params *p, int d) {
     if (!p) return QVG_ERR_INVALID_ARG;
-    if (p->reserved != 0 || p->L < 1 || p->L > 16 || p->C < 0 || p->iters < 0 ||
+    if (p->anchor_every < 0 || p->L < 1 || p->L > 16 || p->C < 0 || p->iters < 0 ||
         p->iters > 10000 || (p->bits != 2 && p->bits != 4) || p->group < 1 ||
         (p->scale_mode != 0 && p->scale_mode != 1) || (p->flags & ~15))
         return QVG_ERR_INVALID_ARG;
@@ -64,6 +64,7 @@ qvg_status check_cache(const qvg_params *p, const qvg_cache *c) {
     if ((p->flags & QVG_PSAC) && (!c->psac_p || !c->psac_s || !c->psac_basis))
         return QVG_ERR_INVALID_ARG;
     if ((p->flags & QVG_OUTLIER) && (!c->outl_val || !c->outl_idx)) return QVG_ERR_INVALID_ARG;
+    if (p->anchor_every > 0 && (!c->anchor || !c->chunk_anchor)) return QVG_ERR_INVALID_ARG;
     return QVG_OK;
 }
 
@@ -132,6 +133,12 @@ qvg_status qvg_cache_bytes(const qvg_params *p, int32_t H, int32_t d, int32_t ca
     const bool outl = p->flags & QVG_OUTLIER;
     out[10] = outl ? L * rows * (d / p->group) * sizeof(uint16_t) : 0;
     out[11] = outl ? L * rows * (d / p->group) : 0;
+    const bool anch = p->anchor_every > 0;
+    const size_t arows = anch ? static_cast<size_t>((max_chunks + p->anchor_every - 1) / p->anchor_every) *
+                                    anchor_stride(cap, max_chunks)
+                              : 0;
+    out[12] = arows * H * d * sizeof(uint16_t);
+    out[13] = anch ? sizeof(int32_t) * static_cast<size_t>(max_chunks) : 0;
     return QVG_OK;
 }
 
@@ -174,6 +181,22 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     const int chunk = cache->n_chunks, slot0 = cache->n_tokens;
+    if (p->anchor_every > 0 && chunk % p->anchor_every == 0) {
+        // temporal anchor: the chunk's bf16 K/V, kept as given
+        const int S = anchor_stride(cache->capacity_tokens, cache->max_chunks);
+        if (N > S) return QVG_ERR_CAPACITY;
+        const int row0 = (chunk / p->anchor_every) * S;
+        if (cudaMemcpyAsync(cache->anchor + static_cast<size_t>(row0) * H * d, x_bf16,
+                            static_cast<size_t>(N) * H * d * sizeof(uint16_t), cudaMemcpyDeviceToDevice,
+                            st) != cudaSuccess)
+            return QVG_ERR_CUDA;
+        if ((s = launch_chunk_table(chunk, slot0, N, cache->chunk_start, cache->chunk_len, cache->tile_chunk,
+                                    cache->chunk_anchor, row0, st)) != QVG_OK)
+            return s;
+        cache->n_chunks = chunk + 1;
+        cache->n_tokens = slot0 + Naligned;
+        return QVG_OK;
+    }
     const int C = p->C, Ce = std::min(C, N), L = p->L;
     const float *w = (p->flags & QVG_QSAC) ? qsac_w : nullptr;
     const bool psac = p->flags & QVG_PSAC, outl = p->flags & QVG_OUTLIER;
@@ -222,7 +245,8 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
             outl ? cache->outl_idx + lrow * ng : nullptr, st);
         if (s != QVG_OK) return s;
     }
-    if ((s = launch_chunk_table(chunk, slot0, N, cache->chunk_start, cache->chunk_len, cache->tile_chunk, st)) != QVG_OK)
+    if ((s = launch_chunk_table(chunk, slot0, N, cache->chunk_start, cache->chunk_len, cache->tile_chunk,
+                                p->anchor_every > 0 ? cache->chunk_anchor : nullptr, -1, st)) != QVG_OK)
         return s;
     cache->n_chunks = chunk + 1;
     cache->n_tokens = slot0 + Naligned;

@@ -51,6 +51,10 @@ struct AttnWsArgs {
     // fp16 value split off and its channel in the group (0xFF: none), or NULL
     const uint16_t *koutv, *voutv;
     const uint8_t *kouti, *vouti;
+    // temporal anchors (blog "project X", section 3.3): anchor chunks are
+    // read as bf16 rows of these arenas; chunk_anchor[c] = first row, or -1
+    const uint16_t *kanch, *vanch;
+    const int32_t *chunk_anchor;
 };
 
 namespace ws {
@@ -96,22 +100,42 @@ __device__ __forceinline__ void group_sync(int i) {
     asm volatile("bar.sync %0, 128;" ::"r"(1 + i) : "memory");
 }
 
-// Tile t covers slots [s0, s0 + QVG_TILE) of which the first nvalid hold
-// tokens.  Tiles below n_ctiles are cache tiles (chunk = the chunk that owns
-// them); the rest hold the current chunk's raw rows (chunk = -1).
+// Tile t covers slots [t QVG_TILE, (t + 1) QVG_TILE), of which the first
+// nvalid hold tokens.  Tiles below n_ctiles are cache tiles (chunk = the
+// chunk that owns them, base = the first slot); the rest hold the current
+// chunk's raw rows (chunk = -1).  A tile of an anchor chunk is read raw as
+// well, from the anchor arena (chunk = -2).  A raw tile's base is the row of
+// its first slot in its source.  RAW = false: no raw tile can occur (no
+// current-chunk rows, no anchors), and the lookup is the cache's alone.
 struct TileInfo {
-    int s0, chunk, nvalid;
+    int base, chunk, nvalid;
 };
 
+template <bool RAW>
 __device__ __forceinline__ TileInfo tile_info(const AttnWsArgs &a, int t) {
     TileInfo ti;
-    ti.s0 = t * QVG_TILE;
-    if (t < a.n_ctiles) {
+    const int s0 = t * QVG_TILE;
+    ti.base = s0;
+    if constexpr (!RAW) {
         ti.chunk = a.tile_chunk[t];
-        ti.nvalid = min(QVG_TILE, max(0, a.chunk_start[ti.chunk] + a.chunk_len[ti.chunk] - ti.s0));
+        ti.nvalid = min(QVG_TILE, max(0, a.chunk_start[ti.chunk] + a.chunk_len[ti.chunk] - s0));
+        return ti;
+    }
+    if (t < a.n_ctiles) {
+        const int c = a.tile_chunk[t], start = a.chunk_start[c];
+        ti.chunk = c;
+        ti.nvalid = min(QVG_TILE, max(0, start + a.chunk_len[c] - s0));
+        if (a.chunk_anchor) {
+            const int arow = a.chunk_anchor[c];
+            if (arow >= 0) {
+                ti.chunk = -2;
+                ti.base = arow + s0 - start;
+            }
+        }
     } else {
         ti.chunk = -1;
         ti.nvalid = min(QVG_TILE, a.n_raw - (t - a.n_ctiles) * QVG_TILE);
+        ti.base = s0 - a.n_slots;
     }
     return ti;
 }
@@ -326,7 +350,8 @@ struct Producer {
     const uint16_t *scales;
     const uint8_t *ids;
     const uint16_t *cent;
-    const uint16_t *raw;  // the current chunk's rows (raw tiles)
+    const uint16_t *raw;   // the current chunk's rows (raw tiles)
+    const uint16_t *anch;  // the anchor arena (anchor tiles)
     const uint16_t *outv;  // outlier split side list, or NULL
     const uint8_t *outi;
     uint8_t *buf0;
@@ -335,13 +360,13 @@ struct Producer {
     bool psac;
 };
 
-template <int D, int BITS, bool OUTL>
+template <int D, int BITS, bool OUTL, bool RAW>
 __device__ __forceinline__ void load_tile_half(const AttnWsArgs &a, const Producer &pr, int h, const TileInfo &ti,
                                                int r, int id, int kb, HalfData<BITS> &hd) {
-    if (ti.chunk >= 0)
-        load_half<D, BITS, OUTL>(a, pr.codes, pr.scales, pr.cent, pr.outv, pr.outi, h, ti.chunk, ti.s0 + r, id, kb, hd);
+    if (!RAW || ti.chunk >= 0)
+        load_half<D, BITS, OUTL>(a, pr.codes, pr.scales, pr.cent, pr.outv, pr.outi, h, ti.chunk, ti.base + r, id, kb, hd);
     else
-        load_half_raw<D, BITS>(pr.raw, a.H, h, ti.s0 - a.n_slots + r, kb, hd);
+        load_half_raw<D, BITS>(ti.chunk == -2 ? pr.anch : pr.raw, a.H, h, ti.base + r, kb, hd);
 }
 
 // One stage, no PSAC.  The loads of one 64-channel half are always in
@@ -349,7 +374,7 @@ __device__ __forceinline__ void load_tile_half(const AttnWsArgs &a, const Produc
 // first half of a tile and B for the second when D = 128); table entries and
 // cluster ids run two tiles ahead (ids are read for cache tiles only, whose
 // slots t * QVG_TILE + r < n_slots <= capacity: in bounds).
-template <int D, int BITS, bool OUTL>
+template <int D, int BITS, bool OUTL, bool RAW>
 __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
                                              int n_tiles, volatile int *vfail) {
     constexpr int KB = D / 64, TB = KB * 16384;
@@ -357,27 +382,27 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
     TileInfo ti0{}, ti1{};
     int id0 = 0, id1 = 0;
     if (n_tiles > 0) {
-        ti0 = tile_info(a, tb);
+        ti0 = tile_info<RAW>(a, tb);
         if (a.C > 0 && ti0.chunk >= 0) id0 = pr.ids[id_row];
     }
     if (n_tiles > 1) {
-        ti1 = tile_info(a, tb + 1);
+        ti1 = tile_info<RAW>(a, tb + 1);
         if (a.C > 0 && ti1.chunk >= 0) id1 = pr.ids[id_row + QVG_TILE];
     }
     HalfData<BITS> A, B;
-    if (n_tiles > 0 && r < ti0.nvalid) load_tile_half<D, BITS, OUTL>(a, pr, h, ti0, r, id0, 0, A);
+    if (n_tiles > 0 && r < ti0.nvalid) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, ti0, r, id0, 0, A);
     for (int t = 0; t < n_tiles; ++t) {
         const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
         uint8_t *T = pr.buf0 + b * TB + r * 128;
         TileInfo ti2{};
         int id2 = 0;
         if (t + 2 < n_tiles) {
-            ti2 = tile_info(a, tb + t + 2);
+            ti2 = tile_info<RAW>(a, tb + t + 2);
             if (a.C > 0 && ti2.chunk >= 0) id2 = pr.ids[id_row + static_cast<size_t>(t + 2) * QVG_TILE];
         }
         const bool valid = r < ti0.nvalid, valid1 = t + 1 < n_tiles && r < ti1.nvalid;
         if constexpr (KB == 2) {
-            if (valid) load_tile_half<D, BITS, OUTL>(a, pr, h, ti0, r, id0, 1, B);
+            if (valid) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, ti0, r, id0, 1, B);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
             if (valid) {
                 decode_store_half<BITS>(A, T, r);
@@ -385,7 +410,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             } else {
                 zero_line(T);
             }
-            if (valid1) load_tile_half<D, BITS, OUTL>(a, pr, h, ti1, r, id1, 0, A);
+            if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, ti1, r, id1, 0, A);
             if (valid) {
                 decode_store_half<BITS>(B, T + 16384, r);
                 if (OUTL) patch_outliers<D, BITS>(a, pr.cent, B, h, ti0.chunk, id0, 1, T + 16384, r);
@@ -394,7 +419,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             }
         } else {
             B = A;
-            if (valid1) load_tile_half<D, BITS, OUTL>(a, pr, h, ti1, r, id1, 0, A);
+            if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, ti1, r, id1, 0, A);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
             if (valid) {
                 decode_store_half<BITS>(B, T, r);
@@ -417,7 +442,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
 template <int D, int BITS>
 __device__ __noinline__ void produce_fast_outl(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
                                                int n_tiles, volatile int *vfail) {
-    produce_fast<D, BITS, true>(a, pr, h, r, tb, n_tiles, vfail);
+    produce_fast<D, BITS, true, true>(a, pr, h, r, tb, n_tiles, vfail);
 }
 
 // Several stages, PSAC, or the outlier split with groups under 32 channels.
@@ -456,7 +481,7 @@ __device__ __forceinline__ void load_stage_ids(const AttnWsArgs &a, const Produc
     for (int i = 0; i < 4; ++i) w[i] = 0u;
     if (a.C == 0 || ti.chunk < 0 || r >= ti.nvalid) return;
     for (int l = 0; l < a.L; ++l) {
-        const uint32_t v = pr.ids[(static_cast<size_t>(l) * a.H + h) * a.cap + ti.s0 + r];
+        const uint32_t v = pr.ids[(static_cast<size_t>(l) * a.H + h) * a.cap + ti.base + r];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             if (i == (l >> 2)) w[i] |= v << (8 * (l & 3));
@@ -474,16 +499,17 @@ __device__ __forceinline__ void load_quarter(const AttnWsArgs &a, const Producer
     qd.oe = 0xFFFFFFFFu;
     qd.ov = make_uint2(0, 0);
     if (r >= ti.nvalid) return;
-    if (ti.chunk < 0) {  // the current chunk's raw row, in stage 0
+    if (ti.chunk < 0) {  // a raw row (the current chunk's or an anchor's), in stage 0
         if (l == 0) {
-            const uint16_t *row = pr.raw + (static_cast<size_t>(ti.s0 - a.n_slots + r) * a.H + h) * D + qt * 32;
+            const uint16_t *row =
+                (ti.chunk == -2 ? pr.anch : pr.raw) + (static_cast<size_t>(ti.base + r) * a.H + h) * D + qt * 32;
 #pragma unroll
             for (int i = 0; i < 4; ++i) qd.cr[i] = *reinterpret_cast<const uint4 *>(row + 8 * i);
         }
         return;
     }
     const int ng = D / a.group;
-    const size_t srow = (static_cast<size_t>(l) * a.H + h) * a.cap + ti.s0 + r;
+    const size_t srow = (static_cast<size_t>(l) * a.H + h) * a.cap + ti.base + r;
     const uint8_t *cp = pr.codes + srow * (D * BITS / 8) + qt * (4 * BITS);
     if constexpr (BITS == 2) {
         const uint2 u = *reinterpret_cast<const uint2 *>(cp);
@@ -575,11 +601,11 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
     uint32_t idw[4], idn[4];
     float pk[QVG_PSAC_RANK];
     if (n_tiles > 0) {
-        ti = tile_info(a, tb);
+        ti = tile_info<true>(a, tb);
         load_stage_ids<D>(a, pr, h, ti, r, idw);
     }
     if (n_tiles > 1) {
-        tn = tile_info(a, tb + 1);
+        tn = tile_info<true>(a, tb + 1);
         load_stage_ids<D>(a, pr, h, tn, r, idn);
     }
     QuarterData<BITS> cur, nxt;
@@ -590,7 +616,7 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
         if (qt == 0 && l == 0) {
             // start of tile t: its PSAC codes (used after the first quarter's stages)
             if (pr.psac && ti.chunk >= 0 && r < ti.nvalid) {
-                const size_t prow = static_cast<size_t>(h) * a.cap + ti.s0 + r;
+                const size_t prow = static_cast<size_t>(h) * a.cap + ti.base + r;
                 const float pS = f16_to_f32(a.psac_s[prow]);
                 const int2 pv = *reinterpret_cast<const int2 *>(a.psac_p + prow * QVG_PSAC_RANK);
 #pragma unroll
@@ -662,7 +688,7 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 #pragma unroll
             for (int i = 0; i < 4; ++i) idw[i] = idn[i];
             if (t1 + 1 < n_tiles) {
-                tn = tile_info(a, tb + t1 + 1);
+                tn = tile_info<true>(a, tb + t1 + 1);
                 load_stage_ids<D>(a, pr, h, tn, r, idn);
             }
         }
@@ -693,7 +719,12 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 //   kfree/vfree  MMA commits -> producer tile consumed (S_0 and S_1 / PV_0 and PV_1)
 //   sfull[i]     MMA commit -> group i   S_i ready
 //   ofull[i]     MMA commit -> group i   PV_i done (P_i free, O_i settled)
-template <int D, int BITS, bool TOP1>
+// MODE 0: one-stage caches without the outlier split or PSAC, no raw tiles;
+// MODE 1: the same with raw bf16 tiles (the current chunk, anchor chunks);
+// MODE 2: several stages, PSAC or the outlier split (out-of-line producers).
+// Separate instantiations keep the out-of-line producers' call sites, which
+// cost the plain kernel 7 % when present, out of modes 0 and 1.
+template <int D, int BITS, bool TOP1, int MODE>
 __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) {
     using namespace ws;
     constexpr int KB = D / 64;
@@ -790,7 +821,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         float m_used = -INFINITY, l_sum = 0.0f, best = -INFINITY;
         int best_slot = 0;
         for (int t = 0; t < n_tiles; ++t) {
-            const TileInfo ti = tile_info(a, tb + t);
+            const TileInfo ti = tile_info<MODE != 0>(a, tb + t);
             if (live) live = __all_sync(0xffffffffu, ws::wait(&sfull[i], t & 1, vfail));
             float corr = 1.0f;
             if (live) {
@@ -835,7 +866,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 if constexpr (TOP1) {
                     if (tmax > best) {
                         best = tmax;
-                        best_slot = ti.s0 + targ;
+                        best_slot = (tb + t) * QVG_TILE + targ;
                     }
                 }
                 bool rescale = false;
@@ -967,18 +998,25 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         // ------------------------------------------------ K / V producers (thread = slot)
         const bool isv = warp >= 12;
         const Producer pr{isv ? a.vcodes : a.kcodes, isv ? a.vscales : a.kscales, isv ? a.vids : a.kids,
-                          isv ? a.vcent : a.kcent, isv ? a.vraw : a.kraw, isv ? a.voutv : a.koutv,
+                          isv ? a.vcent : a.kcent, isv ? a.vraw : a.kraw, isv ? a.vanch : a.kanch,
+                          isv ? a.voutv : a.koutv,
                           isv ? a.vouti : a.kouti, isv ? Vt0 : Kt, isv ? vfull : &kfull,
                           isv ? vfree : &kfree,
                           isv ? 2 : 1, !isv && a.psac_p != nullptr};
-        if (a.L == 1 && !pr.psac && !pr.outi)
-            produce_fast<D, BITS, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
-        else if (a.L == 1 && !pr.psac && a.group >= 32)
-            produce_fast_outl<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
-        else if (pr.outi)
-            produce_general<D, BITS, true>(a, pr, h, tid & 127, tb, n_tiles, vfail);
-        else
-            produce_general<D, BITS, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+        if constexpr (MODE == 0) {
+            produce_fast<D, BITS, false, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+        } else if constexpr (MODE == 1) {
+            produce_fast<D, BITS, false, true>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+        } else {
+            if (a.L == 1 && !pr.psac && !pr.outi)
+                produce_fast<D, BITS, false, true>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+            else if (a.L == 1 && !pr.psac && a.group >= 32)
+                produce_fast_outl<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+            else if (pr.outi)
+                produce_general<D, BITS, true>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+            else
+                produce_general<D, BITS, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+        }
     }
     __syncwarp();
     umma::tc_fence_before();
@@ -1045,12 +1083,12 @@ __global__ void __launch_bounds__(256) k_attn_merge(const float *__restrict__ po
     }
 }
 
-template <int D, int BITS, bool TOP1>
+template <int D, int BITS, bool TOP1, int MODE>
 static qvg_status attn_ws_t(const AttnWsArgs &a, int a_splits, cudaStream_t st) {
     constexpr size_t smem = 5 * (D / 64) * 16384 + 2 * 32768 + 1024;
     static bool attr = false;
     if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(k_attention_ws<D, BITS, TOP1>,
+        const cudaError_t e = cudaFuncSetAttribute(k_attention_ws<D, BITS, TOP1, MODE>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
@@ -1060,14 +1098,18 @@ static qvg_status attn_ws_t(const AttnWsArgs &a, int a_splits, cudaStream_t st) 
         attr = true;
     }
     dim3 grid(ceil_div(a.Nq, 256), a.Hq, a_splits);
-    k_attention_ws<D, BITS, TOP1><<<grid, ws::kThreads, smem, st>>>(a);
+    k_attention_ws<D, BITS, TOP1, MODE><<<grid, ws::kThreads, smem, st>>>(a);
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }
 
 template <int D, int BITS>
 static qvg_status attn_ws(const AttnWsArgs &a, int splits, cudaStream_t st) {
-    return a.top1 ? attn_ws_t<D, BITS, true>(a, splits, st) : attn_ws_t<D, BITS, false>(a, splits, st);
+    if (a.L > 1 || a.psac_p || a.kouti)
+        return a.top1 ? attn_ws_t<D, BITS, true, 2>(a, splits, st) : attn_ws_t<D, BITS, false, 2>(a, splits, st);
+    if (a.n_raw > 0 || a.chunk_anchor)
+        return a.top1 ? attn_ws_t<D, BITS, true, 1>(a, splits, st) : attn_ws_t<D, BITS, false, 1>(a, splits, st);
+    return a.top1 ? attn_ws_t<D, BITS, true, 0>(a, splits, st) : attn_ws_t<D, BITS, false, 0>(a, splits, st);
 }
 
 static int attn_sm_count() {
@@ -1138,6 +1180,11 @@ qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, i
     a.psac_p = psac ? k->psac_p : nullptr;
     a.psac_s = k->psac_s;
     a.psac_basis = k->psac_basis;
+    if (p->anchor_every > 0) {
+        a.kanch = k->anchor;
+        a.vanch = v->anchor;
+        a.chunk_anchor = k->chunk_anchor;
+    }
     if (p->flags & QVG_OUTLIER) {
         a.koutv = k->outl_val;
         a.kouti = k->outl_idx;

@@ -137,9 +137,15 @@ qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, in
                                  uint16_t *psac_s, size_t psac_head_stride, uint16_t *outl_val,
                                  uint8_t *outl_idx, cudaStream_t st);
 qvg_status launch_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start,
-                              int32_t *chunk_len, int32_t *tile_chunk, cudaStream_t st);
+                              int32_t *chunk_len, int32_t *tile_chunk, int32_t *chunk_anchor,
+                              int anchor_row, cudaStream_t st);
 qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, int ntok,
                              void *out, int out_dtype, cudaStream_t st);
+// Rows of the anchor arena reserved per anchor chunk: the capacity per
+// chunk, rounded up to a whole tile.
+inline int anchor_stride(int capacity_tokens, int max_chunks) {
+    return ((capacity_tokens / max_chunks + QVG_TILE - 1) / QVG_TILE) * QVG_TILE;
+}
 qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, int Hq,
                                const qvg_cache *k, const qvg_cache *v, float scale_log2,
                                const uint16_t *k_cur, const uint16_t *v_cur, int n_cur,

@@ -999,12 +999,13 @@ __global__ void __launch_bounds__(256) k_residual_quant(
 }
 
 __global__ void k_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start, int32_t *chunk_len,
-                              int32_t *tile_chunk) {
+                              int32_t *tile_chunk, int32_t *chunk_anchor, int anchor_row) {
     pdl_wait();
     pdl_trigger();
     if (threadIdx.x == 0) {
         chunk_start[chunk] = slot0;
         chunk_len[chunk] = N;
+        if (chunk_anchor) chunk_anchor[chunk] = anchor_row;
     }
     const int t0 = slot0 / QVG_TILE, nt = ceil_div(N, QVG_TILE);
     for (int t = threadIdx.x; t < nt; t += blockDim.x) tile_chunk[t0 + t] = chunk;
@@ -1224,9 +1225,9 @@ qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, in
 }
 
 qvg_status launch_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start, int32_t *chunk_len,
-                              int32_t *tile_chunk, cudaStream_t st) {
+                              int32_t *tile_chunk, int32_t *chunk_anchor, int anchor_row, cudaStream_t st) {
     const cudaError_t e = launch_pdl(k_chunk_table, dim3(1), dim3(256), 0, st, chunk, slot0, N, chunk_start,
-                                     chunk_len, tile_chunk);
+                                     chunk_len, tile_chunk, chunk_anchor, anchor_row);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         note_cuda_error(e);

@@ -5,7 +5,8 @@
 // (stages summed in fp32 in stage order).  QuantWM write-up, PSAC: the
 // stored projection of the key error is added back as P_hat U^T.  Blog
 // "project X", section 3.4 (outlier separation): a value split off from its
-// group is rebuilt from its fp16 copy.
+// group is rebuilt from its fp16 copy; section 3.3 (temporal anchors): an
+// anchor chunk's values are its stored bf16 K/V.
 #include "common.cuh"
 
 namespace qvg {
@@ -21,6 +22,8 @@ struct CacheView {
     const float *psac_basis;
     const uint16_t *outl_val;
     const uint8_t *outl_idx;
+    const uint16_t *anchor;
+    const int32_t *chunk_anchor;
     int H, cap, max_chunks;
 };
 
@@ -47,9 +50,12 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
     const int slot = tok0 + t;
     const int chunk = cv.tile_chunk[slot / QVG_TILE];
     const bool valid = slot >= cv.chunk_start[chunk] && slot < cv.chunk_start[chunk] + cv.chunk_len[chunk];
+    const int arow = cv.chunk_anchor ? cv.chunk_anchor[chunk] : -1;  // an anchor chunk's first row, or -1
+    const uint16_t *arow_p = arow >= 0 && valid ? cv.anchor + (static_cast<size_t>(arow + slot - cv.chunk_start[chunk]) * H + h) * D
+                                                : nullptr;
     float pk[QVG_PSAC_RANK];
     const float *U = nullptr;
-    if (PSAC && valid) {
+    if (PSAC && valid && !arow_p) {
         const size_t prow = static_cast<size_t>(h) * cv.cap + slot;
         const float pSp = f16_to_f32(cv.psac_s[prow]);
 #pragma unroll
@@ -62,7 +68,18 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
         float acc[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
-        if (valid) {
+        if (arow_p) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(arow_p + cb * 32 + 8 * i);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    acc[8 * i + 2 * k] = __uint_as_float(w4[k] << 16);
+                    acc[8 * i + 2 * k + 1] = __uint_as_float(w4[k] & 0xffff0000u);
+                }
+            }
+        } else if (valid) {
             for (int l = 0; l < L; ++l) {
                 const size_t srow = (static_cast<size_t>(l) * H + h) * cv.cap + slot;
                 uint32_t cw[CB / 4];
@@ -148,8 +165,9 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
 qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, int ntok,
                              void *out, int out_dtype, cudaStream_t st) {
     CacheView cv{c->codes, c->scales, c->ids, c->cent, c->chunk_start, c->chunk_len,
-                 c->tile_chunk, c->psac_p, c->psac_s, c->psac_basis, c->outl_val, c->outl_idx, c->H,
-                 c->capacity_tokens, c->max_chunks};
+                 c->tile_chunk, c->psac_p, c->psac_s, c->psac_basis, c->outl_val, c->outl_idx, c->anchor,
+                 c->chunk_anchor, c->H, c->capacity_tokens, c->max_chunks};
+    if (p->anchor_every <= 0) cv.chunk_anchor = nullptr;
     if (!(p->flags & QVG_PSAC)) cv.psac_p = nullptr;
     if (!(p->flags & QVG_OUTLIER)) cv.outl_idx = nullptr;
     float *o32 = out_dtype == QVG_OUT_F32 ? static_cast<float *>(out) : nullptr;
