@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's sources so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "516e47cb19b38dcd393889e44fe5ea42948db7944015b5fdc5b536c4c17869be": 80465664 + 4174080,
+    "9b1b9b82b1ac493e58d4d682630f09480b91265f31467fd1b3d181b743574ead": 80390400 + 3454464,
 }
 
 
