@@ -93,16 +93,22 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
-        self.index, self.proc, self.lines = index, None, []
+        self.index, self.proc, self.lines, self.first = index, None, [], 0
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # nvidia-smi takes a while to start: wait (up to 3 s) for its first
+            # sample so that the samples fall inside the timed region
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.01)
+            self.first = len(self.lines)
         except Exception:
             self.proc = None
 
@@ -121,7 +127,9 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        # samples taken from the start of the timed region on (the last one
+        # read before it started, if none fell inside)
+        for ln in self.lines[self.first:] or self.lines[-1:]:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -394,14 +402,24 @@ def run_own(args):
     out_pin = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     k_d, v_d, q_d = torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(q)
 
+    # the inputs arrive on a copy stream, in the order they are needed, so
+    # that V's and Q's copies run under the compression of K
+    copy_stream = torch.cuda.Stream(dev)
+    arrived = [torch.cuda.Event() for _ in range(3)]
+
     def e2e_step():
         kc.reset(last, last * slots_per_chunk)
         vc.reset(last, last * slots_per_chunk)
-        k_d.copy_(k_pin, non_blocking=True)
-        v_d.copy_(v_pin, non_blocking=True)
-        q_d.copy_(q_pin, non_blocking=True)
+        with torch.cuda.stream(copy_stream):
+            for dst, src, ev in ((k_d, k_pin, arrived[0]), (v_d, v_pin, arrived[1]), (q_d, q_pin, arrived[2])):
+                dst.copy_(src, non_blocking=True)
+                ev.record(copy_stream)
+        cur = torch.cuda.current_stream(dev)
+        cur.wait_event(arrived[0])
         qvg.compress_chunk(p, k_d, kc, workspace=workspace)
+        cur.wait_event(arrived[1])
         qvg.compress_chunk(p, v_d, vc, workspace=workspace)
+        cur.wait_event(arrived[2])
         qvg.attention(p, q_d, kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out)
         out_pin.copy_(out, non_blocking=True)
 
