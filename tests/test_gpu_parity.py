@@ -585,13 +585,18 @@ def test_query_stats_and_basis():
     assert 0.69 < frac.cpu().numpy().min() and frac.cpu().numpy().max() < 0.75
 
 
-@pytest.mark.parametrize("flags", [qvg.QVG_QSAC, qvg.QVG_PSAC, qvg.QVG_QSAC | qvg.QVG_PSAC])
-def test_quantwm_compress_and_attention(flags):
+@pytest.mark.parametrize("flags,anchor_every", [(qvg.QVG_QSAC, 0), (qvg.QVG_PSAC, 0), (qvg.QVG_QSAC | qvg.QVG_PSAC, 0),
+                                                (qvg.QVG_QSAC | qvg.QVG_PSAC, 2)])
+def test_quantwm_compress_and_attention(flags, anchor_every):
+    """QuantWM caches (QSAC weights, PSAC on K; with anchor_every = 2 the
+    first chunk is a bf16 anchor, which carries no PSAC term): compression
+    against the fed oracle, PSAC codes, the rebuild, and attention (plain
+    and AR step) against the fp64 oracle."""
     w = _quantwm_small()
     qh = synth.history_queries(w, 22)
     M, wv, cnt = qvg.query_stats(to_dev(qh), w.H)
     U, _, _ = qvg.psac_basis(M, cnt)
-    p = qvg.Params(C=256, L=1, bits=2, group=64, iters=8, seed=23, flags=flags)
+    p = qvg.Params(C=256, L=1, bits=2, group=64, iters=8, seed=23, flags=flags, anchor_every=anchor_every)
     chunks = [(synth.chunk_kv(w, 23, k, synth.KIND_K), synth.chunk_kv(w, 23, k, synth.KIND_V)) for k in range(2)]
     cap = 2 * (-(-w.N // 128) * 128)
     kc = qvg.CompressedKV(p, w.H, w.d, cap, 2)
@@ -604,6 +609,9 @@ def test_quantwm_compress_and_attention(flags):
     ww = wv.cpu().numpy() if flags & qvg.QVG_QSAC else None
     Uh = U.cpu().numpy() if flags & qvg.QVG_PSAC else None
     for k, (x, _) in enumerate(chunks):
+        if anchor_every and k % anchor_every == 0:
+            np.testing.assert_array_equal(oracle_rebuild(hk, p, k), x)
+            continue
         o, ok = _check_against_fed_oracle(x, hk, p, k, w=ww, psac_U=Uh)
         if Uh is not None:
             sl = chunk_slice(hk, k)
