@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
     // token tile k -> buffer k % NA: each thread's copies arrive on bar_a once
     // done, and each thread arrives once more after its part of the extra K
     // block (core matrix layout: row r, K half kh at (r/8)*256 + kh*128 + (r%8)*16)
-    auto load_tile = [&](int k) {
+    auto load_tokens = [&](int k) {
         const int n0 = (t0 + k * tstep) * 128;
         uint8_t *dst = As + (k % NA) * AB;
 #pragma unroll 4
@@ -237,6 +237,9 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
                              g + (static_cast<size_t>(in ? n0 + r : 0) * H + h) * D + ci * 8, in);
         }
         umma::cp_async_arrive_noinc(&bar_a[k % NA]);
+    };
+    auto load_norms = [&](int k) {
+        const int n0 = (t0 + k * tstep) * 128;
         if (tid < 256) {
             const int r = tid >> 1, kh = tid & 1;
             uint4 v = make_uint4(0, 0, 0, 0);
@@ -251,12 +254,19 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         }
         umma::mbar_arrive(&bar_a[k % NA]);
     };
+    auto load_tile = [&](int k) {
+        load_tokens(k);
+        load_norms(k);
+    };
 
-    // before the previous kernel (the centroid update) has finished: only the
-    // token tiles (this stage's input, written earlier) and their norms
-    for (int k = 0; k < NA - 1 && k < my_tiles; ++k) load_tile(k);
+    // before the previous kernel has finished: only the token tiles (this
+    // stage's input, complete before the kernels in between began); their
+    // norms may come from the kernel just before (the first assignment of a
+    // stage follows the row norms), so they are read after the wait
+    for (int k = 0; k < NA - 1 && k < my_tiles; ++k) load_tokens(k);
     pdl_wait();
     pdl_trigger();
+    for (int k = 0; k < NA - 1 && k < my_tiles; ++k) load_norms(k);
     // centroids (or weighted hi/lo pair) -> swizzled K-major bf16, once
     if constexpr (P == 1) {
 #pragma unroll 4
@@ -1100,8 +1110,11 @@ qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d, const ui
              : assign_tc_impl<128, 1>(g, N, H, cent, hs, Ce, cnorm, C, w, xnorm, ids, st);
 }
 
-// ||x||_w^2 per (token, head) row of the clustering operand: one warp per row,
-// D/32 consecutive channels per lane (fp32, ascending), xor-butterfly sum.
+// ||x||_w^2 per (token, head) row of the clustering operand: a warp takes
+// kNormRows consecutive rows with all their loads in flight, each row D/32
+// consecutive channels per lane (fp32, ascending) and an xor-butterfly sum.
+constexpr int kNormRows = 4;
+
 template <int D>
 __global__ void __launch_bounds__(256) k_row_norms(const uint16_t *__restrict__ g, int N, int H,
                                                    const float *__restrict__ w, float *__restrict__ xnorm) {
@@ -1109,26 +1122,33 @@ __global__ void __launch_bounds__(256) k_row_norms(const uint16_t *__restrict__ 
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (row >= static_cast<long long>(N) * H) return;
-    const int n = static_cast<int>(row / H), h = static_cast<int>(row % H);
-    float v[E];
-    RowLoad<uint16_t>::template load<E>(g + static_cast<size_t>(row) * D + lane * E, v);
-    float sx = 0.0f;
+    const long long row0 = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kNormRows;
+    const long long rows = static_cast<long long>(N) * H;
+    if (row0 >= rows) return;
+    float v[kNormRows][E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const float wj = w ? w[h * D + lane * E + e] : 1.0f;
-        sx = fmaf(wj * v[e], v[e], sx);
+    for (int i = 0; i < kNormRows; ++i)
+        if (row0 + i < rows) RowLoad<uint16_t>::template load<E>(g + static_cast<size_t>(row0 + i) * D + lane * E, v[i]);
+#pragma unroll
+    for (int i = 0; i < kNormRows; ++i) {
+        if (row0 + i >= rows) break;
+        const int n = static_cast<int>((row0 + i) / H), h = static_cast<int>((row0 + i) % H);
+        float sx = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float wj = w ? w[h * D + lane * E + e] : 1.0f;
+            sx = fmaf(wj * v[i][e], v[i][e], sx);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+        if (lane == 0) xnorm[static_cast<size_t>(h) * N + n] = sx;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
-    if (lane == 0) xnorm[static_cast<size_t>(h) * N + n] = sx;
 }
 
 qvg_status launch_row_norms(const uint16_t *g, int N, int H, int d, const float *w, float *xnorm,
                             cudaStream_t st) {
     const long long rows = static_cast<long long>(N) * H;
-    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    const unsigned blocks = static_cast<unsigned>((rows + 8 * kNormRows - 1) / (8 * kNormRows));
     const cudaError_t e = d == 64 ? launch_pdl(k_row_norms<64>, dim3(blocks), dim3(256), 0, st, g, N, H, w, xnorm)
                                   : launch_pdl(k_row_norms<128>, dim3(blocks), dim3(256), 0, st, g, N, H, w, xnorm);
     if (e != cudaSuccess) {
