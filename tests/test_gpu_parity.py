@@ -132,6 +132,25 @@ def test_compress_matches_oracle(name):
             assert abs(rg - ro) <= 0.05 * ro + 1e-6, (rg, ro)
 
 
+@pytest.mark.parametrize("name", ["longcat", "pro_int2_L3", "pro_outlier_L2"])
+def test_compress_is_deterministic(name):
+    """The same chunks compressed three times leave byte-identical caches:
+    every reduction runs in a fixed order, and no kernel reads what the
+    launch before it writes until it has waited for that launch."""
+    w, p, n_chunks = CASES[name]
+    xs = [synth.chunk_kv(w, 34, k, synth.KIND_K) for k in range(n_chunks)]
+    runs = []
+    for _ in range(3):
+        c = _new_cache(w, p, n_chunks)
+        for x in xs:
+            qvg.compress_chunk(p, to_dev(x), c)
+        runs.append(host_cache(c))
+    assert qvg.get_status() == qvg.QVG_OK
+    for other in runs[1:]:
+        for name_ in runs[0]:
+            np.testing.assert_array_equal(other[name_], runs[0][name_], err_msg=name_)
+
+
 @pytest.mark.parametrize("name", ["tiny", "pro_int2_L3", "longcat"])
 def test_kmeans_init_exact(name):
     """Zero Lloyd iterations: the centroids are the seeded picks, bit for bit."""
