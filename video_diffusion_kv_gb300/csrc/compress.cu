@@ -565,7 +565,7 @@ template <> struct RowLoad<float> {
 };
 
 // ---------------------------------------------------------------------------
-// Update, one kernel: each CTA (kUpdSplit per head) first orders the head's
+// Update, one kernel: each CTA (S = gridDim.x per head) first orders the head's
 // token indices by cluster in shared memory, stably (ascending token index
 // inside each cluster).  Warp w owns a contiguous range of tokens: pass 1
 // counts its tokens per cluster (warp match: the lowest lane of each group of
@@ -574,7 +574,7 @@ template <> struct RowLoad<float> {
 // pass 3 walks the range again and places each token at its cluster's start
 // + the offset of its warp + its rank among the earlier equal ids of the
 // warp.  CTA x then finalises the contiguous cluster range
-// [x Ce / kUpdSplit, (x + 1) Ce / kUpdSplit), whose members are contiguous in
+// [x Ce / S, (x + 1) Ce / S), whose members are contiguous in
 // that order; the slice is cut into one equal run of positions per warp, so
 // one very large cluster (the smallest-norm centroid collects the tiny
 // residuals of a later stage) is summed by many warps.  Each warp sums the
@@ -587,7 +587,8 @@ template <> struct RowLoad<float> {
 // Deterministic, with no atomic accumulation of values.  A diagonal weight
 // leaves the minimiser at the plain mean.
 constexpr int kUpdThreads = 1024;
-constexpr int kUpdSplit = 8;  // CTAs per head, each finalising an eighth of the clusters
+// CTAs per head: about one per SM over all heads, 2..16
+inline int update_splits(int H, int n_sm) { return std::max(2, std::min(16, n_sm / std::max(1, H))); }
 
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__restrict__ xin, int N, int H,
@@ -669,8 +670,8 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
     // first cluster, begun before the run; [1]: its last, going on after it)
     float (*part)[2][D] = reinterpret_cast<float (*)[2][D]>(&wc[0][0]);
     static_assert(sizeof(float) * W * 2 * D <= sizeof(int) * W * QVG_MAX_CLUSTERS, "partials fit in wc");
-    const int c_lo = static_cast<int>(static_cast<long long>(Ce) * blockIdx.x / kUpdSplit);
-    const int c_hi = static_cast<int>(static_cast<long long>(Ce) * (blockIdx.x + 1) / kUpdSplit);
+    const int c_lo = static_cast<int>(static_cast<long long>(Ce) * blockIdx.x / gridDim.x);
+    const int c_hi = static_cast<int>(static_cast<long long>(Ce) * (blockIdx.x + 1) / gridDim.x);
     const int p_lo = cnt[c_lo], M = cnt[c_hi] - p_lo;
     auto run_beg = [&](int w2) { return p_lo + static_cast<int>(static_cast<long long>(M) * w2 / W); };
     const int a = run_beg(warp), b = run_beg(warp + 1);
@@ -1163,7 +1164,7 @@ qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int
                                 const int32_t *ids, uint16_t *cent, size_t hs, int Ce, int C, const float *w,
                                 float *cnorm, cudaStream_t st) {
     const size_t smem = static_cast<size_t>(N) * sizeof(uint16_t);
-    dim3 grid(kUpdSplit, H);
+    dim3 grid(update_splits(H, sm_count()), H);
 #define QVG_UPD(D_, T_)                                                                                     \
     do {                                                                                                    \
         static bool attr = false;                                                                           \
