@@ -354,7 +354,7 @@ qvg_status quantwm_query_stats(const void *q_hist_bf16, int32_t n, int32_t Hq,
  *   U        fp32 [H][d][rank]  column k = k-th eigenvector
  *   eigvals  fp32 [H][rank]     eigenvalues of M / count
  *   energy_frac fp32 [H]        sum of the top-rank eigenvalues / trace
- * rank must be QVG_PSAC_RANK; d <= 128.
+ * rank must be QVG_PSAC_RANK; d is 64 or 128.
  */
 qvg_status quantwm_psac_basis(const float *M, const int64_t *count, int32_t H,
                               int32_t d, int32_t rank, float *U,

@@ -323,7 +323,7 @@ qvg_status quantwm_psac_basis(const float *M, const int64_t *count, int32_t H, i
                               void *stream) {
     if (!M || !count || !U || !eigvals || !energy_frac || H < 1) return QVG_ERR_INVALID_ARG;
     if (rank != QVG_PSAC_RANK) return QVG_ERR_UNSUPPORTED;
-    if (d < rank || d > 128 || d % 2 != 0) return QVG_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return QVG_ERR_UNSUPPORTED;
     return launch_psac_basis(M, count, H, d, rank, U, eigvals, energy_frac,
                              static_cast<cudaStream_t>(stream));
 }

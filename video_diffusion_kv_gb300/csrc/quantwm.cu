@@ -92,30 +92,52 @@ qvg_status launch_query_stats(const uint16_t *q, int n, int Hq, int H, int d, in
 // sweeps.
 constexpr int JD = 128;  // maximum head_dim
 
+// Round-robin schedule: position 0 keeps element 0 and positions 1 .. D-1
+// rotate by one each step, so after `step` steps position i >= 1 holds
+// ((i - 1 - step) mod (D - 1)) + 1; pair pi of the step is (position pi,
+// position D - 1 - pi), ordered p < q.
+template <int D>
+__device__ __forceinline__ void jacobi_pair(int pi, int step, int &p, int &q) {
+    auto at = [&](int i) { return i == 0 ? 0 : ((i - 1 - step) % (D - 1) + (D - 1)) % (D - 1) + 1; };
+    p = at(pi);
+    q = at(D - 1 - pi);
+    if (p > q) {
+        const int t = p;
+        p = q;
+        q = t;
+    }
+}
+
+// Shared memory: A and V [D][D] fp32, the step's rotations and pairs.  The
+// row update runs with consecutive threads on consecutive entries of a row
+// (conflict-free); the column update with consecutive threads on different
+// pairs of the same row (a column walk would put a warp in one bank).
+template <int D>
 __global__ void __launch_bounds__(512) k_psac_jacobi(const float *__restrict__ Min,
-                                                    const int64_t *__restrict__ count, int d, int r,
+                                                    const int64_t *__restrict__ count, int r,
                                                     float *__restrict__ U, float *__restrict__ eig,
                                                     float *__restrict__ frac) {
+    constexpr int HALF = D / 2;
     extern __shared__ float js[];
-    float *A = js;                 // [d][d]
-    float *V = A + d * d;          // [d][d]
-    float *cs = V + d * d;         // [JD/2]
-    float *sn = cs + JD / 2;       // [JD/2]
-    int *P = reinterpret_cast<int *>(sn + JD / 2);  // [JD] tournament order
+    float *A = js;                 // [D][D]
+    float *V = A + D * D;          // [D][D]
+    float *cs = V + D * D;         // [D/2]
+    float *sn = cs + HALF;         // [D/2]
+    int *pp = reinterpret_cast<int *>(sn + HALF);  // [D/2]
+    int *qq = pp + HALF;                           // [D/2]
     __shared__ float red[16];
     __shared__ int done;
     __shared__ int top[QVG_PSAC_RANK];
     const int h = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
     const float inv = 1.0f / static_cast<float>(*count);
-    for (int i = tid; i < d * d; i += nt) {
-        A[i] = Min[static_cast<size_t>(h) * d * d + i] * inv;
-        V[i] = (i / d == i % d) ? 1.0f : 0.0f;
+    for (int i = tid; i < D * D; i += nt) {
+        A[i] = Min[static_cast<size_t>(h) * D * D + i] * inv;
+        V[i] = (i / D == i % D) ? 1.0f : 0.0f;
     }
-    for (int i = tid; i < d; i += nt) P[i] = i;
     __syncthreads();
     // ||A||_F
     float part = 0.f;
-    for (int i = tid; i < d * d; i += nt) part += A[i] * A[i];
+    for (int i = tid; i < D * D; i += nt) part += A[i] * A[i];
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if ((tid & 31) == 0) red[tid >> 5] = part;
     __syncthreads();
@@ -126,11 +148,10 @@ __global__ void __launch_bounds__(512) k_psac_jacobi(const float *__restrict__ M
     }
     __syncthreads();
     const float fro2 = red[15];
-    const int half = d / 2;
     for (int sweep = 0; sweep < 40; ++sweep) {
         float off = 0.f;
-        for (int i = tid; i < d * d; i += nt)
-            if (i / d != i % d) off += A[i] * A[i];
+        for (int i = tid; i < D * D; i += nt)
+            if (i / D != i % D) off += A[i] * A[i];
         for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
         __syncthreads();
         if ((tid & 31) == 0) red[tid >> 5] = off;
@@ -142,52 +163,45 @@ __global__ void __launch_bounds__(512) k_psac_jacobi(const float *__restrict__ M
         }
         __syncthreads();
         if (done) break;
-        for (int step = 0; step < d - 1; ++step) {
-            if (tid < half) {
-                int p = P[tid], q = P[d - 1 - tid];
-                if (p > q) { const int t = p; p = q; q = t; }
-                const float apq = A[p * d + q];
+        for (int step = 0; step < D - 1; ++step) {
+            if (tid < HALF) {
+                int p, q;
+                jacobi_pair<D>(tid, step, p, q);
+                const float apq = A[p * D + q];
                 float c = 1.f, s = 0.f;
                 if (apq != 0.f) {
-                    const float theta = (A[q * d + q] - A[p * d + p]) / (2.f * apq);
+                    const float theta = (A[q * D + q] - A[p * D + p]) / (2.f * apq);
                     const float t = (theta >= 0.f ? 1.f : -1.f) / (fabsf(theta) + sqrtf(1.f + theta * theta));
                     c = 1.f / sqrtf(1.f + t * t);
                     s = t * c;
                 }
                 cs[tid] = c;
                 sn[tid] = s;
+                pp[tid] = p;
+                qq[tid] = q;
             }
             __syncthreads();
             // rows: A <- J^T A
-            for (int i = tid; i < half * d; i += nt) {
-                const int pi = i / d, k = i % d;
-                int p = P[pi], q = P[d - 1 - pi];
-                if (p > q) { const int t = p; p = q; q = t; }
+            for (int i = tid; i < HALF * D; i += nt) {
+                const int pi = i / D, k = i % D;
+                const int p = pp[pi], q = qq[pi];
                 const float c = cs[pi], s = sn[pi];
-                const float apk = A[p * d + k], aqk = A[q * d + k];
-                A[p * d + k] = c * apk - s * aqk;
-                A[q * d + k] = s * apk + c * aqk;
+                const float apk = A[p * D + k], aqk = A[q * D + k];
+                A[p * D + k] = c * apk - s * aqk;
+                A[q * D + k] = s * apk + c * aqk;
             }
             __syncthreads();
             // columns: A <- A J, V <- V J
-            for (int i = tid; i < half * d; i += nt) {
-                const int pi = i / d, k = i % d;
-                int p = P[pi], q = P[d - 1 - pi];
-                if (p > q) { const int t = p; p = q; q = t; }
+            for (int i = tid; i < HALF * D; i += nt) {
+                const int k = i / HALF, pi = i % HALF;
+                const int p = pp[pi], q = qq[pi];
                 const float c = cs[pi], s = sn[pi];
-                const float akp = A[k * d + p], akq = A[k * d + q];
-                A[k * d + p] = c * akp - s * akq;
-                A[k * d + q] = s * akp + c * akq;
-                const float vkp = V[k * d + p], vkq = V[k * d + q];
-                V[k * d + p] = c * vkp - s * vkq;
-                V[k * d + q] = s * vkp + c * vkq;
-            }
-            __syncthreads();
-            // next round of the tournament: keep P[0], rotate P[1..d-1]
-            if (tid == 0) {
-                const int last = P[d - 1];
-                for (int i = d - 1; i > 1; --i) P[i] = P[i - 1];
-                P[1] = last;
+                const float akp = A[k * D + p], akq = A[k * D + q];
+                A[k * D + p] = c * akp - s * akq;
+                A[k * D + q] = s * akp + c * akq;
+                const float vkp = V[k * D + p], vkq = V[k * D + q];
+                V[k * D + p] = c * vkp - s * vkq;
+                V[k * D + q] = s * vkp + c * vkq;
             }
             __syncthreads();
         }
@@ -195,18 +209,18 @@ __global__ void __launch_bounds__(512) k_psac_jacobi(const float *__restrict__ M
     // top-r eigenpairs by descending eigenvalue (lowest index on ties)
     if (tid == 0) {
         float tr = 0.f, sum = 0.f;
-        for (int i = 0; i < d; ++i) tr += A[i * d + i];
+        for (int i = 0; i < D; ++i) tr += A[i * D + i];
         for (int k = 0; k < r; ++k) {
             int b = -1;
-            for (int i = 0; i < d; ++i) {
+            for (int i = 0; i < D; ++i) {
                 bool used = false;
                 for (int m = 0; m < k; ++m) used |= (top[m] == i);
                 if (used) continue;
-                if (b < 0 || A[i * d + i] > A[b * d + b]) b = i;
+                if (b < 0 || A[i * D + i] > A[b * D + b]) b = i;
             }
             top[k] = b;
-            eig[h * r + k] = A[b * d + b];
-            sum += A[b * d + b];
+            eig[h * r + k] = A[b * D + b];
+            sum += A[b * D + b];
         }
         frac[h] = tr > 0.f ? sum / tr : 0.f;
     }
@@ -214,20 +228,22 @@ __global__ void __launch_bounds__(512) k_psac_jacobi(const float *__restrict__ M
     if (tid < r) {
         const int col = top[tid];
         int big = 0;
-        for (int k = 1; k < d; ++k)
-            if (fabsf(V[k * d + col]) > fabsf(V[big * d + col])) big = k;
-        const float sg = V[big * d + col] < 0.f ? -1.f : 1.f;
-        for (int k = 0; k < d; ++k) U[(static_cast<size_t>(h) * d + k) * r + tid] = sg * V[k * d + col];
+        for (int k = 1; k < D; ++k)
+            if (fabsf(V[k * D + col]) > fabsf(V[big * D + col])) big = k;
+        const float sg = V[big * D + col] < 0.f ? -1.f : 1.f;
+        for (int k = 0; k < D; ++k) U[(static_cast<size_t>(h) * D + k) * r + tid] = sg * V[k * D + col];
     }
 }
 
 qvg_status launch_psac_basis(const float *M, const int64_t *count, int H, int d, int rank, float *U,
                              float *eig, float *frac, cudaStream_t st) {
-    const size_t smem = (2 * static_cast<size_t>(d) * d + JD) * sizeof(float) + JD * sizeof(int);
+    const size_t smem = (2 * static_cast<size_t>(d) * d + d) * sizeof(float) + d * sizeof(int);
     static bool attr = false;
     if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(k_psac_jacobi, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>((2 * JD * JD + JD) * sizeof(float) + JD * sizeof(int)));
+        const int most = static_cast<int>((2 * JD * JD + JD) * sizeof(float) + JD * sizeof(int));
+        cudaError_t e = cudaFuncSetAttribute(k_psac_jacobi<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_psac_jacobi<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             note_cuda_error(e);
@@ -235,7 +251,12 @@ qvg_status launch_psac_basis(const float *M, const int64_t *count, int H, int d,
         }
         attr = true;
     }
-    k_psac_jacobi<<<H, 512, smem, st>>>(M, count, d, rank, U, eig, frac);
+    if (d == 128)
+        k_psac_jacobi<128><<<H, 512, smem, st>>>(M, count, rank, U, eig, frac);
+    else if (d == 64)
+        k_psac_jacobi<64><<<H, 512, smem, st>>>(M, count, rank, U, eig, frac);
+    else
+        return QVG_ERR_UNSUPPORTED;
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }
