@@ -916,7 +916,7 @@ __global__ void __launch_bounds__(256) k_residual_quant(
         float x[32], c[32];
         load32<TIn>(xr + cb * 32, x);
         if (C > 0) load32<uint16_t>(cr + cb * 32, c);
-        float Sb[4], ob[4];
+        float Sb[4], ib[4], ob[4];
         int ocb[4];
 #pragma unroll
         for (int b8 = 0; b8 < 4; ++b8) {
@@ -932,6 +932,7 @@ __global__ void __launch_bounds__(256) k_residual_quant(
                         ocb[b8] = oc8[4 * q + b8];
                     }
                 }
+            ib[b8] = Sb[b8] > 0.0f ? __fdiv_rn(1.0f, Sb[b8]) : 0.0f;
         }
         uint32_t pw[CB / 4];
 #pragma unroll
@@ -942,7 +943,7 @@ __global__ void __launch_bounds__(256) k_residual_quant(
             const float Sp = Sb[e >> 3];
             const float r = C > 0 ? __fsub_rn(x[e], c[e]) : x[e];
             const bool is_out = OUTL && cb * 32 + e == ocb[e >> 3];
-            const int q = is_out ? 0 : quant_code(r, Sp, BITS);
+            const int q = is_out ? 0 : quant_code_rcp(r, Sp, ib[e >> 3], BITS);
             pw[(e * BITS) / 32] |= static_cast<uint32_t>(q + (1 << (BITS - 1))) << ((e * BITS) % 32);
             const float rh = is_out ? ob[e >> 3] : __fmul_rn(Sp, static_cast<float>(q));
             const float deq = C > 0 ? __fadd_rn(rh, c[e]) : rh;
