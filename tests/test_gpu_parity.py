@@ -439,6 +439,22 @@ def test_attention_with_outlier_split(name):
     _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
 
 
+def test_outlier_split_zero_residual():
+    """C = N: every token is its own centroid, so every residual is zero and
+    every group ties at the top: nothing is split off (index 0xFF, value 0),
+    the scales are 0, and the rebuild is the input."""
+    w = W["tiny"]
+    p = qvg.Params(C=16, L=1, bits=2, group=32, iters=3, seed=35, flags=qvg.QVG_OUTLIER)
+    x = synth.chunk_kv(w, 35, 0, synth.KIND_V)[:16]
+    c = _new_cache(w, p, 1, N=16)
+    qvg.compress_chunk(p, to_dev(x), c)
+    hc = host_cache(c)
+    sl = chunk_slice(hc, 0)
+    assert np.all(hc["outl_idx"][:, :, sl] == 0xFF) and not hc["outl_val"][:, :, sl].any()
+    assert not hc["scales"][:, :, sl].any()
+    np.testing.assert_array_equal(qvg.decompress(p, c, 0, 16).cpu().numpy(), x)
+
+
 def test_outlier_split_longcat():
     """LongCat-like chunks (16 heads, d=128, C=256, INT2 G=64): the split
     lowers the GPU's reconstruction error of V (x300 outlier channels) and
