@@ -43,23 +43,17 @@ __device__ __forceinline__ uint16_t group_scale_f16(float amax, int bits, int mo
     return f32_to_f16(S);
 }
 
-__device__ __forceinline__ int quant_code(float r, float Sp, int bits) {
-    if (!(Sp > 0.0f)) return 0;
-    const float qmax = static_cast<float>((1 << (bits - 1)) - 1);
-    float t = rintf(__fdiv_rn(r, Sp));
-    t = fminf(fmaxf(t, -qmax - 1.0f), qmax);
-    return static_cast<int>(t);
-}
-
-// quant_code without a division per element: inv = fl(1 / Sp) (one division
-// per group), y = fl(r inv).  With x = r / Sp exactly, |y - x| <= |x| 2^-23
+// The code of r at the stored scale Sp: clamp(rint(fl(r / Sp)), -2^{b-1},
+// 2^{b-1} - 1), 0 when Sp is 0 -- without a division per element: inv =
+// fl(1 / Sp) (one division per group), y = fl(r inv).  With x = r / Sp
+// exactly, |y - x| <= |x| 2^-23
 // (two roundings of at most 2^-24 each) and |fl(x) - x| <= |x| 2^-24, so y
 // and the IEEE quotient fl(x) round to the same integer unless a
 // half-integer lies between them or on one of them, which needs y within
 // |y| 2^-21 of a half-integer (a margin of more than twice the bound); those
 // elements take the division.  y - rint(y) is exact (Sterbenz), and beyond
 // 2^23 y is an integer and the clamp decides, so the code is bit for bit
-// that of quant_code.
+// the one the division gives.
 __device__ __forceinline__ int quant_code_rcp(float r, float Sp, float inv, int bits) {
     if (!(Sp > 0.0f)) return 0;
     const float qmax = static_cast<float>((1 << (bits - 1)) - 1);
