@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's sources so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "9b1b9b82b1ac493e58d4d682630f09480b91265f31467fd1b3d181b743574ead": 80390400 + 3454464,
+    "1a413d5bc91ace1c56025a80f18a29d49f45ba99406da65c3373a253a237261d": 80424448 + 3613184,
 }
 
 
