@@ -439,6 +439,27 @@ def test_attention_with_outlier_split(name):
     _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+def test_attention_two_stage_longcat(bits):
+    """LongCat-like caches of two stages (16 heads, d=128, G=64): the
+    multi-stage producer adds each stage into the fp16 tile; attention of
+    4680 queries (64 sampled rows per head) and 16 queries (split cache)
+    against the fp64 oracle on the rebuild of the same bytes."""
+    w, p0, _ = CASES["longcat"]
+    p = qvg.Params(**{**p0.__dict__, "L": 2, "bits": bits})
+    chunks = [(synth.chunk_kv(w, 36, k, synth.KIND_K), synth.chunk_kv(w, 36, k, synth.KIND_V)) for k in range(2)]
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    q = synth.queries(w, 36, 2)
+    out, _, _ = qvg.attention(p, to_dev(q), kc, vc)
+    rows = np.random.default_rng(5).choice(q.shape[0], 64, replace=False)
+    ref, _, _, _, _ = _oracle_attention_on(kc, vc, p, q, rows)
+    _assert_attention(out.cpu().numpy()[rows].astype(np.float64), ref, w.Hq)
+    q16 = np.ascontiguousarray(q[:16])
+    out, _, _ = qvg.attention(p, to_dev(q16), kc, vc)
+    ref, _, _, _, _ = _oracle_attention_on(kc, vc, p, q16)
+    _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
+
+
 def test_outlier_split_zero_residual():
     """C = N: every token is its own centroid, so every residual is zero and
     every group ties at the top: nothing is split off (index 0xFF, value 0),
