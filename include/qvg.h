@@ -9,6 +9,8 @@
  *          KV-Cache Quantization (papernotes.org notes, ICML 2026).
  *   [P1]   The 2-bit quantisation trap in video generation (cloud.baidu.com).
  *   [QWM]  QuantWM write-up (loncent.com): QSAC and PSAC.
+ *   [P2]   Temporally stable 2-bit KV-cache compression for video world models, in practice (hmyw.cn): section 3.3 (temporal anchors), section 3.4
+ *          (outlier separation).
  *
  * Conventions for every call:
  *   - Buffers are device pointers owned by the caller unless stated; the
@@ -209,10 +211,15 @@ qvg_status qvg_workspace_size(const qvg_params *p, int32_t op, int32_t n,
  *   k-means over the chunk's tokens: seeded init, p->iters Lloyd iterations,
  *   one final assignment (distance sum_j w_j (x_j - c_j)^2, w = qsac_w with
  *   QVG_QSAC, else 1; ties to the lowest cluster);
- *   residual r = X_l - C_id; per-group quantisation of r with fp16 scales;
+ *   residual r = X_l - C_id; per-group quantisation of r with fp16 scales
+ *   (with QVG_OUTLIER, first splitting off each group's value above its
+ *   P99 into the fp16 side list, [P2] section 3.4);
  *   X_{l+1} = X_l - (S q + C_id).
  * With QVG_PSAC, the remaining key error E = X_{L+1} is projected on the
  * rank-8 basis and stored as INT8 per token with one fp16 scale.
+ * With p->anchor_every = k > 0, chunk n_chunks is an anchor when
+ * n_chunks % k == 0 ([P2] section 3.3): its bf16 K or V is copied into the
+ * anchor arena as given, and nothing else is computed for it.
  *   x_bf16     bf16 [N][H][d] device, the chunk's K or V (token-major).
  *   N          1 .. 65535 tokens.
  *   qsac_w     fp32 [H][d] device per-channel weights (required with QVG_QSAC,
@@ -225,7 +232,8 @@ qvg_status qvg_workspace_size(const qvg_params *p, int32_t op, int32_t n,
  *              caller has written all L stages' starting centroids into the
  *              new chunk's centroid slot (index n_chunks).
  *   workspace  device scratch of at least qvg_workspace_size(QVG_OP_COMPRESS).
- * Returns QVG_ERR_CAPACITY when the chunk does not fit (nothing written).
+ * Returns QVG_ERR_CAPACITY when the chunk does not fit, in the slots or (an
+ * anchor chunk) in its anchor rows; nothing is written then.
  */
 qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16,
                               int32_t N, const float *qsac_w,

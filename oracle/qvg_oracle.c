@@ -30,6 +30,7 @@
  *          clustering) and PSAC (top-8 eigenvectors of the history-query
  *          second moment, projected key error, quantised, added back to the
  *          logits).
+ *   [P2]   Temporally stable 2-bit KV-cache compression for video world models, in practice (hmyw.cn), section 3.4 (outlier separation).
  *
  * Readings of points the pages leave open are stated where they are used.
  *

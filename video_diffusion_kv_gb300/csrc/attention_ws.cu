@@ -47,11 +47,12 @@ struct AttnWsArgs {
     // n_ctiles = n_slots / QVG_TILE cache tiles; raw row j is slot n_slots + j
     const uint16_t *kraw, *vraw;
     int n_raw, n_ctiles;
-    // outlier split (blog "project X", section 3.4): per stage and group, the
-    // fp16 value split off and its channel in the group (0xFF: none), or NULL
+    // outlier split ("Temporally stable 2-bit KV-cache compression for video
+    // world models, in practice", section 3.4): per stage and group, the fp16
+    // value split off and its channel in the group (0xFF: none), or NULL
     const uint16_t *koutv, *voutv;
     const uint8_t *kouti, *vouti;
-    // temporal anchors (blog "project X", section 3.3): anchor chunks are
+    // temporal anchors (the same page, section 3.3): anchor chunks are
     // read as bf16 rows of these arenas; chunk_anchor[c] = first row, or -1
     const uint16_t *kanch, *vanch;
     const int32_t *chunk_anchor;

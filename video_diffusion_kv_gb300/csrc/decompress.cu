@@ -3,8 +3,9 @@
 // Quant VideoGen notes, "overall framework": X_hat = S_X * X_INT + C_i;
 // "Progressive Residual Quantization": X_hat = X_hat_1 + Delta_hat_1 + ...
 // (stages summed in fp32 in stage order).  QuantWM write-up, PSAC: the
-// stored projection of the key error is added back as P_hat U^T.  Blog
-// "project X", section 3.4 (outlier separation): a value split off from its
+// stored projection of the key error is added back as P_hat U^T.
+// "Temporally stable 2-bit KV-cache compression for video world models, in practice"
+// (hmyw.cn), section 3.4 (outlier separation): a value split off from its
 // group is rebuilt from its fp16 copy; section 3.3 (temporal anchors): an
 // anchor chunk's values are its stored bf16 K/V.
 #include "common.cuh"
