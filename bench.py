@@ -36,19 +36,28 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one k_attention_ws launch of the bench
 # workload, from an ncu capture of `dram__bytes_read.sum,dram__bytes_write.sum`
 # (profiles/k_attention_ws_longcat_8chunks.md), keyed by the SHA-256 of the
-# kernel's sources so that a changed kernel reports null until re-measured.
+# kernel's code (comments stripped) so that a changed kernel reports null
+# until re-measured.
 ATTN_SOURCES = ("attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "1a413d5bc91ace1c56025a80f18a29d49f45ba99406da65c3373a253a237261d": 80424448 + 3613184,
+    "15f336d22d257c991a4c603b24c390ec8a648e30d69880c44102f3f724263a03": 80424448 + 3613184,
 }
 
 
 def _attn_source_hash():
+    """SHA-256 of the attention kernel's sources with comments and blank
+    lines removed, so that only a change of code invalidates the recorded
+    traffic."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ATTN_SOURCES:
-        with open(os.path.join(ROOT, "video_diffusion_kv_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "video_diffusion_kv_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        code = "\n".join(line.rstrip() for line in src.split("\n") if line.strip())
+        h.update(code.encode())
     return h.hexdigest()
 
 
