@@ -262,7 +262,8 @@ def launches_per_compress(p):
 
 def kernel_extras(qvg, p, w, kc, vc, q, k_raw, flush, dev, last, slots_per_chunk, reps=5):
     """Separately timed kernels on the same cache (outside the step): the
-    decompress of the newest chunk (fp32 and bf16 output) and a decode-like
+    decompress of the newest chunk (fp32 and bf16 output) and of the whole
+    cache (fp32), a decode-like
     attention point (16 queries over the whole cache), each with its
     algorithmic bytes and the fraction of the measured HBM peak; and the
     attention of one AR step (older chunks compressed, the newest chunk raw),
@@ -297,6 +298,18 @@ def kernel_extras(qvg, p, w, kc, vc, q, k_raw, flush, dev, last, slots_per_chunk
         res[name] = {"ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms / 1e3) / 1e9,
                      "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm,
                      "what": "newest chunk of the K cache (%d tokens x %d heads)" % (w.N, w.H)}
+    # the whole cache (every chunk), where the launch's fixed costs are small
+    # against its bytes
+    # (every slot: the tile padding of each chunk is written as zeros)
+    nslots = kc.n_tokens
+    dall = torch.empty((nslots, w.H, w.d), dtype=torch.float32, device=dev)
+    ms = timed(lambda: qvg.decompress(p, kc, 0, nslots, out_dtype=qvg.QVG_OUT_F32, out=dall))
+    nbytes = w.tokens * w.H * row_bytes + w.n_chunks * cent_bytes + nslots * w.H * w.d * 4
+    res["decompress_f32_cache"] = {"ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                                   "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm,
+                                   "what": "whole K cache (%d tokens in %d slots x %d heads)"
+                                           % (w.tokens, nslots, w.H)}
+    del dall
     q16 = q[:16].contiguous()
     out16 = torch.empty((16, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
     ms = timed(lambda: qvg.attention(p, q16, kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out16))
