@@ -214,6 +214,27 @@ def test_decompress_exact_and_bf16(name):
         np.testing.assert_array_equal(half[sl], synth.bf16_values(ref))
 
 
+@pytest.mark.parametrize("name", ["tiny", "pro_outlier_L2", "longcat"])
+def test_decompress_ragged_range(name):
+    """A slot range that starts off a warp boundary and ends in a ragged
+    tail (not a multiple of 32) gives the same values as the whole-cache
+    rebuild, in fp32 and bf16, and writes nothing past its last row."""
+    import torch
+    w, p, n_chunks = CASES[name]
+    kc = _new_cache(w, p, n_chunks)
+    for k in range(n_chunks):
+        qvg.compress_chunk(p, to_dev(synth.chunk_kv(w, 15, k, synth.KIND_K)), kc)
+    full = qvg.decompress(p, kc, 0, kc.n_tokens)
+    for tok0, ntok in ((37, kc.n_tokens - 37 - 19), (5, 1), (kc.n_tokens - 45, 45)):
+        for dt, tdt in ((qvg.QVG_OUT_F32, torch.float32), (qvg.QVG_OUT_BF16, torch.bfloat16)):
+            guard = 40
+            big = torch.full((ntok + guard, w.H, w.d), 7.0, dtype=tdt, device="cuda")
+            qvg.decompress(p, kc, tok0, ntok, out_dtype=dt, out=big[:ntok])
+            want = full[tok0:tok0 + ntok].to(tdt)
+            assert torch.equal(big[:ntok], want), (tok0, ntok, dt)
+            assert bool((big[ntok:] == 7.0).all()), (tok0, ntok, dt)
+
+
 def _cache_with_chunks(w, p, chunks_kv, seed=0):
     n = len(chunks_kv)
     cap = sum(-(-c[0].shape[0] // 128) * 128 for c in chunks_kv)

@@ -31,13 +31,14 @@ struct CacheView {
 // Thread = token slot: a warp rebuilds 32 consecutive slots of one head
 // (their codes, scales and ids are contiguous), each thread its own row in
 // blocks of 32 channels (the block's codes, scales and centroid piece are
-// loaded before its arithmetic).  Per element, in stage order:
+// loaded before its arithmetic); the block's 32 x 32 results are stored
+// row by row through shared memory.  Per element, in stage order:
 // acc += fl(fl(S q) + c), then the PSAC term as an fp32 FMA chain over the
 // rank -- the same operations, in the same order, as any other rebuild.
 // OUTL: at the channel a stage split off from its group (code 0), the
 // stage's value is fl(o + c), o the stored fp16 outlier.
 template <int D, int BITS, bool PSAC, bool OUTL>
-__global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, int group,
+__global__ void __launch_bounds__(256, (PSAC || OUTL) ? 2 : 3) k_decompress(CacheView cv, int L, int C, int group,
                                                    int tok0, int ntok, float *out32,
                                                    uint16_t *out16) {
     constexpr int NB = D * BITS / 8, CB = 32 * BITS / 8;  // code bytes per row / per 32-channel block
@@ -46,11 +47,14 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
     const int nblk = ceil_div(ntok, 32);
     const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (wid >= static_cast<long long>(H) * nblk) return;
-    const int h = static_cast<int>(wid / nblk), t = static_cast<int>(wid % nblk) * 32 + lane;
-    if (t >= ntok) return;
-    const int slot = tok0 + t;
+    // t0 < ntok (nblk = ceil(ntok / 32)); a lane past the end decodes nothing
+    // and takes part only in the warp's staged stores
+    const int h = static_cast<int>(wid / nblk), t0 = static_cast<int>(wid % nblk) * 32, t = t0 + lane;
+    const bool live = t < ntok;
+    const int nrow = min(32, ntok - t0);
+    const int slot = tok0 + (live ? t : t0);
     const int chunk = cv.tile_chunk[slot / QVG_TILE];
-    const bool valid = slot >= cv.chunk_start[chunk] && slot < cv.chunk_start[chunk] + cv.chunk_len[chunk];
+    const bool valid = live && slot >= cv.chunk_start[chunk] && slot < cv.chunk_start[chunk] + cv.chunk_len[chunk];
     const int arow = cv.chunk_anchor ? cv.chunk_anchor[chunk] : -1;  // an anchor chunk's first row, or -1
     const uint16_t *arow_p = arow >= 0 && valid ? cv.anchor + (static_cast<size_t>(arow + slot - cv.chunk_start[chunk]) * H + h) * D
                                                 : nullptr;
@@ -63,7 +67,12 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
         for (int k = 0; k < QVG_PSAC_RANK; ++k) pk[k] = pSp * static_cast<float>(cv.psac_p[prow * QVG_PSAC_RANK + k]);
         U = cv.psac_basis + (static_cast<size_t>(chunk) * H + h) * D * QVG_PSAC_RANK;
     }
-    const size_t orow = (static_cast<size_t>(t) * H + h) * D;
+    // the warp's 32 rows x 32 channels pass through shared memory (one row
+    // per lane in, one row per store out), so that each store instruction
+    // writes whole 128-byte lines instead of 16 bytes of 32 lines
+    __shared__ float stage[8][32][33];
+    float (*st)[33] = stage[threadIdx.x >> 5];
+    uint32_t (*st16)[17] = reinterpret_cast<uint32_t (*)[17]>(&stage[threadIdx.x >> 5][0][0]);
 #pragma unroll 1
     for (int cb = 0; cb < D / 32; ++cb) {
         float acc[32];
@@ -145,21 +154,23 @@ __global__ void __launch_bounds__(256) k_decompress(CacheView cv, int L, int C, 
             }
         }
         if (out32) {
-            float4 *o = reinterpret_cast<float4 *>(out32 + orow + cb * 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+            for (int e = 0; e < 32; ++e) st[lane][e] = acc[e];
+            __syncwarp();
+            float *o = out32 + (static_cast<size_t>(t0) * H + h) * D + cb * 32 + lane;
+            for (int r = 0; r < nrow; ++r) o[static_cast<size_t>(r) * H * D] = st[r][lane];
         } else {
-            uint4 *o = reinterpret_cast<uint4 *>(out16 + orow + cb * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    w4[k] = static_cast<uint32_t>(f32_to_bf16(acc[8 * i + 2 * k])) |
-                            (static_cast<uint32_t>(f32_to_bf16(acc[8 * i + 2 * k + 1])) << 16);
-                o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+            for (int k = 0; k < 16; ++k)
+                st16[lane][k] = static_cast<uint32_t>(f32_to_bf16(acc[2 * k])) |
+                                (static_cast<uint32_t>(f32_to_bf16(acc[2 * k + 1])) << 16);
+            __syncwarp();
+            // two rows per store: lanes 0-15 the even row, 16-31 the odd one
+            uint32_t *o = reinterpret_cast<uint32_t *>(out16 + (static_cast<size_t>(t0) * H + h) * D + cb * 32) +
+                          (lane & 15);
+            for (int r = lane >> 4; r < nrow; r += 2) o[static_cast<size_t>(r) * H * D / 2] = st16[r][lane & 15];
         }
+        __syncwarp();  // the stage is read before the next block overwrites it
     }
 }
 
