@@ -220,12 +220,14 @@ qvg_status qvg_workspace_size(const qvg_params *p, int32_t op, int32_t n,
  * With p->anchor_every = k > 0, chunk n_chunks is an anchor when
  * n_chunks % k == 0 ([P2] section 3.3): its bf16 K or V is copied into the
  * anchor arena as given, and nothing else is computed for it.
- *   x_bf16     bf16 [N][H][d] device, the chunk's K or V (token-major).
+ *   x_bf16     bf16 [N][H][d] device, the chunk's K or V (token-major),
+ *              16-byte aligned.
  *   N          1 .. 65535 tokens.
  *   qsac_w     fp32 [H][d] device per-channel weights (required with QVG_QSAC,
  *              else ignored); positive and finite.
- *   psac_basis fp32 [H][d][8] device (required with QVG_PSAC, else ignored);
- *              copied into the cache's per-chunk basis slot.
+ *   psac_basis fp32 [H][d][8] device, 16-byte aligned (required with
+ *              QVG_PSAC, else ignored); copied into the cache's per-chunk
+ *              basis slot.
  *   cache      appended in place: the chunk occupies slots
  *              [n_tokens, n_tokens + N); n_chunks += 1 and n_tokens advances to
  *              the next multiple of QVG_TILE.  With QVG_GIVEN_CENTROIDS the
@@ -275,7 +277,13 @@ qvg_status qvg_compress_chunk_noalloc(const qvg_params *p, const void *x_bf16,
  * framework": X_hat = S_X * X_INT + C_i, summed over stages per
  * "Progressive Residual Quantization"; with PSAC data present, plus the
  * correction P_hat U^T of [QWM] PSAC).  Stages are summed in fp32 in stage
- * order.  out: [ntok][H][d] fp32 or bf16 (out_dtype).  Padding slots give 0.
+ * order.  With QVG_OUTLIER, a value split off from its group is rebuilt as
+ * its fp16 copy plus the centroid ([P2] section 3.4); an anchor chunk's
+ * slots give its stored bf16 K/V ([P2] section 3.3).
+ *   out      [ntok][H][d] fp32 or bf16 (out_dtype), 4-byte aligned; the
+ *            caller's device buffer.  Padding slots give 0.
+ * Errors: QVG_ERR_INVALID_ARG for tok0 < 0, ntok < 0, tok0 + ntok past
+ * n_tokens or a misaligned out; ntok = 0 does nothing.
  */
 qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache,
                           int32_t tok0, int32_t ntok, void *out,
@@ -288,9 +296,10 @@ qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache,
  * co-design": dequantisation fused with attention):
  *   O = softmax(scale * Q K_hat^T) V_hat, K_hat including the PSAC
  *   correction when the K cache holds PSAC data.
- *   q_bf16   bf16 [Nq][Hq][d]; query head hq reads KV head hq / (Hq / H).
+ *   q_bf16   bf16 [Nq][Hq][d], 16-byte aligned; query head hq reads KV head
+ *            hq / (Hq / H).
  *   scale    softmax scale; <= 0 selects 1/sqrt(d).
- *   out      [Nq][Hq][d] fp32 or bf16.
+ *   out      [Nq][Hq][d] fp32 or bf16, 16-byte aligned.
  *   lse      fp32 [Hq][Nq] natural-log log-sum-exp of the scaled logits, or NULL.
  *   top1     int32 [Hq][Nq] slot of the largest logit (lowest on ties), or NULL.
  *   workspace, ws_bytes  optional device scratch (256-byte aligned).  When
@@ -303,7 +312,8 @@ qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache,
  *            workspace, or a smaller one, the call runs unsplit; the results
  *            agree within fp32 rounding of the merge.
  * No mask: every cached token precedes the queries.  k and v must hold the
- * same chunks.  Errors: QVG_ERR_WORKSPACE for a misaligned workspace.
+ * same chunks.  Errors: QVG_ERR_INVALID_ARG for a misaligned q_bf16 or out
+ * (Nq > 0), QVG_ERR_WORKSPACE for a misaligned workspace.
  */
 qvg_status qvg_attention(const qvg_params *p, const void *q_bf16, int32_t Nq,
                          int32_t Hq, const qvg_cache *k, const qvg_cache *v,

@@ -132,6 +132,13 @@ def test_compress_rejects_on_host(lib):
     assert lib.qvg_compress_chunk(ct.byref(pq), x, 100, None, None, ct.byref(c), ws, 1 << 30, None) == qvg.QVG_ERR_INVALID_ARG
     bad = _fake_cache(cap=500)
     assert lib.qvg_compress_chunk(ct.byref(p), x, 100, None, None, ct.byref(bad), ws, 1 << 30, None) == qvg.QVG_ERR_INVALID_ARG
+    # the chunk and the PSAC basis are read in 16-byte vectors
+    assert lib.qvg_compress_chunk(ct.byref(p), ct.c_void_p(0x2008), 100, None, None, ct.byref(c), ws, 1 << 30,
+                                  None) == qvg.QVG_ERR_INVALID_ARG
+    pp = _params(C=16, group=32, flags=qvg.QVG_PSAC)
+    basis = ct.cast(ct.c_void_p(0x5004), ct.POINTER(ct.c_float))
+    assert lib.qvg_compress_chunk(ct.byref(pp), x, 100, None, basis, ct.byref(c), ws, 1 << 30,
+                                  None) == qvg.QVG_ERR_INVALID_ARG
     # the counters are untouched by a rejected call
     assert c.n_chunks == 0 and c.n_tokens == 0
 
@@ -148,6 +155,14 @@ def test_attention_and_decompress_reject_on_host(lib):
     assert lib.qvg_attention(ct.byref(p), q, 4, 2, ct.byref(empty), ct.byref(empty), 0.0, o, 0, None, None, None, 0, None) == qvg.QVG_ERR_INVALID_ARG
     assert lib.qvg_decompress(ct.byref(p), ct.byref(k), 0, 200, o, 0, None) == qvg.QVG_ERR_INVALID_ARG
     assert lib.qvg_decompress(ct.byref(p), ct.byref(k), -1, 10, o, 0, None) == qvg.QVG_ERR_INVALID_ARG
+    # tok0 + ntok past the end even where int32 addition would wrap
+    assert lib.qvg_decompress(ct.byref(p), ct.byref(k), 2**31 - 10, 2**31 - 10, o, 0, None) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_decompress(ct.byref(p), ct.byref(k), 0, 64, ct.c_void_p(0x4002), 0, None) == qvg.QVG_ERR_INVALID_ARG
+    # queries and outputs move in 16-byte vectors
+    kk = _fake_cache(n_chunks=1, n_tokens=128)
+    for qq, oo in ((ct.c_void_p(0x3008), o), (q, ct.c_void_p(0x4004))):
+        assert lib.qvg_attention(ct.byref(p), qq, 4, 2, ct.byref(kk), ct.byref(kk), 0.0, oo, 0, None, None, None, 0,
+                                 None) == qvg.QVG_ERR_INVALID_ARG
 
 
 def test_outlier_split_arguments(lib):

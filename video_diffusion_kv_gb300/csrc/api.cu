@@ -170,9 +170,11 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
     if ((p->flags & QVG_QSAC) && !qsac_w) return QVG_ERR_INVALID_ARG;
     if ((p->flags & QVG_PSAC) && !psac_basis) return QVG_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(x_bf16) % 16 != 0) return QVG_ERR_INVALID_ARG;
+    if ((p->flags & QVG_PSAC) && reinterpret_cast<uintptr_t>(psac_basis) % 16 != 0) return QVG_ERR_INVALID_ARG;
     const int H = cache->H, d = cache->d;
     const int Naligned = ceil_div(N, QVG_TILE) * QVG_TILE;
-    if (cache->n_chunks >= cache->max_chunks || cache->n_tokens + Naligned > cache->capacity_tokens)
+    if (cache->n_chunks >= cache->max_chunks ||
+        static_cast<int64_t>(cache->n_tokens) + Naligned > cache->capacity_tokens)
         return QVG_ERR_CAPACITY;
     const CompressWs need = carve_compress(p, N, H, d, nullptr);
     if (need.bytes > 0 && (!workspace || ws_bytes < need.bytes)) return QVG_ERR_WORKSPACE;
@@ -260,7 +262,8 @@ qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache, int32_t t
     if (s != QVG_OK) return s;
     if ((s = check_cache(p, cache)) != QVG_OK) return s;
     if (out_dtype != QVG_OUT_F32 && out_dtype != QVG_OUT_BF16) return QVG_ERR_INVALID_ARG;
-    if (tok0 < 0 || ntok < 0 || tok0 + ntok > cache->n_tokens) return QVG_ERR_INVALID_ARG;
+    if (tok0 < 0 || ntok < 0 || static_cast<int64_t>(tok0) + ntok > cache->n_tokens) return QVG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(out) % 4 != 0) return QVG_ERR_INVALID_ARG;  // stored in 32-bit words
     if (ntok == 0) return QVG_OK;
     return launch_decompress(p, cache, tok0, ntok, out, out_dtype, static_cast<cudaStream_t>(stream));
 }
@@ -273,6 +276,9 @@ qvg_status qvg_attention_ar(const qvg_params *p, const void *q_bf16, int32_t Nq,
     if (!k || !v || (!q_bf16 && Nq > 0) || (!out && Nq > 0)) return QVG_ERR_INVALID_ARG;
     if (n_cur < 0 || (n_cur > 0 && (!k_cur_bf16 || !v_cur_bf16))) return QVG_ERR_INVALID_ARG;
     if (n_cur > 0 && ((reinterpret_cast<uintptr_t>(k_cur_bf16) | reinterpret_cast<uintptr_t>(v_cur_bf16)) & 15u))
+        return QVG_ERR_INVALID_ARG;
+    // queries are read and outputs written in 16-byte vectors
+    if (Nq > 0 && ((reinterpret_cast<uintptr_t>(q_bf16) | reinterpret_cast<uintptr_t>(out)) & 15u))
         return QVG_ERR_INVALID_ARG;
     qvg_status s = check_params(p, k->d);
     if (s != QVG_OK) return s;
