@@ -37,7 +37,7 @@ def _worker(rank, world, port, out):
 
 def test_two_ranks_max_step_time():
     world, port = 2, _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of a multi-threaded test process
     out = mgr.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     assert dict(out) == {0: 15.0, 1: 15.0}
@@ -61,7 +61,7 @@ def _ref_worker(rank, world, port, out):
 
 def test_reference_arm_other_ranks_exit_quietly():
     world, port = 2, _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of a multi-threaded test process
     out = mgr.dict()
     mp.spawn(_ref_worker, args=(world, port, out), nprocs=world, join=True)
     assert out[1] == (0, "")
