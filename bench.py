@@ -469,6 +469,9 @@ def run_own(args):
     # operands, fp32 accumulation): tensor roofline, dense 16-bit peak.
     tc_peak = peaks["bf16_tflops"]
     in_bytes = 2 * w.N * w.H * w.d * 2
+    # the distance GEMMs of compress (K and V, iters + 1 assignments each),
+    # against the bf16 tensor peak: the compress path is bound by compute
+    comp_gflop = 2.0 * 2 * w.N * w.C * w.d * (w.iters + 1) * w.H / 1e9
     line = {
         "metric": METRIC, "value": ws * w.Nq / (ms_step / 1e3), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -479,7 +482,8 @@ def run_own(args):
                                "out_dtype": "bf16"}),
         "compress": {"ms": ms_comp, "GB/s": in_bytes / (ms_comp / 1e3) / 1e9,
                      "frac_hbm": (in_bytes / (ms_comp / 1e3) / 1e9) / peaks["hbm_gbs"],
-                     "gflop": 2.0 * 2 * w.N * w.C * w.d * (w.iters + 1) * w.H / 1e9},
+                     "gflop": comp_gflop, "TFLOP/s": comp_gflop / ms_comp,
+                     "frac_tensor": comp_gflop / ms_comp / peaks["bf16_tflops"]},
         "attention": {"ms": ms_attn, "tok/s": w.Nq / (ms_attn / 1e3), "TFLOP/s": achieved},
         "kernels": extras,
         "roofline": {"kernel": "k_attention_ws", "bound": "tensor", "achieved": achieved,
