@@ -25,8 +25,12 @@
  *   - bf16 / fp16 values travel as their 16-bit patterns (uint16_t).
  *   - Layouts are row-major; "[a][b][c]" lists dimensions outermost first.
  *   - Thread safety: calls on different streams may run concurrently as long
- *     as they do not write the same buffers; the only library state is the
- *     per-device error word.
+ *     as they do not write the same buffers.  Library state: the per-device
+ *     error word, the no-alloc scratch (qvg_compress_chunk_noalloc), and a
+ *     launch set-up made once per process on first use (each kernel's
+ *     shared-memory limit, the SM count) for the device current then.  So a
+ *     process drives one device, and its first call of each operation
+ *     completes before other host threads make theirs.
  */
 #ifndef QVG_H
 #define QVG_H
