@@ -237,7 +237,8 @@ def run_reference(args):
         walls.append(wall)
     ms = 1e3 * statistics.mean(times)
     value = w.Nq / (ms / 1e3)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+    # n_gpus is the launch's N (the oracle itself runs on rank 0's host cores)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config(w, {"parallelism": "host threads"}),
