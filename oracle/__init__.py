@@ -273,6 +273,17 @@ def top1(q, k, nthreads=1):
     return am
 
 
+def shift_rate(q, k_ref, k_hat, nthreads=1):
+    """Top-1 attention-token shift rate (QuantWM write-up, results and the
+    ablation: the share of (query, query head) pairs whose highest-logit
+    history token differs between the reference cache and the reconstructed
+    one).  q [Nq,Hq,d], k_ref and k_hat [Nk,H,d]; ties go to the lowest
+    token on both sides."""
+    a = top1(q, k_ref, nthreads)
+    b = top1(q, k_hat, nthreads)
+    return float((a != b).mean())
+
+
 def query_stats(q, H, M=None, count=0):
     """Accumulate M [H,d,d] (fp64) += sum q q^T; returns (M, count)."""
     lib = _load()

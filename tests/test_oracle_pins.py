@@ -291,6 +291,44 @@ def test_attention_brute_force(orc):
             np.testing.assert_allclose(out[:, 0], np.repeat(v[:, 0], Nq, 0))
 
 
+def test_top1_brute_force_ties_and_gqa(orc):
+    """orc_top1 (the oracle side of the top-1 shift rate, QuantWM write-up,
+    results: the share of queries whose most-attended history token moves)
+    against numpy's argmax of q.k, which returns the first of equal maxima.
+    Small-integer operands make every dot product exact, so planted
+    duplicate keys give exact ties that must go to the lowest index; query
+    heads read KV head hq // (Hq / H) (GQA with Hq = 2H and 4H), and the KV
+    heads differ, so a wrong head map fails."""
+    rng = np.random.default_rng(11)
+    for Nq, Nk, H, Hq in [(7, 9, 2, 4), (5, 13, 1, 4), (6, 6, 3, 3)]:
+        d = 8
+        q = rng.integers(-3, 4, (Nq, Hq, d)).astype(np.float32)
+        k = rng.integers(-3, 4, (Nk, H, d)).astype(np.float32)
+        k[Nk - 1] = k[1]          # a duplicate of key 1 (tie goes to 1)
+        k[Nk - 2] = k[0]          # and of key 0
+        q[0] = 0.0                # all logits 0: the tie goes to slot 0
+        am = orc.top1(q, k)
+        assert am.shape == (Hq, Nq)
+        for hq in range(Hq):
+            h = hq // (Hq // H)
+            ref = (q[:, hq].astype(np.float64) @ k[:, h].T.astype(np.float64)).argmax(-1)
+            np.testing.assert_array_equal(am[hq], ref)
+        assert (am[:, 0] == 0).all()
+        # top1 agrees with the full attention's argmax (another route)
+        _, _, am2 = orc.attention(q, k, k)
+        np.testing.assert_array_equal(am, am2)
+    # the shift rate: 0 for the same cache; each query whose best key changes counts once
+    q = rng.standard_normal((40, 2, 16)).astype(np.float32)
+    k = rng.standard_normal((30, 2, 16)).astype(np.float32)
+    assert orc.shift_rate(q, k, k) == 0.0
+    base = orc.top1(q, k)
+    k2 = k.copy()
+    k2[base[0, 0], 0] = -k2[base[0, 0], 0]  # the best key of query 0, head 0, flips sign
+    moved = (orc.top1(q, k2) != base)
+    assert moved[0, 0]
+    assert orc.shift_rate(q, k, k2) == pytest.approx(moved.mean())
+
+
 def test_attention_exact_when_lossless(orc):
     """C = N makes the compressed cache exact, so attention over it equals
     attention over the bf16 cache."""
