@@ -35,9 +35,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) of one k_attention_ws launch of the bench
 # workload, from an ncu capture of `dram__bytes_read.sum,dram__bytes_write.sum`
-# (profiles/k_attention_ws_longcat_8chunks.md), keyed by the SHA-256 of the
-# kernel's code (comments stripped) so that a changed kernel reports null
-# until re-measured.
+# on the same command, keyed by the SHA-256 of the kernel's code (comments
+# stripped) so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
     "15f336d22d257c991a4c603b24c390ec8a648e30d69880c44102f3f724263a03": 80424448 + 3613184,
