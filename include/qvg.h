@@ -21,16 +21,20 @@
  *     host before anything is launched and leave all buffers untouched.
  *     A failed launch returns QVG_ERR_CUDA.  Errors found on the device
  *     (an exceeded wait bound) are latched in a per-device status word and
- *     reported by qvg_get_status.
+ *     reported by qvg_get_status(stream).
  *   - bf16 / fp16 values travel as their 16-bit patterns (uint16_t).
  *   - Layouts are row-major; "[a][b][c]" lists dimensions outermost first.
- *   - Thread safety: calls on different streams may run concurrently as long
- *     as they do not write the same buffers.  Library state: the per-device
- *     error word, the no-alloc scratch (qvg_compress_chunk_noalloc), and a
- *     launch set-up made once per process on first use (each kernel's
- *     shared-memory limit, the SM count) for the device current then.  So a
- *     process drives one device, and its first call of each operation
- *     completes before other host threads make theirs.
+ *   - Thread safety: calls on different streams, from any host threads, may
+ *     run concurrently as long as they do not write the same buffers.  Each
+ *     call works on the device current on its host thread.  Library state:
+ *     the per-device error word, the no-alloc scratch
+ *     (qvg_compress_chunk_noalloc), and per-device launch set-up tables
+ *     (each kernel's shared-memory limit, the SM count, the error word's
+ *     address), each entry made once per device by the first call that
+ *     needs it and published atomically, so first calls may race and one
+ *     process may drive several devices.  Per host thread: the last CUDA
+ *     error (qvg_last_cuda_error) and the wait settings of
+ *     qvg_debug_set_wait.
  */
 #ifndef QVG_H
 #define QVG_H
@@ -60,6 +64,8 @@ typedef enum {
 #define QVG_OUTLIER 8         /* outlier split in the residual quantiser: per    */
                               /* group, a value above the group's P99 is kept   */
                               /* in fp16 (G <= 64; see outl_val below)           */
+#define QVG_KEEP_MEANS 16     /* qvg_compress_chunk leaves each stage's fp32     */
+                              /* centroid means in the workspace (see there)     */
 
 #define QVG_TILE 128      /* chunks start at multiples of this many token slots */
 #define QVG_PSAC_RANK 8   /* PSAC subspace rank ([QWM] PSAC: top-8 directions)  */
@@ -86,7 +92,8 @@ typedef enum {
  *   iters      Lloyd iterations (assign + update) before the final assign.
  *   scale_mode 0: S = max|r| / (2^{b-1} - 1)  ([QVG] "core tension");
  *              1: S = max|r| / 2, codes in [-2, 1]  ([P1] section 2; bits = 2).
- *   flags      QVG_QSAC | QVG_PSAC | QVG_GIVEN_CENTROIDS | QVG_OUTLIER.
+ *   flags      QVG_QSAC | QVG_PSAC | QVG_GIVEN_CENTROIDS | QVG_OUTLIER |
+ *              QVG_KEEP_MEANS.
  *   anchor_every  temporal anchors ([P2] section 3.3: the first frames of
  *              each window are kept at high precision so that errors do not
  *              pile up from window to window): 0 = none; k > 0 = chunk c of
@@ -238,6 +245,11 @@ qvg_status qvg_workspace_size(const qvg_params *p, int32_t op, int32_t n,
  *              caller has written all L stages' starting centroids into the
  *              new chunk's centroid slot (index n_chunks).
  *   workspace  device scratch of at least qvg_workspace_size(QVG_OP_COMPRESS).
+ *              With QVG_KEEP_MEANS (and C > 0, iters >= 1) its first
+ *              L*H*C*d*4 bytes hold, after the call, fp32 [L][H][C][d]: each
+ *              stage's centroids of its last Lloyd update before the bf16
+ *              rounding (the member mean in fp32; an empty cluster's kept
+ *              centroid), for checking the update against a reference.
  * Returns QVG_ERR_CAPACITY when the chunk does not fit, in the slots or (an
  * anchor chunk) in its anchor rows; nothing is written then.
  */
@@ -260,7 +272,9 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16,
  * device-wide synchronisation of cudaMalloc / cudaFree).  Same arguments,
  * results and errors as qvg_compress_chunk, which it calls; the workspace is
  * a fixed scratch array of QVG_NOALLOC_SCRATCH_BYTES inside the library.
- *   - Returns QVG_ERR_WORKSPACE, before anything is launched, when
+ *   - Checks its arguments and the cache's capacity first, in the order
+ *     and with the codes of qvg_compress_chunk; then returns
+ *     QVG_ERR_WORKSPACE, before anything is launched, when
  *     qvg_workspace_size(QVG_OP_COMPRESS) for this call exceeds the scratch
  *     (for example L > 1 or PSAC on large chunks: use qvg_compress_chunk).
  *   - The first call on a device, made with that device current, looks up
@@ -390,11 +404,34 @@ qvg_status quantwm_psac_basis(const float *M, const int64_t *count, int32_t H,
 const char *qvg_last_cuda_error(void);
 
 /*
- * Synchronise with the current device, then return and clear its latched
- * device-side error (QVG_OK if none).  Also returns QVG_ERR_CUDA when a
- * CUDA error is pending.
+ * Synchronise with `stream` (NULL: with the whole current device), then
+ * return and clear the current device's latched device-side error (QVG_OK
+ * if none).  The word is per device, so an error raised by work on another
+ * stream that has completed is reported too; work still running elsewhere
+ * may latch one after the read.  Returns QVG_ERR_CUDA when the
+ * synchronisation reports a CUDA error.
  */
-qvg_status qvg_get_status(void);
+qvg_status qvg_get_status(void *stream);
+
+/*
+ * Device-side waits, a test hook for the failure path (the pages have no
+ * counterpart).  Every wait of a kernel on a barrier (the k-means
+ * assignment's tile and MMA hand-offs, the attention pipeline's) is bounded;
+ * when the bound runs out the kernel stops its work, waits at the default
+ * bound for the tensor-core work it has issued, frees its tensor memory,
+ * latches QVG_ERR_TIMEOUT in the device word and returns, leaving the
+ * context usable.  This call sets, for the kernels that the calling host
+ * thread launches afterwards:
+ *   limit_ns  the bound of those waits in nanoseconds; 0 restores the
+ *             default of 2 s.
+ *   inject    1: each such kernel additionally waits once on a barrier that
+ *             nothing completes, with tensor-core work in flight, so that
+ *             the bound runs out (qvg_get_status then reports
+ *             QVG_ERR_TIMEOUT and the call's outputs are undefined);
+ *             0: no such wait.
+ * Errors: QVG_ERR_INVALID_ARG for inject other than 0 or 1.
+ */
+qvg_status qvg_debug_set_wait(uint64_t limit_ns, int32_t inject);
 
 #ifdef __cplusplus
 }

@@ -252,3 +252,40 @@ def test_attention_workspace_only_for_split_queries(lib):
     assert small >= 2 * 16 * 16 * (128 + 3) * 4  # at least two splits
     assert small % 256 == 0
     assert qvg.workspace_size(p, qvg.QVG_OP_ATTENTION, 4680, 16, 128, 16) == 0
+
+
+def test_debug_set_wait_arguments(lib):
+    """The bounded-wait test hook takes inject 0 or 1 and touches no device
+    (it only sets the calling host thread's launch settings)."""
+    assert lib.qvg_debug_set_wait(ct.c_uint64(1000), 2) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_debug_set_wait(ct.c_uint64(1000), -1) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_debug_set_wait(ct.c_uint64(1000000), 1) == qvg.QVG_OK
+    assert lib.qvg_debug_set_wait(ct.c_uint64(0), 0) == qvg.QVG_OK  # back to the default
+
+
+def test_noalloc_checks_arguments_before_scratch_size(lib):
+    """qvg_compress_chunk_noalloc reports argument and capacity errors with
+    qvg_compress_chunk's codes, and QVG_ERR_WORKSPACE only for a valid call
+    whose workspace would exceed the fixed scratch."""
+    p = _params(C=16, group=32)
+    x = ct.c_void_p(0x2000)
+    c = _fake_cache()
+    assert lib.qvg_compress_chunk_noalloc(ct.byref(p), None, 100, None, None, ct.byref(c), None) == qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_compress_chunk_noalloc(ct.byref(p), x, 70000, None, None, ct.byref(c), None) == qvg.QVG_ERR_INVALID_ARG
+    full = _fake_cache(n_chunks=2, n_tokens=256)
+    assert lib.qvg_compress_chunk_noalloc(ct.byref(p), x, 10, None, None, ct.byref(full), None) == qvg.QVG_ERR_CAPACITY
+    # a valid three-stage chunk of 65,535 tokens x 32 heads needs far more than the scratch
+    p3 = _params(C=16, group=32, L=3)
+    big = _fake_cache(H=32, cap=65536, max_chunks=1)
+    assert qvg.workspace_size(qvg.Params(C=16, L=3, bits=2, group=32), qvg.QVG_OP_COMPRESS, 65535, 32, 64) \
+        > qvg.NOALLOC_SCRATCH_BYTES
+    assert lib.qvg_compress_chunk_noalloc(ct.byref(p3), x, 65535, None, None, ct.byref(big), None) == qvg.QVG_ERR_WORKSPACE
+    assert c.n_chunks == 0 and full.n_chunks == 2 and big.n_chunks == 0
+
+
+def test_noalloc_scratch_size_matches_header():
+    """The binding's scratch size is the header's QVG_NOALLOC_SCRATCH_BYTES."""
+    src = open(os.path.join(ROOT, "include", "qvg.h")).read()
+    m = re.search(r"#define\s+QVG_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "QVG_NOALLOC_SCRATCH_BYTES not found"
+    assert qvg.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

@@ -79,6 +79,26 @@ def test_history_queries_hold_the_planted_energy():
         assert abs(frac - (0.70 + 0.30 * 8 / w.d)) < 0.03, frac
 
 
+def test_history_queries_channel_activity():
+    """The queries' per-channel activity (mean q_j^2, the QSAC weight) is
+    3.1 on the quarter of channels that carry the planted directions and
+    0.3 on the rest; its mean over channels is 1 (E||q||^2 = d)."""
+    w = W["quantwm"]
+    act = synth.active_channels(w, 9)
+    assert act.shape == (w.H, w.d // 4)
+    U = synth.planted_basis(w, 9)
+    for h in range(w.H):
+        off = np.setdiff1d(np.arange(w.d), act[h])
+        assert np.abs(U[h][off]).max() == 0.0
+    q = synth.history_queries(w, 9, n_tokens=20000).astype(np.float64)
+    for h in (0, w.H - 1):
+        m = (q[:, h] ** 2).mean(0)
+        on = np.zeros(w.d, bool)
+        on[act[h]] = True
+        assert abs(m[on].mean() - 3.1) < 0.1 and abs(m[~on].mean() - 0.3) < 0.02
+        assert abs(m.mean() - 1.0) < 0.03
+
+
 # ------------------------------------------------------------------ benchmark helpers
 
 def test_attention_hash_ignores_comments_only(tmp_path, monkeypatch):

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libqvg.so")
 
 QVG_OK, QVG_ERR_INVALID_ARG, QVG_ERR_UNSUPPORTED, QVG_ERR_CUDA = 0, 1, 2, 3
 QVG_ERR_TIMEOUT, QVG_ERR_WORKSPACE, QVG_ERR_CAPACITY = 4, 5, 6
-QVG_QSAC, QVG_PSAC, QVG_GIVEN_CENTROIDS, QVG_OUTLIER = 1, 2, 4, 8
+QVG_QSAC, QVG_PSAC, QVG_GIVEN_CENTROIDS, QVG_OUTLIER, QVG_KEEP_MEANS = 1, 2, 4, 8, 16
 QVG_TILE = 128
 QVG_PSAC_RANK = 8
 QVG_CACHE_NBUF = 14
@@ -32,6 +32,7 @@ EXPORTED = (
     "qvg_status_string", "qvg_cache_bytes", "qvg_workspace_size", "qvg_compress_chunk",
     "qvg_decompress", "qvg_attention", "quantwm_query_stats", "quantwm_psac_basis",
     "qvg_get_status", "qvg_last_cuda_error", "qvg_compress_chunk_noalloc", "qvg_attention_ar",
+    "qvg_debug_set_wait",
 )
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -85,7 +86,8 @@ def lib():
                                        sz, vp]
         L.quantwm_query_stats.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
         L.quantwm_psac_basis.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
-        L.qvg_get_status.argtypes = []
+        L.qvg_get_status.argtypes = [vp]
+        L.qvg_debug_set_wait.argtypes = [ct.c_uint64, i32]
         L.qvg_last_cuda_error.restype = ct.c_char_p
         L.qvg_last_cuda_error.argtypes = []
         _lib = L
@@ -199,7 +201,9 @@ class CompressedKV:
 def compress_chunk(params: Params, x, cache: CompressedKV, qsac_w=None, psac_basis=None,
                    workspace=None, stream=None):
     """Append one chunk x (bf16 [N, H, d], contiguous, on the GPU) to cache.
-    Returns the first token slot of the chunk."""
+    Returns the first token slot of the chunk.  With QVG_KEEP_MEANS in
+    params.flags, pass a workspace and read the fp32 means from it with
+    kept_means()."""
     import torch
     assert x.dtype == torch.bfloat16 and x.is_contiguous() and x.dim() == 3
     N = x.shape[0]
@@ -214,6 +218,14 @@ def compress_chunk(params: Params, x, cache: CompressedKV, qsac_w=None, psac_bas
     _check(s, "qvg_compress_chunk")
     cache.n_chunks, cache.n_tokens = c.n_chunks, c.n_tokens
     return slot0
+
+
+def kept_means(params: Params, workspace, H, d):
+    """fp32 [L, H, C, d] view of the centroid means a QVG_KEEP_MEANS
+    compression left at the start of its workspace."""
+    import torch
+    n = params.L * H * params.C * d
+    return workspace[:4 * n].view(torch.float32).view(params.L, H, params.C, d)
 
 
 def compress_chunk_noalloc(params: Params, x, cache: CompressedKV, qsac_w=None, psac_basis=None,
@@ -249,9 +261,11 @@ def decompress(params: Params, cache: CompressedKV, tok0, ntok, out_dtype=QVG_OU
 
 def attention(params: Params, q, kc: CompressedKV, vc: CompressedKV, scale=0.0,
               out_dtype=QVG_OUT_F32, want_lse=False, want_top1=False, out=None, workspace=None,
-              stream=None):
+              stream=None, allow_split=True):
     """O = softmax(scale Q K_hat^T) V_hat over every cached token.
-    q: bf16 [Nq, Hq, d].  Returns (out, lse or None, top1 or None)."""
+    q: bf16 [Nq, Hq, d].  Returns (out, lse or None, top1 or None).
+    allow_split=False passes no workspace, so the cache is never split over
+    extra CTAs."""
     import torch
     assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 3
     Nq, Hq, d = q.shape
@@ -260,8 +274,10 @@ def attention(params: Params, q, kc: CompressedKV, vc: CompressedKV, scale=0.0,
         out = torch.empty((Nq, Hq, d), dtype=dt, device=q.device)
     lse = torch.empty((Hq, Nq), dtype=torch.float32, device=q.device) if want_lse else None
     top1 = torch.empty((Hq, Nq), dtype=torch.int32, device=q.device) if want_top1 else None
-    need = workspace_size(params, QVG_OP_ATTENTION, Nq, kc.H, d, Hq)
-    if need and (workspace is None or workspace.numel() < need):
+    need = workspace_size(params, QVG_OP_ATTENTION, Nq, kc.H, d, Hq) if allow_split else 0
+    if not allow_split:
+        workspace = None
+    elif need and (workspace is None or workspace.numel() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     k, v = kc.c(), vc.c()
     p = params.c()
@@ -333,9 +349,17 @@ def psac_basis(M, count, rank=QVG_PSAC_RANK, stream=None):
     return U, eig, frac
 
 
-def get_status():
-    """Synchronise and return (and clear) the device-side error status."""
-    return lib().qvg_get_status()
+def get_status(stream=None):
+    """Synchronise with `stream` (default: the whole device) and return (and
+    clear) the device-side error status."""
+    return lib().qvg_get_status(None if stream is None else ct.c_void_p(stream.cuda_stream))
+
+
+def debug_set_wait(limit_ns=0, inject=False):
+    """Bound of the device-side waits of the kernels this host thread launches
+    next (0: the default 2 s) and the failure-path test hook (see
+    qvg_debug_set_wait in include/qvg.h)."""
+    _check(lib().qvg_debug_set_wait(int(limit_ns), int(bool(inject))), "qvg_debug_set_wait")
 
 
 def compression_ratio(params: Params, H, d, tokens_per_chunk, n_chunks, with_psac=False):

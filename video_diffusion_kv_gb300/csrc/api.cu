@@ -1,7 +1,9 @@
 // api.cu -- the extern "C" entry points of libqvg: argument validation,
 // workspace carving and the launch sequence of each call.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -11,18 +13,79 @@ __device__ int g_qvg_error = 0;
 static thread_local cudaError_t t_last_cuda_error = cudaSuccess;
 void note_cuda_error(cudaError_t e) { t_last_cuda_error = e; }
 
-int *device_error_word() {
-    static int *ptr[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!ptr[dev]) {
-        void *a = nullptr;
-        if (cudaGetSymbolAddress(&a, g_qvg_error) != cudaSuccess) return nullptr;
-        ptr[dev] = static_cast<int *>(a);
+namespace {
+// Per-device tables of the launch set-up; each entry is written once, by
+// the first call that needs it on that device, and published atomically
+// (a racing second writer stores the same value).
+std::atomic<int *> g_error_word[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+std::mutex g_attr_mutex;  // serialises cudaFuncSetAttribute calls of first launches
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
     }
-    return ptr[dev];
+    return dev >= 0 && dev < kMaxDevices ? dev : -1;
 }
+
+// Bounded-wait settings of the calling host thread (qvg_debug_set_wait).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+thread_local uint64_t t_wait_ns = kDefaultWaitNs;
+thread_local int t_wait_inject = 0;
+}  // namespace
+
+uint64_t wait_limit_ns() { return t_wait_ns; }
+int wait_inject() { return t_wait_inject; }
+
+int *device_error_word() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    int *p = g_error_word[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_qvg_error) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        p = static_cast<int *>(a);
+        g_error_word[dev].store(p, std::memory_order_release);
+    }
+    return p;
 }
+
+int sm_count_current() {
+    const int dev = current_device();
+    if (dev < 0) return 152;
+    int n = g_sm_count[dev].load(std::memory_order_acquire);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            return 152;
+        }
+        g_sm_count[dev].store(n, std::memory_order_release);
+    }
+    return n;
+}
+
+qvg_status smem_limit_once(std::atomic<uint64_t> &done, const void *func, int bytes) {
+    const int dev = current_device();
+    if (dev < 0) return QVG_ERR_CUDA;
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return QVG_OK;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    if (done.load(std::memory_order_acquire) & bit) return QVG_OK;
+    const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        note_cuda_error(e);
+        return QVG_ERR_CUDA;
+    }
+    done.fetch_or(bit, std::memory_order_release);
+    return QVG_OK;
+}
+}  // namespace qvg
 
 using namespace qvg;
 
@@ -37,7 +100,7 @@ qvg_status check_params(const qvg_params *p, int d) {
     if (!p) return QVG_ERR_INVALID_ARG;
     if (p->anchor_every < 0 || p->L < 1 || p->L > 16 || p->C < 0 || p->iters < 0 ||
         p->iters > 10000 || (p->bits != 2 && p->bits != 4) || p->group < 1 ||
-        (p->scale_mode != 0 && p->scale_mode != 1) || (p->flags & ~15))
+        (p->scale_mode != 0 && p->scale_mode != 1) || (p->flags & ~31))
         return QVG_ERR_INVALID_ARG;
     if (p->scale_mode == 1 && p->bits != 2) return QVG_ERR_INVALID_ARG;
     if (p->C > QVG_MAX_CLUSTERS) return QVG_ERR_UNSUPPORTED;
@@ -69,6 +132,7 @@ qvg_status check_cache(const qvg_params *p, const qvg_cache *c) {
 }
 
 struct CompressWs {
+    float *means;  // QVG_KEEP_MEANS: [L][H][C][d] at offset 0
     int32_t *ids;
     float *cnorm;
     float *xnorm;
@@ -85,6 +149,9 @@ CompressWs carve_compress(const qvg_params *p, int N, int H, int d, char *base) 
         off += align_up(bytes);
         return ptr;
     };
+    if (p->flags & QVG_KEEP_MEANS)
+        w.means = reinterpret_cast<float *>(
+            take(sizeof(float) * static_cast<size_t>(p->L) * H * std::max(p->C, 1) * d));
     w.ids = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * static_cast<size_t>(H) * N));
     w.cnorm = reinterpret_cast<float *>(take(sizeof(float) * static_cast<size_t>(H) * std::max(p->C, 1)));
     w.xnorm = reinterpret_cast<float *>(take(sizeof(float) * static_cast<size_t>(H) * N));
@@ -96,6 +163,27 @@ CompressWs carve_compress(const qvg_params *p, int N, int H, int d, char *base) 
 }
 
 }  // namespace
+
+namespace qvg {
+qvg_status check_compress_args(const qvg_params *p, const void *x_bf16, int N, const float *qsac_w,
+                               const float *psac_basis, const qvg_cache *cache, size_t *ws_need) {
+    if (!cache || !x_bf16) return QVG_ERR_INVALID_ARG;
+    qvg_status s = check_params(p, cache->d);
+    if (s != QVG_OK) return s;
+    if ((s = check_cache(p, cache)) != QVG_OK) return s;
+    if (N < 1 || N > 65535) return QVG_ERR_INVALID_ARG;
+    if ((p->flags & QVG_QSAC) && !qsac_w) return QVG_ERR_INVALID_ARG;
+    if ((p->flags & QVG_PSAC) && !psac_basis) return QVG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(x_bf16) % 16 != 0) return QVG_ERR_INVALID_ARG;
+    if ((p->flags & QVG_PSAC) && reinterpret_cast<uintptr_t>(psac_basis) % 16 != 0) return QVG_ERR_INVALID_ARG;
+    const int Naligned = ceil_div(N, QVG_TILE) * QVG_TILE;
+    if (cache->n_chunks >= cache->max_chunks ||
+        static_cast<int64_t>(cache->n_tokens) + Naligned > cache->capacity_tokens)
+        return QVG_ERR_CAPACITY;
+    *ws_need = carve_compress(p, N, cache->H, cache->d, nullptr).bytes;
+    return QVG_OK;
+}
+}  // namespace qvg
 
 extern "C" {
 
@@ -159,25 +247,16 @@ qvg_status qvg_workspace_size(const qvg_params *p, int32_t op, int32_t n, int32_
     return QVG_ERR_INVALID_ARG;
 }
 
+
 qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N,
                               const float *qsac_w, const float *psac_basis, qvg_cache *cache,
                               void *workspace, size_t ws_bytes, void *stream) {
-    if (!cache || !x_bf16) return QVG_ERR_INVALID_ARG;
-    qvg_status s = check_params(p, cache->d);
+    size_t need_bytes = 0;
+    qvg_status s = check_compress_args(p, x_bf16, N, qsac_w, psac_basis, cache, &need_bytes);
     if (s != QVG_OK) return s;
-    if ((s = check_cache(p, cache)) != QVG_OK) return s;
-    if (N < 1 || N > 65535) return QVG_ERR_INVALID_ARG;
-    if ((p->flags & QVG_QSAC) && !qsac_w) return QVG_ERR_INVALID_ARG;
-    if ((p->flags & QVG_PSAC) && !psac_basis) return QVG_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(x_bf16) % 16 != 0) return QVG_ERR_INVALID_ARG;
-    if ((p->flags & QVG_PSAC) && reinterpret_cast<uintptr_t>(psac_basis) % 16 != 0) return QVG_ERR_INVALID_ARG;
     const int H = cache->H, d = cache->d;
     const int Naligned = ceil_div(N, QVG_TILE) * QVG_TILE;
-    if (cache->n_chunks >= cache->max_chunks ||
-        static_cast<int64_t>(cache->n_tokens) + Naligned > cache->capacity_tokens)
-        return QVG_ERR_CAPACITY;
-    const CompressWs need = carve_compress(p, N, H, d, nullptr);
-    if (need.bytes > 0 && (!workspace || ws_bytes < need.bytes)) return QVG_ERR_WORKSPACE;
+    if (need_bytes > 0 && (!workspace || ws_bytes < need_bytes)) return QVG_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return QVG_ERR_WORKSPACE;
     const CompressWs ws = carve_compress(p, N, H, d, static_cast<char *>(workspace));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -228,7 +307,9 @@ qvg_status qvg_compress_chunk(const qvg_params *p, const void *x_bf16, int32_t N
                 if ((s = launch_kmeans_assign(g, N, H, d, cent, cent_hs, Ce, ws.cnorm, C, w, ws.xnorm, ws.ids, st)) !=
                     QVG_OK)
                     return s;
-                if ((s = launch_kmeans_update(xin, f32, N, H, d, ws.ids, cent, cent_hs, Ce, C, w, ws.cnorm, st)) !=
+                float *means = ws.means && it == p->iters - 1 ? ws.means + static_cast<size_t>(l) * H * C * d : nullptr;
+                if ((s = launch_kmeans_update(xin, f32, N, H, d, ws.ids, cent, cent_hs, Ce, C, w, ws.cnorm, means,
+                                              st)) !=
                     QVG_OK)
                     return s;
             }
@@ -336,17 +417,35 @@ qvg_status quantwm_psac_basis(const float *M, const int64_t *count, int32_t H, i
 
 const char *qvg_last_cuda_error(void) { return cudaGetErrorName(t_last_cuda_error); }
 
-qvg_status qvg_get_status(void) {
-    const cudaError_t e = cudaDeviceSynchronize();
+qvg_status qvg_debug_set_wait(uint64_t limit_ns, int32_t inject) {
+    if (inject != 0 && inject != 1) return QVG_ERR_INVALID_ARG;
+    t_wait_ns = limit_ns == 0 ? kDefaultWaitNs : limit_ns;
+    t_wait_inject = inject;
+    return QVG_OK;
+}
+
+qvg_status qvg_get_status(void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = st ? cudaStreamSynchronize(st) : cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         note_cuda_error(e);
         return QVG_ERR_CUDA;
     }
+    int *word = device_error_word();
+    if (!word) return QVG_ERR_CUDA;
     int err = 0;
-    const int zero = 0;
-    if (cudaMemcpyFromSymbol(&err, g_qvg_error, sizeof(int)) != cudaSuccess) return QVG_ERR_CUDA;
-    if (err != 0 && cudaMemcpyToSymbol(g_qvg_error, &zero, sizeof(int)) != cudaSuccess) return QVG_ERR_CUDA;
+    e = cudaMemcpyAsync(&err, word, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && err != 0) {
+        e = cudaMemsetAsync(word, 0, sizeof(int), st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        note_cuda_error(e);
+        return QVG_ERR_CUDA;
+    }
     return static_cast<qvg_status>(err);
 }
 

@@ -56,6 +56,10 @@ struct AttnWsArgs {
     // read as bf16 rows of these arenas; chunk_anchor[c] = first row, or -1
     const uint16_t *kanch, *vanch;
     const int32_t *chunk_anchor;
+    // bound of the pipeline's waits (ns); inject: the test hook that makes
+    // each softmax group's issuer wait once on a barrier nothing completes
+    uint64_t wait_ns;
+    int inject;
 };
 
 namespace ws {
@@ -81,7 +85,7 @@ __device__ __forceinline__ float ex2(float x) {
 // Bounded wait that also gives up as soon as another role has failed.  The
 // global timer (slow to read) is consulted only after 32 unsuccessful
 // try_waits, so a short wait never reads it.
-__device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, volatile int *fail) {
+__device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, volatile int *fail, uint64_t limit_ns) {
     for (int i = 0; i < 32; ++i)
         if (umma::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = umma::globaltimer_ns();
@@ -89,7 +93,7 @@ __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, volatile in
         for (int i = 0; i < 32; ++i)
             if (umma::mbar_try_wait(bar, parity)) return true;
         if (*fail) return false;
-        if (umma::globaltimer_ns() - t0 > kWaitNs) {
+        if (umma::globaltimer_ns() - t0 > limit_ns) {
             *fail = 1;
             return false;
         }
@@ -404,7 +408,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         const bool valid = r < ti0.nvalid, valid1 = t + 1 < n_tiles && r < ti1.nvalid;
         if constexpr (KB == 2) {
             if (valid) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, ti0, r, id0, 1, B);
-            if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
+            if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
                 decode_store_half<BITS>(A, T, r);
                 if (OUTL) patch_outliers<D, BITS>(a, pr.cent, A, h, ti0.chunk, id0, 0, T, r);
@@ -421,7 +425,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         } else {
             B = A;
             if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, ti1, r, id1, 0, A);
-            if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
+            if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
                 decode_store_half<BITS>(B, T, r);
                 if (OUTL) patch_outliers<D, BITS>(a, pr.cent, B, h, ti0.chunk, id0, 0, T, r);
@@ -650,7 +654,7 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
         if (l == L - 1) {
             const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
             uint8_t *T = pr.buf0 + b * TB + r * 128;
-            if (qt == 0 && use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail)) return;
+            if (qt == 0 && use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             float v[32];
 #pragma unroll
             for (int k = 0; k < 16; ++k) up2(acc[k], v[2 * k], v[2 * k + 1]);
@@ -734,7 +738,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
     uint8_t *Q0 = sm, *Q1 = Q0 + TB, *Kt = Q1 + TB, *Vt0 = Kt + TB, *P0 = Vt0 + 2 * TB, *P1 = P0 + PB;
-    __shared__ uint64_t kfull, kfree, vfull[2], vfree[2], sfull[2], ofull[2], drain;
+    __shared__ uint64_t kfull, kfree, vfull[2], vfree[2], sfull[2], ofull[2], drain, never;
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
 
@@ -765,6 +769,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         umma::mbar_init(&kfull, 128);
         umma::mbar_init(&kfree, 2);
         umma::mbar_init(&drain, 2);
+        umma::mbar_init(&never, 1);  // nothing arrives: the bounded-wait test hook
         for (int i = 0; i < 2; ++i) {
             umma::mbar_init(&vfull[i], 128);
             umma::mbar_init(&vfree[i], 2);
@@ -813,17 +818,21 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         // wait a warp only stops doing work (live is warp-uniform).
         bool ok_issue = true;
         if (issuer && n_tiles > 0) {
-            if (ws::wait(&kfull, 0, vfail))
+            if (ws::wait(&kfull, 0, vfail, a.wait_ns))
                 issue_S();
             else
                 ok_issue = false;
+            // test hook: with S_i(0) in flight, wait on a barrier that nothing
+            // completes; the bound runs out, every role stops, and the drain
+            // below waits for the MMA
+            if (ok_issue && a.inject && !ws::wait(&never, 0, vfail, a.wait_ns)) ok_issue = false;
         }
         bool live = __all_sync(0xffffffffu, ok_issue);
         float m_used = -INFINITY, l_sum = 0.0f, best = -INFINITY;
         int best_slot = 0;
         for (int t = 0; t < n_tiles; ++t) {
             const TileInfo ti = tile_info<MODE != 0>(a, tb + t);
-            if (live) live = __all_sync(0xffffffffu, ws::wait(&sfull[i], t & 1, vfail));
+            if (live) live = __all_sync(0xffffffffu, ws::wait(&sfull[i], t & 1, vfail, a.wait_ns));
             float corr = 1.0f;
             if (live) {
                 umma::tc_fence_after();
@@ -877,7 +886,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                     m_used = tmax;
                 }
                 if (t > 0) {  // PV_i of the previous tile done: P_i is free and O_i settled
-                    live = __all_sync(0xffffffffu, ws::wait(&ofull[i], (t - 1) & 1, vfail));
+                    live = __all_sync(0xffffffffu, ws::wait(&ofull[i], (t - 1) & 1, vfail, a.wait_ns));
                     if (live) {
                         umma::tc_fence_after();
                         if (__any_sync(0xffffffffu, rescale)) {
@@ -925,7 +934,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             umma::tc_fence_before();
             group_sync(i);
             if (issuer && live) {
-                if (ws::wait(&vfull[t & 1], (t >> 1) & 1, vfail)) {
+                if (ws::wait(&vfull[t & 1], (t >> 1) & 1, vfail, a.wait_ns)) {
                     umma::tc_fence_after();
                     const uint64_t dp = umma::desc_sw128(pa), dv = umma::desc_sw128_mn(va0 + (t & 1) * TB, 16384);
 #pragma unroll 1
@@ -936,7 +945,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                     umma::mma_commit(&ofull[i]);
                     umma::mma_commit(&vfree[t & 1]);
                     if (more && !s_next) {
-                        if (ws::wait(&kfull, (t + 1) & 1, vfail))
+                        if (ws::wait(&kfull, (t + 1) & 1, vfail, a.wait_ns))
                             issue_S();
                         else
                             ok_issue = false;
@@ -948,7 +957,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             live = live && __all_sync(0xffffffffu, ok_issue);
         }
         // epilogue: O_i / l
-        bool ok = live && !*vfail && n_tiles > 0 && ws::wait(&ofull[i], (n_tiles - 1) & 1, vfail);
+        bool ok = live && !*vfail && n_tiles > 0 && ws::wait(&ofull[i], (n_tiles - 1) & 1, vfail, a.wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             umma::tc_fence_after();
@@ -1087,16 +1096,11 @@ __global__ void __launch_bounds__(256) k_attn_merge(const float *__restrict__ po
 template <int D, int BITS, bool TOP1, int MODE>
 static qvg_status attn_ws_t(const AttnWsArgs &a, int a_splits, cudaStream_t st) {
     constexpr size_t smem = 5 * (D / 64) * 16384 + 2 * 32768 + 1024;
-    static bool attr = false;
-    if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(k_attention_ws<D, BITS, TOP1, MODE>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            note_cuda_error(e);
-            return QVG_ERR_CUDA;
-        }
-        attr = true;
+    {
+        static std::atomic<uint64_t> done{0};
+        const qvg_status s = smem_limit_once(done, reinterpret_cast<const void *>(k_attention_ws<D, BITS, TOP1, MODE>),
+                                             static_cast<int>(smem));
+        if (s != QVG_OK) return s;
     }
     dim3 grid(ceil_div(a.Nq, 256), a.Hq, a_splits);
     k_attention_ws<D, BITS, TOP1, MODE><<<grid, ws::kThreads, smem, st>>>(a);
@@ -1113,16 +1117,7 @@ static qvg_status attn_ws(const AttnWsArgs &a, int splits, cudaStream_t st) {
     return a.top1 ? attn_ws_t<D, BITS, true, 0>(a, splits, st) : attn_ws_t<D, BITS, false, 0>(a, splits, st);
 }
 
-static int attn_sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 152;
-    }
-    return n;
-}
+static int attn_sm_count() { return sm_count_current(); }
 
 // Number of cache splits: when (query blocks x query heads) CTAs leave SMs
 // idle, each (block, head) pair is split over enough CTAs to reach about two
@@ -1198,6 +1193,8 @@ qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, i
     a.lse = lse;
     a.top1 = top1;
     a.err = device_error_word();
+    a.wait_ns = wait_limit_ns();
+    a.inject = wait_inject();
     if (Nq == 0) return QVG_OK;
     const int d = k->d;
     // split the cache over more CTAs when the query blocks alone leave SMs idle

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/qvg.h"
 
@@ -120,8 +121,38 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Device address of this device's error word (looked up once per device).
+// Device address of the current device's error word (looked up once per
+// device, race-free), or NULL if the current device cannot be determined.
 int *device_error_word();
+
+// ---- per-device launch set-up -------------------------------------------
+// Everything a launch needs to know about the device is looked up once per
+// device (the device current on the calling host thread) and kept in tables
+// indexed by device number; each entry is published atomically, so first
+// calls may come from several host threads at once, and one process may
+// drive several devices.
+constexpr int kMaxDevices = 64;
+
+// Multiprocessor count of the current device (152 if it cannot be read).
+int sm_count_current();
+
+// Raises `func`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device: `done` is the call site's bit mask of devices
+// already set up (a function-local static at every call site).
+qvg_status smem_limit_once(std::atomic<uint64_t> &done, const void *func, int bytes);
+
+// Bound of the device-side waits of the kernels that the calling host thread
+// launches next (nanoseconds), and whether those launches add one wait on a
+// barrier that nothing arrives at (the bounded-wait test hook,
+// qvg_debug_set_wait in qvg.h).
+uint64_t wait_limit_ns();
+int wait_inject();
+
+// The argument checks of qvg_compress_chunk, in its order, without the
+// workspace: QVG_OK and the workspace the call needs (*ws_need), or the
+// first error.
+qvg_status check_compress_args(const qvg_params *p, const void *x_bf16, int N, const float *qsac_w,
+                               const float *psac_basis, const qvg_cache *cache, size_t *ws_need);
 
 // Launchers implemented in the kernel translation units.  All return a
 // qvg_status and only enqueue work on `st`.
@@ -138,9 +169,11 @@ qvg_status launch_kmeans_assign(const uint16_t *g, int N, int H, int d,
                                 int32_t *ids, cudaStream_t st);
 qvg_status launch_row_norms(const uint16_t *g, int N, int H, int d, const float *w, float *xnorm,
                             cudaStream_t st);
+// means (optional) [H][C][d]: the fp32 member means before the bf16
+// rounding (an empty cluster: its kept centroid).
 qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int d,
                                 const int32_t *ids, uint16_t *cent, size_t cent_head_stride, int Ce, int C,
-                                const float *w, float *cnorm, cudaStream_t st);
+                                const float *w, float *cnorm, float *means, cudaStream_t st);
 qvg_status launch_residual_quant(const void *xin, bool xin_f32, int N, int H, int d,
                                  const uint16_t *cent, size_t cent_head_stride, int C,
                                  const int32_t *ids, int bits, int group, int mode,

@@ -185,7 +185,8 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
                                                             int Ce, int Np, const float *__restrict__ cnorm,
                                                             int C, const float *__restrict__ w,
                                                             const float *__restrict__ xnorm,
-                                                            int32_t *__restrict__ ids, int *err) {
+                                                            int32_t *__restrict__ ids, int *err,
+                                                            uint64_t wait_ns, int inject) {
     constexpr int KB = D / 64;                       // 64-element K blocks
     constexpr int AB = KB * 128 * 128;               // one token tile
     constexpr int NA = P == 1 ? 3 : 2;               // token tile buffers
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
     uint8_t *Ax = As + NA * AB;                      // NA x extra K block of the tokens (4 KB)
     uint8_t *Bs = Ax + NA * 4096;                    // P x KB x [Np rows x 128 B]
     uint8_t *Bx = Bs + static_cast<size_t>(P) * KB * Np * 128;  // extra K block of the centroids
-    __shared__ uint64_t bar_mma[2], bar_a[NA], bar_drain;
+    __shared__ uint64_t bar_mma[2], bar_a[NA], bar_drain, bar_never;
     __shared__ uint32_t tmem_base;
     __shared__ float xs[kAssignGroups][128][2];  // each warp group's two best scores per row
     __shared__ int xk[kAssignGroups][128][2];    // ... and their clusters
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         umma::mbar_init(&bar_mma[0], 1);
         umma::mbar_init(&bar_mma[1], 1);
         umma::mbar_init(&bar_drain, 1);
+        umma::mbar_init(&bar_never, 1);  // nothing arrives: the bounded-wait test hook
         for (int i = 0; i < NA; ++i) umma::mbar_init(&bar_a[i], 2 * kAssignThreads);
         umma::fence_barrier_init();
     }
@@ -348,12 +350,16 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
     };
     bool ok = true;
     if (tid == 0 && my_tiles > 0) {
-        if (umma::mbar_wait(&bar_a[0], 0, kWaitNs)) {
+        if (umma::mbar_wait(&bar_a[0], 0, wait_ns)) {
             umma::tc_fence_after();
             issue(0);
         } else {
             ok = false;
         }
+        // test hook: with tile 0's MMA in flight, wait on a barrier that
+        // nothing completes, so that the bound runs out and the drain below
+        // has an MMA to wait for
+        if (ok && inject && !umma::mbar_wait(&bar_never, 0, wait_ns)) ok = false;
     }
     ok = __syncthreads_and(ok);
     for (int k = 0; ok && k < my_tiles; ++k) {
@@ -362,7 +368,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         // (1) with three buffers, tile k+1 is already loaded: start its MMA now
         // (its accumulator's previous tile, k-1, ended at the last barrier)
         if (NA == 3 && tid == 0 && k + 1 < my_tiles) {
-            if (umma::mbar_wait(&bar_a[(k + 1) % NA], ((k + 1) / NA) & 1, kWaitNs)) {
+            if (umma::mbar_wait(&bar_a[(k + 1) % NA], ((k + 1) / NA) & 1, wait_ns)) {
                 umma::tc_fence_after();
                 issue(k + 1);
             } else {
@@ -372,7 +378,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         // (2) refill the buffer of tile k - 1 (its epilogue ended at the last barrier)
         if (k + NA - 1 < my_tiles) load_tile(k + NA - 1);
         // (3) epilogue of tile k
-        if (!umma::mbar_wait(&bar_mma[k & 1], (k >> 1) & 1, kWaitNs)) ok = false;
+        if (!umma::mbar_wait(&bar_mma[k & 1], (k >> 1) & 1, wait_ns)) ok = false;
         ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
         umma::tc_fence_after();
         const int r = (warp & 3) * 32 + lane;
@@ -508,7 +514,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         }
         // (4) with two buffers, tile k+1's loads were issued in (2): start its MMA
         if (NA == 2 && tid == 0 && k + 1 < my_tiles) {
-            if (umma::mbar_wait(&bar_a[(k + 1) % NA], ((k + 1) / NA) & 1, kWaitNs)) {
+            if (umma::mbar_wait(&bar_a[(k + 1) % NA], ((k + 1) / NA) & 1, wait_ns)) {
                 umma::tc_fence_after();
                 issue(k + 1);
             } else {
@@ -519,8 +525,19 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         ok = __syncthreads_and(ok);
         umma::tc_fence_after();
     }
-    if (!ok && tid == 0) raise_error(err, QVG_ERR_TIMEOUT);
-    // every MMA issued by thread 0 completes before TMEM is released
+    if (!ok) {
+        // a wait ran out and the assignment is incomplete: every row of this
+        // CTA's tiles gets cluster 0, so that the kernels after this one read
+        // valid ids (the call's results are undefined; its status is TIMEOUT)
+        if (tid == 0) raise_error(err, QVG_ERR_TIMEOUT);
+        for (int k = 0; k < my_tiles; ++k)
+            for (int r = tid; r < 128; r += kAssignThreads) {
+                const int n = (t0 + k * tstep) * 128 + r;
+                if (n < N) ids[static_cast<size_t>(h) * N + n] = 0;
+            }
+    }
+    // every MMA issued by thread 0 completes before TMEM is released (at the
+    // default bound, whatever the pipeline's waits were given)
     if (tid == 0 && my_tiles > 0) {
         umma::mma_commit(&bar_drain);
         umma::mbar_wait(&bar_drain, 0, kWaitNs);
@@ -595,7 +612,8 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
                                                               const int32_t *__restrict__ ids,
                                                               uint16_t *__restrict__ cent, size_t hs, int Ce,
                                                               const float *__restrict__ w,
-                                                              float *__restrict__ cnorm, int C) {
+                                                              float *__restrict__ cnorm, int C,
+                                                              float *__restrict__ means) {
     constexpr int W = kUpdThreads / 32;
     constexpr int E = D / 32;
     extern __shared__ __align__(16) uint16_t order[];          // [N] token indices, by cluster
@@ -609,10 +627,12 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
     pdl_wait();  // the assignment that wrote ids has finished
     pdl_trigger();
     __syncthreads();
-    // pass 1: per-warp counts
+    // pass 1: per-warp counts (an id outside [0, Ce) -- which the assignment
+    // never writes -- counts as no member, so no access leaves the tables)
     for (int b0 = n_beg; b0 < n_end; b0 += 32) {
         const int n = b0 + lane;
-        const int c = n < n_end ? hid[n] : -1;
+        int c = n < n_end ? hid[n] : -1;
+        c = static_cast<unsigned>(c) < static_cast<unsigned>(Ce) ? c : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, c);
         if (c >= 0 && (peers & ((1u << lane) - 1u)) == 0) wc[warp][c] += __popc(peers);
         __syncwarp();
@@ -656,7 +676,8 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
     // pass 3: placement in token order
     for (int b0 = n_beg; b0 < n_end; b0 += 32) {
         const int n = b0 + lane;
-        const int c = n < n_end ? hid[n] : -1;
+        int c = n < n_end ? hid[n] : -1;
+        c = static_cast<unsigned>(c) < static_cast<unsigned>(Ce) ? c : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, c);
         const unsigned before = peers & ((1u << lane) - 1u);
         if (c >= 0) order[cnt[c] + wc[warp][c] + __popc(before)] = static_cast<uint16_t>(n);
@@ -681,7 +702,9 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
         float nrm = 0.0f;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-            const uint16_t cb = f32_to_bf16(__fdiv_rn(acc[e], cntf));
+            const float mean = __fdiv_rn(acc[e], cntf);
+            if (means) means[(static_cast<size_t>(h) * C + c) * D + lane * E + e] = mean;
+            const uint16_t cb = f32_to_bf16(mean);
             row[e] = cb;
             const float cv = bf16_to_f32(cb);
             const float wj = w ? w[h * D + lane * E + e] : 1.0f;
@@ -690,6 +713,14 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
         for (int o = 16; o > 0; o >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o);
         if (lane == 0) cnorm[h * C + c] = nrm;
     };
+    if (means) {  // an empty cluster keeps its centroid: that is its fp32 value too
+        for (int i = tid; i < (c_hi - c_lo) * D; i += kUpdThreads) {
+            const int c = c_lo + i / D, j = i % D;
+            if (cnt[c + 1] == cnt[c])
+                means[(static_cast<size_t>(h) * C + c) * D + j] =
+                    bf16_to_f32(cent[static_cast<size_t>(h) * hs + static_cast<size_t>(c) * D + j]);
+        }
+    }
     int split_c = -1;  // a cluster that starts in this run and goes on after it
     if (a < b) {
         int c = c_lo;
@@ -805,7 +836,10 @@ __global__ void __launch_bounds__(256) k_residual_quant(
     const int h = static_cast<int>(wid / nblk), n = static_cast<int>(wid % nblk) * 32 + lane;
     if (n >= N) return;
     const int ng = D / group, g8 = group / 8;  // groups per row, 8-channel blocks per group
-    const int id = C > 0 ? ids[static_cast<size_t>(h) * N + n] : 0;
+    // (an id outside [0, C) never comes from the assignment; clamped so that
+    // no access leaves the centroid table)
+    const unsigned uid = C > 0 ? static_cast<unsigned>(ids[static_cast<size_t>(h) * N + n]) : 0u;
+    const int id = uid < static_cast<unsigned>(C) ? static_cast<int>(uid) : max(C - 1, 0);
     const size_t trow = static_cast<size_t>(n) * H + h;  // token-major row of the stage buffers
     const TIn *xr = xin + trow * D;
     const uint16_t *cr = C > 0 ? cent + static_cast<size_t>(h) * hs + static_cast<size_t>(id) * D : nullptr;
@@ -1026,16 +1060,7 @@ __global__ void k_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start,
 // ---------------------------------------------------------------------------
 // Launchers.
 
-static int sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 152;
-    }
-    return n;
-}
+static int sm_count() { return sm_count_current(); }
 
 qvg_status launch_kmeans_init(const uint16_t *g, int N, int H, int d, int C, int Ce, uint64_t seed,
                               int chunk, int stage, uint16_t *cent, size_t hs, const float *w, float *cnorm,
@@ -1072,20 +1097,14 @@ static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t
     constexpr int KB = D / 64, NA = P == 1 ? 3 : 2;
     const size_t smem = NA * (static_cast<size_t>(KB) * 128 * 128 + 4096) + static_cast<size_t>(P) * KB * Np * 128 +
                         static_cast<size_t>(Np) * 32 + 1024;
-    static bool attr = false;
-    if (!attr) {
-        // the largest request of this instantiation (Np = 256)
+    {
+        // the largest request of this instantiation (Np = 256), once per device
+        static std::atomic<uint64_t> done{0};
         const size_t most = NA * (static_cast<size_t>(KB) * 128 * 128 + 4096) +
                             static_cast<size_t>(P) * KB * QVG_MAX_CLUSTERS * 128 + QVG_MAX_CLUSTERS * 32 + 1024;
-        const cudaError_t e = cudaFuncSetAttribute(k_kmeans_assign_tc<D, P>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(most));
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            note_cuda_error(e);
-            return QVG_ERR_CUDA;
-        }
-        attr = true;
+        const qvg_status s = smem_limit_once(done, reinterpret_cast<const void *>(k_kmeans_assign_tc<D, P>),
+                                             static_cast<int>(most));
+        if (s != QVG_OK) return s;
     }
     // one CTA per SM in total, spread over the heads; each walks
     // ceil(tiles / ctas_per_head) token tiles of its head
@@ -1093,7 +1112,8 @@ static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t
     const int per_head = std::max(1, std::min(n_tiles, sm_count() / std::max(1, H)));
     dim3 grid(per_head, H);
     const cudaError_t e = launch_pdl(k_kmeans_assign_tc<D, P>, grid, dim3(kAssignThreads), smem, st, g, N, H, cent,
-                                     hs, Ce, Np, cnorm, C, w, xnorm, ids, device_error_word());
+                                     hs, Ce, Np, cnorm, C, w, xnorm, ids, device_error_word(), wait_limit_ns(),
+                                     wait_inject());
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         note_cuda_error(e);
@@ -1163,24 +1183,18 @@ qvg_status launch_row_norms(const uint16_t *g, int N, int H, int d, const float 
 
 qvg_status launch_kmeans_update(const void *xin, bool xin_f32, int N, int H, int d,
                                 const int32_t *ids, uint16_t *cent, size_t hs, int Ce, int C, const float *w,
-                                float *cnorm, cudaStream_t st) {
+                                float *cnorm, float *means, cudaStream_t st) {
     const size_t smem = static_cast<size_t>(N) * sizeof(uint16_t);
     dim3 grid(update_splits(H, sm_count()), H);
 #define QVG_UPD(D_, T_)                                                                                     \
     do {                                                                                                    \
-        static bool attr = false;                                                                           \
-        if (!attr) {                                                                                        \
-            const cudaError_t e = cudaFuncSetAttribute(k_kmeans_update<D_, T_>,                             \
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 131072); \
-            if (e != cudaSuccess) {                                                                         \
-                (void)cudaGetLastError();                                                                   \
-                note_cuda_error(e);                                                                         \
-                return QVG_ERR_CUDA;                                                                        \
-            }                                                                                               \
-            attr = true;                                                                                    \
-        }                                                                                                   \
+        static std::atomic<uint64_t> done{0};                                                               \
+        const qvg_status as = smem_limit_once(done, reinterpret_cast<const void *>(k_kmeans_update<D_, T_>), \
+                                              131072);                                                      \
+        if (as != QVG_OK) return as;                                                                        \
         const cudaError_t le = launch_pdl(k_kmeans_update<D_, T_>, grid, dim3(kUpdThreads), smem, st,        \
-                                          static_cast<const T_ *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C); \
+                                          static_cast<const T_ *>(xin), N, H, ids, cent, hs, Ce, w, cnorm, C, \
+                                          means);                                                           \
         if (le != cudaSuccess) {                                                                            \
             (void)cudaGetLastError();                                                                       \
             note_cuda_error(le);                                                                            \

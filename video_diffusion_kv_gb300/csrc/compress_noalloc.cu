@@ -54,9 +54,9 @@ qvg_status scratch_for_current_device(void **out) {
 extern "C" qvg_status qvg_compress_chunk_noalloc(const qvg_params *p, const void *x_bf16, int32_t N,
                                                  const float *qsac_w, const float *psac_basis,
                                                  qvg_cache *cache, void *stream) {
-    if (!p || !cache) return QVG_ERR_INVALID_ARG;
+    // argument, capacity and size errors first, in qvg_compress_chunk's order
     size_t need = 0;
-    qvg_status s = qvg_workspace_size(p, QVG_OP_COMPRESS, N, cache->H, cache->d, cache->H, &need);
+    qvg_status s = qvg::check_compress_args(p, x_bf16, N, qsac_w, psac_basis, cache, &need);
     if (s != QVG_OK) return s;
     if (need > kScratchBytes) return QVG_ERR_WORKSPACE;  // beyond the fixed scratch: use qvg_compress_chunk
     void *scratch = nullptr;

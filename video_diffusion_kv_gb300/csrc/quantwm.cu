@@ -238,18 +238,12 @@ __global__ void __launch_bounds__(512) k_psac_jacobi(const float *__restrict__ M
 qvg_status launch_psac_basis(const float *M, const int64_t *count, int H, int d, int rank, float *U,
                              float *eig, float *frac, cudaStream_t st) {
     const size_t smem = (2 * static_cast<size_t>(d) * d + d) * sizeof(float) + d * sizeof(int);
-    static bool attr = false;
-    if (!attr) {
+    {
+        static std::atomic<uint64_t> done128{0}, done64{0};
         const int most = static_cast<int>((2 * JD * JD + JD) * sizeof(float) + JD * sizeof(int));
-        cudaError_t e = cudaFuncSetAttribute(k_psac_jacobi<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_psac_jacobi<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            note_cuda_error(e);
-            return QVG_ERR_CUDA;
-        }
-        attr = true;
+        qvg_status s = smem_limit_once(done128, reinterpret_cast<const void *>(k_psac_jacobi<128>), most);
+        if (s == QVG_OK) s = smem_limit_once(done64, reinterpret_cast<const void *>(k_psac_jacobi<64>), most);
+        if (s != QVG_OK) return s;
     }
     if (d == 128)
         k_psac_jacobi<128><<<H, 512, smem, st>>>(M, count, rank, U, eig, frac);
