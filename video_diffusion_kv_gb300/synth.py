@@ -13,7 +13,8 @@ rollout.  Value structure: token-varying outlier channels with max|K|~1e2 and
 max|V|~1e3 (QVG notes, "core tension"), spatio-temporally correlated
 prototypes (QVG notes, "entry angle": neighbouring frames and patches hold
 similar tokens), and history queries whose energy sits in 8 directions
-(QuantWM write-up, PSAC: top-8 directions hold >71% of query energy).
+(QuantWM write-up, PSAC: top-8 directions hold >71% of query energy) on a
+quarter of the channels (QSAC: queries are more active on some channels).
 
 Every array is float32 holding bf16-representable values, layout
 [tokens, heads, head_dim] (token-major, tokens in raster order
@@ -178,13 +179,28 @@ def queries(w: Workload, seed: int, chunk: int) -> np.ndarray:
     return bf16_values(x)
 
 
+ACTIVE_FRACTION = 4  # 1 / ACTIVE_FRACTION of the channels carry the planted directions
+
+
+def active_channels(w: Workload, seed: int) -> np.ndarray:
+    """The d / 4 channels of each KV head that the queries are most active on
+    ([H, d/4], sorted): the QuantWM write-up's QSAC measures how active the
+    history queries are on each channel, i.e. which channels they care about
+    more, so the channels are not all alike."""
+    g = _rng(seed, KIND_QHIST, 4243)
+    n = w.d // ACTIVE_FRACTION
+    return np.stack([np.sort(g.permutation(w.d)[:n]) for _ in range(w.H)])
+
+
 def planted_basis(w: Workload, seed: int) -> np.ndarray:
-    """Random orthonormal directions u_1..u_8 per KV head: [H, d, 8]."""
+    """Random orthonormal directions u_1..u_8 per KV head, supported on that
+    head's active channels: [H, d, 8]."""
     g = _rng(seed, KIND_QHIST, 4242)
-    out = np.empty((w.H, w.d, 8), np.float64)
+    act = active_channels(w, seed)
+    out = np.zeros((w.H, w.d, 8), np.float64)
     for h in range(w.H):
-        qm, _ = np.linalg.qr(g.standard_normal((w.d, 8)))
-        out[h] = qm
+        qm, _ = np.linalg.qr(g.standard_normal((act.shape[1], 8)))
+        out[h, act[h]] = qm
     return out
 
 
@@ -200,7 +216,9 @@ def planted_spectrum(d: int, energy_in_span: float = 0.70, ratio: float = 0.8):
 
 def history_queries(w: Workload, seed: int, n_tokens: int = None, stream: int = 0) -> np.ndarray:
     """Queries q = sum_r a_r u_r + isotropic noise, a_r ~ N(0, lambda_r):
-    70% of the expected energy in the 8 planted directions.  [n, Hq, d]."""
+    70% of the expected energy in the 8 planted directions, which live on a
+    quarter of the channels, so those channels' mean q_j^2 is
+    0.7 * 4 + 0.3 = 3.1 against 0.3 elsewhere.  [n, Hq, d]."""
     if n_tokens is None:
         n_tokens = w.hist_frames * w.frame_hw[0] * w.frame_hw[1]
     U = planted_basis(w, seed)
