@@ -250,14 +250,22 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ own arm
 
-def launches_per_compress(p):
-    """Kernels one qvg_compress_chunk call launches (see csrc/api.cu)."""
-    per_stage = 1  # residual quantise (+ pack, stage residual, PSAC)
-    if p.C > 0:
-        # row norms, init with norms (or norms of given centroids), iters x (assign, update),
-        # final assign
-        per_stage += 1 + 1 + 2 * p.iters + 1
-    return per_stage * p.L + 1  # + chunk table
+def launches_per_compress(p, fused_first_stage=True):
+    """Kernels one qvg_compress_chunk call launches (see csrc/api.cu): per
+    stage the residual quantiser, and with centroids the init; the first
+    stage without QSAC weights runs all Lloyd iterations in one cluster
+    launch, the others launch row norms, iters x (assign, update) and the
+    final assignment."""
+    n = 1  # chunk table
+    for l in range(p.L):
+        n += 1  # residual quantise (+ pack, stage residual, PSAC)
+        if p.C > 0:
+            n += 1  # init (or the norms of given centroids)
+            if l == 0 and fused_first_stage and not p.flags & 1:
+                n += 1
+            else:
+                n += 1 + 2 * p.iters + 1
+    return n
 
 
 def kernel_extras(qvg, p, w, kc, vc, q, k_raw, flush, dev, last, slots_per_chunk, reps=5):
@@ -499,6 +507,17 @@ def run_own(args):
         "wall_s_timed": t_wall,
         "peaks_source": peak_src,
     }
+    if not args.no_configs:
+        # the other configurations of the workload list, measured on the same GPU after the timed steps
+        cfgs = {}
+        for name, fn in (("tiny", measure_tiny), ("qvgpro", measure_qvgpro), ("quantwm", measure_quantwm),
+                         ("rollout", measure_rollout)):
+            t0 = time.perf_counter()
+            cfgs[name] = fn(qvg, synth, flush, peaks, dev)
+            cfgs[name]["bench_wall_s"] = time.perf_counter() - t0
+            torch.cuda.empty_cache()
+        line["configs"] = cfgs
+        line["device_status_after_configs"] = int(qvg.get_status())
     if ws == 1 and not args.no_cpu_baseline:
         t_full, thr, desc, _ = oracle_step_sample(w, seed=seed)
         line["cpu_baseline"] = {"value": w.Nq / t_full, "unit": UNIT, "cores": thr, "kind": "oracle",
@@ -514,135 +533,318 @@ def _rel(x, y):
     return float(np.linalg.norm((x - y).astype(np.float64)) / np.linalg.norm(x.astype(np.float64)))
 
 
-def study_qvgpro(args):
-    """QVG-Pro on the tiny shapes: INT2 G=32 with L = 1, 2, 3 and INT4 G=32
-    with L = 1, 2; relative Frobenius error of K and V after each stage count
-    and the compression ratio counting codes, fp16 scales, ids and bf16
-    centroids."""
+def _timer(flush, reps=5, warm=2):
+    """Median CUDA-event time (ms) of fn() on the current stream, L2 flushed
+    before each timed call (outside the events); before() runs untimed."""
     import torch
 
-    import __graft_entry__
-    __graft_entry__.build()
-    import video_diffusion_kv_gb300 as qvg
-    from video_diffusion_kv_gb300 import synth
+    def timed(fn, before=None):
+        ts = []
+        for rep in range(warm + reps):
+            if before:
+                before()
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if rep >= warm:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+    return timed
+
+
+def _rates(nbytes=None, flops=None, ms=None, peaks=None):
+    """Throughput of one timed call and its fractions of the measured HBM and
+    dense 16-bit tensor peaks."""
+    out = {"ms": ms}
+    if nbytes is not None:
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out.update({"bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]})
+    if flops is not None:
+        tf = flops / (ms / 1e3) / 1e12
+        out.update({"flops": flops, "TFLOP/s": tf, "frac_tensor": tf / peaks["bf16_tflops"]})
+    return out
+
+
+def _compress_counts(w, p, N=None):
+    """Algorithmic bytes (bf16 input read, compressed rows written) and the
+    distance-GEMM flops of compressing one chunk of K and one of V."""
+    N = N or w.N
+    nb, ng = w.d * p.bits // 8, w.d // p.group
+    row = nb + 2 * ng + (1 if p.C > 0 else 0)
+    in_b = 2 * N * w.H * w.d * 2
+    out_b = 2 * p.L * (N * w.H * row + w.H * p.C * w.d * 2)
+    flops = 2 * p.L * 2.0 * N * min(p.C, N) * w.d * (p.iters + 1) * w.H
+    return in_b + out_b, flops
+
+
+def _cache_read_bytes(w, p, n_tokens):
+    nb, ng = w.d * p.bits // 8, w.d // p.group
+    row = nb + 2 * ng + (1 if p.C > 0 else 0)
+    n_chunks = -(-n_tokens // w.N)
+    return 2 * p.L * (n_tokens * w.H * row + n_chunks * w.H * p.C * w.d * 2)
+
+
+def measure_tiny(qvg, synth, flush, peaks, dev="cuda"):
+    """Config 1: 2 heads, d=64, 4 chunks x 256 tokens, C=16, INT2 G=32, 10
+    Lloyd iterations; 256 queries over the 1024 cached tokens."""
+    import torch
+    w = synth.WORKLOADS["tiny"]
+    seed = 31
+    p = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=seed)
+    per = -(-w.N // 128) * 128
+    kc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks, device=dev)
+    vc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks, device=dev)
+    kd = [synth_dev(synth.chunk_kv(w, seed, k, synth.KIND_K), dev) for k in range(w.n_chunks)]
+    vd = [synth_dev(synth.chunk_kv(w, seed, k, synth.KIND_V), dev) for k in range(w.n_chunks)]
+    ws = torch.empty(qvg.workspace_size(p, qvg.QVG_OP_COMPRESS, w.N, w.H, w.d), dtype=torch.uint8, device=dev)
+    for k in range(w.n_chunks):
+        qvg.compress_chunk(p, kd[k], kc, workspace=ws)
+        qvg.compress_chunk(p, vd[k], vc, workspace=ws)
+    last = w.n_chunks - 1
+    q = synth_dev(synth.queries(w, seed, w.n_chunks), dev)
+    out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    timed = _timer(flush)
+
+    def rewind():
+        kc.reset(last, last * per)
+        vc.reset(last, last * per)
+
+    def comp():
+        qvg.compress_chunk(p, kd[last], kc, workspace=ws)
+        qvg.compress_chunk(p, vd[last], vc, workspace=ws)
+
+    ms_c = timed(comp, rewind)
+    nbytes, flops = _compress_counts(w, p)
+    ms_a = timed(lambda: qvg.attention(p, q, kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out))
+    dall = torch.empty((kc.n_tokens, w.H, w.d), dtype=torch.float32, device=dev)
+    ms_d = timed(lambda: qvg.decompress(p, kc, 0, kc.n_tokens, out=dall))
+    return {"workload": "tiny: 2 KV heads, d=64, 4 chunks x 256 tokens, C=16, INT2 G=32, 10 Lloyd iters",
+            "compress_KV_newest": dict(_rates(nbytes, flops, ms_c, peaks), what="K and V of one 256-token chunk; "
+                                       "launch-bound (report absolute time)"),
+            "attention": dict(_rates(_cache_read_bytes(w, p, w.tokens), 4.0 * w.Nq * w.tokens * w.d * w.Hq, ms_a, peaks),
+                              **{"tok/s": w.Nq / (ms_a / 1e3), "what": "256 queries over 1024 cached tokens"}),
+            "decompress_f32_cache": _rates(_cache_read_bytes(w, p, w.tokens) / 2 + kc.n_tokens * w.H * w.d * 4,
+                                           None, ms_d, peaks),
+            "ratio": qvg.compression_ratio(p, w.H, w.d, w.N, w.n_chunks)}
+
+
+def measure_qvgpro(qvg, synth, flush, peaks, dev="cuda"):
+    """Config 3, QVG-Pro on the tiny shapes: INT2 G=32 with L = 1, 2, 3 and
+    INT4 G=32 with L = 1, 2; relative Frobenius error of K and V after each
+    stage count, the compression ratio counting codes, fp16 scales, ids and
+    bf16 centroids, and the compress / attention times."""
+    import numpy as np
+    import torch
     w = synth.WORKLOADS["qvgpro"]
+    seed = 5
+    per = -(-w.N // 128) * 128
+    timed = _timer(flush)
+    xs = {kind: [synth.chunk_kv(w, seed, k, kind) for k in range(w.n_chunks)] for kind in (synth.KIND_K, synth.KIND_V)}
+    xd = {kind: [synth_dev(x, dev) for x in xs[kind]] for kind in xs}
+    q = synth_dev(synth.queries(w, seed, w.n_chunks), dev)
+    out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
     arms = []
     for bits, stages in ((2, 3), (4, 2)):
         for L in range(1, stages + 1):
-            p = qvg.Params(C=w.C, L=L, bits=bits, group=w.group, iters=w.iters, seed=5)
+            p = qvg.Params(C=w.C, L=L, bits=bits, group=w.group, iters=w.iters, seed=seed)
+            cs = {}
             errs = {}
+            ws = torch.empty(qvg.workspace_size(p, qvg.QVG_OP_COMPRESS, w.N, w.H, w.d), dtype=torch.uint8, device=dev)
             for kind, name in ((synth.KIND_K, "K"), (synth.KIND_V, "V")):
-                c = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * 256, w.n_chunks)
-                xs = [synth.chunk_kv(w, 5, k, kind) for k in range(w.n_chunks)]
-                for x in xs:
-                    qvg.compress_chunk(p, synth_dev(x, "cuda"), c)
+                c = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks, device=dev)
+                for x in xd[kind]:
+                    qvg.compress_chunk(p, x, c, workspace=ws)
                 xh = qvg.decompress(p, c, 0, c.n_tokens).cpu().numpy()
-                import numpy as np
-                errs[name] = _rel(np.concatenate(xs, 0), xh)
+                errs[name] = _rel(np.concatenate(xs[kind], 0), xh)
+                cs[name] = c
+            last = w.n_chunks - 1
+
+            def rewind():
+                for c in cs.values():
+                    c.reset(last, last * per)
+
+            def comp():
+                qvg.compress_chunk(p, xd[synth.KIND_K][last], cs["K"], workspace=ws)
+                qvg.compress_chunk(p, xd[synth.KIND_V][last], cs["V"], workspace=ws)
+
+            ms_c = timed(comp, rewind)
+            ms_a = timed(lambda: qvg.attention(p, q, cs["K"], cs["V"], out_dtype=qvg.QVG_OUT_BF16, out=out))
             rtn = qvg.Params(C=0, L=1, bits=bits, group=w.group, iters=0)
+            nbytes, flops = _compress_counts(w, p)
             arms.append({"bits": bits, "stages": L, "rel_err_K": errs["K"], "rel_err_V": errs["V"],
-                         "ratio": qvg.compression_ratio(p, w.H, w.d, 256, w.n_chunks),
-                         "ratio_rtn_same_bits": qvg.compression_ratio(rtn, w.H, w.d, 256, w.n_chunks)})
-    print(json.dumps({"study": "qvgpro", "workload": "2 heads, d=64, 4 chunks x 256 tokens, C=16, G=32, 10 iters",
-                      "arms": arms}), flush=True)
-    return 0
+                         "ratio": qvg.compression_ratio(p, w.H, w.d, w.N, w.n_chunks),
+                         "ratio_rtn_same_bits": qvg.compression_ratio(rtn, w.H, w.d, w.N, w.n_chunks),
+                         "compress_KV_newest": _rates(nbytes, flops, ms_c, peaks),
+                         "attention": _rates(_cache_read_bytes(w, p, w.tokens), 4.0 * w.Nq * w.tokens * w.d * w.Hq,
+                                             ms_a, peaks)})
+    return {"workload": "QVG-Pro on the tiny shapes: 2 heads, d=64, 4 chunks x 256 tokens, C=16, G=32, 10 iters",
+            "arms": arms}
 
 
-def study_quantwm(args):
-    """QuantWM world-model cache: 24 heads, d=128, 8 chunks of 3 frames of
-    22x40 (21,120 tokens).  History queries (4 frames) give the QSAC weights
-    and the PSAC basis; the top-1 attention-token shift rate of an 880-token
-    query frame is measured against the oracle's argmax over the bf16 cache
-    for the arms QVG, +QSAC, +PSAC and both."""
+def measure_quantwm(qvg, synth, flush, peaks, dev="cuda", nthreads=None):
+    """Config 4, the QuantWM world-model cache: 24 heads, d=128, 8 chunks of
+    3 frames of 22x40 (21,120 tokens), C=256, INT2 G=64, 8 iterations.
+    History queries (4 frames) give the QSAC weights and the PSAC basis; the
+    top-1 attention-token shift rate of an 880-token query frame (the GPU's
+    top-1 over the compressed cache) is measured against the oracle's argmax
+    over the bf16 cache for the arms QVG, +QSAC, +PSAC and both."""
     import numpy as np
     import torch
 
-    import __graft_entry__
-    __graft_entry__.build()
     import oracle
-    import video_diffusion_kv_gb300 as qvg
-    from video_diffusion_kv_gb300 import synth
     w = synth.WORKLOADS["quantwm"]
     seed = 7
-    qh = synth_dev(synth.history_queries(w, seed), "cuda")
+    timed = _timer(flush)
+    qh = synth_dev(synth.history_queries(w, seed), dev)
     M, wq, cnt = qvg.query_stats(qh, w.H)
     U, eig, frac = qvg.psac_basis(M, cnt)
+    ms_stats = timed(lambda: qvg.query_stats(qh, w.H, M=M, w=wq, count=cnt))
+    ms_basis = timed(lambda: qvg.psac_basis(M, cnt))
+    wh = wq.cpu().numpy()
+    act = synth.active_channels(w, seed)
+    on = np.zeros(wh.shape, bool)
+    for h in range(w.H):
+        on[h, act[h]] = True
     ks = [synth.chunk_kv(w, seed, k, synth.KIND_K) for k in range(w.n_chunks)]
     vs = [synth.chunk_kv(w, seed, k, synth.KIND_V) for k in range(w.n_chunks)]
-    qf = synth.history_queries(w, seed, n_tokens=880, stream=1)
+    kd = [synth_dev(x, dev) for x in ks]
+    vd = [synth_dev(x, dev) for x in vs]
+    qf = synth.history_queries(w, seed, n_tokens=w.Nq, stream=1)
+    qfd = synth_dev(qf, dev)
     kall = np.concatenate(ks, 0)
-    ref = oracle.top1(qf, kall, nthreads=os.cpu_count() or 1)     # [Hq, Nq] token indices
+    t0 = time.perf_counter()
+    ref = oracle.top1(qf, kall, nthreads=nthreads or os.cpu_count() or 1)  # [Hq, Nq] token indices
+    t_oracle = time.perf_counter() - t0
+    per = -(-w.N // 128) * 128
+    keep = np.concatenate([np.arange(k * per, k * per + w.N) for k in range(w.n_chunks)])
     arms = {}
     for name, flags in (("QVG", 0), ("QSAC", qvg.QVG_QSAC), ("PSAC", qvg.QVG_PSAC),
                         ("QSAC+PSAC", qvg.QVG_QSAC | qvg.QVG_PSAC)):
         p = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=seed, flags=flags)
         pv = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=seed)
-        cap = w.n_chunks * (-(-w.N // 128) * 128)
-        kc = qvg.CompressedKV(p, w.H, w.d, cap, w.n_chunks)
-        vc = qvg.CompressedKV(pv, w.H, w.d, cap, w.n_chunks)
+        kc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks, device=dev)
+        vc = qvg.CompressedKV(pv, w.H, w.d, w.n_chunks * per, w.n_chunks, device=dev)
+        ws = torch.empty(qvg.workspace_size(p, qvg.QVG_OP_COMPRESS, w.N, w.H, w.d), dtype=torch.uint8, device=dev)
         for k in range(w.n_chunks):
-            qvg.compress_chunk(p, synth_dev(ks[k], "cuda"), kc, qsac_w=wq, psac_basis=U)
-            qvg.compress_chunk(pv, synth_dev(vs[k], "cuda"), vc)
-        _, _, top1 = qvg.attention(p, synth_dev(qf, "cuda"), kc, vc, want_top1=True)
+            qvg.compress_chunk(p, kd[k], kc, qsac_w=wq, psac_basis=U, workspace=ws)
+            qvg.compress_chunk(pv, vd[k], vc, workspace=ws)
+        _, _, top1 = qvg.attention(p, qfd, kc, vc, want_top1=True)
         slots = top1.cpu().numpy()
-        # slot -> token index (chunks start at multiples of 128 slots)
-        per = -(-w.N // 128) * 128
-        tok = (slots // per) * w.N + slots % per
+        tok = (slots // per) * w.N + slots % per  # slot -> token index
         kh = qvg.decompress(p, kc, 0, kc.n_tokens).cpu().numpy()
-        keep = np.concatenate([np.arange(k * per, k * per + w.N) for k in range(w.n_chunks)])
+        last = w.n_chunks - 1
+
+        def rewind():
+            kc.reset(last, last * per)
+            vc.reset(last, last * per)
+
+        def comp():
+            qvg.compress_chunk(p, kd[last], kc, qsac_w=wq, psac_basis=U, workspace=ws)
+            qvg.compress_chunk(pv, vd[last], vc, workspace=ws)
+
+        ms_c = timed(comp, rewind)
+        ms_a = timed(lambda: qvg.attention(p, qfd, kc, vc))
+        nbytes, flops = _compress_counts(w, p)
         arms[name] = {"shift_rate": float((tok != ref).mean()),
                       "rel_err_K": _rel(kall, kh[keep]),
                       "ratio_K": qvg.compression_ratio(p, w.H, w.d, w.N, w.n_chunks,
-                                                      with_psac=bool(flags & qvg.QVG_PSAC))}
-    print(json.dumps({"study": "quantwm", "workload": "24 heads, d=128, 8 chunks x 2640 tokens, C=256, INT2 G=64, 8 iters; 880 query tokens",
-                      "energy_frac_top8": [float(x) for x in frac.cpu().numpy()[:4]],
-                      "energy_frac_mean": float(frac.mean().item()), "arms": arms}), flush=True)
-    return 0
+                                                      with_psac=bool(flags & qvg.QVG_PSAC)),
+                      "compress_KV_newest": _rates(nbytes, flops * (2 if flags & qvg.QVG_QSAC else 1), ms_c, peaks),
+                      "attention": dict(_rates(_cache_read_bytes(w, p, w.tokens),
+                                               4.0 * w.Nq * w.tokens * w.d * w.Hq, ms_a, peaks),
+                                        **{"tok/s": w.Nq / (ms_a / 1e3)})}
+        del kc, vc
+    return {"workload": "QuantWM: 24 heads, d=128, 8 chunks x 2640 tokens (21,120), C=256, INT2 G=64, 8 iters; "
+                        "880 query tokens; shift rate = GPU top-1 over the compressed cache vs the oracle's "
+                        "argmax over the bf16 cache",
+            "qsac_weight": {"active_channels_mean": float(wh[on].mean()), "other_channels_mean": float(wh[~on].mean()),
+                            "min": float(wh.min()), "max": float(wh.max())},
+            "energy_frac_top8_mean": float(frac.mean().item()),
+            "query_stats_ms": ms_stats, "psac_basis_ms": ms_basis,
+            "oracle_top1_s": t_oracle, "arms": arms}
 
 
-def study_rollout(args):
-    """One-minute rollout: 288 frames of 30x52 streamed in 96 chunks of 4680
-    tokens, 8 heads, d=128, INT2 C=256.  After compressing each chunk its
-    4680 queries attend over the whole compressed cache; attention time is
-    reported against the cache length.  Chunks are drawn from the stationary
+def measure_rollout(qvg, synth, flush, peaks, dev="cuda"):
+    """Config 5, the one-minute rollout: 288 frames of 30x52 streamed in 96
+    chunks of 4680 tokens (449,280), 8 heads, d=128, INT2 C=256 G=64, 8
+    iterations.  After compressing each chunk its 4680 queries attend over
+    the whole compressed cache.  Chunks are drawn from the stationary
     16-prototype mixture; 12 distinct chunks are generated and cycled."""
     import torch
-
-    import __graft_entry__
-    __graft_entry__.build()
-    import video_diffusion_kv_gb300 as qvg
-    from video_diffusion_kv_gb300 import synth
     w = synth.WORKLOADS["rollout"]
-    p = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=9)
+    seed = 9
+    p = qvg.Params(C=w.C, L=1, bits=w.bits, group=w.group, iters=w.iters, seed=seed)
     per = -(-w.N // 128) * 128
-    kc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks)
-    vc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks)
+    kc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks, device=dev)
+    vc = qvg.CompressedKV(p, w.H, w.d, w.n_chunks * per, w.n_chunks, device=dev)
     uniq = 12
-    K = [synth_dev(synth.chunk_kv(w, 9, k, synth.KIND_K), "cuda") for k in range(uniq)]
-    V = [synth_dev(synth.chunk_kv(w, 9, k, synth.KIND_V), "cuda") for k in range(uniq)]
-    Q = [synth_dev(synth.queries(w, 9, k), "cuda") for k in range(uniq)]
-    out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
-    points = []
+    K = [synth_dev(synth.chunk_kv(w, seed, k, synth.KIND_K), dev) for k in range(uniq)]
+    V = [synth_dev(synth.chunk_kv(w, seed, k, synth.KIND_V), dev) for k in range(uniq)]
+    Q = [synth_dev(synth.queries(w, seed, k), dev) for k in range(uniq)]
+    out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(qvg.workspace_size(p, qvg.QVG_OP_COMPRESS, w.N, w.H, w.d), dtype=torch.uint8, device=dev)
+    points, comp_ms, step_ms = [], [], []
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
     for k in range(w.n_chunks):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         e[0].record()
-        qvg.compress_chunk(p, K[k % uniq], kc)
-        qvg.compress_chunk(p, V[k % uniq], vc)
+        qvg.compress_chunk(p, K[k % uniq], kc, workspace=ws)
+        qvg.compress_chunk(p, V[k % uniq], vc, workspace=ws)
         e[1].record()
         qvg.attention(p, Q[k % uniq], kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out)
         e[2].record()
         torch.cuda.synchronize()
+        comp_ms.append(e[0].elapsed_time(e[1]))
+        step_ms.append(e[0].elapsed_time(e[2]))
         if k in (0, 7, 23, 47, 71, 95):
             nk = (k + 1) * w.N
             ms = e[1].elapsed_time(e[2])
-            points.append({"chunks": k + 1, "cache_tokens": nk, "compress_ms": e[0].elapsed_time(e[1]),
-                           "attention_ms": ms, "attention_TFLOP/s": 4.0 * w.Nq * nk * w.d * w.Hq / ms / 1e9})
-    comp = kc.nbytes + vc.nbytes
-    print(json.dumps({"study": "rollout", "workload": "8 heads, d=128, 96 chunks x 4680 tokens (449,280), C=256, INT2 G=64, 8 iters",
-                      "status": qvg.get_status(), "points": points,
-                      "cache_bytes_compressed": comp,
-                      "cache_bytes_bf16": qvg.kv_bytes_uncompressed(1, w.H, w.d, w.tokens)}), flush=True)
-    return 0
+            points.append(dict(_rates(_cache_read_bytes(w, p, nk), 4.0 * w.Nq * nk * w.d * w.Hq, ms, peaks),
+                               chunks=k + 1, cache_tokens=nk))
+    t_wall = time.perf_counter() - t_wall
+    timed = _timer(flush)
+    ms_last = timed(lambda: qvg.attention(p, Q[(w.n_chunks - 1) % uniq], kc, vc, out_dtype=qvg.QVG_OUT_BF16, out=out))
+    dall = torch.empty((w.N, w.H, w.d), dtype=torch.float32, device=dev)
+    ms_d = timed(lambda: qvg.decompress(p, kc, kc.n_tokens - per, w.N, out=dall))
+    nbytes, flops = _compress_counts(w, p)
+    return {"workload": "rollout: 8 heads, d=128, 96 chunks x 4680 tokens (449,280), C=256, INT2 G=64, 8 iters",
+            "points": points,
+            "last_chunk_attention": dict(_rates(_cache_read_bytes(w, p, w.tokens),
+                                                4.0 * w.Nq * w.tokens * w.d * w.Hq, ms_last, peaks),
+                                         **{"tok/s": w.Nq / (ms_last / 1e3),
+                                            "what": "4680 queries over 449,280 cached tokens, L2 flushed"}),
+            "compress_KV_per_chunk": _rates(nbytes, flops, statistics.median(comp_ms), peaks),
+            "decompress_newest_chunk_f32": _rates(_cache_read_bytes(w, p, w.N) / 2 + w.N * w.H * w.d * 4, None,
+                                                  ms_d, peaks),
+            "rollout_s": sum(step_ms) / 1e3, "rollout_wall_s": t_wall,
+            "cache_bytes_compressed": kc.nbytes + vc.nbytes,
+            "cache_bytes_bf16": qvg.kv_bytes_uncompressed(1, w.H, w.d, w.tokens)}
+
+
+def _study(fn, name):
+    def run(args):
+        import torch
+
+        import __graft_entry__
+        __graft_entry__.build()
+        import video_diffusion_kv_gb300 as qvg
+        from video_diffusion_kv_gb300 import synth
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        peaks, _ = _peaks()
+        res = fn(qvg, synth, flush, peaks)
+        print(json.dumps({"study": name, "status": qvg.get_status(), **res}), flush=True)
+        return 0
+    return run
+
+
+study_tiny = _study(measure_tiny, "tiny")
+study_qvgpro = _study(measure_qvgpro, "qvgpro")
+study_quantwm = _study(measure_quantwm, "quantwm")
+study_rollout = _study(measure_rollout, "rollout")
 
 
 def study_outlier(args):
@@ -888,7 +1090,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="time the device step only (profiling)")
     ap.add_argument("--cache-chunks", type=int, default=None, help="smaller cache (profiling cases)")
-    ap.add_argument("--workload", default="longcat", choices=["longcat", "qvgpro", "quantwm", "rollout", "outlier", "paths", "layers"],
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configurations' measurements")
+    ap.add_argument("--workload", default="longcat",
+                    choices=["longcat", "tiny", "qvgpro", "quantwm", "rollout", "outlier", "paths", "layers"],
                     help="longcat: the benchmark line; the others print their study line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "own":
@@ -896,7 +1100,7 @@ def main():
     if args.impl == "reference":
         return run_reference(args)
     if args.workload != "longcat":
-        return {"qvgpro": study_qvgpro, "quantwm": study_quantwm, "rollout": study_rollout,
+        return {"tiny": study_tiny, "qvgpro": study_qvgpro, "quantwm": study_quantwm, "rollout": study_rollout,
                 "outlier": study_outlier, "paths": study_paths, "layers": study_layers}[args.workload](args)
     return run_own(args)
 
