@@ -250,22 +250,15 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ own arm
 
-def launches_per_compress(p, fused_first_stage=True):
+def launches_per_compress(p):
     """Kernels one qvg_compress_chunk call launches (see csrc/api.cu): per
-    stage the residual quantiser, and with centroids the init; the first
-    stage without QSAC weights runs all Lloyd iterations in one cluster
-    launch, the others launch row norms, iters x (assign, update) and the
-    final assignment."""
-    n = 1  # chunk table
-    for l in range(p.L):
-        n += 1  # residual quantise (+ pack, stage residual, PSAC)
-        if p.C > 0:
-            n += 1  # init (or the norms of given centroids)
-            if l == 0 and fused_first_stage and not p.flags & 1:
-                n += 1
-            else:
-                n += 1 + 2 * p.iters + 1
-    return n
+    stage the residual quantiser, and with centroids the row norms, the
+    init, iters x (assign, update) and the final assignment; then the chunk
+    table."""
+    per_stage = 1  # residual quantise (+ pack, stage residual, PSAC)
+    if p.C > 0:
+        per_stage += 1 + 1 + 2 * p.iters + 1
+    return per_stage * p.L + 1
 
 
 def kernel_extras(qvg, p, w, kc, vc, q, k_raw, flush, dev, last, slots_per_chunk, reps=5):

@@ -163,16 +163,12 @@ def test_clock_record_parsing():
 
 
 def test_launch_count_per_compress():
-    """One compress call: per stage, init + quantise, and the k-means: one
-    cluster launch for a first stage without QSAC weights, else row norms
-    + iters x (assign, update) + final assign; then the chunk table."""
+    """One compress call: per stage, row norms + init + iters x (assign,
+    update) + final assign + quantise; then the chunk table."""
     p = qvg.Params(C=256, L=1, bits=2, group=64, iters=8)
-    assert bench.launches_per_compress(p) == 1 + 1 + 1 + 1
-    assert bench.launches_per_compress(p, fused_first_stage=False) == 1 + 1 + 16 + 1 + 1 + 1
-    pq = qvg.Params(C=256, L=1, bits=2, group=64, iters=8, flags=qvg.QVG_QSAC)
-    assert bench.launches_per_compress(pq) == 1 + 1 + 16 + 1 + 1 + 1
+    assert bench.launches_per_compress(p) == 1 + 1 + 16 + 1 + 1 + 1
     p3 = qvg.Params(C=16, L=3, bits=2, group=32, iters=10)
-    assert bench.launches_per_compress(p3) == (1 + 1 + 1) + 2 * (1 + 1 + 20 + 1 + 1) + 1
+    assert bench.launches_per_compress(p3) == 3 * (1 + 1 + 20 + 1 + 1) + 1
     rtn = qvg.Params(C=0, L=1, bits=2, group=32, iters=0)
     assert bench.launches_per_compress(rtn) == 2
 
