@@ -17,6 +17,11 @@
 //                     members summed in token order -> bf16 centroid + norm
 //   k_residual_quant  r = x - c_id, per-group scale, codes, packing, stage
 //                     residual for the next stage, PSAC INT8 projection
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -110,9 +115,11 @@ __global__ void k_centroid_norms(const uint16_t *__restrict__ cent, size_t hs, i
 // are ||x||_w^2 / 2 and ||c||_w^2 / 2 split into three bf16 parts (exact to
 // 2^-24).  So f_c = -d_c / 2 with d_c = sum_j w_j (x_j - c_j)^2, accumulated in
 // fp32 in tensor memory by tcgen05.mma (M=128, N=Np = Ce rounded up to 16).
-// Token tiles arrive by cp.async into NA buffers (completion counted on an
-// mbarrier per buffer), and the MMA of tile k+1 runs while the epilogue of
-// tile k reads the other accumulator.
+// Token tiles arrive by TMA (a tensor map over the stage's bf16 [N][H][d]
+// operand, 128-byte swizzle, zero fill past N) into NA buffers, the
+// centroids likewise once per launch; completion is counted on an mbarrier
+// per buffer, and the MMA of tile k+1 runs while the epilogue of tile k reads
+// the other accumulator.
 //
 // Epilogue, thread = token row (the four warp groups take interleaved
 // 32-column chunks).  For f <= 0 a larger f has a smaller bit pattern as an
@@ -180,7 +187,9 @@ __device__ __forceinline__ void merge2(float &bv, int &bi, float &sv, int &si, f
 }
 
 template <int D, int P>
-__global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const uint16_t *__restrict__ g, int N, int H,
+__global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const __grid_constant__ CUtensorMap tm_x,
+                                                            const __grid_constant__ CUtensorMap tm_c,
+                                                            const uint16_t *__restrict__ g, int N, int H,
                                                             const uint16_t *__restrict__ cent, size_t hs,
                                                             int Ce, int Np, const float *__restrict__ cnorm,
                                                             int C, const float *__restrict__ w,
@@ -198,7 +207,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
     uint8_t *Ax = As + NA * AB;                      // NA x extra K block of the tokens (4 KB)
     uint8_t *Bs = Ax + NA * 4096;                    // P x KB x [Np rows x 128 B]
     uint8_t *Bx = Bs + static_cast<size_t>(P) * KB * Np * 128;  // extra K block of the centroids
-    __shared__ uint64_t bar_mma[2], bar_a[NA], bar_drain, bar_never;
+    __shared__ uint64_t bar_mma[2], bar_a[NA], bar_drain, bar_never, bar_cent;
     __shared__ uint32_t tmem_base;
     __shared__ float xs[kAssignGroups][128][2];  // each warp group's two best scores per row
     __shared__ int xk[kAssignGroups][128][2];    // ... and their clusters
@@ -220,25 +229,30 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         umma::mbar_init(&bar_mma[1], 1);
         umma::mbar_init(&bar_drain, 1);
         umma::mbar_init(&bar_never, 1);  // nothing arrives: the bounded-wait test hook
-        for (int i = 0; i < NA; ++i) umma::mbar_init(&bar_a[i], 2 * kAssignThreads);
+        umma::mbar_init(&bar_cent, 1);
+        // per tile: the TMA's arrival (with its byte count) and one per thread
+        // once its part of the extra K block is written
+        for (int i = 0; i < NA; ++i) umma::mbar_init(&bar_a[i], kAssignThreads + 1);
+        umma::tma_prefetch_map(&tm_x);
+        if (P == 1) umma::tma_prefetch_map(&tm_c);
         umma::fence_barrier_init();
     }
     __syncthreads();
 
-    // token tile k -> buffer k % NA: each thread's copies arrive on bar_a once
-    // done, and each thread arrives once more after its part of the extra K
-    // block (core matrix layout: row r, K half kh at (r/8)*256 + kh*128 + (r%8)*16)
+    // token tile k -> buffer k % NA: thread 0's TMA arrives on bar_a with the
+    // tile's bytes, and each thread arrives once more after its part of the
+    // extra K block (core matrix layout: row r, K half kh at (r/8)*256 +
+    // kh*128 + (r%8)*16); n_issued counts thread 0's tile copies (for the drain)
+    int n_issued = 0;
     auto load_tokens = [&](int k) {
-        const int n0 = (t0 + k * tstep) * 128;
-        uint8_t *dst = As + (k % NA) * AB;
-#pragma unroll 4
-        for (int i = tid; i < 128 * (D / 8); i += kAssignThreads) {
-            const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
-            const bool in = n0 + r < N;
-            umma::cp_async16(dst + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4),
-                             g + (static_cast<size_t>(in ? n0 + r : 0) * H + h) * D + ci * 8, in);
+        if (tid == 0) {
+            const int n0 = (t0 + k * tstep) * 128;
+            uint8_t *dst = As + (k % NA) * AB;
+            umma::mbar_arrive_expect_tx(&bar_a[k % NA], AB);
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) umma::tma_load_3d(dst + kb * 16384, &tm_x, kb * 64, h, n0, &bar_a[k % NA]);
+            n_issued = k + 1;
         }
-        umma::cp_async_arrive_noinc(&bar_a[k % NA]);
     };
     auto load_norms = [&](int k) {
         const int n0 = (t0 + k * tstep) * 128;
@@ -269,16 +283,16 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
     pdl_wait();
     pdl_trigger();
     for (int k = 0; k < NA - 1 && k < my_tiles; ++k) load_norms(k);
-    // centroids (or weighted hi/lo pair) -> swizzled K-major bf16, once
+    // centroids (or weighted hi/lo pair) -> swizzled K-major bf16, once; the
+    // plain centroids by TMA (rows past C read 0; rows Ce .. C-1, unused
+    // clusters, get a huge norm below)
     if constexpr (P == 1) {
-#pragma unroll 4
-        for (int i = tid; i < Np * (D / 8); i += kAssignThreads) {
-            const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
-            const bool in = r < Ce;
-            umma::cp_async16(Bs + static_cast<size_t>(kb) * Np * 128 + r * 128 + ((c ^ (r & 7)) << 4),
-                             ch + static_cast<size_t>(in ? r : 0) * D + ci * 8, in);
+        if (tid == 0) {
+            umma::mbar_arrive_expect_tx(&bar_cent, KB * Np * 128);
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)
+                umma::tma_load_3d(Bs + static_cast<size_t>(kb) * Np * 128, &tm_c, kb * 64, 0, h, &bar_cent);
         }
-        umma::cp_async_commit();
     } else {
         for (int i = tid; i < Np * (D / 8); i += kAssignThreads) {
             const int r = i / (D / 8), ci = i % (D / 8), kb = ci >> 3, c = ci & 7;
@@ -323,13 +337,12 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         }
         *reinterpret_cast<uint4 *>(Bx + (c >> 3) * 256 + kh * 128 + (c & 7) * 16) = v;
     }
-    // the centroid copies (and the earlier token-tile copies, which the
-    // commit sweeps into the same group) have landed; the tiles' mbarriers
-    // count them as well
-    umma::cp_async_wait_group<0>();
+    // the centroids have landed (every thread reads them in the re-scoring)
+    bool c_ok = true;
+    if (P == 1) c_ok = umma::mbar_wait(&bar_cent, 0, wait_ns);
     umma::fence_proxy_async_smem();
     umma::tc_fence_before();
-    __syncthreads();
+    const bool cent_ok = __syncthreads_and(c_ok);
     umma::tc_fence_after();
     const uint32_t tmem = tmem_base;
     const uint32_t idesc = umma::idesc_f16(128, Np, 1);
@@ -348,9 +361,11 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
                       umma::desc_noswz(umma::smem_u32(Bx), 128, 256), idesc, 1u);
         umma::mma_commit(&bar_mma[k & 1]);
     };
-    bool ok = true;
-    if (tid == 0 && my_tiles > 0) {
+    bool ok = cent_ok;
+    int n_waited = 0;  // thread 0: tile copies it has waited for
+    if (tid == 0 && my_tiles > 0 && ok) {
         if (umma::mbar_wait(&bar_a[0], 0, wait_ns)) {
+            n_waited = 1;
             umma::tc_fence_after();
             issue(0);
         } else {
@@ -369,6 +384,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         // (its accumulator's previous tile, k-1, ended at the last barrier)
         if (NA == 3 && tid == 0 && k + 1 < my_tiles) {
             if (umma::mbar_wait(&bar_a[(k + 1) % NA], ((k + 1) / NA) & 1, wait_ns)) {
+                n_waited = k + 2;
                 umma::tc_fence_after();
                 issue(k + 1);
             } else {
@@ -377,8 +393,10 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         }
         // (2) refill the buffer of tile k - 1 (its epilogue ended at the last barrier)
         if (k + NA - 1 < my_tiles) load_tile(k + NA - 1);
-        // (3) epilogue of tile k
+        // (3) epilogue of tile k (every thread also observes tile k's copy: the
+        // re-scoring reads rows of it)
         if (!umma::mbar_wait(&bar_mma[k & 1], (k >> 1) & 1, wait_ns)) ok = false;
+        if (ok && !umma::mbar_wait(&bar_a[buf], (k / NA) & 1, wait_ns)) ok = false;
         ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
         umma::tc_fence_after();
         const int r = (warp & 3) * 32 + lane;
@@ -515,6 +533,7 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
         // (4) with two buffers, tile k+1's loads were issued in (2): start its MMA
         if (NA == 2 && tid == 0 && k + 1 < my_tiles) {
             if (umma::mbar_wait(&bar_a[(k + 1) % NA], ((k + 1) / NA) & 1, wait_ns)) {
+                n_waited = k + 2;
                 umma::tc_fence_after();
                 issue(k + 1);
             } else {
@@ -541,8 +560,10 @@ __global__ void __launch_bounds__(kAssignThreads, 1) k_kmeans_assign_tc(const ui
     if (tid == 0 && my_tiles > 0) {
         umma::mma_commit(&bar_drain);
         umma::mbar_wait(&bar_drain, 0, kWaitNs);
+        // tile copies issued but never waited for (a wait ran out)
+        for (int j = n_waited; j < n_issued; ++j)
+            umma::mbar_wait(&bar_a[j % NA], static_cast<uint32_t>(j / NA) & 1u, kWaitNs);
     }
-    umma::cp_async_wait_all();
     umma::tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -1062,6 +1083,39 @@ __global__ void k_chunk_table(int chunk, int slot0, int N, int32_t *chunk_start,
 
 static int sm_count() { return sm_count_current(); }
 
+// cuTensorMapEncodeTiled from the driver (looked up once; no link to libcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map (dims d0 innermost .. d2, byte strides of dims 1 and 2),
+// boxes of box0 x box1 x box2 elements with the 128-byte swizzle, zero fill
+// outside the tensor.  A host-side description only: nothing is allocated.
+static bool bf16_tensor_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                            uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2) {
+    const auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1, stride2};
+    const cuuint32_t box[3] = {box0, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 qvg_status launch_kmeans_init(const uint16_t *g, int N, int H, int d, int C, int Ce, uint64_t seed,
                               int chunk, int stage, uint16_t *cent, size_t hs, const float *w, float *cnorm,
                               cudaStream_t st) {
@@ -1111,9 +1165,16 @@ static qvg_status assign_tc_impl(const uint16_t *g, int N, int H, const uint16_t
     const int n_tiles = ceil_div(N, 128);
     const int per_head = std::max(1, std::min(n_tiles, sm_count() / std::max(1, H)));
     dim3 grid(per_head, H);
-    const cudaError_t e = launch_pdl(k_kmeans_assign_tc<D, P>, grid, dim3(kAssignThreads), smem, st, g, N, H, cent,
-                                     hs, Ce, Np, cnorm, C, w, xnorm, ids, device_error_word(), wait_limit_ns(),
-                                     wait_inject());
+    // the stage operand [N][H][D] in boxes of (64 channels, 1 head, 128 tokens);
+    // this chunk's centroids [H][C][D] (head stride hs) in boxes of (64, Np, 1)
+    CUtensorMap tm_x, tm_c;
+    if (!bf16_tensor_map(&tm_x, g, D, H, N, D * 2ull, static_cast<uint64_t>(H) * D * 2, 64, 1, 128) ||
+        (P == 1 && !bf16_tensor_map(&tm_c, cent, D, C, H, D * 2ull, hs * 2, 64, Np, 1)))
+        return QVG_ERR_CUDA;
+    if (P != 1) tm_c = tm_x;  // (unused: the weighted centroids are staged by the threads)
+    const cudaError_t e = launch_pdl(k_kmeans_assign_tc<D, P>, grid, dim3(kAssignThreads), smem, st, tm_x, tm_c, g,
+                                     N, H, cent, hs, Ce, Np, cnorm, C, w, xnorm, ids, device_error_word(),
+                                     wait_limit_ns(), wait_inject());
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         note_cuda_error(e);
