@@ -57,7 +57,7 @@ struct AttnWsArgs {
     const uint16_t *kanch, *vanch;
     const int32_t *chunk_anchor;
     // bound of the pipeline's waits (ns); inject: the test hook that makes
-    // each softmax group's issuer wait once on a barrier nothing completes
+    // each softmax group's S issuer wait once on a barrier nothing completes
     uint64_t wait_ns;
     int inject;
 };
@@ -98,11 +98,6 @@ __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, volatile in
             return false;
         }
     }
-}
-
-// Named barrier over the 128 threads of one softmax group (ids 1 and 2).
-__device__ __forceinline__ void group_sync(int i) {
-    asm volatile("bar.sync %0, 128;" ::"r"(1 + i) : "memory");
 }
 
 // Tile t covers slots [t QVG_TILE, (t + 1) QVG_TILE), of which the first
@@ -738,7 +733,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
     uint8_t *Q0 = sm, *Q1 = Q0 + TB, *Kt = Q1 + TB, *Vt0 = Kt + TB, *P0 = Vt0 + 2 * TB, *P1 = P0 + PB;
-    __shared__ uint64_t kfull, kfree, vfull[2], vfree[2], sfull[2], ofull[2], drain, never;
+    __shared__ uint64_t kfull, kfree, vfull[2], vfree[2], sfull[2], ofull[2], sfree[2], pfull[2], drain, never;
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
 
@@ -768,13 +763,15 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     if (tid == 0) {
         umma::mbar_init(&kfull, 128);
         umma::mbar_init(&kfree, 2);
-        umma::mbar_init(&drain, 2);
+        umma::mbar_init(&drain, 4);  // the four issuing lanes (S and PV of each group)
         umma::mbar_init(&never, 1);  // nothing arrives: the bounded-wait test hook
         for (int i = 0; i < 2; ++i) {
             umma::mbar_init(&vfull[i], 128);
             umma::mbar_init(&vfree[i], 2);
             umma::mbar_init(&sfull[i], 1);
             umma::mbar_init(&ofull[i], 1);
+            umma::mbar_init(&sfree[i], 4);
+            umma::mbar_init(&pfull[i], 4);
         }
         umma::fence_barrier_init();
         fail = 0;
@@ -789,7 +786,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     if (warp < 8) {
         // ------------------------------------------------ softmax of tile i
         const int i = warp >> 2, r = tid & 127;
-        const bool issuer = (warp & 3) == 0 && lane == 0;
+        // lane 0 of the group's first warp issues its PV products, lane 0 of
+        // its second warp its S products: issuing a tcgen05.mma waits until
+        // the tensor pipe takes it, so the two waits fall on different warps,
+        // and the other warps of the group never wait for either
+        const bool pv_issuer = (warp & 3) == 0 && lane == 0, s_issuer = (warp & 3) == 1 && lane == 0;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + i * 128 + lane_off, tO = tmem + 256 + i * 128 + lane_off;
         uint8_t *Pi = i ? P1 : P0;
@@ -813,11 +814,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             umma::mma_commit(&sfull[i]);
             umma::mma_commit(&kfree);
         };
-        // A group never leaves its tile loop early: the named barriers below
-        // are executed by all four warps on every tile, and after a failed
-        // wait a warp only stops doing work (live is warp-uniform).
+        // A warp never leaves its tile loop early: it arrives on sfree[i] and
+        // pfull[i] on every tile, and after a failed wait it only stops doing
+        // work (live is warp-uniform).
         bool ok_issue = true;
-        if (issuer && n_tiles > 0) {
+        if (s_issuer && n_tiles > 0) {
             if (ws::wait(&kfull, 0, vfail, a.wait_ns))
                 issue_S();
             else
@@ -917,24 +918,38 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                     umma::tmem_ld_wait_regs(v);
                 }
                 if (c0 == 96) {
-                    // every thread of the group holds its last S_i columns:
-                    // S_i(t + 1) may overwrite them if K(t + 1) is ready
+                    // this warp holds its last S_i columns; S_i(t + 1) may
+                    // overwrite them once all four warps have arrived, if
+                    // K(t + 1) is ready (else after this tile)
                     umma::tc_fence_before();
-                    group_sync(i);
-                    if (issuer && live && more && umma::mbar_test_wait(&kfull, (t + 1) & 1)) {
-                        issue_S();
+                    __syncwarp();
+                    if (lane == 0) umma::mbar_arrive(&sfree[i]);
+                    if (s_issuer && live && more && umma::mbar_test_wait(&kfull, (t + 1) & 1)) {
+                        if (ws::wait(&sfree[i], t & 1, vfail, a.wait_ns))
+                            issue_S();
+                        else
+                            ok_issue = false;
                         s_next = true;
                     }
                 }
                 if (live) softmax_chunk(v, c0, ti.nvalid, sl2, nm2, Prow, r, acc);
             }
             l_sum = l_sum * corr + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-            // P_i(t) complete in shared memory (and O_i rescaled): PV_i(t)
+            // this warp's rows of P_i(t) are in shared memory and O_i is
+            // rescaled: PV_i(t) once all four warps have arrived
             umma::fence_proxy_async_smem();
             umma::tc_fence_before();
-            group_sync(i);
-            if (issuer && live) {
-                if (ws::wait(&vfull[t & 1], (t >> 1) & 1, vfail, a.wait_ns)) {
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(&pfull[i]);
+            if (s_issuer && live && more && !s_next) {
+                if (ws::wait(&kfull, (t + 1) & 1, vfail, a.wait_ns) && ws::wait(&sfree[i], t & 1, vfail, a.wait_ns))
+                    issue_S();
+                else
+                    ok_issue = false;
+            }
+            if (pv_issuer && live) {
+                if (ws::wait(&pfull[i], t & 1, vfail, a.wait_ns) &&
+                    ws::wait(&vfull[t & 1], (t >> 1) & 1, vfail, a.wait_ns)) {
                     umma::tc_fence_after();
                     const uint64_t dp = umma::desc_sw128(pa), dv = umma::desc_sw128_mn(va0 + (t & 1) * TB, 16384);
 #pragma unroll 1
@@ -944,12 +959,6 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                     }
                     umma::mma_commit(&ofull[i]);
                     umma::mma_commit(&vfree[t & 1]);
-                    if (more && !s_next) {
-                        if (ws::wait(&kfull, (t + 1) & 1, vfail, a.wait_ns))
-                            issue_S();
-                        else
-                            ok_issue = false;
-                    }
                 } else {
                     ok_issue = false;
                 }
@@ -1000,7 +1009,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             }
         }
         // every MMA this group issued completes before TMEM is released
-        if (issuer) {
+        if (pv_issuer || s_issuer) {
             umma::mma_commit(&drain);
             umma::mbar_wait(&drain, 0, kWaitNs);
         }
