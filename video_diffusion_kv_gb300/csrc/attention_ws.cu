@@ -11,10 +11,11 @@
 // tensor core computes one tile's products while the other tile's softmax
 // runs); the warp roles and barriers are listed above the kernel.
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
-// O1 [384,384+D), fp32.  Per cache tile t:
-//   S_i = Q_i K_t^T              (M=128, N=128 slots, K=D; fp16 operands)
+// O1 [384,384+D), fp32; P_i (fp16 pairs) over S_i's first 64 columns.  Per
+// cache tile t:
+//   S_i = Q_i K_t^T              (M=128, N=128 slots, K=D; Q, K_hat from shared memory)
 //   P_i = exp2(s * scale*log2e - m_i), fp16, m_i raised lazily (by > 8)
-//   O_i += P_i V_t               (M=128, N=D, K=128 slots)
+//   O_i += P_i V_t               (M=128, N=D, K=128 slots; P_i from TMEM)
 // fp16 operands carry K_hat, V_hat, Q and P with a relative rounding of
 // 2^-11; on the synthetic LongCat-like and world-model caches this keeps
 // max|dO| / max|O| near 6e-5 against the fp64 oracle.
@@ -57,7 +58,7 @@ struct AttnWsArgs {
     const uint16_t *kanch, *vanch;
     const int32_t *chunk_anchor;
     // bound of the pipeline's waits (ns); inject: the test hook that makes
-    // each softmax group's S issuer wait once on a barrier nothing completes
+    // each softmax group's MMA issuer wait once on a barrier nothing completes
     uint64_t wait_ns;
     int inject;
 };
@@ -66,6 +67,7 @@ namespace ws {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
+constexpr int kNbuf = 2;  // K_hat and V_hat tiles in flight, each
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescale = 8.0f;
 
@@ -312,14 +314,14 @@ __device__ __forceinline__ void add_f16x2_to(uint32_t p, float &s0, float &s1) {
         : "r"(p));
 }
 
-// P = exp2(s * scale_log2 - m) for 32 logits of one row, rounded to fp16 and
-// stored as four 16-byte chunks of the row's swizzled P_i line.  The row sum
-// adds the same fp16 values the PV product uses, so the weights of O are
-// normalised exactly (a one-slot cache returns V_hat unchanged).  Columns at
-// or past nvalid (relative to c0) give 0.
+// P = exp2(s * scale_log2 - m) for 32 logits of one row, rounded to fp16
+// and packed in pairs (column 2k in the low half of pk[k]), ready to be
+// written over the row's S columns in tensor memory.  The row sum adds the
+// same fp16 values the PV product uses, so the weights of O are normalised
+// exactly (a one-slot cache returns V_hat unchanged).  Columns at or past
+// nvalid (relative to c0) give 0.
 __device__ __forceinline__ void softmax_chunk(const uint32_t (&v)[32], int c0, int nvalid, uint64_t sl2,
-                                              uint64_t nm2, uint8_t *Prow, int r, float (&acc)[4]) {
-    uint32_t pk[16];
+                                              uint64_t nm2, uint32_t (&pk)[16], float (&acc)[4]) {
     const bool full = c0 + 32 <= nvalid;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
@@ -332,12 +334,6 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&v)[32], int c0, i
         }
         pk[k] = h2(p0, p1);
         add_f16x2_to(pk[k], acc[2 * (k & 1)], acc[2 * (k & 1) + 1]);
-    }
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-        const int ci = c0 / 8 + x, kb = ci >> 3, c = ci & 7;
-        *reinterpret_cast<uint4 *>(Prow + kb * 16384 + ((c ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
     }
 }
 
@@ -392,7 +388,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
     HalfData<BITS> A, B;
     if (n_tiles > 0 && r < ti0.nvalid) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, ti0, r, id0, 0, A);
     for (int t = 0; t < n_tiles; ++t) {
-        const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
+        const int b = t % pr.nbuf, use = t / pr.nbuf;
         uint8_t *T = pr.buf0 + b * TB + r * 128;
         TileInfo ti2{};
         int id2 = 0;
@@ -647,7 +643,7 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
         }
         accumulate_quarter<BITS, OUTL>(cur, acc);
         if (l == L - 1) {
-            const int b = pr.nbuf == 2 ? (t & 1) : 0, use = pr.nbuf == 2 ? (t >> 1) : t;
+            const int b = t % pr.nbuf, use = t / pr.nbuf;
             uint8_t *T = pr.buf0 + b * TB + r * 128;
             if (qt == 0 && use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             float v[32];
@@ -702,23 +698,34 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 
 // Warp roles (16 warps):
 //   0-3, 4-7   softmax + epilogue of query tile i = 0 / 1 (thread = query row);
-//              lane 0 of warp 4i issues the tcgen05.mma of tile i (S_i and
-//              PV_i), and warp 0 owns the TMEM allocation
+//              lane 0 of warp 4i issues the tcgen05.mma of tile i, and warp 0
+//              owns the TMEM allocation
 //   8-11       K producers: rebuild the 128-slot K_hat tile (thread = slot)
-//   12-15      V producers: rebuild V_hat into one of two buffers (thread = slot)
+//   12-15      V producers: the same for V_hat
 // Both producers write a tile as [64-channel block][slot][64 channels] with
 // the 128-byte swizzle: K-major for the S = Q K_hat^T product (N = slots,
 // K = channels) and, read through an MN-major descriptor, the B operand of
-// O += P V_hat (N = channels, K = slots), so V needs no transpose.
-// Per cache tile t, group i: once all its threads hold the last columns of
-// S_i(t) (named barrier), S_i(t + 1) is issued if K(t + 1) is already
-// written; once P_i(t) is in shared memory (named barrier), PV_i(t) is issued
-// after V(t) is written, then S_i(t + 1) if it was deferred.
-// mbarriers (phase = tile index, per buffer for V):
+// O += P V_hat (N = channels, K = slots), so V needs no transpose.  K and V
+// tiles rotate through kNbuf buffers each.
+// P_i(t) is written in fp16 over the first 64 columns of S_i(t) in TMEM and
+// is the A operand of PV_i(t), read from TMEM.  Once the group's four warps
+// have written P_i(t), its issuer issues PV_i(t) and then S_i(t + 1); the
+// tensor pipe runs one thread's MMAs in issue order, so S_i(t + 1)
+// overwrites P_i(t) only after PV_i(t) has read it, and the commit that
+// reports S_i(t + 1) also reports PV_i(t): once group i sees S_i(t + 1), O_i
+// is settled and may be rescaled.  Issuing holds the issuing thread until
+// the tensor pipe takes the MMA, but here the whole group waits for
+// S_i(t + 1) at that point anyway.  The two groups run in step: the
+// tensor pipe's N = 128 products lose about 40 % of their rate while other
+// warps stream TMEM loads and stores, and a group's softmax alone on its
+// sub-partitions is latency-bound, so overlapping one group's products
+// with the other's softmax (issue turns) measured slower.
+// mbarriers (phase = tile index / kNbuf for the buffers, tile index else):
 //   kfull/vfull  producers -> issuers   tile written (one arrival per slot)
 //   kfree/vfree  MMA commits -> producer tile consumed (S_0 and S_1 / PV_0 and PV_1)
-//   sfull[i]     MMA commit -> group i   S_i ready
-//   ofull[i]     MMA commit -> group i   PV_i done (P_i free, O_i settled)
+//   sfull[i]     MMA commit -> group i   S_i(t) ready (and PV_i(t - 1) done)
+//   pfull[i]     group i -> its issuer   P_i(t) in TMEM, O_i rescaled (one arrival per warp)
+//   ofull[i]     MMA commit -> group i   the last PV_i done (epilogue)
 // MODE 0: one-stage caches without the outlier split or PSAC, no raw tiles;
 // MODE 1: the same with raw bf16 tiles (the current chunk, anchor chunks);
 // MODE 2: several stages, PSAC or the outlier split (out-of-line producers).
@@ -728,12 +735,12 @@ template <int D, int BITS, bool TOP1, int MODE>
 __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) {
     using namespace ws;
     constexpr int KB = D / 64;
-    constexpr int TB = KB * 16384;       // one 128 x D fp16 tile
-    constexpr int PB = 32768;            // 128 x 128 fp16
+    constexpr int TB = KB * 16384;  // one 128 x D fp16 tile
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
-    uint8_t *Q0 = sm, *Q1 = Q0 + TB, *Kt = Q1 + TB, *Vt0 = Kt + TB, *P0 = Vt0 + 2 * TB, *P1 = P0 + PB;
-    __shared__ uint64_t kfull, kfree, vfull[2], vfree[2], sfull[2], ofull[2], sfree[2], pfull[2], drain, never;
+    uint8_t *Q0 = sm, *Q1 = Q0 + TB, *Kt0 = Q1 + TB, *Vt0 = Kt0 + kNbuf * TB;
+    __shared__ uint64_t kfull[kNbuf], kfree[kNbuf], vfull[kNbuf], vfree[kNbuf], sfull[2], pfull[2], ofull[2], drain,
+        never;
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
 
@@ -761,18 +768,19 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         umma::tmem_relinquish();
     }
     if (tid == 0) {
-        umma::mbar_init(&kfull, 128);
-        umma::mbar_init(&kfree, 2);
-        umma::mbar_init(&drain, 4);  // the four issuing lanes (S and PV of each group)
-        umma::mbar_init(&never, 1);  // nothing arrives: the bounded-wait test hook
-        for (int i = 0; i < 2; ++i) {
-            umma::mbar_init(&vfull[i], 128);
-            umma::mbar_init(&vfree[i], 2);
-            umma::mbar_init(&sfull[i], 1);
-            umma::mbar_init(&ofull[i], 1);
-            umma::mbar_init(&sfree[i], 4);
-            umma::mbar_init(&pfull[i], 4);
+        for (int b = 0; b < kNbuf; ++b) {
+            umma::mbar_init(&kfull[b], 128);
+            umma::mbar_init(&kfree[b], 2);
+            umma::mbar_init(&vfull[b], 128);
+            umma::mbar_init(&vfree[b], 2);
         }
+        for (int i = 0; i < 2; ++i) {
+            umma::mbar_init(&sfull[i], 1);
+            umma::mbar_init(&pfull[i], 4);
+            umma::mbar_init(&ofull[i], 1);
+        }
+        umma::mbar_init(&drain, 2);  // the two issuing lanes
+        umma::mbar_init(&never, 1);  // nothing arrives: the bounded-wait test hook
         umma::fence_barrier_init();
         fail = 0;
     }
@@ -786,187 +794,149 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     if (warp < 8) {
         // ------------------------------------------------ softmax of tile i
         const int i = warp >> 2, r = tid & 127;
-        // lane 0 of the group's first warp issues its PV products, lane 0 of
-        // its second warp its S products: issuing a tcgen05.mma waits until
-        // the tensor pipe takes it, so the two waits fall on different warps,
-        // and the other warps of the group never wait for either
-        const bool pv_issuer = (warp & 3) == 0 && lane == 0, s_issuer = (warp & 3) == 1 && lane == 0;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + i * 128 + lane_off, tO = tmem + 256 + i * 128 + lane_off;
-        uint8_t *Pi = i ? P1 : P0;
-        uint8_t *Prow = Pi + r * 128;
+        const bool issuer = (warp & 3) == 0 && lane == 0;
         const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16_bmn(128, D, 0);
-        const uint32_t qa = umma::smem_u32(i ? Q1 : Q0), pa = umma::smem_u32(Pi);
-        const uint32_t ka = umma::smem_u32(Kt), va0 = umma::smem_u32(Vt0);
-        // S_i = Q_i K_t^T into TMEM columns [128 i, 128 i + 128)
-        // (issue loops are kept rolled so that their descriptors are not
-        // hoisted into registers held across the whole tile loop; a
-        // descriptor's low 14 bits are the shared address / 16, which the
-        // offsets below never carry out of)
-        auto issue_S = [&]() {
+        const uint32_t qa = umma::smem_u32(i ? Q1 : Q0), ka = umma::smem_u32(Kt0), va = umma::smem_u32(Vt0);
+        // S_i(t) = Q_i K(t)^T into TMEM columns [128 i, 128 i + 128) once K(t)
+        // is written (rolled issue loops: a descriptor's low 14 bits are the
+        // shared address / 16, which these offsets never carry out of)
+        auto issue_S = [&](int t) -> bool {
+            const int b = t % kNbuf;
+            if (!ws::wait(&kfull[b], (t / kNbuf) & 1, vfail, a.wait_ns)) return false;
             umma::tc_fence_after();
-            const uint64_t dq = umma::desc_sw128(qa), dk = umma::desc_sw128(ka);
+            const uint64_t dq = umma::desc_sw128(qa), dk = umma::desc_sw128(ka + b * TB);
 #pragma unroll 1
             for (int s = 0; s < D / 16; ++s) {
                 const uint32_t off16 = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
                 umma::mma_f16(tmem + i * 128, dq + off16, dk + off16, idS, s != 0);
             }
             umma::mma_commit(&sfull[i]);
-            umma::mma_commit(&kfree);
+            umma::mma_commit(&kfree[b]);
+            return true;
         };
-        // A warp never leaves its tile loop early: it arrives on sfree[i] and
-        // pfull[i] on every tile, and after a failed wait it only stops doing
-        // work (live is warp-uniform).
-        bool ok_issue = true;
-        if (s_issuer && n_tiles > 0) {
-            if (ws::wait(&kfull, 0, vfail, a.wait_ns))
-                issue_S();
-            else
-                ok_issue = false;
+        bool live = true;
+        if (issuer && n_tiles > 0) {
+            live = issue_S(0);
             // test hook: with S_i(0) in flight, wait on a barrier that nothing
             // completes; the bound runs out, every role stops, and the drain
             // below waits for the MMA
-            if (ok_issue && a.inject && !ws::wait(&never, 0, vfail, a.wait_ns)) ok_issue = false;
+            if (live && a.inject && !ws::wait(&never, 0, vfail, a.wait_ns)) live = false;
         }
-        bool live = __all_sync(0xffffffffu, ok_issue);
+        live = __all_sync(0xffffffffu, live);
         float m_used = -INFINITY, l_sum = 0.0f, best = -INFINITY;
         int best_slot = 0;
-        for (int t = 0; t < n_tiles; ++t) {
+        for (int t = 0; t < n_tiles && live; ++t) {
             const TileInfo ti = tile_info<MODE != 0>(a, tb + t);
-            if (live) live = __all_sync(0xffffffffu, ws::wait(&sfull[i], t & 1, vfail, a.wait_ns));
+            live = __all_sync(0xffffffffu, ws::wait(&sfull[i], t & 1, vfail, a.wait_ns));
+            if (!live) break;
+            umma::tc_fence_after();
+            // row maximum of the raw logits (the scale is positive), scaled
+            // once; the top-1 variant keeps one in-order chain so that ties
+            // resolve to the lowest slot
+            float rmax = -INFINITY;
+            int targ = 0;
+            if constexpr (TOP1) {
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t v[32];
+                    umma::tmem_ld32(tS + c0, v);
+                    umma::tmem_ld_wait_regs(v);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const float x = c0 + k < ti.nvalid ? __uint_as_float(v[k]) : -INFINITY;
+                        if (x > rmax) { rmax = x; targ = c0 + k; }
+                    }
+                }
+            } else {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t v[32];
+                    umma::tmem_ld32(tS + c0, v);
+                    umma::tmem_ld_wait_regs(v);
+                    if (c0 + 32 <= ti.nvalid) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            m4[k & 3] = max3(m4[k & 3], __uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            if (c0 + k < ti.nvalid) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(v[k]));
+                    }
+                }
+                rmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            }
+            const float tmax = rmax * a.scale_log2;
+            if constexpr (TOP1) {
+                if (tmax > best) {
+                    best = tmax;
+                    best_slot = (tb + t) * QVG_TILE + targ;
+                }
+            }
             float corr = 1.0f;
-            if (live) {
-                umma::tc_fence_after();
-                // row maximum of the raw logits (the scale is positive), scaled
-                // once; the top-1 variant keeps one in-order chain so that ties
-                // resolve to the lowest slot
-                float rmax = -INFINITY;
-                int targ = 0;
-                if constexpr (TOP1) {
+            bool rescale = false;
+            if (tmax > m_used + kRescale) {
+                corr = ex2(m_used - tmax);
+                rescale = t > 0;
+                m_used = tmax;
+            }
+            // PV_i(t - 1) is done (reported with S_i(t)): O_i may be rescaled
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float f = rescale ? corr : 1.0f;
 #pragma unroll
-                    for (int c0 = 0; c0 < 128; c0 += 32) {
-                        uint32_t v[32];
-                        umma::tmem_ld32(tS + c0, v);
-                        umma::tmem_ld_wait_regs(v);
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t v[32];
+                    umma::tmem_ld32(tO + c0, v);
+                    umma::tmem_ld_wait_regs(v);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const float x = c0 + k < ti.nvalid ? __uint_as_float(v[k]) : -INFINITY;
-                            if (x > rmax) { rmax = x; targ = c0 + k; }
-                        }
-                    }
-                } else {
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                    for (int c0 = 0; c0 < 128; c0 += 32) {
-                        uint32_t v[32];
-                        umma::tmem_ld32(tS + c0, v);
-                        umma::tmem_ld_wait_regs(v);
-                        if (c0 + 32 <= ti.nvalid) {
-#pragma unroll
-                            for (int k = 0; k < 16; ++k)
-                                m4[k & 3] = max3(m4[k & 3], __uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                if (c0 + k < ti.nvalid) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(v[k]));
-                        }
-                    }
-                    rmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                }
-                const float tmax = rmax * a.scale_log2;
-                if constexpr (TOP1) {
-                    if (tmax > best) {
-                        best = tmax;
-                        best_slot = (tb + t) * QVG_TILE + targ;
-                    }
-                }
-                bool rescale = false;
-                if (tmax > m_used + kRescale) {
-                    corr = ex2(m_used - tmax);
-                    rescale = t > 0;
-                    m_used = tmax;
-                }
-                if (t > 0) {  // PV_i of the previous tile done: P_i is free and O_i settled
-                    live = __all_sync(0xffffffffu, ws::wait(&ofull[i], (t - 1) & 1, vfail, a.wait_ns));
-                    if (live) {
-                        umma::tc_fence_after();
-                        if (__any_sync(0xffffffffu, rescale)) {
-                            const float f = rescale ? corr : 1.0f;
-#pragma unroll
-                            for (int c0 = 0; c0 < D; c0 += 32) {
-                                uint32_t v[32];
-                                umma::tmem_ld32(tO + c0, v);
-                                umma::tmem_ld_wait_regs(v);
-#pragma unroll
-                                for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
-                                umma::tmem_st32(tO + c0, v);
-                            }
-                            umma::tmem_st_wait();
-                        }
-                    }
+                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
+                    umma::tmem_st32(tO + c0, v);
                 }
             }
             const uint64_t sl2 = pk2(a.scale_log2, a.scale_log2), nm2 = pk2(-m_used, -m_used);
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const bool more = t + 1 < n_tiles;
-            bool s_next = false;
+            // P_i(t) over S_i(t): chunk c0 of S (columns [c0, c0 + 32)) becomes
+            // columns [c0 / 2, c0 / 2 + 16), which hold logits already read
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
-                uint32_t v[32];
-                if (live) {
-                    umma::tmem_ld32(tS + c0, v);
-                    umma::tmem_ld_wait_regs(v);
-                }
-                if (c0 == 96) {
-                    // this warp holds its last S_i columns; S_i(t + 1) may
-                    // overwrite them once all four warps have arrived, if
-                    // K(t + 1) is ready (else after this tile)
-                    umma::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) umma::mbar_arrive(&sfree[i]);
-                    if (s_issuer && live && more && umma::mbar_test_wait(&kfull, (t + 1) & 1)) {
-                        if (ws::wait(&sfree[i], t & 1, vfail, a.wait_ns))
-                            issue_S();
-                        else
-                            ok_issue = false;
-                        s_next = true;
-                    }
-                }
-                if (live) softmax_chunk(v, c0, ti.nvalid, sl2, nm2, Prow, r, acc);
+                uint32_t v[32], pk[16];
+                umma::tmem_ld32(tS + c0, v);
+                umma::tmem_ld_wait_regs(v);
+                softmax_chunk(v, c0, ti.nvalid, sl2, nm2, pk, acc);
+                umma::tmem_st16(tS + c0 / 2, pk);
             }
             l_sum = l_sum * corr + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-            // this warp's rows of P_i(t) are in shared memory and O_i is
-            // rescaled: PV_i(t) once all four warps have arrived
-            umma::fence_proxy_async_smem();
+            umma::tmem_st_wait();
             umma::tc_fence_before();
             __syncwarp();
             if (lane == 0) umma::mbar_arrive(&pfull[i]);
-            if (s_issuer && live && more && !s_next) {
-                if (ws::wait(&kfull, (t + 1) & 1, vfail, a.wait_ns) && ws::wait(&sfree[i], t & 1, vfail, a.wait_ns))
-                    issue_S();
-                else
-                    ok_issue = false;
-            }
-            if (pv_issuer && live) {
-                if (ws::wait(&pfull[i], t & 1, vfail, a.wait_ns) &&
-                    ws::wait(&vfull[t & 1], (t >> 1) & 1, vfail, a.wait_ns)) {
+            if (issuer) {
+                // O_i += P_i(t) V(t), P_i from TMEM (columns [128 i, 128 i + 64)),
+                // once all four warps have written P_i(t); then S_i(t + 1)
+                const int b = t % kNbuf;
+                bool ok = ws::wait(&pfull[i], t & 1, vfail, a.wait_ns) &&
+                          ws::wait(&vfull[b], (t / kNbuf) & 1, vfail, a.wait_ns);
+                if (ok) {
                     umma::tc_fence_after();
-                    const uint64_t dp = umma::desc_sw128(pa), dv = umma::desc_sw128_mn(va0 + (t & 1) * TB, 16384);
+                    const uint64_t dv = umma::desc_sw128_mn(va + b * TB, 16384);
 #pragma unroll 1
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t aoff16 = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
-                        umma::mma_f16(tmem + 256 + i * 128, dp + aoff16, dv + ((s * 2048) >> 4), idO, (t | s) != 0);
-                    }
-                    umma::mma_commit(&ofull[i]);
-                    umma::mma_commit(&vfree[t & 1]);
-                } else {
-                    ok_issue = false;
+                    for (int s = 0; s < 8; ++s)
+                        umma::mma_f16_ts(tmem + 256 + i * 128, tmem + i * 128 + s * 8, dv + ((s * 2048) >> 4), idO,
+                                         (t | s) != 0);
+                    umma::mma_commit(&vfree[b]);
+                    if (t + 1 < n_tiles)
+                        ok = issue_S(t + 1);
+                    else
+                        umma::mma_commit(&ofull[i]);
                 }
+                live = ok;
             }
-            live = live && __all_sync(0xffffffffu, ok_issue);
+            live = __all_sync(0xffffffffu, live);
         }
         // epilogue: O_i / l
-        bool ok = live && !*vfail && n_tiles > 0 && ws::wait(&ofull[i], (n_tiles - 1) & 1, vfail, a.wait_ns);
+        bool ok = live && !*vfail && n_tiles > 0 && ws::wait(&ofull[i], 0, vfail, a.wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             umma::tc_fence_after();
@@ -1009,19 +979,19 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             }
         }
         // every MMA this group issued completes before TMEM is released
-        if (pv_issuer || s_issuer) {
+        if (issuer) {
             umma::mma_commit(&drain);
             umma::mbar_wait(&drain, 0, kWaitNs);
         }
-    } else if (warp < 16) {
+    } else {
         // ------------------------------------------------ K / V producers (thread = slot)
         const bool isv = warp >= 12;
         const Producer pr{isv ? a.vcodes : a.kcodes, isv ? a.vscales : a.kscales, isv ? a.vids : a.kids,
                           isv ? a.vcent : a.kcent, isv ? a.vraw : a.kraw, isv ? a.vanch : a.kanch,
                           isv ? a.voutv : a.koutv,
-                          isv ? a.vouti : a.kouti, isv ? Vt0 : Kt, isv ? vfull : &kfull,
-                          isv ? vfree : &kfree,
-                          isv ? 2 : 1, !isv && a.psac_p != nullptr};
+                          isv ? a.vouti : a.kouti, isv ? Vt0 : Kt0, isv ? vfull : kfull,
+                          isv ? vfree : kfree,
+                          kNbuf, !isv && a.psac_p != nullptr};
         if constexpr (MODE == 0) {
             produce_fast<D, BITS, false, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         } else if constexpr (MODE == 1) {
@@ -1104,7 +1074,7 @@ __global__ void __launch_bounds__(256) k_attn_merge(const float *__restrict__ po
 
 template <int D, int BITS, bool TOP1, int MODE>
 static qvg_status attn_ws_t(const AttnWsArgs &a, int a_splits, cudaStream_t st) {
-    constexpr size_t smem = 5 * (D / 64) * 16384 + 2 * 32768 + 1024;
+    constexpr size_t smem = (2 + 2 * ws::kNbuf) * (D / 64) * 16384 + 1024;
     {
         static std::atomic<uint64_t> done{0};
         const qvg_status s = smem_limit_once(done, reinterpret_cast<const void *>(k_attention_ws<D, BITS, TOP1, MODE>),
