@@ -20,6 +20,7 @@
 // 2^-11; on the synthetic LongCat-like and world-model caches this keeps
 // max|dO| / max|O| near 6e-5 against the fp64 oracle.
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "umma.cuh"
@@ -68,6 +69,13 @@ namespace ws {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kNbuf = 2;  // K_hat and V_hat tiles in flight, each
+// Per-CTA tile table in shared memory (chunk; valid slots and first row),
+// filled once at launch: the tile lookup otherwise chains three dependent
+// global loads (tile -> chunk -> start / length) in every producer's and
+// softmax warp's tile loop.  Tiles past kTabMax, or whose first row does not
+// fit the packed field, are looked up directly.
+constexpr int kTabMax = 4096;
+constexpr int kTabDirect = INT_MIN;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescale = 8.0f;
 
@@ -140,6 +148,23 @@ __device__ __forceinline__ TileInfo tile_info(const AttnWsArgs &a, int t) {
         ti.base = s0 - a.n_slots;
     }
     return ti;
+}
+
+template <bool RAW>
+__device__ __forceinline__ int2 tile_entry(const AttnWsArgs &a, int t) {
+    const TileInfo ti = tile_info<RAW>(a, t);
+    if (ti.base >= (1 << 23)) return make_int2(kTabDirect, 0);
+    return make_int2(ti.chunk, ti.nvalid | (ti.base << 8));
+}
+
+// Tile tb + t from the CTA's table (t counts from tb).
+template <bool RAW>
+__device__ __forceinline__ TileInfo tile_at(const AttnWsArgs &a, const int2 *tab, int tb, int t) {
+    if (t < kTabMax) {
+        const int2 e = tab[t];
+        if (e.x != kTabDirect) return TileInfo{e.y >> 8, e.x, e.y & 0xFF};
+    }
+    return tile_info<RAW>(a, tb + t);
 }
 
 // Eight bf16 values -> eight fp16 values (exact inside fp16's normal range).
@@ -354,6 +379,7 @@ struct Producer {
     uint64_t *full, *freeb;
     int nbuf;
     bool psac;
+    const int2 *tab;  // the CTA's tile table
 };
 
 template <int D, int BITS, bool OUTL, bool RAW>
@@ -378,11 +404,11 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
     TileInfo ti0{}, ti1{};
     int id0 = 0, id1 = 0;
     if (n_tiles > 0) {
-        ti0 = tile_info<RAW>(a, tb);
+        ti0 = tile_at<RAW>(a, pr.tab, tb, 0);
         if (a.C > 0 && ti0.chunk >= 0) id0 = pr.ids[id_row];
     }
     if (n_tiles > 1) {
-        ti1 = tile_info<RAW>(a, tb + 1);
+        ti1 = tile_at<RAW>(a, pr.tab, tb, 1);
         if (a.C > 0 && ti1.chunk >= 0) id1 = pr.ids[id_row + QVG_TILE];
     }
     HalfData<BITS> A, B;
@@ -393,7 +419,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         TileInfo ti2{};
         int id2 = 0;
         if (t + 2 < n_tiles) {
-            ti2 = tile_info<RAW>(a, tb + t + 2);
+            ti2 = tile_at<RAW>(a, pr.tab, tb, t + 2);
             if (a.C > 0 && ti2.chunk >= 0) id2 = pr.ids[id_row + static_cast<size_t>(t + 2) * QVG_TILE];
         }
         const bool valid = r < ti0.nvalid, valid1 = t + 1 < n_tiles && r < ti1.nvalid;
@@ -597,11 +623,11 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
     uint32_t idw[4], idn[4];
     float pk[QVG_PSAC_RANK];
     if (n_tiles > 0) {
-        ti = tile_info<true>(a, tb);
+        ti = tile_at<true>(a, pr.tab, tb, 0);
         load_stage_ids<D>(a, pr, h, ti, r, idw);
     }
     if (n_tiles > 1) {
-        tn = tile_info<true>(a, tb + 1);
+        tn = tile_at<true>(a, pr.tab, tb, 1);
         load_stage_ids<D>(a, pr, h, tn, r, idn);
     }
     QuarterData<BITS> cur, nxt;
@@ -684,7 +710,7 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 #pragma unroll
             for (int i = 0; i < 4; ++i) idw[i] = idn[i];
             if (t1 + 1 < n_tiles) {
-                tn = tile_info<true>(a, tb + t1 + 1);
+                tn = tile_at<true>(a, pr.tab, tb, t1 + 1);
                 load_stage_ids<D>(a, pr, h, tn, r, idn);
             }
         }
@@ -743,6 +769,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         never;
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
+    __shared__ int2 tile_tab[kTabMax];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hq = blockIdx.y, h = hq / a.grp, q0 = blockIdx.x * 256;
@@ -763,6 +790,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         }
         *reinterpret_cast<uint4 *>((rr < 128 ? Q0 : Q1) + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
+    for (int j = tid; j < min(n_tiles, kTabMax); j += kThreads) tile_tab[j] = tile_entry<MODE != 0>(a, tb + j);
     if (warp == 0) {
         umma::tmem_alloc(&tmem_base, 512);
         umma::tmem_relinquish();
@@ -828,7 +856,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         float m_used = -INFINITY, l_sum = 0.0f, best = -INFINITY;
         int best_slot = 0;
         for (int t = 0; t < n_tiles && live; ++t) {
-            const TileInfo ti = tile_info<MODE != 0>(a, tb + t);
+            const TileInfo ti = tile_at<MODE != 0>(a, tile_tab, tb, t);
             live = __all_sync(0xffffffffu, ws::wait(&sfull[i], t & 1, vfail, a.wait_ns));
             if (!live) break;
             umma::tc_fence_after();
@@ -991,7 +1019,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                           isv ? a.voutv : a.koutv,
                           isv ? a.vouti : a.kouti, isv ? Vt0 : Kt0, isv ? vfull : kfull,
                           isv ? vfree : kfree,
-                          kNbuf, !isv && a.psac_p != nullptr};
+                          kNbuf, !isv && a.psac_p != nullptr, tile_tab};
         if constexpr (MODE == 0) {
             produce_fast<D, BITS, false, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         } else if constexpr (MODE == 1) {
