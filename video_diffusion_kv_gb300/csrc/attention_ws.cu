@@ -1127,15 +1127,16 @@ static qvg_status attn_ws(const AttnWsArgs &a, int splits, cudaStream_t st) {
 static int attn_sm_count() { return sm_count_current(); }
 
 // Number of cache splits: when (query blocks x query heads) CTAs leave SMs
-// idle, each (block, head) pair is split over enough CTAs to reach about two
-// per SM, with at least kMinSplitTiles cache tiles per split, at most
-// kMaxSplits.
+// idle, each (block, head) pair is split over as many CTAs as fill the SMs
+// once (one CTA per SM: the kernel's shared and tensor memory allow no
+// more, and a second wave would pay every split's pipeline start again),
+// with at least kMinSplitTiles cache tiles per split, at most kMaxSplits.
 constexpr int kMaxSplits = 32, kMinSplitTiles = 4;
 int attention_splits(int Nq, int Hq, int n_tiles) {
     const int ctas = ceil_div(std::max(Nq, 1), 256) * Hq;
     const int sm = attn_sm_count();
     if (ctas >= sm) return 1;
-    int s = std::min(kMaxSplits, ceil_div(2 * sm, ctas));
+    int s = std::min(kMaxSplits, sm / ctas);
     if (n_tiles >= 0) s = std::min(s, std::max(1, n_tiles / kMinSplitTiles));
     return std::max(1, s);
 }
