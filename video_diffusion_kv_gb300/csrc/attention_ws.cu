@@ -748,7 +748,8 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 // with the other's softmax (issue turns) measured slower.
 // mbarriers (phase = tile index / kNbuf for the buffers, tile index else):
 //   kfull/vfull  producers -> issuers   tile written (one arrival per slot)
-//   kfree/vfree  MMA commits -> producer tile consumed (S_0 and S_1 / PV_0 and PV_1)
+//   kfree/vfree  MMA commits -> producer tile consumed (S_0 and S_1 / PV_0 and PV_1;
+//                S_0 / PV_0 alone when query tile 1 is past Nq)
 //   sfull[i]     MMA commit -> group i   S_i(t) ready (and PV_i(t - 1) done)
 //   pfull[i]     group i -> its issuer   P_i(t) in TMEM, O_i rescaled (one arrival per warp)
 //   ofull[i]     MMA commit -> group i   the last PV_i done (epilogue)
@@ -778,6 +779,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     const int n_all = a.n_ctiles + ceil_div(a.n_raw, QVG_TILE), z = blockIdx.z;
     const int tb = static_cast<int>(static_cast<long long>(n_all) * z / gridDim.z);
     const int n_tiles = static_cast<int>(static_cast<long long>(n_all) * (z + 1) / gridDim.z) - tb;
+    // query tiles with at least one query row: a second tile past Nq issues
+    // no products and runs no softmax
+    const int n_grp = q0 + 128 < a.Nq ? 2 : 1;
 
     // Q tiles -> fp16 (exact for bf16 values in fp16's normal range), swizzled K-major
     for (int i = tid; i < 256 * (D / 8); i += kThreads) {
@@ -798,16 +802,16 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     if (tid == 0) {
         for (int b = 0; b < kNbuf; ++b) {
             umma::mbar_init(&kfull[b], 128);
-            umma::mbar_init(&kfree[b], 2);
+            umma::mbar_init(&kfree[b], n_grp);
             umma::mbar_init(&vfull[b], 128);
-            umma::mbar_init(&vfree[b], 2);
+            umma::mbar_init(&vfree[b], n_grp);
         }
         for (int i = 0; i < 2; ++i) {
             umma::mbar_init(&sfull[i], 1);
             umma::mbar_init(&pfull[i], 4);
             umma::mbar_init(&ofull[i], 1);
         }
-        umma::mbar_init(&drain, 2);  // the two issuing lanes
+        umma::mbar_init(&drain, n_grp);  // the issuing lanes
         umma::mbar_init(&never, 1);  // nothing arrives: the bounded-wait test hook
         umma::fence_barrier_init();
         fail = 0;
@@ -819,7 +823,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     const uint32_t tmem = tmem_base;
     volatile int *vfail = &fail;
 
-    if (warp < 8) {
+    if (warp < 4 * n_grp) {
         // ------------------------------------------------ softmax of tile i
         const int i = warp >> 2, r = tid & 127;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -1011,7 +1015,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
             umma::mma_commit(&drain);
             umma::mbar_wait(&drain, 0, kWaitNs);
         }
-    } else {
+    } else if (warp >= 8) {
         // ------------------------------------------------ K / V producers (thread = slot)
         const bool isv = warp >= 12;
         const Producer pr{isv ? a.vcodes : a.kcodes, isv ? a.vscales : a.kscales, isv ? a.vids : a.kids,
