@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # stripped) so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "15f336d22d257c991a4c603b24c390ec8a648e30d69880c44102f3f724263a03": 80424448 + 3613184,
+    "272c4611a81c06db02391dd52d818238566167769b2032049a8fc80ae5df3210": 80422144 + 3709440,
 }
 
 
