@@ -159,8 +159,8 @@ __device__ __forceinline__ int2 tile_entry(const AttnWsArgs &a, int t) {
 
 // Tile tb + t from the CTA's table (t counts from tb).
 template <bool RAW>
-__device__ __forceinline__ TileInfo tile_at(const AttnWsArgs &a, const int2 *tab, int tb, int t) {
-    if (t < kTabMax) {
+__device__ __forceinline__ TileInfo tile_at(const AttnWsArgs &a, const int2 *tab, int tab_n, int tb, int t) {
+    if (t < tab_n) {
         const int2 e = tab[t];
         if (e.x != kTabDirect) return TileInfo{e.y >> 8, e.x, e.y & 0xFF};
     }
@@ -379,7 +379,9 @@ struct Producer {
     uint64_t *full, *freeb;
     int nbuf;
     bool psac;
-    const int2 *tab;  // the CTA's tile table
+    const int2 *tab;  // the CTA's tile table and its length
+    int tab_n;
+    uint8_t *pbuf;    // PSAC on the tensor core: the P_hat operand of each K buffer, or NULL
 };
 
 template <int D, int BITS, bool OUTL, bool RAW>
@@ -391,12 +393,17 @@ __device__ __forceinline__ void load_tile_half(const AttnWsArgs &a, const Produc
         load_half_raw<D, BITS>(ti.chunk == -2 ? pr.anch : pr.raw, a.H, h, ti.base + r, kb, hd);
 }
 
-// One stage, no PSAC.  The loads of one 64-channel half are always in
-// flight while the previous half is decoded (two register sets, A for the
-// first half of a tile and B for the second when D = 128); table entries and
-// cluster ids run two tiles ahead (ids are read for cache tiles only, whose
-// slots t * QVG_TILE + r < n_slots <= capacity: in bounds).
-template <int D, int BITS, bool OUTL, bool RAW>
+// One stage.  The loads of one 64-channel half are always in flight while
+// the previous half is decoded (two register sets, A for the first half of a
+// tile and B for the second when D = 128); table entries and cluster ids run
+// two tiles ahead (ids are read for cache tiles only, whose slots
+// t * QVG_TILE + r < n_slots <= capacity: in bounds).
+// PSAC (K only): the slot's correction P_hat U^T is not added here; the slot
+// writes P_hat = fp16(S_P p_k), k < 8, as row r of the tile's K = 16 operand
+// (no swizzle: row r at (r / 8) * 256 + (r % 8) * 16, columns 8..15 zero),
+// and the S product adds (Q U) P_hat^T on the tensor core.  Raw tiles and
+// padding slots write zeros.
+template <int D, int BITS, bool OUTL, bool RAW, bool PSAC = false>
 __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
                                              int n_tiles, volatile int *vfail) {
     constexpr int KB = D / 64, TB = KB * 16384;
@@ -404,11 +411,11 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
     TileInfo ti0{}, ti1{};
     int id0 = 0, id1 = 0;
     if (n_tiles > 0) {
-        ti0 = tile_at<RAW>(a, pr.tab, tb, 0);
+        ti0 = tile_at<RAW>(a, pr.tab, pr.tab_n, tb, 0);
         if (a.C > 0 && ti0.chunk >= 0) id0 = pr.ids[id_row];
     }
     if (n_tiles > 1) {
-        ti1 = tile_at<RAW>(a, pr.tab, tb, 1);
+        ti1 = tile_at<RAW>(a, pr.tab, pr.tab_n, tb, 1);
         if (a.C > 0 && ti1.chunk >= 0) id1 = pr.ids[id_row + QVG_TILE];
     }
     HalfData<BITS> A, B;
@@ -419,10 +426,19 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         TileInfo ti2{};
         int id2 = 0;
         if (t + 2 < n_tiles) {
-            ti2 = tile_at<RAW>(a, pr.tab, tb, t + 2);
+            ti2 = tile_at<RAW>(a, pr.tab, pr.tab_n, tb, t + 2);
             if (a.C > 0 && ti2.chunk >= 0) id2 = pr.ids[id_row + static_cast<size_t>(t + 2) * QVG_TILE];
         }
         const bool valid = r < ti0.nvalid, valid1 = t + 1 < n_tiles && r < ti1.nvalid;
+        int2 pv = make_int2(0, 0);
+        uint32_t ps = 0u;
+        if constexpr (PSAC) {
+            if (valid && ti0.chunk >= 0) {
+                const size_t prow = static_cast<size_t>(h) * a.cap + ti0.base + r;
+                pv = *reinterpret_cast<const int2 *>(a.psac_p + prow * QVG_PSAC_RANK);
+                ps = a.psac_s[prow];
+            }
+        }
         if constexpr (KB == 2) {
             if (valid) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, ti0, r, id0, 1, B);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
@@ -449,6 +465,17 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             } else {
                 zero_line(T);
             }
+        }
+        if constexpr (PSAC) {
+            const float S = f16_to_f32(static_cast<uint16_t>(ps));
+            float pk[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                pk[k] = S * static_cast<float>(static_cast<int8_t>((pv.x >> (8 * k)) & 0xff));
+                pk[k + 4] = S * static_cast<float>(static_cast<int8_t>((pv.y >> (8 * k)) & 0xff));
+            }
+            *reinterpret_cast<uint4 *>(pr.pbuf + b * 4096 + (r >> 3) * 256 + (r & 7) * 16) =
+                make_uint4(h2(pk[0], pk[1]), h2(pk[2], pk[3]), h2(pk[4], pk[5]), h2(pk[6], pk[7]));
         }
         umma::fence_proxy_async_smem();
         umma::mbar_arrive(&pr.full[b]);
@@ -623,11 +650,11 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
     uint32_t idw[4], idn[4];
     float pk[QVG_PSAC_RANK];
     if (n_tiles > 0) {
-        ti = tile_at<true>(a, pr.tab, tb, 0);
+        ti = tile_at<true>(a, pr.tab, pr.tab_n, tb, 0);
         load_stage_ids<D>(a, pr, h, ti, r, idw);
     }
     if (n_tiles > 1) {
-        tn = tile_at<true>(a, pr.tab, tb, 1);
+        tn = tile_at<true>(a, pr.tab, pr.tab_n, tb, 1);
         load_stage_ids<D>(a, pr, h, tn, r, idn);
     }
     QuarterData<BITS> cur, nxt;
@@ -710,7 +737,7 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 #pragma unroll
             for (int i = 0; i < 4; ++i) idw[i] = idn[i];
             if (t1 + 1 < n_tiles) {
-                tn = tile_at<true>(a, pr.tab, tb, t1 + 1);
+                tn = tile_at<true>(a, pr.tab, pr.tab_n, tb, t1 + 1);
                 load_stage_ids<D>(a, pr, h, tn, r, idn);
             }
         }
@@ -755,7 +782,14 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 //   ofull[i]     MMA commit -> group i   the last PV_i done (epilogue)
 // MODE 0: one-stage caches without the outlier split or PSAC, no raw tiles;
 // MODE 1: the same with raw bf16 tiles (the current chunk, anchor chunks);
-// MODE 2: several stages, PSAC or the outlier split (out-of-line producers).
+// MODE 2: several stages, PSAC or the outlier split (out-of-line producers);
+// MODE 3: one stage with PSAC on K and no outlier split (raw tiles allowed):
+//         the correction runs on the tensor core as S_i += (Q_i U_c) P_hat^T,
+//         one K = 16 product per S batch.  Q_i U_c (fp16, 128 x 8, computed
+//         in fp32 by the softmax threads when a chunk c starts) and P_hat
+//         (written by the K producers) are no-swizzle K-major operands of
+//         4 KB, zero in columns 8..15; the tile table is cut to 2048 entries
+//         to make room.
 // Separate instantiations keep the out-of-line producers' call sites, which
 // cost the plain kernel 7 % when present, out of modes 0 and 1.
 template <int D, int BITS, bool TOP1, int MODE>
@@ -763,14 +797,17 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     using namespace ws;
     constexpr int KB = D / 64;
     constexpr int TB = KB * 16384;  // one 128 x D fp16 tile
+    constexpr bool PTC = MODE == 3;
+    constexpr int kTab = PTC ? 2048 : kTabMax;
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     uint8_t *sm = sm_raw + ((1024u - (umma::smem_u32(sm_raw) & 1023u)) & 1023u);
     uint8_t *Q0 = sm, *Q1 = Q0 + TB, *Kt0 = Q1 + TB, *Vt0 = Kt0 + kNbuf * TB;
+    uint8_t *PA = Vt0 + kNbuf * TB, *PB = PA + 2 * 4096;  // MODE 3: Q_i U_c (two), P_hat (kNbuf)
     __shared__ uint64_t kfull[kNbuf], kfree[kNbuf], vfull[kNbuf], vfree[kNbuf], sfull[2], pfull[2], ofull[2], drain,
         never;
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
-    __shared__ int2 tile_tab[kTabMax];
+    __shared__ int2 tile_tab[kTab];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hq = blockIdx.y, h = hq / a.grp, q0 = blockIdx.x * 256;
@@ -794,7 +831,10 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         }
         *reinterpret_cast<uint4 *>((rr < 128 ? Q0 : Q1) + kb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
-    for (int j = tid; j < min(n_tiles, kTabMax); j += kThreads) tile_tab[j] = tile_entry<MODE != 0>(a, tb + j);
+    for (int j = tid; j < min(n_tiles, kTab); j += kThreads) tile_tab[j] = tile_entry<MODE != 0>(a, tb + j);
+    if constexpr (PTC) {
+        for (int j = tid; j < (2 + kNbuf) * 4096 / 16; j += kThreads) reinterpret_cast<uint4 *>(PA)[j] = make_uint4(0, 0, 0, 0);
+    }
     if (warp == 0) {
         umma::tmem_alloc(&tmem_base, 512);
         umma::tmem_relinquish();
@@ -831,6 +871,47 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         const bool issuer = (warp & 3) == 0 && lane == 0;
         const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16_bmn(128, D, 0);
         const uint32_t qa = umma::smem_u32(i ? Q1 : Q0), ka = umma::smem_u32(Kt0), va = umma::smem_u32(Vt0);
+        const uint32_t pa = umma::smem_u32(PA + i * 4096), pb = umma::smem_u32(PB);
+        // MODE 3: row r of Q_i U_c, fp32 FMAs in ascending channel order, to fp16
+        int a_chunk = -1;
+        auto psac_qu = [&](int c) {
+            const float *U = a.psac_basis + (static_cast<size_t>(c) * a.H + h) * D * QVG_PSAC_RANK;
+            const uint8_t *Qi = i ? Q1 : Q0;
+            float acc[QVG_PSAC_RANK];
+#pragma unroll
+            for (int k = 0; k < QVG_PSAC_RANK; ++k) acc[k] = 0.0f;
+#pragma unroll 1
+            for (int ci = 0; ci < D / 8; ++ci) {
+                const uint4 qv = *reinterpret_cast<const uint4 *>(Qi + (ci >> 3) * 16384 + r * 128 + (((ci & 7) ^ (r & 7)) << 4));
+                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float q = f16_to_f32(static_cast<uint16_t>(qw[e >> 1] >> (16 * (e & 1))));
+                    const float4 u0 = *reinterpret_cast<const float4 *>(U + (ci * 8 + e) * QVG_PSAC_RANK);
+                    const float4 u1 = *reinterpret_cast<const float4 *>(U + (ci * 8 + e) * QVG_PSAC_RANK + 4);
+                    acc[0] = fmaf(q, u0.x, acc[0]);
+                    acc[1] = fmaf(q, u0.y, acc[1]);
+                    acc[2] = fmaf(q, u0.z, acc[2]);
+                    acc[3] = fmaf(q, u0.w, acc[3]);
+                    acc[4] = fmaf(q, u1.x, acc[4]);
+                    acc[5] = fmaf(q, u1.y, acc[5]);
+                    acc[6] = fmaf(q, u1.z, acc[6]);
+                    acc[7] = fmaf(q, u1.w, acc[7]);
+                }
+            }
+            *reinterpret_cast<uint4 *>(PA + i * 4096 + (r >> 3) * 256 + (r & 7) * 16) =
+                make_uint4(h2(acc[0], acc[1]), h2(acc[2], acc[3]), h2(acc[4], acc[5]), h2(acc[6], acc[7]));
+            umma::fence_proxy_async_smem();
+            a_chunk = c;
+        };
+        if constexpr (PTC) {
+            // the first chunk's Q_i U, complete before this group's first S product
+            if (n_tiles > 0) {
+                const int c0 = tile_at<true>(a, tile_tab, kTab, tb, 0).chunk;
+                if (c0 >= 0) psac_qu(c0);
+            }
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + i) : "memory");
+        }
         // S_i(t) = Q_i K(t)^T into TMEM columns [128 i, 128 i + 128) once K(t)
         // is written (rolled issue loops: a descriptor's low 14 bits are the
         // shared address / 16, which these offsets never carry out of)
@@ -844,6 +925,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 const uint32_t off16 = ((s >> 2) * 16384 + (s & 3) * 32) >> 4;
                 umma::mma_f16(tmem + i * 128, dq + off16, dk + off16, idS, s != 0);
             }
+            if constexpr (PTC)
+                umma::mma_f16(tmem + i * 128, umma::desc_noswz(pa, 128, 256), umma::desc_noswz(pb + b * 4096, 128, 256),
+                              idS, 1u);
             umma::mma_commit(&sfull[i]);
             umma::mma_commit(&kfree[b]);
             return true;
@@ -860,7 +944,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         float m_used = -INFINITY, l_sum = 0.0f, best = -INFINITY;
         int best_slot = 0;
         for (int t = 0; t < n_tiles && live; ++t) {
-            const TileInfo ti = tile_at<MODE != 0>(a, tile_tab, tb, t);
+            const TileInfo ti = tile_at<MODE != 0>(a, tile_tab, kTab, tb, t);
             live = __all_sync(0xffffffffu, ws::wait(&sfull[i], t & 1, vfail, a.wait_ns));
             if (!live) break;
             umma::tc_fence_after();
@@ -940,6 +1024,14 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                 umma::tmem_st16(tS + c0 / 2, pk);
             }
             l_sum = l_sum * corr + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+            if constexpr (PTC) {
+                // S_i(t + 1) is issued after this group's P_i(t): Q_i U of its
+                // chunk goes in now (S_i(t), the last reader, has completed)
+                if (t + 1 < n_tiles) {
+                    const int c1 = tile_at<true>(a, tile_tab, kTab, tb, t + 1).chunk;
+                    if (c1 >= 0 && c1 != a_chunk) psac_qu(c1);
+                }
+            }
             umma::tmem_st_wait();
             umma::tc_fence_before();
             __syncwarp();
@@ -1023,9 +1115,14 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                           isv ? a.voutv : a.koutv,
                           isv ? a.vouti : a.kouti, isv ? Vt0 : Kt0, isv ? vfull : kfull,
                           isv ? vfree : kfree,
-                          kNbuf, !isv && a.psac_p != nullptr, tile_tab};
+                          kNbuf, !isv && a.psac_p != nullptr, tile_tab, kTab, PTC ? PB : nullptr};
         if constexpr (MODE == 0) {
             produce_fast<D, BITS, false, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+        } else if constexpr (MODE == 3) {
+            if (isv)
+                produce_fast<D, BITS, false, true, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+            else
+                produce_fast<D, BITS, false, true, true>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         } else if constexpr (MODE == 1) {
             produce_fast<D, BITS, false, true>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         } else {
@@ -1106,7 +1203,7 @@ __global__ void __launch_bounds__(256) k_attn_merge(const float *__restrict__ po
 
 template <int D, int BITS, bool TOP1, int MODE>
 static qvg_status attn_ws_t(const AttnWsArgs &a, int a_splits, cudaStream_t st) {
-    constexpr size_t smem = (2 + 2 * ws::kNbuf) * (D / 64) * 16384 + 1024;
+    constexpr size_t smem = (2 + 2 * ws::kNbuf) * (D / 64) * 16384 + (MODE == 3 ? (2 + ws::kNbuf) * 4096 : 0) + 1024;
     {
         static std::atomic<uint64_t> done{0};
         const qvg_status s = smem_limit_once(done, reinterpret_cast<const void *>(k_attention_ws<D, BITS, TOP1, MODE>),
@@ -1121,6 +1218,8 @@ static qvg_status attn_ws_t(const AttnWsArgs &a, int a_splits, cudaStream_t st) 
 
 template <int D, int BITS>
 static qvg_status attn_ws(const AttnWsArgs &a, int splits, cudaStream_t st) {
+    if (a.L == 1 && a.psac_p && !a.kouti)
+        return a.top1 ? attn_ws_t<D, BITS, true, 3>(a, splits, st) : attn_ws_t<D, BITS, false, 3>(a, splits, st);
     if (a.L > 1 || a.psac_p || a.kouti)
         return a.top1 ? attn_ws_t<D, BITS, true, 2>(a, splits, st) : attn_ws_t<D, BITS, false, 2>(a, splits, st);
     if (a.n_raw > 0 || a.chunk_anchor)
