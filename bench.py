@@ -37,7 +37,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # workload, from an ncu capture of `dram__bytes_read.sum,dram__bytes_write.sum`
 # on the same command, keyed by the SHA-256 of the kernel's code (comments
 # stripped) so that a changed kernel reports null until re-measured.
-ATTN_SOURCES = ("attention_ws.cu", "umma.cuh", "common.cuh")
+ATTN_SOURCES = ("attention_ws.cuh", "attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
     "272c4611a81c06db02391dd52d818238566167769b2032049a8fc80ae5df3210": 80422144 + 3709440,
 }
