@@ -119,7 +119,9 @@ typedef struct {
  * grows chunk by chunk ([QVG] "overall framework": the cache is processed
  * chunk by chunk; [P1] section 1: the cache grows linearly with frames).
  * Every buffer is caller-allocated device memory of the size that
- * qvg_cache_bytes reports.  Chunks start at slot multiples of QVG_TILE; the
+ * qvg_cache_bytes reports, 16-byte aligned (the kernels read it with vector
+ * loads; a misaligned buffer is refused with QVG_ERR_INVALID_ARG before any
+ * launch).  Chunks start at slot multiples of QVG_TILE; the
  * slots between a chunk's end and the next multiple are padding.
  *   codes      uint8 [L][H][capacity][d*bits/8]  packed offset-binary codes:
  *              element j of a row at bits (j*bits)%8 of byte (j*bits)/8,

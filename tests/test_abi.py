@@ -283,6 +283,39 @@ def test_noalloc_checks_arguments_before_scratch_size(lib):
     assert c.n_chunks == 0 and full.n_chunks == 2 and big.n_chunks == 0
 
 
+def test_misaligned_cache_buffer_is_refused(lib):
+    """Every cache buffer must be 16-byte aligned (the kernels read them with
+    vector loads): a cache with any one buffer 8 bytes off is refused by
+    compress, decompress and attention before anything is launched.  The
+    calls are otherwise valid, so this runs only where no GPU is visible."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only check: the fake cache pointers must never reach a device")
+    fields = [f for f, _ in qvg._Cache._fields_[6:]]
+    assert len(fields) == qvg.QVG_CACHE_NBUF
+    p = _params(C=16, group=32, flags=qvg.QVG_OUTLIER)
+    p.anchor_every = 4
+    x, q, o = ct.c_void_p(0x2000), ct.c_void_p(0x3000), ct.c_void_p(0x4000)
+    ws = ct.c_void_p(0x100000)
+    # control: the same calls on an aligned cache pass the host checks (and
+    # then fail for want of a device), so the refusals below are the alignment's
+    c = _fake_cache(n_chunks=1, n_tokens=128)
+    assert lib.qvg_decompress(ct.byref(p), ct.byref(c), 0, 64, o, 0, None) != qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_attention(ct.byref(p), q, 4, 2, ct.byref(c), ct.byref(c), 0.0, o, 0, None, None, None, 0,
+                             None) != qvg.QVG_ERR_INVALID_ARG
+    assert lib.qvg_compress_chunk(ct.byref(p), x, 100, None, None, ct.byref(c), ws, 1 << 30,
+                                  None) != qvg.QVG_ERR_INVALID_ARG
+    for f in fields:
+        c = _fake_cache(n_chunks=1, n_tokens=128)
+        setattr(c, f, ct.c_void_p(0x1008))
+        assert lib.qvg_decompress(ct.byref(p), ct.byref(c), 0, 64, o, 0, None) == qvg.QVG_ERR_INVALID_ARG, f
+        assert lib.qvg_attention(ct.byref(p), q, 4, 2, ct.byref(c), ct.byref(c), 0.0, o, 0, None, None, None, 0,
+                                 None) == qvg.QVG_ERR_INVALID_ARG, f
+        assert lib.qvg_compress_chunk(ct.byref(p), x, 100, None, None, ct.byref(c), ws, 1 << 30,
+                                      None) == qvg.QVG_ERR_INVALID_ARG, f
+        assert c.n_chunks == 1 and c.n_tokens == 128
+
+
 def test_noalloc_scratch_size_matches_header():
     """The binding's scratch size is the header's QVG_NOALLOC_SCRATCH_BYTES."""
     src = open(os.path.join(ROOT, "include", "qvg.h")).read()

@@ -128,6 +128,11 @@ qvg_status check_cache(const qvg_params *p, const qvg_cache *c) {
         return QVG_ERR_INVALID_ARG;
     if ((p->flags & QVG_OUTLIER) && (!c->outl_val || !c->outl_idx)) return QVG_ERR_INVALID_ARG;
     if (p->anchor_every > 0 && (!c->anchor || !c->chunk_anchor)) return QVG_ERR_INVALID_ARG;
+    // every buffer is read with vector loads of up to 16 bytes
+    const void *bufs[] = {c->codes,  c->scales, c->ids,        c->cent,     c->chunk_start, c->chunk_len, c->tile_chunk,
+                          c->psac_p, c->psac_s, c->psac_basis, c->outl_val, c->outl_idx,    c->anchor,    c->chunk_anchor};
+    for (const void *b : bufs)
+        if (reinterpret_cast<uintptr_t>(b) % 16 != 0) return QVG_ERR_INVALID_ARG;
     return QVG_OK;
 }
 
