@@ -185,11 +185,14 @@ struct HalfData {
     uint4 cw[BITS == 2 ? 1 : 2];  // 64 codes
     uint32_t s2[4];               // fp16 scales of the 8-channel blocks, two per word
     uint4 cr[8];                  // 64 bf16 centroid channels
-    uint32_t oi, ov;              // outlier split, groups of >= 32 channels: per group of the
-                                  // half, the channel split off (byte; 0xFF none) and its fp16
+    uint32_t oi[2], ov[4];        // outlier split: per group of the half (1, 2, 4 or 8 groups of
+                                  // 64, 32, 16 or 8 channels), the channel split off (byte g of
+                                  // oi; 0xFF none) and its fp16 value (half g of ov)
 };
 
-template <int D, int BITS, bool OUTL>
+// OUTL: 0 without the outlier split, else the groups per 64-channel half
+// (1, 2, 4 or 8 for groups of 64, 32, 16 or 8 channels).
+template <int D, int BITS, int OUTL>
 __device__ __forceinline__ void load_half(const AttnWsArgs &a, const uint8_t *codes, const uint16_t *scales,
                                           const uint16_t *cent, const uint16_t *outv, const uint8_t *outi, int h,
                                           int chunk, int slot, int id, int kb, HalfData<BITS> &hd) {
@@ -197,15 +200,34 @@ __device__ __forceinline__ void load_half(const AttnWsArgs &a, const uint8_t *co
     constexpr int HB = 64 * BITS / 8;
     const int ng = D / a.group;
     const size_t srow = static_cast<size_t>(h) * a.cap + slot;
-    hd.oi = 0xFFFFu;
-    hd.ov = 0u;
-    if (OUTL) {  // one group per half (G = 64) or two (G = 32)
-        const int g0 = (kb * 64) / a.group;
-        hd.oi = (hd.oi & 0xFF00u) | outi[srow * ng + g0];
-        hd.ov = outv[srow * ng + g0];
-        if (a.group == 32) {
-            hd.oi = (hd.oi & 0x00FFu) | (static_cast<uint32_t>(outi[srow * ng + g0 + 1]) << 8);
-            hd.ov |= static_cast<uint32_t>(outv[srow * ng + g0 + 1]) << 16;
+    hd.oi[0] = hd.oi[1] = 0xFFFFFFFFu;
+    hd.ov[0] = hd.ov[1] = hd.ov[2] = hd.ov[3] = 0u;
+    if (OUTL) {
+        // the half's NG groups are entries [srow * ng + kb * NG, + NG) of the
+        // side list: a multiple of NG, so one aligned vector (the cache's
+        // buffers are 16-byte aligned)
+        constexpr int NG = OUTL;
+        const size_t e0 = srow * ng + static_cast<size_t>(kb) * NG;
+        if constexpr (NG == 1) {
+            hd.oi[0] = 0xFFFFFF00u | outi[e0];
+            hd.ov[0] = outv[e0];
+        } else if constexpr (NG == 2) {
+            hd.oi[0] = 0xFFFF0000u | *reinterpret_cast<const uint16_t *>(outi + e0);
+            hd.ov[0] = *reinterpret_cast<const uint32_t *>(outv + e0);
+        } else if constexpr (NG == 4) {
+            hd.oi[0] = *reinterpret_cast<const uint32_t *>(outi + e0);
+            const uint2 v = *reinterpret_cast<const uint2 *>(outv + e0);
+            hd.ov[0] = v.x;
+            hd.ov[1] = v.y;
+        } else {
+            const uint2 i2 = *reinterpret_cast<const uint2 *>(outi + e0);
+            hd.oi[0] = i2.x;
+            hd.oi[1] = i2.y;
+            const uint4 v = *reinterpret_cast<const uint4 *>(outv + e0);
+            hd.ov[0] = v.x;
+            hd.ov[1] = v.y;
+            hd.ov[2] = v.z;
+            hd.ov[3] = v.w;
         }
     }
 #pragma unroll
@@ -239,8 +261,8 @@ __device__ __forceinline__ void load_half_raw(const uint16_t *raw, int H, int h,
     for (int i = 0; i < (BITS == 2 ? 1 : 2); ++i) hd.cw[i] = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) hd.s2[i] = 0u;
-    hd.oi = 0xFFFFu;
-    hd.ov = 0u;
+    hd.oi[0] = hd.oi[1] = 0xFFFFFFFFu;
+    hd.ov[0] = hd.ov[1] = hd.ov[2] = hd.ov[3] = 0u;
     const uint16_t *row = raw + (static_cast<size_t>(j) * H + h) * D + kb * 64;
 #pragma unroll
     for (int i = 0; i < 8; ++i) hd.cr[i] = *reinterpret_cast<const uint4 *>(row + 8 * i);
@@ -314,20 +336,21 @@ __device__ __forceinline__ void decode_store_half(const HalfData<BITS> &hd, uint
 // rebuild of an outlier, o its stored fp16 value.  c is read back from that
 // slot: bf16 -> fp16 is exact for |c| >= 2^-14 (and for 0), and only a
 // centroid channel in fp16's subnormal range is re-read from the row.
-template <int D, int BITS>
+template <int D, int BITS, int NG>
 __device__ __forceinline__ void patch_outliers(const AttnWsArgs &a, const uint16_t *cent, const HalfData<BITS> &hd,
                                                int h, int chunk, int id, int kb, uint8_t *dst, int r) {
+    constexpr int G = 64 / NG;
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        const uint32_t oi = (hd.oi >> (8 * g)) & 0xFFu;
-        if (oi != 0xFFu && (g == 0 || a.group == 32)) {
-            const int j = g * a.group + static_cast<int>(oi);  // channel within the half
+    for (int g = 0; g < NG; ++g) {
+        const uint32_t oi = (hd.oi[g >> 2] >> (8 * (g & 3))) & 0xFFu;
+        if (oi != 0xFFu) {
+            const int j = g * G + static_cast<int>(oi);  // channel within the half
             __half *p = reinterpret_cast<__half *>(dst + (((j >> 3) ^ (r & 7)) << 4) + (j & 7) * 2);
             float c = __half2float(*p);
             if (a.C > 0 && c != 0.0f && fabsf(c) < 6.103515625e-05f)
                 c = __uint_as_float(static_cast<uint32_t>(
                         cent[((static_cast<size_t>(h) * a.max_chunks + chunk) * a.C + id) * D + kb * 64 + j]) << 16);
-            *p = __float2half_rn(__fadd_rn(f16_to_f32(static_cast<uint16_t>(hd.ov >> (16 * g))), c));
+            *p = __float2half_rn(__fadd_rn(f16_to_f32(static_cast<uint16_t>(hd.ov[g >> 1] >> (16 * (g & 1)))), c));
         }
     }
 }
@@ -389,7 +412,7 @@ struct Producer {
 // Stage l of a cache tile reads the stage's rows: every compressed array is
 // [L][H][...], so stage l of head h is row l * H + h (hl below).  A raw tile
 // has stage 0 only.
-template <int D, int BITS, bool OUTL, bool RAW>
+template <int D, int BITS, int OUTL, bool RAW>
 __device__ __forceinline__ void load_tile_half(const AttnWsArgs &a, const Producer &pr, int h, int hl,
                                                const TileInfo &ti, int r, int id, int kb, HalfData<BITS> &hd) {
     if (!RAW || ti.chunk >= 0)
@@ -414,7 +437,7 @@ __device__ __forceinline__ void load_tile_half(const AttnWsArgs &a, const Produc
 // of the tile's K = 16 operand (no swizzle: row r at (r / 8) * 256 +
 // (r % 8) * 16, columns 8..15 zero), and the S product adds (Q U) P_hat^T on
 // the tensor core.  Raw tiles and padding slots write zeros.
-template <int D, int BITS, bool OUTL, bool RAW, bool PSAC = false>
+template <int D, int BITS, int OUTL, bool RAW, bool PSAC = false>
 __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
                                              int n_tiles, volatile int *vfail, int L = 1) {
     constexpr int KB = D / 64, TB = KB * 16384;
@@ -460,14 +483,14 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
                 decode_store_half<BITS>(A, T, r);
-                if (OUTL) patch_outliers<D, BITS>(a, pr.cent, A, hl0, ti0.chunk, id0, 0, T, r);
+                if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, A, hl0, ti0.chunk, id0, 0, T, r);
             } else {
                 zero_line(T);
             }
             if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, l1 * a.H + h, ti1, r, id1, 0, A);
             if (valid) {
                 decode_store_half<BITS>(B, T + 16384, r);
-                if (OUTL) patch_outliers<D, BITS>(a, pr.cent, B, hl0, ti0.chunk, id0, 1, T + 16384, r);
+                if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, B, hl0, ti0.chunk, id0, 1, T + 16384, r);
             } else {
                 zero_line(T + 16384);
             }
@@ -477,7 +500,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
                 decode_store_half<BITS>(B, T, r);
-                if (OUTL) patch_outliers<D, BITS>(a, pr.cent, B, hl0, ti0.chunk, id0, 0, T, r);
+                if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, B, hl0, ti0.chunk, id0, 0, T, r);
             } else {
                 zero_line(T);
             }
@@ -510,14 +533,14 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
 
 // The outlier-split variant, out of line so that its register allocation
 // stays apart from the plain path's (inlined, both spill).
-template <int D, int BITS>
+template <int D, int BITS, int NG>
 __device__ __noinline__ void produce_fast_outl(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
                                                int n_tiles, volatile int *vfail, int L) {
-    produce_fast<D, BITS, true, true>(a, pr, h, r, tb, n_tiles, vfail, L);
+    produce_fast<D, BITS, NG, true>(a, pr, h, r, tb, n_tiles, vfail, L);
 }
 
-// Several stages, PSAC, or the outlier split with groups under 32 channels.
-// Work runs in steps of one 32-channel quarter of the slot's row and one
+// The outlier split together with PSAC (every other case takes the fast
+// producer, one stage per buffer fill).  Work runs in steps of one 32-channel quarter of the slot's row and one
 // stage, in the order (tile, quarter, stage).  Each step's codes, scales,
 // centroid slice and outlier entries are loaded one step ahead (register
 // sets A and B); the next tile's stage ids, table entry and PSAC codes one
@@ -805,9 +828,9 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 // MODE 0: one-stage caches without the outlier split or PSAC, no raw tiles;
 // MODE 1: no outlier split or PSAC, with raw bf16 tiles (the current chunk,
 //         anchor chunks) or several stages (one buffer fill per stage);
-// MODE 2: the outlier split (out-of-line producers: per-stage fills for
-//         groups of >= 32 channels without PSAC, else the general producer,
-//         which sums the stages and adds PSAC itself);
+// MODE 2: the outlier split (out-of-line producers: per-stage fills
+//         without PSAC, else the general producer, which sums the stages and
+//         adds PSAC itself);
 // MODE 3: PSAC on K without the outlier split (raw tiles and stages allowed):
 //         the correction runs on the tensor core as S_i += (Q_i U_c) P_hat^T,
 //         one K = 16 product after each tile's S batch.  Q_i U_c (fp16, 128 x 8, computed
@@ -848,7 +871,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     const int n_grp = q0 + 128 < a.Nq ? 2 : 1;
     // buffer fills per tile: one per stage, except where a producer sums the
     // stages itself (the general producer of mode 2)
-    const int n_stage = LS == 1 ? 1 : (MODE == 2 && (a.psac_p || a.group < 32)) ? 1 : a.L;
+    const int n_stage = LS == 1 ? 1 : (MODE == 2 && a.psac_p) ? 1 : a.L;
     static_assert(MODE >= 0 && MODE <= 3 && (LS == 1 || MODE != 0), "attention mode");
 
     // Q tiles -> fp16 (exact for bf16 values in fp16's normal range), swizzled K-major
@@ -1159,20 +1182,29 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                           isv ? vfree : kfree,
                           kNbuf, !isv && a.psac_p != nullptr, tile_tab, kTab, PTC ? PB : nullptr};
         if constexpr (MODE == 0) {
-            produce_fast<D, BITS, false, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
+            produce_fast<D, BITS, 0, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         } else if constexpr (MODE == 3) {
             if (isv)
-                produce_fast<D, BITS, false, true, false>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
+                produce_fast<D, BITS, 0, true, false>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
             else
-                produce_fast<D, BITS, false, true, true>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
+                produce_fast<D, BITS, 0, true, true>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
         } else if constexpr (MODE == 1) {
-            produce_fast<D, BITS, false, true>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
+            produce_fast<D, BITS, 0, true>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
         } else {
             // the outlier split: one stage per fill through the fast producer
-            // when groups have >= 32 channels and PSAC is off, else the
-            // general producer, which sums the stages itself (n_stage = 1)
-            if (!a.psac_p && a.group >= 32)
-                produce_fast_outl<D, BITS>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
+            // when PSAC is off, else the general producer, which sums the
+            // stages and adds the PSAC term itself (n_stage = 1)
+            if (!a.psac_p) {
+                const int ng = 64 / a.group;  // 1, 2, 4 or 8 (groups of 8 ... 64 channels)
+                if (ng == 1)
+                    produce_fast_outl<D, BITS, 1>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
+                else if (ng == 2)
+                    produce_fast_outl<D, BITS, 2>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
+                else if (ng == 4)
+                    produce_fast_outl<D, BITS, 4>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
+                else
+                    produce_fast_outl<D, BITS, 8>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
+            }
             else if (pr.outi)
                 produce_general<D, BITS, true>(a, pr, h, tid & 127, tb, n_tiles, vfail);
             else
