@@ -51,6 +51,7 @@ CASES = {
     "tiny_outlier": (W["tiny"], qvg.Params(C=16, L=1, bits=2, group=32, iters=10, seed=24, flags=qvg.QVG_OUTLIER), 2),
     "pro_outlier_L2": (W["qvgpro"], qvg.Params(C=16, L=2, bits=2, group=32, iters=10, seed=25, flags=qvg.QVG_OUTLIER), 2),
     "rtn_outlier_g8": (W["tiny"], qvg.Params(C=0, L=1, bits=4, group=8, iters=0, flags=qvg.QVG_OUTLIER), 2),
+    "tiny_outlier_g16": (W["tiny"], qvg.Params(C=16, L=1, bits=2, group=16, iters=10, seed=27, flags=qvg.QVG_OUTLIER), 2),
     "longcat_outlier": (W["longcat"], qvg.Params(C=256, L=1, bits=2, group=64, iters=8, seed=26, flags=qvg.QVG_OUTLIER), 2),
 }
 OUTL = lambda p: bool(p.flags & qvg.QVG_OUTLIER)
@@ -439,7 +440,7 @@ def test_attention_ar_longcat(Nq):
     assert top1.max().item() < kc.n_tokens + len(k_cur)
 
 
-@pytest.mark.parametrize("name", ["tiny_outlier", "pro_outlier_L2", "rtn_outlier_g8"])
+@pytest.mark.parametrize("name", ["tiny_outlier", "pro_outlier_L2", "rtn_outlier_g8", "tiny_outlier_g16"])
 def test_attention_with_outlier_split(name):
     """Attention and the AR step over caches whose K and V carry the
     outlier side list (one and two stages, RTN with G = 8), against the fp64
@@ -662,22 +663,27 @@ def test_query_stats_and_basis():
     assert 0.69 < frac.cpu().numpy().min() and frac.cpu().numpy().max() < 0.75
 
 
-@pytest.mark.parametrize("flags,anchor_every", [(qvg.QVG_QSAC, 0), (qvg.QVG_PSAC, 0), (qvg.QVG_QSAC | qvg.QVG_PSAC, 0),
-                                                (qvg.QVG_QSAC | qvg.QVG_PSAC, 2)])
-def test_quantwm_compress_and_attention(flags, anchor_every):
+@pytest.mark.parametrize("flags,anchor_every,L", [(qvg.QVG_QSAC, 0, 1), (qvg.QVG_PSAC, 0, 1),
+                                                  (qvg.QVG_QSAC | qvg.QVG_PSAC, 0, 1),
+                                                  (qvg.QVG_QSAC | qvg.QVG_PSAC, 2, 1), (qvg.QVG_PSAC, 0, 2),
+                                                  (qvg.QVG_PSAC | qvg.QVG_OUTLIER, 0, 1)])
+def test_quantwm_compress_and_attention(flags, anchor_every, L):
     """QuantWM caches (QSAC weights, PSAC on K; with anchor_every = 2 the
-    first chunk is a bf16 anchor, which carries no PSAC term): compression
-    against the fed oracle, PSAC codes, the rebuild, and attention (plain
-    and AR step) against the fp64 oracle."""
+    first chunk is a bf16 anchor, which carries no PSAC term; two stages
+    with PSAC; PSAC with the outlier split, which K and V then both carry):
+    compression against the fed oracle, PSAC codes, the rebuild, and
+    attention (plain and AR step) against the fp64 oracle.  The attention
+    kernel takes PSAC as a tensor-core product, one buffer fill per stage,
+    and with the outlier split the general producer."""
     w = _quantwm_small()
     qh = synth.history_queries(w, 22)
     M, wv, cnt = qvg.query_stats(to_dev(qh), w.H)
     U, _, _ = qvg.psac_basis(M, cnt)
-    p = qvg.Params(C=256, L=1, bits=2, group=64, iters=8, seed=23, flags=flags, anchor_every=anchor_every)
+    p = qvg.Params(C=256, L=L, bits=2, group=64, iters=8, seed=23, flags=flags, anchor_every=anchor_every)
     chunks = [(synth.chunk_kv(w, 23, k, synth.KIND_K), synth.chunk_kv(w, 23, k, synth.KIND_V)) for k in range(2)]
     cap = 2 * (-(-w.N // 128) * 128)
     kc = qvg.CompressedKV(p, w.H, w.d, cap, 2)
-    pv = qvg.Params(**{**p.__dict__, "flags": 0})
+    pv = qvg.Params(**{**p.__dict__, "flags": flags & qvg.QVG_OUTLIER})
     vc = qvg.CompressedKV(pv, w.H, w.d, cap, 2)
     for k, v in chunks:
         qvg.compress_chunk(p, to_dev(k), kc, qsac_w=wv, psac_basis=U)
