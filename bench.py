@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # stripped) so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cuh", "attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "272c4611a81c06db02391dd52d818238566167769b2032049a8fc80ae5df3210": 80422144 + 3709440,
+    "756afce020cc34f20d446d10d325c0c8b056025510d81d950a055326fcf5fe17": 80509952 + 3677696,
 }
 
 
