@@ -4,12 +4,12 @@
 // Quant VideoGen notes, "algorithm-system co-design": dequantisation is
 // fused with attention and the 2-bit codes stay packed in memory.  The
 // reconstructed K_hat = sum_l (S_l q_l + C_l) (+ the PSAC term P_hat U^T of
-// the QuantWM write-up) and V_hat only ever exist as fp16 tiles in shared
-// memory.
+// the QuantWM write-up) and V_hat only ever exist in shared memory (as fp16
+// tiles, one per stage) and as products in tensor memory.
 //
-// One CTA = two 128-row query tiles of one query head (ping-pong, so the
-// tensor core computes one tile's products while the other tile's softmax
-// runs); the warp roles and barriers are listed above the kernel.
+// One CTA = two 128-row query tiles of one query head, which share every
+// rebuilt K_hat / V_hat tile; the warp roles and barriers are listed above
+// the kernel.
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
 // O1 [384,384+D), fp32; P_i (fp16 pairs) over S_i's first 64 columns.  Per
 // cache tile t:
