@@ -706,12 +706,15 @@ def test_quantwm_compress_and_attention(flags, anchor_every, L):
             ref = oracle_rebuild(hk, p, k)
             assert np.abs(gpu - ref).max() <= 1e-3 * np.abs(ref).max()
     q = synth.history_queries(w, 24, n_tokens=300, stream=1)
-    out, _, _ = qvg.attention(p, to_dev(q), kc, vc)
+    out, _, top1 = qvg.attention(p, to_dev(q), kc, vc, want_top1=True)
     hv = host_cache(vc)
     kh = np.concatenate([oracle_rebuild(hk, p, k) for k in range(2)], 0)
     vh = np.concatenate([oracle_rebuild(hv, pv, k) for k in range(2)], 0)
-    ref, _, _ = oracle.attention(q, kh, vh, nthreads=NT)
+    ref, _, ram = oracle.attention(q, kh, vh, nthreads=NT)
     _assert_attention(out.cpu().numpy().astype(np.float64), ref, w.Hq)
+    # the top-1 slot (the shift rate's GPU side) over the rebuilt keys,
+    # PSAC term included
+    _assert_top1(top1.cpu().numpy(), q, kh, _slot_of_token(hk, 2), ram)
     # AR step on the same cache: the third chunk's raw K/V join the keys
     # (the PSAC term corrects cached keys only)
     kr, vr = synth.chunk_kv(w, 23, 2, synth.KIND_K)[:700], synth.chunk_kv(w, 23, 2, synth.KIND_V)[:700]
