@@ -796,7 +796,7 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 
 // Warp roles (16 warps):
 //   0-3, 4-7   softmax + epilogue of query tile i = 0 / 1 (thread = query row);
-//              lane 0 of warp 4i issues the tcgen05.mma of tile i, and warp 0
+//              lane 0 of warp 5i issues the tcgen05.mma of tile i, and warp 0
 //              owns the TMEM allocation
 //   8-11       K producers: rebuild the 128-slot K_hat tile (thread = slot)
 //   12-15      V producers: the same for V_hat
@@ -922,7 +922,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
         const int i = warp >> 2, r = tid & 127;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + i * 128 + lane_off, tO = tmem + 256 + i * 128 + lane_off;
-        const bool issuer = (warp & 3) == 0 && lane == 0;
+        // the issuing lanes sit in warps 0 and 5, on two different
+        // sub-partitions (warp w runs on sub-partition w % 4): on one they
+        // shared its issue slots with two producer warps, and the kernel
+        // took 4 % longer
+        const bool issuer = (warp & 3) == i && lane == 0;
         const uint32_t idS = umma::idesc_f16(128, 128, 0), idO = umma::idesc_f16_bmn(128, D, 0);
         const uint32_t qa = umma::smem_u32(i ? Q1 : Q0), ka = umma::smem_u32(Kt0), va = umma::smem_u32(Vt0);
         const uint32_t pa = umma::smem_u32(PA + i * 4096), pb = umma::smem_u32(PB);
