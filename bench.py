@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # stripped) so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cuh", "attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "756afce020cc34f20d446d10d325c0c8b056025510d81d950a055326fcf5fe17": 80509952 + 3677696,
+    "bcabf656761d1834226d4b101713ae568837a06e1376771d441a0c5cd59daa46": 80398592 + 3668480,
 }
 
 
