@@ -300,10 +300,12 @@ qvg_status qvg_compress_chunk_noalloc(const qvg_params *p, const void *x_bf16,
  * order.  With QVG_OUTLIER, a value split off from its group is rebuilt as
  * its fp16 copy plus the centroid ([P2] section 3.4); an anchor chunk's
  * slots give its stored bf16 K/V ([P2] section 3.3).
- *   out      [ntok][H][d] fp32 or bf16 (out_dtype), 4-byte aligned; the
- *            caller's device buffer.  Padding slots give 0.
+ *   out      [ntok][H][d] fp32 or bf16 (out_dtype), 4-byte aligned (16-byte
+ *            for fp32 and 8-byte for bf16 take vector stores); the caller's
+ *            device buffer.  Padding slots give 0.
  * Errors: QVG_ERR_INVALID_ARG for tok0 < 0, ntok < 0, tok0 + ntok past
- * n_tokens or a misaligned out; ntok = 0 does nothing.
+ * n_tokens or a misaligned out; QVG_ERR_UNSUPPORTED for H > 65535;
+ * ntok = 0 does nothing.
  */
 qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache,
                           int32_t tok0, int32_t ntok, void *out,

@@ -234,6 +234,17 @@ def test_decompress_ragged_range(name):
             want = full[tok0:tok0 + ntok].to(tdt)
             assert torch.equal(big[:ntok], want), (tok0, ntok, dt)
             assert bool((big[ntok:] == 7.0).all()), (tok0, ntok, dt)
+    # an output that is 4-byte but not vector aligned (one fp32 / two bf16
+    # elements past a 16-byte boundary) takes the 32-bit store path
+    tok0, ntok = 37, kc.n_tokens - 37 - 19
+    for dt, tdt, skip in ((qvg.QVG_OUT_F32, torch.float32, 1), (qvg.QVG_OUT_BF16, torch.bfloat16, 2)):
+        n = ntok * w.H * w.d
+        flat = torch.full((n + skip + 64,), 7.0, dtype=tdt, device="cuda")
+        view = flat[skip:skip + n].view(ntok, w.H, w.d)
+        assert view.data_ptr() % 16 != 0
+        qvg.decompress(p, kc, tok0, ntok, out_dtype=dt, out=view)
+        assert torch.equal(view, full[tok0:tok0 + ntok].to(tdt)), dt
+        assert bool((flat[:skip] == 7.0).all()) and bool((flat[skip + n:] == 7.0).all()), dt
 
 
 def _cache_with_chunks(w, p, chunks_kv, seed=0):

@@ -28,149 +28,269 @@ struct CacheView {
     int H, cap, max_chunks;
 };
 
-// Thread = token slot: a warp rebuilds 32 consecutive slots of one head
-// (their codes, scales and ids are contiguous), each thread its own row in
-// blocks of 32 channels (the block's codes, scales and centroid piece are
-// loaded before its arithmetic); the block's 32 x 32 results are stored
-// row by row through shared memory.  Per element, in stage order:
+// Thread = (token slot, 32 channels): D / 32 threads (TPR) rebuild one row
+// of one head, and each owns eight 4-channel pieces interleaved with the
+// row's other threads (piece i + TPR m, m = 0..7, for thread i), so that the
+// m-th store of the row's TPR threads writes 4 TPR contiguous channels --
+// whole 32-byte sectors -- and every store instruction of a warp is fully
+// used.  The row's packed codes are read whole by each of its threads (one
+// to four 16-byte loads) and the pieces' codes picked out of them.  Block
+// (x, y) takes consecutive slots of head y, whose codes, scales and ids are
+// contiguous.  A row costs two dependent memory round trips per stage:
+// first what depends on the slot alone (tile table entry, codes, scales,
+// id, outlier entries), then what needs the chunk (its start, length and
+// anchor row, the centroid pieces).  Per element, in stage order:
 // acc += fl(fl(S q) + c), then the PSAC term as an fp32 FMA chain over the
 // rank -- the same operations, in the same order, as any other rebuild.
 // OUTL: at the channel a stage split off from its group (code 0), the
-// stage's value is fl(o + c), o the stored fp16 outlier.
-template <int D, int BITS, bool PSAC, bool OUTL>
-__global__ void __launch_bounds__(256, (PSAC || OUTL) ? 2 : 3) k_decompress(CacheView cv, int L, int C, int group,
-                                                   int tok0, int ntok, float *out32,
-                                                   uint16_t *out16) {
-    constexpr int NB = D * BITS / 8, CB = 32 * BITS / 8;  // code bytes per row / per 32-channel block
-    const int lane = threadIdx.x & 31;
-    const int H = cv.H, ng = D / group;
-    const int nblk = ceil_div(ntok, 32);
-    const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (wid >= static_cast<long long>(H) * nblk) return;
-    // t0 < ntok (nblk = ceil(ntok / 32)); a lane past the end decodes nothing
-    // and takes part only in the warp's staged stores
-    const int h = static_cast<int>(wid / nblk), t0 = static_cast<int>(wid % nblk) * 32, t = t0 + lane;
-    const bool live = t < ntok;
-    const int nrow = min(32, ntok - t0);
-    const int slot = tok0 + (live ? t : t0);
-    const int chunk = cv.tile_chunk[slot / QVG_TILE];
-    const bool valid = live && slot >= cv.chunk_start[chunk] && slot < cv.chunk_start[chunk] + cv.chunk_len[chunk];
-    const int arow = cv.chunk_anchor ? cv.chunk_anchor[chunk] : -1;  // an anchor chunk's first row, or -1
-    const uint16_t *arow_p = arow >= 0 && valid ? cv.anchor + (static_cast<size_t>(arow + slot - cv.chunk_start[chunk]) * H + h) * D
-                                                : nullptr;
-    float pk[QVG_PSAC_RANK];
-    const float *U = nullptr;
-    if (PSAC && valid && !arow_p) {
-        const size_t prow = static_cast<size_t>(h) * cv.cap + slot;
-        const float pSp = f16_to_f32(cv.psac_s[prow]);
+// stage's value is fl(o + c), o the stored fp16 outlier.  VEC: the output is
+// 16-byte (fp32) or 8-byte (bf16) aligned and each piece takes one vector
+// store; otherwise 32-bit stores.
+template <int D, int BITS>
+struct RowStage {
+    static constexpr int NW = D * BITS / 32;  // 32-bit words of packed codes per row
+    uint32_t w[NW];
+    float S[8], ov[8];
+    int oc[8];  // channel split off in each piece's group, or -1
+    int id;
+};
+
+template <int D, int BITS, bool OUTL>
+__device__ __forceinline__ void load_row_stage(const CacheView &cv, int l, int h, int slot, int i, int group,
+                                               bool want_id, RowStage<D, BITS> &rs) {
+    constexpr int TPR = D / 32, NB = D * BITS / 8;
+    const int ng = D / group;
+    const size_t srow = (static_cast<size_t>(l) * cv.H + h) * cv.cap + slot;
+    const uint4 *cp = reinterpret_cast<const uint4 *>(cv.codes + srow * NB);
 #pragma unroll
-        for (int k = 0; k < QVG_PSAC_RANK; ++k) pk[k] = pSp * static_cast<float>(cv.psac_p[prow * QVG_PSAC_RANK + k]);
-        U = cv.psac_basis + (static_cast<size_t>(chunk) * H + h) * D * QVG_PSAC_RANK;
+    for (int k = 0; k < NB / 16; ++k) {
+        const uint4 u = cp[k];
+        rs.w[4 * k] = u.x;
+        rs.w[4 * k + 1] = u.y;
+        rs.w[4 * k + 2] = u.z;
+        rs.w[4 * k + 3] = u.w;
     }
-    // the warp's 32 rows x 32 channels pass through shared memory (one row
-    // per lane in, one row per store out), so that each store instruction
-    // writes whole 128-byte lines instead of 16 bytes of 32 lines
-    __shared__ float stage[8][32][33];
-    float (*st)[33] = stage[threadIdx.x >> 5];
-    uint32_t (*st16)[17] = reinterpret_cast<uint32_t (*)[17]>(&stage[threadIdx.x >> 5][0][0]);
-#pragma unroll 1
-    for (int cb = 0; cb < D / 32; ++cb) {
-        float acc[32];
+    const uint16_t *sp = cv.scales + srow * ng;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
-        if (arow_p) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(arow_p + cb * 32 + 8 * i);
-                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    acc[8 * i + 2 * k] = __uint_as_float(w4[k] << 16);
-                    acc[8 * i + 2 * k + 1] = __uint_as_float(w4[k] & 0xffff0000u);
-                }
-            }
-        } else if (valid) {
-            for (int l = 0; l < L; ++l) {
-                const size_t srow = (static_cast<size_t>(l) * H + h) * cv.cap + slot;
-                uint32_t cw[CB / 4];
-                if constexpr (CB == 8) {
-                    const uint2 u = *reinterpret_cast<const uint2 *>(cv.codes + srow * NB + cb * CB);
-                    cw[0] = u.x;
-                    cw[1] = u.y;
-                } else {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(cv.codes + srow * NB + cb * CB);
-                    cw[0] = u.x;
-                    cw[1] = u.y;
-                    cw[2] = u.z;
-                    cw[3] = u.w;
-                }
-                float S[4], ov[4];
-                int oc[4];  // channel split off in each 8-channel block's group, or -1
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    const int gi = (cb * 32 + g8 * 8) / group;
-                    S[g8] = f16_to_f32(cv.scales[srow * ng + gi]);
-                    oc[g8] = -1;
-                    ov[g8] = 0.0f;
-                    if constexpr (OUTL) {
-                        const int oi = cv.outl_idx[srow * ng + gi];
-                        if (oi != 0xFF) {
-                            oc[g8] = gi * group + oi;
-                            ov[g8] = f16_to_f32(cv.outl_val[srow * ng + gi]);
-                        }
-                    }
-                }
-                uint4 cr[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                               make_uint4(0, 0, 0, 0)};
-                if (C > 0) {
-                    const uint16_t *crow = cv.cent + ((static_cast<size_t>(l) * H + h) * cv.max_chunks + chunk) * C * D +
-                                           static_cast<size_t>(cv.ids[srow]) * D + cb * 32;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) cr[i] = *reinterpret_cast<const uint4 *>(crow + 8 * i);
-                }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const uint32_t word = cw[(e * BITS) / 32];
-                    const int q = static_cast<int>((word >> ((e * BITS) % 32)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
-                    float v = __fmul_rn(S[e >> 3], static_cast<float>(q));
-                    if (OUTL && cb * 32 + e == oc[e >> 3]) v = ov[e >> 3];
-                    if (C > 0) {
-                        const uint4 c4 = cr[e >> 3];
-                        const uint32_t cwd = (e & 7) < 2 ? c4.x : (e & 7) < 4 ? c4.y : (e & 7) < 6 ? c4.z : c4.w;
-                        v = __fadd_rn(v, __uint_as_float((e & 1) ? (cwd & 0xffff0000u) : (cwd << 16)));
-                    }
-                    acc[e] = __fadd_rn(acc[e], v);
-                }
-            }
-            if (U) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float *u = U + (cb * 32 + e) * QVG_PSAC_RANK;
-                    float corr = 0.0f;
-#pragma unroll
-                    for (int k = 0; k < QVG_PSAC_RANK; ++k) corr = fmaf(pk[k], u[k], corr);
-                    acc[e] = acc[e] + corr;
-                }
+    for (int m = 0; m < 8; ++m) {
+        const int g = 4 * (i + TPR * m) / group;
+        rs.S[m] = f16_to_f32(sp[g]);
+        rs.oc[m] = -1;
+        rs.ov[m] = 0.0f;
+        if constexpr (OUTL) {
+            const int oi = cv.outl_idx[srow * ng + g];
+            if (oi != 0xFF) {
+                rs.oc[m] = g * group + oi;
+                rs.ov[m] = f16_to_f32(cv.outl_val[srow * ng + g]);
             }
         }
-        if (out32) {
+    }
+    rs.id = want_id ? cv.ids[srow] : 0;
+}
+
+// The 4 codes of piece m of thread i (channels 4 (i + TPR m) .. + 3), as
+// the low 4 BITS bits of the result.
+template <int D, int BITS>
+__device__ __forceinline__ uint32_t piece_codes(const RowStage<D, BITS> &rs, int i, int m) {
+    constexpr int TPR = D / 32;
+    if constexpr (BITS == 2) {
+        // byte i + TPR m of the row: word TPR m / 4, byte i + (TPR m mod 4)
+        return (rs.w[(TPR * m) >> 2] >> (8 * (i + ((TPR * m) & 3)))) & 0xffu;
+    } else {
+        // 16-bit half i + TPR m: word (i + TPR m) / 2, half (i + TPR m) mod 2
+        const int hw = i + TPR * m;
+        const uint32_t word = (TPR == 4) ? ((i >> 1) ? rs.w[2 * m + 1] : rs.w[2 * m]) : rs.w[(TPR * m) >> 1];
+        return (word >> (16 * (hw & 1))) & 0xffffu;
+    }
+}
+
+// Centroid pieces of stage l: 4 bf16 channels each.  The id is clamped so
+// that a padding slot (whose id is not a cluster) still reads inside the
+// chunk's centroids -- its values are then discarded.
+template <int D>
+__device__ __forceinline__ void load_cent_row(const CacheView &cv, int l, int h, int chunk, int C, int id, int i,
+                                              uint2 (&cr)[8]) {
+    constexpr int TPR = D / 32;
+    const int idc = id < C ? id : C - 1;
+    const uint16_t *crow = cv.cent + ((static_cast<size_t>(l) * cv.H + h) * cv.max_chunks + chunk) * C * D +
+                           static_cast<size_t>(idc) * D;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) st[lane][e] = acc[e];
-            __syncwarp();
-            float *o = out32 + (static_cast<size_t>(t0) * H + h) * D + cb * 32 + lane;
-            for (int r = 0; r < nrow; ++r) o[static_cast<size_t>(r) * H * D] = st[r][lane];
+    for (int m = 0; m < 8; ++m) cr[m] = *reinterpret_cast<const uint2 *>(crow + 4 * (i + TPR * m));
+}
+
+// acc += this stage's values of piece m
+template <int D, int BITS, bool OUTL>
+__device__ __forceinline__ void add_piece(const RowStage<D, BITS> &rs, uint2 cr, bool cent, int i, int m,
+                                          float (&acc)[4]) {
+    constexpr int TPR = D / 32;
+    const uint32_t code = piece_codes<D, BITS>(rs, i, m);
+    const uint32_t cw[2] = {cr.x, cr.y};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int q = static_cast<int>((code >> (k * BITS)) & ((1u << BITS) - 1u)) - (1 << (BITS - 1));
+        float v = __fmul_rn(rs.S[m], static_cast<float>(q));
+        if (OUTL && 4 * (i + TPR * m) + k == rs.oc[m]) v = rs.ov[m];
+        if (cent) v = __fadd_rn(v, __uint_as_float((k & 1) ? (cw[k >> 1] & 0xffff0000u) : (cw[k >> 1] << 16)));
+        acc[k] = __fadd_rn(acc[k], v);
+    }
+}
+
+template <int D, int BITS, bool OUTL>
+__device__ __forceinline__ void add_row_stage(const RowStage<D, BITS> &rs, const uint2 (&cr)[8], bool cent, int i,
+                                              float (&acc)[8][4]) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) add_piece<D, BITS, OUTL>(rs, cr[m], cent, i, m, acc[m]);
+}
+
+// The 4 bf16 anchor values of piece m (channels 4 (i + TPR m) .. + 3).
+template <int D>
+__device__ __forceinline__ void anchor_piece(const uint16_t *ap, int i, int m, float (&o)[4]) {
+    constexpr int TPR = D / 32;
+    const uint2 u = *reinterpret_cast<const uint2 *>(ap + 4 * (i + TPR * m));
+    o[0] = __uint_as_float(u.x << 16);
+    o[1] = __uint_as_float(u.x & 0xffff0000u);
+    o[2] = __uint_as_float(u.y << 16);
+    o[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+
+template <int D, bool VEC>
+__device__ __forceinline__ void store_piece(float *out32, uint16_t *out16, size_t orow, int i, int m,
+                                            const float (&o)[4]) {
+    constexpr int TPR = D / 32;
+    const size_t off = orow + 4 * (i + TPR * m);
+    if (out32) {
+        if constexpr (VEC) {
+            *reinterpret_cast<float4 *>(out32 + off) = make_float4(o[0], o[1], o[2], o[3]);
         } else {
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                st16[lane][k] = static_cast<uint32_t>(f32_to_bf16(acc[2 * k])) |
-                                (static_cast<uint32_t>(f32_to_bf16(acc[2 * k + 1])) << 16);
-            __syncwarp();
-            // two rows per store: lanes 0-15 the even row, 16-31 the odd one
-            uint32_t *o = reinterpret_cast<uint32_t *>(out16 + (static_cast<size_t>(t0) * H + h) * D + cb * 32) +
-                          (lane & 15);
-            for (int r = lane >> 4; r < nrow; r += 2) o[static_cast<size_t>(r) * H * D / 2] = st16[r][lane & 15];
+            for (int k = 0; k < 4; ++k) out32[off + k] = o[k];
         }
-        __syncwarp();  // the stage is read before the next block overwrites it
+    } else {
+        const uint32_t w0 = static_cast<uint32_t>(f32_to_bf16(o[0])) | (static_cast<uint32_t>(f32_to_bf16(o[1])) << 16);
+        const uint32_t w1 = static_cast<uint32_t>(f32_to_bf16(o[2])) | (static_cast<uint32_t>(f32_to_bf16(o[3])) << 16);
+        if constexpr (VEC) {
+            *reinterpret_cast<uint2 *>(out16 + off) = make_uint2(w0, w1);
+        } else {
+            uint32_t *o32 = reinterpret_cast<uint32_t *>(out16 + off);
+            o32[0] = w0;
+            o32[1] = w1;
+        }
+    }
+}
+
+// MULTI: more than one stage, or the PSAC term; otherwise each piece is
+// rebuilt and stored at once, so that few values are live and three blocks
+// fit on an SM (two for MULTI, one with the PSAC term, without spills).
+template <int D, int BITS, bool PSAC, bool OUTL, bool VEC, bool MULTI>
+__global__ void __launch_bounds__(256, PSAC ? 1 : MULTI ? 2 : 3) k_decompress(CacheView cv, int L, int C, int group, int tok0, int ntok,
+                                                    float *out32, uint16_t *out16) {
+    constexpr int TPR = D / 32, RPB = 256 / TPR;  // threads per row, rows per block
+    const int i = threadIdx.x % TPR, h = blockIdx.y, H = cv.H;
+    const int t = blockIdx.x * RPB + threadIdx.x / TPR;
+    if (t >= ntok) return;
+    const int slot = tok0 + t;
+    // slot-only loads: tile table entry and stage 0
+    const int chunk = cv.tile_chunk[slot / QVG_TILE];
+    RowStage<D, BITS> rs;
+    load_row_stage<D, BITS, OUTL>(cv, 0, h, slot, i, group, C > 0, rs);
+    // chunk-dependent loads: the chunk's extent and anchor row, the centroid
+    // pieces of stage 0
+    const int cs = cv.chunk_start[chunk], cl = cv.chunk_len[chunk];
+    const bool valid = slot >= cs && slot < cs + cl;
+    int arow = cv.chunk_anchor ? cv.chunk_anchor[chunk] : -1;  // the slot's anchor row, or -1
+    if (arow >= 0) arow += slot - cs;
+    uint2 cr[8];
+    if (C > 0) load_cent_row<D>(cv, 0, h, chunk, C, rs.id, i, cr);
+    const size_t orow = (static_cast<size_t>(t) * H + h) * D;
+    if constexpr (!MULTI) {
+        const uint16_t *ap = valid && arow >= 0 ? cv.anchor + (static_cast<size_t>(arow) * H + h) * D : nullptr;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            float o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (ap)
+                anchor_piece<D>(ap, i, m, o);
+            else if (valid)
+                add_piece<D, BITS, OUTL>(rs, cr[m], C > 0, i, m, o);
+            store_piece<D, VEC>(out32, out16, orow, i, m, o);
+        }
+    } else {
+        float acc[8][4];
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[m][k] = 0.0f;
+        add_row_stage<D, BITS, OUTL>(rs, cr, C > 0, i, acc);
+#pragma unroll 1
+        for (int l = 1; l < L; ++l) {
+            load_row_stage<D, BITS, OUTL>(cv, l, h, slot, i, group, C > 0, rs);
+            if (C > 0) load_cent_row<D>(cv, l, h, chunk, C, rs.id, i, cr);
+            add_row_stage<D, BITS, OUTL>(rs, cr, C > 0, i, acc);
+        }
+        if (!valid) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[m][k] = 0.0f;
+        } else if (arow >= 0) {
+            // an anchor chunk's row is its stored bf16 K/V
+            const uint16_t *ap = cv.anchor + (static_cast<size_t>(arow) * H + h) * D;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) anchor_piece<D>(ap, i, m, acc[m]);
+        } else if constexpr (PSAC) {
+            const size_t prow = static_cast<size_t>(h) * cv.cap + slot;
+            const float pSp = f16_to_f32(cv.psac_s[prow]);
+            const uint2 pu = *reinterpret_cast<const uint2 *>(cv.psac_p + prow * QVG_PSAC_RANK);
+            float pk[QVG_PSAC_RANK];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                pk[k] = pSp * static_cast<float>(static_cast<int8_t>(pu.x >> (8 * k)));
+                pk[4 + k] = pSp * static_cast<float>(static_cast<int8_t>(pu.y >> (8 * k)));
+            }
+            const float *U = cv.psac_basis + (static_cast<size_t>(chunk) * H + h) * D * QVG_PSAC_RANK;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float *u = U + (4 * (i + TPR * m) + k) * QVG_PSAC_RANK;
+                    const float4 u0 = *reinterpret_cast<const float4 *>(u);
+                    const float4 u1 = *reinterpret_cast<const float4 *>(u + 4);
+                    const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                    float corr = 0.0f;
+#pragma unroll
+                    for (int r = 0; r < QVG_PSAC_RANK; ++r) corr = fmaf(pk[r], uu[r], corr);
+                    acc[m][k] = acc[m][k] + corr;
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) store_piece<D, VEC>(out32, out16, orow, i, m, acc[m]);
+    }
+}
+
+template <int D, int BITS, bool PSAC, bool OUTL>
+void launch_dq(const CacheView &cv, const qvg_params *p, int tok0, int ntok, float *o32, uint16_t *o16, bool vec,
+               cudaStream_t st) {
+    constexpr int RPB = 256 / (D / 32);
+    const dim3 grid(static_cast<unsigned>((ntok + RPB - 1) / RPB), cv.H);
+    const int L = p->L, C = p->C, G = p->group;
+    if (PSAC || L > 1) {
+        if (vec) k_decompress<D, BITS, PSAC, OUTL, true, true><<<grid, 256, 0, st>>>(cv, L, C, G, tok0, ntok, o32, o16);
+        else k_decompress<D, BITS, PSAC, OUTL, false, true><<<grid, 256, 0, st>>>(cv, L, C, G, tok0, ntok, o32, o16);
+    } else if constexpr (!PSAC) {
+        if (vec) k_decompress<D, BITS, false, OUTL, true, false><<<grid, 256, 0, st>>>(cv, L, C, G, tok0, ntok, o32, o16);
+        else k_decompress<D, BITS, false, OUTL, false, false><<<grid, 256, 0, st>>>(cv, L, C, G, tok0, ntok, o32, o16);
+    }
+}
+
+template <int D, int BITS>
+void launch_dq_flags(const CacheView &cv, const qvg_params *p, int tok0, int ntok, float *o32, uint16_t *o16, bool vec,
+                     cudaStream_t st) {
+    if (cv.psac_p) {
+        if (cv.outl_idx) launch_dq<D, BITS, true, true>(cv, p, tok0, ntok, o32, o16, vec, st);
+        else launch_dq<D, BITS, true, false>(cv, p, tok0, ntok, o32, o16, vec, st);
+    } else {
+        if (cv.outl_idx) launch_dq<D, BITS, false, true>(cv, p, tok0, ntok, o32, o16, vec, st);
+        else launch_dq<D, BITS, false, false>(cv, p, tok0, ntok, o32, o16, vec, st);
     }
 }
 
@@ -184,19 +304,15 @@ qvg_status launch_decompress(const qvg_params *p, const qvg_cache *c, int tok0, 
     if (!(p->flags & QVG_OUTLIER)) cv.outl_idx = nullptr;
     float *o32 = out_dtype == QVG_OUT_F32 ? static_cast<float *>(out) : nullptr;
     uint16_t *o16 = out_dtype == QVG_OUT_BF16 ? static_cast<uint16_t *>(out) : nullptr;
-    const long long warps = static_cast<long long>(c->H) * ceil_div(std::max(ntok, 1), 32);
-    const int blocks = static_cast<int>(std::max(1LL, (warps + 7) / 8));
-#define QVG_DQ2(D_, B_, O_)                                                                                        \
-    (cv.psac_p ? k_decompress<D_, B_, true, O_><<<blocks, 256, 0, st>>>(cv, p->L, p->C, p->group, tok0, ntok, o32, o16) \
-               : k_decompress<D_, B_, false, O_><<<blocks, 256, 0, st>>>(cv, p->L, p->C, p->group, tok0, ntok, o32, o16))
-#define QVG_DQ(D_, B_) (cv.outl_idx ? QVG_DQ2(D_, B_, true) : QVG_DQ2(D_, B_, false))
+    // vector stores need each thread's 4-channel piece aligned to its size
+    const bool vec = reinterpret_cast<uintptr_t>(out) % (o32 ? 16 : 8) == 0;
     if (c->d == 64) {
-        if (p->bits == 2) QVG_DQ(64, 2); else QVG_DQ(64, 4);
+        if (p->bits == 2) launch_dq_flags<64, 2>(cv, p, tok0, ntok, o32, o16, vec, st);
+        else launch_dq_flags<64, 4>(cv, p, tok0, ntok, o32, o16, vec, st);
     } else {
-        if (p->bits == 2) QVG_DQ(128, 2); else QVG_DQ(128, 4);
+        if (p->bits == 2) launch_dq_flags<128, 2>(cv, p, tok0, ntok, o32, o16, vec, st);
+        else launch_dq_flags<128, 4>(cv, p, tok0, ntok, o32, o16, vec, st);
     }
-#undef QVG_DQ
-#undef QVG_DQ2
     QVG_LAUNCH_CHECK();
     return QVG_OK;
 }
