@@ -304,8 +304,7 @@ qvg_status qvg_compress_chunk_noalloc(const qvg_params *p, const void *x_bf16,
  *            for fp32 and 8-byte for bf16 take vector stores); the caller's
  *            device buffer.  Padding slots give 0.
  * Errors: QVG_ERR_INVALID_ARG for tok0 < 0, ntok < 0, tok0 + ntok past
- * n_tokens or a misaligned out; QVG_ERR_UNSUPPORTED for H > 65535;
- * ntok = 0 does nothing.
+ * n_tokens or a misaligned out; ntok = 0 does nothing.
  */
 qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache,
                           int32_t tok0, int32_t ntok, void *out,

@@ -350,7 +350,6 @@ qvg_status qvg_decompress(const qvg_params *p, const qvg_cache *cache, int32_t t
     if (out_dtype != QVG_OUT_F32 && out_dtype != QVG_OUT_BF16) return QVG_ERR_INVALID_ARG;
     if (tok0 < 0 || ntok < 0 || static_cast<int64_t>(tok0) + ntok > cache->n_tokens) return QVG_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(out) % 4 != 0) return QVG_ERR_INVALID_ARG;  // stored in 32-bit words
-    if (cache->H > 65535) return QVG_ERR_UNSUPPORTED;  // one grid row per head
     if (ntok == 0) return QVG_OK;
     return launch_decompress(p, cache, tok0, ntok, out, out_dtype, static_cast<cudaStream_t>(stream));
 }

@@ -795,15 +795,24 @@ __global__ void __launch_bounds__(kUpdThreads) k_kmeans_update(const TIn *__rest
 }
 
 // ---------------------------------------------------------------------------
-// Residual quantisation of one stage, thread = (token, head) row: a warp
-// takes 32 consecutive tokens of one head (their ids, codes and scales are
-// contiguous), each thread its own row in blocks of 32 channels.  Pass 1
-// takes each group's amax of r = x - c; pass 2 recomputes r, quantises,
-// packs and writes.  Writes codes, fp16 scales and the cluster id;
-// optionally the next stage's input X_{l+1} = X_l - deq (fp32 and its bf16
-// rounding, the next clustering operand); optionally (last stage of a key
-// chunk with PSAC) the INT8 projection of X_{L+1} on the basis U, an fp32
-// FMA chain in ascending channel order.
+// Residual quantisation of one stage, thread = (token, head) row x 32-channel
+// block: D / 32 adjacent lanes (TPR) share a row, so each load or store
+// instruction of a warp covers 8 (d = 128) or 16 (d = 64) whole rows, and a
+// block of 256 threads takes consecutive tokens of one head; the grid runs
+// over the heads first, so the blocks in flight cover every head of a token
+// range and read the token-major input in whole DRAM pages.  Pass 1 forms
+// r = x - c (kept in registers) and each 8-channel block's amax; a group's
+// amax is combined over its blocks in channel order and, for a group wider
+// than 32 channels, over the row's lanes by xor shuffles (every lane of the
+// group gets the same result), and its scale is computed once.  Pass 2
+// quantises and packs; only when the next stage or PSAC needs the
+// reconstruction error does a third pass re-read the block (from L1).
+// Writes codes, fp16 scales and the cluster id; optionally the
+// next stage's input X_{l+1} = X_l - deq (fp32 and its bf16 rounding, the
+// next clustering operand); optionally (last stage of a key chunk with
+// PSAC) the INT8 projection of X_{L+1} on the basis U, an fp32 FMA chain in
+// ascending channel order -- run block after block by the row's lanes in
+// turn, each continuing the chain of the one before (handed on by shuffle).
 // OUTL (outlier split): pass 1 also keeps, per group, the second-largest
 // |r| and the signed value and channel of the largest.  The largest is an
 // outlier exactly when it is strictly above the second: for G <= 100 the
@@ -838,8 +847,23 @@ __device__ __forceinline__ void load32<float>(const float *p, float (&v)[32]) {
     }
 }
 
-template <int D, int BITS, typename TIn, bool OUTL>
-__global__ void __launch_bounds__(256) k_residual_quant(
+// Group statistics of a run of channels: amax m, second-largest m2, and the
+// signed value rv and row channel ix of the first largest.
+struct GStat {
+    float m, m2, rv;
+    int ix;
+};
+// a's channels come before b's: the combined statistics are those of a
+// sequential pass over a then b
+__device__ __forceinline__ GStat gmerge(const GStat &a, const GStat &b) {
+    if (b.m > a.m) return GStat{b.m, fmaxf(a.m, b.m2), b.rv, b.ix};
+    return GStat{a.m, fmaxf(a.m2, b.m), a.rv, a.ix};
+}
+
+// DELTA: the call writes the next stage's input or the PSAC projection
+// (delta_out or psacU set); without it the kernel ends after the codes.
+template <int D, int BITS, typename TIn, bool OUTL, bool DELTA>
+__global__ void __launch_bounds__(256, DELTA ? 2 : 3) k_residual_quant(
     const TIn *__restrict__ xin, int N, int H, const uint16_t *__restrict__ cent, size_t hs, int C,
     const int32_t *__restrict__ ids, int group, int mode, uint8_t *__restrict__ codes,
     uint16_t *__restrict__ scales, uint8_t *__restrict__ ids_out, size_t shs,
@@ -847,221 +871,262 @@ __global__ void __launch_bounds__(256) k_residual_quant(
     int8_t *__restrict__ psac_p, uint16_t *__restrict__ psac_s, size_t phs, uint16_t *__restrict__ outl_val,
     uint8_t *__restrict__ outl_idx) {
     constexpr int NB = D * BITS / 8, CB = 32 * BITS / 8;  // code bytes per row / per 32-channel block
-    constexpr int NG8 = D / 8;                             // 8-channel blocks
+    constexpr int TPR = D / 32, RPB = 256 / TPR;           // lanes per row, rows per block
     pdl_wait();  // the final assignment (which reads this stage's operand) has finished
     pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const int nblk = ceil_div(N, 32);
-    const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (wid >= static_cast<long long>(H) * nblk) return;
-    const int h = static_cast<int>(wid / nblk), n = static_cast<int>(wid % nblk) * 32 + lane;
-    if (n >= N) return;
-    const int ng = D / group, g8 = group / 8;  // groups per row, 8-channel blocks per group
+    const int lane = threadIdx.x & 31, cb = lane % TPR, h = blockIdx.x;
+    const int n_row = blockIdx.y * RPB + threadIdx.x / TPR;
+    // every lane takes part in the shuffles below; a row past N repeats row
+    // N - 1 and stores nothing
+    const bool live = n_row < N;
+    const int n = live ? n_row : N - 1;
+    const int ng = D / group;
     // (an id outside [0, C) never comes from the assignment; clamped so that
     // no access leaves the centroid table)
     const unsigned uid = C > 0 ? static_cast<unsigned>(ids[static_cast<size_t>(h) * N + n]) : 0u;
     const int id = uid < static_cast<unsigned>(C) ? static_cast<int>(uid) : max(C - 1, 0);
     const size_t trow = static_cast<size_t>(n) * H + h;  // token-major row of the stage buffers
-    const TIn *xr = xin + trow * D;
-    const uint16_t *cr = C > 0 ? cent + static_cast<size_t>(h) * hs + static_cast<size_t>(id) * D : nullptr;
-    // pass 1: amax of each 8-channel block, then of each group (with the
-    // outlier split: also the second-largest |r| and the largest's signed
-    // value and channel, the first one on ties)
-    float am8[NG8], sm8[NG8], rv8[NG8];
-    int ix8[NG8];
-#pragma unroll 1
-    for (int cb = 0; cb < D / 32; ++cb) {
+    const TIn *xr = xin + trow * D + cb * 32;
+    const uint16_t *cr = C > 0 ? cent + static_cast<size_t>(h) * hs + static_cast<size_t>(id) * D + cb * 32 : nullptr;
+    // pass 1: r = x - c for the lane's 32 channels (kept for pass 2) and the
+    // statistics of each 8-channel block
+    float r[32];
+    {
         float x[32], c[32];
-        load32<TIn>(xr + cb * 32, x);
-        if (C > 0) load32<uint16_t>(cr + cb * 32, c);
+        load32<TIn>(xr, x);
+        if (C > 0) load32<uint16_t>(cr, c);
 #pragma unroll
-        for (int b8 = 0; b8 < 4; ++b8) {
-            float m = 0.0f, m2 = 0.0f, rv = 0.0f;
-            int ix = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float r = C > 0 ? __fsub_rn(x[8 * b8 + e], c[8 * b8 + e]) : x[8 * b8 + e];
-                const float a = fabsf(r);
-                if constexpr (OUTL) {
-                    if (a > m) {
-                        m2 = m;
-                        m = a;
-                        rv = r;
-                        ix = e;
-                    } else {
-                        m2 = fmaxf(m2, a);
-                    }
-                } else {
-                    m = fmaxf(m, a);
-                }
-            }
-            // cb is a loop variable: keep the block values in registers through a static index
-#pragma unroll
-            for (int q = 0; q < NG8 / 4; ++q)
-                if (q == cb) {
-                    am8[4 * q + b8] = m;
-                    if constexpr (OUTL) {
-                        sm8[4 * q + b8] = m2;
-                        rv8[4 * q + b8] = rv;
-                        ix8[4 * q + b8] = (4 * q + b8) * 8 + ix;
-                    }
-                }
-        }
+        for (int e = 0; e < 32; ++e) r[e] = C > 0 ? __fsub_rn(x[e], c[e]) : x[e];
     }
-    float Sp8[NG8];  // the scale each 8-channel block uses
-    int oc8[NG8];    // (outlier split) the channel split off in the block's group, or -1
-    float ov8[NG8];  // and its fp16 value
-    const size_t srow = static_cast<size_t>(h) * shs + n;
+    GStat st8[4];
 #pragma unroll
-    for (int g = 0; g < NG8; ++g) {
-        Sp8[g] = 0.0f;
-        oc8[g] = -1;
-        ov8[g] = 0.0f;
-    }
-    for (int gi = 0; gi < ng; ++gi) {
+    for (int b8 = 0; b8 < 4; ++b8) {
         float m = 0.0f, m2 = 0.0f, rv = 0.0f;
         int ix = 0;
 #pragma unroll
-        for (int g = 0; g < NG8; ++g)
-            if (g / g8 == gi) {
-                if constexpr (OUTL) {
-                    if (am8[g] > m) {
-                        m2 = fmaxf(m, sm8[g]);
-                        m = am8[g];
-                        rv = rv8[g];
-                        ix = ix8[g];
-                    } else {
-                        m2 = fmaxf(m2, am8[g]);
-                    }
+        for (int e = 0; e < 8; ++e) {
+            const float a = fabsf(r[8 * b8 + e]);
+            if constexpr (OUTL) {
+                if (a > m) {
+                    m2 = m;
+                    m = a;
+                    rv = r[8 * b8 + e];
+                    ix = e;
                 } else {
-                    m = fmaxf(m, am8[g]);
+                    m2 = fmaxf(m2, a);
                 }
+            } else {
+                m = fmaxf(m, a);
             }
-        const uint16_t sb = group_scale_f16(OUTL ? m2 : m, BITS, mode);
-        scales[srow * ng + gi] = sb;
-        const float Sp = f16_to_f32(sb);
-        int oc = -1;
-        float ov = 0.0f;
-        if constexpr (OUTL) {
-            uint16_t ob = 0;
-            if (m > m2) {
-                oc = ix;
-                ob = f32_to_f16(fminf(fmaxf(rv, -65504.0f), 65504.0f));
-                ov = f16_to_f32(ob);
-            }
-            outl_val[srow * ng + gi] = ob;
-            outl_idx[srow * ng + gi] = static_cast<uint8_t>(oc < 0 ? 0xFF : oc - gi * group);
         }
-#pragma unroll
-        for (int g = 0; g < NG8; ++g)
-            if (g / g8 == gi) {
-                Sp8[g] = Sp;
-                oc8[g] = oc;
-                ov8[g] = ov;
-            }
+        st8[b8] = GStat{m, m2, rv, cb * 32 + 8 * b8 + ix};
     }
-    if (ids_out) ids_out[srow] = static_cast<uint8_t>(id);  // no ids without centroids (C = 0)
-    float P[QVG_PSAC_RANK];
-#pragma unroll
-    for (int k = 0; k < QVG_PSAC_RANK; ++k) P[k] = 0.0f;
-    const float *Uh = psacU ? psacU + static_cast<size_t>(h) * D * QVG_PSAC_RANK : nullptr;
-    // pass 2: quantise, pack, residual for the next stage, PSAC projection
-#pragma unroll 1
-    for (int cb = 0; cb < D / 32; ++cb) {
-        float x[32], c[32];
-        load32<TIn>(xr + cb * 32, x);
-        if (C > 0) load32<uint16_t>(cr + cb * 32, c);
-        float Sb[4], ib[4], ob[4];
-        int ocb[4];
+    // each 8-channel block's group statistics: groups of 8, 16 or 32
+    // channels lie inside the lane's block; wider ones span 2 or 4 lanes
+    GStat gs8[4];
+    const GStat zero{0.0f, 0.0f, 0.0f, 0};
+    if (group <= 32) {
+        const int g8 = group / 8;  // 1, 2 or 4 blocks per group
 #pragma unroll
         for (int b8 = 0; b8 < 4; ++b8) {
-            Sb[b8] = 0.0f;
-            ob[b8] = 0.0f;
-            ocb[b8] = -1;
+            GStat acc = zero;
 #pragma unroll
-            for (int q = 0; q < NG8 / 4; ++q)
-                if (q == cb) {
-                    Sb[b8] = Sp8[4 * q + b8];
-                    if constexpr (OUTL) {
-                        ob[b8] = ov8[4 * q + b8];
-                        ocb[b8] = oc8[4 * q + b8];
-                    }
-                }
-            ib[b8] = Sb[b8] > 0.0f ? __fdiv_rn(1.0f, Sb[b8]) : 0.0f;
+            for (int k = 0; k < 4; ++k)
+                if (k / g8 == b8 / g8) acc = OUTL ? gmerge(acc, st8[k]) : GStat{fmaxf(acc.m, st8[k].m), 0.0f, 0.0f, 0};
+            gs8[b8] = acc;
         }
-        uint32_t pw[CB / 4];
+    } else {
+        GStat acc = zero;
 #pragma unroll
-        for (int k = 0; k < CB / 4; ++k) pw[k] = 0u;
-        float dl[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const float Sp = Sb[e >> 3];
-            const float r = C > 0 ? __fsub_rn(x[e], c[e]) : x[e];
-            const bool is_out = OUTL && cb * 32 + e == ocb[e >> 3];
-            const int q = is_out ? 0 : quant_code_rcp(r, Sp, ib[e >> 3], BITS);
-            pw[(e * BITS) / 32] |= static_cast<uint32_t>(q + (1 << (BITS - 1))) << ((e * BITS) % 32);
-            const float rh = is_out ? ob[e >> 3] : __fmul_rn(Sp, static_cast<float>(q));
-            const float deq = C > 0 ? __fadd_rn(rh, c[e]) : rh;
-            dl[e] = __fsub_rn(x[e], deq);
+        for (int k = 0; k < 4; ++k) acc = OUTL ? gmerge(acc, st8[k]) : GStat{fmaxf(acc.m, st8[k].m), 0.0f, 0.0f, 0};
+        // lanes cb ^ o (o < group / 32) of the row hold the group's other blocks
+        for (int o = 1; o < group / 32; o <<= 1) {
+            GStat pt;
+            pt.m = __shfl_xor_sync(0xffffffffu, acc.m, o);
+            if constexpr (OUTL) {
+                pt.m2 = __shfl_xor_sync(0xffffffffu, acc.m2, o);
+                pt.rv = __shfl_xor_sync(0xffffffffu, acc.rv, o);
+                pt.ix = __shfl_xor_sync(0xffffffffu, acc.ix, o);
+                acc = (cb & o) ? gmerge(pt, acc) : gmerge(acc, pt);  // the lower channels first
+            } else {
+                acc.m = fmaxf(acc.m, pt.m);
+            }
         }
+#pragma unroll
+        for (int b8 = 0; b8 < 4; ++b8) gs8[b8] = acc;
+    }
+    // scales (and the outlier entries) of each block's group, computed once
+    // per group; the lane with the group's first block writes them
+    const size_t srow = static_cast<size_t>(h) * shs + n;
+    float Sb[4], ib[4], ob[4];
+    int ocb[4];
+    uint16_t sbits[4], obits[4];
+    auto group_scale = [&](int b8) {
+        const GStat &g = gs8[b8];
+        sbits[b8] = group_scale_f16(OUTL ? g.m2 : g.m, BITS, mode);
+        Sb[b8] = f16_to_f32(sbits[b8]);
+        ib[b8] = Sb[b8] > 0.0f ? __fdiv_rn(1.0f, Sb[b8]) : 0.0f;
+        ocb[b8] = -1;
+        ob[b8] = 0.0f;
+        obits[b8] = 0;
+        if constexpr (OUTL) {
+            if (g.m > g.m2) {
+                ocb[b8] = g.ix;
+                obits[b8] = f32_to_f16(fminf(fmaxf(g.rv, -65504.0f), 65504.0f));
+                ob[b8] = f16_to_f32(obits[b8]);
+            }
+        }
+    };
+    if (group >= 32) {
+        group_scale(0);
+#pragma unroll
+        for (int b8 = 1; b8 < 4; ++b8) {
+            Sb[b8] = Sb[0];
+            ib[b8] = ib[0];
+            ob[b8] = ob[0];
+            ocb[b8] = ocb[0];
+            sbits[b8] = sbits[0];
+            obits[b8] = obits[0];
+        }
+    } else {
+#pragma unroll
+        for (int b8 = 0; b8 < 4; ++b8) group_scale(b8);
+    }
+#pragma unroll
+    for (int b8 = 0; b8 < 4; ++b8) {
+        const int ch = cb * 32 + 8 * b8, gi = ch / group;
+        if (live && ch % group == 0) {
+            scales[srow * ng + gi] = sbits[b8];
+            if constexpr (OUTL) {
+                outl_val[srow * ng + gi] = obits[b8];
+                outl_idx[srow * ng + gi] = static_cast<uint8_t>(ocb[b8] < 0 ? 0xFF : ocb[b8] - gi * group);
+            }
+        }
+    }
+    if (ids_out && live && cb == 0) ids_out[srow] = static_cast<uint8_t>(id);  // no ids without centroids (C = 0)
+    // pass 2: the codes, clamp(rint(r / S)) as quant_code_rcp (common.cuh)
+    // gives them -- rint(r fl(1 / S)), with the division redone, after the
+    // loop, for the rare element whose product lies within |y| 2^-21 of a
+    // half-integer; an outlier's code is 0
+    constexpr float kQmax = static_cast<float>((1 << (BITS - 1)) - 1);
+    uint32_t pw[CB / 4];
+#pragma unroll
+    for (int k = 0; k < CB / 4; ++k) pw[k] = 0u;
+    uint32_t near = 0u;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        const int b8 = e >> 3;
+        int q = 0;
+        if (!(OUTL && cb * 32 + e == ocb[b8]) && Sb[b8] > 0.0f) {
+            const float y = __fmul_rn(r[e], ib[b8]);
+            const float t = rintf(y);
+            if (0.5f - fabsf(y - t) <= fabsf(y) * 0x1p-21f) near |= 1u << e;
+            q = static_cast<int>(fminf(fmaxf(t, -kQmax - 1.0f), kQmax));
+        }
+        pw[(e * BITS) / 32] |= static_cast<uint32_t>(q + (1 << (BITS - 1))) << ((e * BITS) % 32);
+    }
+    if (near) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            if ((near >> e) & 1u) {
+                const float t = rintf(__fdiv_rn(r[e], Sb[e >> 3]));
+                const int q = static_cast<int>(fminf(fmaxf(t, -kQmax - 1.0f), kQmax));
+                const int wi = (e * BITS) / 32, sh = (e * BITS) % 32;
+                pw[wi] = (pw[wi] & ~(((1u << BITS) - 1u) << sh)) | (static_cast<uint32_t>(q + (1 << (BITS - 1))) << sh);
+            }
+    }
+    if (live) {
         uint8_t *cdst = codes + srow * NB + cb * CB;
         if constexpr (CB == 8)
             *reinterpret_cast<uint2 *>(cdst) = make_uint2(pw[0], pw[1]);
         else
             *reinterpret_cast<uint4 *>(cdst) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-        if (delta_out) {
-            float4 *dp = reinterpret_cast<float4 *>(delta_out + trow * D + cb * 32);
+    }
+    // the stage's reconstruction error X - (S q + c) (or the outlier's fp16
+    // value + c): the next stage's input and the PSAC operand
+    if constexpr (!DELTA) return;
+    float dl[32];
+    {
+        float x[32], c[32];
+        load32<TIn>(xr, x);
+        if (C > 0) load32<uint16_t>(cr, c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dp[i] = make_float4(dl[4 * i], dl[4 * i + 1], dl[4 * i + 2], dl[4 * i + 3]);
-            if (gbf_out) {
-                uint4 *gp = reinterpret_cast<uint4 *>(gbf_out + trow * D + cb * 32);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        w4[k] = static_cast<uint32_t>(f32_to_bf16(dl[8 * i + 2 * k])) |
-                                (static_cast<uint32_t>(f32_to_bf16(dl[8 * i + 2 * k + 1])) << 16);
-                    gp[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                }
-            }
+        for (int e = 0; e < 32; ++e) {
+            const int q = static_cast<int>((pw[(e * BITS) / 32] >> ((e * BITS) % 32)) & ((1u << BITS) - 1u)) -
+                          (1 << (BITS - 1));
+            const bool is_out = OUTL && cb * 32 + e == ocb[e >> 3];
+            const float rh = is_out ? ob[e >> 3] : __fmul_rn(Sb[e >> 3], static_cast<float>(q));
+            const float deq = C > 0 ? __fadd_rn(rh, c[e]) : rh;
+            dl[e] = __fsub_rn(x[e], deq);
         }
-        if (Uh) {
+    }
+    if (live && delta_out) {
+        float4 *dp = reinterpret_cast<float4 *>(delta_out + trow * D + cb * 32);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float4 u0 = *reinterpret_cast<const float4 *>(Uh + (cb * 32 + e) * QVG_PSAC_RANK);
-                const float4 u1 = *reinterpret_cast<const float4 *>(Uh + (cb * 32 + e) * QVG_PSAC_RANK + 4);
-                const float de = dl[e];
-                P[0] = fmaf(de, u0.x, P[0]);
-                P[1] = fmaf(de, u0.y, P[1]);
-                P[2] = fmaf(de, u0.z, P[2]);
-                P[3] = fmaf(de, u0.w, P[3]);
-                P[4] = fmaf(de, u1.x, P[4]);
-                P[5] = fmaf(de, u1.y, P[5]);
-                P[6] = fmaf(de, u1.z, P[6]);
-                P[7] = fmaf(de, u1.w, P[7]);
+        for (int i = 0; i < 8; ++i) dp[i] = make_float4(dl[4 * i], dl[4 * i + 1], dl[4 * i + 2], dl[4 * i + 3]);
+        if (gbf_out) {
+            uint4 *gp = reinterpret_cast<uint4 *>(gbf_out + trow * D + cb * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    w4[k] = static_cast<uint32_t>(f32_to_bf16(dl[8 * i + 2 * k])) |
+                            (static_cast<uint32_t>(f32_to_bf16(dl[8 * i + 2 * k + 1])) << 16);
+                gp[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
         }
     }
-    if (Uh) {
-        float pa = 0.0f;
+    if (psacU) {
+        // the projection chain over the row's channels in ascending order:
+        // lane block j continues the chain of blocks 0 .. j - 1
+        const float *Uh = psacU + static_cast<size_t>(h) * D * QVG_PSAC_RANK;
+        const int row_lane0 = lane - cb;
+        float P[QVG_PSAC_RANK];
 #pragma unroll
-        for (int k = 0; k < QVG_PSAC_RANK; ++k) pa = fmaxf(pa, fabsf(P[k]));
-        const uint16_t psb = f32_to_f16(fminf(__fdiv_rn(pa, 127.0f), 65504.0f));
-        const float pSp = f16_to_f32(psb);
-        uint32_t pq[2] = {0u, 0u};
+        for (int k = 0; k < QVG_PSAC_RANK; ++k) P[k] = 0.0f;
+#pragma unroll 1
+        for (int j = 0; j < TPR; ++j) {
+            if (cb == j) {
 #pragma unroll
-        for (int k = 0; k < QVG_PSAC_RANK; ++k) {
-            int qp = 0;
-            if (pSp > 0.0f) {
-                float t = rintf(__fdiv_rn(P[k], pSp));
-                t = fminf(fmaxf(t, -127.0f), 127.0f);
-                qp = static_cast<int>(t);
+                for (int e = 0; e < 32; ++e) {
+                    const float4 u0 = *reinterpret_cast<const float4 *>(Uh + (cb * 32 + e) * QVG_PSAC_RANK);
+                    const float4 u1 = *reinterpret_cast<const float4 *>(Uh + (cb * 32 + e) * QVG_PSAC_RANK + 4);
+                    const float de = dl[e];
+                    P[0] = fmaf(de, u0.x, P[0]);
+                    P[1] = fmaf(de, u0.y, P[1]);
+                    P[2] = fmaf(de, u0.z, P[2]);
+                    P[3] = fmaf(de, u0.w, P[3]);
+                    P[4] = fmaf(de, u1.x, P[4]);
+                    P[5] = fmaf(de, u1.y, P[5]);
+                    P[6] = fmaf(de, u1.z, P[6]);
+                    P[7] = fmaf(de, u1.w, P[7]);
+                }
             }
-            pq[k >> 2] |= (static_cast<uint32_t>(qp) & 0xffu) << (8 * (k & 3));
+#pragma unroll
+            for (int k = 0; k < QVG_PSAC_RANK; ++k) P[k] = __shfl_sync(0xffffffffu, P[k], row_lane0 + j);
         }
-        *reinterpret_cast<uint2 *>(psac_p + (static_cast<size_t>(h) * phs + n) * QVG_PSAC_RANK) = make_uint2(pq[0], pq[1]);
-        psac_s[static_cast<size_t>(h) * phs + n] = psb;
+        if (live && cb == 0) {
+            float pa = 0.0f;
+#pragma unroll
+            for (int k = 0; k < QVG_PSAC_RANK; ++k) pa = fmaxf(pa, fabsf(P[k]));
+            const uint16_t psb = f32_to_f16(fminf(__fdiv_rn(pa, 127.0f), 65504.0f));
+            const float pSp = f16_to_f32(psb);
+            uint32_t pq[2] = {0u, 0u};
+#pragma unroll
+            for (int k = 0; k < QVG_PSAC_RANK; ++k) {
+                int qp = 0;
+                if (pSp > 0.0f) {
+                    float t = rintf(__fdiv_rn(P[k], pSp));
+                    t = fminf(fmaxf(t, -127.0f), 127.0f);
+                    qp = static_cast<int>(t);
+                }
+                pq[k >> 2] |= (static_cast<uint32_t>(qp) & 0xffu) << (8 * (k & 3));
+            }
+            *reinterpret_cast<uint2 *>(psac_p + (static_cast<size_t>(h) * phs + n) * QVG_PSAC_RANK) =
+                make_uint2(pq[0], pq[1]);
+            psac_s[static_cast<size_t>(h) * phs + n] = psb;
+        }
     }
 }
 
@@ -1278,15 +1343,22 @@ static cudaError_t rq_launch(const void *xin, bool f32, int N, int H, const uint
                              uint16_t *scales, uint8_t *ids_out, size_t shs, float *delta_out,
                              uint16_t *gbf_out, const float *U, int8_t *pp, uint16_t *ps, size_t phs,
                              uint16_t *ov, uint8_t *oi, cudaStream_t st) {
-    const long long warps = static_cast<long long>(H) * ceil_div(std::max(N, 1), 32);
-    const int blocks = static_cast<int>((warps + 7) / 8);
+    // block (x, y): head x, tokens [y RPB, (y + 1) RPB), RPB = 256 / (D / 32)
+    // -- the heads vary fastest, so the blocks in flight read whole token rows
+    // [h = 0 .. H) of the token-major input (N <= 65535: y fits the grid)
+    const dim3 grid(H, static_cast<unsigned>(ceil_div(std::max(N, 1), 256 / (D / 32))));
+#define QVG_RQ(T_, DL_)                                                                                   \
+    launch_pdl(k_residual_quant<D, BITS, T_, OUTL, DL_>, grid, dim3(256), 0, st, static_cast<const T_ *>(xin), N, \
+               H, cent, hs, C, ids, group, mode, codes, scales, ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, \
+               ov, oi)
+    const bool delta = delta_out != nullptr || U != nullptr;
+    cudaError_t e;
     if (f32)
-        return launch_pdl(k_residual_quant<D, BITS, float, OUTL>, dim3(blocks), dim3(256), 0, st,
-                          static_cast<const float *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
-                          ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, ov, oi);
-    return launch_pdl(k_residual_quant<D, BITS, uint16_t, OUTL>, dim3(blocks), dim3(256), 0, st,
-                      static_cast<const uint16_t *>(xin), N, H, cent, hs, C, ids, group, mode, codes, scales,
-                      ids_out, shs, delta_out, gbf_out, U, pp, ps, phs, ov, oi);
+        e = delta ? QVG_RQ(float, true) : QVG_RQ(float, false);
+    else
+        e = delta ? QVG_RQ(uint16_t, true) : QVG_RQ(uint16_t, false);
+#undef QVG_RQ
+    return e;
 }
 
 template <int D, int BITS>

@@ -34,10 +34,11 @@ struct CacheView {
 // m-th store of the row's TPR threads writes 4 TPR contiguous channels --
 // whole 32-byte sectors -- and every store instruction of a warp is fully
 // used.  The row's packed codes are read whole by each of its threads (one
-// to four 16-byte loads) and the pieces' codes picked out of them.  Block
-// (x, y) takes consecutive slots of head y, whose codes, scales and ids are
-// contiguous.  A row costs two dependent memory round trips per stage:
-// first what depends on the slot alone (tile table entry, codes, scales,
+// to four 16-byte loads) and the pieces' codes picked out of them.  A block
+// takes consecutive slots of one head, whose codes, scales and ids are
+// contiguous; the heads vary fastest over the blocks.  A row costs two
+// dependent memory round trips per stage: first what depends on the slot
+// alone (tile table entry, codes, scales,
 // id, outlier entries), then what needs the chunk (its start, length and
 // anchor row, the centroid pieces).  Per element, in stage order:
 // acc += fl(fl(S q) + c), then the PSAC term as an fp32 FMA chain over the
@@ -185,8 +186,12 @@ template <int D, int BITS, bool PSAC, bool OUTL, bool VEC, bool MULTI>
 __global__ void __launch_bounds__(256, PSAC ? 1 : MULTI ? 2 : 3) k_decompress(CacheView cv, int L, int C, int group, int tok0, int ntok,
                                                     float *out32, uint16_t *out16) {
     constexpr int TPR = D / 32, RPB = 256 / TPR;  // threads per row, rows per block
-    const int i = threadIdx.x % TPR, h = blockIdx.y, H = cv.H;
-    const int t = blockIdx.x * RPB + threadIdx.x / TPR;
+    const int H = cv.H, i = threadIdx.x % TPR;
+    // block x: head x % H, slots [(x / H) RPB, + RPB) -- the heads vary
+    // fastest, so the blocks in flight write whole token rows of the
+    // token-major output
+    const int h = static_cast<int>(blockIdx.x % static_cast<unsigned>(H));
+    const int t = static_cast<int>(blockIdx.x / static_cast<unsigned>(H)) * RPB + threadIdx.x / TPR;
     if (t >= ntok) return;
     const int slot = tok0 + t;
     // slot-only loads: tile table entry and stage 0
@@ -271,7 +276,7 @@ template <int D, int BITS, bool PSAC, bool OUTL>
 void launch_dq(const CacheView &cv, const qvg_params *p, int tok0, int ntok, float *o32, uint16_t *o16, bool vec,
                cudaStream_t st) {
     constexpr int RPB = 256 / (D / 32);
-    const dim3 grid(static_cast<unsigned>((ntok + RPB - 1) / RPB), cv.H);
+    const dim3 grid(static_cast<unsigned>((ntok + RPB - 1) / RPB) * static_cast<unsigned>(cv.H));
     const int L = p->L, C = p->C, G = p->group;
     if (PSAC || L > 1) {
         if (vec) k_decompress<D, BITS, PSAC, OUTL, true, true><<<grid, 256, 0, st>>>(cv, L, C, G, tok0, ntok, o32, o16);
