@@ -40,6 +40,9 @@ def _gpu():
 
 
 W = synth.WORKLOADS
+# 2 heads of d = 128, chunks of one 16 x 20 frame (320 tokens: two and a half tiles)
+W128 = synth.Workload("d128_small", H=2, d=128, frame_hw=(16, 20), frames_per_chunk=1, n_chunks=2, dist="ar1",
+                      C=16, L=2, bits=2, group=128, iters=6, Hq=2, Nq=320)
 CASES = {
     "tiny": (W["tiny"], qvg.Params(C=16, L=1, bits=2, group=32, iters=10, seed=3), 4),
     "pro_int2_L3": (W["qvgpro"], qvg.Params(C=16, L=3, bits=2, group=32, iters=10, seed=4), 2),
@@ -53,6 +56,13 @@ CASES = {
     "rtn_outlier_g8": (W["tiny"], qvg.Params(C=0, L=1, bits=4, group=8, iters=0, flags=qvg.QVG_OUTLIER), 2),
     "tiny_outlier_g16": (W["tiny"], qvg.Params(C=16, L=1, bits=2, group=16, iters=10, seed=27, flags=qvg.QVG_OUTLIER), 2),
     "longcat_outlier": (W["longcat"], qvg.Params(C=256, L=1, bits=2, group=64, iters=8, seed=26, flags=qvg.QVG_OUTLIER), 2),
+    # groups wider than the 32 channels one lane of the quantiser holds: the
+    # group statistics are combined across 2 (d = 64, G = 64) or 4 (d = 128,
+    # G = 128) lanes of a row, with and without the outlier split
+    "tiny_g64_int4": (W["tiny"], qvg.Params(C=16, L=1, bits=4, group=64, iters=10, seed=28), 2),
+    "tiny_outlier_g64_L2": (W["tiny"], qvg.Params(C=16, L=2, bits=2, group=64, iters=10, seed=29,
+                                                  flags=qvg.QVG_OUTLIER), 2),
+    "d128_g128_L2": (W128, qvg.Params(C=16, L=2, bits=2, group=128, iters=6, seed=30), 2),
 }
 OUTL = lambda p: bool(p.flags & qvg.QVG_OUTLIER)
 
@@ -199,7 +209,8 @@ def test_lloyd_update_step(name):
     assert exact >= 0.99 * w.H * p0.C * w.d
 
 
-@pytest.mark.parametrize("name", ["pro_int2_L3", "pro_outlier_L2", "rtn_outlier_g8"])
+@pytest.mark.parametrize("name", ["pro_int2_L3", "pro_outlier_L2", "rtn_outlier_g8", "tiny_outlier_g64_L2",
+                                  "d128_g128_L2"])
 def test_decompress_exact_and_bf16(name):
     w, p, n_chunks = CASES[name]
     kc = _new_cache(w, p, n_chunks)
@@ -451,7 +462,8 @@ def test_attention_ar_longcat(Nq):
     assert top1.max().item() < kc.n_tokens + len(k_cur)
 
 
-@pytest.mark.parametrize("name", ["tiny_outlier", "pro_outlier_L2", "rtn_outlier_g8", "tiny_outlier_g16"])
+@pytest.mark.parametrize("name", ["tiny_outlier", "pro_outlier_L2", "rtn_outlier_g8", "tiny_outlier_g16",
+                                  "tiny_outlier_g64_L2"])
 def test_attention_with_outlier_split(name):
     """Attention and the AR step over caches whose K and V carry the
     outlier side list (one and two stages, RTN with G = 8), against the fp64
