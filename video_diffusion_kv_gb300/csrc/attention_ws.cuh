@@ -472,7 +472,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
         int2 pv = make_int2(0, 0);
         uint32_t ps = 0u;
         if constexpr (PSAC) {
-            if (last && r < ti0.nvalid && ti0.chunk >= 0) {
+            if (pr.pbuf && last && r < ti0.nvalid && ti0.chunk >= 0) {
                 const size_t prow = static_cast<size_t>(h) * a.cap + ti0.base + r;
                 pv = *reinterpret_cast<const int2 *>(a.psac_p + prow * QVG_PSAC_RANK);
                 ps = a.psac_s[prow];
@@ -506,7 +506,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             }
         }
         if constexpr (PSAC) {
-            if (last) {
+            if (pr.pbuf && last) {
                 const float S = f16_to_f32(static_cast<uint16_t>(ps));
                 float pk[8];
 #pragma unroll
@@ -1184,14 +1184,15 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                           isv ? a.voutv : a.koutv,
                           isv ? a.vouti : a.kouti, isv ? Vt0 : Kt0, isv ? vfull : kfull,
                           isv ? vfree : kfree,
-                          kNbuf, !isv && a.psac_p != nullptr, tile_tab, kTab, PTC ? PB : nullptr};
+                          kNbuf, !isv && a.psac_p != nullptr, tile_tab, kTab, PTC && !isv ? PB : nullptr};
         if constexpr (MODE == 0) {
             produce_fast<D, BITS, 0, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         } else if constexpr (MODE == 3) {
-            if (isv)
-                produce_fast<D, BITS, 0, true, false>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
-            else
-                produce_fast<D, BITS, 0, true, true>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
+            // one call site for both roles (two inlined copies of the producer
+            // loop cost 60 %, as the roles' code then competes for the
+            // instruction cache); the V role has no P_hat buffer and skips
+            // the PSAC part at run time
+            produce_fast<D, BITS, 0, true, true>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
         } else if constexpr (MODE == 1) {
             produce_fast<D, BITS, 0, true>(a, pr, h, tid & 127, tb, n_tiles, vfail, n_stage);
         } else {
