@@ -268,10 +268,24 @@ __device__ __forceinline__ void load_half_raw(const uint16_t *raw, int H, int h,
     for (int i = 0; i < 8; ++i) hd.cr[i] = *reinterpret_cast<const uint4 *>(row + 8 * i);
 }
 
+// A 16-byte store into a tile line.  SH: by 32-bit shared address, for the
+// out-of-line producers, where the compiler cannot see that the line is in
+// shared memory (a generic store there took the G = 16 outlier read path
+// from 3.75 to 3.98 ms); inlined, the plain store is left to the compiler
+// (the explicit form took the inlined PSAC producer from 2.38 to 3.37 ms).
+template <bool SH>
+__device__ __forceinline__ void st_line16(uint8_t *dst, uint4 v) {
+    if constexpr (SH)
+        umma::st_shared_v4(umma::smem_u32(dst), v);
+    else
+        *reinterpret_cast<uint4 *>(dst) = v;
+}
+
 // Zeroes one slot's 128-byte line of a 64-channel block (padding slots).
+template <bool SH>
 __device__ __forceinline__ void zero_line(uint8_t *dst) {
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4 *>(dst + (c8 << 4)) = make_uint4(0, 0, 0, 0);
+    for (int c8 = 0; c8 < 8; ++c8) st_line16<SH>(dst + (c8 << 4), make_uint4(0, 0, 0, 0));
 }
 
 // Packed fp32 pairs (Blackwell f32x2 arithmetic).
@@ -303,7 +317,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // matching offsets gives q = c - 2^(B-1) exactly (every intermediate is an
 // integer below 2^24), and K_hat = fma(S, q, c_bf16) has the single
 // rounding of the plain fp32 expression.
-template <int BITS>
+template <int BITS, bool SH = false>
 __device__ __forceinline__ void decode_store_half(const HalfData<BITS> &hd, uint8_t *dst, int r) {
     constexpr uint32_t M = (1u << BITS) - 1u, MAGIC = 0x4B000000u;
     constexpr float E23 = 8388608.0f, HALF = static_cast<float>(1 << (BITS - 1));
@@ -327,7 +341,7 @@ __device__ __forceinline__ void decode_store_half(const HalfData<BITS> &hd, uint
             up2(v2, v0, v1);
             w[e] = h2(v0, v1);
         }
-        *reinterpret_cast<uint4 *>(dst + ((i ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        st_line16<SH>(dst + ((i ^ (r & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
     }
 }
 
@@ -345,12 +359,12 @@ __device__ __forceinline__ void patch_outliers(const AttnWsArgs &a, const uint16
         const uint32_t oi = (hd.oi[g >> 2] >> (8 * (g & 3))) & 0xFFu;
         if (oi != 0xFFu) {
             const int j = g * G + static_cast<int>(oi);  // channel within the half
-            __half *p = reinterpret_cast<__half *>(dst + (((j >> 3) ^ (r & 7)) << 4) + (j & 7) * 2);
-            float c = __half2float(*p);
+            const uint32_t p = umma::smem_u32(dst + (((j >> 3) ^ (r & 7)) << 4) + (j & 7) * 2);
+            float c = f16_to_f32(umma::ld_shared_u16(p));
             if (a.C > 0 && c != 0.0f && fabsf(c) < 6.103515625e-05f)
                 c = __uint_as_float(static_cast<uint32_t>(
                         cent[((static_cast<size_t>(h) * a.max_chunks + chunk) * a.C + id) * D + kb * 64 + j]) << 16);
-            *p = __float2half_rn(__fadd_rn(f16_to_f32(static_cast<uint16_t>(hd.ov[g >> 1] >> (16 * (g & 1)))), c));
+            umma::st_shared_u16(p, f32_to_f16(__fadd_rn(f16_to_f32(static_cast<uint16_t>(hd.ov[g >> 1] >> (16 * (g & 1)))), c)));
         }
     }
 }
@@ -482,27 +496,27 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             if (valid) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, hl0, ti0, r, id0, 1, B);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
-                decode_store_half<BITS>(A, T, r);
+                decode_store_half<BITS, OUTL != 0>(A, T, r);
                 if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, A, hl0, ti0.chunk, id0, 0, T, r);
             } else {
-                zero_line(T);
+                zero_line<OUTL != 0>(T);
             }
             if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, l1 * a.H + h, ti1, r, id1, 0, A);
             if (valid) {
-                decode_store_half<BITS>(B, T + 16384, r);
+                decode_store_half<BITS, OUTL != 0>(B, T + 16384, r);
                 if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, B, hl0, ti0.chunk, id0, 1, T + 16384, r);
             } else {
-                zero_line(T + 16384);
+                zero_line<OUTL != 0>(T + 16384);
             }
         } else {
             B = A;
             if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, l1 * a.H + h, ti1, r, id1, 0, A);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
-                decode_store_half<BITS>(B, T, r);
+                decode_store_half<BITS, OUTL != 0>(B, T, r);
                 if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, B, hl0, ti0.chunk, id0, 0, T, r);
             } else {
-                zero_line(T);
+                zero_line<OUTL != 0>(T);
             }
         }
         if constexpr (PSAC) {

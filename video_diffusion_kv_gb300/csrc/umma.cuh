@@ -20,6 +20,24 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Shared-memory accesses by 32-bit shared address (no generic-address
+// resolution, also where the compiler cannot see that a pointer is shared:
+// the out-of-line producers).  No memory clobber, so that the compiler still
+// moves the producers' global loads across them; as volatile statements they
+// keep their order among themselves and with the fences and mbarrier
+// arrivals that publish the tile.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v));
+}
+
 // Byte offset of element k (16-bit elements, 0 <= k < 64) of row r inside a
 // swizzled K block.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t k) {
