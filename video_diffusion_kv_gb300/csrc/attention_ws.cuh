@@ -550,7 +550,8 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
 template <int D, int BITS, int NG>
 __device__ __noinline__ void produce_fast_outl(const AttnWsArgs &a, const Producer &pr, int h, int r, int tb,
                                                int n_tiles, volatile int *vfail, int L) {
-    produce_fast<D, BITS, NG, true>(a, pr, h, r, tb, n_tiles, vfail, L);
+    const Producer prv = pr;  // the role's pointers in registers, read once
+    produce_fast<D, BITS, NG, true>(a, prv, h, r, tb, n_tiles, vfail, L);
 }
 
 // The outlier split together with PSAC (every other case takes the fast
