@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # stripped) so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cuh", "attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "bcabf656761d1834226d4b101713ae568837a06e1376771d441a0c5cd59daa46": 80398592 + 3668480,
+    "42cee29455876a68c19f0aedff9d2d2d98e41a496ce560fe23986ab3e2d99f3d": 80398592 + 3685632,
 }
 
 
@@ -779,6 +779,15 @@ def measure_rollout(qvg, synth, flush, peaks, dev="cuda"):
     Q = [synth_dev(synth.queries(w, seed, k), dev) for k in range(uniq)]
     out = torch.empty((w.Nq, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(qvg.workspace_size(p, qvg.QVG_OP_COMPRESS, w.N, w.H, w.d), dtype=torch.uint8, device=dev)
+    # one untimed chunk through a scratch cache first, so that the first
+    # timed step does not include the kernels' first-launch loading
+    scratch_k = qvg.CompressedKV(p, w.H, w.d, per, 1, device=dev)
+    scratch_v = qvg.CompressedKV(p, w.H, w.d, per, 1, device=dev)
+    qvg.compress_chunk(p, K[0], scratch_k, workspace=ws)
+    qvg.compress_chunk(p, V[0], scratch_v, workspace=ws)
+    qvg.attention(p, Q[0], scratch_k, scratch_v, out_dtype=qvg.QVG_OUT_BF16, out=out)
+    torch.cuda.synchronize()
+    del scratch_k, scratch_v
     points, comp_ms, step_ms = [], [], []
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
