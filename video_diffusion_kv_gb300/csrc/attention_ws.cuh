@@ -855,8 +855,10 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
 //         to make room.
 // Separate instantiations keep the out-of-line producers' call sites, which
 // cost the plain kernel 7 % when present, out of modes 0 and 1.
-// LS = 1: one stage per tile, known at compile time (every pseudo-tile
-// index is a tile index); LS = 0: a.L stages, one buffer fill each.
+// LS >= 1: LS stages per tile, one buffer fill each, known at compile time
+// (with LS = 1 every pseudo-tile index is a tile index; LS = 2 serves
+// two-stage QVG-Pro caches, 3.90 -> 3.81 ms against the run-time count);
+// LS = 0: a.L stages.
 template <int D, int BITS, bool TOP1, int MODE, int LS>
 __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) {
     using namespace ws;
@@ -886,7 +888,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
     const int n_grp = q0 + 128 < a.Nq ? 2 : 1;
     // buffer fills per tile: one per stage, except where a producer sums the
     // stages itself (the general producer of mode 2)
-    const int n_stage = LS == 1 ? 1 : (MODE == 2 && a.psac_p) ? 1 : a.L;
+    const int n_stage = LS >= 1 ? LS : (MODE == 2 && a.psac_p) ? 1 : a.L;
     static_assert(MODE >= 0 && MODE <= 3 && (LS == 1 || MODE != 0), "attention mode");
 
     // Q tiles -> fp16 (exact for bf16 values in fp16's normal range), swizzled K-major
@@ -1266,6 +1268,7 @@ qvg_status attn_ws(const AttnWsArgs &a, int splits, cudaStream_t st) {
     const bool one = a.L == 1;
     if (a.kouti) return one ? attn_ws_m<D, BITS, 2, 1>(a, splits, st) : attn_ws_m<D, BITS, 2, 0>(a, splits, st);
     if (a.psac_p) return one ? attn_ws_m<D, BITS, 3, 1>(a, splits, st) : attn_ws_m<D, BITS, 3, 0>(a, splits, st);
+    if (a.L == 2) return attn_ws_m<D, BITS, 1, 2>(a, splits, st);
     if (!one) return attn_ws_m<D, BITS, 1, 0>(a, splits, st);
     if (a.n_raw > 0 || a.chunk_anchor) return attn_ws_m<D, BITS, 1, 1>(a, splits, st);
     return attn_ws_m<D, BITS, 0, 1>(a, splits, st);
