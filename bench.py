@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # stripped) so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cuh", "attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "42cee29455876a68c19f0aedff9d2d2d98e41a496ce560fe23986ab3e2d99f3d": 80398592 + 3685632,
+    "9fefbc019843d34b5d6a6df26ef7e612a05b578906b1d407f3d2cde5ef7cd27a": 80397824 + 3758080,
 }
 
 
