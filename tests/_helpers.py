@@ -73,6 +73,50 @@ def oracle_rebuild(hc, p, k):
     return oracle.decompress(codes, scales, ids, cent, p.C, p.bits, p.group, **kw)
 
 
+def stage_abs_rebuild(hc, p, k):
+    """sum_l |K_hat_l| [N,H,d] of chunk k, stage by stage (the magnitudes the
+    attention kernel rounds to fp16, one stage per buffer fill); an anchor
+    chunk's rows, or a one-stage chunk, as |K_hat|."""
+    if p.L == 1 or ("chunk_anchor" in hc and hc["chunk_anchor"][k] >= 0):
+        return np.abs(oracle_rebuild(hc, p, k))
+    codes, scales, ids, cent = chunk_arrays(hc, p, k)
+    sl = chunk_slice(hc, k)
+    out = 0.0
+    for l in range(p.L):
+        kw = {}
+        if "outl_val" in hc:
+            kw = dict(outl_val=hc["outl_val"][l:l + 1, :, sl], outl_idx=hc["outl_idx"][l:l + 1, :, sl])
+        out = out + np.abs(oracle.decompress(codes[l:l + 1], scales[l:l + 1], ids[l:l + 1], cent[l:l + 1],
+                                             p.C, p.bits, p.group, **kw))
+    return out
+
+
+# Log-sum-exp.  The kernel's operands are fp16 (reading R21: unit roundoff
+# 2^-11; Q's bf16 values are exact in fp16, each stage of K_hat is rounded
+# once), so logit j of a row moves by at most
+#   scale * sum_c |q_c| sum_l |K_hat_l,jc| * 2^-11,
+# and the row sum of the fp16-rounded weights by a factor within 1 +- 2^-11;
+# the natural-log LSE, 1-Lipschitz in the logits' max norm, then moves by at
+# most the largest logit bound + 2^-11.  The checks allow the larger of that
+# bound and 2e-3.
+LSE_TOL = 2e-3
+
+
+def lse_tolerance(q, k_abs, grp, scale=None):
+    """Per-(query head, query) LSE tolerance [Hq, Nq] for queries q [Nq,Hq,d]
+    over keys with stage magnitudes k_abs [Nk,H,d] (query head hq reads key
+    head hq // grp)."""
+    q = np.abs(np.asarray(q, np.float64))
+    Nq, Hq, d = q.shape
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    out = np.empty((Hq, Nq))
+    for hq in range(Hq):
+        kh = np.asarray(k_abs[:, hq // grp], np.float64)
+        b = (q[:, hq] @ kh.T).max(axis=1) if len(kh) else np.zeros(Nq)
+        out[hq] = scale * b * 2.0 ** -11 + 2.0 ** -11
+    return np.maximum(out, LSE_TOL)
+
+
 def assignment_mismatches(g, cent_bf16_bits, ids_gpu, w=None):
     """Compare GPU ids for one (head, stage) with the oracle's argmin over the
     same centroids.  Returns (number of mismatches, number outside near ties)."""
