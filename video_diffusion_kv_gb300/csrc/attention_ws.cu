@@ -103,6 +103,7 @@ qvg_status launch_attention_ws(const qvg_params *p, const uint16_t *q, int Nq, i
     a.L = p->L;
     a.C = p->C;
     a.group = p->group;
+    a.glog2 = __builtin_ctz(static_cast<unsigned>(p->group));  // a power of two (check_params)
     a.cap = k->capacity_tokens;
     a.max_chunks = k->max_chunks;
     a.n_slots = k->n_tokens;

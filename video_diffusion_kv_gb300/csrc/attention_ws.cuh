@@ -32,6 +32,7 @@ namespace qvg {
 struct AttnWsArgs {
     const uint16_t *q;
     int Nq, Hq, H, grp, L, C, group, cap, max_chunks, n_slots;
+    int glog2;  // log2(group): groups are powers of two, so the producers shift instead of divide
     const uint8_t *kcodes, *vcodes;
     const uint16_t *kscales, *vscales;
     const uint8_t *kids, *vids;
@@ -198,7 +199,7 @@ __device__ __forceinline__ void load_half(const AttnWsArgs &a, const uint8_t *co
                                           int chunk, int slot, int id, int kb, HalfData<BITS> &hd) {
     constexpr int NB = D * BITS / 8;
     constexpr int HB = 64 * BITS / 8;
-    const int ng = D / a.group;
+    const int ng = D >> a.glog2;
     const size_t srow = static_cast<size_t>(h) * a.cap + slot;
     hd.oi[0] = hd.oi[1] = 0xFFFFFFFFu;
     hd.ov[0] = hd.ov[1] = hd.ov[2] = hd.ov[3] = 0u;
@@ -233,14 +234,14 @@ __device__ __forceinline__ void load_half(const AttnWsArgs &a, const uint8_t *co
 #pragma unroll
     for (int i = 0; i < HB / 16; ++i) hd.cw[i] = *reinterpret_cast<const uint4 *>(codes + srow * NB + kb * HB + 16 * i);
     if (a.group >= 64) {
-        const uint32_t s0 = scales[srow * ng + (kb * 64) / a.group];
+        const uint32_t s0 = scales[srow * ng + ((kb * 64) >> a.glog2)];
 #pragma unroll
         for (int i = 0; i < 4; ++i) hd.s2[i] = s0 | (s0 << 16);
     } else {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            hd.s2[i] = static_cast<uint32_t>(scales[srow * ng + (kb * 64 + 16 * i) / a.group]) |
-                       (static_cast<uint32_t>(scales[srow * ng + (kb * 64 + 16 * i + 8) / a.group]) << 16);
+            hd.s2[i] = static_cast<uint32_t>(scales[srow * ng + ((kb * 64 + 16 * i) >> a.glog2)]) |
+                       (static_cast<uint32_t>(scales[srow * ng + ((kb * 64 + 16 * i + 8) >> a.glog2)]) << 16);
     }
     if (a.C > 0) {
         const uint16_t *row = cent + ((static_cast<size_t>(h) * a.max_chunks + chunk) * a.C + id) * D + kb * 64;
@@ -617,7 +618,7 @@ __device__ __forceinline__ void load_quarter(const AttnWsArgs &a, const Producer
         }
         return;
     }
-    const int ng = D / a.group;
+    const int ng = D >> a.glog2;
     const size_t srow = (static_cast<size_t>(l) * a.H + h) * a.cap + ti.base + r;
     const uint8_t *cp = pr.codes + srow * (D * BITS / 8) + qt * (4 * BITS);
     if constexpr (BITS == 2) {
@@ -632,12 +633,12 @@ __device__ __forceinline__ void load_quarter(const AttnWsArgs &a, const Producer
         qd.cw[3] = u.w;
     }
     if (a.group >= 32) {
-        const uint32_t s0 = pr.scales[srow * ng + (qt * 32) / a.group];
+        const uint32_t s0 = pr.scales[srow * ng + ((qt * 32) >> a.glog2)];
         qd.s2[0] = qd.s2[1] = s0 | (s0 << 16);
     } else {
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-            qd.s2[b >> 1] |= static_cast<uint32_t>(pr.scales[srow * ng + (qt * 32 + 8 * b) / a.group]) << (16 * (b & 1));
+            qd.s2[b >> 1] |= static_cast<uint32_t>(pr.scales[srow * ng + ((qt * 32 + 8 * b) >> a.glog2)]) << (16 * (b & 1));
     }
     if (a.C > 0) {
         const uint16_t *crow =
@@ -649,7 +650,7 @@ __device__ __forceinline__ void load_quarter(const AttnWsArgs &a, const Producer
     if constexpr (OUTL) {
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const int gi = (qt * 32 + 8 * b) / a.group;
+            const int gi = (qt * 32 + 8 * b) >> a.glog2;
             const int oi = pr.outi[srow * ng + gi];
             const int e = gi * a.group + oi - (qt * 32 + 8 * b);
             if (oi != 0xFF && e >= 0 && e < 8) {

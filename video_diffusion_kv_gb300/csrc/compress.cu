@@ -880,7 +880,8 @@ __global__ void __launch_bounds__(256, DELTA ? 2 : 3) k_residual_quant(
     // N - 1 and stores nothing
     const bool live = n_row < N;
     const int n = live ? n_row : N - 1;
-    const int ng = D / group;
+    const int glog = __ffs(group) - 1;  // groups are powers of two: shifts, not divisions
+    const int ng = D >> glog;
     // (an id outside [0, C) never comes from the assignment; clamped so that
     // no access leaves the centroid table)
     const unsigned uid = C > 0 ? static_cast<unsigned>(ids[static_cast<size_t>(h) * N + n]) : 0u;
@@ -926,13 +927,13 @@ __global__ void __launch_bounds__(256, DELTA ? 2 : 3) k_residual_quant(
     GStat gs8[4];
     const GStat zero{0.0f, 0.0f, 0.0f, 0};
     if (group <= 32) {
-        const int g8 = group / 8;  // 1, 2 or 4 blocks per group
+        const int g8log = glog - 3;  // 1, 2 or 4 blocks per group (log2: 0, 1, 2)
 #pragma unroll
         for (int b8 = 0; b8 < 4; ++b8) {
             GStat acc = zero;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                if (k / g8 == b8 / g8) acc = OUTL ? gmerge(acc, st8[k]) : GStat{fmaxf(acc.m, st8[k].m), 0.0f, 0.0f, 0};
+                if ((k >> g8log) == (b8 >> g8log)) acc = OUTL ? gmerge(acc, st8[k]) : GStat{fmaxf(acc.m, st8[k].m), 0.0f, 0.0f, 0};
             gs8[b8] = acc;
         }
     } else {
@@ -940,7 +941,7 @@ __global__ void __launch_bounds__(256, DELTA ? 2 : 3) k_residual_quant(
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc = OUTL ? gmerge(acc, st8[k]) : GStat{fmaxf(acc.m, st8[k].m), 0.0f, 0.0f, 0};
         // lanes cb ^ o (o < group / 32) of the row hold the group's other blocks
-        for (int o = 1; o < group / 32; o <<= 1) {
+        for (int o = 1; o < (group >> 5); o <<= 1) {
             GStat pt;
             pt.m = __shfl_xor_sync(0xffffffffu, acc.m, o);
             if constexpr (OUTL) {
@@ -994,8 +995,8 @@ __global__ void __launch_bounds__(256, DELTA ? 2 : 3) k_residual_quant(
     }
 #pragma unroll
     for (int b8 = 0; b8 < 4; ++b8) {
-        const int ch = cb * 32 + 8 * b8, gi = ch / group;
-        if (live && ch % group == 0) {
+        const int ch = cb * 32 + 8 * b8, gi = ch >> glog;
+        if (live && (ch & (group - 1)) == 0) {
             scales[srow * ng + gi] = sbits[b8];
             if constexpr (OUTL) {
                 outl_val[srow * ng + gi] = obits[b8];

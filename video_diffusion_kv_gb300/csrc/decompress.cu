@@ -60,7 +60,8 @@ template <int D, int BITS, bool OUTL>
 __device__ __forceinline__ void load_row_stage(const CacheView &cv, int l, int h, int slot, int i, int group,
                                                bool want_id, RowStage<D, BITS> &rs) {
     constexpr int TPR = D / 32, NB = D * BITS / 8;
-    const int ng = D / group;
+    const int glog = __ffs(group) - 1;  // groups are powers of two: shifts, not divisions
+    const int ng = D >> glog;
     const size_t srow = (static_cast<size_t>(l) * cv.H + h) * cv.cap + slot;
     const uint4 *cp = reinterpret_cast<const uint4 *>(cv.codes + srow * NB);
 #pragma unroll
@@ -74,7 +75,7 @@ __device__ __forceinline__ void load_row_stage(const CacheView &cv, int l, int h
     const uint16_t *sp = cv.scales + srow * ng;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-        const int g = 4 * (i + TPR * m) / group;
+        const int g = (4 * (i + TPR * m)) >> glog;
         rs.S[m] = f16_to_f32(sp[g]);
         rs.oc[m] = -1;
         rs.ov[m] = 0.0f;
