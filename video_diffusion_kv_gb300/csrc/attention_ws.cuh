@@ -403,7 +403,7 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&v)[32], int c0, i
 }
 
 // One producer role: the compressed stream it rebuilds and its buffers.
-// Tile t goes to buffer t % nbuf (QVG_TILE slots x D channels, 64-channel
+// Tile t goes to buffer t % kNbuf (QVG_TILE slots x D channels, 64-channel
 // blocks of 128-byte swizzled lines); full[b] gets one arrival per slot
 // thread, free[b] is committed by the MMAs that read the buffer.
 struct Producer {
@@ -417,7 +417,6 @@ struct Producer {
     const uint8_t *outi;
     uint8_t *buf0;
     uint64_t *full, *freeb;
-    int nbuf;
     bool psac;
     const int2 *tab;  // the CTA's tile table and its length
     int tab_n;
@@ -475,7 +474,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
     HalfData<BITS> A, B;
     if (v0) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, l0 * a.H + h, ti0, r, id0, 0, A);
     for (int u = 0; u < n_u; ++u) {
-        const int b = u % pr.nbuf, use = u / pr.nbuf;
+        const int b = u % kNbuf, use = u / kNbuf;
         uint8_t *T = pr.buf0 + b * TB + r * 128;
         const int hl0 = l0 * a.H + h;
         TileInfo ti2{};
@@ -757,7 +756,7 @@ __device__ __noinline__ void produce_general(const AttnWsArgs &a, const Producer
         }
         accumulate_quarter<BITS, OUTL>(cur, acc);
         if (l == L - 1) {
-            const int b = t % pr.nbuf, use = t / pr.nbuf;
+            const int b = t % kNbuf, use = t / kNbuf;
             uint8_t *T = pr.buf0 + b * TB + r * 128;
             if (qt == 0 && use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             float v[32];
@@ -1202,7 +1201,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1) k_attention_ws(AttnWsArgs a) 
                           isv ? a.voutv : a.koutv,
                           isv ? a.vouti : a.kouti, isv ? Vt0 : Kt0, isv ? vfull : kfull,
                           isv ? vfree : kfree,
-                          kNbuf, !isv && a.psac_p != nullptr, tile_tab, kTab, PTC && !isv ? PB : nullptr};
+                          !isv && a.psac_p != nullptr, tile_tab, kTab, PTC && !isv ? PB : nullptr};
         if constexpr (MODE == 0) {
             produce_fast<D, BITS, 0, false>(a, pr, h, tid & 127, tb, n_tiles, vfail);
         } else if constexpr (MODE == 3) {
