@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # stripped) so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cuh", "attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "9fefbc019843d34b5d6a6df26ef7e612a05b578906b1d407f3d2cde5ef7cd27a": 80397824 + 3758080,
+    "76267a5509757af7d84424b9dad1cf015dbfa5254383fb1c1768b302e09fc314": 80436480 + 3579648,
 }
 
 
