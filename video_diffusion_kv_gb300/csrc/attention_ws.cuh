@@ -312,31 +312,42 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // Decodes the half and stores it as the eight swizzled 16-byte chunks of the
 // slot's 128-byte line `dst` (chunk c at position c ^ (r % 8)), one chunk as
 // soon as its four words are ready.  Codes become floats without a
-// conversion instruction: OR-ing a B-bit code c into the mantissa of 2^23
-// (0x4B000000) gives the float 2^23 + c exactly, or 2^23 + c 2^B for the
-// odd code of a pair left at bit B; one packed FMA with (1, 2^-B) and the
-// matching offsets gives q = c - 2^(B-1) exactly (every intermediate is an
-// integer below 2^24), and K_hat = fma(S, q, c_bf16) has the single
-// rounding of the plain fp32 expression.
-template <int BITS, bool SH = false>
+// conversion instruction: OR-ing a B-bit code c, at bit k of a word, into the
+// mantissa of 2^23 (0x4B000000) gives the float 2^23 + c 2^k exactly
+// (k + B <= 23); one packed FMA with (2^-k0, 2^-k1) and the matching offsets
+// gives q = c - 2^(B-1) exactly for both codes of a pair (every
+// intermediate is an integer below 2^24), and K_hat = fma(S, q, c_bf16) has
+// the single rounding of the plain fp32 expression.
+// NOSHIFT: each pair's codes are taken where they sit in the block's word
+// (a block's upper half is shifted down once where k + B <= 23 would not
+// hold, for B = 4), with four (scale, offset) constant pairs; otherwise the
+// pair is shifted down to bit 0 first, with one constant pair.  Without the
+// shifts the one-stage, outlier-split and PSAC kernels run 0.5-3.5 % faster;
+// the raw-tile kernel (mode 1) loses up to 20 % to the constants' registers.
+template <int BITS, bool SH = false, bool NOSHIFT = false>
 __device__ __forceinline__ void decode_store_half(const HalfData<BITS> &hd, uint8_t *dst, int r) {
     constexpr uint32_t M = (1u << BITS) - 1u, MAGIC = 0x4B000000u;
     constexpr float E23 = 8388608.0f, HALF = static_cast<float>(1 << (BITS - 1));
-    const uint64_t P2 = pk2(1.0f, 1.0f / static_cast<float>(1 << BITS));
-    const uint64_t N2 = pk2(-(E23 + HALF), -(E23 / static_cast<float>(1 << BITS) + HALF));
     const uint32_t *cb = reinterpret_cast<const uint32_t *>(hd.cw);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint32_t blk = cb[(8 * i * BITS) / 32] >> ((8 * i * BITS) % 32);
+        const uint32_t blk_hi = blk >> 16;  // used only where a code would sit above bit 23 - B
         const float S = f16_to_f32(static_cast<uint16_t>(hd.s2[i >> 1] >> (16 * (i & 1))));
         const uint64_t S2 = pk2(S, S);
         const uint32_t c4[4] = {hd.cr[i].x, hd.cr[i].y, hd.cr[i].z, hd.cr[i].w};
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const uint32_t x = blk >> (2 * e * BITS);
-            const uint64_t mag = pk2(__uint_as_float((x & M) | MAGIC), __uint_as_float((x & (M << BITS)) | MAGIC));
-            const uint64_t q2 = fma2(mag, P2, N2);
+            // the pair's codes at bits k0 and k0 + B of x
+            constexpr int kMax = 23 - 2 * BITS;  // highest k0 whose pair fits the mantissa
+            const int kp = 2 * e * BITS;
+            const bool hi = NOSHIFT && kp > kMax;
+            const uint32_t x = !NOSHIFT ? blk >> kp : hi ? blk_hi : blk;
+            const int k0 = !NOSHIFT ? 0 : hi ? kp - 16 : kp, k1 = k0 + BITS;
+            const uint64_t mag = pk2(__uint_as_float((x & (M << k0)) | MAGIC), __uint_as_float((x & (M << k1)) | MAGIC));
+            const float s0 = 1.0f / static_cast<float>(1 << k0), s1 = 1.0f / static_cast<float>(1 << k1);
+            const uint64_t q2 = fma2(mag, pk2(s0, s1), pk2(-(E23 * s0 + HALF), -(E23 * s1 + HALF)));
             const uint64_t v2 = fma2(S2, q2, pk2(__uint_as_float(c4[e] << 16), __uint_as_float(c4[e] & 0xffff0000u)));
             float v0, v1;
             up2(v2, v0, v1);
@@ -496,14 +507,14 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             if (valid) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, hl0, ti0, r, id0, 1, B);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
-                decode_store_half<BITS, OUTL != 0>(A, T, r);
+                decode_store_half<BITS, OUTL != 0, (!RAW || OUTL != 0 || PSAC)>(A, T, r);
                 if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, A, hl0, ti0.chunk, id0, 0, T, r);
             } else {
                 zero_line<OUTL != 0>(T);
             }
             if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, l1 * a.H + h, ti1, r, id1, 0, A);
             if (valid) {
-                decode_store_half<BITS, OUTL != 0>(B, T + 16384, r);
+                decode_store_half<BITS, OUTL != 0, (!RAW || OUTL != 0 || PSAC)>(B, T + 16384, r);
                 if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, B, hl0, ti0.chunk, id0, 1, T + 16384, r);
             } else {
                 zero_line<OUTL != 0>(T + 16384);
@@ -513,7 +524,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, l1 * a.H + h, ti1, r, id1, 0, A);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
-                decode_store_half<BITS, OUTL != 0>(B, T, r);
+                decode_store_half<BITS, OUTL != 0, (!RAW || OUTL != 0 || PSAC)>(B, T, r);
                 if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, B, hl0, ti0.chunk, id0, 0, T, r);
             } else {
                 zero_line<OUTL != 0>(T);
