@@ -322,8 +322,10 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // (a block's upper half is shifted down once where k + B <= 23 would not
 // hold, for B = 4), with four (scale, offset) constant pairs; otherwise the
 // pair is shifted down to bit 0 first, with one constant pair.  Without the
-// shifts the one-stage, outlier-split and PSAC kernels run 0.5-3.5 % faster;
-// the raw-tile kernel (mode 1) loses up to 20 % to the constants' registers.
+// shifts the outlier-split and PSAC kernels run 1-3.5 % faster; the
+// raw-tile kernel (mode 1) loses up to 20 % to the constants' registers, and
+// the plain one (mode 0) gains 0.8 % on 16 heads but loses 7 % on a one-wave
+// 8-head grid and 3.5 % at 16 queries, so both keep the shifts.
 template <int BITS, bool SH = false, bool NOSHIFT = false>
 __device__ __forceinline__ void decode_store_half(const HalfData<BITS> &hd, uint8_t *dst, int r) {
     constexpr uint32_t M = (1u << BITS) - 1u, MAGIC = 0x4B000000u;
@@ -507,14 +509,14 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             if (valid) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, hl0, ti0, r, id0, 1, B);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
-                decode_store_half<BITS, OUTL != 0, (!RAW || OUTL != 0 || PSAC)>(A, T, r);
+                decode_store_half<BITS, OUTL != 0, (OUTL != 0 || PSAC)>(A, T, r);
                 if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, A, hl0, ti0.chunk, id0, 0, T, r);
             } else {
                 zero_line<OUTL != 0>(T);
             }
             if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, l1 * a.H + h, ti1, r, id1, 0, A);
             if (valid) {
-                decode_store_half<BITS, OUTL != 0, (!RAW || OUTL != 0 || PSAC)>(B, T + 16384, r);
+                decode_store_half<BITS, OUTL != 0, (OUTL != 0 || PSAC)>(B, T + 16384, r);
                 if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, B, hl0, ti0.chunk, id0, 1, T + 16384, r);
             } else {
                 zero_line<OUTL != 0>(T + 16384);
@@ -524,7 +526,7 @@ __device__ __forceinline__ void produce_fast(const AttnWsArgs &a, const Producer
             if (valid1) load_tile_half<D, BITS, OUTL, RAW>(a, pr, h, l1 * a.H + h, ti1, r, id1, 0, A);
             if (use > 0 && !wait(&pr.freeb[b], (use - 1) & 1, vfail, a.wait_ns)) return;
             if (valid) {
-                decode_store_half<BITS, OUTL != 0, (!RAW || OUTL != 0 || PSAC)>(B, T, r);
+                decode_store_half<BITS, OUTL != 0, (OUTL != 0 || PSAC)>(B, T, r);
                 if constexpr (OUTL != 0) patch_outliers<D, BITS, OUTL>(a, pr.cent, B, hl0, ti0.chunk, id0, 0, T, r);
             } else {
                 zero_line<OUTL != 0>(T);
