@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # stripped) so that a changed kernel reports null until re-measured.
 ATTN_SOURCES = ("attention_ws.cuh", "attention_ws.cu", "umma.cuh", "common.cuh")
 ATTN_TRAFFIC = {
-    "76267a5509757af7d84424b9dad1cf015dbfa5254383fb1c1768b302e09fc314": 80436480 + 3579648,
+    "7c1747e6d35b97ea03205edafaf6f72f8da0695c97a526e7fe74b55fe0a24d75": 80429056 + 3645440,
 }
 
 
