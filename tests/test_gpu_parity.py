@@ -386,6 +386,38 @@ def test_attention_split_cache(Nq):
     assert (top11.cpu().numpy() == top1.cpu().numpy()).mean() >= 0.999
 
 
+@pytest.mark.parametrize("name,n_chunks,Nq,Hq_mult", [("tiny", 5, 5, 1), ("tiny", 5, 40, 2), ("longcat", 2, 16, 1),
+                                                      ("longcat", 2, 100, 1)])
+def test_attention_split_no_top1(name, n_chunks, Nq, Hq_mult):
+    """Few queries over a one-stage cache without top-1 output, through the
+    split-cache path: tiny (d = 64) splits 10 tiles into two CTAs of 5 per
+    head, the LongCat-like layer (d = 128) 74 tiles into nine of 8 or 9,
+    with GQA and ragged query counts.  Checked against the fp64 oracle
+    (the log-sum-exp within the bound of the fp16 rounding of K_hat) and
+    against the unsplit call."""
+    w, p, _ = CASES[name]
+    chunks = [(synth.chunk_kv(w, 41, k, synth.KIND_K), synth.chunk_kv(w, 41, k, synth.KIND_V)) for k in range(n_chunks)]
+    kc, vc = _cache_with_chunks(w, p, chunks)
+    q = synth.queries(w, 41, n_chunks)
+    if Hq_mult > 1:  # two query heads per KV head
+        q = np.concatenate([q, synth.queries(w, 42, n_chunks)], 1)[:, [0, 2, 1, 3]]
+    q = np.ascontiguousarray(q[:Nq])
+    Hq = q.shape[1]
+    assert qvg.workspace_size(p, qvg.QVG_OP_ATTENTION, Nq, w.H, w.d, Hq) > 0
+    out, lse, _ = qvg.attention(p, to_dev(q), kc, vc, want_lse=True)
+    ref, rlse, _, _, hk = _oracle_attention_on(kc, vc, p, q)
+    got = out.cpu().numpy().astype(np.float64)
+    _assert_attention(got, ref, Hq)
+    # the log-sum-exp within the bound of the fp16 rounding of K_hat
+    k_abs = np.concatenate([stage_abs_rebuild(hk, p, k) for k in range(kc.n_chunks)], 0)
+    tol = lse_tolerance(q, k_abs, Hq // w.H)
+    assert (np.abs(lse.cpu().numpy() - rlse) <= tol).all(), np.abs(lse.cpu().numpy() - rlse).max()
+    one, lse1, _ = qvg.attention(p, to_dev(q), kc, vc, want_lse=True, allow_split=False)
+    one_np = one.cpu().numpy().astype(np.float64)
+    assert np.abs(one_np - got).max() <= 1e-4 * np.abs(one_np).max()
+    np.testing.assert_allclose(lse1.cpu().numpy(), lse.cpu().numpy(), atol=1e-3, rtol=0)
+
+
 def _oracle_ar(kc, vc, p, q, k_cur, v_cur, rows=None):
     hk, hv = host_cache(kc), host_cache(vc)
     n = kc.n_chunks
