@@ -386,16 +386,28 @@ def test_attention_split_cache(Nq):
     assert (top11.cpu().numpy() == top1.cpu().numpy()).mean() >= 0.999
 
 
+FEW_Q = {
+    "tiny": CASES["tiny"][:2],
+    "longcat": CASES["longcat"][:2],
+    # d = 128 with 8-channel groups: each 64-channel half of a slot carries
+    # eight scales
+    "d128_int2_g8": (W128, qvg.Params(C=16, L=1, bits=2, group=8, iters=6, seed=31)),
+    "d128_int4_g8": (W128, qvg.Params(C=16, L=1, bits=4, group=8, iters=6, seed=32)),
+}
+
+
 @pytest.mark.parametrize("name,n_chunks,Nq,Hq_mult", [("tiny", 5, 5, 1), ("tiny", 5, 40, 2), ("longcat", 2, 16, 1),
-                                                      ("longcat", 2, 100, 1)])
-def test_attention_split_no_top1(name, n_chunks, Nq, Hq_mult):
-    """Few queries over a one-stage cache without top-1 output, through the
-    split-cache path: tiny (d = 64) splits 10 tiles into two CTAs of 5 per
-    head, the LongCat-like layer (d = 128) 74 tiles into nine of 8 or 9,
-    with GQA and ragged query counts.  Checked against the fp64 oracle
-    (the log-sum-exp within the bound of the fp16 rounding of K_hat) and
-    against the unsplit call."""
-    w, p, _ = CASES[name]
+                                                      ("longcat", 2, 100, 1), ("d128_int2_g8", 2, 24, 1),
+                                                      ("d128_int4_g8", 2, 128, 1)])
+def test_attention_few_queries(name, n_chunks, Nq, Hq_mult):
+    """At most 128 queries over a one-stage cache without top-1 output.
+    Split cache: tiny (d = 64) 10 tiles in two CTAs of 5 per head, the
+    LongCat-like layer (d = 128) 74 tiles in nine CTAs of 8 or 9; unsplit:
+    d = 128 with 8-channel groups in INT2 and INT4, 6 tiles per head.  With
+    GQA and ragged query counts, checked against the fp64 oracle (the
+    log-sum-exp within the bound of the fp16 rounding of K_hat) and against
+    the call without a workspace."""
+    w, p = FEW_Q[name]
     chunks = [(synth.chunk_kv(w, 41, k, synth.KIND_K), synth.chunk_kv(w, 41, k, synth.KIND_V)) for k in range(n_chunks)]
     kc, vc = _cache_with_chunks(w, p, chunks)
     q = synth.queries(w, 41, n_chunks)
